@@ -1,0 +1,248 @@
+"""Seeded synthetic workloads for the token-choice MoE FFN block.
+
+This module only draws inputs: shapes, dtypes, seeds and value distributions.
+It holds none of the block's arithmetic (no routing, no activation, no
+combine), so both the CUDA path and the fp64 oracle can be fed from it.
+
+Shapes follow the pages:
+  * Arcee AFMoE issue (mlxcel #845), "Checkpoint confirmed": Trinity-Nano has
+    hidden 1024 and 128 experts; "Routing detail": route_scale 2.826.
+  * HF Transformers AFMoE docs, ``AfmoeConfig`` signature: hidden_size 2048,
+    moe_intermediate_size 1408, num_experts 64, num_experts_per_tok 6,
+    num_shared_experts 2, route_scale 1.0, initializer_range 0.02.
+  * MiniMax-M3 issue (mlxcel #763), "Architecture specification": hidden 6144,
+    128 experts of width 3072, top-4, routed_scaling_factor 2.0, one shared
+    expert of width 3072 packed as expert index 128, clamp-SwiGLU.
+
+Recipe (all workloads):
+  * X ~ N(0, 1); router, expert and shared weights ~ N(0, 0.02);
+  * expert_bias ~ U(-0.1, 0.1), or, for the load-skew sweep, a Zipf(s=1.2)
+    profile r^-1.2 over ranks r = 1..E, min-max scaled to [0, 0.5] and assigned
+    to experts through a seeded random permutation;
+  * draw order: router, bias, gate, up, down (all E or E+1 slices), shared
+    gate/up/down, then X from its own generator;
+  * bf16 workloads round every drawn value to bf16 (round-to-nearest-even).
+    Router weights are rounded to bf16 too but stored as fp32, so the router
+    of both sides sees identical fp32 values;
+  * the tiny workload keeps fp32 for X, router and expert weights.
+
+A caller may pass ``row_filter``: a function of the host copy of
+(X, router_w, expert_bias) returning a boolean mask of token rows to redraw.
+The parity tests use it to enforce a gap of at least 1e-3 between the k-th and
+(k+1)-th biased router scores, so that top-k sets are unique.  Redrawn rows
+come from a generator seeded with (x_seed, attempt).
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from typing import Callable, Optional
+
+import torch
+
+WEIGHT_STD = 0.02
+BIAS_HALF_RANGE = 0.1
+ZIPF_S = 1.2
+ZIPF_MAX = 0.5
+
+
+@dataclasses.dataclass(frozen=True)
+class MoeShape:
+    """One workload: the MoE block's config keys plus the token count."""
+
+    name: str
+    T: int
+    hidden_size: int
+    num_experts: int
+    num_experts_per_tok: int
+    moe_intermediate_size: int
+    num_shared_experts: int
+    shared_intermediate_size: int  # total shared width S
+    shared_packed: bool
+    hidden_act: str  # "silu" | "swigluoai"
+    score_func: str  # "sigmoid" | "softmax"
+    route_norm: bool
+    route_scale: float
+    dtype: str  # "f32" | "bf16"
+    bias_kind: str  # "uniform" | "zipf"
+    seed: int
+    x_seed: int
+    act_alpha: float = 1.702
+    act_limit: float = 7.0
+    act_beta: float = 1.0
+
+    @property
+    def H(self) -> int:
+        return self.hidden_size
+
+    @property
+    def E(self) -> int:
+        return self.num_experts
+
+    @property
+    def k(self) -> int:
+        return self.num_experts_per_tok
+
+    @property
+    def I(self) -> int:  # noqa: E743 - the pages' name for the expert width
+        return self.moe_intermediate_size
+
+    @property
+    def S(self) -> int:
+        return self.shared_intermediate_size
+
+    @property
+    def stacked_experts(self) -> int:
+        """Slices of the stacked gate/up/down tensors (E, or E+1 when packed)."""
+        return self.E + (1 if self.shared_packed else 0)
+
+    def with_tokens(self, T: int, x_seed: Optional[int] = None) -> "MoeShape":
+        return dataclasses.replace(self, T=T, x_seed=self.x_seed if x_seed is None else x_seed)
+
+    def replace(self, **kw) -> "MoeShape":
+        return dataclasses.replace(self, **kw)
+
+
+def _afmoe_default(T: int, bias_kind: str, seed: int, x_seed: int, name: str) -> MoeShape:
+    return MoeShape(
+        name=name, T=T, hidden_size=2048, num_experts=64, num_experts_per_tok=6,
+        moe_intermediate_size=1408, num_shared_experts=2, shared_intermediate_size=2 * 1408,
+        shared_packed=False, hidden_act="silu", score_func="sigmoid", route_norm=True,
+        route_scale=1.0, dtype="bf16", bias_kind=bias_kind, seed=seed, x_seed=x_seed)
+
+
+TINY = MoeShape(
+    name="tiny_f32_T64_H256_E16_k4", T=64, hidden_size=256, num_experts=16, num_experts_per_tok=4,
+    moe_intermediate_size=128, num_shared_experts=1, shared_intermediate_size=128,
+    shared_packed=False, hidden_act="silu", score_func="sigmoid", route_norm=True,
+    route_scale=2.826, dtype="f32", bias_kind="uniform", seed=1001, x_seed=1101)
+
+NANO_DECODE = MoeShape(
+    name="nano_decode_T256_H1024_E128_k8", T=256, hidden_size=1024, num_experts=128,
+    num_experts_per_tok=8, moe_intermediate_size=256, num_shared_experts=1,
+    shared_intermediate_size=256, shared_packed=False, hidden_act="silu", score_func="sigmoid",
+    route_norm=True, route_scale=2.826, dtype="bf16", bias_kind="uniform", seed=1002, x_seed=1102)
+
+AFMOE_PREFILL = _afmoe_default(4096, "uniform", 1003, 1103, "afmoe_prefill_T4096_H2048_E64_k6")
+
+M3 = MoeShape(
+    name="m3_T2048_H6144_E128_k4_packed", T=2048, hidden_size=6144, num_experts=128,
+    num_experts_per_tok=4, moe_intermediate_size=3072, num_shared_experts=1,
+    shared_intermediate_size=3072, shared_packed=True, hidden_act="swigluoai",
+    score_func="sigmoid", route_norm=False, route_scale=2.0, dtype="bf16", bias_kind="uniform",
+    seed=1004, x_seed=1104)
+
+ZIPF_TOKENS = (1, 8, 64, 512, 4096, 16384)
+
+
+def zipf_sweep(T: int) -> MoeShape:
+    return _afmoe_default(T, "zipf", 1005, 2000 + T, f"afmoe_zipf_T{T}")
+
+
+WORKLOADS = {
+    "tiny": TINY,
+    "nano_decode": NANO_DECODE,
+    "afmoe_prefill": AFMOE_PREFILL,
+    "m3": M3,
+    **{f"zipf_T{t}": zipf_sweep(t) for t in ZIPF_TOKENS},
+}
+
+
+def _torch_dtype(name: str) -> torch.dtype:
+    return {"f32": torch.float32, "bf16": torch.bfloat16}[name]
+
+
+def _normal(gen: torch.Generator, shape, std: float, dtype: torch.dtype, device) -> torch.Tensor:
+    v = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    if std != 1.0:
+        v.mul_(std)
+    return v.to(dtype)
+
+
+def _stacked(gen, n, rows, cols, dtype, device) -> torch.Tensor:
+    out = torch.empty((n, rows, cols), dtype=dtype, device=device)
+    for e in range(n):  # one slice at a time bounds the fp32 temporary
+        out[e].copy_(_normal(gen, (rows, cols), WEIGHT_STD, dtype, device))
+    return out
+
+
+def _bias(shape: MoeShape, gen: torch.Generator, device) -> torch.Tensor:
+    E = shape.E
+    if shape.bias_kind == "uniform":
+        u = torch.rand((E,), generator=gen, device=device, dtype=torch.float32)
+        return (u * 2.0 - 1.0) * BIAS_HALF_RANGE
+    if shape.bias_kind == "zipf":
+        ranks = torch.arange(1, E + 1, dtype=torch.float64)
+        z = ranks.pow(-ZIPF_S)
+        z = ZIPF_MAX * (z - z.min()) / (z.max() - z.min())
+        perm = torch.randperm(E, generator=gen, device=device).cpu()
+        b = torch.empty(E, dtype=torch.float64)
+        b[perm] = z  # expert perm[r-1] gets rank r
+        return b.to(torch.float32).to(device)
+    raise ValueError(shape.bias_kind)
+
+
+def make_inputs(shape: MoeShape, device="cpu",
+                row_filter: Optional[Callable[[torch.Tensor, torch.Tensor, torch.Tensor], torch.Tensor]] = None,
+                max_attempts: int = 64) -> dict:
+    """Draw every tensor of one workload on ``device``.
+
+    Returns a dict with X [T,H], router_w [E,H] fp32, expert_bias [E] fp32,
+    gate/up [E',I,H], down [E',H,I] (E' = E+1 when the shared expert is packed)
+    and, for a separate shared expert, sh_gate/sh_up [S,H], sh_down [H,S].
+    Expert tensors are fp32 for the f32 workload and bf16 otherwise.
+    ``redraws`` counts the token rows that ``row_filter`` sent back.
+    """
+    device = torch.device(device)
+    dt = _torch_dtype(shape.dtype)
+    g = torch.Generator(device=device)
+    g.manual_seed(shape.seed)
+    E, H, I, S = shape.E, shape.H, shape.I, shape.S
+    Ep = shape.stacked_experts
+
+    router_w = _normal(g, (E, H), WEIGHT_STD, dt, device).to(torch.float32)
+    expert_bias = _bias(shape, g, device)
+    gate = _stacked(g, Ep, I, H, dt, device)
+    up = _stacked(g, Ep, I, H, dt, device)
+    down = _stacked(g, Ep, H, I, dt, device)
+    sh_gate = sh_up = sh_down = None
+    if not shape.shared_packed and S > 0:
+        sh_gate = _normal(g, (S, H), WEIGHT_STD, dt, device)
+        sh_up = _normal(g, (S, H), WEIGHT_STD, dt, device)
+        sh_down = _normal(g, (H, S), WEIGHT_STD, dt, device)
+
+    gx = torch.Generator(device=device)
+    gx.manual_seed(shape.x_seed)
+    X = _normal(gx, (shape.T, H), 1.0, dt, device)
+
+    redraws = 0
+    if row_filter is not None and shape.T > 0:
+        for attempt in range(max_attempts):
+            bad = row_filter(X.cpu(), router_w.cpu(), expert_bias.cpu())
+            bad = torch.as_tensor(bad, dtype=torch.bool)
+            n_bad = int(bad.sum())
+            if n_bad == 0:
+                break
+            redraws += n_bad
+            gr = torch.Generator(device=device)
+            gr.manual_seed(shape.x_seed * 1_000_003 + attempt + 1)
+            rows = bad.nonzero().flatten().to(device)
+            X[rows] = _normal(gr, (n_bad, H), 1.0, dt, device)
+        else:
+            raise RuntimeError(f"{shape.name}: rows still rejected after {max_attempts} redraws")
+
+    return dict(X=X, router_w=router_w, expert_bias=expert_bias, gate=gate, up=up, down=down,
+                sh_gate=sh_gate, sh_up=sh_up, sh_down=sh_down, redraws=redraws)
+
+
+def expert_weights_bf16(inputs: dict) -> dict:
+    """bf16 (round-to-nearest-even) copies of the expert tensors, for the CUDA path.
+
+    The f32 workload stores fp32 expert weights; the CUDA path takes bf16 expert
+    weights, so they are rounded once here.  bf16 workloads pass through.
+    """
+    out = {}
+    for key in ("gate", "up", "down", "sh_gate", "sh_up", "sh_down"):
+        t = inputs[key]
+        out[key] = None if t is None else t.to(torch.bfloat16).contiguous()
+    return out

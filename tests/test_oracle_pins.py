@@ -1,0 +1,317 @@
+"""Pins of the fp64 oracle against things other than itself.
+
+Each test ties one step of the oracle to brute force, a closed form, a library
+routine (numpy matmul, scipy expit/softmax) on a special case, or an invariant
+the pages imply.  Shapes use H != I != S so a transposed operand fails.
+"""
+
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit, softmax
+
+import oracle
+from expert_routed_ffn_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _tiny(seed, T=7, H=24, E=8, k=3, I=40, S=0, packed=False, f32=True):
+    r = _rng(seed)
+    X = r.standard_normal((T, H)).astype(np.float32)
+    Wr = (r.standard_normal((E, H)) * 0.3).astype(np.float32)
+    b = r.uniform(-0.1, 0.1, E).astype(np.float32)
+    Ep = E + (1 if packed else 0)
+    Wg = (r.standard_normal((Ep, I, H)) * 0.2).astype(np.float32)
+    Wu = (r.standard_normal((Ep, I, H)) * 0.2).astype(np.float32)
+    Wd = (r.standard_normal((Ep, H, I)) * 0.2).astype(np.float32)
+    sh = (None, None, None)
+    if S:
+        sh = ((r.standard_normal((S, H)) * 0.2).astype(np.float32),
+              (r.standard_normal((S, H)) * 0.2).astype(np.float32),
+              (r.standard_normal((H, S)) * 0.2).astype(np.float32))
+    return X, Wr, b, Wg, Wu, Wd, sh
+
+
+def _silu_glu(g, u):
+    return g * expit(g) * u
+
+
+def _mlp_np(x, Wg, Wu, Wd, act=_silu_glu):
+    """Library-routine expert MLP: matmuls of numpy fp64."""
+    g = x.astype(np.float64) @ Wg.astype(np.float64).T
+    u = x.astype(np.float64) @ Wu.astype(np.float64).T
+    return act(g, u) @ Wd.astype(np.float64).T
+
+
+# ----------------------------------------------------------------- routing
+
+def test_logits_scores_biased_against_library_routines():
+    X, Wr, b, *_ = _tiny(1)
+    cfg = oracle.make_cfg(24, 8, 3, 40)
+    r = oracle.route(cfg, X, Wr, b)
+    l = X.astype(np.float64) @ Wr.astype(np.float64).T
+    np.testing.assert_allclose(r["logits"], l, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(r["scores"], expit(l), rtol=1e-13)
+    # the bias is added to the score, not the logit
+    np.testing.assert_allclose(r["biased"] - r["scores"], np.broadcast_to(b.astype(np.float64), l.shape),
+                               atol=1e-15)
+
+
+def test_softmax_variant_against_scipy():
+    X, Wr, b, *_ = _tiny(2)
+    cfg = oracle.make_cfg(24, 8, 3, 40, score_func="softmax")
+    r = oracle.route(cfg, X, Wr, b)
+    l = X.astype(np.float64) @ Wr.astype(np.float64).T
+    np.testing.assert_allclose(r["scores"], softmax(l, axis=1), rtol=1e-13)
+    np.testing.assert_allclose(r["scores"].sum(1), 1.0, rtol=1e-14)
+
+
+@pytest.mark.parametrize("E,k", [(5, 1), (6, 2), (8, 3), (10, 4), (7, 7)])
+def test_topk_set_is_brute_force_maximiser(E, k):
+    X, Wr, b, *_ = _tiny(10 + E * k, T=12, E=E, k=k)
+    r = oracle.route(oracle.make_cfg(24, E, k, 40), X, Wr, b)
+    for t in range(X.shape[0]):
+        c = r["biased"][t]
+        best = max(itertools.combinations(range(E), k), key=lambda s: sum(c[list(s)]))
+        assert sorted(r["idx"][t].tolist()) == sorted(best)
+        # returned in descending biased score
+        assert np.all(np.diff(c[r["idx"][t]]) <= 0)
+
+
+def test_tie_break_lowest_index():
+    H, E, k = 24, 8, 3
+    X = np.zeros((2, H), np.float32)  # logits 0 -> every score 0.5
+    Wr = np.ones((E, H), np.float32)
+    cfg = oracle.make_cfg(H, E, k, 40)
+    r = oracle.route(cfg, X, Wr, np.zeros(E, np.float32))
+    assert r["idx"].tolist() == [[0, 1, 2]] * 2
+    b = np.array([0, .1, .1, 0, .1, .1, 0, 0], np.float32)
+    r = oracle.route(cfg, X, Wr, b)
+    assert r["idx"].tolist() == [[1, 2, 4]] * 2
+
+
+def test_route_norm_and_scale():
+    X, Wr, b, *_ = _tiny(3, T=16)
+    cfg = oracle.make_cfg(24, 8, 3, 40, route_norm=True, route_scale=2.826)
+    r = oracle.route(cfg, X, Wr, b)
+    np.testing.assert_allclose(r["w"].sum(1), 2.826, rtol=1e-15)
+    s_sel = np.take_along_axis(r["scores"], r["idx"].astype(np.int64), 1)
+    np.testing.assert_allclose(r["w"], 2.826 * s_sel / s_sel.sum(1, keepdims=True), rtol=1e-14)
+    cfg_off = oracle.make_cfg(24, 8, 3, 40, route_norm=False, route_scale=2.0)
+    r2 = oracle.route(cfg_off, X, Wr, b)
+    np.testing.assert_allclose(r2["w"], 2.0 * expit(np.take_along_axis(r2["logits"], r2["idx"].astype(np.int64), 1)),
+                               rtol=1e-14)
+
+
+def test_bias_changes_selection_never_weights():
+    X, Wr, b, *_ = _tiny(4, T=10)
+    cfg = oracle.make_cfg(24, 8, 3, 40)
+    r0 = oracle.route(cfg, X, Wr, b)
+    # shift every bias by a constant: nothing changes
+    r1 = oracle.route(cfg, X, Wr, (b + np.float32(0.25)).astype(np.float32))
+    assert np.array_equal(r0["idx"], r1["idx"])
+    assert np.array_equal(r0["w"], r1["w"])
+    # raise the bias of already-selected experts of token 0: same set, same weights
+    b2 = b.copy()
+    b2[r0["idx"][0]] += np.float32(0.05)
+    r2 = oracle.route(cfg, X[:1], Wr, b2)
+    assert sorted(r2["idx"][0]) == sorted(r0["idx"][0])
+    w_by_e0 = dict(zip(r0["idx"][0].tolist(), r0["w"][0].tolist()))
+    w_by_e2 = dict(zip(r2["idx"][0].tolist(), r2["w"][0].tolist()))
+    assert w_by_e0 == w_by_e2
+    # a large bias on an unselected expert pulls it in; its weight is its UNBIASED score
+    out = [e for e in range(8) if e not in r0["idx"][0]][0]
+    b3 = b.copy()
+    b3[out] = np.float32(5.0)
+    r3 = oracle.route(cfg, X[:1], Wr, b3)
+    assert r3["idx"][0][0] == out
+    s = r3["scores"][0]
+    sel = r3["idx"][0]
+    np.testing.assert_allclose(r3["w"][0][0], s[out] / s[sel].sum(), rtol=1e-14)
+
+
+def test_margin_definition():
+    X, Wr, b, *_ = _tiny(5, T=9)
+    r = oracle.route(oracle.make_cfg(24, 8, 3, 40), X, Wr, b)
+    srt = -np.sort(-r["biased"], axis=1)
+    np.testing.assert_allclose(r["margin"], srt[:, 2] - srt[:, 3], rtol=1e-15)
+    rk = oracle.route(oracle.make_cfg(24, 8, 8, 40), X, Wr, b)
+    assert np.all(np.isinf(rk["margin"]))
+
+
+# ------------------------------------------------------------- activations
+
+def test_swigluoai_hand_points():
+    cfg = oracle.make_cfg(4, 1, 1, 4, act="swigluoai", alpha=1.702, limit=7.0, beta=1.0)
+    sig = lambda z: 1.0 / (1.0 + math.exp(-z))  # noqa: E731
+    # gate above the limit clamps to 7; up below -limit clamps to -7
+    assert oracle.act(cfg, 10.0, -9.0) == pytest.approx(7.0 * sig(1.702 * 7.0) * (-7.0 + 1.0), rel=1e-15)
+    # inside the limits nothing is clamped
+    assert oracle.act(cfg, 2.0, 3.0) == pytest.approx(2.0 * sig(1.702 * 2.0) * 4.0, rel=1e-15)
+    # the gate is clamped from above only
+    assert oracle.act(cfg, -12.0, 0.5) == pytest.approx(-12.0 * sig(-1.702 * 12.0) * 1.5, rel=1e-15)
+    # up clamps from above too
+    assert oracle.act(cfg, 1.0, 8.0) == pytest.approx(1.0 * sig(1.702) * 8.0, rel=1e-15)
+
+
+def test_swigluoai_reduces_to_silu_glu():
+    silu = oracle.make_cfg(4, 1, 1, 4, act="silu")
+    oai = oracle.make_cfg(4, 1, 1, 4, act="swigluoai", alpha=1.0, limit=float("inf"), beta=0.0)
+    r = _rng(6)
+    for g, u in r.standard_normal((50, 2)) * 6:
+        assert oracle.act(oai, g, u) == oracle.act(silu, g, u)
+        assert oracle.act(silu, g, u) == pytest.approx(g * expit(g) * u, rel=1e-14, abs=1e-300)
+
+
+def test_page_constants_match_workloads():
+    vals = {}
+    with open(os.path.join(GOLDEN, "page_constants.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                key, val, _cite = line.split()
+                vals[key] = float(val)
+    assert wl.NANO_DECODE.route_scale == vals["trinity_route_scale"] == wl.TINY.route_scale
+    assert wl.NANO_DECODE.H == vals["trinity_nano_hidden"] and wl.NANO_DECODE.E == vals["trinity_nano_experts"]
+    a = wl.AFMOE_PREFILL
+    assert (a.H, a.I, a.E, a.k, a.num_shared_experts, a.route_scale) == (
+        vals["afmoe_hidden_size"], vals["afmoe_moe_intermediate_size"], vals["afmoe_num_experts"],
+        vals["afmoe_num_experts_per_tok"], vals["afmoe_num_shared_experts"], vals["afmoe_route_scale"])
+    assert wl.WEIGHT_STD == vals["afmoe_initializer_range"]
+    m = wl.M3
+    assert (m.H, m.E, m.k, m.route_scale, m.S) == (
+        vals["m3_hidden_size"], vals["m3_num_local_experts"], vals["m3_num_experts_per_tok"],
+        vals["m3_routed_scaling_factor"], vals["m3_shared_intermediate_size"])
+    assert m.shared_packed and m.stacked_experts - 1 == vals["m3_packed_shared_index"]
+    assert (m.act_alpha, m.act_limit, m.act_beta) == (
+        vals["swigluoai_alpha"], vals["swigluoai_limit"], vals["swigluoai_beta"])
+
+
+# ------------------------------------------------------------ expert MLPs
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_single_expert_reduces_to_plain_swiglu_mlp(dtype):
+    """E = 1, k = 1, norm on, scale 1, no shared: Y is one SwiGLU MLP."""
+    X, Wr, b, Wg, Wu, Wd, _ = _tiny(7, T=5, E=1, k=1)
+    cfg = oracle.make_cfg(24, 1, 1, 40, route_norm=True, route_scale=1.0)
+    if dtype == "bf16":
+        Wg, Wu, Wd = (torch.from_numpy(a).to(torch.bfloat16) for a in (Wg, Wu, Wd))
+        ref = _mlp_np(X, Wg[0].double().numpy(), Wu[0].double().numpy(), Wd[0].double().numpy())
+    else:
+        ref = _mlp_np(X, Wg[0], Wu[0], Wd[0])
+    Y = oracle.forward(cfg, X, Wr, b, Wg, Wu, Wd)
+    np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_expert_intermediates_against_numpy():
+    X, Wr, b, Wg, Wu, Wd, _ = _tiny(8, T=1)
+    cfg = oracle.make_cfg(24, 8, 3, 40, act="swigluoai", alpha=1.702, limit=0.5, beta=1.0)
+    g, u, a, y = oracle.expert(cfg, X[0], Wg[2], Wu[2], Wd[2], 40)
+    x = X[0].astype(np.float64)
+    np.testing.assert_allclose(g, Wg[2].astype(np.float64) @ x, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(u, Wu[2].astype(np.float64) @ x, rtol=1e-13, atol=1e-15)
+    assert (np.abs(u) > 0.5).any() and (g > 0.5).any()  # the clamp fires at limit 0.5
+    gc, uc = np.minimum(g, 0.5), np.clip(u, -0.5, 0.5)
+    np.testing.assert_allclose(a, gc * expit(1.702 * gc) * (uc + 1.0), rtol=1e-14)
+    np.testing.assert_allclose(y, Wd[2].astype(np.float64) @ a, rtol=1e-12, atol=1e-15)
+
+
+def _dense_mask_reference(X, Wr, b, Wg, Wu, Wd, sh, E, k, route_norm, scale, packed=False):
+    """Every expert on every token, masked by a brute-force top-k set."""
+    l = X.astype(np.float64) @ Wr.astype(np.float64).T
+    s = expit(l)
+    c = s + b.astype(np.float64)
+    Y = np.zeros((X.shape[0], X.shape[1]))
+    ys = np.stack([_mlp_np(X, Wg[e], Wu[e], Wd[e]) for e in range(E)], 1)  # [T,E,H]
+    for t in range(X.shape[0]):
+        sel = list(max(itertools.combinations(range(E), k), key=lambda q: sum(c[t, list(q)])))
+        m = np.zeros(E)
+        m[sel] = 1.0
+        w = s[t] * m
+        if route_norm:
+            w = w / w.sum()
+        Y[t] = (scale * w) @ ys[t]
+    if packed:
+        Y += _mlp_np(X, Wg[E], Wu[E], Wd[E])
+    elif sh[0] is not None:
+        Y += _mlp_np(X, *sh)
+    return Y
+
+
+@pytest.mark.parametrize("route_norm,scale", [(True, 2.826), (False, 2.0)])
+def test_forward_equals_dense_mask_formulation(route_norm, scale):
+    X, Wr, b, Wg, Wu, Wd, sh = _tiny(9, T=9, E=6, k=2, S=56)
+    cfg = oracle.make_cfg(24, 6, 2, 40, S=56, route_norm=route_norm, route_scale=scale)
+    Y = oracle.forward(cfg, X, Wr, b, Wg, Wu, Wd, *sh)
+    ref = _dense_mask_reference(X, Wr, b, Wg, Wu, Wd, sh, 6, 2, route_norm, scale)
+    np.testing.assert_allclose(Y, ref, rtol=1e-11, atol=1e-13)
+
+
+def test_topk_equals_E_zero_bias_is_dense_weighted_sum():
+    E = 5
+    X, Wr, _, Wg, Wu, Wd, sh = _tiny(11, T=6, E=E, k=E, S=32)
+    cfg = oracle.make_cfg(24, E, E, 40, S=32, route_norm=True, route_scale=1.7)
+    Y = oracle.forward(cfg, X, Wr, np.zeros(E, np.float32), Wg, Wu, Wd, *sh)
+    s = expit(X.astype(np.float64) @ Wr.astype(np.float64).T)
+    ref = sum((1.7 * s[:, e] / s.sum(1))[:, None] * _mlp_np(X, Wg[e], Wu[e], Wd[e]) for e in range(E))
+    ref = ref + _mlp_np(X, *sh)
+    np.testing.assert_allclose(Y, ref, rtol=1e-11, atol=1e-13)
+
+
+def test_packed_shared_equals_separate_shared_mlp():
+    E = 6
+    X, Wr, b, Wg, Wu, Wd, _ = _tiny(12, T=8, E=E, k=2, packed=True)
+    packed = oracle.make_cfg(24, E, 2, 40, shared_packed=True, route_norm=False, route_scale=2.0)
+    sep = oracle.make_cfg(24, E, 2, 40, S=40, route_norm=False, route_scale=2.0)
+    Yp = oracle.forward(packed, X, Wr, b, Wg, Wu, Wd)
+    Ys = oracle.forward(sep, X, Wr, b, Wg[:E], Wu[:E], Wd[:E], Wg[E], Wu[E], Wd[E])
+    assert np.array_equal(Yp, Ys)
+    # and the packed slice never enters top-k: routing sees only E experts
+    r = oracle.route(packed, X, Wr, b)
+    assert r["idx"].max() < E
+    ref = _dense_mask_reference(X, Wr, b, Wg, Wu, Wd, None, E, 2, False, 2.0, packed=True)
+    np.testing.assert_allclose(Yp, ref, rtol=1e-11, atol=1e-13)
+
+
+def test_two_shared_experts_equal_one_of_double_width():
+    X, Wr, b, Wg, Wu, Wd, sh = _tiny(13, T=5, S=40)
+    X2, _, _, _, _, _, sh2 = _tiny(14, T=5, S=40)
+    cfg1 = oracle.make_cfg(24, 8, 3, 40, S=80)
+    cat = (np.concatenate([sh[0], sh2[0]]), np.concatenate([sh[1], sh2[1]]),
+           np.concatenate([sh[2], sh2[2]], axis=1))
+    Y = oracle.forward(cfg1, X, Wr, b, Wg, Wu, Wd, *cat)
+    cfg0 = oracle.make_cfg(24, 8, 3, 40, S=0)
+    Yr = oracle.forward(cfg0, X, Wr, b, Wg, Wu, Wd)
+    for t in range(X.shape[0]):
+        _, _, _, y1 = oracle.expert(cfg1, X[t], *sh, 40)
+        _, _, _, y2 = oracle.expert(cfg1, X[t], *sh2, 40)
+        np.testing.assert_allclose(Y[t], Yr[t] + y1 + y2, rtol=1e-12, atol=1e-14)
+
+
+def test_token_permutation_equivariance_and_thread_independence():
+    X, Wr, b, Wg, Wu, Wd, sh = _tiny(15, T=11, S=24)
+    cfg = oracle.make_cfg(24, 8, 3, 40, S=24, route_scale=2.826)
+    Y = oracle.forward(cfg, X, Wr, b, Wg, Wu, Wd, *sh, nthreads=3)
+    perm = _rng(16).permutation(11)
+    Yp = oracle.forward(cfg, X[perm], Wr, b, Wg, Wu, Wd, *sh, nthreads=1)
+    assert np.array_equal(Yp, Y[perm])
+    Ysub = oracle.forward(cfg, X, Wr, b, Wg, Wu, Wd, *sh, tokens=[7, 2, 7])
+    assert np.array_equal(Ysub, Y[[7, 2, 7]])
+
+
+def test_margin_filter_drives_generator_redraws():
+    shape = wl.TINY.replace(T=48)
+    inp = wl.make_inputs(shape, "cpu", row_filter=oracle.margin_filter(shape))
+    r = oracle.route_inputs(shape, inp)
+    assert r["margin"].min() >= 1e-3
+    # same seed, same draws
+    inp2 = wl.make_inputs(shape, "cpu", row_filter=oracle.margin_filter(shape))
+    assert torch.equal(inp["X"], inp2["X"]) and inp["redraws"] == inp2["redraws"]
