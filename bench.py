@@ -1,0 +1,372 @@
+#!/usr/bin/env python
+"""Throughput of the token-choice MoE FFN block (AFMoE / MiniMax-M3) on GB300.
+
+One step = one moe_forward over one batch of T synthetic tokens (router,
+dispatch sort, gate/up + activation, down, combine), inputs resident in HBM.
+L2 is flushed (a 256 MiB write) before every step, outside the timed events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica
+of the block on its own GPU (the block has no cross-GPU exchange): weak scaling.
+--impl reference times the fp64 CPU oracle on the host cores instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (bf16) and % of roofline (tensor peak / HBM GB/s at small T)"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def work_model(shape, U: int):
+    """Algorithmic FLOPs and HBM bytes of one forward and of its expert kernels.
+
+    FLOPs  F = T (2HE + 6HIk + 6HS); bytes B = U*3HI*2 + 3HS*2 + 4EH + 4E + 2*2TH,
+    U = experts that received at least one token (the packed shared expert's
+    weights are its 3HS*2 bytes).  Intermediate buffers are implementation
+    traffic and are not counted."""
+    T, H, E, k, I, S = shape.T, shape.H, shape.E, shape.k, shape.I, shape.S
+    F = T * (2 * H * E + 6 * H * I * k + 6 * H * S)
+    B = U * 3 * H * I * 2 + 3 * H * S * 2 + 4 * E * H + 4 * E + 2 * 2 * T * H
+    kernels = {
+        "gate_up": dict(flops=4 * T * H * (k * I + S), bytes=(U * 2 * H * I + 2 * H * S) * 2 + 2 * T * H),
+        "down": dict(flops=2 * T * H * (k * I + S), bytes=(U * H * I + H * S) * 2 + 2 * T * H),
+    }
+    return F, B, kernels
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.proc = None
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(", ") for r in self.f.read().splitlines() if r.count(",") >= 8]
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != gpus:
+        raise SystemExit(f"--gpus {gpus} but WORLD_SIZE {world}")
+    return world, rank, local
+
+
+def run_ours(args, shape):
+    import torch
+    import torch.distributed as dist
+
+    from expert_routed_ffn_gb300 import build as moe_build
+    from expert_routed_ffn_gb300 import capi
+    from expert_routed_ffn_gb300 import workloads as wl
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 or world == 1:
+        moe_build.build()
+    if world > 1:
+        dist.barrier()
+    dev = torch.device("cuda", local)
+    inputs = wl.make_inputs(shape, dev)
+    blk = capi.block_from_inputs(shape, inputs, max_tokens=shape.T)
+    if args.path:
+        blk.set_option(capi.MOE_OPT_PATH, {"decode": capi.PATH_DECODE, "grouped": capi.PATH_GROUPED}[args.path])
+    blk.set_option(capi.MOE_OPT_STAGE_EVENTS, 1)
+    X = inputs["X"]
+    Y = torch.empty_like(X)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        flush.fill_(1)  # evicts L2; not inside the timed events
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record()
+        blk.forward(X, Y)
+        e.record()
+        return s, e
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if blk.sync_status() != capi.MOE_OK:
+        raise SystemExit("device error during warm-up")
+    idx = blk.inspect(capi.MOE_BUF_TOPK_IDX, shape.T * shape.k, torch.int32)
+    U = int(torch.unique(idx).numel())
+    launches = blk.stats().kernel_launches
+    path = blk.stats().path
+    names = capi.STAGE_NAMES_DECODE if path == capi.PATH_DECODE else capi.STAGE_NAMES_GROUPED
+
+    sampler = ClockSampler(getattr(torch.cuda.get_device_properties(dev), "uuid", None) and
+                           f"GPU-{torch.cuda.get_device_properties(dev).uuid}")
+    t_end = time.perf_counter() + 1.0  # untimed pre-roll: steady clocks, samples under load
+    while time.perf_counter() < t_end:
+        step()
+        torch.cuda.synchronize()
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    per_step, stage_sum = [], [0.0] * len(names)
+    for _ in range(args.steps):
+        s, e = step()
+        st = blk.stage_times()  # waits for this step's events
+        per_step.append(s.elapsed_time(e))
+        for i, v in enumerate(st[:len(names)]):
+            stage_sum[i] += v
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    status = blk.sync_status()
+    if status != capi.MOE_OK:
+        raise SystemExit(f"device error during the timed steps: {capi.STATUS_NAMES[status]}")
+
+    ms = sum(per_step) / len(per_step)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * shape.T / (ms / 1e3)
+
+    # end to end through the host-buffer entry point: H2D of X, forward, D2H of Y per step
+    Xh = X.cpu().pin_memory()
+    Yh = torch.empty_like(Xh).pin_memory()
+    for _ in range(max(1, args.warmup)):
+        blk.forward_host(Xh, Yh)
+    e2e_t = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        blk.forward_host(Xh, Yh)
+        e2e_t.append(time.perf_counter() - t0)
+    e2e_s = sum(e2e_t) / len(e2e_t)
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    xbytes = Xh.numel() * Xh.element_size()
+
+    pk, pk_src = peaks()
+    F, B, kern = work_model(shape, U)
+    t_tc, t_hbm = F / (pk["bf16_tflops"] * 1e12), B / (pk["hbm_gbs"] * 1e9)
+    stage_avg = {n: stage_sum[i] / args.steps for i, n in enumerate(names)}
+    dom = max(stage_avg, key=stage_avg.get)
+    roof = None
+    key = {"gate_up_gemm": "gate_up", "decode_gate_up": "gate_up", "down_gemm": "down",
+           "decode_down": "down"}.get(dom)
+    if key is not None:
+        kw = kern[key]
+        dur = stage_avg[dom] / 1e3
+        tensor_time = kw["flops"] / (pk["bf16_tflops"] * 1e12)
+        hbm_time = kw["bytes"] / (pk["hbm_gbs"] * 1e9)
+        if tensor_time > hbm_time:
+            ach = kw["flops"] / dur / 1e12
+            roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": round(ach / pk["bf16_tflops"], 4)}
+        else:
+            ach = kw["bytes"] / dur / 1e9
+            roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(ach / pk["hbm_gbs"], 4)}
+        roof.update({"kernel": dom, "peak_source": pk_src, "traffic": traffic_of(dom, shape.name),
+                     "algorithmic_per_launch": kw["bytes"] if roof["bound"] == "hbm" else kw["flops"]})
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, U(-0.1,0.1) or Zipf bias)",
+        "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "E": shape.E, "k": shape.k,
+                   "I": shape.I, "S": shape.S, "shared_packed": shape.shared_packed,
+                   "hidden_act": shape.hidden_act, "path": {1: "decode", 2: "grouped"}[path],
+                   "parallelism": f"replicas{world}",
+                   "l2": "flushed before every step (256 MiB write), flush outside the timed events"},
+        "roofline": roof,
+        "block_roofline": {"t_roof_us": round(max(t_tc, t_hbm) * 1e6, 2), "t_meas_us": round(ms * 1e3, 2),
+                           "frac": round(max(t_tc, t_hbm) / (ms / 1e3), 4),
+                           "bound": "tensor" if t_tc > t_hbm else "hbm", "flops": F, "bytes": B,
+                           "experts_touched": U, "tflops": round(F / (ms / 1e3) / 1e12, 2),
+                           "gbs": round(B / (ms / 1e3) / 1e9, 1), "peak_source": pk_src},
+        "stage_us": {n: round(v * 1e3, 2) for n, v in stage_avg.items()},
+        "e2e": {"value": round(world * shape.T / e2e_s, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": xbytes, "d2h_bytes_per_step": xbytes},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(shape, inputs, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    blk.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def traffic_of(stage: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of that kernel; else None."""
+    import hashlib
+    src = {"gate_up_gemm": "gemm_tc.cu", "down_gemm": "gemm_tc.cu", "decode_gate_up": "stream.cu",
+           "decode_down": "stream.cu"}.get(stage)
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if src is None or not os.path.exists(path):
+        return None
+    with open(os.path.join(ROOT, "expert_routed_ffn_gb300", "csrc", src), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == stage and parts[1] == workload \
+                    and parts[3] == sha:
+                return int(float(parts[2]))
+    return None
+
+
+def cpu_baseline(shape, inputs, budget_s=10.0):
+    """The fp64 oracle, as it stands, on the host cores: whole-workload passes
+    (or a token sample of it) until about budget_s of wall time."""
+    import torch
+
+    import oracle
+    host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inputs.items()}
+    cores = os.cpu_count() or 1
+    n = shape.T
+    t0 = time.perf_counter()
+    oracle.forward_inputs(shape, host, tokens=list(range(min(n, cores))), nthreads=cores)
+    per_tok = (time.perf_counter() - t0) / min(n, cores)
+    n = max(1, min(shape.T, int(budget_s / 3 / max(per_tok, 1e-9))))
+    toks = list(range(n))
+    times = []
+    t_start = time.perf_counter()
+    while len(times) < 3 or time.perf_counter() - t_start < budget_s:
+        t0 = time.perf_counter()
+        oracle.forward_inputs(shape, host, tokens=toks, nthreads=cores)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > 3 * budget_s:
+            break
+    med = statistics.median(times)
+    return {"value": round(n / med, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"tokens 0..{n - 1} of the {shape.name} workload, {len(times)} passes, median"}
+
+
+def run_reference(args, shape):
+    """The fp64 CPU oracle as the reference arm, on the host cores."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from expert_routed_ffn_gb300 import workloads as wl
+    oracle.build()
+    inputs = wl.make_inputs(shape, "cpu")
+    cores = os.cpu_count() or 1
+    # size each step to about one second of oracle work
+    t0 = time.perf_counter()
+    oracle.forward_inputs(shape, inputs, tokens=list(range(min(shape.T, cores))), nthreads=cores)
+    per_tok = (time.perf_counter() - t0) / min(shape.T, cores)
+    n = max(1, min(shape.T, int(1.0 / max(per_tok, 1e-9))))
+    toks = list(range(n))
+    for _ in range(args.warmup):
+        oracle.forward_inputs(shape, inputs, tokens=toks, nthreads=cores)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.forward_inputs(shape, inputs, tokens=toks, nthreads=cores)
+        times.append(time.perf_counter() - t0)
+    s = sum(times) / len(times)
+    value = n / s
+    sample = f"tokens 0..{n - 1} of the {shape.name} workload per step"
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, same recipe as the GPU arm)",
+        "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "E": shape.E, "k": shape.k,
+                   "I": shape.I, "S": shape.S, "tokens_per_step": n},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="nano_decode")
+    ap.add_argument("--path", choices=["decode", "grouped"], default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    from expert_routed_ffn_gb300 import workloads as wl
+    shape = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, shape)
+    else:
+        run_ours(args, shape)
+
+
+if __name__ == "__main__":
+    main()

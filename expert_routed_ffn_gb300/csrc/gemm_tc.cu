@@ -1,0 +1,372 @@
+// Grouped GEMMs of the expert MLPs on the 5th-generation tensor cores (K3, K4, K5).
+//
+//   gate/up (glu = 1):  H_out[r, i] = act( A[r,:] . Wg[g][i,:],  A[r,:] . Wu[g][i,:] )
+//   down    (glu = 0):  Y_out[r, j] = A[r,:] . Wd[g][j,:]
+//
+// One launch covers up to two segments: the routed experts (rows grouped by
+// expert through the dispatch offsets, weight slice = expert id) and the
+// shared expert (all T token rows, one weight slice).  Weights are the
+// pre-stacked [groups, out, in] tensors (Arcee AFMoE issue, "Checkpoint weight
+// layout"; the packed shared expert of the MiniMax-M3 issue is slice E).
+//
+// Persistent kernel, one CTA per SM, 6 warps:
+//   warp 0     TMA producer: A tile 128 x 64 and B tile 256 x 64 (gate/up: 128
+//              gate rows + 128 up rows) per stage, 128-byte swizzle, 4 stages
+//   warp 1     allocates 512 TMEM columns; lane 0 issues tcgen05.mma
+//              (M 128, N 256, K 16, bf16 in, fp32 accumulate) into one of two
+//              TMEM accumulators, so the epilogue of one tile overlaps the
+//              main loop of the next
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
+//              32*(w%4)..+31 = tile rows), activation (gate/up), bf16 stores
+// Tiles are (segment, group, m-tile, n-tile), handed out round-robin; inside a
+// group the m-tiles of one n-tile are adjacent so concurrent CTAs share the
+// weight tile in L2.  Every wait is bounded: on timeout the kernel records
+// ERR_TIMEOUT, stops all roles, drains its in-flight copies and MMAs, frees
+// TMEM and returns.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kABytes = kGemmBM * kGemmBK * 2;  // 16 KB
+constexpr int kBBytes = kGemmBN * kGemmBK * 2;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;             // two 128 x 256 fp32 accumulators
+constexpr uint64_t kDrainNs = 1000000000ull;    // bound of the drain after an abort
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+
+struct Tile {
+    int seg, group, mt, nt, row0, m_valid;
+};
+
+__device__ __forceinline__ int seg_tiles(const GemmSegment &s) {
+    if (s.dense) return ((s.m_dense + kGemmBM - 1) / kGemmBM) * s.n_tiles;
+    return s.tile_offs[s.num_groups] * s.n_tiles;
+}
+
+__device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, int tiles0) {
+    Tile t;
+    t.seg = 0;
+    if (tile >= tiles0) {
+        t.seg = 1;
+        tile -= tiles0;
+    }
+    const GemmSegment &s = p.seg[t.seg];
+    if (s.dense) {
+        const int mtiles = (s.m_dense + kGemmBM - 1) / kGemmBM;
+        t.group = 0;
+        t.nt = tile / mtiles;
+        t.mt = tile % mtiles;
+        t.row0 = t.mt * kGemmBM;
+        t.m_valid = min(kGemmBM, s.m_dense - t.row0);
+    } else {
+        // largest group whose first tile is <= tile (empty groups own no tiles)
+        int lo = 0, hi = s.num_groups - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s.tile_offs[mid] * s.n_tiles <= tile)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int mt_g = s.tile_offs[lo + 1] - s.tile_offs[lo];
+        const int local = tile - s.tile_offs[lo] * s.n_tiles;
+        t.group = lo;
+        t.nt = local / mt_g;
+        t.mt = local % mt_g;
+        const int start = s.offs[lo];
+        t.row0 = start + t.mt * kGemmBM;
+        t.m_valid = min(kGemmBM, s.offs[lo + 1] - t.row0);
+    }
+    return t;
+}
+
+__device__ __forceinline__ void raise_abort(int *err, volatile int *abort_flag) {
+    if (err != nullptr) atomicOr(err, ERR_TIMEOUT);
+    *abort_flag = 1;
+}
+
+template <bool GLU>
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sA = smem_u32(smem);
+    const uint32_t sB = sA + kStages * kABytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+    const uint32_t bar0 = smem_u32(bars);
+    // barriers: full[kStages], empty[kStages], tfull[2], tempty[2], drain
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto tfull_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kStages + a); };
+    auto tempty_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *tile_count = reinterpret_cast<int *>(tmem_slot + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (uint32_t a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 128);
+        }
+        mbar_init(drain_bar, 1);
+        fence_mbar_init();
+        *abort_flag = 0;
+        const int t0 = seg_tiles(p.seg[0]);
+        tile_count[0] = t0;
+        tile_count[1] = t0 + (p.num_segs > 1 ? seg_tiles(p.seg[1]) : 0);
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&p.A0);
+        tma_prefetch_desc(&p.B0);
+        if (GLU) tma_prefetch_desc(&p.B1);
+        if (p.num_segs > 1) {
+            tma_prefetch_desc(&p.A1);
+            tma_prefetch_desc(&p.B2);
+            if (GLU) tma_prefetch_desc(&p.B3);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int tiles0 = tile_count[0], total = tile_count[1];
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t L = 0;  // loads issued so far; stage = L % kStages
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const Tile t = decode_tile(p, tile, tiles0);
+                const GemmSegment &sg = p.seg[t.seg];
+                const CUtensorMap *mA = t.seg ? &p.A1 : &p.A0;
+                const CUtensorMap *mB = t.seg ? &p.B2 : &p.B0;
+                const CUtensorMap *mB2 = t.seg ? &p.B3 : &p.B1;
+                const int g = sg.group_base + t.group;
+                for (int kb = 0; kb < sg.k_blocks; ++kb) {
+                    const int s = L % kStages;
+                    const uint32_t ph = (L / kStages) & 1u;
+                    if (!mbar_wait(empty_bar(s), ph ^ 1u, p.wait_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+                    tma_load_2d(sA + s * kABytes, mA, full_bar(s), kb * kGemmBK, t.row0);
+                    if (GLU) {
+                        tma_load_3d(sB + s * kBBytes, mB, full_bar(s), kb * kGemmBK, t.nt * 128, g);
+                        tma_load_3d(sB + s * kBBytes + kBBytes / 2, mB2, full_bar(s), kb * kGemmBK,
+                                    t.nt * 128, g);
+                    } else {
+                        tma_load_3d(sB + s * kBBytes, mB, full_bar(s), kb * kGemmBK, t.nt * kGemmBN, g);
+                    }
+                    ++L;
+                }
+            }
+            if (!ok) {
+                raise_abort(p.err, abort_flag);
+                // wait for the copies still in flight (the last load of each stage)
+                for (uint32_t i = 0; i < (uint32_t)kStages && i < L; ++i) {
+                    const uint32_t l = L - 1 - i;
+                    mbar_wait(full_bar(l % kStages), (l / kStages) & 1u, kDrainNs, nullptr);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kGemmBM, kGemmBN);
+            uint32_t L = 0, n_acc = 0;
+            bool ok = true, issued = false;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const Tile t = decode_tile(p, tile, tiles0);
+                const GemmSegment &sg = p.seg[t.seg];
+                const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
+                if (!mbar_wait(tempty_bar(a), aph ^ 1u, p.wait_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + a * kGemmBN;
+                for (int kb = 0; kb < sg.k_blocks; ++kb) {
+                    const int s = L % kStages;
+                    const uint32_t ph = (L / kStages) & 1u;
+                    if (!mbar_wait(full_bar(s), ph, p.wait_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = smem_desc_k128(sA + s * kABytes);
+                    const uint64_t bd = smem_desc_k128(sB + s * kBBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes per K step of 16
+                        tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    issued = true;
+                    tc_commit(empty_bar(s));  // frees the stage once these MMAs have read it
+                    ++L;
+                }
+                if (!ok) break;
+                tc_commit(tfull_bar(a));  // accumulator complete
+                ++n_acc;
+            }
+            if (!ok) {
+                raise_abort(p.err, abort_flag);
+                if (issued) {
+                    tc_commit(drain_bar);
+                    mbar_wait(drain_bar, 0, kDrainNs, nullptr);
+                }
+            }
+        }
+    } else {
+        // ----------------------------------------------------------- epilogue
+        const int q = warp & 3;  // TMEM lane quadrant this warp may read
+        const int r = q * 32 + lane;
+        uint32_t n_acc = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            const Tile t = decode_tile(p, tile, tiles0);
+            const GemmSegment &sg = p.seg[t.seg];
+            const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
+            // every lane waits; the answer is made warp-uniform because the
+            // tcgen05.ld below is .sync.aligned
+            const bool ready = __all_sync(0xffffffffu, mbar_wait(tfull_bar(a), aph, p.wait_ns, abort_flag));
+            if (!ready) {
+                if (lane == 0) raise_abort(p.err, abort_flag);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + a * kGemmBN;
+            const bool row_ok = r < t.m_valid;
+            bf16 *orow = sg.out + (size_t)(t.row0 + (row_ok ? r : 0)) * sg.ldo;
+            if (GLU) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    uint32_t g[32], u[32];
+                    tmem_ld32(tb + c0, g);
+                    tmem_ld32(tb + 128 + c0, u);
+                    tmem_ld_wait();
+                    const int col = t.nt * 128 + c0;
+                    if (row_ok && col < sg.n_out) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack_bf16x2(
+                                glu_act(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), p.act,
+                                        p.alpha, p.limit, p.beta),
+                                glu_act(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]),
+                                        p.act, p.alpha, p.limit, p.beta));
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c0 = 0; c0 < kGemmBN; c0 += 32) {
+                    uint32_t v32[32];
+                    tmem_ld32(tb + c0, v32);
+                    tmem_ld_wait();
+                    const int col = t.nt * kGemmBN + c0;
+                    if (row_ok && col < sg.n_out) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack_bf16x2(__uint_as_float(v32[2 * i]), __uint_as_float(v32[2 * i + 1]));
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tempty_bar(a));
+            ++n_acc;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+size_t gemm_tc_smem_bytes() { return kSmemBytes; }
+
+CUresult encode_map_a(CUtensorMap *m, const void *ptr, int rows, int K) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kGemmBK, (cuuint32_t)kGemmBM};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult encode_map_b(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)groups};
+    const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)rows * K * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)kGemmBK, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
+    if (a.glu)
+        gemm_tc_kernel<true><<<a.num_ctas, kThreads, kSmemBytes, s>>>(a);
+    else
+        gemm_tc_kernel<false><<<a.num_ctas, kThreads, kSmemBytes, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

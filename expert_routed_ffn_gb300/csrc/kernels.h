@@ -1,0 +1,156 @@
+// Host-side launchers of the MoE kernels (internal to libmoe.so).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+using bf16 = __nv_bfloat16;
+
+// Bits of the device error word.
+enum : int { ERR_TIMEOUT = 1, ERR_BOUNDS = 2 };
+
+// ---------------------------------------------------------------- router (K1)
+// Per token: fp32 logits against the fp32 router weights, sigmoid (or softmax)
+// scores, top-k of score + bias (ties to the lower expert index), weights
+// gathered from the unbiased scores, optional renormalisation, route_scale.
+// Each CTA also writes the expert histogram of its tokens to blk_hist.
+struct RouterArgs {
+    const void *X;         // [T, H], bf16 or fp32
+    int x_f32;             // 1 when X is fp32
+    int T, H, E, k;
+    const float *Wr;       // [E, H]
+    const float *bias;     // [E] or nullptr
+    int score_func;        // 0 sigmoid, 1 softmax
+    int route_norm;
+    float route_scale;
+    int32_t *topk_idx;     // [T, k]
+    float *topk_w;         // [T, k]
+    int32_t *blk_hist;     // [num_blocks, E] or nullptr
+    __nv_bfloat16 *x_bf16; // [T, H] bf16 copy of fp32 X, or nullptr
+    int tokens_per_block;  // 16 or 32
+};
+int router_tokens_per_block(int T, int num_sms);
+cudaError_t launch_router(const RouterArgs &a, cudaStream_t s);
+
+// ------------------------------------------------------- dispatch sort (K2)
+// offs[e] = first sorted row of expert e (exclusive scan of the counts),
+// tile_offs[e] = exclusive scan of ceil(count_e / 128), active[0..n) = experts
+// with rows, active[E] = n.  blk_hist becomes the first row of each
+// (block, expert) pair.  Rows are ordered by (expert, token, slot): stable.
+struct ScanArgs {
+    int32_t *blk_hist;  // [nb, E] in: counts, out: base rows
+    int nb, E;
+    int32_t *offs;      // [E + 1]
+    int32_t *tile_offs; // [E + 1]
+    int32_t *active;    // [E + 1]
+};
+cudaError_t launch_scan(const ScanArgs &a, cudaStream_t s);
+
+struct ScatterArgs {
+    const int32_t *topk_idx;  // [T, k]
+    const int32_t *blk_base;  // [nb, E]
+    int T, k, E, H;
+    int tokens_per_block;
+    const void *X;            // [T, H]
+    int x_f32;
+    int32_t *sorted_tok;      // [T*k]
+    int32_t *slot_of;         // [T*k]
+    __nv_bfloat16 *x_sorted;  // [T*k, H]
+    int *err;
+};
+cudaError_t launch_scatter(const ScatterArgs &a, cudaStream_t s);
+
+// --------------------------------------------------------------- combine (K7)
+// Y[t] = sum_j w[t,j] * Yslot[slot_of[t,j]] + Ys[t]  (fp32 sum, fixed order).
+struct CombineArgs {
+    const __nv_bfloat16 *yslot;  // [T*k, H]
+    const __nv_bfloat16 *ys;     // [T, H] or nullptr
+    const float *topk_w;         // [T, k]
+    const int32_t *slot_of;      // [T, k]
+    int T, k, H;
+    void *Y;                     // [T, H]
+    int y_f32;
+};
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
+
+// ------------------------------------------- tcgen05 grouped GEMMs (K3/K4/K5)
+constexpr int kGemmBM = 128;   // rows (tokens) per tile: the MMA's M
+constexpr int kGemmBK = 64;    // K per pipeline stage (one 128-byte swizzle row of bf16)
+constexpr int kGemmBN = 256;   // MMA N; gate/up tiles hold 128 gate + 128 up columns
+
+struct GemmSegment {
+    int dense;             // 1: one group of m_dense rows from row 0; 0: groups by offs
+    int num_groups;
+    int group_base;        // weight-map coordinate of group 0
+    int m_dense;
+    const int32_t *offs;   // [num_groups + 1] (grouped)
+    const int32_t *tile_offs;
+    int n_tiles;           // output tiles per group along N
+    int k_blocks;          // K / 64
+    int n_out;             // valid output columns
+    __nv_bfloat16 *out;    // [rows, ldo]
+    int ldo;
+};
+
+struct GemmArgs {
+    // maps: segment 0 reads A0 and B0 (+B1 for gate/up); segment 1 reads A1 and B2 (+B3)
+    CUtensorMap A0, A1, B0, B1, B2, B3;
+    GemmSegment seg[2];
+    int num_segs;
+    int glu;               // 1: gate/up with activation epilogue; 0: plain (down)
+    int act;
+    float alpha, limit, beta;
+    int *err;
+    unsigned long long wait_ns;
+    int num_ctas;
+};
+cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s);
+size_t gemm_tc_smem_bytes();
+
+// Tensor maps (TMA descriptors) for the GEMMs.  A: [rows, K] bf16, box 128 x 64.
+// B: [groups, rows, K] bf16, box box_rows x 64.  Both with 128-byte swizzle.
+CUresult encode_map_a(CUtensorMap *m, const void *ptr, int rows, int K);
+CUresult encode_map_b(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int box_rows);
+
+// ------------------------------------------------- decode streamers (K6)
+// CUDA-core kernels for few tokens per expert: each CTA streams a block of
+// weight rows of one expert once (128-bit loads) and applies it to that
+// expert's tokens, staged in shared memory.
+struct DecodeGroups {
+    const int32_t *offs;     // [E + 1] routed rows per expert
+    const int32_t *active;   // [E + 1] active experts, count at active[E]
+    int E;
+    int shared;              // 1: one more group, the shared expert, over rows [0, T)
+    int T;
+};
+struct DecodeGluArgs {
+    DecodeGroups g;
+    const __nv_bfloat16 *x_routed;  // [T*k, H] expert-sorted rows
+    const __nv_bfloat16 *x_shared;  // [T, H]
+    const __nv_bfloat16 *gate, *up; // [E', I, H]
+    const __nv_bfloat16 *sh_gate, *sh_up;  // [S, H]
+    int H, I, S;
+    __nv_bfloat16 *h_routed;        // [T*k, I]
+    __nv_bfloat16 *h_shared;        // [T, S]
+    int act;
+    float alpha, limit, beta;
+};
+cudaError_t launch_decode_glu(const DecodeGluArgs &a, cudaStream_t s);
+
+struct DecodeDownArgs {
+    DecodeGroups g;
+    const __nv_bfloat16 *h_routed;  // [T*k, I]
+    const __nv_bfloat16 *h_shared;  // [T, S]
+    const __nv_bfloat16 *down;      // [E', H, I]
+    const __nv_bfloat16 *sh_down;   // [H, S]
+    int H, I, S;
+    __nv_bfloat16 *y_routed;        // [T*k, H]
+    __nv_bfloat16 *y_shared;        // [T, H]
+};
+cudaError_t launch_decode_down(const DecodeDownArgs &a, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,615 @@
+// Host runtime and C ABI of libmoe.so (declared in include/moe.h).
+//
+// A handle owns one device allocation (the workspace, sized by max_tokens),
+// the TMA descriptors of the borrowed weight tensors and of its workspace
+// buffers, and a device error word.  moe_forward enqueues, on the caller's
+// stream:
+//   router (K1) -> dispatch scan + stable scatter/gather (K2) ->
+//   gate/up + activation (K3/K5) -> down (K4/K5) -> combine (K7)
+// where the two expert stages are either the tcgen05 grouped GEMMs (routed and
+// shared expert tiles in one persistent launch each) or, for few tokens, the
+// weight-streaming decode kernels (K6).
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <cmath>
+#include <string>
+
+#include "kernels.h"
+#include "moe.h"
+
+using moe::bf16;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status fail(moe_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+moe_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+constexpr int kPathAuto = 0, kPathDecode = 1, kPathGrouped = 2;
+// Auto path: the decode kernels while every expert sees at most a few tokens.
+constexpr int kDecodeMaxTokens = 16;
+
+}  // namespace
+
+struct moe_handle {
+    moe_config cfg;
+    moe_weights w;
+    int device = 0, num_sms = 0;
+    int H = 0, E = 0, Ep = 0, k = 0, I = 0, S = 0;  // S: shared width actually used (I when packed)
+    bool has_shared = false, x_f32 = false;
+    const bf16 *sh_gate = nullptr, *sh_up = nullptr, *sh_down = nullptr;  // shared tensors (or slice E)
+    int path_opt = kPathAuto;
+    unsigned long long wait_ns = 500000000ull;
+
+    // workspace
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    int32_t *topk_idx = nullptr, *blk_hist = nullptr, *offs = nullptr, *tile_offs = nullptr,
+            *active = nullptr, *sorted_tok = nullptr, *slot_of = nullptr;
+    float *topk_w = nullptr;
+    bf16 *x_sorted = nullptr, *x_bf16 = nullptr, *hbuf = nullptr, *hs = nullptr, *yslot = nullptr,
+         *ys = nullptr;
+    void *x_stage = nullptr, *y_stage = nullptr;
+    int *err = nullptr;
+
+    // TMA descriptors fixed at create
+    CUtensorMap m_xsorted, m_hbuf, m_hs, m_xbf16, m_gate, m_up, m_down, m_shg, m_shu, m_shd;
+    // descriptor of the caller's X for the shared-expert GEMM (cached by pointer and T)
+    CUtensorMap m_x;
+    const void *m_x_ptr = nullptr;
+    int m_x_rows = 0;
+
+    int last_path = 0, last_launches = 0, last_T = 0;
+
+    // optional per-kernel timing of moe_forward
+    static constexpr int kMaxStages = 8;
+    bool stage_events = false;
+    cudaEvent_t ev[kMaxStages + 1] = {};
+    int ev_recorded = 0;
+};
+
+namespace {
+
+moe_status validate_config(const moe_config *c, int *S_eff) {
+    if (c->hidden_size < 64 || c->hidden_size % 64 != 0 || c->hidden_size > 8192)
+        return fail(MOE_ERR_UNSUPPORTED, "hidden_size %d: need a multiple of 64 in [64, 8192]",
+                    c->hidden_size);
+    if (c->num_experts < 1 || c->num_experts > 256)
+        return fail(MOE_ERR_UNSUPPORTED, "num_experts %d: need 1..256", c->num_experts);
+    if (c->num_experts_per_tok < 1 || c->num_experts_per_tok > c->num_experts ||
+        c->num_experts_per_tok > 16)
+        return fail(MOE_ERR_INVALID_ARG, "num_experts_per_tok %d: need 1..min(num_experts, 16)",
+                    c->num_experts_per_tok);
+    if (c->moe_intermediate_size < 64 || c->moe_intermediate_size % 64 != 0 ||
+        c->moe_intermediate_size > 8192)
+        return fail(MOE_ERR_UNSUPPORTED, "moe_intermediate_size %d: need a multiple of 64 in [64, 8192]",
+                    c->moe_intermediate_size);
+    if (c->num_shared_experts < 0 || c->shared_intermediate_size < 0)
+        return fail(MOE_ERR_INVALID_ARG, "negative shared expert count or width");
+    int S = 0;
+    if (c->shared_packed) {
+        if (c->shared_intermediate_size != 0 && c->shared_intermediate_size != c->moe_intermediate_size)
+            return fail(MOE_ERR_INVALID_ARG,
+                        "a packed shared expert has the routed width (%d), got shared_intermediate_size %d",
+                        c->moe_intermediate_size, c->shared_intermediate_size);
+        S = c->moe_intermediate_size;
+    } else {
+        S = c->shared_intermediate_size ? c->shared_intermediate_size
+                                        : c->num_shared_experts * c->moe_intermediate_size;
+        if (S % 64 != 0 || S > 8192)
+            return fail(MOE_ERR_UNSUPPORTED, "shared width %d: need a multiple of 64, at most 8192", S);
+    }
+    if (c->score_func != MOE_SCORE_SIGMOID && c->score_func != MOE_SCORE_SOFTMAX)
+        return fail(MOE_ERR_INVALID_ARG, "score_func %d", c->score_func);
+    if (c->hidden_act != MOE_ACT_SILU && c->hidden_act != MOE_ACT_SWIGLU_OAI)
+        return fail(MOE_ERR_INVALID_ARG, "hidden_act %d", c->hidden_act);
+    if (c->act_dtype != MOE_DTYPE_BF16 && c->act_dtype != MOE_DTYPE_F32)
+        return fail(MOE_ERR_INVALID_ARG, "act_dtype %d", c->act_dtype);
+    if (!std::isfinite(c->route_scale))
+        return fail(MOE_ERR_INVALID_ARG, "route_scale is not finite");
+    if (c->max_tokens < 1 || (long long)c->max_tokens * c->num_experts_per_tok > (1ll << 24))
+        return fail(MOE_ERR_INVALID_ARG, "max_tokens %d: need 1..2^24/k", c->max_tokens);
+    *S_eff = S;
+    return MOE_OK;
+}
+
+struct Carver {
+    size_t off = 0;
+    template <class T>
+    T *take(void *base, size_t count) {
+        off = round_up(off, 256);
+        T *p = base ? reinterpret_cast<T *>(static_cast<char *>(base) + off) : nullptr;
+        off += count * sizeof(T);
+        return p;
+    }
+};
+
+void carve(moe_handle *h, void *base) {
+    const size_t MT = h->cfg.max_tokens, k = h->k, H = h->H, E = h->E;
+    const size_t nb = (MT + 15) / 16;
+    const size_t elt = h->x_f32 ? 4 : 2;
+    Carver c;
+    h->err = c.take<int>(base, 64);
+    h->topk_idx = c.take<int32_t>(base, MT * k);
+    h->topk_w = c.take<float>(base, MT * k);
+    h->blk_hist = c.take<int32_t>(base, nb * E);
+    h->offs = c.take<int32_t>(base, E + 1);
+    h->tile_offs = c.take<int32_t>(base, E + 1);
+    h->active = c.take<int32_t>(base, E + 1);
+    h->sorted_tok = c.take<int32_t>(base, MT * k);
+    h->slot_of = c.take<int32_t>(base, MT * k);
+    h->x_sorted = c.take<bf16>(base, MT * k * H);
+    h->x_bf16 = h->x_f32 ? c.take<bf16>(base, MT * H) : nullptr;
+    h->hbuf = c.take<bf16>(base, MT * k * h->I);
+    h->hs = h->has_shared ? c.take<bf16>(base, MT * h->S) : nullptr;
+    h->yslot = c.take<bf16>(base, MT * k * H);
+    h->ys = h->has_shared ? c.take<bf16>(base, MT * H) : nullptr;
+    h->x_stage = c.take<char>(base, MT * H * elt);
+    h->y_stage = c.take<char>(base, MT * H * elt);
+    h->ws_bytes = round_up(c.off, 256);
+}
+
+moe_status build_maps(moe_handle *h) {
+    const int MT = h->cfg.max_tokens, k = h->k, H = h->H, I = h->I, S = h->S, Ep = h->Ep;
+    CUresult r = CUDA_SUCCESS;
+#define MAP(call)                                                                        \
+    do {                                                                                 \
+        r = (call);                                                                      \
+        if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", #call, (int)r); \
+    } while (0)
+    MAP(moe::encode_map_a(&h->m_xsorted, h->x_sorted, MT * k, H));
+    MAP(moe::encode_map_a(&h->m_hbuf, h->hbuf, MT * k, I));
+    MAP(moe::encode_map_b(&h->m_gate, h->w.gate, Ep, I, H, 128));
+    MAP(moe::encode_map_b(&h->m_up, h->w.up, Ep, I, H, 128));
+    MAP(moe::encode_map_b(&h->m_down, h->w.down, Ep, H, I, moe::kGemmBN));
+    if (h->has_shared) {
+        MAP(moe::encode_map_a(&h->m_hs, h->hs, MT, S));
+        if (h->x_f32) MAP(moe::encode_map_a(&h->m_xbf16, h->x_bf16, MT, H));
+        if (h->cfg.shared_packed) {
+            h->m_shg = h->m_gate;
+            h->m_shu = h->m_up;
+            h->m_shd = h->m_down;
+        } else {
+            MAP(moe::encode_map_b(&h->m_shg, h->w.sh_gate, 1, S, H, 128));
+            MAP(moe::encode_map_b(&h->m_shu, h->w.sh_up, 1, S, H, 128));
+            MAP(moe::encode_map_b(&h->m_shd, h->w.sh_down, 1, H, S, moe::kGemmBN));
+        }
+    }
+#undef MAP
+    return MOE_OK;
+}
+
+moe_status check_launch(cudaError_t e, const char *what) {
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, what);
+}
+
+// Event after kernel number n (n = 0: before the first kernel).
+void mark(moe_handle *h, int n, cudaStream_t s) {
+    if (!h->stage_events || n > moe_handle::kMaxStages) return;
+    cudaEventRecord(h->ev[n], s);
+    h->ev_recorded = n + 1;
+}
+
+moe_status launched(moe_handle *h, cudaError_t e, const char *what, int *n, cudaStream_t s) {
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    ++*n;
+    mark(h, *n, s);
+    return MOE_OK;
+}
+
+// Router + dispatch, shared by both paths.  Returns launches through *n.
+moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n) {
+    const int TT = moe::router_tokens_per_block(T, h->num_sms);
+    const int nb = (T + TT - 1) / TT;
+    moe::RouterArgs ra{};
+    ra.X = X;
+    ra.x_f32 = h->x_f32;
+    ra.T = T;
+    ra.H = h->H;
+    ra.E = h->E;
+    ra.k = h->k;
+    ra.Wr = h->w.router_w;
+    ra.bias = h->w.expert_bias;
+    ra.score_func = h->cfg.score_func;
+    ra.route_norm = h->cfg.route_norm;
+    ra.route_scale = h->cfg.route_scale;
+    ra.topk_idx = h->topk_idx;
+    ra.topk_w = h->topk_w;
+    ra.blk_hist = h->blk_hist;
+    ra.x_bf16 = h->x_f32 && h->has_shared ? h->x_bf16 : nullptr;
+    ra.tokens_per_block = TT;
+    moe_status st = launched(h, moe::launch_router(ra, s), "router launch", n, s);
+    if (st != MOE_OK) return st;
+
+    moe::ScanArgs sa{h->blk_hist, nb, h->E, h->offs, h->tile_offs, h->active};
+    st = launched(h, moe::launch_scan(sa, s), "scan launch", n, s);
+    if (st != MOE_OK) return st;
+
+    moe::ScatterArgs xa{};
+    xa.topk_idx = h->topk_idx;
+    xa.blk_base = h->blk_hist;
+    xa.T = T;
+    xa.k = h->k;
+    xa.E = h->E;
+    xa.H = h->H;
+    xa.tokens_per_block = TT;
+    xa.X = X;
+    xa.x_f32 = h->x_f32;
+    xa.sorted_tok = h->sorted_tok;
+    xa.slot_of = h->slot_of;
+    xa.x_sorted = h->x_sorted;
+    xa.err = h->err;
+    st = launched(h, moe::launch_scatter(xa, s), "scatter launch", n, s);
+    if (st != MOE_OK) return st;
+    return MOE_OK;
+}
+
+moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int *n) {
+    const int H = h->H, I = h->I, S = h->S, E = h->E;
+    moe::GemmArgs g{};
+    g.err = h->err;
+    g.wait_ns = h->wait_ns;
+    g.act = h->cfg.hidden_act;
+    g.alpha = h->cfg.act_alpha;
+    g.limit = h->cfg.act_limit;
+    g.beta = h->cfg.act_beta;
+    g.num_ctas = h->num_sms;
+
+    // gate/up: routed rows of X_sorted against the stacked gate/up slices;
+    // shared expert over all T rows of X
+    g.glu = 1;
+    g.A0 = h->m_xsorted;
+    g.B0 = h->m_gate;
+    g.B1 = h->m_up;
+    g.seg[0] = moe::GemmSegment{0, E, 0, 0, h->offs, h->tile_offs, (I + 127) / 128, H / 64, I, h->hbuf, I};
+    g.num_segs = 1;
+    if (h->has_shared) {
+        if (h->x_f32) {
+            g.A1 = h->m_xbf16;
+        } else {
+            if (h->m_x_ptr != X || h->m_x_rows != T) {
+                CUresult r = moe::encode_map_a(&h->m_x, X, T, H);
+                if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(X) failed: %d", (int)r);
+                h->m_x_ptr = X;
+                h->m_x_rows = T;
+            }
+            g.A1 = h->m_x;
+        }
+        g.B2 = h->m_shg;
+        g.B3 = h->m_shu;
+        g.seg[1] = moe::GemmSegment{1, 1, h->cfg.shared_packed ? E : 0, T, nullptr, nullptr,
+                                    (S + 127) / 128, H / 64, S, h->hs, S};
+        g.num_segs = 2;
+    }
+    moe_status st = launched(h, moe::launch_gemm_tc(g, s), "gate/up GEMM launch", n, s);
+    if (st != MOE_OK) return st;
+
+    // down: routed hidden rows against the stacked down slices; shared hidden rows
+    g.glu = 0;
+    g.A0 = h->m_hbuf;
+    g.B0 = h->m_down;
+    g.seg[0] = moe::GemmSegment{0, E, 0, 0, h->offs, h->tile_offs, (H + moe::kGemmBN - 1) / moe::kGemmBN,
+                                I / 64, H, h->yslot, H};
+    g.num_segs = 1;
+    if (h->has_shared) {
+        g.A1 = h->m_hs;
+        g.B2 = h->m_shd;
+        g.seg[1] = moe::GemmSegment{1, 1, h->cfg.shared_packed ? E : 0, T, nullptr, nullptr,
+                                    (H + moe::kGemmBN - 1) / moe::kGemmBN, S / 64, H, h->ys, H};
+        g.num_segs = 2;
+    }
+    st = launched(h, moe::launch_gemm_tc(g, s), "down GEMM launch", n, s);
+    if (st != MOE_OK) return st;
+    return MOE_OK;
+}
+
+moe_status run_decode(moe_handle *h, const void *X, int T, cudaStream_t s, int *n) {
+    moe::DecodeGroups grp{h->offs, h->active, h->E, h->has_shared ? 1 : 0, T};
+    moe::DecodeGluArgs ga{};
+    ga.g = grp;
+    ga.x_routed = h->x_sorted;
+    ga.x_shared = h->x_f32 ? h->x_bf16 : static_cast<const bf16 *>(X);
+    ga.gate = static_cast<const bf16 *>(h->w.gate);
+    ga.up = static_cast<const bf16 *>(h->w.up);
+    ga.sh_gate = h->sh_gate;
+    ga.sh_up = h->sh_up;
+    ga.H = h->H;
+    ga.I = h->I;
+    ga.S = h->S;
+    ga.h_routed = h->hbuf;
+    ga.h_shared = h->hs;
+    ga.act = h->cfg.hidden_act;
+    ga.alpha = h->cfg.act_alpha;
+    ga.limit = h->cfg.act_limit;
+    ga.beta = h->cfg.act_beta;
+    moe_status st = launched(h, moe::launch_decode_glu(ga, s), "decode gate/up launch", n, s);
+    if (st != MOE_OK) return st;
+    moe::DecodeDownArgs da{};
+    da.g = grp;
+    da.h_routed = h->hbuf;
+    da.h_shared = h->hs;
+    da.down = static_cast<const bf16 *>(h->w.down);
+    da.sh_down = h->sh_down;
+    da.H = h->H;
+    da.I = h->I;
+    da.S = h->S;
+    da.y_routed = h->yslot;
+    da.y_shared = h->ys;
+    st = launched(h, moe::launch_decode_down(da, s), "decode down launch", n, s);
+    if (st != MOE_OK) return st;
+    return MOE_OK;
+}
+
+moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStream_t s) {
+    int n = 0;
+    const int path = h->path_opt != kPathAuto ? h->path_opt
+                                              : (T <= kDecodeMaxTokens ? kPathDecode : kPathGrouped);
+    h->ev_recorded = 0;
+    mark(h, 0, s);
+    moe_status st = run_front(h, X, T, s, &n);
+    if (st == MOE_OK) st = path == kPathDecode ? run_decode(h, X, T, s, &n) : run_grouped(h, X, T, s, &n);
+    if (st == MOE_OK) {
+        moe::CombineArgs ca{h->yslot, h->has_shared ? h->ys : nullptr, h->topk_w, h->slot_of,
+                            T, h->k, h->H, Y, h->x_f32 ? 1 : 0};
+        st = launched(h, moe::launch_combine(ca, s), "combine launch", &n, s);
+    }
+    h->last_path = path;
+    h->last_launches = n;
+    h->last_T = T;
+    return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_create(const moe_config *config, const moe_weights *weights, moe_handle **out) {
+    if (out == nullptr) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (config == nullptr || weights == nullptr) return fail(MOE_ERR_INVALID_ARG, "config or weights is NULL");
+    int S = 0;
+    moe_status st = validate_config(config, &S);
+    if (st != MOE_OK) return st;
+    const moe_weights &w = *weights;
+    if (!w.router_w || !w.gate || !w.up || !w.down)
+        return fail(MOE_ERR_INVALID_ARG, "router_w, gate, up and down are required");
+    const void *ptrs[] = {w.router_w, w.expert_bias, w.gate, w.up, w.down, w.sh_gate, w.sh_up, w.sh_down};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "weight pointer %p is not 16-byte aligned", p);
+    const bool has_shared = S > 0;
+    if (has_shared && !config->shared_packed && (!w.sh_gate || !w.sh_up || !w.sh_down))
+        return fail(MOE_ERR_INVALID_ARG, "shared width %d needs sh_gate, sh_up and sh_down", S);
+
+    moe_handle *h = new moe_handle();
+    h->cfg = *config;
+    h->w = w;
+    h->H = config->hidden_size;
+    h->E = config->num_experts;
+    h->Ep = config->num_experts + (config->shared_packed ? 1 : 0);
+    h->k = config->num_experts_per_tok;
+    h->I = config->moe_intermediate_size;
+    h->S = S;
+    h->has_shared = has_shared;
+    h->x_f32 = config->act_dtype == MOE_DTYPE_F32;
+    if (config->shared_packed) {
+        const size_t slice = (size_t)h->E * h->I * h->H;
+        h->sh_gate = static_cast<const bf16 *>(w.gate) + slice;
+        h->sh_up = static_cast<const bf16 *>(w.up) + slice;
+        h->sh_down = static_cast<const bf16 *>(w.down) + slice;
+    } else {
+        h->sh_gate = static_cast<const bf16 *>(w.sh_gate);
+        h->sh_up = static_cast<const bf16 *>(w.sh_up);
+        h->sh_down = static_cast<const bf16 *>(w.sh_down);
+    }
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+    if (e != cudaSuccess) {
+        delete h;
+        return cuda_fail(e, "device query");
+    }
+    carve(h, nullptr);
+    e = cudaMalloc(&h->ws, h->ws_bytes);
+    if (e != cudaSuccess) {
+        const size_t h_bytes = h->ws_bytes;
+        cudaGetLastError();
+        delete h;
+        return fail(MOE_ERR_OOM, "workspace of %zu bytes: %s", h_bytes, cudaGetErrorString(e));
+    }
+    carve(h, h->ws);
+    e = cudaMemset(h->err, 0, sizeof(int));
+    if (e != cudaSuccess) {
+        cudaFree(h->ws);
+        delete h;
+        return cuda_fail(e, "cudaMemset");
+    }
+    st = build_maps(h);
+    if (st != MOE_OK) {
+        cudaFree(h->ws);
+        delete h;
+        return st;
+    }
+    *out = h;
+    return MOE_OK;
+}
+
+moe_status moe_route(moe_handle *h, const void *X, int T, int32_t *topk_idx, float *topk_w,
+                     moe_stream_t stream) {
+    if (h == nullptr) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+    if (T < 0 || T > h->cfg.max_tokens)
+        return fail(MOE_ERR_INVALID_ARG, "T = %d outside [0, max_tokens = %d]", T, h->cfg.max_tokens);
+    h->last_launches = 0;
+    if (T == 0) return MOE_OK;
+    if (!X || !topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "X, topk_idx and topk_w are required");
+    if (!aligned16(X)) return fail(MOE_ERR_INVALID_ARG, "X is not 16-byte aligned");
+    moe::RouterArgs ra{};
+    ra.X = X;
+    ra.x_f32 = h->x_f32;
+    ra.T = T;
+    ra.H = h->H;
+    ra.E = h->E;
+    ra.k = h->k;
+    ra.Wr = h->w.router_w;
+    ra.bias = h->w.expert_bias;
+    ra.score_func = h->cfg.score_func;
+    ra.route_norm = h->cfg.route_norm;
+    ra.route_scale = h->cfg.route_scale;
+    ra.topk_idx = topk_idx;
+    ra.topk_w = topk_w;
+    ra.blk_hist = nullptr;
+    ra.x_bf16 = nullptr;
+    ra.tokens_per_block = moe::router_tokens_per_block(T, h->num_sms);
+    moe_status st = check_launch(moe::launch_router(ra, reinterpret_cast<cudaStream_t>(stream)), "router launch");
+    if (st == MOE_OK) h->last_launches = 1;
+    return st;
+}
+
+moe_status moe_forward(moe_handle *h, const void *X, int T, void *Y, moe_stream_t stream) {
+    if (h == nullptr) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+    if (T < 0 || T > h->cfg.max_tokens)
+        return fail(MOE_ERR_INVALID_ARG, "T = %d outside [0, max_tokens = %d]", T, h->cfg.max_tokens);
+    h->last_launches = 0;
+    if (T == 0) return MOE_OK;
+    if (!X || !Y) return fail(MOE_ERR_INVALID_ARG, "X and Y are required");
+    if (!aligned16(X) || !aligned16(Y)) return fail(MOE_ERR_INVALID_ARG, "X and Y must be 16-byte aligned");
+    const size_t bytes = (size_t)T * h->H * (h->x_f32 ? 4 : 2);
+    const char *xb = static_cast<const char *>(X), *yb = static_cast<const char *>(Y);
+    if (xb < yb + bytes && yb < xb + bytes) return fail(MOE_ERR_INVALID_ARG, "X and Y overlap");
+    return forward_device(h, X, T, Y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_host(moe_handle *h, const void *X_host, int T, void *Y_host, moe_stream_t stream) {
+    if (h == nullptr) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+    if (T < 0 || T > h->cfg.max_tokens)
+        return fail(MOE_ERR_INVALID_ARG, "T = %d outside [0, max_tokens = %d]", T, h->cfg.max_tokens);
+    h->last_launches = 0;
+    if (T == 0) return MOE_OK;
+    if (!X_host || !Y_host) return fail(MOE_ERR_INVALID_ARG, "X_host and Y_host are required");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t bytes = (size_t)T * h->H * (h->x_f32 ? 4 : 2);
+    cudaError_t e = cudaMemcpyAsync(h->x_stage, X_host, bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy of X");
+    moe_status st = forward_device(h, h->x_stage, T, h->y_stage, s);
+    if (st != MOE_OK) return st;
+    e = cudaMemcpyAsync(Y_host, h->y_stage, bytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy of Y");
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
+    return MOE_OK;
+}
+
+moe_status moe_sync_status(moe_handle *h) {
+    if (h == nullptr) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "synchronise");
+    int word = 0;
+    e = cudaMemcpy(&word, h->err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "read of the device error word");
+    if (word & moe::ERR_TIMEOUT)
+        return fail(MOE_ERR_TIMEOUT, "a device wait ran out of its bound (error word 0x%x)", word);
+    if (word & moe::ERR_BOUNDS)
+        return fail(MOE_ERR_DEVICE_CHECK, "a device bounds check failed (error word 0x%x)", word);
+    return MOE_OK;
+}
+
+void moe_destroy(moe_handle *h) {
+    if (h == nullptr) return;
+    cudaDeviceSynchronize();
+    for (auto &e : h->ev)
+        if (e != nullptr) cudaEventDestroy(e);
+    cudaFree(h->ws);
+    delete h;
+}
+
+const char *moe_last_error(void) { return g_last_error.c_str(); }
+
+moe_status moe_set_option(moe_handle *h, int option, long long value) {
+    if (h == nullptr) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+    switch (option) {
+    case MOE_OPT_PATH:
+        if (value < kPathAuto || value > kPathGrouped) return fail(MOE_ERR_INVALID_ARG, "path %lld", value);
+        h->path_opt = (int)value;
+        return MOE_OK;
+    case MOE_OPT_WAIT_LIMIT_NS:
+        if (value < 0) return fail(MOE_ERR_INVALID_ARG, "wait limit %lld", value);
+        h->wait_ns = (unsigned long long)value;
+        return MOE_OK;
+    case MOE_OPT_STAGE_EVENTS:
+        if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "stage events %lld", value);
+        if (value && h->ev[0] == nullptr) {
+            for (auto &e : h->ev) {
+                cudaError_t r = cudaEventCreate(&e);
+                if (r != cudaSuccess) return cuda_fail(r, "cudaEventCreate");
+            }
+        }
+        h->stage_events = value != 0;
+        h->ev_recorded = 0;
+        return MOE_OK;
+    default:
+        return fail(MOE_ERR_INVALID_ARG, "unknown option %d", option);
+    }
+}
+
+moe_status moe_get_stats(const moe_handle *h, moe_stats *out) {
+    if (h == nullptr || out == nullptr) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    out->path = h->last_path;
+    out->kernel_launches = h->last_launches;
+    out->workspace_bytes = (long long)h->ws_bytes;
+    return MOE_OK;
+}
+
+moe_status moe_get_stage_times(moe_handle *h, float *ms, int max, int *n) {
+    if (h == nullptr || ms == nullptr || n == nullptr) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    if (!h->stage_events || h->ev_recorded < 2)
+        return fail(MOE_ERR_INVALID_ARG, "no timed forward (enable MOE_OPT_STAGE_EVENTS first)");
+    cudaError_t e = cudaEventSynchronize(h->ev[h->ev_recorded - 1]);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    int count = 0;
+    for (int i = 0; i + 1 < h->ev_recorded && count < max; ++i) {
+        e = cudaEventElapsedTime(&ms[count], h->ev[i], h->ev[i + 1]);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+        ++count;
+    }
+    *n = count;
+    return MOE_OK;
+}
+
+moe_status moe_inspect(const moe_handle *h, int buffer, void *dst, size_t bytes, moe_stream_t stream) {
+    if (h == nullptr || dst == nullptr) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    const size_t MT = h->cfg.max_tokens, k = h->k;
+    const void *src = nullptr;
+    size_t cap = 0;
+    switch (buffer) {
+    case MOE_BUF_TOPK_IDX: src = h->topk_idx; cap = MT * k * 4; break;
+    case MOE_BUF_TOPK_W: src = h->topk_w; cap = MT * k * 4; break;
+    case MOE_BUF_EXPERT_OFFS: src = h->offs; cap = (h->E + 1) * 4; break;
+    case MOE_BUF_SORTED_TOKEN: src = h->sorted_tok; cap = MT * k * 4; break;
+    case MOE_BUF_SLOT: src = h->slot_of; cap = MT * k * 4; break;
+    case MOE_BUF_HIDDEN: src = h->hbuf; cap = MT * k * h->I * 2; break;
+    default: return fail(MOE_ERR_INVALID_ARG, "unknown buffer %d", buffer);
+    }
+    if (bytes > cap) return fail(MOE_ERR_INVALID_ARG, "%zu bytes requested, buffer holds %zu", bytes, cap);
+    cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice,
+                                    reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "inspect copy");
+}
+
+}  // extern "C"

@@ -1,0 +1,195 @@
+/*
+ * moe.h - C ABI of libmoe.so: the token-choice mixture-of-experts feed-forward
+ * block of AFMoE (Arcee Trinity) and of MiniMax-M3, on one GB300 (sm_103a).
+ *
+ * What the block computes, per token x = X[t,:] (H values):
+ *   logits   l_e = x . Wr[e,:]                  in fp32, e in [0, E)
+ *   scores   s_e = sigmoid(l_e)  (or softmax over e)
+ *   select   the k experts with the largest s_e + b_e (b = expert_bias, used for
+ *            the choice only; ties go to the lower expert index), in
+ *            descending biased score
+ *   weights  w_j = s_{idx_j}; if route_norm: w_j /= sum_j w_j; w_j *= route_scale
+ *   experts  y_e = Wd[e] . act(Wg[e] . x, Wu[e] . x)
+ *   shared   y_s = the same MLP over the shared tensors (or the packed slice E),
+ *            weight 1.0, never selected, never normalised, never scaled
+ *   output   Y[t,:] = sum_j w_j y_{idx_j} + y_s
+ * Sources: Arcee AFMoE issue (mlxcel #845), "Routing detail" (sigmoid scores,
+ * selection-only expert_bias, route_norm then route_scale) and "Checkpoint
+ * weight layout" (pre-stacked experts.{gate,up,down}_proj, router.gate,
+ * expert_bias, shared_experts); HF Transformers AFMoE docs, AfmoeConfig
+ * (num_experts, num_experts_per_tok, num_shared_experts, moe_intermediate_size,
+ * route_scale, hidden_act) and "expert routing" / "shared experts"; MiniMax-M3
+ * issue (mlxcel #763), "Architecture specification" (packed shared expert at
+ * index E with score 1.0; clamp-SwiGLU x_glu*sigmoid(alpha*x_glu)*(x_linear+beta),
+ * alpha 1.702, limit 7.0, beta 1.0).
+ *
+ * Conventions for every entry point:
+ *   - Tensors are row-major and contiguous.  Device pointers must be 16-byte
+ *     aligned.  Every pointer is BORROWED: the library never frees it.
+ *   - Calls that take a stream are asynchronous on that stream (NULL = the
+ *     legacy default stream); results are valid once the stream is synchronised.
+ *   - Argument errors are detected on the host, before anything is launched,
+ *     and return MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED.
+ *   - A failed device-side check (a bounded wait that ran out, an index out of
+ *     range) sets a device error word; moe_sync_status() reports it as
+ *     MOE_ERR_TIMEOUT / MOE_ERR_DEVICE_CHECK and clears it.
+ *   - moe_last_error() returns a per-thread message for the last failure.
+ *   - A handle is not thread-safe: calls on one handle must not overlap.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the runtime's stream handle), passed through unchanged. */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* a NULL, misaligned or out-of-range argument */
+    MOE_ERR_UNSUPPORTED = 2,  /* a valid config outside what the kernels handle */
+    MOE_ERR_CUDA = 3,         /* a CUDA runtime call failed; see moe_last_error() */
+    MOE_ERR_OOM = 4,          /* workspace allocation failed */
+    MOE_ERR_TIMEOUT = 5,      /* a bounded device wait ran out (device error word) */
+    MOE_ERR_DEVICE_CHECK = 6  /* a device-side bounds check failed (device error word) */
+} moe_status;
+
+/* score_func: HF AFMoE docs list sigmoid or softmax routing; Trinity and M3 use
+ * sigmoid ("Routing detail"; MiniMax-M3 "Architecture specification"). */
+typedef enum { MOE_SCORE_SIGMOID = 0, MOE_SCORE_SOFTMAX = 1 } moe_score_func;
+
+/* hidden_act: "silu" gives a = silu(g) * u (AfmoeConfig default); "swigluoai"
+ * gives a = min(g,limit) * sigmoid(alpha*min(g,limit)) * (clamp(u,-limit,limit) + beta)
+ * (MiniMax-M3, Activation bullet; the clamp placement follows the gpt-oss
+ * convention that bullet names). */
+typedef enum { MOE_ACT_SILU = 0, MOE_ACT_SWIGLU_OAI = 1 } moe_act;
+
+/* dtype of X and Y.  Expert weights are always bf16; router weights and the
+ * expert bias are always fp32. */
+typedef enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 } moe_dtype;
+
+typedef struct {
+    int hidden_size;              /* H; multiple of 64 */
+    int num_experts;              /* E routed experts; 1..256 */
+    int num_experts_per_tok;      /* k; 1..min(E, 16) */
+    int num_shared_experts;       /* 0, or the count of always-on shared experts */
+    int moe_intermediate_size;    /* I, width of one routed expert; multiple of 64 */
+    int shared_intermediate_size; /* S, total shared width; 0 => num_shared_experts * I */
+    int shared_packed;            /* 1 => the shared expert is slice E of the stacked
+                                     gate/up/down tensors (width I, score 1.0) */
+    int score_func;               /* moe_score_func */
+    int route_norm;               /* 1 => renormalise the k gathered weights */
+    float route_scale;            /* multiplies the routed weights after route_norm */
+    int hidden_act;               /* moe_act */
+    float act_alpha, act_limit, act_beta; /* swigluoai constants (1.702, 7.0, 1.0) */
+    int act_dtype;                /* moe_dtype of X and Y */
+    int max_tokens;               /* largest T any later call may pass; sizes the workspace */
+} moe_config;
+
+/* Device pointers to the block's weights.  BORROWED: they must stay valid and
+ * unchanged until moe_destroy().  E' = E + 1 when shared_packed, else E. */
+typedef struct {
+    const float *router_w;    /* [E, H] fp32 (mlp.router.gate) */
+    const float *expert_bias; /* [E] fp32 (mlp.expert_bias); NULL => zeros */
+    const void *gate;         /* [E', I, H] bf16 (experts.gate_proj, [out, in] per expert) */
+    const void *up;           /* [E', I, H] bf16 (experts.up_proj) */
+    const void *down;         /* [E', H, I] bf16 (experts.down_proj) */
+    const void *sh_gate;      /* [S, H] bf16 (shared_experts.gate_proj); NULL when packed or S == 0 */
+    const void *sh_up;        /* [S, H] bf16 */
+    const void *sh_down;      /* [H, S] bf16 */
+} moe_weights;
+
+typedef struct moe_handle moe_handle;
+
+/* Validate the config, record the borrowed weights, allocate the workspace
+ * (sized by max_tokens) and build the TMA descriptors of the weight tensors on
+ * the current CUDA device.  On success *out owns the handle (free it with
+ * moe_destroy).  Errors: INVALID_ARG (NULL, misaligned, inconsistent keys),
+ * UNSUPPORTED (sizes outside the kernels' limits above), OOM, CUDA. */
+moe_status moe_create(const moe_config *config, const moe_weights *weights, moe_handle **out);
+
+/* Router only: for X [T, H] (act_dtype, device) write topk_idx [T, k] int32
+ * (experts in descending biased score, ties to the lower index) and topk_w
+ * [T, k] fp32 (unbiased scores, renormalised and scaled).  T == 0 is a no-op.
+ * Errors: INVALID_ARG (NULL pointer, T < 0 or T > max_tokens), CUDA. */
+moe_status moe_route(moe_handle *h, const void *X, int T, int32_t *topk_idx, float *topk_w,
+                     moe_stream_t stream);
+
+/* The whole block: Y [T, H] (act_dtype, device) from X [T, H] (device).
+ * X and Y must not overlap.  T == 0 is a no-op.
+ * Errors: INVALID_ARG, CUDA. */
+moe_status moe_forward(moe_handle *h, const void *X, int T, void *Y, moe_stream_t stream);
+
+/* moe_forward with HOST buffers: copies X_host to the handle's device staging
+ * buffer, runs the block and copies the result back to Y_host, all on
+ * `stream`; the call returns once Y_host holds the result.  Pinned host
+ * memory makes the copies asynchronous DMA; pageable memory works but is
+ * slower.  Errors: INVALID_ARG, CUDA. */
+moe_status moe_forward_host(moe_handle *h, const void *X_host, int T, void *Y_host,
+                            moe_stream_t stream);
+
+/* Synchronise the handle's work and read (then clear) its device error word.
+ * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_CHECK or MOE_ERR_CUDA. */
+moe_status moe_sync_status(moe_handle *h);
+
+/* Free the workspace and the handle.  NULL is a no-op.  Synchronises first. */
+void moe_destroy(moe_handle *h);
+
+/* Message of the last failure on the calling thread ("" if none). */
+const char *moe_last_error(void);
+
+/* ----------------------------------------------------------------------------
+ * Options, statistics and inspection (tests and measurement).
+ */
+typedef enum {
+    MOE_OPT_PATH = 0,          /* 0 auto, 1 weight-streaming decode kernels, 2 tcgen05 grouped GEMMs */
+    MOE_OPT_WAIT_LIMIT_NS = 1, /* bound of every device-side wait in ns (default 500000000);
+                                  0 makes the first wait that finds its data not ready give up,
+                                  which exercises the timeout path */
+    MOE_OPT_STAGE_EVENTS = 2   /* 1: record a CUDA event on the stream before the first and after
+                                  every kernel of moe_forward, for moe_get_stage_times (default 0) */
+} moe_option;
+
+/* Set an option.  Errors: INVALID_ARG (unknown option or value). */
+moe_status moe_set_option(moe_handle *h, int option, long long value);
+
+typedef struct {
+    int path;              /* path of the last forward: 1 decode, 2 grouped */
+    int kernel_launches;   /* kernels the last forward (or route) launched */
+    long long workspace_bytes;
+} moe_stats;
+
+/* Statistics of the last call on this handle (host-side; no synchronisation). */
+moe_status moe_get_stats(const moe_handle *h, moe_stats *out);
+
+/* With MOE_OPT_STAGE_EVENTS on: wait for the last moe_forward and write the
+ * duration in ms of each of its kernels, in launch order (router, dispatch
+ * scan, dispatch scatter, gate/up, down, combine), to ms[0..*n).  At most
+ * `max` values are written.  Errors: INVALID_ARG (events off, no forward yet,
+ * NULL argument), CUDA. */
+moe_status moe_get_stage_times(moe_handle *h, float *ms, int max, int *n);
+
+typedef enum {
+    MOE_BUF_TOPK_IDX = 0,     /* [T, k] int32, routing of the last forward */
+    MOE_BUF_TOPK_W = 1,       /* [T, k] fp32 */
+    MOE_BUF_EXPERT_OFFS = 2,  /* [E + 1] int32: rows of expert e are [offs[e], offs[e+1]) */
+    MOE_BUF_SORTED_TOKEN = 3, /* [T * k] int32: token of each expert-sorted row */
+    MOE_BUF_SLOT = 4,         /* [T * k] int32: sorted row of routing slot (t, j) */
+    MOE_BUF_HIDDEN = 5        /* [T * k, I] bf16: act(gate, up) of each sorted row */
+} moe_buffer;
+
+/* Copy `bytes` of an internal buffer, as the last forward left it, to the
+ * device pointer dst (stream-ordered on `stream`).  Errors: INVALID_ARG
+ * (unknown buffer, bytes beyond its size). */
+moe_status moe_inspect(const moe_handle *h, int buffer, void *dst, size_t bytes, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

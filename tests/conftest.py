@@ -24,3 +24,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write the output-parity errors the GPU tests measured to gpurun_out/."""
+    try:
+        from tests import parity
+    except Exception:
+        return
+    if not parity.RESULTS:
+        return
+    import json
+    out = os.path.join(ROOT, "gpurun_out")
+    os.makedirs(out, exist_ok=True)
+    with open(os.path.join(out, "parity_summary.json"), "w") as f:
+        json.dump([{"case": c, "max_abs_err_over_rms": a, "err_over_bound": b} for c, a, b in parity.RESULTS],
+                  f, indent=1)
