@@ -86,7 +86,8 @@ def load():
     L.moe_get_stats.argtypes = [P, ctypes.POINTER(MoeStats)]
     L.moe_inspect.argtypes = [P, I, P, ctypes.c_size_t, P]
     L.moe_get_stage_times.argtypes = [P, ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I)]
-    for name in ("moe_create", "moe_route", "moe_forward", "moe_forward_host", "moe_sync_status",
+    L.moe_dispatch_noalloc.argtypes = [P, I, I, I, P, P, P, P, P]
+    for name in ("moe_create", "moe_route", "moe_forward", "moe_forward_host", "moe_sync_status", "moe_dispatch_noalloc",
                  "moe_set_option", "moe_get_stats", "moe_inspect", "moe_get_stage_times"):
         getattr(L, name).restype = I
     _lib = L

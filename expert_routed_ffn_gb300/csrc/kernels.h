@@ -154,3 +154,6 @@ struct DecodeDownArgs {
 cudaError_t launch_decode_down(const DecodeDownArgs &a, cudaStream_t s);
 
 }  // namespace moe
+
+// Sets the calling thread's moe_last_error() message (defined with the C ABI).
+__attribute__((visibility("hidden"))) void moe_set_last_error_internal(const char *msg);

@@ -49,6 +49,8 @@ constexpr int kDecodeMaxTokens = 16;
 
 }  // namespace
 
+void moe_set_last_error_internal(const char *msg) { g_last_error = msg; }
+
 struct moe_handle {
     moe_config cfg;
     moe_weights w;

@@ -188,6 +188,39 @@ typedef enum {
  * (unknown buffer, bytes beyond its size). */
 moe_status moe_inspect(const moe_handle *h, int buffer, void *dst, size_t bytes, moe_stream_t stream);
 
+/* ----------------------------------------------------------------------------
+ * Dispatch sort without device allocation.  The pages have no counterpart of
+ * this call; it is a library facility.
+ *
+ * Who it is for: callers that cannot allocate device memory at the point where
+ * they route tokens -- an inference server whose memory pool owns the whole
+ * device, a plugin handed a fixed memory budget, or a latency-critical loop
+ * that cannot afford cudaMalloc's implicit device synchronisation.  This is
+ * the dispatch step of moe_forward as a standalone call whose scratch (the
+ * per-block expert histograms and their scan) lives in a static device array
+ * inside libmoe.so: MOE_DISPATCH_NOALLOC_SCRATCH_INTS int32 values (1 MiB),
+ * held by every GPU that loads the library until the process exits.  The call
+ * allocates nothing; the caller passes the inputs and outputs.
+ *
+ * In:  topk_idx [T, k] int32 (device): expert ids, normally in [0, E).
+ * Out (device): expert_offs [E + 1]: the rows of expert e are
+ *      [expert_offs[e], expert_offs[e + 1]); sorted_token [T * k]: the token
+ *      of each row, rows ordered by (expert, token, slot); slot [T * k]: the
+ *      row of routing slot (t, j), or -1 when topk_idx[t, j] is out of range;
+ *      bad_index [1] int: 1 when some index was out of range, else 0.
+ * Limits: 1 <= k <= 16, 1 <= E <= 256 and ceil(T / 32) * E + 2 * (E + 1) <=
+ *      MOE_DISPATCH_NOALLOC_SCRATCH_INTS (for E = 128: T <= 65440); larger
+ *      sizes return MOE_ERR_UNSUPPORTED with a message, before any launch.
+ * The first call on a device looks up the device address of the array (with
+ * that device current); make that first call before any stream capture.  All
+ * calls on one device share the array and it keeps the last call's contents
+ * (every entry a call reads it writes first, so nothing needs clearing); calls
+ * that overlap on the GPU race on it, so the caller must serialise them.
+ * Asynchronous on `stream`.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+#define MOE_DISPATCH_NOALLOC_SCRATCH_INTS (1 << 18)
+moe_status moe_dispatch_noalloc(const int32_t *topk_idx, int T, int k, int E, int32_t *expert_offs,
+                                int32_t *sorted_token, int32_t *slot, int *bad_index, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
