@@ -25,8 +25,6 @@ MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
 MOE_ACT_SILU, MOE_ACT_SWIGLU_OAI = 0, 1
 MOE_DTYPE_BF16, MOE_DTYPE_F32 = 0, 1
 MOE_OPT_PATH, MOE_OPT_WAIT_LIMIT_NS, MOE_OPT_STAGE_EVENTS = 0, 1, 2
-STAGE_NAMES_GROUPED = ["router", "dispatch_scan", "dispatch_scatter", "gate_up_gemm", "down_gemm", "combine"]
-STAGE_NAMES_DECODE = ["router", "dispatch_scan", "dispatch_scatter", "decode_gate_up", "decode_down", "combine"]
 PATH_AUTO, PATH_DECODE, PATH_GROUPED = 0, 1, 2
 (MOE_BUF_TOPK_IDX, MOE_BUF_TOPK_W, MOE_BUF_EXPERT_OFFS, MOE_BUF_SORTED_TOKEN, MOE_BUF_SLOT,
  MOE_BUF_HIDDEN) = range(6)
@@ -86,6 +84,8 @@ def load():
     L.moe_get_stats.argtypes = [P, ctypes.POINTER(MoeStats)]
     L.moe_inspect.argtypes = [P, I, P, ctypes.c_size_t, P]
     L.moe_get_stage_times.argtypes = [P, ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I)]
+    L.moe_get_stage_name.argtypes = [P, I]
+    L.moe_get_stage_name.restype = ctypes.c_char_p
     L.moe_dispatch_noalloc.argtypes = [P, I, I, I, P, P, P, P, P]
     for name in ("moe_create", "moe_route", "moe_forward", "moe_forward_host", "moe_sync_status", "moe_dispatch_noalloc",
                  "moe_set_option", "moe_get_stats", "moe_inspect", "moe_get_stage_times"):
@@ -199,6 +199,10 @@ class MoeBlock:
         n = ctypes.c_int()
         check(load().moe_get_stage_times(self.h, buf, 8, ctypes.byref(n)), "moe_get_stage_times")
         return [buf[i] for i in range(n.value)]
+
+    def stage_names(self) -> list:
+        L = load()
+        return [L.moe_get_stage_name(self.h, i).decode() for i in range(self.stats().kernel_launches)]
 
     def inspect(self, buffer: int, count: int, dtype, stream=None):
         torch = self._torch

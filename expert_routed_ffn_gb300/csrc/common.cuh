@@ -32,6 +32,14 @@ __device__ __forceinline__ float glu_act(float g, float u, int act, float alpha,
     return g / (1.0f + expf(-g)) * u;
 }
 
+// Programmatic dependent launch: a kernel launched with launch_pdl may start
+// while the previous kernel on its stream is finishing.  pdl_wait() blocks until
+// the previous kernels have completed and their writes are visible, so it comes
+// before the first access to memory they produce or read; pdl_trigger() lets
+// the next kernel begin launching.  Both are no-ops without the launch attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -108,7 +108,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int *tile_count = reinterpret_cast<int *>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -123,9 +122,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         mbar_init(drain_bar, 1);
         fence_mbar_init();
         *abort_flag = 0;
-        const int t0 = seg_tiles(p.seg[0]);
-        tile_count[0] = t0;
-        tile_count[1] = t0 + (p.num_segs > 1 ? seg_tiles(p.seg[1]) : 0);
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.A0);
@@ -144,8 +140,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the prologue above overlaps the previous kernel; the dispatch results
+    // (offsets, tile counts) and the A rows are read only after this point
+    pdl_wait();
+    pdl_trigger();
     const uint32_t tmem_base = *tmem_slot;
-    const int tiles0 = tile_count[0], total = tile_count[1];
+    const int tiles0 = seg_tiles(p.seg[0]);
+    const int total = tiles0 + (p.num_segs > 1 ? seg_tiles(p.seg[1]) : 0);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -362,11 +363,8 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
         cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     });
-    if (a.glu)
-        gemm_tc_kernel<true><<<a.num_ctas, kThreads, kSmemBytes, s>>>(a);
-    else
-        gemm_tc_kernel<false><<<a.num_ctas, kThreads, kSmemBytes, s>>>(a);
-    return cudaGetLastError();
+    if (a.glu) return launch_pdl(gemm_tc_kernel<true>, dim3(a.num_ctas), dim3(kThreads), kSmemBytes, s, a);
+    return launch_pdl(gemm_tc_kernel<false>, dim3(a.num_ctas), dim3(kThreads), kSmemBytes, s, a);
 }
 
 }  // namespace moe

@@ -6,7 +6,27 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace moe {
+
+// Launch `kernel` with programmatic dependent launch allowed (the kernel calls
+// pdl_wait() before touching memory that earlier kernels on the stream use).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 using bf16 = __nv_bfloat16;
 
@@ -29,12 +49,55 @@ struct RouterArgs {
     float route_scale;
     int32_t *topk_idx;     // [T, k]
     float *topk_w;         // [T, k]
-    int32_t *blk_hist;     // [num_blocks, E] or nullptr
+    int32_t *blk_hist;     // block histograms or nullptr; count (b, e) at b*hb + e*he
+    int hb, he;
     __nv_bfloat16 *x_bf16; // [T, H] bf16 copy of fp32 X, or nullptr
     int tokens_per_block;  // 16 or 32
 };
 int router_tokens_per_block(int T, int num_sms);
 cudaError_t launch_router(const RouterArgs &a, cudaStream_t s);
+
+// Router logits on the tensor cores: 128 tokens per CTA, fp32 logits to
+// global memory.  The fp32 router weights are held as `parts` bf16 slices
+// [parts, E, H] whose sum is exact (see launch_split_router).
+struct RouterTcArgs {
+    CUtensorMap mapX;      // X [T, H] bf16, box 128 x 64
+    CUtensorMap mapW;      // router weight parts [parts, E, H] bf16, box Np x 64
+    int T, H, E, Np, parts, stages, tmem_cols;
+    int kb_per_split;      // 64-wide k-blocks per CTA along grid.y (split-K)
+    float *logits;         // [splits, T, Np] fp32 partial logits
+    int *err;
+    unsigned long long wait_ns;
+};
+// Routing rule from logits: a group of lanes per token (8 experts per lane),
+// topk_tokens_per_block(E) tokens per CTA; writes the expert histogram of each
+// CTA's tokens to blk_hist.  With offs set, the last CTA to finish also runs
+// the dispatch scan.
+constexpr int kMaxRouterSplits = 4;
+int topk_tokens_per_block(int E);
+struct TopkArgs {
+    const float *logits;   // [splits, T, ld] partial logits, summed in split order
+    int ld, T, E, k, splits;
+    int hb, he;            // histogram strides, as in ScanArgs
+    int tile_m;            // m-tile of the grouped GEMM (tile_offs), 0 = kGemmBM
+    const float *bias;     // [E] or nullptr
+    int score_func, route_norm;
+    float route_scale;
+    int32_t *topk_idx;     // [T, k]
+    float *topk_w;         // [T, k]
+    int32_t *blk_hist;     // [ceil(T/32), E] or nullptr
+    int *counter;          // CTA ticket for the fused scan (0 between calls)
+    int32_t *offs, *tile_offs, *active;  // scan outputs, or nullptr for no fused scan
+};
+cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s);
+struct RouterTcPlan {
+    int Np, tmem_cols, stages, smem, parts;
+};
+RouterTcPlan plan_router_tc(int E, int parts);
+cudaError_t launch_router_tc(const RouterTcArgs &a, int smem, cudaStream_t s);
+// Split fp32 weights w into bf16 hi + mid + lo == w; *flags |= 1 when some w
+// needs mid, |= 2 when some w needs lo.
+cudaError_t launch_split_router(const float *wr, int E, int H, bf16 *parts, int *flags, cudaStream_t s);
 
 // ------------------------------------------------------- dispatch sort (K2)
 // offs[e] = first sorted row of expert e (exclusive scan of the counts),
@@ -42,19 +105,23 @@ cudaError_t launch_router(const RouterArgs &a, cudaStream_t s);
 // with rows, active[E] = n.  blk_hist becomes the first row of each
 // (block, expert) pair.  Rows are ordered by (expert, token, slot): stable.
 struct ScanArgs {
-    int32_t *blk_hist;  // [nb, E] in: counts, out: base rows
+    int32_t *blk_hist;  // in: counts, out: base rows; (b, e) at b*hb + e*he
     int nb, E;
     int32_t *offs;      // [E + 1]
     int32_t *tile_offs; // [E + 1]
     int32_t *active;    // [E + 1]
+    int hb, he;         // 0, 0: row-major [nb, E]
+    int tile_m;         // m-tile counted by tile_offs; 0: kGemmBM
 };
 cudaError_t launch_scan(const ScanArgs &a, cudaStream_t s);
 
 struct ScatterArgs {
-    const int32_t *topk_idx;  // [T, k]
-    const int32_t *blk_base;  // [nb, E]
+    const int32_t *topk_idx;  // [T, k]; the k experts of a token are distinct
+    const int32_t *blk_base;  // (b, e) at b*hb + e*he
+    int hb, he;
     int T, k, E, H;
-    int tokens_per_block;
+    int tokens_per_block;     // 16, 32 or 128 (the router's blocking)
+    int gather_split;         // CTAs per token block sharing the row gather
     const void *X;            // [T, H]
     int x_f32;
     int32_t *sorted_tok;      // [T*k]

@@ -44,8 +44,10 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 constexpr int kPathAuto = 0, kPathDecode = 1, kPathGrouped = 2;
-// Auto path: the decode kernels while every expert sees at most a few tokens.
-constexpr int kDecodeMaxTokens = 16;
+// Auto path: the decode kernels only up to this many tokens.  Measured on
+// GB300, the tcgen05 grouped path is at least as fast down to T = 1, so the
+// auto path always takes it; the decode kernels stay selectable.
+constexpr int kDecodeMaxTokens = 0;
 
 }  // namespace
 
@@ -71,9 +73,15 @@ struct moe_handle {
          *ys = nullptr;
     void *x_stage = nullptr, *y_stage = nullptr;
     int *err = nullptr;
+    bf16 *wr_parts = nullptr;  // router weights as exact bf16 splits [3, E, H]
+    float *logits = nullptr;   // split-K partial router logits [splits, T, Np]
+    int hist_stride = 0;       // block histograms are [E, hist_stride]
+    int *counter = nullptr;    // CTA ticket of the top-k kernel's fused scan
+    int *wr_flags = nullptr;
+    moe::RouterTcPlan rplan{};
 
     // TMA descriptors fixed at create
-    CUtensorMap m_xsorted, m_hbuf, m_hs, m_xbf16, m_gate, m_up, m_down, m_shg, m_shu, m_shd;
+    CUtensorMap m_xsorted, m_hbuf, m_hs, m_xbf16, m_gate, m_up, m_down, m_shg, m_shu, m_shd, m_wr;
     // descriptor of the caller's X for the shared-expert GEMM (cached by pointer and T)
     CUtensorMap m_x;
     const void *m_x_ptr = nullptr;
@@ -86,6 +94,7 @@ struct moe_handle {
     bool stage_events = false;
     cudaEvent_t ev[kMaxStages + 1] = {};
     int ev_recorded = 0;
+    const char *stage_name[kMaxStages] = {};
 };
 
 namespace {
@@ -152,6 +161,7 @@ void carve(moe_handle *h, void *base) {
     h->err = c.take<int>(base, 64);
     h->topk_idx = c.take<int32_t>(base, MT * k);
     h->topk_w = c.take<float>(base, MT * k);
+    h->hist_stride = (int)nb;
     h->blk_hist = c.take<int32_t>(base, nb * E);
     h->offs = c.take<int32_t>(base, E + 1);
     h->tile_offs = c.take<int32_t>(base, E + 1);
@@ -166,6 +176,12 @@ void carve(moe_handle *h, void *base) {
     h->ys = h->has_shared ? c.take<bf16>(base, MT * H) : nullptr;
     h->x_stage = c.take<char>(base, MT * H * elt);
     h->y_stage = c.take<char>(base, MT * H * elt);
+    h->wr_parts = c.take<bf16>(base, 3 * E * H);
+    // split-K keeps splits * T <= max(max_tokens, 128 * SMs) rows
+    const size_t lrows = MT > (size_t)h->num_sms * 128 ? MT : (size_t)h->num_sms * 128;
+    h->logits = c.take<float>(base, lrows * ((E + 31) / 32 * 32));
+    h->counter = c.take<int>(base, 64);
+    h->wr_flags = c.take<int>(base, 64);
     h->ws_bytes = round_up(c.off, 256);
 }
 
@@ -182,6 +198,7 @@ moe_status build_maps(moe_handle *h) {
     MAP(moe::encode_map_b(&h->m_gate, h->w.gate, Ep, I, H, 128));
     MAP(moe::encode_map_b(&h->m_up, h->w.up, Ep, I, H, 128));
     MAP(moe::encode_map_b(&h->m_down, h->w.down, Ep, H, I, moe::kGemmBN));
+    MAP(moe::encode_map_b(&h->m_wr, h->wr_parts, h->rplan.parts, h->E, H, h->rplan.Np));
     if (h->has_shared) {
         MAP(moe::encode_map_a(&h->m_hs, h->hs, MT, S));
         if (h->x_f32) MAP(moe::encode_map_a(&h->m_xbf16, h->x_bf16, MT, H));
@@ -210,17 +227,89 @@ void mark(moe_handle *h, int n, cudaStream_t s) {
     h->ev_recorded = n + 1;
 }
 
+// Count a launch (named by `what`, e.g. "router_logits") and mark its end.
 moe_status launched(moe_handle *h, cudaError_t e, const char *what, int *n, cudaStream_t s) {
     if (e != cudaSuccess) return cuda_fail(e, what);
+    if (*n < moe_handle::kMaxStages) h->stage_name[*n] = what;
     ++*n;
     mark(h, *n, s);
     return MOE_OK;
 }
 
+// TMA descriptor of the caller's bf16 X (router and shared-expert A operand),
+// re-encoded only when the pointer or T changes.
+moe_status x_map(moe_handle *h, const void *X, int T) {
+    if (h->m_x_ptr == X && h->m_x_rows == T) return MOE_OK;
+    CUresult r = moe::encode_map_a(&h->m_x, X, T, h->H);
+    if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(X) failed: %d", (int)r);
+    h->m_x_ptr = X;
+    h->m_x_rows = T;
+    return MOE_OK;
+}
+
+// Router for bf16 X: logits on the tensor cores, then the routing rule, one
+// warp per token.  Two launches.
+moe_status run_router_tc(moe_handle *h, const void *X, int T, int32_t *topk_idx, float *topk_w,
+                         int32_t *blk_hist, cudaStream_t s, int *n) {
+    moe_status st = x_map(h, X, T);
+    if (st != MOE_OK) return st;
+    moe::RouterTcArgs ra{};
+    ra.mapX = h->m_x;
+    ra.mapW = h->m_wr;
+    ra.T = T;
+    ra.H = h->H;
+    ra.E = h->E;
+    ra.Np = h->rplan.Np;
+    ra.parts = h->rplan.parts;
+    ra.stages = h->rplan.stages;
+    ra.tmem_cols = h->rplan.tmem_cols;
+    ra.logits = h->logits;
+    ra.err = h->err;
+    ra.wait_ns = h->wait_ns;
+    {
+        // split the H reduction so that about one CTA runs per SM
+        const int nk = h->H / 64, mtiles = (T + 127) / 128;
+        int want = h->num_sms / mtiles;
+        want = want < 1 ? 1 : (want > moe::kMaxRouterSplits ? moe::kMaxRouterSplits : want);
+        ra.kb_per_split = (nk + want - 1) / want;
+    }
+    const int splits = (h->H / 64 + ra.kb_per_split - 1) / ra.kb_per_split;
+    st = launched(h, moe::launch_router_tc(ra, h->rplan.smem, s), "router_logits", n, s);
+    if (st != MOE_OK) return st;
+    moe::TopkArgs ta{};
+    ta.logits = h->logits;
+    ta.ld = h->rplan.Np;
+    ta.splits = splits;
+    ta.hb = 1;  // expert-major histograms: the scan reads each expert's blocks contiguously
+    ta.he = h->hist_stride;
+    ta.T = T;
+    ta.E = h->E;
+    ta.k = h->k;
+    ta.bias = h->w.expert_bias;
+    ta.score_func = h->cfg.score_func;
+    ta.route_norm = h->cfg.route_norm;
+    ta.route_scale = h->cfg.route_scale;
+    ta.topk_idx = topk_idx;
+    ta.topk_w = topk_w;
+    ta.blk_hist = blk_hist;
+    ta.counter = h->counter;
+    if (blk_hist != nullptr) {  // the forward path: the last top-k CTA runs the dispatch scan
+        ta.offs = h->offs;
+        ta.tile_offs = h->tile_offs;
+        ta.active = h->active;
+    }
+    return launched(h, moe::launch_topk(ta, s), blk_hist ? "router_topk_scan" : "router_topk", n, s);
+}
+
 // Router + dispatch, shared by both paths.  Returns launches through *n.
 moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n) {
-    const int TT = moe::router_tokens_per_block(T, h->num_sms);
+    // bf16 X: tensor-core logits + grouped-lane top-k; fp32 X: CUDA-core router
+    const int TT = h->x_f32 ? moe::router_tokens_per_block(T, h->num_sms) : moe::topk_tokens_per_block(h->E);
     const int nb = (T + TT - 1) / TT;
+    if (!h->x_f32) {
+        moe_status st = run_router_tc(h, X, T, h->topk_idx, h->topk_w, h->blk_hist, s, n);
+        if (st != MOE_OK) return st;
+    } else {
     moe::RouterArgs ra{};
     ra.X = X;
     ra.x_f32 = h->x_f32;
@@ -237,29 +326,44 @@ moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n
     ra.topk_w = h->topk_w;
     ra.blk_hist = h->blk_hist;
     ra.x_bf16 = h->x_f32 && h->has_shared ? h->x_bf16 : nullptr;
+    ra.hb = 1;
+    ra.he = h->hist_stride;
     ra.tokens_per_block = TT;
-    moe_status st = launched(h, moe::launch_router(ra, s), "router launch", n, s);
+    moe_status st = launched(h, moe::launch_router(ra, s), "router", n, s);
     if (st != MOE_OK) return st;
+    }
 
-    moe::ScanArgs sa{h->blk_hist, nb, h->E, h->offs, h->tile_offs, h->active};
-    st = launched(h, moe::launch_scan(sa, s), "scan launch", n, s);
-    if (st != MOE_OK) return st;
+    moe_status st = MOE_OK;
+    if (h->x_f32) {
+        moe::ScanArgs sa{h->blk_hist, nb, h->E, h->offs, h->tile_offs, h->active, 1, h->hist_stride, 0};
+        st = launched(h, moe::launch_scan(sa, s), "dispatch_scan", n, s);
+        if (st != MOE_OK) return st;
+    }
 
     moe::ScatterArgs xa{};
     xa.topk_idx = h->topk_idx;
     xa.blk_base = h->blk_hist;
+    xa.hb = 1;
+    xa.he = h->hist_stride;
     xa.T = T;
     xa.k = h->k;
     xa.E = h->E;
     xa.H = h->H;
     xa.tokens_per_block = TT;
+    {
+        // spread the row gather over about two CTAs per SM, at least 8 rows per CTA
+        const int per_block_rows = TT * h->k;
+        int g = (2 * h->num_sms + nb - 1) / nb;
+        const int gmax = (per_block_rows + 7) / 8;
+        xa.gather_split = g < 1 ? 1 : (g > gmax ? gmax : g);
+    }
     xa.X = X;
     xa.x_f32 = h->x_f32;
     xa.sorted_tok = h->sorted_tok;
     xa.slot_of = h->slot_of;
     xa.x_sorted = h->x_sorted;
     xa.err = h->err;
-    st = launched(h, moe::launch_scatter(xa, s), "scatter launch", n, s);
+    st = launched(h, moe::launch_scatter(xa, s), "dispatch_scatter", n, s);
     if (st != MOE_OK) return st;
     return MOE_OK;
 }
@@ -287,12 +391,8 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         if (h->x_f32) {
             g.A1 = h->m_xbf16;
         } else {
-            if (h->m_x_ptr != X || h->m_x_rows != T) {
-                CUresult r = moe::encode_map_a(&h->m_x, X, T, H);
-                if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(X) failed: %d", (int)r);
-                h->m_x_ptr = X;
-                h->m_x_rows = T;
-            }
+            moe_status st = x_map(h, X, T);
+            if (st != MOE_OK) return st;
             g.A1 = h->m_x;
         }
         g.B2 = h->m_shg;
@@ -301,7 +401,7 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
                                     (S + 127) / 128, H / 64, S, h->hs, S};
         g.num_segs = 2;
     }
-    moe_status st = launched(h, moe::launch_gemm_tc(g, s), "gate/up GEMM launch", n, s);
+    moe_status st = launched(h, moe::launch_gemm_tc(g, s), "gate_up_gemm", n, s);
     if (st != MOE_OK) return st;
 
     // down: routed hidden rows against the stacked down slices; shared hidden rows
@@ -318,7 +418,7 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
                                     (H + moe::kGemmBN - 1) / moe::kGemmBN, S / 64, H, h->ys, H};
         g.num_segs = 2;
     }
-    st = launched(h, moe::launch_gemm_tc(g, s), "down GEMM launch", n, s);
+    st = launched(h, moe::launch_gemm_tc(g, s), "down_gemm", n, s);
     if (st != MOE_OK) return st;
     return MOE_OK;
 }
@@ -342,7 +442,7 @@ moe_status run_decode(moe_handle *h, const void *X, int T, cudaStream_t s, int *
     ga.alpha = h->cfg.act_alpha;
     ga.limit = h->cfg.act_limit;
     ga.beta = h->cfg.act_beta;
-    moe_status st = launched(h, moe::launch_decode_glu(ga, s), "decode gate/up launch", n, s);
+    moe_status st = launched(h, moe::launch_decode_glu(ga, s), "decode_gate_up", n, s);
     if (st != MOE_OK) return st;
     moe::DecodeDownArgs da{};
     da.g = grp;
@@ -355,7 +455,7 @@ moe_status run_decode(moe_handle *h, const void *X, int T, cudaStream_t s, int *
     da.S = h->S;
     da.y_routed = h->yslot;
     da.y_shared = h->ys;
-    st = launched(h, moe::launch_decode_down(da, s), "decode down launch", n, s);
+    st = launched(h, moe::launch_decode_down(da, s), "decode_down", n, s);
     if (st != MOE_OK) return st;
     return MOE_OK;
 }
@@ -371,7 +471,7 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     if (st == MOE_OK) {
         moe::CombineArgs ca{h->yslot, h->has_shared ? h->ys : nullptr, h->topk_w, h->slot_of,
                             T, h->k, h->H, Y, h->x_f32 ? 1 : 0};
-        st = launched(h, moe::launch_combine(ca, s), "combine launch", &n, s);
+        st = launched(h, moe::launch_combine(ca, s), "combine", &n, s);
     }
     h->last_path = path;
     h->last_launches = n;
@@ -437,11 +537,17 @@ moe_status moe_create(const moe_config *config, const moe_weights *weights, moe_
     }
     carve(h, h->ws);
     e = cudaMemset(h->err, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(h->wr_flags, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(h->counter, 0, sizeof(int));
+    if (e == cudaSuccess) e = moe::launch_split_router(w.router_w, h->E, h->H, h->wr_parts, h->wr_flags, 0);
+    int flags = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&flags, h->wr_flags, sizeof(int), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) {
         cudaFree(h->ws);
         delete h;
-        return cuda_fail(e, "cudaMemset");
+        return cuda_fail(e, "router weight split");
     }
+    h->rplan = moe::plan_router_tc(h->E, (flags & 2) ? 3 : (flags & 1) ? 2 : 1);
     st = build_maps(h);
     if (st != MOE_OK) {
         cudaFree(h->ws);
@@ -461,6 +567,12 @@ moe_status moe_route(moe_handle *h, const void *X, int T, int32_t *topk_idx, flo
     if (T == 0) return MOE_OK;
     if (!X || !topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "X, topk_idx and topk_w are required");
     if (!aligned16(X)) return fail(MOE_ERR_INVALID_ARG, "X is not 16-byte aligned");
+    if (!h->x_f32) {
+        int n = 0;
+        moe_status st = run_router_tc(h, X, T, topk_idx, topk_w, nullptr, reinterpret_cast<cudaStream_t>(stream), &n);
+        h->last_launches = n;
+        return st;
+    }
     moe::RouterArgs ra{};
     ra.X = X;
     ra.x_f32 = h->x_f32;
@@ -592,6 +704,11 @@ moe_status moe_get_stage_times(moe_handle *h, float *ms, int max, int *n) {
     }
     *n = count;
     return MOE_OK;
+}
+
+const char *moe_get_stage_name(const moe_handle *h, int i) {
+    if (h == nullptr || i < 0 || i >= h->last_launches || i >= moe_handle::kMaxStages) return nullptr;
+    return h->stage_name[i];
 }
 
 moe_status moe_inspect(const moe_handle *h, int buffer, void *dst, size_t bytes, moe_stream_t stream) {

@@ -44,6 +44,104 @@ __device__ __forceinline__ bool better(float c, int e, float bc, int be) {
     return c > bc || (c == bc && e < be);
 }
 
+// The routing rule for one token, by a group of LPT consecutive lanes: lane
+// `sub` of the group holds the logits of experts sub, sub+LPT, ... in lg[0..7]
+// (E <= 8*LPT).  s = sigmoid(l) (or softmax over e); k times, the largest
+// s + bias among the experts not chosen yet (equal values: lower expert index)
+// is chosen; weights from the unbiased s, renormalised when route_norm is set,
+// then times route_scale.  Every lane of the warp must call it (shuffles);
+// only groups with `valid` write slots (lane sub writes slots r = sub mod LPT)
+// and count the chosen experts in hist (shared memory) when it is given.
+template <int LPT>
+__device__ __forceinline__ void route_token_group(const float (&lg)[8], int sub, bool valid, int t, int E,
+                                                  int k, const float *bias, int score_func, int route_norm,
+                                                  float route_scale, int32_t *topk_idx, float *topk_w,
+                                                  int *hist) {
+    float s[8], c[8];
+    if (score_func == 1) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (sub + LPT * j < E) m = fmaxf(m, lg[j]);
+#pragma unroll
+        for (int o = LPT / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o, LPT));
+        float z = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            s[j] = (sub + LPT * j < E) ? expf(lg[j] - m) : 0.f;
+            z += s[j];
+        }
+#pragma unroll
+        for (int o = LPT / 2; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o, LPT);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s[j] = s[j] / z;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s[j] = 1.0f / (1.0f + expf(-lg[j]));
+    }
+    uint32_t open = 0;  // bit j: expert sub + LPT*j is still a candidate
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int e = sub + LPT * j;
+        if (e < E) {
+            const float cj = s[j] + (bias ? __ldg(bias + e) : 0.f);
+            c[j] = (cj != cj) ? -INFINITY : cj;  // NaN never wins
+            open |= 1u << j;
+        } else {
+            c[j] = -INFINITY;
+        }
+    }
+    float sel_s[16], wsum = 0.f;
+    int sel_e[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        sel_s[r] = 0.f;
+        sel_e[r] = 0;
+        if (r < k) {
+            float bc = -INFINITY;
+            int be = 0x7fffffff;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if ((open >> j & 1u) && better(c[j], sub + LPT * j, bc, be)) {
+                    bc = c[j];
+                    be = sub + LPT * j;
+                }
+#pragma unroll
+            for (int o = LPT / 2; o > 0; o >>= 1) {
+                const float oc = __shfl_xor_sync(0xffffffffu, bc, o, LPT);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, o, LPT);
+                if (better(oc, oe, bc, be)) {
+                    bc = oc;
+                    be = oe;
+                }
+            }
+            const int owner = be & (LPT - 1), jj = be / LPT;
+            float sv = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j == jj) sv = s[j];
+            if (sub == owner) open &= ~(1u << jj);
+            sv = __shfl_sync(0xffffffffu, sv, owner, LPT);
+            sel_s[r] = sv;
+            sel_e[r] = be;
+            wsum += sv;
+        }
+    }
+    if (valid) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            if (r < k && (r & (LPT - 1)) == sub) {
+                float w = sel_s[r];
+                if (route_norm) w = w / wsum;
+                w = w * route_scale;
+                topk_idx[(size_t)t * k + r] = sel_e[r];
+                topk_w[(size_t)t * k + r] = w;
+                if (hist != nullptr) atomicAdd(&hist[sel_e[r]], 1);
+            }
+        }
+    }
+}
+
 // One CTA = TT tokens.  Warp w owns tokens [w*TT/8, (w+1)*TT/8); lane l owns
 // experts l, l+32, ... so each warp ends with its tokens' logits in registers.
 template <int TT>
@@ -56,6 +154,8 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
 
     const int E = a.E, H = a.H, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t0 = blockIdx.x * TT;
+    pdl_wait();
+    pdl_trigger();
     for (int e = tid; e < E; e += kRouterThreads) hist[e] = 0;
 
     float acc[TPW][8];
@@ -119,86 +219,139 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
     for (int i = 0; i < TPW; ++i) {
         const int t = t0 + warp * TPW + i;
         if (t >= a.T) break;  // warp-uniform
-        float s[8], c[8];
-        if (a.score_func == 1) {
-            float m = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (lane + 32 * j < E) m = fmaxf(m, acc[i][j]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            float z = 0.f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                s[j] = (lane + 32 * j < E) ? expf(acc[i][j] - m) : 0.f;
-                z += s[j];
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) s[j] = s[j] / z;
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) s[j] = 1.0f / (1.0f + expf(-acc[i][j]));
-        }
-        uint32_t open = 0;  // bit j: expert lane+32j is a candidate
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int e = lane + 32 * j;
-            if (e < E) {
-                const float cj = s[j] + (a.bias ? __ldg(a.bias + e) : 0.f);
-                c[j] = (cj != cj) ? -INFINITY : cj;  // NaN never wins
-                open |= 1u << j;
-            } else {
-                c[j] = -INFINITY;
-            }
-        }
-        float wsum = 0.f, my_s = 0.f;
-        int my_e = 0;
-        for (int r = 0; r < a.k; ++r) {
-            float bc = -INFINITY;
-            int be = 0x7fffffff;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if ((open >> j & 1u) && better(c[j], lane + 32 * j, bc, be)) {
-                    bc = c[j];
-                    be = lane + 32 * j;
-                }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float oc = __shfl_xor_sync(0xffffffffu, bc, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (better(oc, oe, bc, be)) {
-                    bc = oc;
-                    be = oe;
-                }
-            }
-            const int owner = be & 31, jj = be >> 5;
-            float sv = 0.f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j == jj) sv = s[j];
-            if (lane == owner) open &= ~(1u << jj);
-            sv = __shfl_sync(0xffffffffu, sv, owner);
-            wsum += sv;
-            if (lane == r) {
-                my_e = be;
-                my_s = sv;
-            }
-        }
-        if (lane < a.k) {
-            float w = my_s;
-            if (a.route_norm) w = w / wsum;
-            w = w * a.route_scale;
-            a.topk_idx[(size_t)t * a.k + lane] = my_e;
-            a.topk_w[(size_t)t * a.k + lane] = w;
-            if (a.blk_hist != nullptr) atomicAdd(&hist[my_e], 1);
-        }
+        route_token_group<32>(acc[i], lane, true, t, a.E, a.k, a.bias, a.score_func, a.route_norm,
+                              a.route_scale, a.topk_idx, a.topk_w, a.blk_hist ? hist : nullptr);
     }
     if (a.blk_hist != nullptr) {
         __syncthreads();
         for (int e = tid; e < E; e += kRouterThreads)
-            a.blk_hist[(size_t)blockIdx.x * E + e] = hist[e];
+            a.blk_hist[(size_t)blockIdx.x * a.hb + (size_t)e * a.he] = hist[e];
+    }
+}
+
+// Dispatch scan over block histograms, by one CTA of 1024 threads.  Per expert
+// (one warp each): total over blocks; one warp scans the totals over experts
+// (offs, tile_offs, active); then per expert the exclusive scan over blocks,
+// offset by the expert's first row, replaces the block counts in place.
+constexpr int kScanThreads = 1024;
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+__device__ void dispatch_scan_block(int32_t *blk_hist, int nb, int E, int hb, int he, int tile_m,
+                                    int32_t *offs, int32_t *tile_offs, int32_t *active) {
+    __shared__ int cnt[256];
+    __shared__ int base[256];
+    if (hb == 0 && he == 0) {
+        hb = E;
+        he = 1;
+    }
+    if (tile_m <= 0) tile_m = kGemmBM;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int kWarps = blockDim.x / 32;
+    for (int e = warp; e < E; e += kWarps) {
+        int s = 0;
+        for (int b = lane; b < nb; b += 32) s += __ldcg(blk_hist + (size_t)b * hb + (size_t)e * he);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) cnt[e] = s;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int run = 0, trun = 0, nact = 0;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            const int c = e < E ? cnt[e] : 0;
+            const int tl = (c + tile_m - 1) / tile_m;
+            const int inc = warp_incl_scan(c, lane), tinc = warp_incl_scan(tl, lane);
+            const unsigned act = __ballot_sync(0xffffffffu, c > 0);
+            if (e < E) {
+                base[e] = run + inc - c;
+                offs[e] = run + inc - c;
+                tile_offs[e] = trun + tinc - tl;
+                if (c > 0) active[nact + __popc(act & ((1u << lane) - 1u))] = e;
+            }
+            run += __shfl_sync(0xffffffffu, inc, 31);
+            trun += __shfl_sync(0xffffffffu, tinc, 31);
+            nact += __popc(act);
+        }
+        if (lane == 0) {
+            offs[E] = run;
+            tile_offs[E] = trun;
+            active[E] = nact;
+        }
+    }
+    __syncthreads();
+    for (int e = warp; e < E; e += kWarps) {
+        int carry = base[e];
+        for (int b0 = 0; b0 < nb; b0 += 32) {
+            const int b = b0 + lane;
+            const int v = b < nb ? __ldcg(blk_hist + (size_t)b * hb + (size_t)e * he) : 0;
+            const int inc = warp_incl_scan(v, lane);
+            if (b < nb) blk_hist[(size_t)b * hb + (size_t)e * he] = carry + inc - v;
+            carry += __shfl_sync(0xffffffffu, inc, 31);
+        }
+    }
+}
+
+// Routing rule from the fp32 logits of the tensor-core router (partial sums of
+// its split-K CTAs, added in split order): LPT lanes per token, 8 experts per
+// lane, TT = min(128, 1024 / LPT) tokens per CTA, expert histogram per CTA.
+// The last CTA to finish runs the dispatch scan (its ticket comes from an
+// atomic counter; no CTA waits for another).
+template <int LPT>
+__host__ __device__ constexpr int topk_tt() { return (1024 / LPT) < 128 ? (1024 / LPT) : 128; }
+
+template <int LPT>
+__global__ void __launch_bounds__(1024) topk_kernel(const TopkArgs a) {
+    constexpr int TT = topk_tt<LPT>();
+    __shared__ int hist[256];
+    __shared__ int is_last;
+    const int E = a.E, sub = threadIdx.x & (LPT - 1), grp = threadIdx.x / LPT;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    pdl_wait();
+    pdl_trigger();
+    __syncthreads();
+    const int t = blockIdx.x * TT + grp;
+    const bool valid = t < a.T;
+    float l[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) l[j] = 0.f;
+    if (valid) {
+#pragma unroll
+        for (int z = 0; z < kMaxRouterSplits; ++z)
+            if (z < a.splits) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int e = sub + LPT * j;
+                    if (e < E) l[j] += __ldg(a.logits + ((size_t)z * a.T + t) * a.ld + e);
+                }
+            }
+    }
+    route_token_group<LPT>(l, sub, valid, t, E, a.k, a.bias, a.score_func, a.route_norm, a.route_scale,
+                           a.topk_idx, a.topk_w, a.blk_hist ? hist : nullptr);
+    if (a.blk_hist != nullptr) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            a.blk_hist[(size_t)blockIdx.x * a.hb + (size_t)e * a.he] = hist[e];
+        if (a.offs != nullptr) {
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) is_last = atomicAdd(a.counter, 1) == (int)gridDim.x - 1;
+            __syncthreads();
+            if (is_last) {
+                __threadfence();
+                dispatch_scan_block(a.blk_hist, gridDim.x, E, a.hb, a.he, a.tile_m, a.offs, a.tile_offs,
+                                    a.active);
+                if (threadIdx.x == 0) *a.counter = 0;
+            }
+        }
     }
 }
 
@@ -206,56 +359,49 @@ size_t router_smem(int TT, int E) { return (size_t)(TT + E) * kPad * 4 + (size_t
 
 // ------------------------------------------------------------------- scan
 
-constexpr int kScanThreads = 1024;
-
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs a) {
-    __shared__ int cnt[256];
-    __shared__ int base[257];
-    const int E = a.E, nb = a.nb;
-    for (int e = threadIdx.x; e < E; e += kScanThreads) {
-        int run = 0;
-        for (int b = 0; b < nb; ++b) {  // exclusive scan over blocks, per expert
-            const int v = a.blk_hist[(size_t)b * E + e];
-            a.blk_hist[(size_t)b * E + e] = run;
-            run += v;
-        }
-        cnt[e] = run;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int o = 0, to = 0, n = 0;
-        for (int e = 0; e < E; ++e) {
-            base[e] = o;
-            a.offs[e] = o;
-            a.tile_offs[e] = to;
-            o += cnt[e];
-            to += (cnt[e] + kGemmBM - 1) / kGemmBM;
-            if (cnt[e] > 0) a.active[n++] = e;
-        }
-        a.offs[E] = o;
-        a.tile_offs[E] = to;
-        a.active[E] = n;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < nb * E; i += kScanThreads) a.blk_hist[i] += base[i % E];
+    pdl_wait();
+    pdl_trigger();
+    dispatch_scan_block(a.blk_hist, a.nb, a.E, a.hb, a.he, a.tile_m, a.offs, a.tile_offs, a.active);
 }
 
 // ---------------------------------------------------------------- scatter
 
 constexpr int kScatterThreads = 256;
+constexpr int kMaxTT = 128;
 
+// grid (token blocks, gather_split).  Every CTA of a token block builds, per
+// expert, the bitmask of the block's tokens that chose it; the rank of slot
+// (t, j) among its expert's rows in this block is the number of earlier tokens
+// in that mask (a token's k experts are distinct; a repeat is reported and
+// dropped).  CTA y = 0 writes the index arrays; the CTAs of a block share the
+// copy of the X rows.
 __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterArgs a) {
-    __shared__ int e_s[32 * 16];
-    __shared__ int slot_s[32 * 16];
+    __shared__ uint32_t masks[256][kMaxTT / 32];
+    __shared__ int e_s[kMaxTT * 16];
+    __shared__ int slot_s[kMaxTT * 16];
     const int TT = a.tokens_per_block, k = a.k, E = a.E, H = a.H;
+    const int hb = (a.hb | a.he) ? a.hb : E, he = (a.hb | a.he) ? a.he : 1;
+    const int words = (TT + 31) / 32;
     const int tok0 = blockIdx.x * TT;
+    pdl_wait();
+    pdl_trigger();
     const int n = max(0, min(TT, a.T - tok0)) * k;
     const size_t ent0 = (size_t)tok0 * k;
+    for (int i = threadIdx.x; i < E * words; i += kScatterThreads) masks[i / words][i % words] = 0;
+    __syncthreads();
     for (int i = threadIdx.x; i < n; i += kScatterThreads) {
         int e = a.topk_idx[ent0 + i];
         if (e < 0 || e >= E) {
-            atomicOr(a.err, ERR_BOUNDS);
+            if (blockIdx.y == 0) atomicOr(a.err, ERR_BOUNDS);
             e = -1;
+        } else {
+            const int tl = i / k;
+            const uint32_t bit = 1u << (tl & 31);
+            if (atomicOr(&masks[e][tl >> 5], bit) & bit) {
+                if (blockIdx.y == 0) atomicOr(a.err, ERR_BOUNDS);
+                e = -1;
+            }
         }
         e_s[i] = e;
     }
@@ -264,17 +410,19 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
         const int e = e_s[i];
         int slot = -1;
         if (e >= 0) {
-            int rank = 0;  // entries of the same expert earlier in (token, slot) order
-            for (int q = 0; q < i; ++q) rank += (e_s[q] == e);
-            slot = a.blk_base[(size_t)blockIdx.x * E + e] + rank;
-            a.sorted_tok[slot] = tok0 + i / k;
+            const int tl = i / k;
+            int rank = __popc(masks[e][tl >> 5] & ((1u << (tl & 31)) - 1u));
+            for (int w = 0; w < (tl >> 5); ++w) rank += __popc(masks[e][w]);
+            slot = a.blk_base[(size_t)blockIdx.x * hb + (size_t)e * he] + rank;
+            if (blockIdx.y == 0) a.sorted_tok[slot] = tok0 + tl;
         }
-        a.slot_of[ent0 + i] = slot;
+        if (blockIdx.y == 0) a.slot_of[ent0 + i] = slot;
         slot_s[i] = slot;
     }
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = warp; i < n; i += kScatterThreads / 32) {
+    const int nw = kScatterThreads / 32;
+    for (int i = blockIdx.y * nw + warp; i < n; i += gridDim.y * nw) {
         const int slot = slot_s[i];
         if (slot < 0) continue;
         const size_t src = (size_t)(tok0 + i / k) * H, dst = (size_t)slot * H;
@@ -299,6 +447,8 @@ constexpr int kCombineThreads = 128;
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
     const int t = blockIdx.x, k = a.k, H = a.H;
+    pdl_wait();
+    pdl_trigger();
     for (int c = threadIdx.x * 8; c < H; c += kCombineThreads * 8) {
         float acc[8];
 #pragma unroll
@@ -346,27 +496,50 @@ cudaError_t launch_router(const RouterArgs &a, cudaStream_t s) {
     const int TT = a.tokens_per_block;
     const int nb = (a.T + TT - 1) / TT;
     const size_t smem = router_smem(TT, a.E);
-    if (TT == 32)
-        router_kernel<32><<<nb, kRouterThreads, smem, s>>>(a);
-    else
-        router_kernel<16><<<nb, kRouterThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    if (TT == 32) return launch_pdl(router_kernel<32>, dim3(nb), dim3(kRouterThreads), smem, s, a);
+    return launch_pdl(router_kernel<16>, dim3(nb), dim3(kRouterThreads), smem, s, a);
+}
+
+static int topk_lpt(int E) {
+    int l = 2;
+    while (l * 8 < E) l <<= 1;
+    return l;
+}
+
+int topk_tokens_per_block(int E) {
+    switch (topk_lpt(E)) {
+    case 2: return topk_tt<2>();
+    case 4: return topk_tt<4>();
+    case 8: return topk_tt<8>();
+    case 16: return topk_tt<16>();
+    default: return topk_tt<32>();
+    }
+}
+
+cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s) {
+    const int lpt = topk_lpt(a.E), tt = topk_tokens_per_block(a.E);
+    const dim3 grid((a.T + tt - 1) / tt), block(tt * lpt);
+    switch (lpt) {
+    case 2: return launch_pdl(topk_kernel<2>, grid, block, 0, s, a);
+    case 4: return launch_pdl(topk_kernel<4>, grid, block, 0, s, a);
+    case 8: return launch_pdl(topk_kernel<8>, grid, block, 0, s, a);
+    case 16: return launch_pdl(topk_kernel<16>, grid, block, 0, s, a);
+    default: return launch_pdl(topk_kernel<32>, grid, block, 0, s, a);
+    }
 }
 
 cudaError_t launch_scan(const ScanArgs &a, cudaStream_t s) {
-    scan_kernel<<<1, kScanThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(scan_kernel, dim3(1), dim3(kScanThreads), 0, s, a);
 }
 
 cudaError_t launch_scatter(const ScatterArgs &a, cudaStream_t s) {
     const int nb = (a.T + a.tokens_per_block - 1) / a.tokens_per_block;
-    scatter_kernel<<<nb, kScatterThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(scatter_kernel, dim3(nb, a.gather_split > 0 ? a.gather_split : 1), dim3(kScatterThreads),
+                      0, s, a);
 }
 
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
-    combine_kernel<<<a.T, kCombineThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3(a.T), dim3(kCombineThreads), 0, s, a);
 }
 
 }  // namespace moe

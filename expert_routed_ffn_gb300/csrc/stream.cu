@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(kThreads) decode_glu_kernel(const DecodeGluArg
     extern __shared__ __align__(16) unsigned char dsm[];
     bf16 *xs = reinterpret_cast<bf16 *>(dsm);  // [kMT][H]
     int expert, row0, m;
+    pdl_wait();
+    pdl_trigger();
     if (!pick_group(a.g, expert, row0, m)) return;
     const int H = a.H;
     const bool shared = expert < 0;
@@ -137,6 +139,8 @@ __global__ void __launch_bounds__(kThreads) decode_down_kernel(const DecodeDownA
     extern __shared__ __align__(16) unsigned char dsm[];
     bf16 *hs = reinterpret_cast<bf16 *>(dsm);  // [kMT][K]
     int expert, row0, m;
+    pdl_wait();
+    pdl_trigger();
     if (!pick_group(a.g, expert, row0, m)) return;
     const int H = a.H;
     const bool shared = expert < 0;
@@ -190,8 +194,7 @@ cudaError_t launch_decode_glu(const DecodeGluArgs &a, cudaStream_t s) {
     });
     const int W = a.g.shared ? max(a.I, a.S) : a.I;
     dim3 grid((W + kRowsPerCta - 1) / kRowsPerCta, a.g.E + 1);
-    decode_glu_kernel<<<grid, kThreads, (size_t)kMT * a.H * 2, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_glu_kernel, grid, dim3(kThreads), (size_t)kMT * a.H * 2, s, a);
 }
 
 cudaError_t launch_decode_down(const DecodeDownArgs &a, cudaStream_t s) {
@@ -202,8 +205,7 @@ cudaError_t launch_decode_down(const DecodeDownArgs &a, cudaStream_t s) {
     });
     const int K = a.g.shared ? max(a.I, a.S) : a.I;
     dim3 grid((a.H + kRowsPerCta - 1) / kRowsPerCta, a.g.E + 1);
-    decode_down_kernel<<<grid, kThreads, (size_t)kMT * K * 2, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_down_kernel, grid, dim3(kThreads), (size_t)kMT * K * 2, s, a);
 }
 
 }  // namespace moe

@@ -168,11 +168,15 @@ typedef struct {
 moe_status moe_get_stats(const moe_handle *h, moe_stats *out);
 
 /* With MOE_OPT_STAGE_EVENTS on: wait for the last moe_forward and write the
- * duration in ms of each of its kernels, in launch order (router, dispatch
- * scan, dispatch scatter, gate/up, down, combine), to ms[0..*n).  At most
- * `max` values are written.  Errors: INVALID_ARG (events off, no forward yet,
+ * duration in ms of each of its kernels, in launch order (names from
+ * moe_get_stage_name), to ms[0..*n).  At most `max` values are written.  Errors: INVALID_ARG (events off, no forward yet,
  * NULL argument), CUDA. */
 moe_status moe_get_stage_times(moe_handle *h, float *ms, int max, int *n);
+
+/* Name of kernel i (0-based, launch order) of the last call, e.g. "router_logits",
+ * "router_topk_scan", "dispatch_scatter", "gate_up_gemm", "down_gemm", "combine";
+ * NULL when i is out of range.  The string is static. */
+const char *moe_get_stage_name(const moe_handle *h, int i);
 
 typedef enum {
     MOE_BUF_TOPK_IDX = 0,     /* [T, k] int32, routing of the last forward */
