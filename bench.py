@@ -127,13 +127,15 @@ def run_ours(args, shape):
     inputs = wl.make_inputs(shape, dev)
     blk = capi.block_from_inputs(shape, inputs, max_tokens=shape.T)
     if args.path:
-        blk.set_option(capi.MOE_OPT_PATH, {"decode": capi.PATH_DECODE, "grouped": capi.PATH_GROUPED}[args.path])
+        blk.set_option(capi.MOE_OPT_PATH, {"decode": capi.PATH_DECODE, "grouped": capi.PATH_GROUPED,
+                                           "swapped": capi.PATH_SWAPPED}[args.path])
     X = inputs["X"]
     Y = torch.empty_like(X)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step():
-        flush.fill_(1)  # evicts L2; not inside the timed events
+        if not args.no_flush:
+            flush.fill_(1)  # evicts L2; not inside the timed events
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record()
@@ -215,10 +217,10 @@ def run_ours(args, shape):
     stage_avg = {n: stage_sum[i] / args.steps for i, n in enumerate(names)}
     dom = max(stage_avg, key=stage_avg.get)
     roof = None
-    key = {"gate_up_gemm": "gate_up", "decode_gate_up": "gate_up", "down_gemm": "down",
-           "decode_down": "down"}.get(dom)
+    key = {"gate_up_gemm": "gate_up", "decode_gate_up": "gate_up", "gate_up_gemm_swapped": "gate_up",
+           "down_gemm": "down", "decode_down": "down", "down_gemm_swapped": "down"}.get(dom)
     if key is None:  # report the heavier expert GEMM when a small kernel leads
-        gemms = [n for n in stage_avg if n in ("gate_up_gemm", "decode_gate_up", "down_gemm", "decode_down")]
+        gemms = [n for n in stage_avg if "gemm" in n or n.startswith("decode_")]
         if gemms:
             dom = max(gemms, key=stage_avg.get)
             key = "gate_up" if "gate_up" in dom else "down"
@@ -247,9 +249,10 @@ def run_ours(args, shape):
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, U(-0.1,0.1) or Zipf bias)",
         "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "E": shape.E, "k": shape.k,
                    "I": shape.I, "S": shape.S, "shared_packed": shape.shared_packed,
-                   "hidden_act": shape.hidden_act, "path": {1: "decode", 2: "grouped"}[path],
+                   "hidden_act": shape.hidden_act, "path": {1: "decode", 2: "grouped", 3: "swapped"}[path],
                    "parallelism": f"replicas{world}",
-                   "l2": "flushed before every step (256 MiB write), flush outside the timed events"},
+                   "l2": ("not flushed: inputs larger than L2" if args.no_flush else
+                          "flushed before every step (256 MiB write), flush outside the timed events")},
         "roofline": roof,
         "block_roofline": {"t_roof_us": round(max(t_tc, t_hbm) * 1e6, 2), "t_meas_us": round(ms * 1e3, 2),
                            "frac": round(max(t_tc, t_hbm) / (ms / 1e3), 4),
@@ -276,7 +279,8 @@ def traffic_of(stage: str, workload: str):
     the current source of that kernel; else None."""
     import hashlib
     src = {"gate_up_gemm": "gemm_tc.cu", "down_gemm": "gemm_tc.cu", "decode_gate_up": "stream.cu",
-           "decode_down": "stream.cu"}.get(stage)
+           "decode_down": "stream.cu", "gate_up_gemm_swapped": "gemm_sab.cu",
+           "down_gemm_swapped": "gemm_sab.cu"}.get(stage)
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if src is None or not os.path.exists(path):
         return None
@@ -366,10 +370,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="nano_decode")
-    ap.add_argument("--path", choices=["decode", "grouped"], default=None)
+    ap.add_argument("--path", choices=["decode", "grouped", "swapped"], default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--preroll", type=float, default=1.0, help="seconds of untimed steps before timing")
+    ap.add_argument("--no-flush", action="store_true",
+                    help="skip the L2 flush between steps (only valid when the inputs exceed L2)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

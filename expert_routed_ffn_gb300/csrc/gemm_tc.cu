@@ -44,12 +44,15 @@ struct Tile {
     int seg, group, mt, nt, row0, m_valid;
 };
 
-__device__ __forceinline__ int seg_tiles(const GemmSegment &s) {
+// offs / toffs: shared-memory copies of segment 0's dispatch offsets (only
+// segment 0 may be grouped)
+__device__ __forceinline__ int seg_tiles(const GemmSegment &s, const int *toffs) {
     if (s.dense) return ((s.m_dense + kGemmBM - 1) / kGemmBM) * s.n_tiles;
-    return s.tile_offs[s.num_groups] * s.n_tiles;
+    return toffs[s.num_groups] * s.n_tiles;
 }
 
-__device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, int tiles0) {
+__device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, int tiles0, const int *offs,
+                                            const int *toffs) {
     Tile t;
     t.seg = 0;
     if (tile >= tiles0) {
@@ -69,19 +72,19 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, int til
         int lo = 0, hi = s.num_groups - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (s.tile_offs[mid] * s.n_tiles <= tile)
+            if (toffs[mid] * s.n_tiles <= tile)
                 lo = mid;
             else
                 hi = mid - 1;
         }
-        const int mt_g = s.tile_offs[lo + 1] - s.tile_offs[lo];
-        const int local = tile - s.tile_offs[lo] * s.n_tiles;
+        const int mt_g = toffs[lo + 1] - toffs[lo];
+        const int local = tile - toffs[lo] * s.n_tiles;
         t.group = lo;
         t.nt = local / mt_g;
         t.mt = local % mt_g;
-        const int start = s.offs[lo];
+        const int start = offs[lo];
         t.row0 = start + t.mt * kGemmBM;
-        t.m_valid = min(kGemmBM, s.offs[lo + 1] - t.row0);
+        t.m_valid = min(kGemmBM, offs[lo + 1] - t.row0);
     }
     return t;
 }
@@ -144,9 +147,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // (offsets, tile counts) and the A rows are read only after this point
     pdl_wait();
     pdl_trigger();
+    // every role decodes every tile: keep the dispatch offsets on chip
+    __shared__ int s_offs[257], s_toffs[257];
+    if (!p.seg[0].dense)
+        for (int i = threadIdx.x; i <= p.seg[0].num_groups; i += blockDim.x) {
+            s_offs[i] = p.seg[0].offs[i];
+            s_toffs[i] = p.seg[0].tile_offs[i];
+        }
+    __syncthreads();
     const uint32_t tmem_base = *tmem_slot;
-    const int tiles0 = seg_tiles(p.seg[0]);
-    const int total = tiles0 + (p.num_segs > 1 ? seg_tiles(p.seg[1]) : 0);
+    const int tiles0 = seg_tiles(p.seg[0], s_toffs);
+    const int total = tiles0 + (p.num_segs > 1 ? seg_tiles(p.seg[1], s_toffs) : 0);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -154,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t L = 0;  // loads issued so far; stage = L % kStages
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                const Tile t = decode_tile(p, tile, tiles0);
+                const Tile t = decode_tile(p, tile, tiles0, s_offs, s_toffs);
                 const GemmSegment &sg = p.seg[t.seg];
                 const CUtensorMap *mA = t.seg ? &p.A1 : &p.A0;
                 const CUtensorMap *mB = t.seg ? &p.B2 : &p.B0;
@@ -195,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t L = 0, n_acc = 0;
             bool ok = true, issued = false;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                const Tile t = decode_tile(p, tile, tiles0);
+                const Tile t = decode_tile(p, tile, tiles0, s_offs, s_toffs);
                 const GemmSegment &sg = p.seg[t.seg];
                 const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
                 if (!mbar_wait(tempty_bar(a), aph ^ 1u, p.wait_ns, abort_flag)) {
@@ -239,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const int r = q * 32 + lane;
         uint32_t n_acc = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            const Tile t = decode_tile(p, tile, tiles0);
+            const Tile t = decode_tile(p, tile, tiles0, s_offs, s_toffs);
             const GemmSegment &sg = p.seg[t.seg];
             const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
             // every lane waits; the answer is made warp-uniform because the
@@ -334,11 +345,15 @@ EncodeTiledFn encode_fn() {
 size_t gemm_tc_smem_bytes() { return kSmemBytes; }
 
 CUresult encode_map_a(CUtensorMap *m, const void *ptr, int rows, int K) {
+    return encode_map_a_box(m, ptr, rows, K, kGemmBM);
+}
+
+CUresult encode_map_a_box(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kGemmBK, (cuuint32_t)kGemmBM};
+    const cuuint32_t box[2] = {(cuuint32_t)kGemmBK, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

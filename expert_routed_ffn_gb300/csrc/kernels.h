@@ -70,26 +70,22 @@ struct RouterTcArgs {
     unsigned long long wait_ns;
 };
 // Routing rule from logits: a group of lanes per token (8 experts per lane),
-// topk_tokens_per_block(E) tokens per CTA; writes the expert histogram of each
-// CTA's tokens to blk_hist.  With offs set, the last CTA to finish also runs
-// the dispatch scan.
+// topk_tokens_per_block(E, T, SMs) tokens per CTA; writes the expert
+// histogram of each CTA's tokens to blk_hist.
 constexpr int kMaxRouterSplits = 4;
-int topk_tokens_per_block(int E);
+int topk_tokens_per_block(int E, int T, int num_sms);
 struct TopkArgs {
     const float *logits;   // [splits, T, ld] partial logits, summed in split order
     int ld, T, E, k, splits;
     int hb, he;            // histogram strides, as in ScanArgs
-    int tile_m;            // m-tile of the grouped GEMM (tile_offs), 0 = kGemmBM
     const float *bias;     // [E] or nullptr
     int score_func, route_norm;
     float route_scale;
     int32_t *topk_idx;     // [T, k]
     float *topk_w;         // [T, k]
-    int32_t *blk_hist;     // [ceil(T/32), E] or nullptr
-    int *counter;          // CTA ticket for the fused scan (0 between calls)
-    int32_t *offs, *tile_offs, *active;  // scan outputs, or nullptr for no fused scan
+    int32_t *blk_hist;     // block histograms or nullptr
 };
-cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s);
+cudaError_t launch_topk(const TopkArgs &a, int tokens_per_block, cudaStream_t s);
 struct RouterTcPlan {
     int Np, tmem_cols, stages, smem, parts;
 };
@@ -117,10 +113,12 @@ cudaError_t launch_scan(const ScanArgs &a, cudaStream_t s);
 
 struct ScatterArgs {
     const int32_t *topk_idx;  // [T, k]; the k experts of a token are distinct
-    const int32_t *blk_base;  // (b, e) at b*hb + e*he
+    const int32_t *blk_hist;  // expert counts of each token block; (b, e) at b*hb + e*he
     int hb, he;
+    int32_t *offs, *tile_offs, *active;  // written by CTA (0, 0): as in ScanArgs
+    int tile_m;                          // 0: kGemmBM
     int T, k, E, H;
-    int tokens_per_block;     // 16, 32 or 128 (the router's blocking)
+    int tokens_per_block;     // <= 128: the router's blocking
     int gather_split;         // CTAs per token block sharing the row gather
     const void *X;            // [T, H]
     int x_f32;
@@ -178,9 +176,34 @@ struct GemmArgs {
 cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s);
 size_t gemm_tc_smem_bytes();
 
+// Swapped-operand expert GEMMs for few tokens per expert (gemm_sab.cu): weight
+// rows are the MMA's M = 128, n_tokens (32 or 64) token rows its N.
+struct SabSegment {
+    int dense, num_groups, group_base, m_dense;
+    const int32_t *offs;       // [num_groups + 1] (grouped)
+    const int32_t *tile_offs;  // [num_groups + 1] prefix of ceil(m_g / n_tokens)
+    int w_tiles;               // weight tiles per group (64 gate/up outputs, or 128 down outputs)
+    int k_blocks;              // K / 64
+    int n_out;                 // valid output columns
+    __nv_bfloat16 *out;        // [rows, ldo]
+    int ldo;
+};
+struct SabArgs {
+    // segment 0: weights Wa0 (+Wb0 = up for gate/up), tokens X0; segment 1 likewise
+    CUtensorMap Wa0, Wb0, X0, Wa1, Wb1, X1;
+    SabSegment seg[2];
+    int num_segs, glu, act;
+    float alpha, limit, beta;
+    int *err;
+    unsigned long long wait_ns;
+    int num_ctas, stages;
+};
+cudaError_t launch_gemm_sab(const SabArgs &a, int n_tokens, cudaStream_t s);
+
 // Tensor maps (TMA descriptors) for the GEMMs.  A: [rows, K] bf16, box 128 x 64.
 // B: [groups, rows, K] bf16, box box_rows x 64.  Both with 128-byte swizzle.
 CUresult encode_map_a(CUtensorMap *m, const void *ptr, int rows, int K);
+CUresult encode_map_a_box(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows);
 CUresult encode_map_b(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int box_rows);
 
 // ------------------------------------------------- decode streamers (K6)

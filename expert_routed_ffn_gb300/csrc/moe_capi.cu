@@ -43,7 +43,12 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-constexpr int kPathAuto = 0, kPathDecode = 1, kPathGrouped = 2;
+constexpr int kPathAuto = 0, kPathDecode = 1, kPathGrouped = 2, kPathSwapped = 3;
+// Auto path: the swapped-operand GEMMs only up to this many expected tokens
+// per expert (T*k/E).  Measured on GB300 they tie the grouped GEMMs on decode
+// sizes and lose where the shared expert sees many tokens (each weight tile is
+// re-read per token tile), so the auto path keeps the grouped GEMMs.
+constexpr int kSwapMaxTokensPerExpert = 0;
 // Auto path: the decode kernels only up to this many tokens.  Measured on
 // GB300, the tcgen05 grouped path is at least as fast down to T = 1, so the
 // auto path always takes it; the decode kernels stay selectable.
@@ -82,6 +87,12 @@ struct moe_handle {
 
     // TMA descriptors fixed at create
     CUtensorMap m_xsorted, m_hbuf, m_hs, m_xbf16, m_gate, m_up, m_down, m_shg, m_shu, m_shd, m_wr;
+    // swapped-operand GEMMs: weight boxes of 64 (gate/up) and 128 (down) rows,
+    // token boxes of 32 ([0]) or 64 ([1]) rows
+    CUtensorMap m_gate64, m_up64, m_down128, m_shg64, m_shu64, m_shd128;
+    CUtensorMap m_xs_n[2], m_hb_n[2], m_hs_n[2], m_xbf_n[2], m_x_n[2];
+    const void *m_x_n_ptr[2] = {nullptr, nullptr};
+    int m_x_n_rows[2] = {0, 0};
     // descriptor of the caller's X for the shared-expert GEMM (cached by pointer and T)
     CUtensorMap m_x;
     const void *m_x_ptr = nullptr;
@@ -155,7 +166,7 @@ struct Carver {
 
 void carve(moe_handle *h, void *base) {
     const size_t MT = h->cfg.max_tokens, k = h->k, H = h->H, E = h->E;
-    const size_t nb = (MT + 15) / 16;
+    const size_t nb = (MT + 7) / 8;  // token blocks of at least 8
     const size_t elt = h->x_f32 ? 4 : 2;
     Carver c;
     h->err = c.take<int>(base, 64);
@@ -199,6 +210,16 @@ moe_status build_maps(moe_handle *h) {
     MAP(moe::encode_map_b(&h->m_up, h->w.up, Ep, I, H, 128));
     MAP(moe::encode_map_b(&h->m_down, h->w.down, Ep, H, I, moe::kGemmBN));
     MAP(moe::encode_map_b(&h->m_wr, h->wr_parts, h->rplan.parts, h->E, H, h->rplan.Np));
+    MAP(moe::encode_map_b(&h->m_gate64, h->w.gate, Ep, I, H, 64));
+    MAP(moe::encode_map_b(&h->m_up64, h->w.up, Ep, I, H, 64));
+    MAP(moe::encode_map_b(&h->m_down128, h->w.down, Ep, H, I, 128));
+    for (int v = 0; v < 2; ++v) {
+        const int n = v ? 64 : 32;
+        MAP(moe::encode_map_a_box(&h->m_xs_n[v], h->x_sorted, MT * k, H, n));
+        MAP(moe::encode_map_a_box(&h->m_hb_n[v], h->hbuf, MT * k, I, n));
+        if (h->has_shared) MAP(moe::encode_map_a_box(&h->m_hs_n[v], h->hs, MT, S, n));
+        if (h->has_shared && h->x_f32) MAP(moe::encode_map_a_box(&h->m_xbf_n[v], h->x_bf16, MT, H, n));
+    }
     if (h->has_shared) {
         MAP(moe::encode_map_a(&h->m_hs, h->hs, MT, S));
         if (h->x_f32) MAP(moe::encode_map_a(&h->m_xbf16, h->x_bf16, MT, H));
@@ -206,10 +227,16 @@ moe_status build_maps(moe_handle *h) {
             h->m_shg = h->m_gate;
             h->m_shu = h->m_up;
             h->m_shd = h->m_down;
+            h->m_shg64 = h->m_gate64;
+            h->m_shu64 = h->m_up64;
+            h->m_shd128 = h->m_down128;
         } else {
             MAP(moe::encode_map_b(&h->m_shg, h->w.sh_gate, 1, S, H, 128));
             MAP(moe::encode_map_b(&h->m_shu, h->w.sh_up, 1, S, H, 128));
             MAP(moe::encode_map_b(&h->m_shd, h->w.sh_down, 1, H, S, moe::kGemmBN));
+            MAP(moe::encode_map_b(&h->m_shg64, h->w.sh_gate, 1, S, H, 64));
+            MAP(moe::encode_map_b(&h->m_shu64, h->w.sh_up, 1, S, H, 64));
+            MAP(moe::encode_map_b(&h->m_shd128, h->w.sh_down, 1, H, S, 128));
         }
     }
 #undef MAP
@@ -250,7 +277,7 @@ moe_status x_map(moe_handle *h, const void *X, int T) {
 // Router for bf16 X: logits on the tensor cores, then the routing rule, one
 // warp per token.  Two launches.
 moe_status run_router_tc(moe_handle *h, const void *X, int T, int32_t *topk_idx, float *topk_w,
-                         int32_t *blk_hist, cudaStream_t s, int *n) {
+                         int32_t *blk_hist, cudaStream_t s, int *n, int tile_m) {
     moe_status st = x_map(h, X, T);
     if (st != MOE_OK) return st;
     moe::RouterTcArgs ra{};
@@ -280,7 +307,7 @@ moe_status run_router_tc(moe_handle *h, const void *X, int T, int32_t *topk_idx,
     ta.logits = h->logits;
     ta.ld = h->rplan.Np;
     ta.splits = splits;
-    ta.hb = 1;  // expert-major histograms: the scan reads each expert's blocks contiguously
+    ta.hb = 1;  // expert-major histograms: each expert's blocks are contiguous
     ta.he = h->hist_stride;
     ta.T = T;
     ta.E = h->E;
@@ -292,22 +319,19 @@ moe_status run_router_tc(moe_handle *h, const void *X, int T, int32_t *topk_idx,
     ta.topk_idx = topk_idx;
     ta.topk_w = topk_w;
     ta.blk_hist = blk_hist;
-    ta.counter = h->counter;
-    if (blk_hist != nullptr) {  // the forward path: the last top-k CTA runs the dispatch scan
-        ta.offs = h->offs;
-        ta.tile_offs = h->tile_offs;
-        ta.active = h->active;
-    }
-    return launched(h, moe::launch_topk(ta, s), blk_hist ? "router_topk_scan" : "router_topk", n, s);
+    return launched(h, moe::launch_topk(ta, moe::topk_tokens_per_block(h->E, T, h->num_sms), s), "router_topk",
+                    n, s);
 }
 
-// Router + dispatch, shared by both paths.  Returns launches through *n.
-moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n) {
+// Router + dispatch, shared by all paths (tile_m: rows per tile counted by
+// tile_offs).  Returns launches through *n.
+moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n, int tile_m) {
     // bf16 X: tensor-core logits + grouped-lane top-k; fp32 X: CUDA-core router
-    const int TT = h->x_f32 ? moe::router_tokens_per_block(T, h->num_sms) : moe::topk_tokens_per_block(h->E);
+    const int TT = h->x_f32 ? moe::router_tokens_per_block(T, h->num_sms)
+                            : moe::topk_tokens_per_block(h->E, T, h->num_sms);
     const int nb = (T + TT - 1) / TT;
     if (!h->x_f32) {
-        moe_status st = run_router_tc(h, X, T, h->topk_idx, h->topk_w, h->blk_hist, s, n);
+        moe_status st = run_router_tc(h, X, T, h->topk_idx, h->topk_w, h->blk_hist, s, n, tile_m);
         if (st != MOE_OK) return st;
     } else {
     moe::RouterArgs ra{};
@@ -334,17 +358,16 @@ moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n
     }
 
     moe_status st = MOE_OK;
-    if (h->x_f32) {
-        moe::ScanArgs sa{h->blk_hist, nb, h->E, h->offs, h->tile_offs, h->active, 1, h->hist_stride, 0};
-        st = launched(h, moe::launch_scan(sa, s), "dispatch_scan", n, s);
-        if (st != MOE_OK) return st;
-    }
 
     moe::ScatterArgs xa{};
     xa.topk_idx = h->topk_idx;
-    xa.blk_base = h->blk_hist;
+    xa.blk_hist = h->blk_hist;
     xa.hb = 1;
     xa.he = h->hist_stride;
+    xa.offs = h->offs;
+    xa.tile_offs = h->tile_offs;
+    xa.active = h->active;
+    xa.tile_m = tile_m;
     xa.T = T;
     xa.k = h->k;
     xa.E = h->E;
@@ -460,14 +483,79 @@ moe_status run_decode(moe_handle *h, const void *X, int T, cudaStream_t s, int *
     return MOE_OK;
 }
 
+// Swapped-operand expert GEMMs (weights as M, n_tok tokens as N), routed and
+// shared tiles in one launch per projection.
+moe_status run_swapped(moe_handle *h, const void *X, int T, cudaStream_t s, int *n, int n_tok) {
+    const int H = h->H, I = h->I, S = h->S, E = h->E, v = n_tok == 32 ? 0 : 1;
+    moe::SabArgs g{};
+    g.err = h->err;
+    g.wait_ns = h->wait_ns;
+    g.act = h->cfg.hidden_act;
+    g.alpha = h->cfg.act_alpha;
+    g.limit = h->cfg.act_limit;
+    g.beta = h->cfg.act_beta;
+    g.num_ctas = h->num_sms;
+    const int sh_base = h->cfg.shared_packed ? E : 0;
+
+    g.glu = 1;
+    g.Wa0 = h->m_gate64;
+    g.Wb0 = h->m_up64;
+    g.X0 = h->m_xs_n[v];
+    g.seg[0] = moe::SabSegment{0, E, 0, 0, h->offs, h->tile_offs, (I + 63) / 64, H / 64, I, h->hbuf, I};
+    g.num_segs = 1;
+    if (h->has_shared) {
+        if (h->x_f32) {
+            g.X1 = h->m_xbf_n[v];
+        } else {
+            if (h->m_x_n_ptr[v] != X || h->m_x_n_rows[v] != T) {
+                CUresult r = moe::encode_map_a_box(&h->m_x_n[v], X, T, H, n_tok);
+                if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(X) failed: %d", (int)r);
+                h->m_x_n_ptr[v] = X;
+                h->m_x_n_rows[v] = T;
+            }
+            g.X1 = h->m_x_n[v];
+        }
+        g.Wa1 = h->m_shg64;
+        g.Wb1 = h->m_shu64;
+        g.seg[1] = moe::SabSegment{1, 1, sh_base, T, nullptr, nullptr, (S + 63) / 64, H / 64, S, h->hs, S};
+        g.num_segs = 2;
+    }
+    moe_status st = launched(h, moe::launch_gemm_sab(g, n_tok, s), "gate_up_gemm_swapped", n, s);
+    if (st != MOE_OK) return st;
+
+    g.glu = 0;
+    g.Wa0 = h->m_down128;
+    g.X0 = h->m_hb_n[v];
+    g.seg[0] = moe::SabSegment{0, E, 0, 0, h->offs, h->tile_offs, (H + 127) / 128, I / 64, H, h->yslot, H};
+    g.num_segs = 1;
+    if (h->has_shared) {
+        g.Wa1 = h->m_shd128;
+        g.X1 = h->m_hs_n[v];
+        g.seg[1] = moe::SabSegment{1, 1, sh_base, T, nullptr, nullptr, (H + 127) / 128, S / 64, H, h->ys, H};
+        g.num_segs = 2;
+    }
+    return launched(h, moe::launch_gemm_sab(g, n_tok, s), "down_gemm_swapped", n, s);
+}
+
 moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStream_t s) {
     int n = 0;
-    const int path = h->path_opt != kPathAuto ? h->path_opt
-                                              : (T <= kDecodeMaxTokens ? kPathDecode : kPathGrouped);
+    const long long slots = (long long)T * h->k;
+    int path = h->path_opt;
+    if (path == kPathAuto)
+        path = T <= kDecodeMaxTokens ? kPathDecode
+                                     : (slots <= (long long)kSwapMaxTokensPerExpert * h->E ? kPathSwapped : kPathGrouped);
+    const int n_tok = slots <= 24ll * h->E ? 32 : 64;  // token tile of the swapped GEMMs
     h->ev_recorded = 0;
     mark(h, 0, s);
-    moe_status st = run_front(h, X, T, s, &n);
-    if (st == MOE_OK) st = path == kPathDecode ? run_decode(h, X, T, s, &n) : run_grouped(h, X, T, s, &n);
+    moe_status st = run_front(h, X, T, s, &n, path == kPathSwapped ? n_tok : moe::kGemmBM);
+    if (st == MOE_OK) {
+        if (path == kPathDecode)
+            st = run_decode(h, X, T, s, &n);
+        else if (path == kPathSwapped)
+            st = run_swapped(h, X, T, s, &n, n_tok);
+        else
+            st = run_grouped(h, X, T, s, &n);
+    }
     if (st == MOE_OK) {
         moe::CombineArgs ca{h->yslot, h->has_shared ? h->ys : nullptr, h->topk_w, h->slot_of,
                             T, h->k, h->H, Y, h->x_f32 ? 1 : 0};
@@ -569,7 +657,7 @@ moe_status moe_route(moe_handle *h, const void *X, int T, int32_t *topk_idx, flo
     if (!aligned16(X)) return fail(MOE_ERR_INVALID_ARG, "X is not 16-byte aligned");
     if (!h->x_f32) {
         int n = 0;
-        moe_status st = run_router_tc(h, X, T, topk_idx, topk_w, nullptr, reinterpret_cast<cudaStream_t>(stream), &n);
+        moe_status st = run_router_tc(h, X, T, topk_idx, topk_w, nullptr, reinterpret_cast<cudaStream_t>(stream), &n, 0);
         h->last_launches = n;
         return st;
     }
@@ -659,7 +747,7 @@ moe_status moe_set_option(moe_handle *h, int option, long long value) {
     if (h == nullptr) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
     switch (option) {
     case MOE_OPT_PATH:
-        if (value < kPathAuto || value > kPathGrouped) return fail(MOE_ERR_INVALID_ARG, "path %lld", value);
+        if (value < kPathAuto || value > kPathSwapped) return fail(MOE_ERR_INVALID_ARG, "path %lld", value);
         h->path_opt = (int)value;
         return MOE_OK;
     case MOE_OPT_WAIT_LIMIT_NS:

@@ -302,18 +302,12 @@ __device__ void dispatch_scan_block(int32_t *blk_hist, int nb, int E, int hb, in
 
 // Routing rule from the fp32 logits of the tensor-core router (partial sums of
 // its split-K CTAs, added in split order): LPT lanes per token, 8 experts per
-// lane, TT = min(128, 1024 / LPT) tokens per CTA, expert histogram per CTA.
-// The last CTA to finish runs the dispatch scan (its ticket comes from an
-// atomic counter; no CTA waits for another).
-template <int LPT>
-__host__ __device__ constexpr int topk_tt() { return (1024 / LPT) < 128 ? (1024 / LPT) : 128; }
-
+// lane, blockDim.x / LPT tokens per CTA, expert histogram per CTA.
 template <int LPT>
 __global__ void __launch_bounds__(1024) topk_kernel(const TopkArgs a) {
-    constexpr int TT = topk_tt<LPT>();
     __shared__ int hist[256];
-    __shared__ int is_last;
     const int E = a.E, sub = threadIdx.x & (LPT - 1), grp = threadIdx.x / LPT;
+    const int TT = blockDim.x / LPT;
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
     pdl_wait();
     pdl_trigger();
@@ -340,18 +334,6 @@ __global__ void __launch_bounds__(1024) topk_kernel(const TopkArgs a) {
         __syncthreads();
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             a.blk_hist[(size_t)blockIdx.x * a.hb + (size_t)e * a.he] = hist[e];
-        if (a.offs != nullptr) {
-            __threadfence();
-            __syncthreads();
-            if (threadIdx.x == 0) is_last = atomicAdd(a.counter, 1) == (int)gridDim.x - 1;
-            __syncthreads();
-            if (is_last) {
-                __threadfence();
-                dispatch_scan_block(a.blk_hist, gridDim.x, E, a.hb, a.he, a.tile_m, a.offs, a.tile_offs,
-                                    a.active);
-                if (threadIdx.x == 0) *a.counter = 0;
-            }
-        }
     }
 }
 
@@ -370,25 +352,70 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs a) {
 constexpr int kScatterThreads = 256;
 constexpr int kMaxTT = 128;
 
-// grid (token blocks, gather_split).  Every CTA of a token block builds, per
-// expert, the bitmask of the block's tokens that chose it; the rank of slot
-// (t, j) among its expert's rows in this block is the number of earlier tokens
-// in that mask (a token's k experts are distinct; a repeat is reported and
-// dropped).  CTA y = 0 writes the index arrays; the CTAs of a block share the
-// copy of the X rows.
+// grid (token blocks, gather_split).  Every CTA first derives, from the block
+// histograms, the expert offsets (offs[e] = rows of experts < e) and its own
+// block's first row per expert (offs[e] + rows of expert e in earlier blocks):
+// independent loads and shared-memory sums, no serial pass; CTA (0, 0) also
+// writes offs, tile_offs (ceil(count / tile_m) prefix) and the active-expert
+// list.  Then, per expert, the bitmask of the block's tokens that chose it
+// gives the rank of slot (t, j) among its expert's rows in the block (a
+// token's k experts are distinct; a repeat is reported and dropped).  CTA
+// y = 0 writes the index arrays; the CTAs of a block share the copy of X rows.
 __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterArgs a) {
     __shared__ uint32_t masks[256][kMaxTT / 32];
     __shared__ int e_s[kMaxTT * 16];
     __shared__ int slot_s[kMaxTT * 16];
+    __shared__ int cnt[256], pre[256], base[256];
     const int TT = a.tokens_per_block, k = a.k, E = a.E, H = a.H;
     const int hb = (a.hb | a.he) ? a.hb : E, he = (a.hb | a.he) ? a.he : 1;
     const int words = (TT + 31) / 32;
     const int tok0 = blockIdx.x * TT;
+    const int nbk = gridDim.x, b = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int e = threadIdx.x; e < E; e += kScatterThreads) cnt[e] = pre[e] = 0;
+    for (int i = threadIdx.x; i < E * words; i += kScatterThreads) masks[i / words][i % words] = 0;
     pdl_wait();
     pdl_trigger();
+    __syncthreads();
+    for (int i = threadIdx.x; i < E * nbk; i += kScatterThreads) {
+        const int e = i / nbk, bb = i - e * nbk;
+        const int v = __ldg(a.blk_hist + (size_t)bb * hb + (size_t)e * he);
+        if (v) {
+            atomicAdd(&cnt[e], v);
+            if (bb < b) atomicAdd(&pre[e], v);
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int tile_m = a.tile_m > 0 ? a.tile_m : kGemmBM;
+        const bool writer = blockIdx.x == 0 && blockIdx.y == 0;
+        int run = 0, trun = 0, nact = 0;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            const int c = e < E ? cnt[e] : 0;
+            const int tl = (c + tile_m - 1) / tile_m;
+            const int inc = warp_incl_scan(c, lane), tinc = warp_incl_scan(tl, lane);
+            const unsigned act = __ballot_sync(0xffffffffu, c > 0);
+            if (e < E) {
+                base[e] = run + inc - c + pre[e];
+                if (writer) {
+                    a.offs[e] = run + inc - c;
+                    a.tile_offs[e] = trun + tinc - tl;
+                    if (c > 0) a.active[nact + __popc(act & ((1u << lane) - 1u))] = e;
+                }
+            }
+            run += __shfl_sync(0xffffffffu, inc, 31);
+            trun += __shfl_sync(0xffffffffu, tinc, 31);
+            nact += __popc(act);
+        }
+        if (writer && lane == 0) {
+            a.offs[E] = run;
+            a.tile_offs[E] = trun;
+            a.active[E] = nact;
+        }
+    }
     const int n = max(0, min(TT, a.T - tok0)) * k;
     const size_t ent0 = (size_t)tok0 * k;
-    for (int i = threadIdx.x; i < E * words; i += kScatterThreads) masks[i / words][i % words] = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < n; i += kScatterThreads) {
         int e = a.topk_idx[ent0 + i];
@@ -413,14 +440,13 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
             const int tl = i / k;
             int rank = __popc(masks[e][tl >> 5] & ((1u << (tl & 31)) - 1u));
             for (int w = 0; w < (tl >> 5); ++w) rank += __popc(masks[e][w]);
-            slot = a.blk_base[(size_t)blockIdx.x * hb + (size_t)e * he] + rank;
+            slot = base[e] + rank;
             if (blockIdx.y == 0) a.sorted_tok[slot] = tok0 + tl;
         }
         if (blockIdx.y == 0) a.slot_of[ent0 + i] = slot;
         slot_s[i] = slot;
     }
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nw = kScatterThreads / 32;
     for (int i = blockIdx.y * nw + warp; i < n; i += gridDim.y * nw) {
         const int slot = slot_s[i];
@@ -506,18 +532,18 @@ static int topk_lpt(int E) {
     return l;
 }
 
-int topk_tokens_per_block(int E) {
-    switch (topk_lpt(E)) {
-    case 2: return topk_tt<2>();
-    case 4: return topk_tt<4>();
-    case 8: return topk_tt<8>();
-    case 16: return topk_tt<16>();
-    default: return topk_tt<32>();
-    }
+int topk_tokens_per_block(int E, int T, int num_sms) {
+    // spread the tokens over the SMs: tokens per CTA = next power of two of
+    // T / SMs, within [8 (and a full warp), min(128, 1024 / LPT)]
+    const int lpt = topk_lpt(E);
+    int want = (T + num_sms - 1) / num_sms, tt = 1;
+    while (tt < want) tt <<= 1;
+    const int lo = 32 / lpt > 8 ? 32 / lpt : 8, hi = 1024 / lpt < 128 ? 1024 / lpt : 128;
+    return tt < lo ? lo : (tt > hi ? hi : tt);
 }
 
-cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s) {
-    const int lpt = topk_lpt(a.E), tt = topk_tokens_per_block(a.E);
+cudaError_t launch_topk(const TopkArgs &a, int tokens_per_block, cudaStream_t s) {
+    const int lpt = topk_lpt(a.E), tt = tokens_per_block;
     const dim3 grid((a.T + tt - 1) / tt), block(tt * lpt);
     switch (lpt) {
     case 2: return launch_pdl(topk_kernel<2>, grid, block, 0, s, a);

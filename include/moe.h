@@ -147,7 +147,9 @@ const char *moe_last_error(void);
  * Options, statistics and inspection (tests and measurement).
  */
 typedef enum {
-    MOE_OPT_PATH = 0,          /* 0 auto, 1 weight-streaming decode kernels, 2 tcgen05 grouped GEMMs */
+    MOE_OPT_PATH = 0,          /* 0 auto, 1 weight-streaming decode kernels, 2 tcgen05 grouped GEMMs
+                                  (tokens as M), 3 tcgen05 swapped-operand GEMMs (weights as M, for
+                                  few tokens per expert) */
     MOE_OPT_WAIT_LIMIT_NS = 1, /* bound of every device-side wait in ns (default 500000000);
                                   0 makes the first wait that finds its data not ready give up,
                                   which exercises the timeout path */
@@ -159,7 +161,7 @@ typedef enum {
 moe_status moe_set_option(moe_handle *h, int option, long long value);
 
 typedef struct {
-    int path;              /* path of the last forward: 1 decode, 2 grouped */
+    int path;              /* path of the last forward: 1 decode, 2 grouped, 3 swapped */
     int kernel_launches;   /* kernels the last forward (or route) launched */
     long long workspace_bytes;
 } moe_stats;
@@ -174,7 +176,7 @@ moe_status moe_get_stats(const moe_handle *h, moe_stats *out);
 moe_status moe_get_stage_times(moe_handle *h, float *ms, int max, int *n);
 
 /* Name of kernel i (0-based, launch order) of the last call, e.g. "router_logits",
- * "router_topk_scan", "dispatch_scatter", "gate_up_gemm", "down_gemm", "combine";
+ * "router_topk", "dispatch_scatter", "gate_up_gemm", "down_gemm", "combine";
  * NULL when i is out of range.  The string is static. */
 const char *moe_get_stage_name(const moe_handle *h, int i);
 

@@ -18,7 +18,7 @@ from tests import parity as P
 
 pytestmark = pytest.mark.gpu
 
-PATHS = {"decode": capi.PATH_DECODE, "grouped": capi.PATH_GROUPED}
+PATHS = {"decode": capi.PATH_DECODE, "grouped": capi.PATH_GROUPED, "swapped": capi.PATH_SWAPPED}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -210,4 +210,4 @@ def test_full_m3_packed_clamp_swiglu():
 @pytest.mark.parametrize("T", wl.ZIPF_TOKENS)
 def test_full_zipf_sweep(T):
     _, blk = _full(wl.zipf_sweep(T), n_sample=12)
-    assert blk.stats().path in (capi.PATH_DECODE, capi.PATH_GROUPED)
+    assert blk.stats().path in (capi.PATH_DECODE, capi.PATH_GROUPED, capi.PATH_SWAPPED)
