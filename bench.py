@@ -55,6 +55,8 @@ def work_model(shape, U: int):
         "gate_up": dict(flops=4 * T * H * (k * I + S), bytes=(U * 2 * H * I + 2 * H * S) * 2 + 2 * T * H),
         "down": dict(flops=2 * T * H * (k * I + S), bytes=(U * H * I + H * S) * 2 + 2 * T * H),
     }
+    kernels["experts"] = dict(flops=kernels["gate_up"]["flops"] + kernels["down"]["flops"],
+                              bytes=(U * 3 * H * I + 3 * H * S) * 2 + 2 * 2 * T * H)
     return F, B, kernels
 
 
@@ -129,6 +131,8 @@ def run_ours(args, shape):
     if args.path:
         blk.set_option(capi.MOE_OPT_PATH, {"decode": capi.PATH_DECODE, "grouped": capi.PATH_GROUPED,
                                            "swapped": capi.PATH_SWAPPED}[args.path])
+    if args.two_launch:
+        blk.set_option(capi.MOE_OPT_FUSE_EXPERTS, 0)
     X = inputs["X"]
     Y = torch.empty_like(X)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -218,12 +222,13 @@ def run_ours(args, shape):
     dom = max(stage_avg, key=stage_avg.get)
     roof = None
     key = {"gate_up_gemm": "gate_up", "decode_gate_up": "gate_up", "gate_up_gemm_swapped": "gate_up",
-           "down_gemm": "down", "decode_down": "down", "down_gemm_swapped": "down"}.get(dom)
+           "down_gemm": "down", "decode_down": "down", "down_gemm_swapped": "down",
+           "experts_gemm": "experts"}.get(dom)
     if key is None:  # report the heavier expert GEMM when a small kernel leads
         gemms = [n for n in stage_avg if "gemm" in n or n.startswith("decode_")]
         if gemms:
             dom = max(gemms, key=stage_avg.get)
-            key = "gate_up" if "gate_up" in dom else "down"
+            key = "experts" if dom == "experts_gemm" else ("gate_up" if "gate_up" in dom else "down")
 
     if key is not None:
         kw = kern[key]
@@ -278,7 +283,8 @@ def traffic_of(stage: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current source of that kernel; else None."""
     import hashlib
-    src = {"gate_up_gemm": "gemm_tc.cu", "down_gemm": "gemm_tc.cu", "decode_gate_up": "stream.cu",
+    src = {"gate_up_gemm": "gemm_tc.cu", "down_gemm": "gemm_tc.cu", "experts_gemm": "gemm_tc.cu",
+           "decode_gate_up": "stream.cu",
            "decode_down": "stream.cu", "gate_up_gemm_swapped": "gemm_sab.cu",
            "down_gemm_swapped": "gemm_sab.cu"}.get(stage)
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
@@ -372,6 +378,7 @@ def main():
     ap.add_argument("--workload", default="nano_decode")
     ap.add_argument("--path", choices=["decode", "grouped", "swapped"], default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--two-launch", action="store_true", help="gate/up and down GEMMs as two launches")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--preroll", type=float, default=1.0, help="seconds of untimed steps before timing")
     ap.add_argument("--no-flush", action="store_true",

@@ -3,11 +3,17 @@
 //   gate/up (glu = 1):  H_out[r, i] = act( A[r,:] . Wg[g][i,:],  A[r,:] . Wu[g][i,:] )
 //   down    (glu = 0):  Y_out[r, j] = A[r,:] . Wd[g][j,:]
 //
-// One launch covers up to two segments: the routed experts (rows grouped by
+// One launch covers up to four segments: the routed experts (rows grouped by
 // expert through the dispatch offsets, weight slice = expert id) and the
-// shared expert (all T token rows, one weight slice).  Weights are the
-// pre-stacked [groups, out, in] tensors (Arcee AFMoE issue, "Checkpoint weight
-// layout"; the packed shared expert of the MiniMax-M3 issue is slice E).
+// shared expert (all T token rows, one weight slice), for the gate/up
+// projection, the down projection, or both.  Weights are the pre-stacked
+// [groups, out, in] tensors (Arcee AFMoE issue, "Checkpoint weight layout";
+// the packed shared expert of the MiniMax-M3 issue is slice E).  When both
+// projections share a launch, a down tile first waits until every gate/up
+// tile of its 128 rows has been stored (a per-m-tile counter), so the down
+// tiles of early experts overlap the gate/up tail and the second launch's ramp
+// disappears.  Gate/up tiles never wait and every CTA walks its tiles in
+// increasing order with all CTAs resident (one per SM), so the waits end.
 //
 // Persistent kernel, one CTA per SM, 6 warps:
 //   warp 0     TMA producer: A tile 128 x 64 and B tile 256 x 64 (gate/up: 128
@@ -41,24 +47,21 @@ constexpr uint64_t kDrainNs = 1000000000ull;    // bound of the drain after an a
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
 
 struct Tile {
-    int seg, group, mt, nt, row0, m_valid;
+    int seg, group, mt, nt, row0, m_valid, ready;  // ready: m-tile index for signal / wait
 };
 
-// offs / toffs: shared-memory copies of segment 0's dispatch offsets (only
-// segment 0 may be grouped)
+// offs / toffs: shared-memory copies of the grouped segments' dispatch offsets
 __device__ __forceinline__ int seg_tiles(const GemmSegment &s, const int *toffs) {
     if (s.dense) return ((s.m_dense + kGemmBM - 1) / kGemmBM) * s.n_tiles;
     return toffs[s.num_groups] * s.n_tiles;
 }
 
-__device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, int tiles0, const int *offs,
+__device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, const int *seg_end, const int *offs,
                                             const int *toffs) {
     Tile t;
     t.seg = 0;
-    if (tile >= tiles0) {
-        t.seg = 1;
-        tile -= tiles0;
-    }
+    while (t.seg + 1 < p.num_segs && tile >= seg_end[t.seg]) ++t.seg;
+    if (t.seg > 0) tile -= seg_end[t.seg - 1];
     const GemmSegment &s = p.seg[t.seg];
     if (s.dense) {
         const int mtiles = (s.m_dense + kGemmBM - 1) / kGemmBM;
@@ -67,6 +70,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, int til
         t.mt = tile % mtiles;
         t.row0 = t.mt * kGemmBM;
         t.m_valid = min(kGemmBM, s.m_dense - t.row0);
+        t.ready = s.ready_base + t.mt;
     } else {
         // largest group whose first tile is <= tile (empty groups own no tiles)
         int lo = 0, hi = s.num_groups - 1;
@@ -85,6 +89,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, int til
         const int start = offs[lo];
         t.row0 = start + t.mt * kGemmBM;
         t.m_valid = min(kGemmBM, offs[lo + 1] - t.row0);
+        t.ready = s.ready_base + toffs[lo] + t.mt;
     }
     return t;
 }
@@ -94,7 +99,42 @@ __device__ __forceinline__ void raise_abort(int *err, volatile int *abort_flag) 
     *abort_flag = 1;
 }
 
-template <bool GLU>
+__device__ __forceinline__ int ld_acquire(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait (bounded, like mbar_wait) until *p >= target.
+__device__ __forceinline__ bool wait_counter(const int *p, int target, uint64_t limit_ns, volatile int *abort) {
+    if (ld_acquire(p) >= target) return true;
+    if (limit_ns == 0) return false;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        __nanosleep(64);
+        if (ld_acquire(p) >= target) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Named barrier 1 of the four epilogue warps; and the AND of v over them.
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool epi_all(bool v) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"((uint32_t)v)
+        : "memory");
+    return out != 0;
+}
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -126,16 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         fence_mbar_init();
         *abort_flag = 0;
     }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&p.A0);
-        tma_prefetch_desc(&p.B0);
-        if (GLU) tma_prefetch_desc(&p.B1);
-        if (p.num_segs > 1) {
-            tma_prefetch_desc(&p.A1);
-            tma_prefetch_desc(&p.B2);
-            if (GLU) tma_prefetch_desc(&p.B3);
-        }
-    }
+    if (warp == 0 && lane == 0)
+        for (int m = 0; m < kGemmMaxMaps; ++m) tma_prefetch_desc(&p.maps[m]);
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
@@ -149,15 +181,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     pdl_trigger();
     // every role decodes every tile: keep the dispatch offsets on chip
     __shared__ int s_offs[257], s_toffs[257];
-    if (!p.seg[0].dense)
-        for (int i = threadIdx.x; i <= p.seg[0].num_groups; i += blockDim.x) {
-            s_offs[i] = p.seg[0].offs[i];
-            s_toffs[i] = p.seg[0].tile_offs[i];
+    __shared__ int s_seg_end[kGemmMaxSegments];
+    int grouped = -1;
+    for (int s = 0; s < p.num_segs; ++s)
+        if (!p.seg[s].dense) grouped = s;
+    if (grouped >= 0)
+        for (int i = threadIdx.x; i <= p.seg[grouped].num_groups; i += blockDim.x) {
+            s_offs[i] = p.seg[grouped].offs[i];
+            s_toffs[i] = p.seg[grouped].tile_offs[i];
         }
     __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int s = 0; s < p.num_segs; ++s) {
+            run += seg_tiles(p.seg[s], s_toffs);
+            s_seg_end[s] = run;
+        }
+    }
+    __syncthreads();
     const uint32_t tmem_base = *tmem_slot;
-    const int tiles0 = seg_tiles(p.seg[0], s_toffs);
-    const int total = tiles0 + (p.num_segs > 1 ? seg_tiles(p.seg[1], s_toffs) : 0);
+    const int total = s_seg_end[p.num_segs - 1];
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -165,11 +208,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t L = 0;  // loads issued so far; stage = L % kStages
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                const Tile t = decode_tile(p, tile, tiles0, s_offs, s_toffs);
+                const Tile t = decode_tile(p, tile, s_seg_end, s_offs, s_toffs);
                 const GemmSegment &sg = p.seg[t.seg];
-                const CUtensorMap *mA = t.seg ? &p.A1 : &p.A0;
-                const CUtensorMap *mB = t.seg ? &p.B2 : &p.B0;
-                const CUtensorMap *mB2 = t.seg ? &p.B3 : &p.B1;
+                if (sg.wait != nullptr) {  // A rows written earlier in this launch
+                    if (!wait_counter(sg.wait + t.ready, sg.wait_count, p.wait_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async();  // order the A rows' generic-proxy stores before our TMA reads
+                }
+                const CUtensorMap *mA = &p.maps[sg.map_a];
+                const CUtensorMap *mB = &p.maps[sg.map_b0];
+                const CUtensorMap *mB2 = &p.maps[sg.map_b1];
                 const int g = sg.group_base + t.group;
                 for (int kb = 0; kb < sg.k_blocks; ++kb) {
                     const int s = L % kStages;
@@ -180,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     }
                     mbar_arrive_expect_tx(full_bar(s), kStageBytes);
                     tma_load_2d(sA + s * kABytes, mA, full_bar(s), kb * kGemmBK, t.row0);
-                    if (GLU) {
+                    if (sg.glu) {
                         tma_load_3d(sB + s * kBBytes, mB, full_bar(s), kb * kGemmBK, t.nt * 128, g);
                         tma_load_3d(sB + s * kBBytes + kBBytes / 2, mB2, full_bar(s), kb * kGemmBK,
                                     t.nt * 128, g);
@@ -206,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t L = 0, n_acc = 0;
             bool ok = true, issued = false;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                const Tile t = decode_tile(p, tile, tiles0, s_offs, s_toffs);
+                const Tile t = decode_tile(p, tile, s_seg_end, s_offs, s_toffs);
                 const GemmSegment &sg = p.seg[t.seg];
                 const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
                 if (!mbar_wait(tempty_bar(a), aph ^ 1u, p.wait_ns, abort_flag)) {
@@ -250,13 +300,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const int r = q * 32 + lane;
         uint32_t n_acc = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            const Tile t = decode_tile(p, tile, tiles0, s_offs, s_toffs);
+            const Tile t = decode_tile(p, tile, s_seg_end, s_offs, s_toffs);
             const GemmSegment &sg = p.seg[t.seg];
             const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
-            // every lane waits; the answer is made warp-uniform because the
-            // tcgen05.ld below is .sync.aligned
+            // all four epilogue warps agree to go on or stop (they share barrier 1);
+            // the tcgen05.ld below is .sync.aligned
             const bool ready = __all_sync(0xffffffffu, mbar_wait(tfull_bar(a), aph, p.wait_ns, abort_flag));
-            if (!ready) {
+            if (!epi_all(ready)) {
                 if (lane == 0) raise_abort(p.err, abort_flag);
                 break;
             }
@@ -264,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + a * kGemmBN;
             const bool row_ok = r < t.m_valid;
             bf16 *orow = sg.out + (size_t)(t.row0 + (row_ok ? r : 0)) * sg.ldo;
-            if (GLU) {
+            if (sg.glu) {
 #pragma unroll 1
                 for (int c0 = 0; c0 < 128; c0 += 32) {
                     uint32_t g[32], u[32];
@@ -308,6 +358,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             }
             tc_fence_before();
             mbar_arrive(tempty_bar(a));
+            if (sg.signal != nullptr) {
+                // publish the stored rows: proxy fence for the consumer's TMA reads,
+                // device-scope fence, all four warps done, then one release increment
+                fence_proxy_async();
+                __threadfence();
+                epi_bar();
+                if (q == 0 && lane == 0) atomicAdd(sg.signal + t.ready, 1);
+            }
             ++n_acc;
         }
     }
@@ -375,11 +433,9 @@ CUresult encode_map_b(CUtensorMap *m, const void *ptr, int groups, int rows, int
 cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
     static std::once_flag once;
     std::call_once(once, [] {
-        cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     });
-    if (a.glu) return launch_pdl(gemm_tc_kernel<true>, dim3(a.num_ctas), dim3(kThreads), kSmemBytes, s, a);
-    return launch_pdl(gemm_tc_kernel<false>, dim3(a.num_ctas), dim3(kThreads), kSmemBytes, s, a);
+    return launch_pdl(gemm_tc_kernel, dim3(a.num_ctas), dim3(kThreads), kSmemBytes, s, a);
 }
 
 }  // namespace moe

@@ -117,6 +117,10 @@ struct ScatterArgs {
     int hb, he;
     int32_t *offs, *tile_offs, *active;  // written by CTA (0, 0): as in ScanArgs
     int tile_m;                          // 0: kGemmBM
+    // CTA (0, 0) zeroes the fused expert GEMM's counters: ready[0, routed m-tiles)
+    // and ready[ready_shared_base, + ready_shared_count)
+    int *ready;
+    int ready_shared_base, ready_shared_count;
     int T, k, E, H;
     int tokens_per_block;     // <= 128: the router's blocking
     int gather_split;         // CTAs per token block sharing the row gather
@@ -147,26 +151,35 @@ constexpr int kGemmBM = 128;   // rows (tokens) per tile: the MMA's M
 constexpr int kGemmBK = 64;    // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int kGemmBN = 256;   // MMA N; gate/up tiles hold 128 gate + 128 up columns
 
+constexpr int kGemmMaxSegments = 4;
+constexpr int kGemmMaxMaps = 10;
 struct GemmSegment {
     int dense;             // 1: one group of m_dense rows from row 0; 0: groups by offs
     int num_groups;
     int group_base;        // weight-map coordinate of group 0
     int m_dense;
-    const int32_t *offs;   // [num_groups + 1] (grouped)
+    const int32_t *offs;   // [num_groups + 1] (grouped; every grouped segment of a launch shares them)
     const int32_t *tile_offs;
     int n_tiles;           // output tiles per group along N
     int k_blocks;          // K / 64
     int n_out;             // valid output columns
     __nv_bfloat16 *out;    // [rows, ldo]
     int ldo;
+    int glu;               // 1: gate/up pair (maps b0, b1) with the activation; 0: one projection (map b0)
+    int map_a, map_b0, map_b1;  // indices into GemmArgs::maps
+    // Dependencies inside one launch, per m-tile index (tile_offs[g] + mt, or mt when dense, plus
+    // ready_base): `signal` gets +1 after a tile's outputs are stored; before loading a tile's A
+    // rows the producer waits until wait[index] >= wait_count.
+    int *signal;
+    const int *wait;
+    int wait_count;
+    int ready_base;
 };
 
 struct GemmArgs {
-    // maps: segment 0 reads A0 and B0 (+B1 for gate/up); segment 1 reads A1 and B2 (+B3)
-    CUtensorMap A0, A1, B0, B1, B2, B3;
-    GemmSegment seg[2];
-    int num_segs;
-    int glu;               // 1: gate/up with activation epilogue; 0: plain (down)
+    CUtensorMap maps[kGemmMaxMaps];
+    GemmSegment seg[kGemmMaxSegments];
+    int num_segs;          // tiles of segment s precede those of segment s + 1
     int act;
     float alpha, limit, beta;
     int *err;

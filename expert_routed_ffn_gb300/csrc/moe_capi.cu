@@ -80,6 +80,9 @@ struct moe_handle {
     int *err = nullptr;
     bf16 *wr_parts = nullptr;  // router weights as exact bf16 splits [3, E, H]
     float *logits = nullptr;   // split-K partial router logits [splits, T, Np]
+    int *ready = nullptr;      // per-m-tile gate/up completion counters of the fused expert GEMM
+    int ready_shared_base = 0; // first counter of the shared expert's m-tiles
+    bool fuse_experts = true;  // gate/up and down in one persistent launch
     int hist_stride = 0;       // block histograms are [E, hist_stride]
     int *counter = nullptr;    // CTA ticket of the top-k kernel's fused scan
     int *wr_flags = nullptr;
@@ -192,6 +195,9 @@ void carve(moe_handle *h, void *base) {
     const size_t lrows = MT > (size_t)h->num_sms * 128 ? MT : (size_t)h->num_sms * 128;
     h->logits = c.take<float>(base, lrows * ((E + 31) / 32 * 32));
     h->counter = c.take<int>(base, 64);
+    // routed m-tiles number at most T*k/128 + E; the shared expert's follow
+    h->ready_shared_base = (int)(MT * k / 128 + E + 1);
+    h->ready = c.take<int>(base, (size_t)h->ready_shared_base + (MT + 127) / 128 + 1);
     h->wr_flags = c.take<int>(base, 64);
     h->ws_bytes = round_up(c.off, 256);
 }
@@ -368,6 +374,9 @@ moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n
     xa.tile_offs = h->tile_offs;
     xa.active = h->active;
     xa.tile_m = tile_m;
+    xa.ready = h->ready;
+    xa.ready_shared_base = h->ready_shared_base;
+    xa.ready_shared_count = (T + 127) / 128;
     xa.T = T;
     xa.k = h->k;
     xa.E = h->E;
@@ -391,8 +400,12 @@ moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n
     return MOE_OK;
 }
 
+// tcgen05 grouped GEMMs (tokens as M): routed and shared segments of the
+// gate/up and down projections, in one persistent launch (the down tiles wait
+// per m-tile for their gate/up rows) or in two launches.
 moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int *n) {
     const int H = h->H, I = h->I, S = h->S, E = h->E;
+    enum { kXs = 0, kX = 1, kHb = 2, kHs = 3, kG = 4, kU = 5, kSG = 6, kSU = 7, kD = 8, kSD = 9 };
     moe::GemmArgs g{};
     g.err = h->err;
     g.wait_ns = h->wait_ns;
@@ -401,49 +414,61 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     g.limit = h->cfg.act_limit;
     g.beta = h->cfg.act_beta;
     g.num_ctas = h->num_sms;
-
-    // gate/up: routed rows of X_sorted against the stacked gate/up slices;
-    // shared expert over all T rows of X
-    g.glu = 1;
-    g.A0 = h->m_xsorted;
-    g.B0 = h->m_gate;
-    g.B1 = h->m_up;
-    g.seg[0] = moe::GemmSegment{0, E, 0, 0, h->offs, h->tile_offs, (I + 127) / 128, H / 64, I, h->hbuf, I};
-    g.num_segs = 1;
+    for (auto &m : g.maps) m = h->m_xsorted;  // unused slots hold a valid descriptor
+    g.maps[kXs] = h->m_xsorted;
+    g.maps[kHb] = h->m_hbuf;
+    g.maps[kG] = h->m_gate;
+    g.maps[kU] = h->m_up;
+    g.maps[kD] = h->m_down;
     if (h->has_shared) {
         if (h->x_f32) {
-            g.A1 = h->m_xbf16;
+            g.maps[kX] = h->m_xbf16;
         } else {
             moe_status st = x_map(h, X, T);
             if (st != MOE_OK) return st;
-            g.A1 = h->m_x;
+            g.maps[kX] = h->m_x;
         }
-        g.B2 = h->m_shg;
-        g.B3 = h->m_shu;
-        g.seg[1] = moe::GemmSegment{1, 1, h->cfg.shared_packed ? E : 0, T, nullptr, nullptr,
-                                    (S + 127) / 128, H / 64, S, h->hs, S};
+        g.maps[kHs] = h->m_hs;
+        g.maps[kSG] = h->m_shg;
+        g.maps[kSU] = h->m_shu;
+        g.maps[kSD] = h->m_shd;
+    }
+    const int sh_base = h->cfg.shared_packed ? E : 0;
+    const int nt_gu = (I + 127) / 128, nt_sgu = (S + 127) / 128, nt_d = (H + moe::kGemmBN - 1) / moe::kGemmBN;
+    const bool fused = h->fuse_experts;
+    int *sig = fused ? h->ready : nullptr;
+    const moe::GemmSegment gu{0, E, 0, 0, h->offs, h->tile_offs, nt_gu, H / 64, I, h->hbuf, I,
+                              1, kXs, kG, kU, sig, nullptr, 0, 0};
+    const moe::GemmSegment sgu{1, 1, sh_base, T, nullptr, nullptr, nt_sgu, H / 64, S, h->hs, S,
+                               1, kX, kSG, kSU, sig, nullptr, 0, h->ready_shared_base};
+    const moe::GemmSegment dn{0, E, 0, 0, h->offs, h->tile_offs, nt_d, I / 64, H, h->yslot, H,
+                              0, kHb, kD, kD, nullptr, fused ? h->ready : nullptr, nt_gu, 0};
+    const moe::GemmSegment sdn{1, 1, sh_base, T, nullptr, nullptr, nt_d, S / 64, H, h->ys, H,
+                               0, kHs, kSD, kSD, nullptr, fused ? h->ready : nullptr, nt_sgu, h->ready_shared_base};
+    if (fused) {
+        int ns = 0;
+        g.seg[ns++] = gu;
+        if (h->has_shared) g.seg[ns++] = sgu;
+        g.seg[ns++] = dn;
+        if (h->has_shared) g.seg[ns++] = sdn;
+        g.num_segs = ns;
+        return launched(h, moe::launch_gemm_tc(g, s), "experts_gemm", n, s);
+    }
+    g.seg[0] = gu;
+    g.num_segs = 1;
+    if (h->has_shared) {
+        g.seg[1] = sgu;
         g.num_segs = 2;
     }
     moe_status st = launched(h, moe::launch_gemm_tc(g, s), "gate_up_gemm", n, s);
     if (st != MOE_OK) return st;
-
-    // down: routed hidden rows against the stacked down slices; shared hidden rows
-    g.glu = 0;
-    g.A0 = h->m_hbuf;
-    g.B0 = h->m_down;
-    g.seg[0] = moe::GemmSegment{0, E, 0, 0, h->offs, h->tile_offs, (H + moe::kGemmBN - 1) / moe::kGemmBN,
-                                I / 64, H, h->yslot, H};
+    g.seg[0] = dn;
     g.num_segs = 1;
     if (h->has_shared) {
-        g.A1 = h->m_hs;
-        g.B2 = h->m_shd;
-        g.seg[1] = moe::GemmSegment{1, 1, h->cfg.shared_packed ? E : 0, T, nullptr, nullptr,
-                                    (H + moe::kGemmBN - 1) / moe::kGemmBN, S / 64, H, h->ys, H};
+        g.seg[1] = sdn;
         g.num_segs = 2;
     }
-    st = launched(h, moe::launch_gemm_tc(g, s), "down_gemm", n, s);
-    if (st != MOE_OK) return st;
-    return MOE_OK;
+    return launched(h, moe::launch_gemm_tc(g, s), "down_gemm", n, s);
 }
 
 moe_status run_decode(moe_handle *h, const void *X, int T, cudaStream_t s, int *n) {
@@ -753,6 +778,10 @@ moe_status moe_set_option(moe_handle *h, int option, long long value) {
     case MOE_OPT_WAIT_LIMIT_NS:
         if (value < 0) return fail(MOE_ERR_INVALID_ARG, "wait limit %lld", value);
         h->wait_ns = (unsigned long long)value;
+        return MOE_OK;
+    case MOE_OPT_FUSE_EXPERTS:
+        if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "fuse experts %lld", value);
+        h->fuse_experts = value != 0;
         return MOE_OK;
     case MOE_OPT_STAGE_EVENTS:
         if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "stage events %lld", value);

@@ -413,6 +413,10 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
             a.tile_offs[E] = trun;
             a.active[E] = nact;
         }
+        if (writer && a.ready != nullptr) {
+            for (int i = lane; i < trun; i += 32) a.ready[i] = 0;
+            for (int i = lane; i < a.ready_shared_count; i += 32) a.ready[a.ready_shared_base + i] = 0;
+        }
     }
     const int n = max(0, min(TT, a.T - tok0)) * k;
     const size_t ent0 = (size_t)tok0 * k;

@@ -153,8 +153,11 @@ typedef enum {
     MOE_OPT_WAIT_LIMIT_NS = 1, /* bound of every device-side wait in ns (default 500000000);
                                   0 makes the first wait that finds its data not ready give up,
                                   which exercises the timeout path */
-    MOE_OPT_STAGE_EVENTS = 2   /* 1: record a CUDA event on the stream before the first and after
+    MOE_OPT_STAGE_EVENTS = 2,  /* 1: record a CUDA event on the stream before the first and after
                                   every kernel of moe_forward, for moe_get_stage_times (default 0) */
+    MOE_OPT_FUSE_EXPERTS = 3   /* path 2: 1 (default) runs the gate/up and down GEMMs as one
+                                  persistent launch whose down tiles wait for their gate/up rows;
+                                  0 runs them as two launches */
 } moe_option;
 
 /* Set an option.  Errors: INVALID_ARG (unknown option or value). */
@@ -176,7 +179,8 @@ moe_status moe_get_stats(const moe_handle *h, moe_stats *out);
 moe_status moe_get_stage_times(moe_handle *h, float *ms, int max, int *n);
 
 /* Name of kernel i (0-based, launch order) of the last call, e.g. "router_logits",
- * "router_topk", "dispatch_scatter", "gate_up_gemm", "down_gemm", "combine";
+ * "router_topk", "dispatch_scatter", "experts_gemm" (or "gate_up_gemm", "down_gemm"),
+ * "combine";
  * NULL when i is out of range.  The string is static. */
 const char *moe_get_stage_name(const moe_handle *h, int i);
 

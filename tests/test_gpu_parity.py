@@ -157,6 +157,21 @@ def test_packed_shared_equals_separate_shared_on_gpu():
         assert torch.equal(Yp, Ys)
 
 
+def test_fused_expert_gemm_equals_two_launches():
+    """One persistent launch (down tiles wait for their gate/up rows) and two
+    launches compute the same tiles with the same arithmetic: bit-identical."""
+    for name in ("afmoe_ragged", "m3_small_packed", "nano_decode"):
+        shape = SMALL[name]
+        inputs, blk, Y1 = _run(shape, capi.PATH_GROUPED)
+        assert blk.stage_names()[3] == "experts_gemm"
+        blk.set_option(capi.MOE_OPT_FUSE_EXPERTS, 0)
+        Y2 = blk.forward(inputs["X"])
+        torch.cuda.synchronize()
+        assert blk.sync_status() == capi.MOE_OK
+        assert blk.stage_names()[3:5] == ["gate_up_gemm", "down_gemm"]
+        assert torch.equal(Y1, Y2)
+
+
 def test_token_permutation_equivariance_and_determinism():
     shape = SMALL["afmoe_ragged"]
     for path in PATHS.values():
