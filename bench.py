@@ -133,6 +133,8 @@ def run_ours(args, shape):
                                            "swapped": capi.PATH_SWAPPED}[args.path])
     if args.two_launch:
         blk.set_option(capi.MOE_OPT_FUSE_EXPERTS, 0)
+    if args.no_prefetch:
+        blk.set_option(capi.MOE_OPT_PREFETCH, 0)
     X = inputs["X"]
     Y = torch.empty_like(X)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -379,6 +381,7 @@ def main():
     ap.add_argument("--path", choices=["decode", "grouped", "swapped"], default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--two-launch", action="store_true", help="gate/up and down GEMMs as two launches")
+    ap.add_argument("--no-prefetch", action="store_true", help="no L2 prefetch of expert weights while routing")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--preroll", type=float, default=1.0, help="seconds of untimed steps before timing")
     ap.add_argument("--no-flush", action="store_true",

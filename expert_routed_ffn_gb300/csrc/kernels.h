@@ -91,6 +91,12 @@ struct RouterTcPlan {
 };
 RouterTcPlan plan_router_tc(int E, int parts);
 cudaError_t launch_router_tc(const RouterTcArgs &a, int smem, cudaStream_t s);
+// L2 prefetch of bytes[i] bytes from ptr[i] (16-byte multiples), a hint only.
+struct PrefetchArgs {
+    const void *ptr[2];
+    unsigned long long bytes[2];
+};
+cudaError_t launch_l2_prefetch(const PrefetchArgs &a, cudaStream_t s);
 // Split fp32 weights w into bf16 hi + mid + lo == w; *flags |= 1 when some w
 // needs mid, |= 2 when some w needs lo.
 cudaError_t launch_split_router(const float *wr, int E, int H, bf16 *parts, int *flags, cudaStream_t s);

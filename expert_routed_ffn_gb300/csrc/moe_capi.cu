@@ -53,6 +53,8 @@ constexpr int kSwapMaxTokensPerExpert = 0;
 // GB300, the tcgen05 grouped path is at least as fast down to T = 1, so the
 // auto path always takes it; the decode kernels stay selectable.
 constexpr int kDecodeMaxTokens = 0;
+// L2 budget for the weight prefetch issued while routing (L2 is 129 MB).
+constexpr unsigned long long kPrefetchBytes = 72ull << 20;
 
 }  // namespace
 
@@ -83,6 +85,9 @@ struct moe_handle {
     int *ready = nullptr;      // per-m-tile gate/up completion counters of the fused expert GEMM
     int ready_shared_base = 0; // first counter of the shared expert's m-tiles
     bool fuse_experts = true;  // gate/up and down in one persistent launch
+    bool prefetch_opt = true;  // L2 prefetch of expert weights during routing
+    cudaStream_t side = nullptr;               // the prefetch runs here, beside the routing kernels
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     int hist_stride = 0;       // block histograms are [E, hist_stride]
     int *counter = nullptr;    // CTA ticket of the top-k kernel's fused scan
     int *wr_flags = nullptr;
@@ -307,6 +312,7 @@ moe_status run_router_tc(moe_handle *h, const void *X, int T, int32_t *topk_idx,
         ra.kb_per_split = (nk + want - 1) / want;
     }
     const int splits = (h->H / 64 + ra.kb_per_split - 1) / ra.kb_per_split;
+
     st = launched(h, moe::launch_router_tc(ra, h->rplan.smem, s), "router_logits", n, s);
     if (st != MOE_OK) return st;
     moe::TopkArgs ta{};
@@ -571,6 +577,21 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
                                      : (slots <= (long long)kSwapMaxTokensPerExpert * h->E ? kPathSwapped : kPathGrouped);
     const int n_tok = slots <= 24ll * h->E ? 32 : 64;  // token tile of the swapped GEMMs
     h->ev_recorded = 0;
+    // Decode-sized batches touch nearly every expert (about two or more tokens
+    // per expert expected): while the routing kernels run, a side stream warms
+    // L2 with the first experts' gate and up slices, the fused GEMM's first tiles.
+    const bool prefetch = h->prefetch_opt && path == kPathGrouped && h->fuse_experts &&
+                          slots >= 2ll * h->E && h->side != nullptr;
+    if (prefetch) {
+        const unsigned long long slice = (unsigned long long)h->I * h->H * 2;
+        const unsigned long long each = kPrefetchBytes / 2 / slice * slice, all = slice * h->E;
+        moe::PrefetchArgs pa{{h->w.gate, h->w.up}, {each < all ? each : all, each < all ? each : all}};
+        cudaError_t e = cudaEventRecord(h->ev_fork, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
+        if (e == cudaSuccess) e = moe::launch_l2_prefetch(pa, h->side);
+        if (e == cudaSuccess) e = cudaEventRecord(h->ev_join, h->side);
+        if (e != cudaSuccess) return cuda_fail(e, "weight prefetch");
+    }
     mark(h, 0, s);
     moe_status st = run_front(h, X, T, s, &n, path == kPathSwapped ? n_tok : moe::kGemmBM);
     if (st == MOE_OK) {
@@ -585,6 +606,10 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
         moe::CombineArgs ca{h->yslot, h->has_shared ? h->ys : nullptr, h->topk_w, h->slot_of,
                             T, h->k, h->H, Y, h->x_f32 ? 1 : 0};
         st = launched(h, moe::launch_combine(ca, s), "combine", &n, s);
+    }
+    if (prefetch) {  // the caller's stream ends ordered after the side stream
+        cudaError_t e = cudaStreamWaitEvent(s, h->ev_join, 0);
+        if (e != cudaSuccess && st == MOE_OK) st = cuda_fail(e, "join of the prefetch stream");
     }
     h->last_path = path;
     h->last_launches = n;
@@ -661,6 +686,12 @@ moe_status moe_create(const moe_config *config, const moe_weights *weights, moe_
         return cuda_fail(e, "router weight split");
     }
     h->rplan = moe::plan_router_tc(h->E, (flags & 2) ? 3 : (flags & 1) ? 2 : 1);
+    if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        h->side = nullptr;  // no prefetch without its stream
+    }
     st = build_maps(h);
     if (st != MOE_OK) {
         cudaFree(h->ws);
@@ -682,7 +713,8 @@ moe_status moe_route(moe_handle *h, const void *X, int T, int32_t *topk_idx, flo
     if (!aligned16(X)) return fail(MOE_ERR_INVALID_ARG, "X is not 16-byte aligned");
     if (!h->x_f32) {
         int n = 0;
-        moe_status st = run_router_tc(h, X, T, topk_idx, topk_w, nullptr, reinterpret_cast<cudaStream_t>(stream), &n, 0);
+        moe_status st =
+            run_router_tc(h, X, T, topk_idx, topk_w, nullptr, reinterpret_cast<cudaStream_t>(stream), &n, 0);
         h->last_launches = n;
         return st;
     }
@@ -762,6 +794,9 @@ void moe_destroy(moe_handle *h) {
     cudaDeviceSynchronize();
     for (auto &e : h->ev)
         if (e != nullptr) cudaEventDestroy(e);
+    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+    if (h->ev_join) cudaEventDestroy(h->ev_join);
+    if (h->side) cudaStreamDestroy(h->side);
     cudaFree(h->ws);
     delete h;
 }
@@ -778,6 +813,10 @@ moe_status moe_set_option(moe_handle *h, int option, long long value) {
     case MOE_OPT_WAIT_LIMIT_NS:
         if (value < 0) return fail(MOE_ERR_INVALID_ARG, "wait limit %lld", value);
         h->wait_ns = (unsigned long long)value;
+        return MOE_OK;
+    case MOE_OPT_PREFETCH:
+        if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "prefetch %lld", value);
+        h->prefetch_opt = value != 0;
         return MOE_OK;
     case MOE_OPT_FUSE_EXPERTS:
         if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "fuse experts %lld", value);

@@ -160,6 +160,22 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
     }
 }
 
+// L2 prefetch of byte ranges (a hint; nothing is written).  Runs on a side
+// stream next to the routing kernels: a CTA cannot retire before its bulk
+// prefetches complete, so they must stay off the forward's dependency chain.
+__global__ void __launch_bounds__(32) l2_prefetch_kernel(const PrefetchArgs p) {
+    constexpr unsigned long long kChunk = 128 * 1024;
+    const unsigned long long stride = (unsigned long long)gridDim.x * 32 * kChunk;
+    for (int r = 0; r < 2; ++r) {
+        const unsigned long long n = p.bytes[r];
+        const char *base = static_cast<const char *>(p.ptr[r]);
+        for (unsigned long long c = ((unsigned long long)blockIdx.x * 32 + threadIdx.x) * kChunk; c < n; c += stride) {
+            const unsigned bytes = (unsigned)(n - c < kChunk ? n - c : kChunk);
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + c), "r"(bytes) : "memory");
+        }
+    }
+}
+
 // fp32 router weights -> three bf16 parts hi, mid, lo with hi + mid + lo == w
 // (each part rounds the remainder left by the previous ones); flags bit 0: some
 // weight needs mid, bit 1: some weight needs lo.
@@ -193,6 +209,11 @@ RouterTcPlan plan_router_tc(int E, int parts) {
     pl.smem = pl.stages * stage + 1024 + kMiscBytes;
     pl.parts = parts;
     return pl;
+}
+
+cudaError_t launch_l2_prefetch(const PrefetchArgs &a, cudaStream_t s) {
+    l2_prefetch_kernel<<<64, 32, 0, s>>>(a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_split_router(const float *wr, int E, int H, bf16 *parts, int *flags, cudaStream_t s) {

@@ -155,9 +155,14 @@ typedef enum {
                                   which exercises the timeout path */
     MOE_OPT_STAGE_EVENTS = 2,  /* 1: record a CUDA event on the stream before the first and after
                                   every kernel of moe_forward, for moe_get_stage_times (default 0) */
-    MOE_OPT_FUSE_EXPERTS = 3   /* path 2: 1 (default) runs the gate/up and down GEMMs as one
+    MOE_OPT_FUSE_EXPERTS = 3,  /* path 2: 1 (default) runs the gate/up and down GEMMs as one
                                   persistent launch whose down tiles wait for their gate/up rows;
                                   0 runs them as two launches */
+    MOE_OPT_PREFETCH = 4       /* 1 (default): when T*k >= 2E (nearly every expert is touched), an
+                                  internal side stream prefetches the first experts' gate/up weights
+                                  into L2 while the routing kernels run (forked from and joined back
+                                  into the caller's stream); 0: no prefetch.  A hint: results are
+                                  unchanged */
 } moe_option;
 
 /* Set an option.  Errors: INVALID_ARG (unknown option or value). */
