@@ -187,6 +187,34 @@ def run_ours(args, shape):
         for i, v in enumerate(blk.stage_times()[:len(names)]):
             stage_sum[i] += v
     blk.set_option(capi.MOE_OPT_STAGE_EVENTS, 0)
+    # device timeline of the same steps without events: per kernel, first CTA
+    # start, first CTA past the wait on its predecessor, last CTA end (us)
+    blk.set_option(capi.MOE_OPT_TRACE, 1)
+    tl_sum, tl_n, gw_sum = None, 0, None
+    for _ in range(args.steps):
+        step()
+        tr = blk.trace()
+        if tl_sum is None:
+            tl_sum = [[t[0]] + [0.0] * capi.TRACE_FIELDS for t in tr]
+        for acc, t in zip(tl_sum, tr):
+            for j in range(1, capi.TRACE_FIELDS + 1):
+                acc[j] += t[j]
+        tl_n += 1
+        if "experts_gemm" in names:
+            st = blk.inspect(capi.MOE_BUF_GEMM_STATS, 8, torch.int64).cpu().tolist()
+            gw_sum = st if gw_sum is None else [a + b for a, b in zip(gw_sum, st)]
+    blk.set_option(capi.MOE_OPT_TRACE, 0)
+    gemm_waits = None
+    if gw_sum is not None:
+        # per CTA and step, us: where the fused expert GEMM's roles spend their time
+        per = 1e-3 / (tl_n * torch.cuda.get_device_properties(dev).multi_processor_count)
+        keys = ["producer_wait_stage", "producer_wait_rows", "mma_wait_data", "mma_wait_accum",
+                "epilogue_wait_accum", "epilogue_work", "cta_busy"]
+        gemm_waits = {k: round(v * per, 2) for k, v in zip(keys, gw_sum[:7])}
+        gemm_waits["tiles"] = gw_sum[7] // tl_n
+    # per kernel: first begin, first ready, last ready, first end, last end
+    timeline = ({t[0]: [round(t[j] / tl_n, 2) for j in range(1, capi.TRACE_FIELDS + 1)] for t in tl_sum}
+                if tl_sum else None)
     status = blk.sync_status()
     if status != capi.MOE_OK:
         raise SystemExit(f"device error during the timed steps: {capi.STATUS_NAMES[status]}")
@@ -267,6 +295,8 @@ def run_ours(args, shape):
                            "experts_touched": U, "tflops": round(F / (ms / 1e3) / 1e12, 2),
                            "gbs": round(B / (ms / 1e3) / 1e9, 1), "peak_source": pk_src},
         "stage_us": {n: round(v * 1e3, 2) for n, v in stage_avg.items()},
+        "timeline_us": timeline,
+        "gemm_role_us": gemm_waits,
         "e2e": {"value": round(world * shape.T / e2e_s, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": xbytes, "d2h_bytes_per_step": xbytes},
         "gpu_launches": launches * args.steps,

@@ -43,14 +43,16 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra_flags=(), out_dir: str = BUILD) -> str:
+    """Compile into out_dir (default: the package's _build) and link libmoe.so there."""
+    os.makedirs(out_dir, exist_ok=True)
+    lib = os.path.join(out_dir, "libmoe.so")
     nvcc = _nvcc()
     jobs = []
     objs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(out_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if _stale(o, [s] + HEADERS):
             jobs.append([nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", s, "-o", o])
@@ -67,11 +69,11 @@ def build(verbose: bool = False, extra_flags=()) -> str:
         for msg in ex.map(run, jobs):
             if verbose and msg:
                 print(msg, file=sys.stderr)
-    if jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         run([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

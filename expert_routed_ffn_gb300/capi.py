@@ -25,6 +25,9 @@ MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
 MOE_ACT_SILU, MOE_ACT_SWIGLU_OAI = 0, 1
 MOE_DTYPE_BF16, MOE_DTYPE_F32 = 0, 1
 MOE_OPT_PATH, MOE_OPT_WAIT_LIMIT_NS, MOE_OPT_STAGE_EVENTS, MOE_OPT_FUSE_EXPERTS, MOE_OPT_PREFETCH = 0, 1, 2, 3, 4
+MOE_OPT_TRACE = 5
+MOE_BUF_GEMM_STATS = 6
+TRACE_FIELDS = 5  # first begin, first ready, last ready, first end, last end
 PATH_AUTO, PATH_DECODE, PATH_GROUPED, PATH_SWAPPED = 0, 1, 2, 3
 (MOE_BUF_TOPK_IDX, MOE_BUF_TOPK_W, MOE_BUF_EXPERT_OFFS, MOE_BUF_SORTED_TOKEN, MOE_BUF_SLOT,
  MOE_BUF_HIDDEN) = range(6)
@@ -84,11 +87,12 @@ def load():
     L.moe_get_stats.argtypes = [P, ctypes.POINTER(MoeStats)]
     L.moe_inspect.argtypes = [P, I, P, ctypes.c_size_t, P]
     L.moe_get_stage_times.argtypes = [P, ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I)]
+    L.moe_get_trace.argtypes = [P, ctypes.POINTER(ctypes.c_double), I, ctypes.POINTER(I)]
     L.moe_get_stage_name.argtypes = [P, I]
     L.moe_get_stage_name.restype = ctypes.c_char_p
     L.moe_dispatch_noalloc.argtypes = [P, I, I, I, P, P, P, P, P]
     for name in ("moe_create", "moe_route", "moe_forward", "moe_forward_host", "moe_sync_status", "moe_dispatch_noalloc",
-                 "moe_set_option", "moe_get_stats", "moe_inspect", "moe_get_stage_times"):
+                 "moe_set_option", "moe_get_stats", "moe_inspect", "moe_get_stage_times", "moe_get_trace"):
         getattr(L, name).restype = I
     _lib = L
     return L
@@ -199,6 +203,15 @@ class MoeBlock:
         n = ctypes.c_int()
         check(load().moe_get_stage_times(self.h, buf, 8, ctypes.byref(n)), "moe_get_stage_times")
         return [buf[i] for i in range(n.value)]
+
+    def trace(self) -> list:
+        """(name, first_begin, first_ready, last_ready, first_end, last_end) in us per kernel
+        of the last forward (MOE_OPT_TRACE on)."""
+        buf = (ctypes.c_double * (TRACE_FIELDS * 8))()
+        n = ctypes.c_int()
+        check(load().moe_get_trace(self.h, buf, 8, ctypes.byref(n)), "moe_get_trace")
+        names = self.stage_names()
+        return [(names[i],) + tuple(buf[TRACE_FIELDS * i + f] for f in range(TRACE_FIELDS)) for i in range(n.value)]
 
     def stage_names(self) -> list:
         L = load()

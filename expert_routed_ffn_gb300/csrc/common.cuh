@@ -40,6 +40,31 @@ __device__ __forceinline__ float glu_act(float g, float u, int act, float alpha,
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Device trace of one launch (tr = 5 slots, all start at ~0 and only shrink),
+// global-timer ns: tr[0] earliest CTA start, tr[1] earliest CTA past pdl_wait,
+// tr[2] = ~(latest CTA past pdl_wait), tr[3] earliest CTA end, tr[4] =
+// ~(latest CTA end).  Thread 0 of each CTA records; tr == nullptr turns it off.
+__device__ __forceinline__ uint64_t trace_now() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void trace_mark(unsigned long long *tr, int slot) {
+    if (tr != nullptr && threadIdx.x == 0) {
+        const unsigned long long t = trace_now();
+        atomicMin(tr + slot, t);
+        if (slot == 1) atomicMin(tr + 2, ~t);
+    }
+}
+// call after a CTA-wide barrier, when the CTA's work is done
+__device__ __forceinline__ void trace_exit(unsigned long long *tr) {
+    if (tr != nullptr && threadIdx.x == 0) {
+        const unsigned long long t = trace_now();
+        atomicMin(tr + 3, t);
+        atomicMin(tr + 4, ~t);
+    }
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    trace_mark(p.trace, 0);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full_bar(s), 1);
@@ -178,7 +179,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // the prologue above overlaps the previous kernel; the dispatch results
     // (offsets, tile counts) and the A rows are read only after this point
     pdl_wait();
+    trace_mark(p.trace, 1);
     pdl_trigger();
+    unsigned long long *const stats = p.stats;
+    const uint64_t t_ready = stats ? global_timer_ns() : 0;
     // every role decodes every tile: keep the dispatch offsets on chip
     __shared__ int s_offs[257], s_toffs[257];
     __shared__ int s_seg_end[kGemmMaxSegments];
@@ -207,27 +211,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         if (lane == 0) {
             uint32_t L = 0;  // loads issued so far; stage = L % kStages
             bool ok = true;
+            uint64_t w_empty = 0, w_dep = 0;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const Tile t = decode_tile(p, tile, s_seg_end, s_offs, s_toffs);
                 const GemmSegment &sg = p.seg[t.seg];
+                const int g = sg.group_base + t.group;
                 if (sg.wait != nullptr) {  // A rows written earlier in this launch
+                    const uint64_t t0 = stats ? global_timer_ns() : 0;
                     if (!wait_counter(sg.wait + t.ready, sg.wait_count, p.wait_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
+                    if (stats) w_dep += global_timer_ns() - t0;
                     fence_proxy_async();  // order the A rows' generic-proxy stores before our TMA reads
                 }
                 const CUtensorMap *mA = &p.maps[sg.map_a];
                 const CUtensorMap *mB = &p.maps[sg.map_b0];
                 const CUtensorMap *mB2 = &p.maps[sg.map_b1];
-                const int g = sg.group_base + t.group;
                 for (int kb = 0; kb < sg.k_blocks; ++kb) {
                     const int s = L % kStages;
                     const uint32_t ph = (L / kStages) & 1u;
+                    const uint64_t t0 = stats ? global_timer_ns() : 0;
                     if (!mbar_wait(empty_bar(s), ph ^ 1u, p.wait_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
+                    if (stats) w_empty += global_timer_ns() - t0;
                     mbar_arrive_expect_tx(full_bar(s), kStageBytes);
                     tma_load_2d(sA + s * kABytes, mA, full_bar(s), kb * kGemmBK, t.row0);
                     if (sg.glu) {
@@ -239,6 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     }
                     ++L;
                 }
+            }
+            if (stats) {
+                atomicAdd(stats + 0, (unsigned long long)w_empty);
+                atomicAdd(stats + 1, (unsigned long long)w_dep);
             }
             if (!ok) {
                 raise_abort(p.err, abort_flag);
@@ -255,23 +268,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const uint32_t idesc = idesc_bf16_f32(kGemmBM, kGemmBN);
             uint32_t L = 0, n_acc = 0;
             bool ok = true, issued = false;
+            uint64_t w_full = 0, w_acc = 0;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const Tile t = decode_tile(p, tile, s_seg_end, s_offs, s_toffs);
                 const GemmSegment &sg = p.seg[t.seg];
                 const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
+                const uint64_t t0 = stats ? global_timer_ns() : 0;
                 if (!mbar_wait(tempty_bar(a), aph ^ 1u, p.wait_ns, abort_flag)) {
                     ok = false;
                     break;
                 }
+                if (stats) w_acc += global_timer_ns() - t0;
                 tc_fence_after();
                 const uint32_t d = tmem_base + a * kGemmBN;
                 for (int kb = 0; kb < sg.k_blocks; ++kb) {
                     const int s = L % kStages;
                     const uint32_t ph = (L / kStages) & 1u;
+                    const uint64_t t1 = stats ? global_timer_ns() : 0;
                     if (!mbar_wait(full_bar(s), ph, p.wait_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
+                    if (stats) w_full += global_timer_ns() - t1;
                     tc_fence_after();
                     const uint64_t ad = smem_desc_k128(sA + s * kABytes);
                     const uint64_t bd = smem_desc_k128(sB + s * kBBytes);
@@ -286,6 +304,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 tc_commit(tfull_bar(a));  // accumulator complete
                 ++n_acc;
             }
+            if (stats) {
+                atomicAdd(stats + 2, (unsigned long long)w_full);
+                atomicAdd(stats + 3, (unsigned long long)w_acc);
+                atomicAdd(stats + 7, (unsigned long long)n_acc);
+            }
             if (!ok) {
                 raise_abort(p.err, abort_flag);
                 if (issued) {
@@ -299,13 +322,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
         const int r = q * 32 + lane;
         uint32_t n_acc = 0;
+        uint64_t w_tfull = 0, w_work = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             const Tile t = decode_tile(p, tile, s_seg_end, s_offs, s_toffs);
             const GemmSegment &sg = p.seg[t.seg];
             const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
             // all four epilogue warps agree to go on or stop (they share barrier 1);
             // the tcgen05.ld below is .sync.aligned
+            const uint64_t t0 = stats ? global_timer_ns() : 0;
             const bool ready = __all_sync(0xffffffffu, mbar_wait(tfull_bar(a), aph, p.wait_ns, abort_flag));
+            const uint64_t t1 = stats ? global_timer_ns() : 0;
+            w_tfull += t1 - t0;
             if (!epi_all(ready)) {
                 if (lane == 0) raise_abort(p.err, abort_flag);
                 break;
@@ -366,12 +393,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 epi_bar();
                 if (q == 0 && lane == 0) atomicAdd(sg.signal + t.ready, 1);
             }
+            if (stats) w_work += global_timer_ns() - t1;
             ++n_acc;
+        }
+        if (stats && q == 0 && lane == 0) {
+            atomicAdd(stats + 4, (unsigned long long)w_tfull);
+            atomicAdd(stats + 5, (unsigned long long)w_work);
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    trace_exit(p.trace);
+    if (stats && threadIdx.x == 0) atomicAdd(stats + 6, (unsigned long long)(global_timer_ns() - t_ready));
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();

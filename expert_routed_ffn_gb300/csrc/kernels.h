@@ -53,6 +53,7 @@ struct RouterArgs {
     int hb, he;
     __nv_bfloat16 *x_bf16; // [T, H] bf16 copy of fp32 X, or nullptr
     int tokens_per_block;  // 16 or 32
+    unsigned long long *trace;  // 5 slots, or nullptr
 };
 int router_tokens_per_block(int T, int num_sms);
 cudaError_t launch_router(const RouterArgs &a, cudaStream_t s);
@@ -68,6 +69,7 @@ struct RouterTcArgs {
     float *logits;         // [splits, T, Np] fp32 partial logits
     int *err;
     unsigned long long wait_ns;
+    unsigned long long *trace;
 };
 // Routing rule from logits: a group of lanes per token (8 experts per lane),
 // topk_tokens_per_block(E, T, SMs) tokens per CTA; writes the expert
@@ -84,6 +86,7 @@ struct TopkArgs {
     int32_t *topk_idx;     // [T, k]
     float *topk_w;         // [T, k]
     int32_t *blk_hist;     // block histograms or nullptr
+    unsigned long long *trace;
 };
 cudaError_t launch_topk(const TopkArgs &a, int tokens_per_block, cudaStream_t s);
 struct RouterTcPlan {
@@ -127,6 +130,7 @@ struct ScatterArgs {
     // and ready[ready_shared_base, + ready_shared_count)
     int *ready;
     int ready_shared_base, ready_shared_count;
+    unsigned long long *trace;
     int T, k, E, H;
     int tokens_per_block;     // <= 128: the router's blocking
     int gather_split;         // CTAs per token block sharing the row gather
@@ -149,6 +153,7 @@ struct CombineArgs {
     int T, k, H;
     void *Y;                     // [T, H]
     int y_f32;
+    unsigned long long *trace;
 };
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 
@@ -191,7 +196,14 @@ struct GemmArgs {
     int *err;
     unsigned long long wait_ns;
     int num_ctas;
+    unsigned long long *trace;
+    // nullptr, or kGemmStats ns sums over CTAs: producer waiting for a free
+    // stage, producer waiting for gate/up rows, MMA waiting for data, MMA
+    // waiting for an accumulator, epilogue waiting for an accumulator,
+    // epilogue working, CTA time past the dependency wait, tiles
+    unsigned long long *stats;
 };
+constexpr int kGemmStats = 8;
 cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s);
 size_t gemm_tc_smem_bytes();
 

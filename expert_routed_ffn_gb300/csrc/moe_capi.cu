@@ -89,7 +89,9 @@ struct moe_handle {
     cudaStream_t side = nullptr;               // the prefetch runs here, beside the routing kernels
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     int hist_stride = 0;       // block histograms are [E, hist_stride]
-    int *counter = nullptr;    // CTA ticket of the top-k kernel's fused scan
+    unsigned long long *trace = nullptr;  // [kMaxStages][kTraceSlots] device trace (MOE_OPT_TRACE)
+    bool trace_on = false;
+    unsigned long long *gemm_stats = nullptr;  // [moe::kGemmStats] (MOE_OPT_TRACE)
     int *wr_flags = nullptr;
     moe::RouterTcPlan rplan{};
 
@@ -199,7 +201,8 @@ void carve(moe_handle *h, void *base) {
     // split-K keeps splits * T <= max(max_tokens, 128 * SMs) rows
     const size_t lrows = MT > (size_t)h->num_sms * 128 ? MT : (size_t)h->num_sms * 128;
     h->logits = c.take<float>(base, lrows * ((E + 31) / 32 * 32));
-    h->counter = c.take<int>(base, 64);
+    h->trace = c.take<unsigned long long>(base, MOE_TRACE_FIELDS * moe_handle::kMaxStages);
+    h->gemm_stats = c.take<unsigned long long>(base, moe::kGemmStats);
     // routed m-tiles number at most T*k/128 + E; the shared expert's follow
     h->ready_shared_base = (int)(MT * k / 128 + E + 1);
     h->ready = c.take<int>(base, (size_t)h->ready_shared_base + (MT + 127) / 128 + 1);
@@ -274,6 +277,11 @@ moe_status launched(moe_handle *h, cudaError_t e, const char *what, int *n, cuda
     return MOE_OK;
 }
 
+// Trace slots of the kernel about to be launched as number n, or nullptr.
+unsigned long long *trace_slot(const moe_handle *h, int n) {
+    return h->trace_on && n < moe_handle::kMaxStages ? h->trace + MOE_TRACE_FIELDS * n : nullptr;
+}
+
 // TMA descriptor of the caller's bf16 X (router and shared-expert A operand),
 // re-encoded only when the pointer or T changes.
 moe_status x_map(moe_handle *h, const void *X, int T) {
@@ -282,6 +290,19 @@ moe_status x_map(moe_handle *h, const void *X, int T) {
     if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(X) failed: %d", (int)r);
     h->m_x_ptr = X;
     h->m_x_rows = T;
+    return MOE_OK;
+}
+
+// TMA descriptor of the caller's bf16 X with a box of 32 (v = 0) or 64 (v = 1)
+// rows, cached by pointer and T.
+moe_status x_map_box(moe_handle *h, const void *X, int T, int v, const CUtensorMap **out) {
+    if (h->m_x_n_ptr[v] != X || h->m_x_n_rows[v] != T) {
+        CUresult r = moe::encode_map_a_box(&h->m_x_n[v], X, T, h->H, v ? 64 : 32);
+        if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(X) failed: %d", (int)r);
+        h->m_x_n_ptr[v] = X;
+        h->m_x_n_rows[v] = T;
+    }
+    *out = &h->m_x_n[v];
     return MOE_OK;
 }
 
@@ -304,6 +325,7 @@ moe_status run_router_tc(moe_handle *h, const void *X, int T, int32_t *topk_idx,
     ra.logits = h->logits;
     ra.err = h->err;
     ra.wait_ns = h->wait_ns;
+    ra.trace = trace_slot(h, *n);
     {
         // split the H reduction so that about one CTA runs per SM
         const int nk = h->H / 64, mtiles = (T + 127) / 128;
@@ -331,6 +353,7 @@ moe_status run_router_tc(moe_handle *h, const void *X, int T, int32_t *topk_idx,
     ta.topk_idx = topk_idx;
     ta.topk_w = topk_w;
     ta.blk_hist = blk_hist;
+    ta.trace = trace_slot(h, *n);
     return launched(h, moe::launch_topk(ta, moe::topk_tokens_per_block(h->E, T, h->num_sms), s), "router_topk",
                     n, s);
 }
@@ -365,6 +388,7 @@ moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n
     ra.hb = 1;
     ra.he = h->hist_stride;
     ra.tokens_per_block = TT;
+    ra.trace = trace_slot(h, *n);
     moe_status st = launched(h, moe::launch_router(ra, s), "router", n, s);
     if (st != MOE_OK) return st;
     }
@@ -401,6 +425,7 @@ moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n
     xa.slot_of = h->slot_of;
     xa.x_sorted = h->x_sorted;
     xa.err = h->err;
+    xa.trace = trace_slot(h, *n);
     st = launched(h, moe::launch_scatter(xa, s), "dispatch_scatter", n, s);
     if (st != MOE_OK) return st;
     return MOE_OK;
@@ -450,7 +475,8 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     const moe::GemmSegment dn{0, E, 0, 0, h->offs, h->tile_offs, nt_d, I / 64, H, h->yslot, H,
                               0, kHb, kD, kD, nullptr, fused ? h->ready : nullptr, nt_gu, 0};
     const moe::GemmSegment sdn{1, 1, sh_base, T, nullptr, nullptr, nt_d, S / 64, H, h->ys, H,
-                               0, kHs, kSD, kSD, nullptr, fused ? h->ready : nullptr, nt_sgu, h->ready_shared_base};
+                               0, kHs, kSD, kSD, nullptr, fused ? h->ready : nullptr, nt_sgu,
+                               h->ready_shared_base};
     if (fused) {
         int ns = 0;
         g.seg[ns++] = gu;
@@ -458,6 +484,8 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         g.seg[ns++] = dn;
         if (h->has_shared) g.seg[ns++] = sdn;
         g.num_segs = ns;
+        g.trace = trace_slot(h, *n);
+        g.stats = h->trace_on ? h->gemm_stats : nullptr;
         return launched(h, moe::launch_gemm_tc(g, s), "experts_gemm", n, s);
     }
     g.seg[0] = gu;
@@ -466,6 +494,7 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         g.seg[1] = sgu;
         g.num_segs = 2;
     }
+    g.trace = trace_slot(h, *n);
     moe_status st = launched(h, moe::launch_gemm_tc(g, s), "gate_up_gemm", n, s);
     if (st != MOE_OK) return st;
     g.seg[0] = dn;
@@ -474,6 +503,7 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         g.seg[1] = sdn;
         g.num_segs = 2;
     }
+    g.trace = trace_slot(h, *n);
     return launched(h, moe::launch_gemm_tc(g, s), "down_gemm", n, s);
 }
 
@@ -538,13 +568,10 @@ moe_status run_swapped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         if (h->x_f32) {
             g.X1 = h->m_xbf_n[v];
         } else {
-            if (h->m_x_n_ptr[v] != X || h->m_x_n_rows[v] != T) {
-                CUresult r = moe::encode_map_a_box(&h->m_x_n[v], X, T, H, n_tok);
-                if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(X) failed: %d", (int)r);
-                h->m_x_n_ptr[v] = X;
-                h->m_x_n_rows[v] = T;
-            }
-            g.X1 = h->m_x_n[v];
+            const CUtensorMap *mx = nullptr;
+            moe_status st = x_map_box(h, X, T, v, &mx);
+            if (st != MOE_OK) return st;
+            g.X1 = *mx;
         }
         g.Wa1 = h->m_shg64;
         g.Wb1 = h->m_shu64;
@@ -592,6 +619,12 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
         if (e == cudaSuccess) e = cudaEventRecord(h->ev_join, h->side);
         if (e != cudaSuccess) return cuda_fail(e, "weight prefetch");
     }
+    if (h->trace_on) {  // every slot starts at ~0 and only shrinks (atomicMin)
+        cudaError_t e =
+            cudaMemsetAsync(h->trace, 0xff, MOE_TRACE_FIELDS * moe_handle::kMaxStages * sizeof(unsigned long long), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(h->gemm_stats, 0, moe::kGemmStats * sizeof(unsigned long long), s);
+        if (e != cudaSuccess) return cuda_fail(e, "trace reset");
+    }
     mark(h, 0, s);
     moe_status st = run_front(h, X, T, s, &n, path == kPathSwapped ? n_tok : moe::kGemmBM);
     if (st == MOE_OK) {
@@ -604,7 +637,7 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     }
     if (st == MOE_OK) {
         moe::CombineArgs ca{h->yslot, h->has_shared ? h->ys : nullptr, h->topk_w, h->slot_of,
-                            T, h->k, h->H, Y, h->x_f32 ? 1 : 0};
+                            T, h->k, h->H, Y, h->x_f32 ? 1 : 0, trace_slot(h, n)};
         st = launched(h, moe::launch_combine(ca, s), "combine", &n, s);
     }
     if (prefetch) {  // the caller's stream ends ordered after the side stream
@@ -676,7 +709,6 @@ moe_status moe_create(const moe_config *config, const moe_weights *weights, moe_
     carve(h, h->ws);
     e = cudaMemset(h->err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(h->wr_flags, 0, sizeof(int));
-    if (e == cudaSuccess) e = cudaMemset(h->counter, 0, sizeof(int));
     if (e == cudaSuccess) e = moe::launch_split_router(w.router_w, h->E, h->H, h->wr_parts, h->wr_flags, 0);
     int flags = 0;
     if (e == cudaSuccess) e = cudaMemcpy(&flags, h->wr_flags, sizeof(int), cudaMemcpyDeviceToHost);
@@ -822,6 +854,10 @@ moe_status moe_set_option(moe_handle *h, int option, long long value) {
         if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "fuse experts %lld", value);
         h->fuse_experts = value != 0;
         return MOE_OK;
+    case MOE_OPT_TRACE:
+        if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "trace %lld", value);
+        h->trace_on = value != 0;
+        return MOE_OK;
     case MOE_OPT_STAGE_EVENTS:
         if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "stage events %lld", value);
         if (value && h->ev[0] == nullptr) {
@@ -862,6 +898,33 @@ moe_status moe_get_stage_times(moe_handle *h, float *ms, int max, int *n) {
     return MOE_OK;
 }
 
+moe_status moe_get_trace(moe_handle *h, double *t_us, int max, int *n) {
+    if (h == nullptr || t_us == nullptr || n == nullptr) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    if (!h->trace_on || h->last_launches < 1)
+        return fail(MOE_ERR_INVALID_ARG, "no traced forward (enable MOE_OPT_TRACE first)");
+    cudaError_t e = cudaSetDevice(h->device);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    unsigned long long raw[MOE_TRACE_FIELDS * moe_handle::kMaxStages];
+    if (e == cudaSuccess) e = cudaMemcpy(raw, h->trace, sizeof(raw), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "trace read");
+    const int kernels = h->last_launches < moe_handle::kMaxStages ? h->last_launches : moe_handle::kMaxStages;
+    const unsigned long long none = ~0ull;
+    unsigned long long t0 = none;
+    for (int i = 0; i < kernels; ++i)
+        if (raw[MOE_TRACE_FIELDS * i] < t0) t0 = raw[MOE_TRACE_FIELDS * i];
+    int count = 0;
+    for (int i = 0; i < kernels && count < max; ++i, ++count) {
+        const unsigned long long *r = raw + MOE_TRACE_FIELDS * i;
+        // slots 2 and 4 hold the complement of a maximum
+        const unsigned long long v[MOE_TRACE_FIELDS] = {r[0], r[1], ~r[2], r[3], ~r[4]};
+        const bool ok = r[0] != none && r[1] != none && r[2] != none && r[3] != none && r[4] != none;
+        for (int f = 0; f < MOE_TRACE_FIELDS; ++f)
+            t_us[MOE_TRACE_FIELDS * i + f] = ok ? (double)(v[f] - t0) * 1e-3 : -1.0;
+    }
+    *n = count;
+    return MOE_OK;
+}
+
 const char *moe_get_stage_name(const moe_handle *h, int i) {
     if (h == nullptr || i < 0 || i >= h->last_launches || i >= moe_handle::kMaxStages) return nullptr;
     return h->stage_name[i];
@@ -879,6 +942,7 @@ moe_status moe_inspect(const moe_handle *h, int buffer, void *dst, size_t bytes,
     case MOE_BUF_SORTED_TOKEN: src = h->sorted_tok; cap = MT * k * 4; break;
     case MOE_BUF_SLOT: src = h->slot_of; cap = MT * k * 4; break;
     case MOE_BUF_HIDDEN: src = h->hbuf; cap = MT * k * h->I * 2; break;
+    case MOE_BUF_GEMM_STATS: src = h->gemm_stats; cap = moe::kGemmStats * 8; break;
     default: return fail(MOE_ERR_INVALID_ARG, "unknown buffer %d", buffer);
     }
     if (bytes > cap) return fail(MOE_ERR_INVALID_ARG, "%zu bytes requested, buffer holds %zu", bytes, cap);

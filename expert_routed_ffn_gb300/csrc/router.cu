@@ -91,52 +91,66 @@ __device__ __forceinline__ void route_token_group(const float (&lg)[8], int sub,
             c[j] = -INFINITY;
         }
     }
-    float sel_s[16], wsum = 0.f;
-    int sel_e[16];
+    // Slot r is kept by lane r mod LPT of the group (entry r / LPT of its
+    // own[] arrays), so the k rounds compile to one loop body: the routing
+    // kernels run once per forward with a cold instruction cache.
+    constexpr int kOwn = (16 + LPT - 1) / LPT;
+    float own_s[kOwn];
+    int own_e[kOwn];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-        sel_s[r] = 0.f;
-        sel_e[r] = 0;
-        if (r < k) {
-            float bc = -INFINITY;
-            int be = 0x7fffffff;
+    for (int q = 0; q < kOwn; ++q) {
+        own_s[q] = 0.f;
+        own_e[q] = 0;
+    }
+    float wsum = 0.f;
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+        float bc = -INFINITY;
+        int be = 0x7fffffff;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if ((open >> j & 1u) && better(c[j], sub + LPT * j, bc, be)) {
-                    bc = c[j];
-                    be = sub + LPT * j;
-                }
-#pragma unroll
-            for (int o = LPT / 2; o > 0; o >>= 1) {
-                const float oc = __shfl_xor_sync(0xffffffffu, bc, o, LPT);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o, LPT);
-                if (better(oc, oe, bc, be)) {
-                    bc = oc;
-                    be = oe;
-                }
+        for (int j = 0; j < 8; ++j)
+            if ((open >> j & 1u) && better(c[j], sub + LPT * j, bc, be)) {
+                bc = c[j];
+                be = sub + LPT * j;
             }
-            const int owner = be & (LPT - 1), jj = be / LPT;
-            float sv = 0.f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j == jj) sv = s[j];
-            if (sub == owner) open &= ~(1u << jj);
-            sv = __shfl_sync(0xffffffffu, sv, owner, LPT);
-            sel_s[r] = sv;
-            sel_e[r] = be;
-            wsum += sv;
+        for (int o = LPT / 2; o > 0; o >>= 1) {
+            const float oc = __shfl_xor_sync(0xffffffffu, bc, o, LPT);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o, LPT);
+            if (better(oc, oe, bc, be)) {
+                bc = oc;
+                be = oe;
+            }
+        }
+        const int owner = be & (LPT - 1), jj = be / LPT;
+        float sv = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j == jj) sv = s[j];
+        if (sub == owner) open &= ~(1u << jj);
+        sv = __shfl_sync(0xffffffffu, sv, owner, LPT);
+        wsum += sv;
+        if ((r & (LPT - 1)) == sub) {
+            const int qr = r / LPT;
+#pragma unroll
+            for (int q = 0; q < kOwn; ++q)
+                if (q == qr) {
+                    own_s[q] = sv;
+                    own_e[q] = be;
+                }
         }
     }
     if (valid) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            if (r < k && (r & (LPT - 1)) == sub) {
-                float w = sel_s[r];
+        for (int q = 0; q < kOwn; ++q) {
+            const int r = sub + LPT * q;
+            if (r < k) {
+                float w = own_s[q];
                 if (route_norm) w = w / wsum;
                 w = w * route_scale;
-                topk_idx[(size_t)t * k + r] = sel_e[r];
+                topk_idx[(size_t)t * k + r] = own_e[q];
                 topk_w[(size_t)t * k + r] = w;
-                if (hist != nullptr) atomicAdd(&hist[sel_e[r]], 1);
+                if (hist != nullptr) atomicAdd(&hist[own_e[q]], 1);
             }
         }
     }
@@ -154,7 +168,9 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
 
     const int E = a.E, H = a.H, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t0 = blockIdx.x * TT;
+    trace_mark(a.trace, 0);
     pdl_wait();
+    trace_mark(a.trace, 1);
     pdl_trigger();
     for (int e = tid; e < E; e += kRouterThreads) hist[e] = 0;
 
@@ -227,6 +243,8 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
         for (int e = tid; e < E; e += kRouterThreads)
             a.blk_hist[(size_t)blockIdx.x * a.hb + (size_t)e * a.he] = hist[e];
     }
+    __syncthreads();
+    trace_exit(a.trace);
 }
 
 // Dispatch scan over block histograms, by one CTA of 1024 threads.  Per expert
@@ -309,7 +327,9 @@ __global__ void __launch_bounds__(1024) topk_kernel(const TopkArgs a) {
     const int E = a.E, sub = threadIdx.x & (LPT - 1), grp = threadIdx.x / LPT;
     const int TT = blockDim.x / LPT;
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    trace_mark(a.trace, 0);
     pdl_wait();
+    trace_mark(a.trace, 1);
     pdl_trigger();
     __syncthreads();
     const int t = blockIdx.x * TT + grp;
@@ -335,6 +355,8 @@ __global__ void __launch_bounds__(1024) topk_kernel(const TopkArgs a) {
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             a.blk_hist[(size_t)blockIdx.x * a.hb + (size_t)e * a.he] = hist[e];
     }
+    __syncthreads();
+    trace_exit(a.trace);
 }
 
 size_t router_smem(int TT, int E) { return (size_t)(TT + E) * kPad * 4 + (size_t)E * 4; }
@@ -374,15 +396,32 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int e = threadIdx.x; e < E; e += kScatterThreads) cnt[e] = pre[e] = 0;
     for (int i = threadIdx.x; i < E * words; i += kScatterThreads) masks[i / words][i % words] = 0;
+    trace_mark(a.trace, 0);
     pdl_wait();
+    trace_mark(a.trace, 1);
     pdl_trigger();
     __syncthreads();
-    for (int i = threadIdx.x; i < E * nbk; i += kScatterThreads) {
-        const int e = i / nbk, bb = i - e * nbk;
-        const int v = __ldg(a.blk_hist + (size_t)bb * hb + (size_t)e * he);
-        if (v) {
-            atomicAdd(&cnt[e], v);
-            if (bb < b) atomicAdd(&pre[e], v);
+    {
+        // eight independent loads in flight per thread, then the shared sums
+        constexpr int kU = 8;
+        const int tot = E * nbk;
+        for (int i0 = threadIdx.x; i0 < tot; i0 += kU * kScatterThreads) {
+            int v[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = i0 + u * kScatterThreads;
+                const int e = i / nbk, bb = i - e * nbk;
+                v[u] = i < tot ? __ldg(a.blk_hist + (size_t)bb * hb + (size_t)e * he) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = i0 + u * kScatterThreads;
+                if (v[u]) {
+                    const int e = i / nbk, bb = i - e * nbk;
+                    atomicAdd(&cnt[e], v[u]);
+                    if (bb < b) atomicAdd(&pre[e], v[u]);
+                }
+            }
         }
     }
     __syncthreads();
@@ -469,6 +508,8 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
             *reinterpret_cast<uint4 *>(a.x_sorted + dst + c) = o;
         }
     }
+    __syncthreads();
+    trace_exit(a.trace);
 }
 
 // ---------------------------------------------------------------- combine
@@ -477,7 +518,9 @@ constexpr int kCombineThreads = 128;
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
     const int t = blockIdx.x, k = a.k, H = a.H;
+    trace_mark(a.trace, 0);
     pdl_wait();
+    trace_mark(a.trace, 1);
     pdl_trigger();
     for (int c = threadIdx.x * 8; c < H; c += kCombineThreads * 8) {
         float acc[8];
@@ -510,9 +553,19 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineA
             *reinterpret_cast<uint4 *>(static_cast<bf16 *>(a.Y) + (size_t)t * H + c) = o;
         }
     }
+    __syncthreads();
+    trace_exit(a.trace);
 }
 
 }  // namespace
+
+// The routing kernels overlap the expert GEMM's CTAs (programmatic dependent
+// launch): ask for the largest shared-memory carveout so that an SM running
+// them can still take a GEMM CTA.
+template <typename K>
+static void max_smem_carveout(K kernel) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+}
 
 int router_tokens_per_block(int T, int num_sms) { return (T + 31) / 32 >= num_sms ? 32 : 16; }
 
@@ -522,6 +575,8 @@ cudaError_t launch_router(const RouterArgs &a, cudaStream_t s) {
         const int max_smem = (int)router_smem(32, 256);
         cudaFuncSetAttribute(router_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
         cudaFuncSetAttribute(router_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        max_smem_carveout(router_kernel<16>);
+        max_smem_carveout(router_kernel<32>);
     });
     const int TT = a.tokens_per_block;
     const int nb = (a.T + TT - 1) / TT;
@@ -547,6 +602,14 @@ int topk_tokens_per_block(int E, int T, int num_sms) {
 }
 
 cudaError_t launch_topk(const TopkArgs &a, int tokens_per_block, cudaStream_t s) {
+    static std::once_flag once;
+    std::call_once(once, [] {
+        max_smem_carveout(topk_kernel<2>);
+        max_smem_carveout(topk_kernel<4>);
+        max_smem_carveout(topk_kernel<8>);
+        max_smem_carveout(topk_kernel<16>);
+        max_smem_carveout(topk_kernel<32>);
+    });
     const int lpt = topk_lpt(a.E), tt = tokens_per_block;
     const dim3 grid((a.T + tt - 1) / tt), block(tt * lpt);
     switch (lpt) {
@@ -563,12 +626,16 @@ cudaError_t launch_scan(const ScanArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_scatter(const ScatterArgs &a, cudaStream_t s) {
+    static std::once_flag once;
+    std::call_once(once, [] { max_smem_carveout(scatter_kernel); });
     const int nb = (a.T + a.tokens_per_block - 1) / a.tokens_per_block;
     return launch_pdl(scatter_kernel, dim3(nb, a.gather_split > 0 ? a.gather_split : 1), dim3(kScatterThreads),
                       0, s, a);
 }
 
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
+    static std::once_flag once;
+    std::call_once(once, [] { max_smem_carveout(combine_kernel); });
     return launch_pdl(combine_kernel, dim3(a.T), dim3(kCombineThreads), 0, s, a);
 }
 

@@ -44,6 +44,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    trace_mark(p.trace, 0);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
@@ -66,6 +67,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     pdl_wait();
+    trace_mark(p.trace, 1);
     pdl_trigger();
     const uint32_t tmem_base = *tmem_slot;
     // split-K: this CTA takes k-blocks [kb0, kb0 + nkb) and writes its partial logits
@@ -153,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
 
     tc_fence_before();
     __syncthreads();
+    trace_exit(p.trace);
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -212,6 +215,12 @@ RouterTcPlan plan_router_tc(int E, int parts) {
 }
 
 cudaError_t launch_l2_prefetch(const PrefetchArgs &a, cudaStream_t s) {
+    // runs beside the expert GEMM's CTAs: keep the SM's shared memory available to them
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaFuncSetAttribute(l2_prefetch_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    });
     l2_prefetch_kernel<<<64, 32, 0, s>>>(a);
     return cudaGetLastError();
 }

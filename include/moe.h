@@ -158,11 +158,16 @@ typedef enum {
     MOE_OPT_FUSE_EXPERTS = 3,  /* path 2: 1 (default) runs the gate/up and down GEMMs as one
                                   persistent launch whose down tiles wait for their gate/up rows;
                                   0 runs them as two launches */
-    MOE_OPT_PREFETCH = 4       /* 1 (default): when T*k >= 2E (nearly every expert is touched), an
+    MOE_OPT_PREFETCH = 4,      /* 1 (default): when T*k >= 2E (nearly every expert is touched), an
                                   internal side stream prefetches the first experts' gate/up weights
                                   into L2 while the routing kernels run (forked from and joined back
                                   into the caller's stream); 0: no prefetch.  A hint: results are
                                   unchanged */
+    MOE_OPT_TRACE = 5          /* 1: every kernel of moe_forward on the grouped path records, in a
+                                  device buffer of the handle, when its first CTA started, when its
+                                  first and last CTA passed the wait on the previous kernel, and when
+                                  its first and last CTA finished (the GPU's global timer), for
+                                  moe_get_trace.  Costs a memset and a few atomics per CTA; default 0 */
 } moe_option;
 
 /* Set an option.  Errors: INVALID_ARG (unknown option or value). */
@@ -189,13 +194,38 @@ moe_status moe_get_stage_times(moe_handle *h, float *ms, int max, int *n);
  * NULL when i is out of range.  The string is static. */
 const char *moe_get_stage_name(const moe_handle *h, int i);
 
+/* Fields of one kernel's entry in moe_get_trace, in us from the first kernel's first CTA start. */
+#define MOE_TRACE_FIELDS 5
+typedef enum {
+    MOE_TRACE_FIRST_BEGIN = 0, /* first CTA started */
+    MOE_TRACE_FIRST_READY = 1, /* first CTA passed the wait on the previous kernel */
+    MOE_TRACE_LAST_READY = 2,  /* last CTA passed that wait */
+    MOE_TRACE_FIRST_END = 3,   /* first CTA finished */
+    MOE_TRACE_LAST_END = 4     /* last CTA finished */
+} moe_trace_field;
+
+/* With MOE_OPT_TRACE on: wait for the device to go idle and write, for each kernel of the
+ * last moe_forward in launch order (names from moe_get_stage_name), MOE_TRACE_FIELDS times
+ * to t_us[MOE_TRACE_FIELDS * i + field].  With programmatic dependent launch a kernel
+ * begins before its predecessor ends; FIRST_READY minus the predecessor's LAST_END is the
+ * hand-over gap.  A kernel that records nothing (the decode and swapped paths' GEMMs)
+ * reads -1.  At most `max` kernels; *n = kernels written.  Errors: INVALID_ARG (trace off,
+ * no forward, NULL argument), CUDA. */
+moe_status moe_get_trace(moe_handle *h, double *t_us, int max, int *n);
+
 typedef enum {
     MOE_BUF_TOPK_IDX = 0,     /* [T, k] int32, routing of the last forward */
     MOE_BUF_TOPK_W = 1,       /* [T, k] fp32 */
     MOE_BUF_EXPERT_OFFS = 2,  /* [E + 1] int32: rows of expert e are [offs[e], offs[e+1]) */
     MOE_BUF_SORTED_TOKEN = 3, /* [T * k] int32: token of each expert-sorted row */
     MOE_BUF_SLOT = 4,         /* [T * k] int32: sorted row of routing slot (t, j) */
-    MOE_BUF_HIDDEN = 5        /* [T * k, I] bf16: act(gate, up) of each sorted row */
+    MOE_BUF_HIDDEN = 5,       /* [T * k, I] bf16: act(gate, up) of each sorted row */
+    MOE_BUF_GEMM_STATS = 6    /* [8] uint64, with MOE_OPT_TRACE on and the fused expert GEMM: ns
+                                 summed over its CTAs of: producer waiting for a free stage,
+                                 producer waiting for gate/up rows, MMA waiting for data, MMA
+                                 waiting for an accumulator, epilogue waiting for an accumulator,
+                                 epilogue working, CTA time past the dependency wait; then the
+                                 number of tiles */
 } moe_buffer;
 
 /* Copy `bytes` of an internal buffer, as the last forward left it, to the

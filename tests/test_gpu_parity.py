@@ -172,6 +172,30 @@ def test_fused_expert_gemm_equals_two_launches():
         assert torch.equal(Y1, Y2)
 
 
+def test_device_trace_orders_the_kernels_and_leaves_results_unchanged():
+    """With the trace on, each kernel of the grouped path reports first start <=
+    first ready <= last ready <= last end and first ready <= first end, and a
+    kernel passes its dependency wait only after its predecessor's last CTA
+    ended (the global timer ticks in about 1 us steps, hence the slack)."""
+    for name in ("nano_decode", "tiny_f32"):
+        shape = SMALL[name]
+        inputs, blk, Y1 = _run(shape, capi.PATH_GROUPED)
+        blk.set_option(capi.MOE_OPT_TRACE, 1)
+        Y2 = blk.forward(inputs["X"])
+        tr = blk.trace()
+        assert blk.sync_status() == capi.MOE_OK
+        assert torch.equal(Y1, Y2)
+        assert [t[0] for t in tr] == blk.stage_names()
+        assert min(t[1] for t in tr) == 0.0
+        for name_i, b, r, rl, e0, e in tr:
+            assert 0.0 <= b <= r <= rl <= e < 1e5 and r <= e0 <= e, (name_i, b, r, rl, e0, e)
+        for prev, cur in zip(tr, tr[1:]):
+            assert cur[2] >= prev[5] - 1.5, (prev, cur)
+        blk.set_option(capi.MOE_OPT_TRACE, 0)
+        with pytest.raises(capi.MoeError):
+            blk.trace()
+
+
 def test_token_permutation_equivariance_and_determinism():
     shape = SMALL["afmoe_ragged"]
     for path in PATHS.values():
