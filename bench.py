@@ -190,7 +190,7 @@ def run_ours(args, shape):
     # device timeline of the same steps without events: per kernel, first CTA
     # start, first CTA past the wait on its predecessor, last CTA end (us)
     blk.set_option(capi.MOE_OPT_TRACE, 1)
-    tl_sum, tl_n, gw_sum = None, 0, None
+    tl_sum, tl_n, gw_sum, rw_sum = None, 0, None, None
     for _ in range(args.steps):
         step()
         tr = blk.trace()
@@ -203,6 +203,9 @@ def run_ours(args, shape):
         if "experts_gemm" in names:
             st = blk.inspect(capi.MOE_BUF_GEMM_STATS, 8, torch.int64).cpu().tolist()
             gw_sum = st if gw_sum is None else [a + b for a, b in zip(gw_sum, st)]
+        if "router" in names and not shape.dtype == "f32":
+            st = blk.inspect(capi.MOE_BUF_ROUTER_STATS, 8, torch.int64).cpu().tolist()
+            rw_sum = st if rw_sum is None else [a + b for a, b in zip(rw_sum, st)]
     blk.set_option(capi.MOE_OPT_TRACE, 0)
     gemm_waits = None
     if gw_sum is not None:
@@ -212,6 +215,12 @@ def run_ours(args, shape):
                 "epilogue_wait_accum", "epilogue_work", "cta_busy"]
         gemm_waits = {k: round(v * per, 2) for k, v in zip(keys, gw_sum[:7])}
         gemm_waits["tiles"] = gw_sum[7] // tl_n
+    router_phases = None
+    if rw_sum is not None and rw_sum[5] > 0:
+        # per CTA and step, us: the tensor-core router's phases
+        keys = ["main_loop", "cluster_barrier", "push_partials", "sum_and_route", "histogram"]
+        router_phases = {k: round(v * 1e-3 / rw_sum[5], 2) for k, v in zip(keys, rw_sum[:5])}
+        router_phases["ctas"] = rw_sum[5] // tl_n
     # per kernel: first begin, first ready, last ready, first end, last end
     timeline = ({t[0]: [round(t[j] / tl_n, 2) for j in range(1, capi.TRACE_FIELDS + 1)] for t in tl_sum}
                 if tl_sum else None)
@@ -297,6 +306,7 @@ def run_ours(args, shape):
         "stage_us": {n: round(v * 1e3, 2) for n, v in stage_avg.items()},
         "timeline_us": timeline,
         "gemm_role_us": gemm_waits,
+        "router_phase_us": router_phases,
         "e2e": {"value": round(world * shape.T / e2e_s, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": xbytes, "d2h_bytes_per_step": xbytes},
         "gpu_launches": launches * args.steps,

@@ -11,7 +11,29 @@
 namespace moe {
 
 // Launch `kernel` with programmatic dependent launch allowed (the kernel calls
-// pdl_wait() before touching memory that earlier kernels on the stream use).
+// pdl_wait() before touching memory that earlier kernels on the stream use),
+// in thread-block clusters of `cluster` CTAs.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                      dim3 cluster, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster.x;
+    attr[1].val.clusterDim.y = cluster.y;
+    attr[1].val.clusterDim.z = cluster.z;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// The same without clusters.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               Args &&...args) {
@@ -58,39 +80,38 @@ struct RouterArgs {
 int router_tokens_per_block(int T, int num_sms);
 cudaError_t launch_router(const RouterArgs &a, cudaStream_t s);
 
-// Router logits on the tensor cores: 128 tokens per CTA, fp32 logits to
-// global memory.  The fp32 router weights are held as `parts` bf16 slices
-// [parts, E, H] whose sum is exact (see launch_split_router).
+// Tensor-core router with the routing rule (router_tc.cu): grid (ceil(T/128),
+// splits) in clusters of (1, splits); the splits CTAs of an m-tile share its
+// H reduction and each routes 128 / splits of its tokens.  The fp32 router
+// weights are held as `parts` bf16 slices [parts, E, H] whose sum is exact
+// (see launch_split_router).
+constexpr int kMaxRouterSplits = 8;
 struct RouterTcArgs {
     CUtensorMap mapX;      // X [T, H] bf16, box 128 x 64
     CUtensorMap mapW;      // router weight parts [parts, E, H] bf16, box Np x 64
     int T, H, E, Np, parts, stages, tmem_cols;
-    int kb_per_split;      // 64-wide k-blocks per CTA along grid.y (split-K)
-    float *logits;         // [splits, T, Np] fp32 partial logits
-    int *err;
-    unsigned long long wait_ns;
-    unsigned long long *trace;
-};
-// Routing rule from logits: a group of lanes per token (8 experts per lane),
-// topk_tokens_per_block(E, T, SMs) tokens per CTA; writes the expert
-// histogram of each CTA's tokens to blk_hist.
-constexpr int kMaxRouterSplits = 4;
-int topk_tokens_per_block(int E, int T, int num_sms);
-struct TopkArgs {
-    const float *logits;   // [splits, T, ld] partial logits, summed in split order
-    int ld, T, E, k, splits;
-    int hb, he;            // histogram strides, as in ScanArgs
+    int kb_per_split;      // 64-wide k-blocks per CTA of a cluster
+    int splits;            // cluster size: 1, 2, 4 or 8
+    int staged_push;       // 1: the stage buffers hold two [128][Np + 4] fp32 arrays (plan)
+    int k;
     const float *bias;     // [E] or nullptr
     int score_func, route_norm;
     float route_scale;
     int32_t *topk_idx;     // [T, k]
     float *topk_w;         // [T, k]
-    int32_t *blk_hist;     // block histograms or nullptr
+    int32_t *blk_hist;     // histogram of each (128 / splits)-token block, or nullptr
+    int hb, he;            // its strides, as in ScanArgs
+    int *err;
+    unsigned long long wait_ns;
     unsigned long long *trace;
+    // nullptr, or kRouterStats ns sums over CTAs: main loop, first cluster
+    // barrier, pushing the partials with the second barrier, adding them and
+    // routing, histogram; then the number of CTAs
+    unsigned long long *stats;
 };
-cudaError_t launch_topk(const TopkArgs &a, int tokens_per_block, cudaStream_t s);
+constexpr int kRouterStats = 8;
 struct RouterTcPlan {
-    int Np, tmem_cols, stages, smem, parts;
+    int Np, tmem_cols, stages, smem, parts, staged_push;
 };
 RouterTcPlan plan_router_tc(int E, int parts);
 cudaError_t launch_router_tc(const RouterTcArgs &a, int smem, cudaStream_t s);

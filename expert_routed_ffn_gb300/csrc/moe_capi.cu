@@ -81,7 +81,6 @@ struct moe_handle {
     void *x_stage = nullptr, *y_stage = nullptr;
     int *err = nullptr;
     bf16 *wr_parts = nullptr;  // router weights as exact bf16 splits [3, E, H]
-    float *logits = nullptr;   // split-K partial router logits [splits, T, Np]
     int *ready = nullptr;      // per-m-tile gate/up completion counters of the fused expert GEMM
     int ready_shared_base = 0; // first counter of the shared expert's m-tiles
     bool fuse_experts = true;  // gate/up and down in one persistent launch
@@ -92,6 +91,7 @@ struct moe_handle {
     unsigned long long *trace = nullptr;  // [kMaxStages][kTraceSlots] device trace (MOE_OPT_TRACE)
     bool trace_on = false;
     unsigned long long *gemm_stats = nullptr;  // [moe::kGemmStats] (MOE_OPT_TRACE)
+    unsigned long long *router_stats = nullptr;  // [moe::kRouterStats] (MOE_OPT_TRACE)
     int *wr_flags = nullptr;
     moe::RouterTcPlan rplan{};
 
@@ -198,11 +198,9 @@ void carve(moe_handle *h, void *base) {
     h->x_stage = c.take<char>(base, MT * H * elt);
     h->y_stage = c.take<char>(base, MT * H * elt);
     h->wr_parts = c.take<bf16>(base, 3 * E * H);
-    // split-K keeps splits * T <= max(max_tokens, 128 * SMs) rows
-    const size_t lrows = MT > (size_t)h->num_sms * 128 ? MT : (size_t)h->num_sms * 128;
-    h->logits = c.take<float>(base, lrows * ((E + 31) / 32 * 32));
     h->trace = c.take<unsigned long long>(base, MOE_TRACE_FIELDS * moe_handle::kMaxStages);
     h->gemm_stats = c.take<unsigned long long>(base, moe::kGemmStats);
+    h->router_stats = c.take<unsigned long long>(base, moe::kRouterStats);
     // routed m-tiles number at most T*k/128 + E; the shared expert's follow
     h->ready_shared_base = (int)(MT * k / 128 + E + 1);
     h->ready = c.take<int>(base, (size_t)h->ready_shared_base + (MT + 127) / 128 + 1);
@@ -306,10 +304,22 @@ moe_status x_map_box(moe_handle *h, const void *X, int T, int v, const CUtensorM
     return MOE_OK;
 }
 
-// Router for bf16 X: logits on the tensor cores, then the routing rule, one
-// warp per token.  Two launches.
+// Cluster size of the tensor-core router: the largest power of two that keeps
+// about one CTA per SM and at least one k-block per CTA, up to 8 for at most 8
+// m-tiles (the clusters then fit on the GPU at once) and 4 beyond.
+int router_splits(const moe_handle *h, int T) {
+    const int nk = h->H / 64, mtiles = (T + 127) / 128;
+    const int cap = mtiles <= 8 ? moe::kMaxRouterSplits : 4;
+    int want = h->num_sms / mtiles, sp = 1;
+    while (sp * 2 <= want && sp * 2 <= cap && sp * 2 <= nk) sp *= 2;
+    return sp;
+}
+
+// Router for bf16 X: logits on the tensor cores and the routing rule, one
+// launch (clusters of router_splits CTAs per m-tile).  Token blocks of the
+// histograms hold 128 / router_splits tokens.
 moe_status run_router_tc(moe_handle *h, const void *X, int T, int32_t *topk_idx, float *topk_w,
-                         int32_t *blk_hist, cudaStream_t s, int *n, int tile_m) {
+                         int32_t *blk_hist, cudaStream_t s, int *n) {
     moe_status st = x_map(h, X, T);
     if (st != MOE_OK) return st;
     moe::RouterTcArgs ra{};
@@ -322,51 +332,34 @@ moe_status run_router_tc(moe_handle *h, const void *X, int T, int32_t *topk_idx,
     ra.parts = h->rplan.parts;
     ra.stages = h->rplan.stages;
     ra.tmem_cols = h->rplan.tmem_cols;
-    ra.logits = h->logits;
+    ra.splits = router_splits(h, T);
+    ra.staged_push = h->rplan.staged_push;
+    ra.kb_per_split = (h->H / 64 + ra.splits - 1) / ra.splits;
+    ra.k = h->k;
+    ra.bias = h->w.expert_bias;
+    ra.score_func = h->cfg.score_func;
+    ra.route_norm = h->cfg.route_norm;
+    ra.route_scale = h->cfg.route_scale;
+    ra.topk_idx = topk_idx;
+    ra.topk_w = topk_w;
+    ra.blk_hist = blk_hist;
+    ra.hb = 1;  // expert-major histograms: each expert's blocks are contiguous
+    ra.he = h->hist_stride;
     ra.err = h->err;
     ra.wait_ns = h->wait_ns;
     ra.trace = trace_slot(h, *n);
-    {
-        // split the H reduction so that about one CTA runs per SM
-        const int nk = h->H / 64, mtiles = (T + 127) / 128;
-        int want = h->num_sms / mtiles;
-        want = want < 1 ? 1 : (want > moe::kMaxRouterSplits ? moe::kMaxRouterSplits : want);
-        ra.kb_per_split = (nk + want - 1) / want;
-    }
-    const int splits = (h->H / 64 + ra.kb_per_split - 1) / ra.kb_per_split;
-
-    st = launched(h, moe::launch_router_tc(ra, h->rplan.smem, s), "router_logits", n, s);
-    if (st != MOE_OK) return st;
-    moe::TopkArgs ta{};
-    ta.logits = h->logits;
-    ta.ld = h->rplan.Np;
-    ta.splits = splits;
-    ta.hb = 1;  // expert-major histograms: each expert's blocks are contiguous
-    ta.he = h->hist_stride;
-    ta.T = T;
-    ta.E = h->E;
-    ta.k = h->k;
-    ta.bias = h->w.expert_bias;
-    ta.score_func = h->cfg.score_func;
-    ta.route_norm = h->cfg.route_norm;
-    ta.route_scale = h->cfg.route_scale;
-    ta.topk_idx = topk_idx;
-    ta.topk_w = topk_w;
-    ta.blk_hist = blk_hist;
-    ta.trace = trace_slot(h, *n);
-    return launched(h, moe::launch_topk(ta, moe::topk_tokens_per_block(h->E, T, h->num_sms), s), "router_topk",
-                    n, s);
+    ra.stats = h->trace_on ? h->router_stats : nullptr;
+    return launched(h, moe::launch_router_tc(ra, h->rplan.smem, s), "router", n, s);
 }
 
 // Router + dispatch, shared by all paths (tile_m: rows per tile counted by
 // tile_offs).  Returns launches through *n.
 moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n, int tile_m) {
-    // bf16 X: tensor-core logits + grouped-lane top-k; fp32 X: CUDA-core router
-    const int TT = h->x_f32 ? moe::router_tokens_per_block(T, h->num_sms)
-                            : moe::topk_tokens_per_block(h->E, T, h->num_sms);
+    // bf16 X: tensor-core router; fp32 X: CUDA-core router
+    const int TT = h->x_f32 ? moe::router_tokens_per_block(T, h->num_sms) : 128 / router_splits(h, T);
     const int nb = (T + TT - 1) / TT;
     if (!h->x_f32) {
-        moe_status st = run_router_tc(h, X, T, h->topk_idx, h->topk_w, h->blk_hist, s, n, tile_m);
+        moe_status st = run_router_tc(h, X, T, h->topk_idx, h->topk_w, h->blk_hist, s, n);
         if (st != MOE_OK) return st;
     } else {
     moe::RouterArgs ra{};
@@ -623,6 +616,8 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
         cudaError_t e =
             cudaMemsetAsync(h->trace, 0xff, MOE_TRACE_FIELDS * moe_handle::kMaxStages * sizeof(unsigned long long), s);
         if (e == cudaSuccess) e = cudaMemsetAsync(h->gemm_stats, 0, moe::kGemmStats * sizeof(unsigned long long), s);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(h->router_stats, 0, moe::kRouterStats * sizeof(unsigned long long), s);
         if (e != cudaSuccess) return cuda_fail(e, "trace reset");
     }
     mark(h, 0, s);
@@ -746,7 +741,7 @@ moe_status moe_route(moe_handle *h, const void *X, int T, int32_t *topk_idx, flo
     if (!h->x_f32) {
         int n = 0;
         moe_status st =
-            run_router_tc(h, X, T, topk_idx, topk_w, nullptr, reinterpret_cast<cudaStream_t>(stream), &n, 0);
+            run_router_tc(h, X, T, topk_idx, topk_w, nullptr, reinterpret_cast<cudaStream_t>(stream), &n);
         h->last_launches = n;
         return st;
     }
@@ -943,6 +938,7 @@ moe_status moe_inspect(const moe_handle *h, int buffer, void *dst, size_t bytes,
     case MOE_BUF_SLOT: src = h->slot_of; cap = MT * k * 4; break;
     case MOE_BUF_HIDDEN: src = h->hbuf; cap = MT * k * h->I * 2; break;
     case MOE_BUF_GEMM_STATS: src = h->gemm_stats; cap = moe::kGemmStats * 8; break;
+    case MOE_BUF_ROUTER_STATS: src = h->router_stats; cap = moe::kRouterStats * 8; break;
     default: return fail(MOE_ERR_INVALID_ARG, "unknown buffer %d", buffer);
     }
     if (bytes > cap) return fail(MOE_ERR_INVALID_ARG, "%zu bytes requested, buffer holds %zu", bytes, cap);

@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "routing.cuh"
 
 namespace moe {
 namespace {
@@ -37,122 +38,6 @@ __device__ __forceinline__ void load8_as_f32(const void *X, int x_f32, size_t of
         const uint4 r = __ldg(reinterpret_cast<const uint4 *>(static_cast<const bf16 *>(X) + off));
         v[0] = bf16_lo(r.x); v[1] = bf16_hi(r.x); v[2] = bf16_lo(r.y); v[3] = bf16_hi(r.y);
         v[4] = bf16_lo(r.z); v[5] = bf16_hi(r.z); v[6] = bf16_lo(r.w); v[7] = bf16_hi(r.w);
-    }
-}
-
-__device__ __forceinline__ bool better(float c, int e, float bc, int be) {
-    return c > bc || (c == bc && e < be);
-}
-
-// The routing rule for one token, by a group of LPT consecutive lanes: lane
-// `sub` of the group holds the logits of experts sub, sub+LPT, ... in lg[0..7]
-// (E <= 8*LPT).  s = sigmoid(l) (or softmax over e); k times, the largest
-// s + bias among the experts not chosen yet (equal values: lower expert index)
-// is chosen; weights from the unbiased s, renormalised when route_norm is set,
-// then times route_scale.  Every lane of the warp must call it (shuffles);
-// only groups with `valid` write slots (lane sub writes slots r = sub mod LPT)
-// and count the chosen experts in hist (shared memory) when it is given.
-template <int LPT>
-__device__ __forceinline__ void route_token_group(const float (&lg)[8], int sub, bool valid, int t, int E,
-                                                  int k, const float *bias, int score_func, int route_norm,
-                                                  float route_scale, int32_t *topk_idx, float *topk_w,
-                                                  int *hist) {
-    float s[8], c[8];
-    if (score_func == 1) {
-        float m = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (sub + LPT * j < E) m = fmaxf(m, lg[j]);
-#pragma unroll
-        for (int o = LPT / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o, LPT));
-        float z = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            s[j] = (sub + LPT * j < E) ? expf(lg[j] - m) : 0.f;
-            z += s[j];
-        }
-#pragma unroll
-        for (int o = LPT / 2; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o, LPT);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s[j] = s[j] / z;
-    } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s[j] = 1.0f / (1.0f + expf(-lg[j]));
-    }
-    uint32_t open = 0;  // bit j: expert sub + LPT*j is still a candidate
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int e = sub + LPT * j;
-        if (e < E) {
-            const float cj = s[j] + (bias ? __ldg(bias + e) : 0.f);
-            c[j] = (cj != cj) ? -INFINITY : cj;  // NaN never wins
-            open |= 1u << j;
-        } else {
-            c[j] = -INFINITY;
-        }
-    }
-    // Slot r is kept by lane r mod LPT of the group (entry r / LPT of its
-    // own[] arrays), so the k rounds compile to one loop body: the routing
-    // kernels run once per forward with a cold instruction cache.
-    constexpr int kOwn = (16 + LPT - 1) / LPT;
-    float own_s[kOwn];
-    int own_e[kOwn];
-#pragma unroll
-    for (int q = 0; q < kOwn; ++q) {
-        own_s[q] = 0.f;
-        own_e[q] = 0;
-    }
-    float wsum = 0.f;
-#pragma unroll 1
-    for (int r = 0; r < k; ++r) {
-        float bc = -INFINITY;
-        int be = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if ((open >> j & 1u) && better(c[j], sub + LPT * j, bc, be)) {
-                bc = c[j];
-                be = sub + LPT * j;
-            }
-#pragma unroll
-        for (int o = LPT / 2; o > 0; o >>= 1) {
-            const float oc = __shfl_xor_sync(0xffffffffu, bc, o, LPT);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o, LPT);
-            if (better(oc, oe, bc, be)) {
-                bc = oc;
-                be = oe;
-            }
-        }
-        const int owner = be & (LPT - 1), jj = be / LPT;
-        float sv = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (j == jj) sv = s[j];
-        if (sub == owner) open &= ~(1u << jj);
-        sv = __shfl_sync(0xffffffffu, sv, owner, LPT);
-        wsum += sv;
-        if ((r & (LPT - 1)) == sub) {
-            const int qr = r / LPT;
-#pragma unroll
-            for (int q = 0; q < kOwn; ++q)
-                if (q == qr) {
-                    own_s[q] = sv;
-                    own_e[q] = be;
-                }
-        }
-    }
-    if (valid) {
-#pragma unroll
-        for (int q = 0; q < kOwn; ++q) {
-            const int r = sub + LPT * q;
-            if (r < k) {
-                float w = own_s[q];
-                if (route_norm) w = w / wsum;
-                w = w * route_scale;
-                topk_idx[(size_t)t * k + r] = own_e[q];
-                topk_w[(size_t)t * k + r] = w;
-                if (hist != nullptr) atomicAdd(&hist[own_e[q]], 1);
-            }
-        }
     }
 }
 
@@ -316,47 +201,6 @@ __device__ void dispatch_scan_block(int32_t *blk_hist, int nb, int E, int hb, in
             carry += __shfl_sync(0xffffffffu, inc, 31);
         }
     }
-}
-
-// Routing rule from the fp32 logits of the tensor-core router (partial sums of
-// its split-K CTAs, added in split order): LPT lanes per token, 8 experts per
-// lane, blockDim.x / LPT tokens per CTA, expert histogram per CTA.
-template <int LPT>
-__global__ void __launch_bounds__(1024) topk_kernel(const TopkArgs a) {
-    __shared__ int hist[256];
-    const int E = a.E, sub = threadIdx.x & (LPT - 1), grp = threadIdx.x / LPT;
-    const int TT = blockDim.x / LPT;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
-    trace_mark(a.trace, 0);
-    pdl_wait();
-    trace_mark(a.trace, 1);
-    pdl_trigger();
-    __syncthreads();
-    const int t = blockIdx.x * TT + grp;
-    const bool valid = t < a.T;
-    float l[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) l[j] = 0.f;
-    if (valid) {
-#pragma unroll
-        for (int z = 0; z < kMaxRouterSplits; ++z)
-            if (z < a.splits) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int e = sub + LPT * j;
-                    if (e < E) l[j] += __ldg(a.logits + ((size_t)z * a.T + t) * a.ld + e);
-                }
-            }
-    }
-    route_token_group<LPT>(l, sub, valid, t, E, a.k, a.bias, a.score_func, a.route_norm, a.route_scale,
-                           a.topk_idx, a.topk_w, a.blk_hist ? hist : nullptr);
-    if (a.blk_hist != nullptr) {
-        __syncthreads();
-        for (int e = threadIdx.x; e < E; e += blockDim.x)
-            a.blk_hist[(size_t)blockIdx.x * a.hb + (size_t)e * a.he] = hist[e];
-    }
-    __syncthreads();
-    trace_exit(a.trace);
 }
 
 size_t router_smem(int TT, int E) { return (size_t)(TT + E) * kPad * 4 + (size_t)E * 4; }
@@ -583,42 +427,6 @@ cudaError_t launch_router(const RouterArgs &a, cudaStream_t s) {
     const size_t smem = router_smem(TT, a.E);
     if (TT == 32) return launch_pdl(router_kernel<32>, dim3(nb), dim3(kRouterThreads), smem, s, a);
     return launch_pdl(router_kernel<16>, dim3(nb), dim3(kRouterThreads), smem, s, a);
-}
-
-static int topk_lpt(int E) {
-    int l = 2;
-    while (l * 8 < E) l <<= 1;
-    return l;
-}
-
-int topk_tokens_per_block(int E, int T, int num_sms) {
-    // spread the tokens over the SMs: tokens per CTA = next power of two of
-    // T / SMs, within [8 (and a full warp), min(128, 1024 / LPT)]
-    const int lpt = topk_lpt(E);
-    int want = (T + num_sms - 1) / num_sms, tt = 1;
-    while (tt < want) tt <<= 1;
-    const int lo = 32 / lpt > 8 ? 32 / lpt : 8, hi = 1024 / lpt < 128 ? 1024 / lpt : 128;
-    return tt < lo ? lo : (tt > hi ? hi : tt);
-}
-
-cudaError_t launch_topk(const TopkArgs &a, int tokens_per_block, cudaStream_t s) {
-    static std::once_flag once;
-    std::call_once(once, [] {
-        max_smem_carveout(topk_kernel<2>);
-        max_smem_carveout(topk_kernel<4>);
-        max_smem_carveout(topk_kernel<8>);
-        max_smem_carveout(topk_kernel<16>);
-        max_smem_carveout(topk_kernel<32>);
-    });
-    const int lpt = topk_lpt(a.E), tt = tokens_per_block;
-    const dim3 grid((a.T + tt - 1) / tt), block(tt * lpt);
-    switch (lpt) {
-    case 2: return launch_pdl(topk_kernel<2>, grid, block, 0, s, a);
-    case 4: return launch_pdl(topk_kernel<4>, grid, block, 0, s, a);
-    case 8: return launch_pdl(topk_kernel<8>, grid, block, 0, s, a);
-    case 16: return launch_pdl(topk_kernel<16>, grid, block, 0, s, a);
-    default: return launch_pdl(topk_kernel<32>, grid, block, 0, s, a);
-    }
 }
 
 cudaError_t launch_scan(const ScanArgs &a, cudaStream_t s) {

@@ -220,12 +220,17 @@ typedef enum {
     MOE_BUF_SORTED_TOKEN = 3, /* [T * k] int32: token of each expert-sorted row */
     MOE_BUF_SLOT = 4,         /* [T * k] int32: sorted row of routing slot (t, j) */
     MOE_BUF_HIDDEN = 5,       /* [T * k, I] bf16: act(gate, up) of each sorted row */
-    MOE_BUF_GEMM_STATS = 6    /* [8] uint64, with MOE_OPT_TRACE on and the fused expert GEMM: ns
+    MOE_BUF_GEMM_STATS = 6,   /* [8] uint64, with MOE_OPT_TRACE on and the fused expert GEMM: ns
                                  summed over its CTAs of: producer waiting for a free stage,
                                  producer waiting for gate/up rows, MMA waiting for data, MMA
                                  waiting for an accumulator, epilogue waiting for an accumulator,
                                  epilogue working, CTA time past the dependency wait; then the
                                  number of tiles */
+    MOE_BUF_ROUTER_STATS = 7  /* [8] uint64, with MOE_OPT_TRACE on and the tensor-core router: ns
+                                 summed over its CTAs of: main loop, first cluster barrier,
+                                 pushing the partial logits to the routing CTAs with the second
+                                 barrier, adding them and routing, histogram; then the number of
+                                 CTAs */
 } moe_buffer;
 
 /* Copy `bytes` of an internal buffer, as the last forward left it, to the
