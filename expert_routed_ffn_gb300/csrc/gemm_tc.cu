@@ -12,8 +12,10 @@
 // projections share a launch, a down tile first waits until every gate/up
 // tile of its 128 rows has been stored (a per-m-tile counter), so the down
 // tiles of early experts overlap the gate/up tail and the second launch's ramp
-// disappears.  Gate/up tiles never wait and every CTA walks its tiles in
-// increasing order with all CTAs resident (one per SM), so the waits end.
+// disappears.  Gate/up tiles never wait, tiles are claimed in increasing
+// order, and each CTA's roles take its tiles in claim order with all CTAs
+// resident (one per SM): a down tile only waits for tiles claimed before it,
+// which do not wait, so the waits end.
 //
 // Persistent kernel, one CTA per SM, 6 warps:
 //   warp 0     TMA producer: A tile 128 x 64 and B tile 256 x 64 (gate/up: 128
@@ -24,9 +26,11 @@
 //              main loop of the next
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
 //              32*(w%4)..+31 = tile rows), activation (gate/up), bf16 stores
-// Tiles are (segment, group, m-tile, n-tile), handed out round-robin; inside a
-// group the m-tiles of one n-tile are adjacent so concurrent CTAs share the
-// weight tile in L2.  Every wait is bounded: on timeout the kernel records
+// Tiles are (segment, group, m-tile, n-tile) in a fixed order; the producer
+// claims them from a launch-wide ticket (the CTA that is free first takes the
+// next tile) and passes each id to the MMA and epilogue warps through a ring
+// in shared memory.  Inside a group the m-tiles of one n-tile are adjacent so
+// concurrent CTAs share the weight tile in L2.  Every wait is bounded: on timeout the kernel records
 // ERR_TIMEOUT, stops all roles, drains its in-flight copies and MMAs, frees
 // TMEM and returns.
 #include <mutex>
@@ -44,7 +48,8 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;             // two 128 x 256 fp32 accumulators
 constexpr uint64_t kDrainNs = 1000000000ull;    // bound of the drain after an abort
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kRing = 8;                        // tile ids in flight from the producer to the other roles
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers, tile ring*/;
 
 struct Tile {
     int seg, group, mt, nt, row0, m_valid, ready;  // ready: m-tile index for signal / wait
@@ -143,14 +148,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const uint32_t sB = sA + kStages * kABytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
     const uint32_t bar0 = smem_u32(bars);
-    // barriers: full[kStages], empty[kStages], tfull[2], tempty[2], drain
+    // barriers: full[kStages], empty[kStages], tfull[2], tempty[2], drain, ring_full[kRing], ring_empty[kRing]
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
     auto tfull_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kStages + a); };
     auto tempty_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kStages + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 5);
+    auto ring_full = [&](int i) { return bar0 + 8u * (2 * kStages + 5 + i); };
+    auto ring_empty = [&](int i) { return bar0 + 8u * (2 * kStages + 5 + kRing + i); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 5 + 2 * kRing);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *ring = reinterpret_cast<volatile int *>(tmem_slot + 2);  // [kRing] tile ids
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     trace_mark(p.trace, 0);
@@ -164,6 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             mbar_init(tempty_bar(a), 128);
         }
         mbar_init(drain_bar, 1);
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(ring_full(i), 1);
+            mbar_init(ring_empty(i), 2);  // the MMA thread and the epilogue have read the id
+        }
         fence_mbar_init();
         *abort_flag = 0;
     }
@@ -212,10 +224,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t L = 0;  // loads issued so far; stage = L % kStages
             bool ok = true;
             uint64_t w_empty = 0, w_dep = 0;
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            // tiles: claimed in order from the launch-wide ticket, or round-robin.  The
+            // next tile is claimed three k-blocks before the current one's loads end,
+            // so the atomic's latency hides behind them while the claim stays late.
+            int next = p.tile_counter ? atomicAdd(p.tile_counter, 1) : (int)blockIdx.x;
+            for (int n = 0;; ++n) {
+                const int tile = next < total ? next : total;  // total: the end marker
+                const int slot = n % kRing;
+                if (!mbar_wait(ring_empty(slot), ((n / kRing) & 1u) ^ 1u, p.wait_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ring[slot] = tile;
+                mbar_arrive(ring_full(slot));
+                if (tile >= total) break;
                 const Tile t = decode_tile(p, tile, s_seg_end, s_offs, s_toffs);
                 const GemmSegment &sg = p.seg[t.seg];
                 const int g = sg.group_base + t.group;
+                const int claim_at = sg.k_blocks > 3 ? sg.k_blocks - 3 : 0;
                 if (sg.wait != nullptr) {  // A rows written earlier in this launch
                     const uint64_t t0 = stats ? global_timer_ns() : 0;
                     if (!wait_counter(sg.wait + t.ready, sg.wait_count, p.wait_ns, abort_flag)) {
@@ -231,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 for (int kb = 0; kb < sg.k_blocks; ++kb) {
                     const int s = L % kStages;
                     const uint32_t ph = (L / kStages) & 1u;
+                    if (kb == claim_at) next = p.tile_counter ? atomicAdd(p.tile_counter, 1) : tile + (int)gridDim.x;
                     const uint64_t t0 = stats ? global_timer_ns() : 0;
                     if (!mbar_wait(empty_bar(s), ph ^ 1u, p.wait_ns, abort_flag)) {
                         ok = false;
@@ -248,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     }
                     ++L;
                 }
+                if (!ok) break;
             }
             if (stats) {
                 atomicAdd(stats + 0, (unsigned long long)w_empty);
@@ -269,7 +297,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t L = 0, n_acc = 0;
             bool ok = true, issued = false;
             uint64_t w_full = 0, w_acc = 0;
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            for (int n = 0; ok; ++n) {
+                const int slot = n % kRing;
+                if (!mbar_wait(ring_full(slot), (n / kRing) & 1u, p.wait_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int tile = ring[slot];
+                mbar_arrive(ring_empty(slot));
+                if (tile >= total) break;
                 const Tile t = decode_tile(p, tile, s_seg_end, s_offs, s_toffs);
                 const GemmSegment &sg = p.seg[t.seg];
                 const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
@@ -323,13 +359,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const int r = q * 32 + lane;
         uint32_t n_acc = 0;
         uint64_t w_tfull = 0, w_work = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        for (int n = 0;; ++n) {
+            const int slot = n % kRing;
+            const uint64_t t0 = stats ? global_timer_ns() : 0;
+            const bool have = __all_sync(0xffffffffu, mbar_wait(ring_full(slot), (n / kRing) & 1u, p.wait_ns, abort_flag));
+            const int tile = have ? ring[slot] : total;
+            // all four epilogue warps agree to go on or stop (they share barrier 1), and
+            // have read the id before it is released; the tcgen05.ld below is .sync.aligned
+            if (!epi_all(have)) {
+                if (lane == 0) raise_abort(p.err, abort_flag);
+                break;
+            }
+            if (q == 0 && lane == 0) mbar_arrive(ring_empty(slot));
+            if (tile >= total) break;
             const Tile t = decode_tile(p, tile, s_seg_end, s_offs, s_toffs);
             const GemmSegment &sg = p.seg[t.seg];
             const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
-            // all four epilogue warps agree to go on or stop (they share barrier 1);
-            // the tcgen05.ld below is .sync.aligned
-            const uint64_t t0 = stats ? global_timer_ns() : 0;
             const bool ready = __all_sync(0xffffffffu, mbar_wait(tfull_bar(a), aph, p.wait_ns, abort_flag));
             const uint64_t t1 = stats ? global_timer_ns() : 0;
             w_tfull += t1 - t0;

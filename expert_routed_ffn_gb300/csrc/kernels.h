@@ -151,6 +151,7 @@ struct ScatterArgs {
     // and ready[ready_shared_base, + ready_shared_count)
     int *ready;
     int ready_shared_base, ready_shared_count;
+    int *tile_counters;    // [2] tile tickets of the expert GEMM launches, zeroed by CTA (0, 0), or nullptr
     unsigned long long *trace;
     int T, k, E, H;
     int tokens_per_block;     // <= 128: the router's blocking
@@ -217,6 +218,7 @@ struct GemmArgs {
     int *err;
     unsigned long long wait_ns;
     int num_ctas;
+    int *tile_counter;     // zeroed ticket: tiles claimed in order (dynamic); nullptr: round-robin
     unsigned long long *trace;
     // nullptr, or kGemmStats ns sums over CTAs: producer waiting for a free
     // stage, producer waiting for gate/up rows, MMA waiting for data, MMA

@@ -82,6 +82,7 @@ struct moe_handle {
     int *err = nullptr;
     bf16 *wr_parts = nullptr;  // router weights as exact bf16 splits [3, E, H]
     int *ready = nullptr;      // per-m-tile gate/up completion counters of the fused expert GEMM
+    int *tile_counters = nullptr;  // [2] tile tickets of the expert GEMM launches
     int ready_shared_base = 0; // first counter of the shared expert's m-tiles
     bool fuse_experts = true;  // gate/up and down in one persistent launch
     bool prefetch_opt = true;  // L2 prefetch of expert weights during routing
@@ -205,6 +206,7 @@ void carve(moe_handle *h, void *base) {
     h->ready_shared_base = (int)(MT * k / 128 + E + 1);
     h->ready = c.take<int>(base, (size_t)h->ready_shared_base + (MT + 127) / 128 + 1);
     h->wr_flags = c.take<int>(base, 64);
+    h->tile_counters = c.take<int>(base, 64);
     h->ws_bytes = round_up(c.off, 256);
 }
 
@@ -400,6 +402,7 @@ moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n
     xa.ready = h->ready;
     xa.ready_shared_base = h->ready_shared_base;
     xa.ready_shared_count = (T + 127) / 128;
+    xa.tile_counters = h->tile_counters;
     xa.T = T;
     xa.k = h->k;
     xa.E = h->E;
@@ -477,6 +480,7 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         g.seg[ns++] = dn;
         if (h->has_shared) g.seg[ns++] = sdn;
         g.num_segs = ns;
+        g.tile_counter = h->tile_counters;
         g.trace = trace_slot(h, *n);
         g.stats = h->trace_on ? h->gemm_stats : nullptr;
         return launched(h, moe::launch_gemm_tc(g, s), "experts_gemm", n, s);
@@ -487,6 +491,7 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         g.seg[1] = sgu;
         g.num_segs = 2;
     }
+    g.tile_counter = h->tile_counters;
     g.trace = trace_slot(h, *n);
     moe_status st = launched(h, moe::launch_gemm_tc(g, s), "gate_up_gemm", n, s);
     if (st != MOE_OK) return st;
@@ -496,6 +501,7 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         g.seg[1] = sdn;
         g.num_segs = 2;
     }
+    g.tile_counter = h->tile_counters + 1;
     g.trace = trace_slot(h, *n);
     return launched(h, moe::launch_gemm_tc(g, s), "down_gemm", n, s);
 }
