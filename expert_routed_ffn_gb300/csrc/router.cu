@@ -243,7 +243,9 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
     trace_mark(a.trace, 0);
     pdl_wait();
     trace_mark(a.trace, 1);
-    pdl_trigger();
+    // the expert GEMM is launched only when every CTA has reached the end of its
+    // gather (launch_dependents below): launched earlier, its one-per-SM CTAs
+    // would take the shared memory that this grid's later waves need
     __syncthreads();
     {
         // eight independent loads in flight per thread, then the shared sums
@@ -335,24 +337,38 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
         slot_s[i] = slot;
     }
     __syncthreads();
-    const int nw = kScatterThreads / 32;
+    // row copy: a warp per row, each lane up to kG 16-byte chunks in flight
+    // (all loads of a batch before its stores)
+    constexpr int kG = 8;
+    const int nw = kScatterThreads / 32, chunks = H / 8;
     for (int i = blockIdx.y * nw + warp; i < n; i += gridDim.y * nw) {
         const int slot = slot_s[i];
         if (slot < 0) continue;
         const size_t src = (size_t)(tok0 + i / k) * H, dst = (size_t)slot * H;
-        for (int c = lane * 8; c < H; c += 256) {
-            uint4 o;
-            if (a.x_f32) {
-                float v[8];
-                load8_as_f32(a.X, 1, src + c, v);
-                o.x = pack_bf16x2(v[0], v[1]); o.y = pack_bf16x2(v[2], v[3]);
-                o.z = pack_bf16x2(v[4], v[5]); o.w = pack_bf16x2(v[6], v[7]);
-            } else {
-                o = __ldg(reinterpret_cast<const uint4 *>(static_cast<const bf16 *>(a.X) + src + c));
+        for (int c0 = lane; c0 < chunks; c0 += 32 * kG) {
+            uint4 o[kG];
+#pragma unroll
+            for (int u = 0; u < kG; ++u) {
+                const int c = c0 + 32 * u;
+                if (c >= chunks) break;
+                if (a.x_f32) {
+                    float v[8];
+                    load8_as_f32(a.X, 1, src + 8 * c, v);
+                    o[u].x = pack_bf16x2(v[0], v[1]); o[u].y = pack_bf16x2(v[2], v[3]);
+                    o[u].z = pack_bf16x2(v[4], v[5]); o[u].w = pack_bf16x2(v[6], v[7]);
+                } else {
+                    o[u] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const bf16 *>(a.X) + src + 8 * c));
+                }
             }
-            *reinterpret_cast<uint4 *>(a.x_sorted + dst + c) = o;
+#pragma unroll
+            for (int u = 0; u < kG; ++u) {
+                const int c = c0 + 32 * u;
+                if (c >= chunks) break;
+                *reinterpret_cast<uint4 *>(a.x_sorted + dst + 8 * c) = o[u];
+            }
         }
     }
+    pdl_trigger();
     __syncthreads();
     trace_exit(a.trace);
 }
