@@ -26,6 +26,7 @@ MOE_ACT_SILU, MOE_ACT_SWIGLU_OAI = 0, 1
 MOE_DTYPE_BF16, MOE_DTYPE_F32 = 0, 1
 MOE_OPT_PATH, MOE_OPT_WAIT_LIMIT_NS, MOE_OPT_STAGE_EVENTS, MOE_OPT_FUSE_EXPERTS, MOE_OPT_PREFETCH = 0, 1, 2, 3, 4
 MOE_OPT_TRACE = 5
+MOE_OPT_GEMM_PAIR = 6
 MOE_BUF_GEMM_STATS = 6
 MOE_BUF_ROUTER_STATS = 7
 TRACE_FIELDS = 5  # first begin, first ready, last ready, first end, last end

@@ -41,41 +41,62 @@
 namespace moe {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kABytes = kGemmBM * kGemmBK * 2;  // 16 KB
-constexpr int kBBytes = kGemmBN * kGemmBK * 2;  // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;             // two 128 x 256 fp32 accumulators
 constexpr uint64_t kDrainNs = 1000000000ull;    // bound of the drain after an abort
+constexpr uint64_t kPairDrainNs = 1000000ull;   // CTA pair: grace for the copies in flight after an abort
 constexpr int kRing = 8;                        // tile ids in flight from the producer to the other roles
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers, tile ring*/;
+
+// Per-variant layout.  One CTA: stage = one k-block of 64, A 128 x 64 + B
+// 256 x 64 (48 KB), 4 stages.  CTA pair: each CTA stages its own 128 A rows and
+// half of B (128 rows), two k-blocks per stage loaded as one box each (A and B
+// 32 KB: larger copies keep a CTA's TMA stream near the MMA's rate), 3 stages;
+// a tile is 256 rows (128 per CTA).  A stage holds kKB consecutive 16 KB
+// (A) and kBBytes / kKB (B) k-block tiles.
+template <bool PAIR>
+struct GemmCfg {
+    static constexpr int kKB = PAIR ? 2 : 1;     // k-blocks per stage
+    static constexpr int kStages = PAIR ? 3 : 4;
+    static constexpr int kBBytes = (PAIR ? kGemmBN / 2 : kGemmBN) * kGemmBK * 2 * kKB;
+    static constexpr int kAStage = kABytes * kKB;
+    static constexpr int kStageBytes = kAStage + kBBytes;
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers, tile ring*/;
+    static constexpr int kBM = PAIR ? 2 * kGemmBM : kGemmBM;  // rows per tile
+};
 
 struct Tile {
-    int seg, group, mt, nt, row0, m_valid, ready;  // ready: m-tile index for signal / wait
+    int seg, group, mt, nt, row0, m_valid, ready;  // row0, m_valid: this CTA's rows; ready: its m-tile's counter
 };
 
 // offs / toffs: shared-memory copies of the grouped segments' dispatch offsets
+// (toffs counts tiles of BM rows)
+template <int BM>
 __device__ __forceinline__ int seg_tiles(const GemmSegment &s, const int *toffs) {
-    if (s.dense) return ((s.m_dense + kGemmBM - 1) / kGemmBM) * s.n_tiles;
+    if (s.dense) return ((s.m_dense + BM - 1) / BM) * s.n_tiles;
     return toffs[s.num_groups] * s.n_tiles;
 }
 
+// Tile -> segment, group, m-tile, n-tile.  With CTA pairs (BM = 256) the CTA of
+// cluster rank `half` takes rows [128 * half, 128 * half + 128) of the tile, and
+// the per-128-row counters are numbered 2 * m-tile + half.
+template <int BM>
 __device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, const int *seg_end, const int *offs,
-                                            const int *toffs) {
+                                            const int *toffs, int half) {
     Tile t;
     t.seg = 0;
     while (t.seg + 1 < p.num_segs && tile >= seg_end[t.seg]) ++t.seg;
     if (t.seg > 0) tile -= seg_end[t.seg - 1];
     const GemmSegment &s = p.seg[t.seg];
+    constexpr int kSub = BM / kGemmBM;  // 128-row parts of a tile
     if (s.dense) {
-        const int mtiles = (s.m_dense + kGemmBM - 1) / kGemmBM;
+        const int mtiles = (s.m_dense + BM - 1) / BM;
         t.group = 0;
         t.nt = tile / mtiles;
         t.mt = tile % mtiles;
-        t.row0 = t.mt * kGemmBM;
+        t.row0 = t.mt * BM + half * kGemmBM;
         t.m_valid = min(kGemmBM, s.m_dense - t.row0);
-        t.ready = s.ready_base + t.mt;
+        t.ready = s.ready_base + kSub * t.mt + half;
     } else {
         // largest group whose first tile is <= tile (empty groups own no tiles)
         int lo = 0, hi = s.num_groups - 1;
@@ -92,9 +113,9 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, const i
         t.nt = local / mt_g;
         t.mt = local % mt_g;
         const int start = offs[lo];
-        t.row0 = start + t.mt * kGemmBM;
-        t.m_valid = min(kGemmBM, offs[lo + 1] - t.row0);
-        t.ready = s.ready_base + toffs[lo] + t.mt;
+        t.row0 = start + t.mt * BM + half * kGemmBM;
+        t.m_valid = min(kGemmBM, offs[lo + 1] - t.row0);  // <= 0: the odd CTA of a pair past the group's rows
+        t.ready = s.ready_base + kSub * (toffs[lo] + t.mt) + half;
     }
     return t;
 }
@@ -102,6 +123,12 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, const i
 __device__ __forceinline__ void raise_abort(int *err, volatile int *abort_flag) {
     if (err != nullptr) atomicOr(err, ERR_TIMEOUT);
     *abort_flag = 1;
+}
+// CTA pair: also stop the other CTA's roles
+__device__ __forceinline__ void raise_abort_pair(int *err, volatile int *abort_flag) {
+    raise_abort(err, abort_flag);
+    const uint32_t peer = mapa_shared(smem_u32(const_cast<int *>(abort_flag)), cluster_ctarank() ^ 1u);
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer), "r"(1u) : "memory");
 }
 
 __device__ __forceinline__ int ld_acquire(const int *p) {
@@ -140,12 +167,16 @@ __device__ __forceinline__ bool epi_all(bool v) {
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async;" ::: "memory"); }
 
+template <bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmArgs p) {
+    using C = GemmCfg<PAIR>;
+    constexpr int kStages = C::kStages, kBBytes = C::kBBytes, kStageBytes = C::kStageBytes, kBM = C::kBM;
+    constexpr int kKB = C::kKB, kAStage = C::kAStage;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t sA = smem_u32(smem);
-    const uint32_t sB = sA + kStages * kABytes;
+    const uint32_t sB = sA + kStages * kAStage;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
     const uint32_t bar0 = smem_u32(bars);
     // barriers: full[kStages], empty[kStages], tfull[2], tempty[2], drain, ring_full[kRing], ring_empty[kRing]
@@ -161,6 +192,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     volatile int *ring = reinterpret_cast<volatile int *>(tmem_slot + 2);  // [kRing] tile ids
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // CTA pair: rank 0 issues the MMAs; the full and accumulator-empty barriers
+    // that count both CTAs are rank 0's
+    const int half = PAIR ? (int)cluster_ctarank() : 0;
+    const bool leader = half == 0;
+    auto abort_all = [&]() {
+        if (PAIR)
+            raise_abort_pair(p.err, abort_flag);
+        else
+            raise_abort(p.err, abort_flag);
+    };
     trace_mark(p.trace, 0);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -169,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
         for (uint32_t a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 128);
+            mbar_init(tempty_bar(a), PAIR ? 256 : 128);  // the epilogue threads of both CTAs
         }
         mbar_init(drain_bar, 1);
         for (int i = 0; i < kRing; ++i) {
@@ -182,11 +223,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (warp == 0 && lane == 0)
         for (int m = 0; m < kGemmMaxMaps; ++m) tma_prefetch_desc(&p.maps[m]);
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // both CTAs' barriers exist before any copy or arrival crosses over
     tc_fence_after();
     // the prologue above overlaps the previous kernel; the dispatch results
     // (offsets, tile counts) and the A rows are read only after this point
@@ -210,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (threadIdx.x == 0) {
         int run = 0;
         for (int s = 0; s < p.num_segs; ++s) {
-            run += seg_tiles(p.seg[s], s_toffs);
+            run += seg_tiles<kBM>(p.seg[s], s_toffs);
             s_seg_end[s] = run;
         }
     }
@@ -227,7 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             // tiles: claimed in order from the launch-wide ticket, or round-robin.  The
             // next tile is claimed three k-blocks before the current one's loads end,
             // so the atomic's latency hides behind them while the claim stays late.
-            int next = p.tile_counter ? atomicAdd(p.tile_counter, 1) : (int)blockIdx.x;
+            const bool dyn = !PAIR && p.tile_counter != nullptr;
+            const int stride = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
+            int next = dyn ? atomicAdd(p.tile_counter, 1) : (PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x);
             for (int n = 0;; ++n) {
                 const int tile = next < total ? next : total;  // total: the end marker
                 const int slot = n % kRing;
@@ -238,10 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 ring[slot] = tile;
                 mbar_arrive(ring_full(slot));
                 if (tile >= total) break;
-                const Tile t = decode_tile(p, tile, s_seg_end, s_offs, s_toffs);
+                const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
                 const GemmSegment &sg = p.seg[t.seg];
                 const int g = sg.group_base + t.group;
-                const int claim_at = sg.k_blocks > 3 ? sg.k_blocks - 3 : 0;
+                const int claim_at = sg.k_blocks > 3 * kKB ? sg.k_blocks - 3 * kKB : 0;
                 if (sg.wait != nullptr) {  // A rows written earlier in this launch
                     const uint64_t t0 = stats ? global_timer_ns() : 0;
                     if (!wait_counter(sg.wait + t.ready, sg.wait_count, p.wait_ns, abort_flag)) {
@@ -254,24 +303,38 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const CUtensorMap *mA = &p.maps[sg.map_a];
                 const CUtensorMap *mB = &p.maps[sg.map_b0];
                 const CUtensorMap *mB2 = &p.maps[sg.map_b1];
-                for (int kb = 0; kb < sg.k_blocks; ++kb) {
+                for (int kb = 0; kb < sg.k_blocks; kb += kKB) {
                     const int s = L % kStages;
                     const uint32_t ph = (L / kStages) & 1u;
-                    if (kb == claim_at) next = p.tile_counter ? atomicAdd(p.tile_counter, 1) : tile + (int)gridDim.x;
+                    if (kb == claim_at || (kKB > 1 && kb + 1 == claim_at))
+                        next = dyn ? atomicAdd(p.tile_counter, 1) : tile + stride;
                     const uint64_t t0 = stats ? global_timer_ns() : 0;
                     if (!mbar_wait(empty_bar(s), ph ^ 1u, p.wait_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
                     if (stats) w_empty += global_timer_ns() - t0;
-                    mbar_arrive_expect_tx(full_bar(s), kStageBytes);
-                    tma_load_2d(sA + s * kABytes, mA, full_bar(s), kb * kGemmBK, t.row0);
-                    if (sg.glu) {
-                        tma_load_3d(sB + s * kBBytes, mB, full_bar(s), kb * kGemmBK, t.nt * 128, g);
-                        tma_load_3d(sB + s * kBBytes + kBBytes / 2, mB2, full_bar(s), kb * kGemmBK,
-                                    t.nt * 128, g);
+                    if (PAIR) {
+                        // both CTAs' copies complete on rank 0's full barrier; rank 0 expects their bytes.
+                        // Maps view K as (64, K / 64) so that one box brings k-blocks kb, kb + 1
+                        // (past the last k-block: zero fill, no MMA)
+                        const uint32_t fb = mapa_shared(full_bar(s), 0);
+                        if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * kStageBytes);
+                        tma_load_3d_pair(sA + s * kAStage, mA, fb, 0, t.row0, kb);
+                        if (sg.glu)  // gate rows in rank 0, up rows in rank 1: accumulator columns 0-127 / 128-255
+                            tma_load_4d_pair(sB + s * kBBytes, leader ? mB : mB2, fb, 0, t.nt * 128, kb, g);
+                        else
+                            tma_load_4d_pair(sB + s * kBBytes, mB, fb, 0, t.nt * kGemmBN + half * 128, kb, g);
                     } else {
-                        tma_load_3d(sB + s * kBBytes, mB, full_bar(s), kb * kGemmBK, t.nt * kGemmBN, g);
+                        mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+                        tma_load_2d(sA + s * kAStage, mA, full_bar(s), kb * kGemmBK, t.row0);
+                        if (sg.glu) {
+                            tma_load_3d(sB + s * kBBytes, mB, full_bar(s), kb * kGemmBK, t.nt * 128, g);
+                            tma_load_3d(sB + s * kBBytes + kBBytes / 2, mB2, full_bar(s), kb * kGemmBK,
+                                        t.nt * 128, g);
+                        } else {
+                            tma_load_3d(sB + s * kBBytes, mB, full_bar(s), kb * kGemmBK, t.nt * kGemmBN, g);
+                        }
                     }
                     ++L;
                 }
@@ -282,18 +345,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 atomicAdd(stats + 1, (unsigned long long)w_dep);
             }
             if (!ok) {
-                raise_abort(p.err, abort_flag);
-                // wait for the copies still in flight (the last load of each stage)
-                for (uint32_t i = 0; i < (uint32_t)kStages && i < L; ++i) {
-                    const uint32_t l = L - 1 - i;
-                    mbar_wait(full_bar(l % kStages), (l / kStages) & 1u, kDrainNs, nullptr);
+                abort_all();
+                if (PAIR) {
+                    // a stage's copies complete on rank 0's barrier together with the other
+                    // CTA's, which may never be issued after an abort: wait a fixed time instead
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < kPairDrainNs) __nanosleep(1000);
+                } else {
+                    // wait for the copies still in flight (the last load of each stage)
+                    for (uint32_t i = 0; i < (uint32_t)kStages && i < L; ++i) {
+                        const uint32_t l = L - 1 - i;
+                        mbar_wait(full_bar(l % kStages), (l / kStages) & 1u, kDrainNs, nullptr);
+                    }
                 }
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(kGemmBM, kGemmBN);
+        if (PAIR && !leader && lane == 0) {
+            // rank 1 issues nothing; it only releases its ring slots
+            for (int n = 0;; ++n) {
+                const int slot = n % kRing;
+                if (!mbar_wait(ring_full(slot), (n / kRing) & 1u, p.wait_ns, abort_flag)) break;
+                const int tile = ring[slot];
+                mbar_arrive(ring_empty(slot));
+                if (tile >= total) break;
+            }
+        } else if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * kGemmBM : kGemmBM, kGemmBN);
             uint32_t L = 0, n_acc = 0;
             bool ok = true, issued = false;
             uint64_t w_full = 0, w_acc = 0;
@@ -306,18 +385,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const int tile = ring[slot];
                 mbar_arrive(ring_empty(slot));
                 if (tile >= total) break;
-                const Tile t = decode_tile(p, tile, s_seg_end, s_offs, s_toffs);
+                const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
                 const GemmSegment &sg = p.seg[t.seg];
                 const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
                 const uint64_t t0 = stats ? global_timer_ns() : 0;
-                if (!mbar_wait(tempty_bar(a), aph ^ 1u, p.wait_ns, abort_flag)) {
+                if (!(PAIR ? mbar_wait_cluster(tempty_bar(a), aph ^ 1u, p.wait_ns, abort_flag)
+                           : mbar_wait(tempty_bar(a), aph ^ 1u, p.wait_ns, abort_flag))) {
                     ok = false;
                     break;
                 }
                 if (stats) w_acc += global_timer_ns() - t0;
                 tc_fence_after();
                 const uint32_t d = tmem_base + a * kGemmBN;
-                for (int kb = 0; kb < sg.k_blocks; ++kb) {
+                for (int kb = 0; kb < sg.k_blocks; kb += kKB) {
                     const int s = L % kStages;
                     const uint32_t ph = (L / kStages) & 1u;
                     const uint64_t t1 = stats ? global_timer_ns() : 0;
@@ -327,17 +407,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     }
                     if (stats) w_full += global_timer_ns() - t1;
                     tc_fence_after();
-                    const uint64_t ad = smem_desc_k128(sA + s * kABytes);
-                    const uint64_t bd = smem_desc_k128(sB + s * kBBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes per K step of 16
-                        tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    for (int j = 0; j < kKB; ++j) {
+                        if (kKB > 1 && kb + j >= sg.k_blocks) break;
+                        const uint64_t ad = smem_desc_k128(sA + s * kAStage + j * kABytes);
+                        const uint64_t bd = smem_desc_k128(sB + s * kBBytes + j * (kBBytes / kKB));
+#pragma unroll
+                        for (int kk = 0; kk < kGemmBK / 16; ++kk) {  // +32 bytes per K step of 16
+                            if (PAIR)
+                                tc_mma_bf16_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | j | kk) != 0);
+                            else
+                                tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | j | kk) != 0);
+                        }
+                    }
                     issued = true;
-                    tc_commit(empty_bar(s));  // frees the stage once these MMAs have read it
+                    // frees the stage (in both CTAs of a pair) once these MMAs have read it
+                    if (PAIR)
+                        tc_commit_pair(empty_bar(s), 3);
+                    else
+                        tc_commit(empty_bar(s));
                     ++L;
                 }
                 if (!ok) break;
-                tc_commit(tfull_bar(a));  // accumulator complete
+                if (PAIR)  // accumulator complete, in both CTAs' TMEM
+                    tc_commit_pair(tfull_bar(a), 3);
+                else
+                    tc_commit(tfull_bar(a));
                 ++n_acc;
             }
             if (stats) {
@@ -346,9 +441,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 atomicAdd(stats + 7, (unsigned long long)n_acc);
             }
             if (!ok) {
-                raise_abort(p.err, abort_flag);
+                abort_all();
                 if (issued) {
-                    tc_commit(drain_bar);
+                    if (PAIR)
+                        tc_commit_pair(drain_bar, 1);
+                    else
+                        tc_commit(drain_bar);
                     mbar_wait(drain_bar, 0, kDrainNs, nullptr);
                 }
             }
@@ -367,19 +465,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             // all four epilogue warps agree to go on or stop (they share barrier 1), and
             // have read the id before it is released; the tcgen05.ld below is .sync.aligned
             if (!epi_all(have)) {
-                if (lane == 0) raise_abort(p.err, abort_flag);
+                if (lane == 0) abort_all();
                 break;
             }
             if (q == 0 && lane == 0) mbar_arrive(ring_empty(slot));
             if (tile >= total) break;
-            const Tile t = decode_tile(p, tile, s_seg_end, s_offs, s_toffs);
+            const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
             const GemmSegment &sg = p.seg[t.seg];
             const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
-            const bool ready = __all_sync(0xffffffffu, mbar_wait(tfull_bar(a), aph, p.wait_ns, abort_flag));
+            const bool ready = __all_sync(0xffffffffu, PAIR ? mbar_wait_cluster(tfull_bar(a), aph, p.wait_ns, abort_flag)
+                                                            : mbar_wait(tfull_bar(a), aph, p.wait_ns, abort_flag));
             const uint64_t t1 = stats ? global_timer_ns() : 0;
             w_tfull += t1 - t0;
             if (!epi_all(ready)) {
-                if (lane == 0) raise_abort(p.err, abort_flag);
+                if (lane == 0) abort_all();
                 break;
             }
             tc_fence_after();
@@ -429,7 +528,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 }
             }
             tc_fence_before();
-            mbar_arrive(tempty_bar(a));
+            if (PAIR)  // rank 0's barrier counts both CTAs' epilogue threads
+                mbar_arrive_cluster(mapa_shared(tempty_bar(a), 0));
+            else
+                mbar_arrive(tempty_bar(a));
             if (sg.signal != nullptr) {
                 // publish the stored rows: proxy fence for the consumer's TMA reads,
                 // device-scope fence, all four warps done, then one release increment
@@ -449,12 +551,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // neither CTA leaves while the other may still reach its memory
     trace_exit(p.trace);
     if (stats && threadIdx.x == 0) atomicAdd(stats + 6, (unsigned long long)(global_timer_ns() - t_ready));
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -479,7 +585,7 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-size_t gemm_tc_smem_bytes() { return kSmemBytes; }
+size_t gemm_tc_smem_bytes() { return GemmCfg<false>::kSmemBytes; }
 
 CUresult encode_map_a(CUtensorMap *m, const void *ptr, int rows, int K) {
     return encode_map_a_box(m, ptr, rows, K, kGemmBM);
@@ -509,12 +615,48 @@ CUresult encode_map_b(CUtensorMap *m, const void *ptr, int groups, int rows, int
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// The same tensors viewed with K split as (64, K / 64), box of two 64-column
+// chunks: one copy brings two consecutive k-blocks, each a 128-byte-swizzled
+// [rows][64] tile, one after the other in shared memory (CTA-pair GEMM).
+CUresult encode_map_a_kb2(CUtensorMap *m, const void *ptr, int rows, int K) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t dims[3] = {(cuuint64_t)kGemmBK, (cuuint64_t)rows, (cuuint64_t)(K / kGemmBK)};
+    const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)kGemmBK * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)kGemmBK, (cuuint32_t)kGemmBM, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult encode_map_b_kb2(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t dims[4] = {(cuuint64_t)kGemmBK, (cuuint64_t)rows, (cuuint64_t)(K / kGemmBK), (cuuint64_t)groups};
+    const cuuint64_t strides[3] = {(cuuint64_t)K * 2, (cuuint64_t)kGemmBK * 2, (cuuint64_t)rows * K * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)kGemmBK, (cuuint32_t)box_rows, 2, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
     static std::once_flag once;
     std::call_once(once, [] {
-        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             GemmCfg<false>::kSmemBytes);
+        cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             GemmCfg<true>::kSmemBytes);
     });
-    return launch_pdl(gemm_tc_kernel, dim3(a.num_ctas), dim3(kThreads), kSmemBytes, s, a);
+    if (a.pair) {
+        if (a.num_ctas < 2 || (a.num_ctas & 1) || a.tile_counter != nullptr) return cudaErrorInvalidValue;
+        return launch_pdl_cluster(gemm_tc_kernel<true>, dim3(a.num_ctas), dim3(kThreads),
+                                  (size_t)GemmCfg<true>::kSmemBytes, s, dim3(2, 1, 1), a);
+    }
+    return launch_pdl(gemm_tc_kernel<false>, dim3(a.num_ctas), dim3(kThreads), (size_t)GemmCfg<false>::kSmemBytes,
+                      s, a);
 }
 
 }  // namespace moe

@@ -150,6 +150,7 @@ struct ScatterArgs {
     // CTA (0, 0) zeroes the fused expert GEMM's counters: ready[0, routed m-tiles)
     // and ready[ready_shared_base, + ready_shared_count)
     int *ready;
+    int ready_per_tile;    // counters per routed tile of tile_m rows (2 with CTA pairs)
     int ready_shared_base, ready_shared_count;
     int *tile_counters;    // [2] tile tickets of the expert GEMM launches, zeroed by CTA (0, 0), or nullptr
     unsigned long long *trace;
@@ -218,6 +219,8 @@ struct GemmArgs {
     int *err;
     unsigned long long wait_ns;
     int num_ctas;
+    int pair;              // 1: CTA pairs (cta_group::2, 256-row tiles, static order; num_ctas even,
+                           //    tile_offs counting 256-row tiles; all maps from encode_map_*_kb2)
     int *tile_counter;     // zeroed ticket: tiles claimed in order (dynamic); nullptr: round-robin
     unsigned long long *trace;
     // nullptr, or kGemmStats ns sums over CTAs: producer waiting for a free
@@ -257,6 +260,9 @@ cudaError_t launch_gemm_sab(const SabArgs &a, int n_tokens, cudaStream_t s);
 // Tensor maps (TMA descriptors) for the GEMMs.  A: [rows, K] bf16, box 128 x 64.
 // B: [groups, rows, K] bf16, box box_rows x 64.  Both with 128-byte swizzle.
 CUresult encode_map_a(CUtensorMap *m, const void *ptr, int rows, int K);
+// K viewed as (64, K / 64), box 64 x 128 rows x 2 chunks (CTA-pair expert GEMM)
+CUresult encode_map_a_kb2(CUtensorMap *m, const void *ptr, int rows, int K);
+CUresult encode_map_b_kb2(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int box_rows);
 CUresult encode_map_a_box(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows);
 CUresult encode_map_b(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int box_rows);
 

@@ -85,6 +85,8 @@ struct moe_handle {
     int *tile_counters = nullptr;  // [2] tile tickets of the expert GEMM launches
     int ready_shared_base = 0; // first counter of the shared expert's m-tiles
     bool fuse_experts = true;  // gate/up and down in one persistent launch
+    int pair_opt = 2;          // CTA-pair expert GEMM: 0 never, 1 always, 2 when T*k >= 256*E
+    bool pair_now = false;     // the current forward's choice
     bool prefetch_opt = true;  // L2 prefetch of expert weights during routing
     cudaStream_t side = nullptr;               // the prefetch runs here, beside the routing kernels
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
@@ -104,6 +106,11 @@ struct moe_handle {
     CUtensorMap m_xs_n[2], m_hb_n[2], m_hs_n[2], m_xbf_n[2], m_x_n[2];
     const void *m_x_n_ptr[2] = {nullptr, nullptr};
     int m_x_n_rows[2] = {0, 0};
+    // CTA-pair expert GEMM: the same tensors with K viewed as (64, K / 64), two
+    // k-blocks per box (A: 128 rows; weights: 128 rows)
+    CUtensorMap m_xs2, m_hb2, m_hs2, m_xbf2, m_gate2, m_up2, m_down2, m_shg2, m_shu2, m_shd2, m_x2;
+    const void *m_x2_ptr = nullptr;
+    int m_x2_rows = 0;
     // descriptor of the caller's X for the shared-expert GEMM (cached by pointer and T)
     CUtensorMap m_x;
     const void *m_x_ptr = nullptr;
@@ -203,8 +210,10 @@ void carve(moe_handle *h, void *base) {
     h->gemm_stats = c.take<unsigned long long>(base, moe::kGemmStats);
     h->router_stats = c.take<unsigned long long>(base, moe::kRouterStats);
     // routed m-tiles number at most T*k/128 + E; the shared expert's follow
-    h->ready_shared_base = (int)(MT * k / 128 + E + 1);
-    h->ready = c.take<int>(base, (size_t)h->ready_shared_base + (MT + 127) / 128 + 1);
+    // (with CTA pairs, 2 counters per 256-row tile: at most T*k/128 + 2E + 2 routed and
+    // 2*ceil(T/256) + 2 shared)
+    h->ready_shared_base = (int)(MT * k / 128 + 2 * E + 2);
+    h->ready = c.take<int>(base, (size_t)h->ready_shared_base + 2 * ((MT + 255) / 256) + 2);
     h->wr_flags = c.take<int>(base, 64);
     h->tile_counters = c.take<int>(base, 64);
     h->ws_bytes = round_up(c.off, 256);
@@ -220,6 +229,11 @@ moe_status build_maps(moe_handle *h) {
     } while (0)
     MAP(moe::encode_map_a(&h->m_xsorted, h->x_sorted, MT * k, H));
     MAP(moe::encode_map_a(&h->m_hbuf, h->hbuf, MT * k, I));
+    MAP(moe::encode_map_a_kb2(&h->m_xs2, h->x_sorted, MT * k, H));
+    MAP(moe::encode_map_a_kb2(&h->m_hb2, h->hbuf, MT * k, I));
+    MAP(moe::encode_map_b_kb2(&h->m_gate2, h->w.gate, Ep, I, H, 128));
+    MAP(moe::encode_map_b_kb2(&h->m_up2, h->w.up, Ep, I, H, 128));
+    MAP(moe::encode_map_b_kb2(&h->m_down2, h->w.down, Ep, H, I, 128));
     MAP(moe::encode_map_b(&h->m_gate, h->w.gate, Ep, I, H, 128));
     MAP(moe::encode_map_b(&h->m_up, h->w.up, Ep, I, H, 128));
     MAP(moe::encode_map_b(&h->m_down, h->w.down, Ep, H, I, moe::kGemmBN));
@@ -237,6 +251,8 @@ moe_status build_maps(moe_handle *h) {
     if (h->has_shared) {
         MAP(moe::encode_map_a(&h->m_hs, h->hs, MT, S));
         if (h->x_f32) MAP(moe::encode_map_a(&h->m_xbf16, h->x_bf16, MT, H));
+        MAP(moe::encode_map_a_kb2(&h->m_hs2, h->hs, MT, S));
+        if (h->x_f32) MAP(moe::encode_map_a_kb2(&h->m_xbf2, h->x_bf16, MT, H));
         if (h->cfg.shared_packed) {
             h->m_shg = h->m_gate;
             h->m_shu = h->m_up;
@@ -244,6 +260,9 @@ moe_status build_maps(moe_handle *h) {
             h->m_shg64 = h->m_gate64;
             h->m_shu64 = h->m_up64;
             h->m_shd128 = h->m_down128;
+            h->m_shg2 = h->m_gate2;
+            h->m_shu2 = h->m_up2;
+            h->m_shd2 = h->m_down2;
         } else {
             MAP(moe::encode_map_b(&h->m_shg, h->w.sh_gate, 1, S, H, 128));
             MAP(moe::encode_map_b(&h->m_shu, h->w.sh_up, 1, S, H, 128));
@@ -251,6 +270,9 @@ moe_status build_maps(moe_handle *h) {
             MAP(moe::encode_map_b(&h->m_shg64, h->w.sh_gate, 1, S, H, 64));
             MAP(moe::encode_map_b(&h->m_shu64, h->w.sh_up, 1, S, H, 64));
             MAP(moe::encode_map_b(&h->m_shd128, h->w.sh_down, 1, H, S, 128));
+            MAP(moe::encode_map_b_kb2(&h->m_shg2, h->w.sh_gate, 1, S, H, 128));
+            MAP(moe::encode_map_b_kb2(&h->m_shu2, h->w.sh_up, 1, S, H, 128));
+            MAP(moe::encode_map_b_kb2(&h->m_shd2, h->w.sh_down, 1, H, S, 128));
         }
     }
 #undef MAP
@@ -401,7 +423,8 @@ moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n
     xa.tile_m = tile_m;
     xa.ready = h->ready;
     xa.ready_shared_base = h->ready_shared_base;
-    xa.ready_shared_count = (T + 127) / 128;
+    xa.ready_per_tile = h->pair_now ? 2 : 1;
+    xa.ready_shared_count = h->pair_now ? 2 * ((T + 255) / 256) : (T + 127) / 128;
     xa.tile_counters = h->tile_counters;
     xa.T = T;
     xa.k = h->k;
@@ -440,25 +463,37 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     g.alpha = h->cfg.act_alpha;
     g.limit = h->cfg.act_limit;
     g.beta = h->cfg.act_beta;
-    g.num_ctas = h->num_sms;
+    // CTA pairs: an even grid, static tile order, down weights in 128-row boxes
+    // (each CTA of a pair loads half of a 256-row tile)
+    const bool pair = h->pair_now;
+    g.pair = pair ? 1 : 0;
+    g.num_ctas = pair ? h->num_sms / 2 * 2 : h->num_sms;
     for (auto &m : g.maps) m = h->m_xsorted;  // unused slots hold a valid descriptor
-    g.maps[kXs] = h->m_xsorted;
-    g.maps[kHb] = h->m_hbuf;
-    g.maps[kG] = h->m_gate;
-    g.maps[kU] = h->m_up;
-    g.maps[kD] = h->m_down;
+    g.maps[kXs] = pair ? h->m_xs2 : h->m_xsorted;
+    g.maps[kHb] = pair ? h->m_hb2 : h->m_hbuf;
+    g.maps[kG] = pair ? h->m_gate2 : h->m_gate;
+    g.maps[kU] = pair ? h->m_up2 : h->m_up;
+    g.maps[kD] = pair ? h->m_down2 : h->m_down;
     if (h->has_shared) {
         if (h->x_f32) {
-            g.maps[kX] = h->m_xbf16;
+            g.maps[kX] = pair ? h->m_xbf2 : h->m_xbf16;
+        } else if (pair) {
+            if (h->m_x2_ptr != X || h->m_x2_rows != T) {
+                CUresult r = moe::encode_map_a_kb2(&h->m_x2, X, T, H);
+                if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(X) failed: %d", (int)r);
+                h->m_x2_ptr = X;
+                h->m_x2_rows = T;
+            }
+            g.maps[kX] = h->m_x2;
         } else {
             moe_status st = x_map(h, X, T);
             if (st != MOE_OK) return st;
             g.maps[kX] = h->m_x;
         }
-        g.maps[kHs] = h->m_hs;
-        g.maps[kSG] = h->m_shg;
-        g.maps[kSU] = h->m_shu;
-        g.maps[kSD] = h->m_shd;
+        g.maps[kHs] = pair ? h->m_hs2 : h->m_hs;
+        g.maps[kSG] = pair ? h->m_shg2 : h->m_shg;
+        g.maps[kSU] = pair ? h->m_shu2 : h->m_shu;
+        g.maps[kSD] = pair ? h->m_shd2 : h->m_shd;
     }
     const int sh_base = h->cfg.shared_packed ? E : 0;
     const int nt_gu = (I + 127) / 128, nt_sgu = (S + 127) / 128, nt_d = (H + moe::kGemmBN - 1) / moe::kGemmBN;
@@ -480,7 +515,7 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         g.seg[ns++] = dn;
         if (h->has_shared) g.seg[ns++] = sdn;
         g.num_segs = ns;
-        g.tile_counter = h->tile_counters;
+        g.tile_counter = pair ? nullptr : h->tile_counters;
         g.trace = trace_slot(h, *n);
         g.stats = h->trace_on ? h->gemm_stats : nullptr;
         return launched(h, moe::launch_gemm_tc(g, s), "experts_gemm", n, s);
@@ -491,7 +526,7 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         g.seg[1] = sgu;
         g.num_segs = 2;
     }
-    g.tile_counter = h->tile_counters;
+    g.tile_counter = pair ? nullptr : h->tile_counters;
     g.trace = trace_slot(h, *n);
     moe_status st = launched(h, moe::launch_gemm_tc(g, s), "gate_up_gemm", n, s);
     if (st != MOE_OK) return st;
@@ -501,7 +536,7 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         g.seg[1] = sdn;
         g.num_segs = 2;
     }
-    g.tile_counter = h->tile_counters + 1;
+    g.tile_counter = pair ? nullptr : h->tile_counters + 1;
     g.trace = trace_slot(h, *n);
     return launched(h, moe::launch_gemm_tc(g, s), "down_gemm", n, s);
 }
@@ -626,8 +661,11 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
             e = cudaMemsetAsync(h->router_stats, 0, moe::kRouterStats * sizeof(unsigned long long), s);
         if (e != cudaSuccess) return cuda_fail(e, "trace reset");
     }
+    h->pair_now = path == kPathGrouped && h->num_sms >= 2 &&
+                  (h->pair_opt == 1 || (h->pair_opt == 2 && slots >= 256ll * h->E));
     mark(h, 0, s);
-    moe_status st = run_front(h, X, T, s, &n, path == kPathSwapped ? n_tok : moe::kGemmBM);
+    moe_status st = run_front(h, X, T, s, &n,
+                              path == kPathSwapped ? n_tok : (h->pair_now ? 2 * moe::kGemmBM : moe::kGemmBM));
     if (st == MOE_OK) {
         if (path == kPathDecode)
             st = run_decode(h, X, T, s, &n);
@@ -854,6 +892,10 @@ moe_status moe_set_option(moe_handle *h, int option, long long value) {
     case MOE_OPT_FUSE_EXPERTS:
         if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "fuse experts %lld", value);
         h->fuse_experts = value != 0;
+        return MOE_OK;
+    case MOE_OPT_GEMM_PAIR:
+        if (value < 0 || value > 2) return fail(MOE_ERR_INVALID_ARG, "gemm pair %lld", value);
+        h->pair_opt = (int)value;
         return MOE_OK;
     case MOE_OPT_TRACE:
         if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "trace %lld", value);

@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
         }
         if (writer && a.tile_counters != nullptr && lane < 2) a.tile_counters[lane] = 0;
         if (writer && a.ready != nullptr) {
-            for (int i = lane; i < trun; i += 32) a.ready[i] = 0;
+            for (int i = lane; i < trun * a.ready_per_tile; i += 32) a.ready[i] = 0;
             for (int i = lane; i < a.ready_shared_count; i += 32) a.ready[a.ready_shared_base + i] = 0;
         }
     }

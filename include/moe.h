@@ -163,11 +163,15 @@ typedef enum {
                                   into L2 while the routing kernels run (forked from and joined back
                                   into the caller's stream); 0: no prefetch.  A hint: results are
                                   unchanged */
-    MOE_OPT_TRACE = 5          /* 1: every kernel of moe_forward on the grouped path records, in a
+    MOE_OPT_TRACE = 5,         /* 1: every kernel of moe_forward on the grouped path records, in a
                                   device buffer of the handle, when its first CTA started, when its
                                   first and last CTA passed the wait on the previous kernel, and when
                                   its first and last CTA finished (the GPU's global timer), for
                                   moe_get_trace.  Costs a memset and a few atomics per CTA; default 0 */
+    MOE_OPT_GEMM_PAIR = 6      /* path 2: expert GEMM tiles of 256 rows on CTA pairs (tcgen05 with
+                                  cta_group::2: each CTA of a two-CTA cluster stages its 128 token rows
+                                  and half of the weight tile); 0 never, 1 always, 2 (default) when
+                                  T*k >= 256*E (tensor-bound sizes) */
 } moe_option;
 
 /* Set an option.  Errors: INVALID_ARG (unknown option or value). */

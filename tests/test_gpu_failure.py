@@ -13,12 +13,15 @@ from tests import parity as P
 pytestmark = pytest.mark.gpu
 
 
-def test_wait_bound_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("pair", [0, 1])
+def test_wait_bound_reports_timeout_and_context_survives(pair):
+    """pair = 1: the CTA-pair expert GEMM, whose abort also stops the other CTA."""
     from expert_routed_ffn_gb300 import build
     build.build()
     shape = wl.NANO_DECODE.replace(T=512)
     inputs, blk = P.make_case(shape)
     blk.set_option(capi.MOE_OPT_PATH, capi.PATH_GROUPED)
+    blk.set_option(capi.MOE_OPT_GEMM_PAIR, pair)
     Y0 = blk.forward(inputs["X"]).clone()
     assert blk.sync_status() == capi.MOE_OK
     blk.set_option(capi.MOE_OPT_WAIT_LIMIT_NS, 0)

@@ -18,7 +18,10 @@ from tests import parity as P
 
 pytestmark = pytest.mark.gpu
 
-PATHS = {"decode": capi.PATH_DECODE, "grouped": capi.PATH_GROUPED, "swapped": capi.PATH_SWAPPED}
+# (MOE_OPT_PATH, MOE_OPT_GEMM_PAIR): "grouped" runs one CTA per tile, "pair" the
+# CTA-pair (cta_group::2) expert GEMM on the same path
+PATHS = {"decode": (capi.PATH_DECODE, 0), "grouped": (capi.PATH_GROUPED, 0), "pair": (capi.PATH_GROUPED, 1),
+         "swapped": (capi.PATH_SWAPPED, 0)}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -32,7 +35,9 @@ def _run(shape, path=None, inputs=None, blk=None, max_tokens=None):
     if inputs is None:
         inputs, blk = P.make_case(shape, max_tokens=max_tokens)
     if path is not None:
+        path, pair = path if isinstance(path, tuple) else (path, 0)
         blk.set_option(capi.MOE_OPT_PATH, path)
+        blk.set_option(capi.MOE_OPT_GEMM_PAIR, pair)
     Y = blk.forward(inputs["X"])
     torch.cuda.synchronize()
     assert blk.sync_status() == capi.MOE_OK
@@ -77,7 +82,7 @@ def test_small_workload_every_token(name, path):
     idx, w = _topk(blk, shape.T, shape.k)
     P.check_route(shape, ih, idx, w)
     P.check_output(P.to_np(Y), oracle.forward_inputs(shape, ih), shape.dtype == "bf16", tag=f"{name}-{path}")
-    assert blk.stats().path == PATHS[path]
+    assert blk.stats().path == PATHS[path][0]
 
 
 def test_clamp_swiglu_fires_and_matches():
@@ -196,6 +201,23 @@ def test_device_trace_orders_the_kernels_and_leaves_results_unchanged():
         blk.set_option(capi.MOE_OPT_TRACE, 0)
         with pytest.raises(capi.MoeError):
             blk.trace()
+
+
+def test_pair_gemm_fused_equals_two_launches_and_oracle():
+    """The CTA-pair expert GEMM in one launch and in two launches: bit-identical,
+    and within tolerance of the oracle on every token."""
+    for name in ("afmoe_ragged", "m3_small_packed"):
+        shape = SMALL[name]
+        inputs, blk, Y1 = _run(shape, PATHS["pair"])
+        names = blk.stage_names()
+        assert names[names.index("dispatch_scatter") + 1:] == ["experts_gemm", "combine"]
+        blk.set_option(capi.MOE_OPT_FUSE_EXPERTS, 0)
+        Y2 = blk.forward(inputs["X"])
+        torch.cuda.synchronize()
+        assert blk.sync_status() == capi.MOE_OK
+        assert torch.equal(Y1, Y2)
+        ih = P.host_inputs(inputs)
+        P.check_output(P.to_np(Y1), oracle.forward_inputs(shape, ih), shape.dtype == "bf16", tag=f"{name}-pair-fused")
 
 
 def test_token_permutation_equivariance_and_determinism():
