@@ -17,15 +17,16 @@
 // resident (one per SM): a down tile only waits for tiles claimed before it,
 // which do not wait, so the waits end.
 //
-// Persistent kernel, one CTA per SM, 6 warps:
+// Persistent kernel, one CTA per SM, 10 warps:
 //   warp 0     TMA producer: A tile 128 x 64 and B tile 256 x 64 (gate/up: 128
 //              gate rows + 128 up rows) per stage, 128-byte swizzle, 4 stages
 //   warp 1     allocates 512 TMEM columns; lane 0 issues tcgen05.mma
 //              (M 128, N 256, K 16, bf16 in, fp32 accumulate) into one of two
 //              TMEM accumulators, so the epilogue of one tile overlaps the
 //              main loop of the next
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
-//              32*(w%4)..+31 = tile rows), activation (gate/up), bf16 stores
+//   warps 2-9  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
+//              32*(w%4)..+31 = tile rows; warps 2-5 the first half of the
+//              columns, 6-9 the second), activation (gate/up), bf16 stores
 // Tiles are (segment, group, m-tile, n-tile) in a fixed order; the producer
 // claims them from a launch-wide ticket (the CTA that is free first takes the
 // next tile) and passes each id to the MMA and epilogue warps through a ring
@@ -42,7 +43,9 @@ namespace moe {
 namespace {
 
 constexpr int kABytes = kGemmBM * kGemmBK * 2;  // 16 KB
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                   // two per TMEM lane quadrant, each half of the columns
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 64 + kEpiThreads;     // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr uint32_t kTmemCols = 512;             // two 128 x 256 fp32 accumulators
 constexpr uint64_t kDrainNs = 1000000000ull;    // bound of the drain after an abort
 constexpr uint64_t kPairDrainNs = 1000000ull;   // CTA pair: grace for the copies in flight after an abort
@@ -151,16 +154,16 @@ __device__ __forceinline__ bool wait_counter(const int *p, int target, uint64_t 
 }
 
 // Named barrier 1 of the four epilogue warps; and the AND of v over them.
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); }
 __device__ __forceinline__ bool epi_all(bool v) {
     uint32_t out;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(out)
-        : "r"((uint32_t)v)
+        : "r"((uint32_t)v), "n"(kEpiThreads)
         : "memory");
     return out != 0;
 }
@@ -210,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
         for (uint32_t a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), PAIR ? 256 : 128);  // the epilogue threads of both CTAs
+            mbar_init(tempty_bar(a), PAIR ? 2 * kEpiThreads : kEpiThreads);  // the epilogue threads (of both CTAs)
         }
         mbar_init(drain_bar, 1);
         for (int i = 0; i < kRing; ++i) {
@@ -453,7 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
     } else {
         // ----------------------------------------------------------- epilogue
-        const int q = warp & 3;  // TMEM lane quadrant this warp may read
+        const int q = warp & 3;               // TMEM lane quadrant this warp may read
+        const int part = (warp - 2) / 4;      // which half of the tile's columns
+        const bool lead_thread = q == 0 && part == 0 && lane == 0;
         const int r = q * 32 + lane;
         uint32_t n_acc = 0;
         uint64_t w_tfull = 0, w_work = 0;
@@ -468,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 if (lane == 0) abort_all();
                 break;
             }
-            if (q == 0 && lane == 0) mbar_arrive(ring_empty(slot));
+            if (lead_thread) mbar_arrive(ring_empty(slot));
             if (tile >= total) break;
             const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
             const GemmSegment &sg = p.seg[t.seg];
@@ -487,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             bf16 *orow = sg.out + (size_t)(t.row0 + (row_ok ? r : 0)) * sg.ldo;
             if (sg.glu) {
 #pragma unroll 1
-                for (int c0 = 0; c0 < 128; c0 += 32) {
+                for (int c0 = part * 64; c0 < part * 64 + 64; c0 += 32) {
                     uint32_t g[32], u[32];
                     tmem_ld32(tb + c0, g);
                     tmem_ld32(tb + 128 + c0, u);
@@ -510,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 }
             } else {
 #pragma unroll 1
-                for (int c0 = 0; c0 < kGemmBN; c0 += 32) {
+                for (int c0 = part * (kGemmBN / 2); c0 < (part + 1) * (kGemmBN / 2); c0 += 32) {
                     uint32_t v32[32];
                     tmem_ld32(tb + c0, v32);
                     tmem_ld_wait();
@@ -538,12 +543,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 fence_proxy_async();
                 __threadfence();
                 epi_bar();
-                if (q == 0 && lane == 0) atomicAdd(sg.signal + t.ready, 1);
+                if (lead_thread) atomicAdd(sg.signal + t.ready, 1);
             }
             if (stats) w_work += global_timer_ns() - t1;
             ++n_acc;
         }
-        if (stats && q == 0 && lane == 0) {
+        if (stats && lead_thread) {
             atomicAdd(stats + 4, (unsigned long long)w_tfull);
             atomicAdd(stats + 5, (unsigned long long)w_work);
         }
