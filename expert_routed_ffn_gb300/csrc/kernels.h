@@ -171,6 +171,7 @@ cudaError_t launch_scatter(const ScatterArgs &a, cudaStream_t s);
 struct CombineArgs {
     const __nv_bfloat16 *yslot;  // [T*k, H]
     const __nv_bfloat16 *ys;     // [T, H] or nullptr
+    const __nv_bfloat16 *ys2;    // [T, H] second half of a K-split shared down projection, or nullptr
     const float *topk_w;         // [T, k]
     const int32_t *slot_of;      // [T, k]
     int T, k, H;
@@ -185,7 +186,7 @@ constexpr int kGemmBM = 128;   // rows (tokens) per tile: the MMA's M
 constexpr int kGemmBK = 64;    // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int kGemmBN = 256;   // MMA N; gate/up tiles hold 128 gate + 128 up columns
 
-constexpr int kGemmMaxSegments = 4;
+constexpr int kGemmMaxSegments = 5;
 constexpr int kGemmMaxMaps = 10;
 struct GemmSegment {
     int dense;             // 1: one group of m_dense rows from row 0; 0: groups by offs
@@ -195,7 +196,8 @@ struct GemmSegment {
     const int32_t *offs;   // [num_groups + 1] (grouped; every grouped segment of a launch shares them)
     const int32_t *tile_offs;
     int n_tiles;           // output tiles per group along N
-    int k_blocks;          // K / 64
+    int k_blocks;          // K / 64 (of this segment)
+    int k_base;            // first 64-wide k-block of A's columns and B's columns
     int n_out;             // valid output columns
     __nv_bfloat16 *out;    // [rows, ldo]
     int ldo;

@@ -77,7 +77,7 @@ struct moe_handle {
             *active = nullptr, *sorted_tok = nullptr, *slot_of = nullptr;
     float *topk_w = nullptr;
     bf16 *x_sorted = nullptr, *x_bf16 = nullptr, *hbuf = nullptr, *hs = nullptr, *yslot = nullptr,
-         *ys = nullptr;
+         *ys = nullptr, *ys2 = nullptr;
     void *x_stage = nullptr, *y_stage = nullptr;
     int *err = nullptr;
     bf16 *wr_parts = nullptr;  // router weights as exact bf16 splits [3, E, H]
@@ -87,6 +87,7 @@ struct moe_handle {
     bool fuse_experts = true;  // gate/up and down in one persistent launch
     int pair_opt = 2;          // CTA-pair expert GEMM: 0 never, 1 always, 2 when T*k >= 256*E
     bool pair_now = false;     // the current forward's choice
+    bool shared_split_now = false;  // shared down projection in two K halves (small T)
     bool prefetch_opt = true;  // L2 prefetch of expert weights during routing
     cudaStream_t side = nullptr;               // the prefetch runs here, beside the routing kernels
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
@@ -203,6 +204,7 @@ void carve(moe_handle *h, void *base) {
     h->hs = h->has_shared ? c.take<bf16>(base, MT * h->S) : nullptr;
     h->yslot = c.take<bf16>(base, MT * k * H);
     h->ys = h->has_shared ? c.take<bf16>(base, MT * H) : nullptr;
+    h->ys2 = h->has_shared ? c.take<bf16>(base, MT * H) : nullptr;
     h->x_stage = c.take<char>(base, MT * H * elt);
     h->y_stage = c.take<char>(base, MT * H * elt);
     h->wr_parts = c.take<bf16>(base, 3 * E * H);
@@ -499,21 +501,30 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     const int nt_gu = (I + 127) / 128, nt_sgu = (S + 127) / 128, nt_d = (H + moe::kGemmBN - 1) / moe::kGemmBN;
     const bool fused = h->fuse_experts;
     int *sig = fused ? h->ready : nullptr;
-    const moe::GemmSegment gu{0, E, 0, 0, h->offs, h->tile_offs, nt_gu, H / 64, I, h->hbuf, I,
+    const moe::GemmSegment gu{0, E, 0, 0, h->offs, h->tile_offs, nt_gu, H / 64, 0, I, h->hbuf, I,
                               1, kXs, kG, kU, sig, nullptr, 0, 0};
-    const moe::GemmSegment sgu{1, 1, sh_base, T, nullptr, nullptr, nt_sgu, H / 64, S, h->hs, S,
+    const moe::GemmSegment sgu{1, 1, sh_base, T, nullptr, nullptr, nt_sgu, H / 64, 0, S, h->hs, S,
                                1, kX, kSG, kSU, sig, nullptr, 0, h->ready_shared_base};
-    const moe::GemmSegment dn{0, E, 0, 0, h->offs, h->tile_offs, nt_d, I / 64, H, h->yslot, H,
+    const moe::GemmSegment dn{0, E, 0, 0, h->offs, h->tile_offs, nt_d, I / 64, 0, H, h->yslot, H,
                               0, kHb, kD, kD, nullptr, fused ? h->ready : nullptr, nt_gu, 0};
-    const moe::GemmSegment sdn{1, 1, sh_base, T, nullptr, nullptr, nt_d, S / 64, H, h->ys, H,
-                               0, kHs, kSD, kSD, nullptr, fused ? h->ready : nullptr, nt_sgu,
-                               h->ready_shared_base};
+    // At small T the shared down projection (K = S) is the longest tile chain: its
+    // two K halves run as two segments into two partial outputs, which the
+    // combine adds in fixed order (for two concatenated shared experts of width I
+    // the halves are exactly the two experts).
+    const bool split = h->shared_split_now;
+    const int sk = split ? S / 128 : S / 64;
+    moe::GemmSegment sdn{1, 1, sh_base, T, nullptr, nullptr, nt_d, sk, 0, H, h->ys, H,
+                         0, kHs, kSD, kSD, nullptr, fused ? h->ready : nullptr, nt_sgu, h->ready_shared_base};
+    moe::GemmSegment sdn2 = sdn;
+    sdn2.k_base = sk;
+    sdn2.out = h->ys2;
     if (fused) {
         int ns = 0;
         g.seg[ns++] = gu;
         if (h->has_shared) g.seg[ns++] = sgu;
         g.seg[ns++] = dn;
         if (h->has_shared) g.seg[ns++] = sdn;
+        if (h->has_shared && split) g.seg[ns++] = sdn2;
         g.num_segs = ns;
         g.tile_counter = pair ? nullptr : h->tile_counters;
         g.trace = trace_slot(h, *n);
@@ -535,6 +546,7 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     if (h->has_shared) {
         g.seg[1] = sdn;
         g.num_segs = 2;
+        if (split) g.seg[g.num_segs++] = sdn2;
     }
     g.tile_counter = pair ? nullptr : h->tile_counters + 1;
     g.trace = trace_slot(h, *n);
@@ -663,6 +675,13 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     }
     h->pair_now = path == kPathGrouped && h->num_sms >= 2 &&
                   (h->pair_opt == 1 || (h->pair_opt == 2 && slots >= 256ll * h->E));
+    {
+        // few shared down tiles (a quarter of the SMs or less) and an even number of
+        // k-blocks: split the shared down projection's K in two
+        const long long sh_tiles = (long long)((T + 127) / 128) * ((h->H + moe::kGemmBN - 1) / moe::kGemmBN);
+        h->shared_split_now = path == kPathGrouped && !h->pair_now && h->has_shared && h->S % 128 == 0 &&
+                              sh_tiles * 4 <= h->num_sms;
+    }
     mark(h, 0, s);
     moe_status st = run_front(h, X, T, s, &n,
                               path == kPathSwapped ? n_tok : (h->pair_now ? 2 * moe::kGemmBM : moe::kGemmBM));
@@ -675,7 +694,8 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
             st = run_grouped(h, X, T, s, &n);
     }
     if (st == MOE_OK) {
-        moe::CombineArgs ca{h->yslot, h->has_shared ? h->ys : nullptr, h->topk_w, h->slot_of,
+        moe::CombineArgs ca{h->yslot, h->has_shared ? h->ys : nullptr, h->shared_split_now ? h->ys2 : nullptr,
+                            h->topk_w, h->slot_of,
                             T, h->k, h->H, Y, h->x_f32 ? 1 : 0, trace_slot(h, n)};
         st = launched(h, moe::launch_combine(ca, s), "combine", &n, s);
     }

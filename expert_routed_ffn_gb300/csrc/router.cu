@@ -378,19 +378,29 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
 constexpr int kCombineThreads = 128;
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
+    __shared__ int s_slot[16];
+    __shared__ float s_w[16];
     const int t = blockIdx.x, k = a.k, H = a.H;
     trace_mark(a.trace, 0);
+    // The token's slots and weights come from the router and the dispatch, which
+    // completed before the expert GEMM (this grid's predecessor) passed its own
+    // wait and let this grid launch: they are read ahead of the wait, from L2.
+    if (threadIdx.x < k) {
+        s_slot[threadIdx.x] = __ldcg(a.slot_of + (size_t)t * k + threadIdx.x);
+        s_w[threadIdx.x] = __ldcg(a.topk_w + (size_t)t * k + threadIdx.x);
+    }
     pdl_wait();
     trace_mark(a.trace, 1);
     pdl_trigger();
+    __syncthreads();
     for (int c = threadIdx.x * 8; c < H; c += kCombineThreads * 8) {
         float acc[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[q] = 0.f;
         for (int j = 0; j < k; ++j) {
-            const int slot = __ldg(a.slot_of + (size_t)t * k + j);
+            const int slot = s_slot[j];
             if (slot < 0) continue;
-            const float w = __ldg(a.topk_w + (size_t)t * k + j);
+            const float w = s_w[j];
             const uint4 r = __ldg(reinterpret_cast<const uint4 *>(a.yslot + (size_t)slot * H + c));
             acc[0] = fmaf(w, bf16_lo(r.x), acc[0]); acc[1] = fmaf(w, bf16_hi(r.x), acc[1]);
             acc[2] = fmaf(w, bf16_lo(r.y), acc[2]); acc[3] = fmaf(w, bf16_hi(r.y), acc[3]);
@@ -399,6 +409,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineA
         }
         if (a.ys != nullptr) {
             const uint4 r = __ldg(reinterpret_cast<const uint4 *>(a.ys + (size_t)t * H + c));
+            acc[0] += bf16_lo(r.x); acc[1] += bf16_hi(r.x); acc[2] += bf16_lo(r.y);
+            acc[3] += bf16_hi(r.y); acc[4] += bf16_lo(r.z); acc[5] += bf16_hi(r.z);
+            acc[6] += bf16_lo(r.w); acc[7] += bf16_hi(r.w);
+        }
+        if (a.ys2 != nullptr) {  // the shared expert's second K half
+            const uint4 r = __ldg(reinterpret_cast<const uint4 *>(a.ys2 + (size_t)t * H + c));
             acc[0] += bf16_lo(r.x); acc[1] += bf16_hi(r.x); acc[2] += bf16_lo(r.y);
             acc[3] += bf16_hi(r.y); acc[4] += bf16_lo(r.z); acc[5] += bf16_hi(r.z);
             acc[6] += bf16_lo(r.w); acc[7] += bf16_hi(r.w);
