@@ -24,10 +24,19 @@ Recipe (all workloads):
   * bf16 workloads round every drawn value to bf16 (round-to-nearest-even).
     Router weights are rounded to bf16 too but stored as fp32, so the router
     of both sides sees identical fp32 values;
-  * the tiny workload keeps fp32 for X, router and expert weights.
+  * the tiny workload keeps fp32 for X, router and expert weights;
+  * dense layers (num_experts = 0: the dense prefix of the AFMoE issue, "Dense
+    prefix", and the MiniMax-M3 issue, dense_intermediate_size 12288; width
+    6144 is AfmoeConfig's intermediate_size) draw only their MLP weights, as
+    the shared tensors;
+  * with the sandwich norms (mlp_norm "rms" or "gemma": AFMoE issue, four norms
+    per layer; MiniMax-M3 issue, Gemma-style RMSNorm weight + 1), the
+    pre_mlp / post_mlp norm weights [H] fp32 are drawn after the MLP weights:
+    1 + N(0, 0.1) for "rms", N(0, 0.1) for "gemma" (applied as 1 + w).
 
 A caller may pass ``row_filter``: a function of the host copy of
-(X, router_w, expert_bias) returning a boolean mask of token rows to redraw.
+(X, router_w, expert_bias) (and pre_mlp_norm's weight when the workload has the
+sandwich norms) returning a boolean mask of token rows to redraw.
 The parity tests use it to enforce a gap of at least 1e-3 between the k-th and
 (k+1)-th biased router scores, so that top-k sets are unique.  Redrawn rows
 come from a generator seeded with (x_seed, attempt).
@@ -44,6 +53,7 @@ WEIGHT_STD = 0.02
 BIAS_HALF_RANGE = 0.1
 ZIPF_S = 1.2
 ZIPF_MAX = 0.5
+NORM_STD = 0.1
 
 
 @dataclasses.dataclass(frozen=True)
@@ -70,6 +80,8 @@ class MoeShape:
     act_alpha: float = 1.702
     act_limit: float = 7.0
     act_beta: float = 1.0
+    mlp_norm: str = "none"  # "none" | "rms" | "gemma": pre_mlp / post_mlp RMSNorm around the MLP
+    rms_norm_eps: float = 1e-5
 
     @property
     def H(self) -> int:
@@ -139,12 +151,35 @@ def zipf_sweep(T: int) -> MoeShape:
     return _afmoe_default(T, "zipf", 1005, 2000 + T, f"afmoe_zipf_T{T}")
 
 
+def dense_layer(T: int, model: str) -> MoeShape:
+    """A dense prefix layer: AFMoE (hidden 2048, intermediate_size 6144, silu) or
+    MiniMax-M3 (hidden 6144, dense_intermediate_size 12288, clamp-SwiGLU)."""
+    if model == "afmoe":
+        return MoeShape(name=f"dense_afmoe_T{T}_H2048_I6144", T=T, hidden_size=2048, num_experts=0,
+                        num_experts_per_tok=0, moe_intermediate_size=0, num_shared_experts=1,
+                        shared_intermediate_size=6144, shared_packed=False, hidden_act="silu",
+                        score_func="sigmoid", route_norm=True, route_scale=1.0, dtype="bf16",
+                        bias_kind="uniform", seed=1006, x_seed=3000 + T, mlp_norm="rms")
+    return MoeShape(name=f"dense_m3_T{T}_H6144_I12288", T=T, hidden_size=6144, num_experts=0,
+                    num_experts_per_tok=0, moe_intermediate_size=0, num_shared_experts=1,
+                    shared_intermediate_size=12288, shared_packed=False, hidden_act="swigluoai",
+                    score_func="sigmoid", route_norm=True, route_scale=1.0, dtype="bf16",
+                    bias_kind="uniform", seed=1007, x_seed=4000 + T, mlp_norm="gemma")
+
+
 WORKLOADS = {
     "tiny": TINY,
     "nano_decode": NANO_DECODE,
     "afmoe_prefill": AFMOE_PREFILL,
     "m3": M3,
     **{f"zipf_T{t}": zipf_sweep(t) for t in ZIPF_TOKENS},
+    # the layers around the block (next rows): sandwich norms, dense prefix
+    "afmoe_prefill_sandwich": AFMOE_PREFILL.replace(name="afmoe_prefill_sandwich_T4096", mlp_norm="rms"),
+    "nano_decode_sandwich": NANO_DECODE.replace(name="nano_decode_sandwich_T256", mlp_norm="rms"),
+    "m3_sandwich": M3.replace(name="m3_sandwich_T2048_gemma", mlp_norm="gemma"),
+    "dense_afmoe_prefill": dense_layer(4096, "afmoe"),
+    "dense_afmoe_decode": dense_layer(256, "afmoe"),
+    "dense_m3": dense_layer(2048, "m3"),
 }
 
 
@@ -200,25 +235,33 @@ def make_inputs(shape: MoeShape, device="cpu",
     E, H, I, S = shape.E, shape.H, shape.I, shape.S
     Ep = shape.stacked_experts
 
-    router_w = _normal(g, (E, H), WEIGHT_STD, dt, device).to(torch.float32)
-    expert_bias = _bias(shape, g, device)
-    gate = _stacked(g, Ep, I, H, dt, device)
-    up = _stacked(g, Ep, I, H, dt, device)
-    down = _stacked(g, Ep, H, I, dt, device)
+    router_w = expert_bias = gate = up = down = None
+    if E > 0:
+        router_w = _normal(g, (E, H), WEIGHT_STD, dt, device).to(torch.float32)
+        expert_bias = _bias(shape, g, device)
+        gate = _stacked(g, Ep, I, H, dt, device)
+        up = _stacked(g, Ep, I, H, dt, device)
+        down = _stacked(g, Ep, H, I, dt, device)
     sh_gate = sh_up = sh_down = None
     if not shape.shared_packed and S > 0:
         sh_gate = _normal(g, (S, H), WEIGHT_STD, dt, device)
         sh_up = _normal(g, (S, H), WEIGHT_STD, dt, device)
         sh_down = _normal(g, (H, S), WEIGHT_STD, dt, device)
+    pre_norm_w = post_norm_w = None
+    if shape.mlp_norm != "none":
+        centre = 1.0 if shape.mlp_norm == "rms" else 0.0
+        pre_norm_w = _normal(g, (H,), NORM_STD, torch.float32, device) + centre
+        post_norm_w = _normal(g, (H,), NORM_STD, torch.float32, device) + centre
 
     gx = torch.Generator(device=device)
     gx.manual_seed(shape.x_seed)
     X = _normal(gx, (shape.T, H), 1.0, dt, device)
 
     redraws = 0
-    if row_filter is not None and shape.T > 0:
+    if row_filter is not None and shape.T > 0 and E > 0:
         for attempt in range(max_attempts):
-            bad = row_filter(X.cpu(), router_w.cpu(), expert_bias.cpu())
+            extra = () if pre_norm_w is None else (pre_norm_w.cpu(),)
+            bad = row_filter(X.cpu(), router_w.cpu(), expert_bias.cpu(), *extra)
             bad = torch.as_tensor(bad, dtype=torch.bool)
             n_bad = int(bad.sum())
             if n_bad == 0:
@@ -232,7 +275,8 @@ def make_inputs(shape: MoeShape, device="cpu",
             raise RuntimeError(f"{shape.name}: rows still rejected after {max_attempts} redraws")
 
     return dict(X=X, router_w=router_w, expert_bias=expert_bias, gate=gate, up=up, down=down,
-                sh_gate=sh_gate, sh_up=sh_up, sh_down=sh_down, redraws=redraws)
+                sh_gate=sh_gate, sh_up=sh_up, sh_down=sh_down, pre_norm_w=pre_norm_w,
+                post_norm_w=post_norm_w, redraws=redraws)
 
 
 def expert_weights_bf16(inputs: dict) -> dict:

@@ -70,6 +70,11 @@ def _configure(L):
     L.oracle_expert.restype = ctypes.c_int
     L.oracle_act.argtypes = [ctypes.POINTER(OracleCfg), ctypes.c_double, ctypes.c_double]
     L.oracle_act.restype = ctypes.c_double
+    L.oracle_dense.argtypes = [ctypes.POINTER(OracleCfg), P, ctypes.c_int, P, P, P, ctypes.c_int, ctypes.c_int,
+                               P, P, ctypes.c_int]
+    L.oracle_dense.restype = ctypes.c_int
+    L.oracle_rmsnorm.argtypes = [P, ctypes.c_int, P, ctypes.c_double, ctypes.c_int, P]
+    L.oracle_rmsnorm.restype = ctypes.c_int
     return L
 
 
@@ -121,7 +126,10 @@ def make_cfg(H, E, k, I, S=0, shared_packed=False, score_func="sigmoid", route_n
 
 
 def cfg_from_shape(shape) -> OracleCfg:
-    """Oracle config from a workloads.MoeShape."""
+    """Oracle config from a workloads.MoeShape (E = 0: a dense MLP of width S)."""
+    if shape.E == 0:
+        return make_cfg(shape.H, 0, 0, 0, S=shape.S, act=shape.hidden_act, alpha=shape.act_alpha,
+                        limit=shape.act_limit, beta=shape.act_beta)
     return make_cfg(shape.H, shape.E, shape.k, shape.I, S=(0 if shape.shared_packed else shape.S),
                     shared_packed=shape.shared_packed, score_func=shape.score_func,
                     route_norm=shape.route_norm, route_scale=shape.route_scale,
@@ -257,12 +265,91 @@ def act(cfg: OracleCfg, g: float, u: float) -> float:
     return lib().oracle_act(ctypes.byref(cfg), float(g), float(u))
 
 
+def dense(cfg: OracleCfg, X, Wg, Wu, Wd, tokens=None, nthreads=0) -> np.ndarray:
+    """Dense MLP of width cfg.S (a dense prefix layer) for the listed tokens: [n,H] fp64."""
+    Xh, xd = _as_host(X)
+    T = Xh.shape[0]
+    Wgh, wd = _as_host(Wg)
+    Wuh, _ = _as_host(Wu)
+    Wdh, _ = _as_host(Wd)
+    tk, n = _tokens(tokens, T)
+    Y = np.empty((n, cfg.H))
+    if n == 0:
+        return Y
+    r = lib().oracle_dense(ctypes.byref(cfg), _ptr(Xh), xd, _ptr(Wgh), _ptr(Wuh), _ptr(Wdh), wd, n, _ptr(tk),
+                           _ptr(Y), int(nthreads))
+    if r < 0:
+        raise ValueError("oracle_dense rejected its arguments")
+    return Y
+
+
+def to_f64(a) -> np.ndarray:
+    """Exact fp64 values of an fp32 / bf16 array or tensor (bf16 from its bits)."""
+    h, d = _as_host(a)
+    if d == OR_BF16:
+        return (h.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return h.astype(np.float64)
+
+
+def round_to(a: np.ndarray, dtype: str) -> np.ndarray:
+    """fp64 values rounded to the activation dtype: fp32 (round to nearest even),
+    or bf16 as uint16 bits (fp32 first, then round to nearest even)."""
+    f = np.ascontiguousarray(a, dtype=np.float64).astype(np.float32)
+    if dtype == "f32":
+        return f
+    b = f.view(np.uint32)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def rmsnorm(X, w, eps: float, gemma: bool) -> np.ndarray:
+    """Row-wise RMSNorm of X [n,H] in fp64: x / sqrt(mean(x^2) + eps) * g, g = w or 1 + w."""
+    Xd = np.ascontiguousarray(to_f64(X) if not isinstance(X, np.ndarray) or X.dtype != np.float64 else X)
+    wd = np.ascontiguousarray(to_f64(w) if not isinstance(w, np.ndarray) or w.dtype != np.float64 else w)
+    n, H = Xd.shape
+    Y = np.empty_like(Xd)
+    for i in range(n):
+        if lib().oracle_rmsnorm(_ptr(Xd[i]), H, _ptr(wd), float(eps), int(bool(gemma)), _ptr(Y[i])) < 0:
+            raise ValueError("oracle_rmsnorm rejected its arguments")
+    return Y
+
+
+def normed_input(shape, X, w_pre) -> np.ndarray:
+    """The block's input after pre_mlp_norm, rounded to the activation dtype (the
+    MLP consumes it in that dtype): bf16 bits or fp32 values [T,H]."""
+    return round_to(rmsnorm(X, w_pre, shape.rms_norm_eps, shape.mlp_norm == "gemma"), shape.dtype)
+
+
+def block_output(shape, inputs: dict, tokens=None, nthreads=0) -> np.ndarray:
+    """Output of the layer for the listed tokens, fp64 [n,H].  E > 0: the MoE
+    block; E = 0: a dense MLP of width S.  With the sandwich norms
+    (shape.mlp_norm "rms" or "gemma"): out = X + post_norm(mlp(pre_norm(X))),
+    pre_norm's output rounded to the activation dtype."""
+    X = inputs["X"]
+    xin = X if shape.mlp_norm == "none" else normed_input(shape, X, inputs["pre_norm_w"])
+    cfg = cfg_from_shape(shape)
+    if shape.E == 0:
+        y = dense(cfg, xin, inputs["sh_gate"], inputs["sh_up"], inputs["sh_down"], tokens=tokens,
+                  nthreads=nthreads)
+    else:
+        y = forward(cfg, xin, inputs["router_w"], inputs["expert_bias"], inputs["gate"], inputs["up"],
+                    inputs["down"], inputs["sh_gate"], inputs["sh_up"], inputs["sh_down"], tokens=tokens,
+                    nthreads=nthreads)
+    if shape.mlp_norm == "none":
+        return y
+    x = to_f64(X)
+    if tokens is not None:
+        x = x[np.asarray(tokens)]
+    return x + rmsnorm(y, inputs["post_norm_w"], shape.rms_norm_eps, shape.mlp_norm == "gemma")
+
+
 def margin_filter(shape, min_margin: float = 1e-3, nthreads: int = 0):
     """Row filter for workloads.make_inputs: True for tokens whose gap between
-    the k-th and (k+1)-th biased scores is below ``min_margin``."""
+    the k-th and (k+1)-th biased scores is below ``min_margin`` (routing the
+    pre_mlp_norm output when the workload has the sandwich norms)."""
     cfg = cfg_from_shape(shape)
 
-    def _filter(X, Wr, b):
-        return route(cfg, X, Wr, b, nthreads=nthreads)["margin"] < min_margin
+    def _filter(X, Wr, b, w_pre=None):
+        xin = X if shape.mlp_norm == "none" else normed_input(shape, X, w_pre)
+        return route(cfg, xin, Wr, b, nthreads=nthreads)["margin"] < min_margin
 
     return _filter

@@ -42,6 +42,18 @@
  *      tensors (MiniMax-M3 issue: packed shared expert, fixed score 1.0)
  *        (HF AFMoE docs, "shared experts"; AfmoeConfig num_shared_experts)
  *   8. Y = sum_j w_j y_{idx_j} + y_shared
+ *
+ * Also, for the layers around and before the block:
+ *   - dense MLP of width W (the dense prefix layers: a plain MLP;
+ *       Arcee AFMoE issue, "Dense prefix"; HF AFMoE docs, AfmoeConfig
+ *       intermediate_size and num_dense_layers; MiniMax-M3 issue,
+ *       "Architecture specification": dense_intermediate_size), the same
+ *       expert MLP as step 6 with the layer's weights;
+ *   - RMSNorm of a row, y_h = x_h / sqrt(mean_h x_h^2 + eps) * g_h with
+ *       g = w, or g = 1 + w (Gemma style)
+ *       (Arcee AFMoE issue: pre_mlp_layernorm / post_mlp_layernorm in a
+ *        sandwich; HF AFMoE docs, AfmoeConfig rms_norm_eps; MiniMax-M3 issue:
+ *        Gemma-style RMSNorm, weight + 1, on all norms).
  */
 #include <math.h>
 #include <pthread.h>
@@ -191,7 +203,7 @@ typedef struct {
     int *idx;
     /* forward output */
     double *Y;
-    int next_is_forward;
+    int mode; /* 0 routing, 1 block forward, 2 dense MLP (width S, tensors Wgs/Wus/Wds) */
     int nthreads, tid;
 } job;
 
@@ -234,6 +246,17 @@ static void forward_token(const job *j, int i)
     free(idx);
 }
 
+static void dense_token(const job *j, int i)
+{
+    const oracle_cfg *c = j->c;
+    const int H = c->H;
+    const size_t t = (size_t)token_of(j, i);
+    double *x = (double *)malloc(sizeof(double) * H);
+    for (int h = 0; h < H; h++) x[h] = ld(j->X, j->xd, t * H + h);
+    expert_mlp(c, x, j->Wgs, j->Wus, j->Wds, j->wd, c->S, NULL, NULL, NULL, j->Y + (size_t)i * H);
+    free(x);
+}
+
 static void route_one(const job *j, int i)
 {
     const oracle_cfg *c = j->c;
@@ -248,8 +271,10 @@ static void *worker(void *arg)
 {
     const job *j = (const job *)arg;
     for (int i = j->tid; i < j->n; i += j->nthreads) {
-        if (j->next_is_forward)
+        if (j->mode == 1)
             forward_token(j, i);
+        else if (j->mode == 2)
+            dense_token(j, i);
         else
             route_one(j, i);
     }
@@ -343,8 +368,42 @@ int oracle_forward(const oracle_cfg *c, const void *X, int x_dtype, const float 
     j.tokens = tokens;
     j.n = n;
     j.Y = Y;
-    j.next_is_forward = 1;
+    j.mode = 1;
     return run_jobs(&j, nthreads);
+}
+
+/* Dense MLP of width c->S (router and experts unused) for n tokens: Y [n,H]
+ * doubles.  Wg, Wu: [S,H]; Wd: [H,S]; dtype w_dtype.  Returns threads used, or -1. */
+int oracle_dense(const oracle_cfg *c, const void *X, int x_dtype, const void *Wg, const void *Wu,
+                 const void *Wd, int w_dtype, int n, const int *tokens, double *Y, int nthreads)
+{
+    if (!c || c->H <= 0 || c->S <= 0 || !X || !Wg || !Wu || !Wd || !Y || n < 0) return -1;
+    job j;
+    memset(&j, 0, sizeof j);
+    j.c = c;
+    j.X = X;
+    j.xd = x_dtype;
+    j.Wgs = Wg;
+    j.Wus = Wu;
+    j.Wds = Wd;
+    j.wd = w_dtype;
+    j.tokens = tokens;
+    j.n = n;
+    j.Y = Y;
+    j.mode = 2;
+    return run_jobs(&j, nthreads);
+}
+
+/* RMSNorm of one row of H values: y_h = x_h / sqrt(mean_h x_h^2 + eps) * g_h,
+ * g_h = w_h (gemma = 0) or 1 + w_h (gemma = 1).  Returns 0, or -1. */
+int oracle_rmsnorm(const double *x, int H, const double *w, double eps, int gemma, double *y)
+{
+    if (!x || !w || !y || H <= 0 || eps < 0.0) return -1;
+    double ss = 0.0;
+    for (int h = 0; h < H; h++) ss += x[h] * x[h];
+    const double r = sqrt(ss / (double)H + eps);
+    for (int h = 0; h < H; h++) y[h] = x[h] / r * (gemma ? 1.0 + w[h] : w[h]);
+    return 0;
 }
 
 /* One expert MLP of width W on one token row x (H values of x_dtype), for

@@ -43,6 +43,15 @@ MUTANTS = [
     ("one routed slot dropped", "for (int s = 0; s < k; s++) {\n        const size_t e", "for (int s = 1; s < k; s++) {\n        const size_t e"),
     ("margin off by one", "cb[order[k - 1]] - cb[order[k]]", "cb[order[k - 2 < 0 ? 0 : k - 2]] - cb[order[k]]"),
     ("bf16 decoded with the wrong shift", "<< 16;", "<< 15;"),
+    # the layers around the block
+    ("dense MLP reads the routed width", "expert_mlp(c, x, j->Wgs, j->Wus, j->Wds, j->wd, c->S,",
+     "expert_mlp(c, x, j->Wgs, j->Wus, j->Wds, j->wd, c->S / 2,"),
+    ("rmsnorm without eps", "sqrt(ss / (double)H + eps)", "sqrt(ss / (double)H)"),
+    ("rmsnorm over H - 1", "sqrt(ss / (double)H + eps)", "sqrt(ss / (double)(H - 1) + eps)"),
+    ("rmsnorm by the mean square, not its root", "const double r = sqrt(ss / (double)H + eps);",
+     "const double r = ss / (double)H + eps;"),
+    ("Gemma norm without the + 1", "(gemma ? 1.0 + w[h] : w[h])", "(gemma ? w[h] : w[h])"),
+    ("norm weight ignored", "(gemma ? 1.0 + w[h] : w[h])", "(gemma ? 1.0 + w[h] : 1.0)"),
 ]
 
 PIN_TESTS = [(name, fn) for name, fn in inspect.getmembers(pins, inspect.isfunction)

@@ -193,6 +193,13 @@ def test_page_constants_match_workloads():
     assert m.shared_packed and m.stacked_experts - 1 == vals["m3_packed_shared_index"]
     assert (m.act_alpha, m.act_limit, m.act_beta) == (
         vals["swigluoai_alpha"], vals["swigluoai_limit"], vals["swigluoai_beta"])
+    da, dm = wl.WORKLOADS["dense_afmoe_prefill"], wl.WORKLOADS["dense_m3"]
+    assert (da.H, da.S, da.E) == (vals["afmoe_hidden_size"], vals["afmoe_intermediate_size"], 0)
+    assert (dm.H, dm.S, dm.E) == (vals["m3_hidden_size"], vals["m3_dense_intermediate_size"], 0)
+    assert dm.hidden_act == "swigluoai" and dm.mlp_norm == wl.WORKLOADS["m3_sandwich"].mlp_norm == "gemma"
+    assert da.rms_norm_eps == wl.WORKLOADS["afmoe_prefill_sandwich"].rms_norm_eps == vals["afmoe_rms_norm_eps"]
+    # Gemma-style: weight + 1 (the oracle's offset, on a unit input of one element)
+    assert oracle.rmsnorm(np.ones((1, 1)), np.zeros(1), 0.0, True)[0, 0] == vals["m3_gemma_norm_offset"]
 
 
 # ------------------------------------------------------------ expert MLPs
@@ -315,3 +322,119 @@ def test_margin_filter_drives_generator_redraws():
     # same seed, same draws
     inp2 = wl.make_inputs(shape, "cpu", row_filter=oracle.margin_filter(shape))
     assert torch.equal(inp["X"], inp2["X"]) and inp["redraws"] == inp2["redraws"]
+
+
+# ------------------------------------------------ layers around the block
+
+def test_dense_mlp_equals_numpy_swiglu_and_a_zero_scaled_block():
+    """A dense prefix layer is a plain MLP: numpy matmuls of the same weights; and
+    the MoE block with route_scale 0 (routed experts contribute nothing) and the
+    dense weights as its shared expert gives the same output."""
+    X, Wr, b, Wg, Wu, Wd, sh = _tiny(11, S=56)
+    cfg = oracle.make_cfg(24, 0, 0, 0, S=56)
+    Y = oracle.dense(cfg, X, *sh)
+    ref = _mlp_np(X, *sh)
+    assert np.allclose(Y, ref, rtol=1e-12, atol=1e-12)
+    blk = oracle.make_cfg(24, 8, 3, 40, S=56, route_scale=0.0)
+    Yb = oracle.forward(blk, X, Wr, b, Wg, Wu, Wd, *sh)
+    assert np.allclose(Y, Yb, rtol=1e-12, atol=1e-12)
+    # a subset of tokens gives the same rows
+    assert np.array_equal(oracle.dense(cfg, X, *sh, tokens=[5, 0, 2]), Y[[5, 0, 2]])
+
+
+def test_dense_swigluoai_against_hand_activation():
+    X, *_rest, sh = _tiny(12, S=32)
+    cfg = oracle.make_cfg(24, 0, 0, 0, S=32, act="swigluoai")
+
+    def clamp_glu(g, u):
+        gg = np.minimum(g, 7.0)
+        uu = np.clip(u, -7.0, 7.0)
+        return gg * expit(1.702 * gg) * (uu + 1.0)
+
+    Xs = X * 20  # drive the clamps
+    Y = oracle.dense(cfg, Xs, *sh)
+    assert np.allclose(Y, _mlp_np(Xs, *sh, act=clamp_glu), rtol=1e-12, atol=1e-10)
+
+
+def test_rmsnorm_closed_forms():
+    H = 48
+    w = _rng(13).uniform(0.5, 1.5, H)
+    # a constant row a * 1: mean square a^2, so y = a / sqrt(a^2 + eps) * w
+    for a, eps in ((0.7, 1e-5), (-3.0, 1e-6), (2.0, 0.0)):
+        y = oracle.rmsnorm(np.full((1, H), a), w, eps, False)[0]
+        assert np.allclose(y, a / math.sqrt(a * a + eps) * w, rtol=1e-15, atol=0)
+    # with unit weights and eps = 0 the output has mean square exactly 1
+    x = _rng(14).standard_normal((5, H))
+    y = oracle.rmsnorm(x, np.ones(H), 0.0, False)
+    assert np.allclose((y * y).mean(axis=1), 1.0, rtol=1e-14)
+    # sign and direction are kept: y is a positive multiple of x per row
+    ratio = y / x
+    assert np.allclose(ratio, ratio[:, :1], rtol=1e-13) and (ratio > 0).all()
+
+
+def test_rmsnorm_scale_invariance_and_gemma_offset():
+    x = _rng(15).standard_normal((4, 40))
+    w = _rng(16).standard_normal(40) * 0.1
+    # eps = 0: multiplying a row by 4 leaves the output unchanged (exact in binary)
+    assert np.array_equal(oracle.rmsnorm(4 * x, w, 0.0, False), oracle.rmsnorm(x, w, 0.0, False))
+    # Gemma style scales by 1 + w: the plain form with weight 1 + w
+    g = oracle.rmsnorm(x, w, 1e-5, True)
+    assert np.allclose(g, oracle.rmsnorm(x, 1.0 + w, 1e-5, False), rtol=1e-15, atol=1e-15)
+    # Gemma with w = 0 is the unweighted norm
+    assert np.array_equal(oracle.rmsnorm(x, np.zeros(40), 1e-5, True), oracle.rmsnorm(x, np.ones(40), 1e-5, False))
+
+
+def test_round_to_bf16_is_nearest_even():
+    # bf16 keeps 8 significant bits: the spacing above 1 is 2^-7
+    v = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1.0 + 3 * 2 ** -9, -2.5, 1.0 + 2 ** -7],
+                 dtype=np.float64)
+    back = oracle.to_f64(oracle.round_to(v, "bf16"))
+    # ties go to the even significand: 1 + 2^-8 -> 1, 1 + 3*2^-8 -> 1 + 2^-6;
+    # 1 + 3*2^-9 is nearer 1 + 2^-7; exact bf16 values stay
+    assert np.array_equal(back, [1.0, 1.0, 1.0 + 2 ** -6, 1.0 + 2 ** -7, -2.5, 1.0 + 2 ** -7])
+
+
+def _sandwich_shape(mlp_norm, E=8):
+    base = wl.TINY.replace(name="sw", T=9, hidden_size=64, num_experts=E, num_experts_per_tok=min(3, E),
+                           moe_intermediate_size=32, shared_intermediate_size=48, dtype="bf16",
+                           mlp_norm=mlp_norm)
+    if E == 0:
+        base = base.replace(num_experts_per_tok=0, moe_intermediate_size=0)
+    return base
+
+
+@pytest.mark.parametrize("mlp_norm", ["rms", "gemma"])
+@pytest.mark.parametrize("E", [8, 0])
+def test_sandwich_identity_when_the_mlp_outputs_zero(mlp_norm, E):
+    """out = X + post_norm(mlp(pre_norm(X))): with zero down weights the MLP
+    output is 0, post_norm(0) = 0 (eps > 0), so out equals X exactly."""
+    shape = _sandwich_shape(mlp_norm, E)
+    inputs = wl.make_inputs(shape)
+    inputs["sh_down"] = torch.zeros_like(inputs["sh_down"])
+    if E:
+        inputs["down"] = torch.zeros_like(inputs["down"])
+    out = oracle.block_output(shape, inputs)
+    assert np.array_equal(out, oracle.to_f64(inputs["X"]))
+
+
+@pytest.mark.parametrize("mlp_norm", ["rms", "gemma"])
+@pytest.mark.parametrize("E", [8, 0])
+def test_sandwich_residual_and_input_scale_invariance(mlp_norm, E):
+    """With eps = 0, scaling X by 4 scales the residual term by 4 and leaves the
+    normalised branch unchanged: out(4X) - 4X == out(X) - X (up to the rounding
+    of adding and removing the residual in fp64).  And the branch is the post
+    norm of the plain layer on the rounded pre-norm output (the layer without
+    norms, fed pre_norm(X) as its input)."""
+    shape = _sandwich_shape(mlp_norm, E).replace(rms_norm_eps=0.0)
+    inputs = wl.make_inputs(shape)
+    out = oracle.block_output(shape, inputs)
+    x = oracle.to_f64(inputs["X"])
+    scaled = dict(inputs, X=(inputs["X"].float() * 4).to(torch.bfloat16))
+    out4 = oracle.block_output(shape, scaled)
+    assert np.allclose(out4 - 4 * x, out - x, rtol=0, atol=1e-13)
+    plain = shape.replace(mlp_norm="none")
+    xn_bits = oracle.normed_input(shape, inputs["X"], inputs["pre_norm_w"])
+    xn = torch.from_numpy(xn_bits.view(np.int16)).view(torch.bfloat16)
+    y = oracle.block_output(plain, dict(inputs, X=xn))
+    g = mlp_norm == "gemma"
+    assert np.allclose(out - x, oracle.rmsnorm(y, oracle.to_f64(inputs["post_norm_w"]), 0.0, g), rtol=0, atol=1e-13)
