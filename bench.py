@@ -2,7 +2,10 @@
 """Throughput of the token-choice MoE FFN block (AFMoE / MiniMax-M3) on GB300.
 
 One step = one moe_forward over one batch of T synthetic tokens (router,
-dispatch sort, gate/up + activation, down, combine), inputs resident in HBM.
+dispatch sort, gate/up + activation, down, combine; with the sandwich norms
+also the pre-MLP RMSNorm and, inside the combine, the post-MLP RMSNorm and the
+residual add; a dense prefix layer: its MLP GEMMs and the combine), inputs
+resident in HBM.
 L2 is flushed (a 256 MiB write) before every step, outside the timed events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
@@ -46,11 +49,17 @@ def work_model(shape, U: int):
 
     FLOPs  F = T (2HE + 6HIk + 6HS); bytes B = U*3HI*2 + 3HS*2 + 4EH + 4E + 2*2TH,
     U = experts that received at least one token (the packed shared expert's
-    weights are its 3HS*2 bytes).  Intermediate buffers are implementation
-    traffic and are not counted."""
+    weights are its 3HS*2 bytes; a dense layer has E = k = U = 0 and its MLP of
+    width S as the "shared" term).  With the sandwich norms add the two fp32
+    norm weights (8H bytes) and 8TH FLOPs (square, sum, scale and gain per
+    element of both norms, and the residual add counted with them).
+    Intermediate buffers are implementation traffic and are not counted."""
     T, H, E, k, I, S = shape.T, shape.H, shape.E, shape.k, shape.I, shape.S
     F = T * (2 * H * E + 6 * H * I * k + 6 * H * S)
     B = U * 3 * H * I * 2 + 3 * H * S * 2 + 4 * E * H + 4 * E + 2 * 2 * T * H
+    if shape.mlp_norm != "none":
+        F += 8 * T * H
+        B += 8 * H
     kernels = {
         "gate_up": dict(flops=4 * T * H * (k * I + S), bytes=(U * 2 * H * I + 2 * H * S) * 2 + 2 * T * H),
         "down": dict(flops=2 * T * H * (k * I + S), bytes=(U * H * I + H * S) * 2 + 2 * T * H),
@@ -154,8 +163,10 @@ def run_ours(args, shape):
     torch.cuda.synchronize()
     if blk.sync_status() != capi.MOE_OK:
         raise SystemExit("device error during warm-up")
-    idx = blk.inspect(capi.MOE_BUF_TOPK_IDX, shape.T * shape.k, torch.int32)
-    U = int(torch.unique(idx).numel())
+    U = 0
+    if shape.E > 0:
+        idx = blk.inspect(capi.MOE_BUF_TOPK_IDX, shape.T * shape.k, torch.int32)
+        U = int(torch.unique(idx).numel())
     launches = blk.stats().kernel_launches
     path = blk.stats().path
     names = blk.stage_names()
@@ -293,7 +304,7 @@ def run_ours(args, shape):
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, U(-0.1,0.1) or Zipf bias)",
         "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "E": shape.E, "k": shape.k,
                    "I": shape.I, "S": shape.S, "shared_packed": shape.shared_packed,
-                   "hidden_act": shape.hidden_act, "path": {1: "decode", 2: "grouped", 3: "swapped"}[path],
+                   "hidden_act": shape.hidden_act, "mlp_norm": shape.mlp_norm, "path": {1: "decode", 2: "grouped", 3: "swapped"}[path],
                    "parallelism": f"replicas{world}",
                    "l2": ("not flushed: inputs larger than L2" if args.no_flush else
                           "flushed before every step (256 MiB write), flush outside the timed events")},
@@ -353,7 +364,7 @@ def cpu_baseline(shape, inputs, budget_s=10.0):
     cores = os.cpu_count() or 1
     n = shape.T
     t0 = time.perf_counter()
-    oracle.forward_inputs(shape, host, tokens=list(range(min(n, cores))), nthreads=cores)
+    oracle.block_output(shape, host, tokens=list(range(min(n, cores))), nthreads=cores)
     per_tok = (time.perf_counter() - t0) / min(n, cores)
     n = max(1, min(shape.T, int(budget_s / 3 / max(per_tok, 1e-9))))
     toks = list(range(n))
@@ -361,7 +372,7 @@ def cpu_baseline(shape, inputs, budget_s=10.0):
     t_start = time.perf_counter()
     while len(times) < 3 or time.perf_counter() - t_start < budget_s:
         t0 = time.perf_counter()
-        oracle.forward_inputs(shape, host, tokens=toks, nthreads=cores)
+        oracle.block_output(shape, host, tokens=toks, nthreads=cores)
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_start > 3 * budget_s:
             break
@@ -383,16 +394,16 @@ def run_reference(args, shape):
     cores = os.cpu_count() or 1
     # size each step to about one second of oracle work
     t0 = time.perf_counter()
-    oracle.forward_inputs(shape, inputs, tokens=list(range(min(shape.T, cores))), nthreads=cores)
+    oracle.block_output(shape, inputs, tokens=list(range(min(shape.T, cores))), nthreads=cores)
     per_tok = (time.perf_counter() - t0) / min(shape.T, cores)
     n = max(1, min(shape.T, int(1.0 / max(per_tok, 1e-9))))
     toks = list(range(n))
     for _ in range(args.warmup):
-        oracle.forward_inputs(shape, inputs, tokens=toks, nthreads=cores)
+        oracle.block_output(shape, inputs, tokens=toks, nthreads=cores)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.forward_inputs(shape, inputs, tokens=toks, nthreads=cores)
+        oracle.block_output(shape, inputs, tokens=toks, nthreads=cores)
         times.append(time.perf_counter() - t0)
     s = sum(times) / len(times)
     value = n / s
@@ -403,7 +414,7 @@ def run_reference(args, shape):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded, same recipe as the GPU arm)",
         "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "E": shape.E, "k": shape.k,
-                   "I": shape.I, "S": shape.S, "tokens_per_step": n},
+                   "I": shape.I, "S": shape.S, "mlp_norm": shape.mlp_norm, "tokens_per_step": n},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -24,11 +24,14 @@ STATUS_NAMES = ["MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR
 MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
 MOE_ACT_SILU, MOE_ACT_SWIGLU_OAI = 0, 1
 MOE_DTYPE_BF16, MOE_DTYPE_F32 = 0, 1
+MOE_NORM_NONE, MOE_NORM_RMS, MOE_NORM_GEMMA = 0, 1, 2
 MOE_OPT_PATH, MOE_OPT_WAIT_LIMIT_NS, MOE_OPT_STAGE_EVENTS, MOE_OPT_FUSE_EXPERTS, MOE_OPT_PREFETCH = 0, 1, 2, 3, 4
 MOE_OPT_TRACE = 5
 MOE_OPT_GEMM_PAIR = 6
 MOE_BUF_GEMM_STATS = 6
 MOE_BUF_ROUTER_STATS = 7
+MOE_BUF_NORMED_X = 8
+MOE_BUF_SHARED_HIDDEN = 9
 TRACE_FIELDS = 5  # first begin, first ready, last ready, first end, last end
 PATH_AUTO, PATH_DECODE, PATH_GROUPED, PATH_SWAPPED = 0, 1, 2, 3
 (MOE_BUF_TOPK_IDX, MOE_BUF_TOPK_W, MOE_BUF_EXPERT_OFFS, MOE_BUF_SORTED_TOKEN, MOE_BUF_SLOT,
@@ -43,13 +46,14 @@ class MoeConfig(ctypes.Structure):
         ("shared_packed", ctypes.c_int), ("score_func", ctypes.c_int), ("route_norm", ctypes.c_int),
         ("route_scale", ctypes.c_float), ("hidden_act", ctypes.c_int), ("act_alpha", ctypes.c_float),
         ("act_limit", ctypes.c_float), ("act_beta", ctypes.c_float), ("act_dtype", ctypes.c_int),
-        ("max_tokens", ctypes.c_int),
+        ("max_tokens", ctypes.c_int), ("mlp_norm", ctypes.c_int), ("rms_norm_eps", ctypes.c_float),
     ]
 
 
 class MoeWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("router_w", "expert_bias", "gate", "up", "down", "sh_gate", "sh_up", "sh_down")]
+                ("router_w", "expert_bias", "gate", "up", "down", "sh_gate", "sh_up", "sh_down",
+                 "pre_norm_w", "post_norm_w")]
 
 
 class MoeStats(ctypes.Structure):
@@ -125,7 +129,9 @@ def config_from_shape(shape, max_tokens: int = None) -> MoeConfig:
         hidden_act={"silu": MOE_ACT_SILU, "swigluoai": MOE_ACT_SWIGLU_OAI}[shape.hidden_act],
         act_alpha=shape.act_alpha, act_limit=shape.act_limit, act_beta=shape.act_beta,
         act_dtype={"bf16": MOE_DTYPE_BF16, "f32": MOE_DTYPE_F32}[shape.dtype],
-        max_tokens=max(1, shape.T if max_tokens is None else max_tokens))
+        max_tokens=max(1, shape.T if max_tokens is None else max_tokens),
+        mlp_norm={"none": MOE_NORM_NONE, "rms": MOE_NORM_RMS, "gemma": MOE_NORM_GEMMA}[shape.mlp_norm],
+        rms_norm_eps=shape.rms_norm_eps)
 
 
 def _ptr(t):
@@ -143,7 +149,8 @@ class MoeBlock:
 
     weights: dict with router_w [E,H] fp32, expert_bias [E] fp32 (or None),
     gate/up [E',I,H], down [E',H,I] bf16 and sh_gate/sh_up [S,H], sh_down [H,S]
-    bf16 (or None).  The tensors are kept referenced for the handle's lifetime.
+    bf16 (or None), and pre_norm_w / post_norm_w [H] fp32 with the sandwich
+    norms.  The tensors are kept referenced for the handle's lifetime.
     """
 
     def __init__(self, config: MoeConfig, weights: dict):
@@ -153,7 +160,7 @@ class MoeBlock:
         self._keep = {k: v for k, v in weights.items() if isinstance(v, torch.Tensor)}
         w = MoeWeights(**{k: (None if weights.get(k) is None else weights[k].data_ptr())
                           for k in ("router_w", "expert_bias", "gate", "up", "down", "sh_gate",
-                                    "sh_up", "sh_down")})
+                                    "sh_up", "sh_down", "pre_norm_w", "post_norm_w")})
         h = ctypes.c_void_p()
         check(load().moe_create(ctypes.byref(config), ctypes.byref(w), ctypes.byref(h)), "moe_create")
         self.h = h
@@ -231,6 +238,7 @@ def block_from_inputs(shape, inputs: dict, max_tokens: int = None) -> MoeBlock:
     """MoeBlock over a workloads.make_inputs() dict on the GPU (expert weights
     rounded to bf16 when the workload stores them in fp32)."""
     from .workloads import expert_weights_bf16
-    w = dict(router_w=inputs["router_w"], expert_bias=inputs["expert_bias"], **expert_weights_bf16(inputs))
+    w = dict(router_w=inputs["router_w"], expert_bias=inputs["expert_bias"], **expert_weights_bf16(inputs),
+             pre_norm_w=inputs.get("pre_norm_w"), post_norm_w=inputs.get("post_norm_w"))
     blk = MoeBlock(config_from_shape(shape, max_tokens), w)
     return blk

@@ -178,8 +178,28 @@ struct CombineArgs {
     void *Y;                     // [T, H]
     int y_f32;
     unsigned long long *trace;
+    // post_mlp norm and residual (norm != 0): Y = residual + y * g / sqrt(mean(y^2) + eps),
+    // g = post_w (norm 1) or 1 + post_w (norm 2); residual in Y's dtype
+    int norm;
+    float eps;
+    const float *post_w;
+    const void *residual;
 };
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
+
+// pre_mlp norm of each token row: out = x * g / sqrt(mean(x^2) + eps), g = w (norm 1)
+// or 1 + w (norm 2), in the dtype of X (x_f32), one warp per row
+struct NormArgs {
+    const void *X;
+    int x_f32;
+    int T, H;
+    const float *w;
+    int norm;
+    float eps;
+    void *out;
+    unsigned long long *trace;
+};
+cudaError_t launch_rmsnorm(const NormArgs &a, cudaStream_t s);
 
 // ------------------------------------------- tcgen05 grouped GEMMs (K3/K4/K5)
 constexpr int kGemmBM = 128;   // rows (tokens) per tile: the MMA's M

@@ -66,6 +66,10 @@ struct moe_handle {
     int device = 0, num_sms = 0;
     int H = 0, E = 0, Ep = 0, k = 0, I = 0, S = 0;  // S: shared width actually used (I when packed)
     bool has_shared = false, x_f32 = false;
+    bool dense = false;        // num_experts == 0: a dense MLP layer (the shared segments only)
+    int norm = 0;              // moe_norm of the sandwich norms
+    float eps = 0.f;
+    void *x_norm = nullptr;    // pre_mlp norm output [max_tokens, H] in the activation dtype
     const bf16 *sh_gate = nullptr, *sh_up = nullptr, *sh_down = nullptr;  // shared tensors (or slice E)
     int path_opt = kPathAuto;
     unsigned long long wait_ns = 500000000ull;
@@ -133,8 +137,32 @@ moe_status validate_config(const moe_config *c, int *S_eff) {
     if (c->hidden_size < 64 || c->hidden_size % 64 != 0 || c->hidden_size > 8192)
         return fail(MOE_ERR_UNSUPPORTED, "hidden_size %d: need a multiple of 64 in [64, 8192]",
                     c->hidden_size);
+    if (c->mlp_norm != MOE_NORM_NONE && c->mlp_norm != MOE_NORM_RMS && c->mlp_norm != MOE_NORM_GEMMA)
+        return fail(MOE_ERR_INVALID_ARG, "mlp_norm %d", c->mlp_norm);
+    if (c->mlp_norm != MOE_NORM_NONE && !(std::isfinite(c->rms_norm_eps) && c->rms_norm_eps >= 0.f))
+        return fail(MOE_ERR_INVALID_ARG, "rms_norm_eps must be finite and >= 0");
+    if (c->num_shared_experts < 0 || c->shared_intermediate_size < 0)
+        return fail(MOE_ERR_INVALID_ARG, "negative shared expert count or width");
+    if (c->num_experts == 0) {
+        // a dense MLP layer: no router, the shared tensors are its gate/up/down
+        if (c->num_experts_per_tok != 0 || c->shared_packed)
+            return fail(MOE_ERR_INVALID_ARG, "a dense layer (num_experts 0) has num_experts_per_tok 0, no packing");
+        const int S = c->shared_intermediate_size;
+        if (S < 64 || S % 64 != 0 || S > 16384)
+            return fail(MOE_ERR_UNSUPPORTED, "dense width %d: need a multiple of 64 in [64, 16384]", S);
+        if (c->hidden_act != MOE_ACT_SILU && c->hidden_act != MOE_ACT_SWIGLU_OAI)
+            return fail(MOE_ERR_INVALID_ARG, "hidden_act %d", c->hidden_act);
+        if (c->act_dtype == MOE_DTYPE_F32)  // the dense layers run bf16 activations
+            return fail(MOE_ERR_UNSUPPORTED, "a dense layer takes bf16 activations");
+        if (c->act_dtype != MOE_DTYPE_BF16)
+            return fail(MOE_ERR_INVALID_ARG, "act_dtype %d", c->act_dtype);
+        if (c->max_tokens < 1 || c->max_tokens > (1 << 24))
+            return fail(MOE_ERR_INVALID_ARG, "max_tokens %d: need 1..2^24", c->max_tokens);
+        *S_eff = S;
+        return MOE_OK;
+    }
     if (c->num_experts < 1 || c->num_experts > 256)
-        return fail(MOE_ERR_UNSUPPORTED, "num_experts %d: need 1..256", c->num_experts);
+        return fail(MOE_ERR_UNSUPPORTED, "num_experts %d: need 0 (dense) or 1..256", c->num_experts);
     if (c->num_experts_per_tok < 1 || c->num_experts_per_tok > c->num_experts ||
         c->num_experts_per_tok > 16)
         return fail(MOE_ERR_INVALID_ARG, "num_experts_per_tok %d: need 1..min(num_experts, 16)",
@@ -143,8 +171,6 @@ moe_status validate_config(const moe_config *c, int *S_eff) {
         c->moe_intermediate_size > 8192)
         return fail(MOE_ERR_UNSUPPORTED, "moe_intermediate_size %d: need a multiple of 64 in [64, 8192]",
                     c->moe_intermediate_size);
-    if (c->num_shared_experts < 0 || c->shared_intermediate_size < 0)
-        return fail(MOE_ERR_INVALID_ARG, "negative shared expert count or width");
     int S = 0;
     if (c->shared_packed) {
         if (c->shared_intermediate_size != 0 && c->shared_intermediate_size != c->moe_intermediate_size)
@@ -206,6 +232,7 @@ void carve(moe_handle *h, void *base) {
     h->ys = h->has_shared ? c.take<bf16>(base, MT * H) : nullptr;
     h->ys2 = h->has_shared ? c.take<bf16>(base, MT * H) : nullptr;
     h->x_stage = c.take<char>(base, MT * H * elt);
+    h->x_norm = h->norm ? c.take<char>(base, MT * H * elt) : nullptr;
     h->y_stage = c.take<char>(base, MT * H * elt);
     h->wr_parts = c.take<bf16>(base, 3 * E * H);
     h->trace = c.take<unsigned long long>(base, MOE_TRACE_FIELDS * moe_handle::kMaxStages);
@@ -229,6 +256,7 @@ moe_status build_maps(moe_handle *h) {
         r = (call);                                                                      \
         if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", #call, (int)r); \
     } while (0)
+    if (!h->dense) {
     MAP(moe::encode_map_a(&h->m_xsorted, h->x_sorted, MT * k, H));
     MAP(moe::encode_map_a(&h->m_hbuf, h->hbuf, MT * k, I));
     MAP(moe::encode_map_a_kb2(&h->m_xs2, h->x_sorted, MT * k, H));
@@ -243,10 +271,13 @@ moe_status build_maps(moe_handle *h) {
     MAP(moe::encode_map_b(&h->m_gate64, h->w.gate, Ep, I, H, 64));
     MAP(moe::encode_map_b(&h->m_up64, h->w.up, Ep, I, H, 64));
     MAP(moe::encode_map_b(&h->m_down128, h->w.down, Ep, H, I, 128));
+    }
     for (int v = 0; v < 2; ++v) {
         const int n = v ? 64 : 32;
-        MAP(moe::encode_map_a_box(&h->m_xs_n[v], h->x_sorted, MT * k, H, n));
-        MAP(moe::encode_map_a_box(&h->m_hb_n[v], h->hbuf, MT * k, I, n));
+        if (!h->dense) {
+            MAP(moe::encode_map_a_box(&h->m_xs_n[v], h->x_sorted, MT * k, H, n));
+            MAP(moe::encode_map_a_box(&h->m_hb_n[v], h->hbuf, MT * k, I, n));
+        }
         if (h->has_shared) MAP(moe::encode_map_a_box(&h->m_hs_n[v], h->hs, MT, S, n));
         if (h->has_shared && h->x_f32) MAP(moe::encode_map_a_box(&h->m_xbf_n[v], h->x_bf16, MT, H, n));
     }
@@ -470,12 +501,15 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     const bool pair = h->pair_now;
     g.pair = pair ? 1 : 0;
     g.num_ctas = pair ? h->num_sms / 2 * 2 : h->num_sms;
-    for (auto &m : g.maps) m = h->m_xsorted;  // unused slots hold a valid descriptor
-    g.maps[kXs] = pair ? h->m_xs2 : h->m_xsorted;
-    g.maps[kHb] = pair ? h->m_hb2 : h->m_hbuf;
-    g.maps[kG] = pair ? h->m_gate2 : h->m_gate;
-    g.maps[kU] = pair ? h->m_up2 : h->m_up;
-    g.maps[kD] = pair ? h->m_down2 : h->m_down;
+    // unused slots hold a valid descriptor (a dense layer has only the shared ones)
+    for (auto &m : g.maps) m = h->dense ? h->m_hs : h->m_xsorted;
+    if (!h->dense) {
+        g.maps[kXs] = pair ? h->m_xs2 : h->m_xsorted;
+        g.maps[kHb] = pair ? h->m_hb2 : h->m_hbuf;
+        g.maps[kG] = pair ? h->m_gate2 : h->m_gate;
+        g.maps[kU] = pair ? h->m_up2 : h->m_up;
+        g.maps[kD] = pair ? h->m_down2 : h->m_down;
+    }
     if (h->has_shared) {
         if (h->x_f32) {
             g.maps[kX] = pair ? h->m_xbf2 : h->m_xbf16;
@@ -520,9 +554,9 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     sdn2.out = h->ys2;
     if (fused) {
         int ns = 0;
-        g.seg[ns++] = gu;
+        if (!h->dense) g.seg[ns++] = gu;
         if (h->has_shared) g.seg[ns++] = sgu;
-        g.seg[ns++] = dn;
+        if (!h->dense) g.seg[ns++] = dn;
         if (h->has_shared) g.seg[ns++] = sdn;
         if (h->has_shared && split) g.seg[ns++] = sdn2;
         g.num_segs = ns;
@@ -531,21 +565,17 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         g.stats = h->trace_on ? h->gemm_stats : nullptr;
         return launched(h, moe::launch_gemm_tc(g, s), "experts_gemm", n, s);
     }
-    g.seg[0] = gu;
-    g.num_segs = 1;
-    if (h->has_shared) {
-        g.seg[1] = sgu;
-        g.num_segs = 2;
-    }
+    g.num_segs = 0;
+    if (!h->dense) g.seg[g.num_segs++] = gu;
+    if (h->has_shared) g.seg[g.num_segs++] = sgu;
     g.tile_counter = pair ? nullptr : h->tile_counters;
     g.trace = trace_slot(h, *n);
     moe_status st = launched(h, moe::launch_gemm_tc(g, s), "gate_up_gemm", n, s);
     if (st != MOE_OK) return st;
-    g.seg[0] = dn;
-    g.num_segs = 1;
+    g.num_segs = 0;
+    if (!h->dense) g.seg[g.num_segs++] = dn;
     if (h->has_shared) {
-        g.seg[1] = sdn;
-        g.num_segs = 2;
+        g.seg[g.num_segs++] = sdn;
         if (split) g.seg[g.num_segs++] = sdn2;
     }
     g.tile_counter = pair ? nullptr : h->tile_counters + 1;
@@ -648,12 +678,13 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     if (path == kPathAuto)
         path = T <= kDecodeMaxTokens ? kPathDecode
                                      : (slots <= (long long)kSwapMaxTokensPerExpert * h->E ? kPathSwapped : kPathGrouped);
+    if (h->dense) path = kPathGrouped;  // a dense layer: the grouped GEMM's shared segments
     const int n_tok = slots <= 24ll * h->E ? 32 : 64;  // token tile of the swapped GEMMs
     h->ev_recorded = 0;
     // Decode-sized batches touch nearly every expert (about two or more tokens
     // per expert expected): while the routing kernels run, a side stream warms
     // L2 with the first experts' gate and up slices, the fused GEMM's first tiles.
-    const bool prefetch = h->prefetch_opt && path == kPathGrouped && h->fuse_experts &&
+    const bool prefetch = h->prefetch_opt && !h->dense && path == kPathGrouped && h->fuse_experts &&
                           slots >= 2ll * h->E && h->side != nullptr;
     if (prefetch) {
         const unsigned long long slice = (unsigned long long)h->I * h->H * 2;
@@ -673,8 +704,10 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
             e = cudaMemsetAsync(h->router_stats, 0, moe::kRouterStats * sizeof(unsigned long long), s);
         if (e != cudaSuccess) return cuda_fail(e, "trace reset");
     }
+    // CTA pairs once the weight tiles are reused by 256 rows on average (a dense
+    // layer: T >= 256)
     h->pair_now = path == kPathGrouped && h->num_sms >= 2 &&
-                  (h->pair_opt == 1 || (h->pair_opt == 2 && slots >= 256ll * h->E));
+                  (h->pair_opt == 1 || (h->pair_opt == 2 && (h->dense ? T >= 256 : slots >= 256ll * h->E)));
     {
         // few shared down tiles (a quarter of the SMs or less) and an even number of
         // k-blocks: split the shared down projection's K in two
@@ -683,20 +716,37 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
                               sh_tiles * 4 <= h->num_sms;
     }
     mark(h, 0, s);
-    moe_status st = run_front(h, X, T, s, &n,
-                              path == kPathSwapped ? n_tok : (h->pair_now ? 2 * moe::kGemmBM : moe::kGemmBM));
+    moe_status st = MOE_OK;
+    const void *Xm = X;  // the MLP's input: X, or pre_mlp_norm(X)
+    if (h->norm) {
+        moe::NormArgs na{X, h->x_f32 ? 1 : 0, T, h->H, h->w.pre_norm_w, h->norm, h->eps, h->x_norm,
+                         trace_slot(h, n)};
+        st = launched(h, moe::launch_rmsnorm(na, s), "pre_norm", &n, s);
+        Xm = h->x_norm;
+    }
+    if (st == MOE_OK && h->dense) {
+        // no router and no dispatch: zero what the dispatch would have zeroed for the GEMM
+        cudaError_t e = cudaMemsetAsync(h->ready + h->ready_shared_base, 0,
+                                        sizeof(int) * (size_t)(2 * ((T + 255) / 256) + 2), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(h->tile_counters, 0, 2 * sizeof(int), s);
+        if (e != cudaSuccess) st = cuda_fail(e, "counter reset");
+    } else if (st == MOE_OK) {
+        st = run_front(h, Xm, T, s, &n,
+                       path == kPathSwapped ? n_tok : (h->pair_now ? 2 * moe::kGemmBM : moe::kGemmBM));
+    }
     if (st == MOE_OK) {
         if (path == kPathDecode)
-            st = run_decode(h, X, T, s, &n);
+            st = run_decode(h, Xm, T, s, &n);
         else if (path == kPathSwapped)
-            st = run_swapped(h, X, T, s, &n, n_tok);
+            st = run_swapped(h, Xm, T, s, &n, n_tok);
         else
-            st = run_grouped(h, X, T, s, &n);
+            st = run_grouped(h, Xm, T, s, &n);
     }
     if (st == MOE_OK) {
         moe::CombineArgs ca{h->yslot, h->has_shared ? h->ys : nullptr, h->shared_split_now ? h->ys2 : nullptr,
                             h->topk_w, h->slot_of,
-                            T, h->k, h->H, Y, h->x_f32 ? 1 : 0, trace_slot(h, n)};
+                            T, h->k, h->H, Y, h->x_f32 ? 1 : 0, trace_slot(h, n),
+                            h->norm, h->eps, h->w.post_norm_w, X};
         st = launched(h, moe::launch_combine(ca, s), "combine", &n, s);
     }
     if (prefetch) {  // the caller's stream ends ordered after the side stream
@@ -721,9 +771,13 @@ moe_status moe_create(const moe_config *config, const moe_weights *weights, moe_
     moe_status st = validate_config(config, &S);
     if (st != MOE_OK) return st;
     const moe_weights &w = *weights;
-    if (!w.router_w || !w.gate || !w.up || !w.down)
+    const bool dense = config->num_experts == 0;
+    if (!dense && (!w.router_w || !w.gate || !w.up || !w.down))
         return fail(MOE_ERR_INVALID_ARG, "router_w, gate, up and down are required");
-    const void *ptrs[] = {w.router_w, w.expert_bias, w.gate, w.up, w.down, w.sh_gate, w.sh_up, w.sh_down};
+    if (config->mlp_norm != MOE_NORM_NONE && (!w.pre_norm_w || !w.post_norm_w))
+        return fail(MOE_ERR_INVALID_ARG, "mlp_norm needs pre_norm_w and post_norm_w");
+    const void *ptrs[] = {w.router_w, w.expert_bias, w.gate, w.up, w.down, w.sh_gate, w.sh_up, w.sh_down,
+                          w.pre_norm_w, w.post_norm_w};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "weight pointer %p is not 16-byte aligned", p);
     const bool has_shared = S > 0;
@@ -741,6 +795,9 @@ moe_status moe_create(const moe_config *config, const moe_weights *weights, moe_
     h->S = S;
     h->has_shared = has_shared;
     h->x_f32 = config->act_dtype == MOE_DTYPE_F32;
+    h->dense = dense;
+    h->norm = config->mlp_norm;
+    h->eps = config->rms_norm_eps;
     if (config->shared_packed) {
         const size_t slice = (size_t)h->E * h->I * h->H;
         h->sh_gate = static_cast<const bf16 *>(w.gate) + slice;
@@ -768,15 +825,17 @@ moe_status moe_create(const moe_config *config, const moe_weights *weights, moe_
     carve(h, h->ws);
     e = cudaMemset(h->err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(h->wr_flags, 0, sizeof(int));
-    if (e == cudaSuccess) e = moe::launch_split_router(w.router_w, h->E, h->H, h->wr_parts, h->wr_flags, 0);
     int flags = 0;
-    if (e == cudaSuccess) e = cudaMemcpy(&flags, h->wr_flags, sizeof(int), cudaMemcpyDeviceToHost);
+    if (!dense) {
+        if (e == cudaSuccess) e = moe::launch_split_router(w.router_w, h->E, h->H, h->wr_parts, h->wr_flags, 0);
+        if (e == cudaSuccess) e = cudaMemcpy(&flags, h->wr_flags, sizeof(int), cudaMemcpyDeviceToHost);
+    }
     if (e != cudaSuccess) {
         cudaFree(h->ws);
         delete h;
         return cuda_fail(e, "router weight split");
     }
-    h->rplan = moe::plan_router_tc(h->E, (flags & 2) ? 3 : (flags & 1) ? 2 : 1);
+    if (!dense) h->rplan = moe::plan_router_tc(h->E, (flags & 2) ? 3 : (flags & 1) ? 2 : 1);
     if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) {
@@ -802,8 +861,16 @@ moe_status moe_route(moe_handle *h, const void *X, int T, int32_t *topk_idx, flo
     if (T == 0) return MOE_OK;
     if (!X || !topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "X, topk_idx and topk_w are required");
     if (!aligned16(X)) return fail(MOE_ERR_INVALID_ARG, "X is not 16-byte aligned");
+    if (h->dense) return fail(MOE_ERR_UNSUPPORTED, "a dense layer (num_experts 0) has no router");
+    int n = 0;
+    if (h->norm) {  // the router sees pre_mlp_norm(X)
+        moe::NormArgs na{X, h->x_f32 ? 1 : 0, T, h->H, h->w.pre_norm_w, h->norm, h->eps, h->x_norm, nullptr};
+        moe_status st = launched(h, moe::launch_rmsnorm(na, reinterpret_cast<cudaStream_t>(stream)), "pre_norm", &n,
+                                 reinterpret_cast<cudaStream_t>(stream));
+        if (st != MOE_OK) return st;
+        X = h->x_norm;
+    }
     if (!h->x_f32) {
-        int n = 0;
         moe_status st =
             run_router_tc(h, X, T, topk_idx, topk_w, nullptr, reinterpret_cast<cudaStream_t>(stream), &n);
         h->last_launches = n;
@@ -826,8 +893,9 @@ moe_status moe_route(moe_handle *h, const void *X, int T, int32_t *topk_idx, flo
     ra.blk_hist = nullptr;
     ra.x_bf16 = nullptr;
     ra.tokens_per_block = moe::router_tokens_per_block(T, h->num_sms);
-    moe_status st = check_launch(moe::launch_router(ra, reinterpret_cast<cudaStream_t>(stream)), "router launch");
-    if (st == MOE_OK) h->last_launches = 1;
+    moe_status st = launched(h, moe::launch_router(ra, reinterpret_cast<cudaStream_t>(stream)), "router", &n,
+                             reinterpret_cast<cudaStream_t>(stream));
+    h->last_launches = n;
     return st;
 }
 
@@ -1007,8 +1075,11 @@ moe_status moe_inspect(const moe_handle *h, int buffer, void *dst, size_t bytes,
     case MOE_BUF_HIDDEN: src = h->hbuf; cap = MT * k * h->I * 2; break;
     case MOE_BUF_GEMM_STATS: src = h->gemm_stats; cap = moe::kGemmStats * 8; break;
     case MOE_BUF_ROUTER_STATS: src = h->router_stats; cap = moe::kRouterStats * 8; break;
+    case MOE_BUF_NORMED_X: src = h->x_norm; cap = MT * h->H * (h->x_f32 ? 4 : 2); break;
+    case MOE_BUF_SHARED_HIDDEN: src = h->hs; cap = MT * h->S * 2; break;
     default: return fail(MOE_ERR_INVALID_ARG, "unknown buffer %d", buffer);
     }
+    if (src == nullptr) return fail(MOE_ERR_UNSUPPORTED, "buffer %d does not exist in this layer", buffer);
     if (bytes > cap) return fail(MOE_ERR_INVALID_ARG, "%zu bytes requested, buffer holds %zu", bytes, cap);
     cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice,
                                     reinterpret_cast<cudaStream_t>(stream));

@@ -376,10 +376,58 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
 // ---------------------------------------------------------------- combine
 
 constexpr int kCombineThreads = 128;
+constexpr int kCombineMaxChunks = 8;  // H <= 8 * 128 * 8 = 8192
 
+// Sum of the token's slot outputs (weights w) plus the shared outputs, in fp32,
+// in a fixed order (slots 0..k-1, then the shared expert's parts) for the 8
+// columns at c.
+__device__ __forceinline__ void combine_columns(const CombineArgs &a, int t, int c, const int *s_slot,
+                                                const float *s_w, float (&acc)[8]) {
+    const int H = a.H;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+    for (int j = 0; j < a.k; ++j) {
+        const int slot = s_slot[j];
+        if (slot < 0) continue;
+        const float w = s_w[j];
+        const uint4 r = __ldg(reinterpret_cast<const uint4 *>(a.yslot + (size_t)slot * H + c));
+        acc[0] = fmaf(w, bf16_lo(r.x), acc[0]); acc[1] = fmaf(w, bf16_hi(r.x), acc[1]);
+        acc[2] = fmaf(w, bf16_lo(r.y), acc[2]); acc[3] = fmaf(w, bf16_hi(r.y), acc[3]);
+        acc[4] = fmaf(w, bf16_lo(r.z), acc[4]); acc[5] = fmaf(w, bf16_hi(r.z), acc[5]);
+        acc[6] = fmaf(w, bf16_lo(r.w), acc[6]); acc[7] = fmaf(w, bf16_hi(r.w), acc[7]);
+    }
+    const __nv_bfloat16 *sh[2] = {a.ys, a.ys2};
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {  // the shared expert (and its second K half)
+        if (sh[p] == nullptr) continue;
+        const uint4 r = __ldg(reinterpret_cast<const uint4 *>(sh[p] + (size_t)t * H + c));
+        acc[0] += bf16_lo(r.x); acc[1] += bf16_hi(r.x); acc[2] += bf16_lo(r.y);
+        acc[3] += bf16_hi(r.y); acc[4] += bf16_lo(r.z); acc[5] += bf16_hi(r.z);
+        acc[6] += bf16_lo(r.w); acc[7] += bf16_hi(r.w);
+    }
+}
+
+__device__ __forceinline__ void store8(void *Y, int y_f32, size_t off, const float (&v)[8]) {
+    if (y_f32) {
+        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(Y) + off);
+        dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+        dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+        uint4 o;
+        o.x = pack_bf16x2(v[0], v[1]); o.y = pack_bf16x2(v[2], v[3]);
+        o.z = pack_bf16x2(v[4], v[5]); o.w = pack_bf16x2(v[6], v[7]);
+        *reinterpret_cast<uint4 *>(static_cast<bf16 *>(Y) + off) = o;
+    }
+}
+
+// One CTA per token.  NORM: the token's whole output row stays in registers
+// (8 columns per thread per chunk), its sum of squares is reduced over the CTA
+// (lanes, then warps, in a fixed order), and out = residual + y * g * inv.
+template <bool NORM>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
     __shared__ int s_slot[16];
     __shared__ float s_w[16];
+    __shared__ float s_red[kCombineThreads / 32];
     const int t = blockIdx.x, k = a.k, H = a.H;
     trace_mark(a.trace, 0);
     // The token's slots and weights come from the router and the dispatch, which
@@ -393,41 +441,83 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineA
     trace_mark(a.trace, 1);
     pdl_trigger();
     __syncthreads();
-    for (int c = threadIdx.x * 8; c < H; c += kCombineThreads * 8) {
-        float acc[8];
+    if (!NORM) {
+        for (int c = threadIdx.x * 8; c < H; c += kCombineThreads * 8) {
+            float acc[8];
+            combine_columns(a, t, c, s_slot, s_w, acc);
+            store8(a.Y, a.y_f32, (size_t)t * H + c, acc);
+        }
+    } else {
+        float acc[kCombineMaxChunks][8];
+        float ss = 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const int slot = s_slot[j];
-            if (slot < 0) continue;
-            const float w = s_w[j];
-            const uint4 r = __ldg(reinterpret_cast<const uint4 *>(a.yslot + (size_t)slot * H + c));
-            acc[0] = fmaf(w, bf16_lo(r.x), acc[0]); acc[1] = fmaf(w, bf16_hi(r.x), acc[1]);
-            acc[2] = fmaf(w, bf16_lo(r.y), acc[2]); acc[3] = fmaf(w, bf16_hi(r.y), acc[3]);
-            acc[4] = fmaf(w, bf16_lo(r.z), acc[4]); acc[5] = fmaf(w, bf16_hi(r.z), acc[5]);
-            acc[6] = fmaf(w, bf16_lo(r.w), acc[6]); acc[7] = fmaf(w, bf16_hi(r.w), acc[7]);
+        for (int ci = 0; ci < kCombineMaxChunks; ++ci) {
+            const int c = (threadIdx.x + ci * kCombineThreads) * 8;
+            if (c < H) {
+                combine_columns(a, t, c, s_slot, s_w, acc[ci]);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) ss = fmaf(acc[ci][q], acc[ci][q], ss);
+            }
         }
-        if (a.ys != nullptr) {
-            const uint4 r = __ldg(reinterpret_cast<const uint4 *>(a.ys + (size_t)t * H + c));
-            acc[0] += bf16_lo(r.x); acc[1] += bf16_hi(r.x); acc[2] += bf16_lo(r.y);
-            acc[3] += bf16_hi(r.y); acc[4] += bf16_lo(r.z); acc[5] += bf16_hi(r.z);
-            acc[6] += bf16_lo(r.w); acc[7] += bf16_hi(r.w);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
+        __syncthreads();
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCombineThreads / 32; ++w) tot += s_red[w];
+        const float inv = 1.0f / sqrtf(tot / (float)H + a.eps);
+#pragma unroll
+        for (int ci = 0; ci < kCombineMaxChunks; ++ci) {
+            const int c = (threadIdx.x + ci * kCombineThreads) * 8;
+            if (c < H) {
+                float x[8], o[8];
+                load8_as_f32(a.residual, a.y_f32, (size_t)t * H + c, x);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float g = a.norm == 2 ? 1.0f + __ldg(a.post_w + c + q) : __ldg(a.post_w + c + q);
+                    o[q] = x[q] + acc[ci][q] * inv * g;
+                }
+                store8(a.Y, a.y_f32, (size_t)t * H + c, o);
+            }
         }
-        if (a.ys2 != nullptr) {  // the shared expert's second K half
-            const uint4 r = __ldg(reinterpret_cast<const uint4 *>(a.ys2 + (size_t)t * H + c));
-            acc[0] += bf16_lo(r.x); acc[1] += bf16_hi(r.x); acc[2] += bf16_lo(r.y);
-            acc[3] += bf16_hi(r.y); acc[4] += bf16_lo(r.z); acc[5] += bf16_hi(r.z);
-            acc[6] += bf16_lo(r.w); acc[7] += bf16_hi(r.w);
+    }
+    __syncthreads();
+    trace_exit(a.trace);
+}
+
+// ------------------------------------------------------------- pre-MLP norm
+
+constexpr int kNormThreads = 256;  // 8 warps, one row each
+
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a) {
+    const int lane = threadIdx.x & 31, t = blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5);
+    trace_mark(a.trace, 0);
+    pdl_wait();
+    trace_mark(a.trace, 1);
+    pdl_trigger();
+    if (t < a.T) {
+        const int H = a.H;
+        const size_t row = (size_t)t * H;
+        float ss = 0.f;
+        for (int c = lane * 8; c < H; c += 256) {
+            float v[8];
+            load8_as_f32(a.X, a.x_f32, row + c, v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
         }
-        if (a.y_f32) {
-            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.Y) + (size_t)t * H + c);
-            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        } else {
-            uint4 o;
-            o.x = pack_bf16x2(acc[0], acc[1]); o.y = pack_bf16x2(acc[2], acc[3]);
-            o.z = pack_bf16x2(acc[4], acc[5]); o.w = pack_bf16x2(acc[6], acc[7]);
-            *reinterpret_cast<uint4 *>(static_cast<bf16 *>(a.Y) + (size_t)t * H + c) = o;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float inv = 1.0f / sqrtf(ss / (float)H + a.eps);
+        for (int c = lane * 8; c < H; c += 256) {
+            float v[8];
+            load8_as_f32(a.X, a.x_f32, row + c, v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float g = a.norm == 2 ? 1.0f + __ldg(a.w + c + q) : __ldg(a.w + c + q);
+                v[q] = v[q] * inv * g;
+            }
+            store8(a.out, a.x_f32, row + c, v);
         }
     }
     __syncthreads();
@@ -476,8 +566,23 @@ cudaError_t launch_scatter(const ScatterArgs &a, cudaStream_t s) {
 
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
     static std::once_flag once;
-    std::call_once(once, [] { max_smem_carveout(combine_kernel); });
-    return launch_pdl(combine_kernel, dim3(a.T), dim3(kCombineThreads), 0, s, a);
+    std::call_once(once, [] {
+        max_smem_carveout(combine_kernel<false>);
+        max_smem_carveout(combine_kernel<true>);
+    });
+    if (a.norm != 0) {
+        if (a.H > kCombineMaxChunks * kCombineThreads * 8 || a.residual == nullptr || a.post_w == nullptr)
+            return cudaErrorInvalidValue;
+        return launch_pdl(combine_kernel<true>, dim3(a.T), dim3(kCombineThreads), 0, s, a);
+    }
+    return launch_pdl(combine_kernel<false>, dim3(a.T), dim3(kCombineThreads), 0, s, a);
+}
+
+cudaError_t launch_rmsnorm(const NormArgs &a, cudaStream_t s) {
+    static std::once_flag once;
+    std::call_once(once, [] { max_smem_carveout(rmsnorm_kernel); });
+    const int rows = kNormThreads / 32;
+    return launch_pdl(rmsnorm_kernel, dim3((a.T + rows - 1) / rows), dim3(kNormThreads), 0, s, a);
 }
 
 }  // namespace moe

@@ -73,10 +73,20 @@ typedef enum { MOE_ACT_SILU = 0, MOE_ACT_SWIGLU_OAI = 1 } moe_act;
  * expert bias are always fp32. */
 typedef enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 } moe_dtype;
 
+/* Norms around the MLP (y = x / sqrt(mean(x^2) + eps) * g over the H values of a row). */
+typedef enum {
+    MOE_NORM_NONE = 0,  /* no norms: out = mlp(X) */
+    MOE_NORM_RMS = 1,   /* g = weight */
+    MOE_NORM_GEMMA = 2  /* g = 1 + weight */
+} moe_norm;
+
 typedef struct {
     int hidden_size;              /* H; multiple of 64 */
-    int num_experts;              /* E routed experts; 1..256 */
-    int num_experts_per_tok;      /* k; 1..min(E, 16) */
+    int num_experts;              /* E routed experts; 1..256.  0: a dense MLP layer (the dense
+                                     prefix layers: no router, the "shared" tensors are the
+                                     layer's gate/up/down of width shared_intermediate_size, a
+                                     multiple of 64 up to 16384; bf16 activations only) */
+    int num_experts_per_tok;      /* k; 1..min(E, 16) (0 when E == 0) */
     int num_shared_experts;       /* 0, or the count of always-on shared experts */
     int moe_intermediate_size;    /* I, width of one routed expert; multiple of 64 */
     int shared_intermediate_size; /* S, total shared width; 0 => num_shared_experts * I */
@@ -89,6 +99,10 @@ typedef struct {
     float act_alpha, act_limit, act_beta; /* swigluoai constants (1.702, 7.0, 1.0) */
     int act_dtype;                /* moe_dtype of X and Y */
     int max_tokens;               /* largest T any later call may pass; sizes the workspace */
+    int mlp_norm;                 /* moe_norm: the layer's sandwich norms, out = X +
+                                     post_norm(mlp(pre_norm(X))) (Arcee AFMoE issue: four norms per
+                                     layer; MiniMax-M3 issue: Gemma-style RMSNorm, weight + 1) */
+    float rms_norm_eps;           /* eps of both norms (AfmoeConfig rms_norm_eps 1e-5) */
 } moe_config;
 
 /* Device pointers to the block's weights.  BORROWED: they must stay valid and
@@ -102,6 +116,8 @@ typedef struct {
     const void *sh_gate;      /* [S, H] bf16 (shared_experts.gate_proj); NULL when packed or S == 0 */
     const void *sh_up;        /* [S, H] bf16 */
     const void *sh_down;      /* [H, S] bf16 */
+    const float *pre_norm_w;  /* [H] fp32 (pre_mlp_layernorm.weight); required when mlp_norm != 0 */
+    const float *post_norm_w; /* [H] fp32 (post_mlp_layernorm.weight); required when mlp_norm != 0 */
 } moe_weights;
 
 typedef struct moe_handle moe_handle;
@@ -230,11 +246,15 @@ typedef enum {
                                  waiting for an accumulator, epilogue waiting for an accumulator,
                                  epilogue working, CTA time past the dependency wait; then the
                                  number of tiles */
-    MOE_BUF_ROUTER_STATS = 7  /* [8] uint64, with MOE_OPT_TRACE on and the tensor-core router: ns
+    MOE_BUF_ROUTER_STATS = 7, /* [8] uint64, with MOE_OPT_TRACE on and the tensor-core router: ns
                                  summed over its CTAs of: main loop, first cluster barrier,
                                  pushing the partial logits to the routing CTAs with the second
                                  barrier, adding them and routing, histogram; then the number of
                                  CTAs */
+    MOE_BUF_NORMED_X = 8,     /* [T, H] in the activation dtype: pre_norm(X), the MLP's input
+                                 (mlp_norm != 0 only) */
+    MOE_BUF_SHARED_HIDDEN = 9 /* [T, S] bf16: act(gate, up) of the shared experts (of the dense
+                                 MLP when num_experts == 0) */
 } moe_buffer;
 
 /* Copy `bytes` of an internal buffer, as the last forward left it, to the

@@ -40,7 +40,8 @@ def _weights():
 @pytest.mark.parametrize("field,value,status", [
     ("hidden_size", 100, capi.MOE_ERR_UNSUPPORTED),
     ("hidden_size", 0, capi.MOE_ERR_UNSUPPORTED),
-    ("num_experts", 0, capi.MOE_ERR_UNSUPPORTED),
+    ("num_experts", 0, capi.MOE_ERR_INVALID_ARG),  # a dense layer needs num_experts_per_tok 0
+    ("num_experts", -1, capi.MOE_ERR_UNSUPPORTED),
     ("num_experts", 300, capi.MOE_ERR_UNSUPPORTED),
     ("num_experts_per_tok", 0, capi.MOE_ERR_INVALID_ARG),
     ("num_experts_per_tok", 129, capi.MOE_ERR_INVALID_ARG),
@@ -50,6 +51,7 @@ def _weights():
     ("act_dtype", 3, capi.MOE_ERR_INVALID_ARG),
     ("max_tokens", 0, capi.MOE_ERR_INVALID_ARG),
     ("shared_intermediate_size", 100, capi.MOE_ERR_UNSUPPORTED),
+    ("mlp_norm", 3, capi.MOE_ERR_INVALID_ARG),
 ])
 def test_create_rejects_bad_config(lib, field, value, status):
     cfg = capi.config_from_shape(wl.NANO_DECODE)
@@ -78,6 +80,29 @@ def test_create_rejects_bad_weights(lib):
     assert lib.moe_create(ctypes.byref(packed), ctypes.byref(_weights()), ctypes.byref(h)) == capi.MOE_ERR_INVALID_ARG
     assert lib.moe_create(None, ctypes.byref(_weights()), ctypes.byref(h)) == capi.MOE_ERR_INVALID_ARG
     assert lib.moe_create(ctypes.byref(cfg), ctypes.byref(_weights()), None) == capi.MOE_ERR_INVALID_ARG
+
+
+def test_create_rejects_bad_dense_and_norm_configs(lib):
+    h = ctypes.c_void_p()
+    dense = capi.config_from_shape(wl.WORKLOADS["dense_afmoe_decode"])
+    w = _weights()
+    w.pre_norm_w = w.post_norm_w = ctypes.c_void_p(1 << 20)
+    bad = capi.config_from_shape(wl.WORKLOADS["dense_afmoe_decode"])
+    bad.shared_intermediate_size = 6100  # not a multiple of 64
+    assert lib.moe_create(ctypes.byref(bad), ctypes.byref(w), ctypes.byref(h)) == capi.MOE_ERR_UNSUPPORTED
+    bad = capi.config_from_shape(wl.WORKLOADS["dense_afmoe_decode"])
+    bad.shared_packed = 1  # nothing to pack into
+    assert lib.moe_create(ctypes.byref(bad), ctypes.byref(w), ctypes.byref(h)) == capi.MOE_ERR_INVALID_ARG
+    bad = capi.config_from_shape(wl.WORKLOADS["dense_afmoe_decode"])
+    bad.act_dtype = capi.MOE_DTYPE_F32  # the dense layers run bf16 activations
+    assert lib.moe_create(ctypes.byref(bad), ctypes.byref(w), ctypes.byref(h)) == capi.MOE_ERR_UNSUPPORTED
+    bad = capi.config_from_shape(wl.WORKLOADS["dense_afmoe_decode"])
+    bad.rms_norm_eps = -1.0
+    assert lib.moe_create(ctypes.byref(bad), ctypes.byref(w), ctypes.byref(h)) == capi.MOE_ERR_INVALID_ARG
+    w.post_norm_w = None  # the sandwich needs both norm weights
+    assert lib.moe_create(ctypes.byref(dense), ctypes.byref(w), ctypes.byref(h)) == capi.MOE_ERR_INVALID_ARG
+    assert "norm" in lib.moe_last_error().decode()
+    assert h.value is None
 
 
 def test_null_handle_calls_fail_cleanly(lib):
