@@ -140,6 +140,8 @@ def run_ours(args, shape):
     if args.path:
         blk.set_option(capi.MOE_OPT_PATH, {"decode": capi.PATH_DECODE, "grouped": capi.PATH_GROUPED,
                                            "swapped": capi.PATH_SWAPPED}[args.path])
+    if args.gemm_pair is not None:
+        blk.set_option(capi.MOE_OPT_GEMM_PAIR, args.gemm_pair)
     if args.two_launch:
         blk.set_option(capi.MOE_OPT_FUSE_EXPERTS, 0)
     if args.no_prefetch:
@@ -431,6 +433,8 @@ def main():
     ap.add_argument("--workload", default="nano_decode")
     ap.add_argument("--path", choices=["decode", "grouped", "swapped"], default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gemm-pair", type=int, choices=[0, 1, 2], default=None,
+                    help="CTA-pair expert GEMM: 0 never, 1 always, 2 by size (the default)")
     ap.add_argument("--two-launch", action="store_true", help="gate/up and down GEMMs as two launches")
     ap.add_argument("--no-prefetch", action="store_true", help="no L2 prefetch of expert weights while routing")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

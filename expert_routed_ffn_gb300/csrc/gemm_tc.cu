@@ -72,14 +72,15 @@ struct GemmCfg {
 };
 
 struct Tile {
-    int seg, group, mt, nt, row0, m_valid, ready;  // row0, m_valid: this CTA's rows; ready: its m-tile's counter
+    int seg, group, mt, nt, ks, row0, m_valid, ready;  // ks: K range; row0, m_valid: this CTA's rows;
+                                                       // ready: its m-tile's counter
 };
 
 // offs / toffs: shared-memory copies of the grouped segments' dispatch offsets
 // (toffs counts tiles of BM rows)
 template <int BM>
 __device__ __forceinline__ int seg_tiles(const GemmSegment &s, const int *toffs) {
-    if (s.dense) return ((s.m_dense + BM - 1) / BM) * s.n_tiles;
+    if (s.dense) return ((s.m_dense + BM - 1) / BM) * s.n_tiles * max(s.k_splits, 1);
     return toffs[s.num_groups] * s.n_tiles;
 }
 
@@ -98,6 +99,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, const i
     if (s.dense) {
         const int mtiles = (s.m_dense + BM - 1) / BM;
         t.group = 0;
+        t.ks = tile / (mtiles * s.n_tiles);
+        tile -= t.ks * mtiles * s.n_tiles;
         t.nt = tile / mtiles;
         t.mt = tile % mtiles;
         t.row0 = t.mt * BM + half * kGemmBM;
@@ -116,6 +119,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, const i
         const int mt_g = toffs[lo + 1] - toffs[lo];
         const int local = tile - toffs[lo] * s.n_tiles;
         t.group = lo;
+        t.ks = 0;
         t.nt = local / mt_g;
         t.mt = local % mt_g;
         const int start = offs[lo];
@@ -326,14 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         // (past the last k-block: zero fill, no MMA)
                         const uint32_t fb = mapa_shared(full_bar(s), 0);
                         if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * kStageBytes);
-                        const int kc = sg.k_base + kb;
+                        const int kc = sg.k_base + t.ks * sg.k_blocks + kb;
                         tma_load_3d_pair(sA + s * kAStage, mA, fb, 0, t.row0, kc);
                         if (sg.glu)  // gate rows in rank 0, up rows in rank 1: accumulator columns 0-127 / 128-255
                             tma_load_4d_pair(sB + s * kBBytes, leader ? mB : mB2, fb, 0, t.nt * 128, kc, g);
                         else
                             tma_load_4d_pair(sB + s * kBBytes, mB, fb, 0, t.nt * kGemmBN + half * 128, kc, g);
                     } else {
-                        const int kx = (sg.k_base + kb) * kGemmBK;
+                        const int kx = (sg.k_base + t.ks * sg.k_blocks + kb) * kGemmBK;
                         mbar_arrive_expect_tx(full_bar(s), kStageBytes);
                         tma_load_2d(sA + s * kAStage, mA, full_bar(s), kx, t.row0);
                         if (sg.glu) {
@@ -493,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             tc_fence_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + a * kGemmBN;
             const bool row_ok = r < t.m_valid;
-            bf16 *orow = sg.out + (size_t)(t.row0 + (row_ok ? r : 0)) * sg.ldo;
+            bf16 *orow = sg.out + t.ks * sg.split_stride + (size_t)(t.row0 + (row_ok ? r : 0)) * sg.ldo;
             if (sg.glu) {
                 constexpr int kSpan = 128 / kEpiParts;  // output columns per slice
 #pragma unroll 1

@@ -170,8 +170,9 @@ cudaError_t launch_scatter(const ScatterArgs &a, cudaStream_t s);
 // Y[t] = sum_j w[t,j] * Yslot[slot_of[t,j]] + Ys[t]  (fp32 sum, fixed order).
 struct CombineArgs {
     const __nv_bfloat16 *yslot;  // [T*k, H]
-    const __nv_bfloat16 *ys;     // [T, H] or nullptr
-    const __nv_bfloat16 *ys2;    // [T, H] second half of a K-split shared down projection, or nullptr
+    const __nv_bfloat16 *ys;     // shared output part 0 [T, H], or nullptr
+    int ys_parts;                // parts of a K-split shared down projection (>= 1), summed in order
+    size_t ys_part_stride;       // elements from one part to the next
     const float *topk_w;         // [T, k]
     const int32_t *slot_of;      // [T, k]
     int T, k, H;
@@ -188,7 +189,9 @@ struct CombineArgs {
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 
 // pre_mlp norm of each token row: out = x * g / sqrt(mean(x^2) + eps), g = w (norm 1)
-// or 1 + w (norm 2), in the dtype of X (x_f32), one warp per row
+// or 1 + w (norm 2), in the dtype of X (x_f32), one CTA per row.  After its
+// dependency wait the first CTA also zeroes zero_a[0, zero_a_n) and
+// zero_b[0, zero_b_n) (counters of the kernels that follow), or nothing.
 struct NormArgs {
     const void *X;
     int x_f32;
@@ -198,6 +201,10 @@ struct NormArgs {
     float eps;
     void *out;
     unsigned long long *trace;
+    int *zero_a;
+    int zero_a_n;
+    int *zero_b;
+    int zero_b_n;
 };
 cudaError_t launch_rmsnorm(const NormArgs &a, cudaStream_t s);
 
@@ -230,6 +237,11 @@ struct GemmSegment {
     const int *wait;
     int wait_count;
     int ready_base;
+    // dense segments: K split into k_splits consecutive ranges of k_blocks each (0 or 1:
+    // no split); range j starts at k-block k_base + j * k_blocks and stores its partial
+    // product at out + j * split_stride
+    int k_splits;
+    size_t split_stride;
 };
 
 struct GemmArgs {

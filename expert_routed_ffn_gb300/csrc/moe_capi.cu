@@ -81,7 +81,7 @@ struct moe_handle {
             *active = nullptr, *sorted_tok = nullptr, *slot_of = nullptr;
     float *topk_w = nullptr;
     bf16 *x_sorted = nullptr, *x_bf16 = nullptr, *hbuf = nullptr, *hs = nullptr, *yslot = nullptr,
-         *ys = nullptr, *ys2 = nullptr;
+         *ys = nullptr, *ys_split = nullptr;
     void *x_stage = nullptr, *y_stage = nullptr;
     int *err = nullptr;
     bf16 *wr_parts = nullptr;  // router weights as exact bf16 splits [3, E, H]
@@ -91,7 +91,7 @@ struct moe_handle {
     bool fuse_experts = true;  // gate/up and down in one persistent launch
     int pair_opt = 2;          // CTA-pair expert GEMM: 0 never, 1 always, 2 when T*k >= 256*E
     bool pair_now = false;     // the current forward's choice
-    bool shared_split_now = false;  // shared down projection in two K halves (small T)
+    int shared_parts = 1;      // K ranges of the shared (dense) down projection this forward
     bool prefetch_opt = true;  // L2 prefetch of expert weights during routing
     cudaStream_t side = nullptr;               // the prefetch runs here, beside the routing kernels
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
@@ -198,6 +198,38 @@ moe_status validate_config(const moe_config *c, int *S_eff) {
     return MOE_OK;
 }
 
+// elements of the K-split partial-output buffer: parts * T * H <= SMs * 128 * 256
+// whenever a split is taken (parts * output tiles <= CTAs or CTA pairs)
+size_t split_elems(const moe_handle *h) { return (size_t)h->num_sms * moe::kGemmBM * moe::kGemmBN; }
+
+// K ranges of the shared (dense) down projection on the grouped path.  Its tiles
+// are few at small T and each streams a whole K = S of weights: a MoE layer
+// splits K in two when the tiles fill at most a quarter of the SMs (one CTA per
+// tile); a dense layer, whose down projection is the whole second half of its
+// work, takes the largest power of two (<= 16) that keeps parts x tiles within
+// the CTAs (CTA pairs) and at least 4 k-blocks (an even number with CTA pairs)
+// per part.
+int shared_parts(const moe_handle *h, int T) {
+    const int bm = h->pair_now ? 2 * moe::kGemmBM : moe::kGemmBM;
+    const long long tiles = (long long)((T + bm - 1) / bm) * ((h->H + moe::kGemmBN - 1) / moe::kGemmBN);
+    const int kb = h->S / 64;
+    int parts = 1;
+    if (!h->dense) {
+        if (!h->pair_now && kb % 2 == 0 && tiles * 4 <= h->num_sms) parts = 2;
+    } else {
+        const int units = h->pair_now ? h->num_sms / 2 : h->num_sms;
+        for (int p = 16; p >= 2; p >>= 1) {
+            const int per = kb / p;
+            if (kb % p == 0 && per >= 4 && (!h->pair_now || per % 2 == 0) && tiles * p <= units) {
+                parts = p;
+                break;
+            }
+        }
+    }
+    while (parts > 1 && (size_t)parts * T * h->H > split_elems(h)) parts >>= 1;
+    return parts;
+}
+
 struct Carver {
     size_t off = 0;
     template <class T>
@@ -230,7 +262,9 @@ void carve(moe_handle *h, void *base) {
     h->hs = h->has_shared ? c.take<bf16>(base, MT * h->S) : nullptr;
     h->yslot = c.take<bf16>(base, MT * k * H);
     h->ys = h->has_shared ? c.take<bf16>(base, MT * H) : nullptr;
-    h->ys2 = h->has_shared ? c.take<bf16>(base, MT * H) : nullptr;
+    // partial products of a K-split shared down projection: the split is taken only
+    // while parts x output tiles fit the SMs, so parts * T * H <= SMs * 128 * 256
+    h->ys_split = h->has_shared ? c.take<bf16>(base, split_elems(h)) : nullptr;
     h->x_stage = c.take<char>(base, MT * H * elt);
     h->x_norm = h->norm ? c.take<char>(base, MT * H * elt) : nullptr;
     h->y_stage = c.take<char>(base, MT * H * elt);
@@ -541,24 +575,20 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
                                1, kX, kSG, kSU, sig, nullptr, 0, h->ready_shared_base};
     const moe::GemmSegment dn{0, E, 0, 0, h->offs, h->tile_offs, nt_d, I / 64, 0, H, h->yslot, H,
                               0, kHb, kD, kD, nullptr, fused ? h->ready : nullptr, nt_gu, 0};
-    // At small T the shared down projection (K = S) is the longest tile chain: its
-    // two K halves run as two segments into two partial outputs, which the
-    // combine adds in fixed order (for two concatenated shared experts of width I
-    // the halves are exactly the two experts).
-    const bool split = h->shared_split_now;
-    const int sk = split ? S / 128 : S / 64;
-    moe::GemmSegment sdn{1, 1, sh_base, T, nullptr, nullptr, nt_d, sk, 0, H, h->ys, H,
-                         0, kHs, kSD, kSD, nullptr, fused ? h->ready : nullptr, nt_sgu, h->ready_shared_base};
-    moe::GemmSegment sdn2 = sdn;
-    sdn2.k_base = sk;
-    sdn2.out = h->ys2;
+    // At small T the shared down projection (K = S) is the longest tile chain: its K
+    // runs as `parts` ranges into as many partial outputs, which the combine adds in
+    // fixed order (for two concatenated shared experts of width I and two parts,
+    // the parts are exactly the two experts).
+    const int parts = h->shared_parts;
+    moe::GemmSegment sdn{1, 1, sh_base, T, nullptr, nullptr, nt_d, S / 64 / parts, 0, H,
+                         parts > 1 ? h->ys_split : h->ys, H, 0, kHs, kSD, kSD, nullptr,
+                         fused ? h->ready : nullptr, nt_sgu, h->ready_shared_base, parts, (size_t)T * H};
     if (fused) {
         int ns = 0;
         if (!h->dense) g.seg[ns++] = gu;
         if (h->has_shared) g.seg[ns++] = sgu;
         if (!h->dense) g.seg[ns++] = dn;
         if (h->has_shared) g.seg[ns++] = sdn;
-        if (h->has_shared && split) g.seg[ns++] = sdn2;
         g.num_segs = ns;
         g.tile_counter = pair ? nullptr : h->tile_counters;
         g.trace = trace_slot(h, *n);
@@ -574,10 +604,7 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     if (st != MOE_OK) return st;
     g.num_segs = 0;
     if (!h->dense) g.seg[g.num_segs++] = dn;
-    if (h->has_shared) {
-        g.seg[g.num_segs++] = sdn;
-        if (split) g.seg[g.num_segs++] = sdn2;
-    }
+    if (h->has_shared) g.seg[g.num_segs++] = sdn;
     g.tile_counter = pair ? nullptr : h->tile_counters + 1;
     g.trace = trace_slot(h, *n);
     return launched(h, moe::launch_gemm_tc(g, s), "down_gemm", n, s);
@@ -708,32 +735,29 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     // layer: T >= 256)
     h->pair_now = path == kPathGrouped && h->num_sms >= 2 &&
                   (h->pair_opt == 1 || (h->pair_opt == 2 && (h->dense ? T >= 256 : slots >= 256ll * h->E)));
-    {
-        // few shared down tiles (a quarter of the SMs or less) and an even number of
-        // k-blocks: split the shared down projection's K in two
-        const long long sh_tiles = (long long)((T + 127) / 128) * ((h->H + moe::kGemmBN - 1) / moe::kGemmBN);
-        h->shared_split_now = path == kPathGrouped && !h->pair_now && h->has_shared && h->S % 128 == 0 &&
-                              sh_tiles * 4 <= h->num_sms;
-    }
+    h->shared_parts = path == kPathGrouped && h->has_shared ? shared_parts(h, T) : 1;
     mark(h, 0, s);
     moe_status st = MOE_OK;
     const void *Xm = X;  // the MLP's input: X, or pre_mlp_norm(X)
+    // a dense layer has no router and no dispatch: its GEMM's counters (zeroed by
+    // the dispatch in a MoE layer) are zeroed by the pre-norm kernel, or here
+    int *const zero_a = h->dense ? h->ready + h->ready_shared_base : nullptr;
+    const int zero_a_n = h->dense ? 2 * ((T + 255) / 256) + 2 : 0;
+    int *const zero_b = h->dense ? h->tile_counters : nullptr;
+    const int zero_b_n = h->dense ? 2 : 0;
     if (h->norm) {
         moe::NormArgs na{X, h->x_f32 ? 1 : 0, T, h->H, h->w.pre_norm_w, h->norm, h->eps, h->x_norm,
-                         trace_slot(h, n)};
+                         trace_slot(h, n), zero_a, zero_a_n, zero_b, zero_b_n};
         st = launched(h, moe::launch_rmsnorm(na, s), "pre_norm", &n, s);
         Xm = h->x_norm;
-    }
-    if (st == MOE_OK && h->dense) {
-        // no router and no dispatch: zero what the dispatch would have zeroed for the GEMM
-        cudaError_t e = cudaMemsetAsync(h->ready + h->ready_shared_base, 0,
-                                        sizeof(int) * (size_t)(2 * ((T + 255) / 256) + 2), s);
-        if (e == cudaSuccess) e = cudaMemsetAsync(h->tile_counters, 0, 2 * sizeof(int), s);
+    } else if (h->dense) {
+        cudaError_t e = cudaMemsetAsync(zero_a, 0, sizeof(int) * (size_t)zero_a_n, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(zero_b, 0, sizeof(int) * (size_t)zero_b_n, s);
         if (e != cudaSuccess) st = cuda_fail(e, "counter reset");
-    } else if (st == MOE_OK) {
+    }
+    if (st == MOE_OK && !h->dense)
         st = run_front(h, Xm, T, s, &n,
                        path == kPathSwapped ? n_tok : (h->pair_now ? 2 * moe::kGemmBM : moe::kGemmBM));
-    }
     if (st == MOE_OK) {
         if (path == kPathDecode)
             st = run_decode(h, Xm, T, s, &n);
@@ -743,8 +767,9 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
             st = run_grouped(h, Xm, T, s, &n);
     }
     if (st == MOE_OK) {
-        moe::CombineArgs ca{h->yslot, h->has_shared ? h->ys : nullptr, h->shared_split_now ? h->ys2 : nullptr,
-                            h->topk_w, h->slot_of,
+        const bool split = h->shared_parts > 1;
+        moe::CombineArgs ca{h->yslot, h->has_shared ? (split ? h->ys_split : h->ys) : nullptr, h->shared_parts,
+                            (size_t)T * h->H, h->topk_w, h->slot_of,
                             T, h->k, h->H, Y, h->x_f32 ? 1 : 0, trace_slot(h, n),
                             h->norm, h->eps, h->w.post_norm_w, X};
         st = launched(h, moe::launch_combine(ca, s), "combine", &n, s);

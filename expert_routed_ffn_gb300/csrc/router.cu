@@ -375,35 +375,55 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
 
 // ---------------------------------------------------------------- combine
 
-constexpr int kCombineThreads = 128;
-constexpr int kCombineMaxChunks = 8;  // H <= 8 * 128 * 8 = 8192
+// One CTA per token row, one thread per 8 columns: blockDim = 32 * ceil(H / 256)
+// (H <= 8192).  Loads go out in batches of four slot rows per thread.
+constexpr int kRowMaxThreads = 1024;
+constexpr int kSlotBatch = 4;
+
+__device__ __forceinline__ void fma8(float w, const uint4 &r, float (&acc)[8]) {
+    acc[0] = fmaf(w, bf16_lo(r.x), acc[0]); acc[1] = fmaf(w, bf16_hi(r.x), acc[1]);
+    acc[2] = fmaf(w, bf16_lo(r.y), acc[2]); acc[3] = fmaf(w, bf16_hi(r.y), acc[3]);
+    acc[4] = fmaf(w, bf16_lo(r.z), acc[4]); acc[5] = fmaf(w, bf16_hi(r.z), acc[5]);
+    acc[6] = fmaf(w, bf16_lo(r.w), acc[6]); acc[7] = fmaf(w, bf16_hi(r.w), acc[7]);
+}
+
+__device__ __forceinline__ void add8(const uint4 &r, float (&acc)[8]) {
+    acc[0] += bf16_lo(r.x); acc[1] += bf16_hi(r.x); acc[2] += bf16_lo(r.y); acc[3] += bf16_hi(r.y);
+    acc[4] += bf16_lo(r.z); acc[5] += bf16_hi(r.z); acc[6] += bf16_lo(r.w); acc[7] += bf16_hi(r.w);
+}
 
 // Sum of the token's slot outputs (weights w) plus the shared outputs, in fp32,
-// in a fixed order (slots 0..k-1, then the shared expert's parts) for the 8
-// columns at c.
+// in a fixed order (slots 0..k-1, then the shared expert's parts 0..P-1) for the
+// 8 columns at c.
 __device__ __forceinline__ void combine_columns(const CombineArgs &a, int t, int c, const int *s_slot,
                                                 const float *s_w, float (&acc)[8]) {
     const int H = a.H;
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-    for (int j = 0; j < a.k; ++j) {
-        const int slot = s_slot[j];
-        if (slot < 0) continue;
-        const float w = s_w[j];
-        const uint4 r = __ldg(reinterpret_cast<const uint4 *>(a.yslot + (size_t)slot * H + c));
-        acc[0] = fmaf(w, bf16_lo(r.x), acc[0]); acc[1] = fmaf(w, bf16_hi(r.x), acc[1]);
-        acc[2] = fmaf(w, bf16_lo(r.y), acc[2]); acc[3] = fmaf(w, bf16_hi(r.y), acc[3]);
-        acc[4] = fmaf(w, bf16_lo(r.z), acc[4]); acc[5] = fmaf(w, bf16_hi(r.z), acc[5]);
-        acc[6] = fmaf(w, bf16_lo(r.w), acc[6]); acc[7] = fmaf(w, bf16_hi(r.w), acc[7]);
-    }
-    const __nv_bfloat16 *sh[2] = {a.ys, a.ys2};
+    for (int j0 = 0; j0 < a.k; j0 += kSlotBatch) {
+        uint4 r[kSlotBatch];
 #pragma unroll
-    for (int p = 0; p < 2; ++p) {  // the shared expert (and its second K half)
-        if (sh[p] == nullptr) continue;
-        const uint4 r = __ldg(reinterpret_cast<const uint4 *>(sh[p] + (size_t)t * H + c));
-        acc[0] += bf16_lo(r.x); acc[1] += bf16_hi(r.x); acc[2] += bf16_lo(r.y);
-        acc[3] += bf16_hi(r.y); acc[4] += bf16_lo(r.z); acc[5] += bf16_hi(r.z);
-        acc[6] += bf16_lo(r.w); acc[7] += bf16_hi(r.w);
+        for (int u = 0; u < kSlotBatch; ++u) {
+            const int slot = j0 + u < a.k ? s_slot[j0 + u] : -1;
+            r[u] = slot >= 0 ? __ldg(reinterpret_cast<const uint4 *>(a.yslot + (size_t)slot * H + c))
+                             : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kSlotBatch; ++u)
+            if (j0 + u < a.k && s_slot[j0 + u] >= 0) fma8(s_w[j0 + u], r[u], acc);
+    }
+    if (a.ys != nullptr) {
+        for (int p0 = 0; p0 < a.ys_parts; p0 += kSlotBatch) {
+            uint4 r[kSlotBatch];
+#pragma unroll
+            for (int u = 0; u < kSlotBatch; ++u)
+                if (p0 + u < a.ys_parts)
+                    r[u] = __ldg(reinterpret_cast<const uint4 *>(a.ys + (p0 + u) * a.ys_part_stride +
+                                                                 (size_t)t * H + c));
+#pragma unroll
+            for (int u = 0; u < kSlotBatch; ++u)
+                if (p0 + u < a.ys_parts) add8(r[u], acc);
+        }
     }
 }
 
@@ -420,15 +440,38 @@ __device__ __forceinline__ void store8(void *Y, int y_f32, size_t off, const flo
     }
 }
 
-// One CTA per token.  NORM: the token's whole output row stays in registers
-// (8 columns per thread per chunk), its sum of squares is reduced over the CTA
-// (lanes, then warps, in a fixed order), and out = residual + y * g * inv.
+// The 8 gains at column c: g = w (norm 1) or 1 + w (norm 2)
+__device__ __forceinline__ void gain8(const float *w, int norm, int c, float (&g)[8]) {
+    const float4 lo = __ldg(reinterpret_cast<const float4 *>(w + c));
+    const float4 hi = __ldg(reinterpret_cast<const float4 *>(w + c + 4));
+    g[0] = lo.x; g[1] = lo.y; g[2] = lo.z; g[3] = lo.w; g[4] = hi.x; g[5] = hi.y; g[6] = hi.z; g[7] = hi.w;
+    if (norm == 2) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) g[q] += 1.0f;
+    }
+}
+
+// Sum over the CTA in a fixed order (lanes by butterfly, then warps in index
+// order); every thread gets the total.
+__device__ __forceinline__ float row_sum(float v, float *s_red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float tot = 0.f;
+    const int nw = blockDim.x >> 5;
+    for (int w = 0; w < nw; ++w) tot += s_red[w];
+    return tot;
+}
+
+// NORM: out = residual + y * g / sqrt(mean(y^2) + eps) on the fp32 row y.
 template <bool NORM>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
+__global__ void __launch_bounds__(kRowMaxThreads) combine_kernel(const CombineArgs a) {
     __shared__ int s_slot[16];
     __shared__ float s_w[16];
-    __shared__ float s_red[kCombineThreads / 32];
-    const int t = blockIdx.x, k = a.k, H = a.H;
+    __shared__ float s_red[kRowMaxThreads / 32];
+    const int t = blockIdx.x, k = a.k, H = a.H, c = threadIdx.x * 8;
+    const bool on = c < H;
     trace_mark(a.trace, 0);
     // The token's slots and weights come from the router and the dispatch, which
     // completed before the expert GEMM (this grid's predecessor) passed its own
@@ -437,49 +480,28 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineA
         s_slot[threadIdx.x] = __ldcg(a.slot_of + (size_t)t * k + threadIdx.x);
         s_w[threadIdx.x] = __ldcg(a.topk_w + (size_t)t * k + threadIdx.x);
     }
+    float g[8];
+    if (NORM && on) gain8(a.post_w, a.norm, c, g);  // weights: not written by any kernel
     pdl_wait();
     trace_mark(a.trace, 1);
     pdl_trigger();
     __syncthreads();
+    float acc[8];
+    if (on) combine_columns(a, t, c, s_slot, s_w, acc);
     if (!NORM) {
-        for (int c = threadIdx.x * 8; c < H; c += kCombineThreads * 8) {
-            float acc[8];
-            combine_columns(a, t, c, s_slot, s_w, acc);
-            store8(a.Y, a.y_f32, (size_t)t * H + c, acc);
-        }
+        if (on) store8(a.Y, a.y_f32, (size_t)t * H + c, acc);
     } else {
-        float acc[kCombineMaxChunks][8];
-        float ss = 0.f;
+        float x[8], ss = 0.f;
+        if (on) {
+            load8_as_f32(a.residual, a.y_f32, (size_t)t * H + c, x);
 #pragma unroll
-        for (int ci = 0; ci < kCombineMaxChunks; ++ci) {
-            const int c = (threadIdx.x + ci * kCombineThreads) * 8;
-            if (c < H) {
-                combine_columns(a, t, c, s_slot, s_w, acc[ci]);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) ss = fmaf(acc[ci][q], acc[ci][q], ss);
-            }
+            for (int q = 0; q < 8; ++q) ss = fmaf(acc[q], acc[q], ss);
         }
+        const float inv = 1.0f / sqrtf(row_sum(ss, s_red) / (float)H + a.eps);
+        if (on) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
-        __syncthreads();
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < kCombineThreads / 32; ++w) tot += s_red[w];
-        const float inv = 1.0f / sqrtf(tot / (float)H + a.eps);
-#pragma unroll
-        for (int ci = 0; ci < kCombineMaxChunks; ++ci) {
-            const int c = (threadIdx.x + ci * kCombineThreads) * 8;
-            if (c < H) {
-                float x[8], o[8];
-                load8_as_f32(a.residual, a.y_f32, (size_t)t * H + c, x);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float g = a.norm == 2 ? 1.0f + __ldg(a.post_w + c + q) : __ldg(a.post_w + c + q);
-                    o[q] = x[q] + acc[ci][q] * inv * g;
-                }
-                store8(a.Y, a.y_f32, (size_t)t * H + c, o);
-            }
+            for (int q = 0; q < 8; ++q) x[q] += acc[q] * inv * g[q];
+            store8(a.Y, a.y_f32, (size_t)t * H + c, x);
         }
     }
     __syncthreads();
@@ -488,37 +510,32 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineA
 
 // ------------------------------------------------------------- pre-MLP norm
 
-constexpr int kNormThreads = 256;  // 8 warps, one row each
-
-__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a) {
-    const int lane = threadIdx.x & 31, t = blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5);
+__global__ void __launch_bounds__(kRowMaxThreads) rmsnorm_kernel(const NormArgs a) {
+    __shared__ float s_red[kRowMaxThreads / 32];
+    const int t = blockIdx.x, H = a.H, c = threadIdx.x * 8;
+    const bool on = c < H;
     trace_mark(a.trace, 0);
+    float g[8];
+    if (on) gain8(a.w, a.norm, c, g);
     pdl_wait();
     trace_mark(a.trace, 1);
     pdl_trigger();
-    if (t < a.T) {
-        const int H = a.H;
-        const size_t row = (size_t)t * H;
-        float ss = 0.f;
-        for (int c = lane * 8; c < H; c += 256) {
-            float v[8];
-            load8_as_f32(a.X, a.x_f32, row + c, v);
+    if (t == 0) {
+        for (int i = threadIdx.x; i < a.zero_a_n; i += blockDim.x) a.zero_a[i] = 0;
+        for (int i = threadIdx.x; i < a.zero_b_n; i += blockDim.x) a.zero_b[i] = 0;
+    }
+    const size_t off = (size_t)t * H + c;
+    float v[8], ss = 0.f;
+    if (on) {
+        load8_as_f32(a.X, a.x_f32, off, v);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
-        }
+        for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
+    }
+    const float inv = 1.0f / sqrtf(row_sum(ss, s_red) / (float)H + a.eps);
+    if (on) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float inv = 1.0f / sqrtf(ss / (float)H + a.eps);
-        for (int c = lane * 8; c < H; c += 256) {
-            float v[8];
-            load8_as_f32(a.X, a.x_f32, row + c, v);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float g = a.norm == 2 ? 1.0f + __ldg(a.w + c + q) : __ldg(a.w + c + q);
-                v[q] = v[q] * inv * g;
-            }
-            store8(a.out, a.x_f32, row + c, v);
-        }
+        for (int q = 0; q < 8; ++q) v[q] = v[q] * inv * g[q];
+        store8(a.out, a.x_f32, off, v);
     }
     __syncthreads();
     trace_exit(a.trace);
@@ -564,25 +581,29 @@ cudaError_t launch_scatter(const ScatterArgs &a, cudaStream_t s) {
                       0, s, a);
 }
 
+// threads of a row kernel: one per 8 columns, whole warps
+static int row_threads(int H) { return ((H / 8 + 31) / 32) * 32; }
+
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
     static std::once_flag once;
     std::call_once(once, [] {
         max_smem_carveout(combine_kernel<false>);
         max_smem_carveout(combine_kernel<true>);
     });
+    if (a.H % 8 != 0 || row_threads(a.H) > kRowMaxThreads || a.k > 16 || (a.ys != nullptr && a.ys_parts < 1))
+        return cudaErrorInvalidValue;
     if (a.norm != 0) {
-        if (a.H > kCombineMaxChunks * kCombineThreads * 8 || a.residual == nullptr || a.post_w == nullptr)
-            return cudaErrorInvalidValue;
-        return launch_pdl(combine_kernel<true>, dim3(a.T), dim3(kCombineThreads), 0, s, a);
+        if (a.residual == nullptr || a.post_w == nullptr) return cudaErrorInvalidValue;
+        return launch_pdl(combine_kernel<true>, dim3(a.T), dim3(row_threads(a.H)), 0, s, a);
     }
-    return launch_pdl(combine_kernel<false>, dim3(a.T), dim3(kCombineThreads), 0, s, a);
+    return launch_pdl(combine_kernel<false>, dim3(a.T), dim3(row_threads(a.H)), 0, s, a);
 }
 
 cudaError_t launch_rmsnorm(const NormArgs &a, cudaStream_t s) {
     static std::once_flag once;
     std::call_once(once, [] { max_smem_carveout(rmsnorm_kernel); });
-    const int rows = kNormThreads / 32;
-    return launch_pdl(rmsnorm_kernel, dim3((a.T + rows - 1) / rows), dim3(kNormThreads), 0, s, a);
+    if (a.H % 8 != 0 || row_threads(a.H) > kRowMaxThreads) return cudaErrorInvalidValue;
+    return launch_pdl(rmsnorm_kernel, dim3(a.T), dim3(row_threads(a.H)), 0, s, a);
 }
 
 }  // namespace moe

@@ -175,6 +175,10 @@ DENSE = {
                                                        shared_intermediate_size=192, mlp_norm="none"),
     "dense_T1": wl.dense_layer(1, "m3").replace(name="dense_T1", hidden_size=1024,
                                                 shared_intermediate_size=2048),
+    # K of the down projection in 16 ranges (8 with T = 1 above, 2 for dense_m3_small
+    # on one CTA per tile): partial outputs summed by the combine
+    "dense_split16": wl.dense_layer(100, "afmoe").replace(name="dense_split16", hidden_size=512,
+                                                        shared_intermediate_size=4096),
 }
 
 
