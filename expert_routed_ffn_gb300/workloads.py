@@ -82,6 +82,7 @@ class MoeShape:
     act_beta: float = 1.0
     mlp_norm: str = "none"  # "none" | "rms" | "gemma": pre_mlp / post_mlp RMSNorm around the MLP
     rms_norm_eps: float = 1e-5
+    weight_format: str = "bf16"  # "bf16" | "mxfp8" | "mxfp4": storage of the expert weights
 
     @property
     def H(self) -> int:
@@ -180,6 +181,11 @@ WORKLOADS = {
     "dense_afmoe_prefill": dense_layer(4096, "afmoe"),
     "dense_afmoe_decode": dense_layer(256, "afmoe"),
     "dense_m3": dense_layer(2048, "m3"),
+    # block-scaled expert weights (next row): the same draws, stored as MXFP8 / MXFP4
+    "nano_decode_mxfp8": NANO_DECODE.replace(name="nano_decode_mxfp8_T256", weight_format="mxfp8"),
+    "nano_decode_mxfp4": NANO_DECODE.replace(name="nano_decode_mxfp4_T256", weight_format="mxfp4"),
+    "afmoe_prefill_mxfp8": AFMOE_PREFILL.replace(name="afmoe_prefill_mxfp8_T4096", weight_format="mxfp8"),
+    "m3_mxfp8": M3.replace(name="m3_mxfp8_T2048", weight_format="mxfp8"),
 }
 
 
@@ -199,6 +205,44 @@ def _stacked(gen, n, rows, cols, dtype, device) -> torch.Tensor:
     for e in range(n):  # one slice at a time bounds the fp32 temporary
         out[e].copy_(_normal(gen, (rows, cols), WEIGHT_STD, dtype, device))
     return out
+
+
+MX_BLOCK = 32
+# largest exponent of the MX element types (E4M3: 448 = 1.75 * 2^8; E2M1: 6 = 1.5 * 2^2)
+_MX_EMAX = {"mxfp8": 8, "mxfp4": 2}
+_E2M1_MIDPOINTS = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)  # between 0, .5, 1, 1.5, 2, 3, 4, 6
+
+
+def mx_quantize(w: torch.Tensor, fmt: str):
+    """[rows, cols] fp32 -> (element codes, block scales) in the OCP MX layout
+    used by the block: blocks of 32 along cols share the E8M0 exponent
+    floor(log2(max |w|)) - emax(element), elements rounded to nearest and
+    saturated.  Codes: [rows, cols] uint8 (E4M3) or [rows, cols / 2] uint8
+    (E2M1, element 2j in the low nibble); scales [cols / 32, rows] uint8
+    (block-major)."""
+    rows, cols = w.shape
+    b = w.float().reshape(rows, cols // MX_BLOCK, MX_BLOCK)
+    amax = b.abs().amax(-1)
+    _, ex = torch.frexp(amax)  # amax = m * 2^ex, m in [0.5, 1): floor(log2 amax) = ex - 1
+    e = torch.where(amax > 0, ex - 1 - _MX_EMAX[fmt], torch.full_like(ex, -127)).clamp(-127, 127)
+    v = b * torch.exp2(-e.float())[..., None]
+    if fmt == "mxfp8":
+        codes = v.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).reshape(rows, cols)
+    else:
+        mids = torch.tensor(_E2M1_MIDPOINTS, dtype=torch.float32, device=w.device)
+        mag = torch.bucketize(v.abs().clamp(max=6.0), mids).to(torch.uint8)  # code order = value order
+        nib = (mag | ((v < 0).to(torch.uint8) << 3)).reshape(rows, cols)
+        codes = nib[:, 0::2] | (nib[:, 1::2] << 4)
+    return codes.contiguous(), (e + 127).to(torch.uint8).t().contiguous()
+
+
+def _stacked_mx(gen, n, rows, cols, fmt, device):
+    per = cols if fmt == "mxfp8" else cols // 2
+    codes = torch.empty((n, rows, per), dtype=torch.uint8, device=device)
+    scales = torch.empty((n, cols // MX_BLOCK, rows), dtype=torch.uint8, device=device)
+    for e in range(n):  # the same draws as the bf16 tensors, quantized slice by slice
+        codes[e], scales[e] = mx_quantize(_normal(gen, (rows, cols), WEIGHT_STD, torch.float32, device), fmt)
+    return codes, scales
 
 
 def _bias(shape: MoeShape, gen: torch.Generator, device) -> torch.Tensor:
@@ -235,18 +279,31 @@ def make_inputs(shape: MoeShape, device="cpu",
     E, H, I, S = shape.E, shape.H, shape.I, shape.S
     Ep = shape.stacked_experts
 
+    wf = shape.weight_format
+    scales = {}
     router_w = expert_bias = gate = up = down = None
     if E > 0:
         router_w = _normal(g, (E, H), WEIGHT_STD, dt, device).to(torch.float32)
         expert_bias = _bias(shape, g, device)
-        gate = _stacked(g, Ep, I, H, dt, device)
-        up = _stacked(g, Ep, I, H, dt, device)
-        down = _stacked(g, Ep, H, I, dt, device)
+        if wf == "bf16":
+            gate = _stacked(g, Ep, I, H, dt, device)
+            up = _stacked(g, Ep, I, H, dt, device)
+            down = _stacked(g, Ep, H, I, dt, device)
+        else:
+            gate, scales["gate_scale"] = _stacked_mx(g, Ep, I, H, wf, device)
+            up, scales["up_scale"] = _stacked_mx(g, Ep, I, H, wf, device)
+            down, scales["down_scale"] = _stacked_mx(g, Ep, H, I, wf, device)
     sh_gate = sh_up = sh_down = None
     if not shape.shared_packed and S > 0:
-        sh_gate = _normal(g, (S, H), WEIGHT_STD, dt, device)
-        sh_up = _normal(g, (S, H), WEIGHT_STD, dt, device)
-        sh_down = _normal(g, (H, S), WEIGHT_STD, dt, device)
+        if wf == "bf16":
+            sh_gate = _normal(g, (S, H), WEIGHT_STD, dt, device)
+            sh_up = _normal(g, (S, H), WEIGHT_STD, dt, device)
+            sh_down = _normal(g, (H, S), WEIGHT_STD, dt, device)
+        else:
+            sh_gate, scales["sh_gate_scale"] = mx_quantize(_normal(g, (S, H), WEIGHT_STD, torch.float32, device), wf)
+            sh_up, scales["sh_up_scale"] = mx_quantize(_normal(g, (S, H), WEIGHT_STD, torch.float32, device), wf)
+            sh_down, scales["sh_down_scale"] = mx_quantize(_normal(g, (H, S), WEIGHT_STD, torch.float32, device),
+                                                           wf)
     pre_norm_w = post_norm_w = None
     if shape.mlp_norm != "none":
         centre = 1.0 if shape.mlp_norm == "rms" else 0.0
@@ -276,7 +333,7 @@ def make_inputs(shape: MoeShape, device="cpu",
 
     return dict(X=X, router_w=router_w, expert_bias=expert_bias, gate=gate, up=up, down=down,
                 sh_gate=sh_gate, sh_up=sh_up, sh_down=sh_down, pre_norm_w=pre_norm_w,
-                post_norm_w=post_norm_w, redraws=redraws)
+                post_norm_w=post_norm_w, redraws=redraws, **scales)
 
 
 def expert_weights_bf16(inputs: dict) -> dict:
@@ -288,5 +345,6 @@ def expert_weights_bf16(inputs: dict) -> dict:
     out = {}
     for key in ("gate", "up", "down", "sh_gate", "sh_up", "sh_down"):
         t = inputs[key]
-        out[key] = None if t is None else t.to(torch.bfloat16).contiguous()
+        # MX element codes (uint8) pass through, like bf16 tensors
+        out[key] = None if t is None else (t if t.dtype == torch.uint8 else t.to(torch.bfloat16).contiguous())
     return out

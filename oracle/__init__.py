@@ -28,7 +28,10 @@ _SRC = os.path.join(_HERE, "moe_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_BUILD, "libmoe_oracle.so")
 
-OR_F32, OR_BF16 = 0, 1
+OR_F32, OR_BF16, OR_MXFP8, OR_MXFP4 = 0, 1, 2, 3
+# expert weight formats of a workload -> the oracle's dtype code (None: as stored)
+WEIGHT_FORMATS = {"bf16": None, "mxfp8": OR_MXFP8, "mxfp4": OR_MXFP4}
+SCALE_KEYS = ("gate_scale", "up_scale", "down_scale", "sh_gate_scale", "sh_up_scale", "sh_down_scale")
 OR_SIGMOID, OR_SOFTMAX = 0, 1
 OR_SILU, OR_SWIGLU_OAI = 0, 1
 
@@ -63,18 +66,20 @@ def _configure(L):
                                P, P, P, P, P, P, P, ctypes.c_int]
     L.oracle_route.restype = ctypes.c_int
     L.oracle_forward.argtypes = [ctypes.POINTER(OracleCfg), P, ctypes.c_int, P, P, P, P, P,
-                                 P, P, P, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int]
+                                 P, P, P, ctypes.c_int, P, ctypes.c_int, P, P, ctypes.c_int]
     L.oracle_forward.restype = ctypes.c_int
     L.oracle_expert.argtypes = [ctypes.POINTER(OracleCfg), P, ctypes.c_int, P, P, P,
-                                ctypes.c_int, ctypes.c_int, P, P, P, P]
+                                ctypes.c_int, P, ctypes.c_int, P, P, P, P]
     L.oracle_expert.restype = ctypes.c_int
     L.oracle_act.argtypes = [ctypes.POINTER(OracleCfg), ctypes.c_double, ctypes.c_double]
     L.oracle_act.restype = ctypes.c_double
-    L.oracle_dense.argtypes = [ctypes.POINTER(OracleCfg), P, ctypes.c_int, P, P, P, ctypes.c_int, ctypes.c_int,
-                               P, P, ctypes.c_int]
+    L.oracle_dense.argtypes = [ctypes.POINTER(OracleCfg), P, ctypes.c_int, P, P, P, ctypes.c_int, P,
+                               ctypes.c_int, P, P, ctypes.c_int]
     L.oracle_dense.restype = ctypes.c_int
     L.oracle_rmsnorm.argtypes = [P, ctypes.c_int, P, ctypes.c_double, ctypes.c_int, P]
     L.oracle_rmsnorm.restype = ctypes.c_int
+    L.oracle_mx_value.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    L.oracle_mx_value.restype = ctypes.c_double
     return L
 
 
@@ -166,6 +171,45 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _u8(a):
+    """uint8 array (or tensor) of MX element or scale codes."""
+    if a is None:
+        return None
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            a = a.detach().contiguous().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint8:
+        raise TypeError("MX element and scale codes are uint8")
+    return a
+
+
+def _weights(tensors, wfmt, scales):
+    """Expert weight tensors -> (host arrays, dtype code, ctypes array of the
+    scale pointers or None, the scale arrays kept alive)."""
+    code = WEIGHT_FORMATS[wfmt]
+    if code is None:
+        hs, ds = zip(*[(None, None) if t is None else _as_host(t) for t in tensors])
+        used = {d for d in ds if d is not None}
+        if len(used) != 1:
+            raise TypeError("the expert tensors must share one dtype")
+        return list(hs), used.pop(), None, None
+    if scales is None or len(scales) != len(tensors):
+        raise ValueError("MX weights need one scale tensor per weight tensor")
+    hs = [_u8(t) for t in tensors]
+    sc = [_u8(t) for t in scales]
+    arr = (ctypes.c_void_p * len(sc))(*[None if a is None else a.ctypes.data for a in sc])
+    return hs, code, arr, sc
+
+
+def mx_value(wfmt: str, code: int, scale: int) -> float:
+    """Decoded MX element (E4M3 byte or E2M1 nibble) times its E8M0 scale."""
+    return lib().oracle_mx_value(WEIGHT_FORMATS[wfmt], int(code), int(scale))
+
+
 def _f32(a):
     if a is None:
         return None
@@ -206,40 +250,43 @@ def route(cfg: OracleCfg, X, Wr, bias=None, tokens=None, nthreads=0) -> dict:
 
 
 def forward(cfg: OracleCfg, X, Wr, bias, Wg, Wu, Wd, Wgs=None, Wus=None, Wds=None,
-            tokens=None, nthreads=0) -> np.ndarray:
-    """Block output Y [n,H] (fp64) for the listed tokens."""
+            tokens=None, nthreads=0, wfmt="bf16", scales=None) -> np.ndarray:
+    """Block output Y [n,H] (fp64) for the listed tokens.  wfmt "mxfp8" /
+    "mxfp4": the six weight tensors hold uint8 element codes and ``scales`` the
+    six block-major uint8 scale tensors (None where a tensor is unused)."""
     Xh, xd = _as_host(X)
     T = Xh.shape[0]
     Wrh, bh = _f32(Wr), _f32(bias)
-    Wgh, wd = _as_host(Wg)
-    Wuh, wd2 = _as_host(Wu)
-    Wdh, wd3 = _as_host(Wd)
-    if not (wd == wd2 == wd3):
-        raise TypeError("gate/up/down must share a dtype")
-    sh = [None, None, None]
-    if not cfg.shared_packed and cfg.S > 0:
-        for i, t in enumerate((Wgs, Wus, Wds)):
-            sh[i], d = _as_host(t)
-            if d != wd:
-                raise TypeError("shared tensors must share the expert dtype")
+    use_sh = not cfg.shared_packed and cfg.S > 0
+    tensors = [Wg, Wu, Wd] + ([Wgs, Wus, Wds] if use_sh else [None, None, None])
+    if scales is not None and not use_sh:
+        scales = list(scales[:3]) + [None, None, None]
+    hs, wd, sc_arr, _keep = _weights(tensors, wfmt, scales)
     tk, n = _tokens(tokens, T)
     Y = np.empty((n, cfg.H))
     if n == 0:
         return Y
-    r = lib().oracle_forward(ctypes.byref(cfg), _ptr(Xh), xd, _ptr(Wrh), _ptr(bh), _ptr(Wgh),
-                             _ptr(Wuh), _ptr(Wdh), _ptr(sh[0]), _ptr(sh[1]), _ptr(sh[2]), wd, n,
-                             _ptr(tk), _ptr(Y), int(nthreads))
+    r = lib().oracle_forward(ctypes.byref(cfg), _ptr(Xh), xd, _ptr(Wrh), _ptr(bh), _ptr(hs[0]),
+                             _ptr(hs[1]), _ptr(hs[2]), _ptr(hs[3]), _ptr(hs[4]), _ptr(hs[5]), wd,
+                             sc_arr, n, _ptr(tk), _ptr(Y), int(nthreads))
     if r < 0:
         raise ValueError("oracle_forward rejected its arguments")
     return Y
 
 
+def _scales(shape, inputs: dict):
+    if shape.weight_format == "bf16":
+        return None
+    return [inputs.get(k) for k in SCALE_KEYS]
+
+
 def forward_inputs(shape, inputs: dict, tokens=None, nthreads=0) -> np.ndarray:
     """Block output for a workloads.make_inputs() dict (the oracle sees the
-    workload's own dtypes: fp32 expert weights stay fp32)."""
+    workload's own dtypes: fp32 expert weights stay fp32, MX codes are decoded)."""
     return forward(cfg_from_shape(shape), inputs["X"], inputs["router_w"], inputs["expert_bias"],
                    inputs["gate"], inputs["up"], inputs["down"], inputs["sh_gate"],
-                   inputs["sh_up"], inputs["sh_down"], tokens=tokens, nthreads=nthreads)
+                   inputs["sh_up"], inputs["sh_down"], tokens=tokens, nthreads=nthreads,
+                   wfmt=shape.weight_format, scales=_scales(shape, inputs))
 
 
 def route_inputs(shape, inputs: dict, tokens=None, nthreads=0) -> dict:
@@ -247,15 +294,14 @@ def route_inputs(shape, inputs: dict, tokens=None, nthreads=0) -> dict:
                  tokens=tokens, nthreads=nthreads)
 
 
-def expert(cfg: OracleCfg, x, Wg, Wu, Wd, width: int):
-    """One expert MLP on one token: returns (g, u, a, y) in fp64."""
+def expert(cfg: OracleCfg, x, Wg, Wu, Wd, width: int, wfmt="bf16", scales=None):
+    """One expert MLP on one token: returns (g, u, a, y) in fp64 (MX weights:
+    uint8 codes and the three scale tensors)."""
     xh, xd = _as_host(x)
-    Wgh, wd = _as_host(Wg)
-    Wuh, _ = _as_host(Wu)
-    Wdh, _ = _as_host(Wd)
+    hs, wd, sc_arr, _keep = _weights([Wg, Wu, Wd], wfmt, scales)
     g, u, a, y = (np.empty(width), np.empty(width), np.empty(width), np.empty(cfg.H))
-    r = lib().oracle_expert(ctypes.byref(cfg), _ptr(xh), xd, _ptr(Wgh), _ptr(Wuh), _ptr(Wdh), wd,
-                            int(width), _ptr(g), _ptr(u), _ptr(a), _ptr(y))
+    r = lib().oracle_expert(ctypes.byref(cfg), _ptr(xh), xd, _ptr(hs[0]), _ptr(hs[1]), _ptr(hs[2]), wd,
+                            sc_arr, int(width), _ptr(g), _ptr(u), _ptr(a), _ptr(y))
     if r < 0:
         raise ValueError("oracle_expert rejected its arguments")
     return g, u, a, y
@@ -265,19 +311,17 @@ def act(cfg: OracleCfg, g: float, u: float) -> float:
     return lib().oracle_act(ctypes.byref(cfg), float(g), float(u))
 
 
-def dense(cfg: OracleCfg, X, Wg, Wu, Wd, tokens=None, nthreads=0) -> np.ndarray:
+def dense(cfg: OracleCfg, X, Wg, Wu, Wd, tokens=None, nthreads=0, wfmt="bf16", scales=None) -> np.ndarray:
     """Dense MLP of width cfg.S (a dense prefix layer) for the listed tokens: [n,H] fp64."""
     Xh, xd = _as_host(X)
     T = Xh.shape[0]
-    Wgh, wd = _as_host(Wg)
-    Wuh, _ = _as_host(Wu)
-    Wdh, _ = _as_host(Wd)
+    hs, wd, sc_arr, _keep = _weights([Wg, Wu, Wd], wfmt, scales)
     tk, n = _tokens(tokens, T)
     Y = np.empty((n, cfg.H))
     if n == 0:
         return Y
-    r = lib().oracle_dense(ctypes.byref(cfg), _ptr(Xh), xd, _ptr(Wgh), _ptr(Wuh), _ptr(Wdh), wd, n, _ptr(tk),
-                           _ptr(Y), int(nthreads))
+    r = lib().oracle_dense(ctypes.byref(cfg), _ptr(Xh), xd, _ptr(hs[0]), _ptr(hs[1]), _ptr(hs[2]), wd, sc_arr,
+                           n, _ptr(tk), _ptr(Y), int(nthreads))
     if r < 0:
         raise ValueError("oracle_dense rejected its arguments")
     return Y
@@ -327,13 +371,14 @@ def block_output(shape, inputs: dict, tokens=None, nthreads=0) -> np.ndarray:
     X = inputs["X"]
     xin = X if shape.mlp_norm == "none" else normed_input(shape, X, inputs["pre_norm_w"])
     cfg = cfg_from_shape(shape)
+    sc = _scales(shape, inputs)
     if shape.E == 0:
         y = dense(cfg, xin, inputs["sh_gate"], inputs["sh_up"], inputs["sh_down"], tokens=tokens,
-                  nthreads=nthreads)
+                  nthreads=nthreads, wfmt=shape.weight_format, scales=None if sc is None else sc[3:])
     else:
         y = forward(cfg, xin, inputs["router_w"], inputs["expert_bias"], inputs["gate"], inputs["up"],
                     inputs["down"], inputs["sh_gate"], inputs["sh_up"], inputs["sh_down"], tokens=tokens,
-                    nthreads=nthreads)
+                    nthreads=nthreads, wfmt=shape.weight_format, scales=sc)
     if shape.mlp_norm == "none":
         return y
     x = to_f64(X)

@@ -54,6 +54,21 @@
  *       (Arcee AFMoE issue: pre_mlp_layernorm / post_mlp_layernorm in a
  *        sandwich; HF AFMoE docs, AfmoeConfig rms_norm_eps; MiniMax-M3 issue:
  *        Gemma-style RMSNorm, weight + 1, on all norms).
+ *
+ * Block-scaled expert weights (the pages' checkpoints are 4-bit (Arcee AFMoE
+ * issue, "Checkpoint confirmed") and MXFP8 (MiniMax-M3 issue, "Validation")):
+ * an element is decoded exactly to double and multiplied by its block's scale,
+ * following the OCP Microscaling Formats (MX) v1.0 specification:
+ *   - E8M0 scale: 2^(s - 127); s = 255 is NaN;
+ *   - E4M3 element (MXFP8): sign, 4 exponent bits (bias 7), 3 mantissa bits;
+ *       exponent 0 is subnormal (2^-6 * m/8); S.1111.111 is NaN, no infinities;
+ *   - E2M1 element (MXFP4): sign, 2 exponent bits (bias 1), 1 mantissa bit;
+ *       exponent 0 is subnormal (m/2): the values 0, 0.5, 1, 1.5, 2, 3, 4, 6;
+ *   - one scale per 32 consecutive elements along the reduction index.
+ * Storage (this library's reading; the pages give no layout): element codes
+ * row-major like the bf16 tensors, one per byte (E4M3) or two per byte (E2M1,
+ * element 2j in the low nibble); scales of a [rows, cols] matrix block-major,
+ * scale[(c / 32) * rows + r] for element (r, c).
  */
 #include <math.h>
 #include <pthread.h>
@@ -62,7 +77,7 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { OR_F32 = 0, OR_BF16 = 1 };
+enum { OR_F32 = 0, OR_BF16 = 1, OR_MXFP8 = 2, OR_MXFP4 = 3 };
 enum { OR_SIGMOID = 0, OR_SOFTMAX = 1 };
 enum { OR_SILU = 0, OR_SWIGLU_OAI = 1 };
 
@@ -88,6 +103,44 @@ static double ld(const void *p, int dtype, size_t i)
     }
     return (double)((const float *)p)[i];
 }
+
+static double e8m0(uint8_t s) { return s == 255 ? NAN : ldexp(1.0, (int)s - 127); }
+
+static double e4m3(uint8_t b)
+{
+    const int e = (b >> 3) & 15, m = b & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return (b & 0x80) ? -v : v;
+}
+
+static double e2m1(uint8_t n)
+{
+    const int e = (n >> 1) & 3, m = n & 1;
+    const double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return (n & 8) ? -v : v;
+}
+
+/* Element (r, c) of a [rows, cols] weight matrix (c: the reduction index) of
+ * dtype wd; scale: the MX block scales (block-major), or NULL. */
+static double wget(const void *q, const uint8_t *scale, int wd, size_t r, size_t c, size_t rows, size_t cols)
+{
+    const size_t i = r * cols + c;
+    if (wd == OR_MXFP8) return e8m0(scale[(c / 32) * rows + r]) * e4m3(((const uint8_t *)q)[i]);
+    if (wd == OR_MXFP4) {
+        const uint8_t b = ((const uint8_t *)q)[i / 2];
+        return e8m0(scale[(c / 32) * rows + r]) * e2m1((uint8_t)((i & 1) ? b >> 4 : b & 15));
+    }
+    return ld(q, wd, i);
+}
+
+/* bytes of n elements of dtype wd (n even for E2M1) */
+static size_t wbytes(int wd, size_t n)
+{
+    return wd == OR_F32 ? 4 * n : wd == OR_BF16 ? 2 * n : wd == OR_MXFP8 ? n : n / 2;
+}
+
+static int mx(int wd) { return wd == OR_MXFP8 || wd == OR_MXFP4; }
 
 static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
 
@@ -161,18 +214,20 @@ static void route_token(const oracle_cfg *c, const void *X, int xd, size_t row,
 }
 
 /* One expert MLP of width W on one token: g = Wg x, u = Wu x, a = act(g,u),
- * y = Wd a.  Wg, Wu are [W,H]; Wd is [H,W]; all of dtype wd.  x: H doubles.
- * g, u, a may be NULL.  y: H doubles (overwritten). */
+ * y = Wd a.  Wg, Wu are [W,H]; Wd is [H,W]; all of dtype wd, with block scales
+ * sg, su, sd for the MX formats.  x: H doubles.  g, u, a may be NULL.  y: H
+ * doubles (overwritten). */
 static void expert_mlp(const oracle_cfg *c, const double *x, const void *Wg, const void *Wu,
-                       const void *Wd, int wd, int W, double *g, double *u, double *a, double *y)
+                       const void *Wd, int wd, const uint8_t *sg, const uint8_t *su, const uint8_t *sd,
+                       int W, double *g, double *u, double *a, double *y)
 {
     const int H = c->H;
     double *act = (double *)malloc(sizeof(double) * W);
     for (int i = 0; i < W; i++) {
         double gi = 0.0, ui = 0.0;
         for (int h = 0; h < H; h++) {
-            gi += ld(Wg, wd, (size_t)i * H + h) * x[h];
-            ui += ld(Wu, wd, (size_t)i * H + h) * x[h];
+            gi += wget(Wg, sg, wd, (size_t)i, (size_t)h, (size_t)W, (size_t)H) * x[h];
+            ui += wget(Wu, su, wd, (size_t)i, (size_t)h, (size_t)W, (size_t)H) * x[h];
         }
         act[i] = oracle_act(c, gi, ui);
         if (g) g[i] = gi;
@@ -181,7 +236,7 @@ static void expert_mlp(const oracle_cfg *c, const double *x, const void *Wg, con
     }
     for (int h = 0; h < H; h++) {
         double acc = 0.0;
-        for (int i = 0; i < W; i++) acc += ld(Wd, wd, (size_t)h * W + i) * act[i];
+        for (int i = 0; i < W; i++) acc += wget(Wd, sd, wd, (size_t)h, (size_t)i, (size_t)H, (size_t)W) * act[i];
         y[h] = acc;
     }
     free(act);
@@ -196,6 +251,7 @@ typedef struct {
     const float *Wr, *bias;
     const void *Wg, *Wu, *Wd, *Wgs, *Wus, *Wds;
     int wd;
+    const uint8_t *sc[6]; /* MX block scales of Wg, Wu, Wd, Wgs, Wus, Wds */
     const int *tokens;
     int n;
     /* route outputs */
@@ -224,20 +280,21 @@ static void forward_token(const job *j, int i)
     for (int h = 0; h < H; h++) y[h] = 0.0;
 
     const size_t gsz = (size_t)I * H; /* one slice of the stacked gate/up/down */
-    for (int s = 0; s < k; s++) {
-        const size_t e = (size_t)idx[s];
-        const size_t off = e * gsz * (j->wd == OR_BF16 ? 2 : 4);
+    const int m = mx(j->wd);
+    for (int s = 0; s <= k; s++) {
+        /* the k routed experts, then the packed shared expert (slice E, weight 1.0) */
+        if (s == k && !c->shared_packed) break;
+        const size_t e = s < k ? (size_t)idx[s] : (size_t)c->E;
+        const size_t off = wbytes(j->wd, e * gsz), soff = e * gsz / 32;
         expert_mlp(c, x, (const char *)j->Wg + off, (const char *)j->Wu + off,
-                   (const char *)j->Wd + off, j->wd, I, NULL, NULL, NULL, ye);
-        for (int h = 0; h < H; h++) y[h] += w[s] * ye[h];
+                   (const char *)j->Wd + off, j->wd, m ? j->sc[0] + soff : NULL,
+                   m ? j->sc[1] + soff : NULL, m ? j->sc[2] + soff : NULL, I, NULL, NULL, NULL, ye);
+        const double ws = s < k ? w[s] : 1.0;
+        for (int h = 0; h < H; h++) y[h] += ws * ye[h];
     }
-    if (c->shared_packed) {
-        const size_t off = (size_t)c->E * gsz * (j->wd == OR_BF16 ? 2 : 4);
-        expert_mlp(c, x, (const char *)j->Wg + off, (const char *)j->Wu + off,
-                   (const char *)j->Wd + off, j->wd, I, NULL, NULL, NULL, ye);
-        for (int h = 0; h < H; h++) y[h] += 1.0 * ye[h];
-    } else if (c->S > 0) {
-        expert_mlp(c, x, j->Wgs, j->Wus, j->Wds, j->wd, c->S, NULL, NULL, NULL, ye);
+    if (!c->shared_packed && c->S > 0) {
+        expert_mlp(c, x, j->Wgs, j->Wus, j->Wds, j->wd, j->sc[3], j->sc[4], j->sc[5], c->S, NULL, NULL, NULL,
+                   ye);
         for (int h = 0; h < H; h++) y[h] += 1.0 * ye[h];
     }
     for (int h = 0; h < H; h++) j->Y[(size_t)i * H + h] = y[h];
@@ -253,7 +310,8 @@ static void dense_token(const job *j, int i)
     const size_t t = (size_t)token_of(j, i);
     double *x = (double *)malloc(sizeof(double) * H);
     for (int h = 0; h < H; h++) x[h] = ld(j->X, j->xd, t * H + h);
-    expert_mlp(c, x, j->Wgs, j->Wus, j->Wds, j->wd, c->S, NULL, NULL, NULL, j->Y + (size_t)i * H);
+    expert_mlp(c, x, j->Wgs, j->Wus, j->Wds, j->wd, j->sc[3], j->sc[4], j->sc[5], c->S, NULL, NULL, NULL,
+               j->Y + (size_t)i * H);
     free(x);
 }
 
@@ -340,17 +398,30 @@ int oracle_route(const oracle_cfg *c, const void *X, int x_dtype, const float *W
     return run_jobs(&j, nthreads);
 }
 
+/* the six MX scale pointers are present for the tensors that are used */
+static int scales_ok(const uint8_t *const *sc, int w_dtype, int routed, int shared)
+{
+    if (!mx(w_dtype)) return 1;
+    if (!sc) return 0;
+    for (int i = 0; i < 3; i++)
+        if ((routed && !sc[i]) || (shared && !sc[3 + i])) return 0;
+    return 1;
+}
+
 /* Full block output for n tokens: Y [n,H] doubles.  Expert tensors: Wg, Wu
  * [E',I,H], Wd [E',H,I] with E' = E (+1 when packed), dtype w_dtype; shared
- * tensors Wgs, Wus [S,H], Wds [H,S] (ignored when packed or S == 0).
+ * tensors Wgs, Wus [S,H], Wds [H,S] (ignored when packed or S == 0).  MX
+ * dtypes: scales[6] = block scales of Wg, Wu, Wd, Wgs, Wus, Wds ([E', H/32, I],
+ * [E', H/32, I], [E', I/32, H], [H/32, S], [H/32, S], [S/32, H]); else NULL.
  * Returns threads used, or -1. */
 int oracle_forward(const oracle_cfg *c, const void *X, int x_dtype, const float *Wr,
                    const float *bias, const void *Wg, const void *Wu, const void *Wd,
-                   const void *Wgs, const void *Wus, const void *Wds, int w_dtype, int n,
-                   const int *tokens, double *Y, int nthreads)
+                   const void *Wgs, const void *Wus, const void *Wds, int w_dtype,
+                   const uint8_t *const *scales, int n, const int *tokens, double *Y, int nthreads)
 {
     if (!cfg_ok(c) || !X || !Wr || !Wg || !Wu || !Wd || !Y || n < 0) return -1;
     if (!c->shared_packed && c->S > 0 && (!Wgs || !Wus || !Wds)) return -1;
+    if (!scales_ok(scales, w_dtype, 1, !c->shared_packed && c->S > 0)) return -1;
     job j;
     memset(&j, 0, sizeof j);
     j.c = c;
@@ -365,6 +436,8 @@ int oracle_forward(const oracle_cfg *c, const void *X, int x_dtype, const float 
     j.Wus = Wus;
     j.Wds = Wds;
     j.wd = w_dtype;
+    if (mx(w_dtype))
+        for (int i = 0; i < 6; i++) j.sc[i] = scales[i];
     j.tokens = tokens;
     j.n = n;
     j.Y = Y;
@@ -373,11 +446,14 @@ int oracle_forward(const oracle_cfg *c, const void *X, int x_dtype, const float 
 }
 
 /* Dense MLP of width c->S (router and experts unused) for n tokens: Y [n,H]
- * doubles.  Wg, Wu: [S,H]; Wd: [H,S]; dtype w_dtype.  Returns threads used, or -1. */
+ * doubles.  Wg, Wu: [S,H]; Wd: [H,S]; dtype w_dtype, MX scales[3] of Wg, Wu,
+ * Wd or NULL.  Returns threads used, or -1. */
 int oracle_dense(const oracle_cfg *c, const void *X, int x_dtype, const void *Wg, const void *Wu,
-                 const void *Wd, int w_dtype, int n, const int *tokens, double *Y, int nthreads)
+                 const void *Wd, int w_dtype, const uint8_t *const *scales, int n, const int *tokens,
+                 double *Y, int nthreads)
 {
     if (!c || c->H <= 0 || c->S <= 0 || !X || !Wg || !Wu || !Wd || !Y || n < 0) return -1;
+    if (!scales_ok(scales, w_dtype, 1, 0)) return -1;
     job j;
     memset(&j, 0, sizeof j);
     j.c = c;
@@ -387,6 +463,8 @@ int oracle_dense(const oracle_cfg *c, const void *X, int x_dtype, const void *Wg
     j.Wus = Wu;
     j.Wds = Wd;
     j.wd = w_dtype;
+    if (mx(w_dtype))
+        for (int i = 0; i < 3; i++) j.sc[3 + i] = scales[i];
     j.tokens = tokens;
     j.n = n;
     j.Y = Y;
@@ -408,15 +486,29 @@ int oracle_rmsnorm(const double *x, int H, const double *w, double eps, int gemm
 
 /* One expert MLP of width W on one token row x (H values of x_dtype), for
  * checking intermediate values: g, u, a [W] and y [H] doubles (g, u, a may be
- * NULL).  Wg, Wu: [W,H]; Wd: [H,W]; dtype w_dtype. */
+ * NULL).  Wg, Wu: [W,H]; Wd: [H,W]; dtype w_dtype, MX scales[3] of Wg, Wu, Wd
+ * or NULL. */
 int oracle_expert(const oracle_cfg *c, const void *x, int x_dtype, const void *Wg,
-                  const void *Wu, const void *Wd, int w_dtype, int W, double *g, double *u,
-                  double *a, double *y)
+                  const void *Wu, const void *Wd, int w_dtype, const uint8_t *const *scales, int W,
+                  double *g, double *u, double *a, double *y)
 {
     if (!c || c->H <= 0 || !x || !Wg || !Wu || !Wd || !y || W <= 0) return -1;
+    if (!scales_ok(scales, w_dtype, 1, 0)) return -1;
     double *xd = (double *)malloc(sizeof(double) * c->H);
     for (int h = 0; h < c->H; h++) xd[h] = ld(x, x_dtype, (size_t)h);
-    expert_mlp(c, xd, Wg, Wu, Wd, w_dtype, W, g, u, a, y);
+    const int m = mx(w_dtype);
+    expert_mlp(c, xd, Wg, Wu, Wd, w_dtype, m ? scales[0] : NULL, m ? scales[1] : NULL, m ? scales[2] : NULL, W,
+               g, u, a, y);
     free(xd);
     return 0;
+}
+
+/* Decoded value of one MX element code (dtype OR_MXFP8: a byte; OR_MXFP4: a
+ * nibble) times the E8M0 scale code, for checking the decoders. */
+double oracle_mx_value(int w_dtype, int code, int scale)
+{
+    const double sc = e8m0((uint8_t)scale);
+    if (w_dtype == OR_MXFP8) return sc * e4m3((uint8_t)code);
+    if (w_dtype == OR_MXFP4) return sc * e2m1((uint8_t)(code & 15));
+    return NAN;
 }

@@ -32,26 +32,37 @@ MUTANTS = [
     ("beta dropped", "(uc + c->beta)", "(uc)"),
     ("alpha dropped", "sigmoid(c->alpha * gc)", "sigmoid(gc)"),
     ("silu on the up projection", "return g * sigmoid(g) * u;", "return g * sigmoid(u) * u;"),
-    ("down projection transposed", "ld(Wd, wd, (size_t)h * W + i)", "ld(Wd, wd, (size_t)i * H + h)"),
-    ("gate/up swapped", "gi += ld(Wg, wd, (size_t)i * H + h) * x[h];\n            ui += ld(Wu, wd, (size_t)i * H + h) * x[h];",
-     "gi += ld(Wu, wd, (size_t)i * H + h) * x[h];\n            ui += ld(Wg, wd, (size_t)i * H + h) * x[h];"),
+    ("down projection transposed", "wget(Wd, sd, wd, (size_t)h, (size_t)i, (size_t)H, (size_t)W)",
+     "wget(Wd, sd, wd, (size_t)i, (size_t)h, (size_t)W, (size_t)H)"),
+    ("gate/up swapped", "gi += wget(Wg, sg, wd,", "gi += wget(Wu, su, wd,"),
     ("router weight transposed", "(double)Wr[(size_t)e * H + h]", "(double)Wr[(size_t)h * E + e]"),
     ("shared expert scaled by route_scale", "for (int h = 0; h < H; h++) y[h] += 1.0 * ye[h];",
      "for (int h = 0; h < H; h++) y[h] += c->route_scale * ye[h];"),
-    ("packed shared read from slice 0", "const size_t off = (size_t)c->E * gsz", "const size_t off = (size_t)0 * gsz"),
-    ("shared expert dropped", "} else if (c->S > 0) {", "} else if (0) {"),
-    ("one routed slot dropped", "for (int s = 0; s < k; s++) {\n        const size_t e", "for (int s = 1; s < k; s++) {\n        const size_t e"),
+    ("packed shared read from slice 0", "(size_t)idx[s] : (size_t)c->E;", "(size_t)idx[s] : (size_t)0;"),
+    ("packed shared scaled by route_scale", "w[s] : 1.0;", "w[s] : c->route_scale;"),
+    ("shared expert dropped", "if (!c->shared_packed && c->S > 0) {\n        expert_mlp", "if (0) {\n        expert_mlp"),
+    ("one routed slot dropped", "for (int s = 0; s <= k; s++) {", "for (int s = 1; s <= k; s++) {"),
     ("margin off by one", "cb[order[k - 1]] - cb[order[k]]", "cb[order[k - 2 < 0 ? 0 : k - 2]] - cb[order[k]]"),
     ("bf16 decoded with the wrong shift", "<< 16;", "<< 15;"),
     # the layers around the block
-    ("dense MLP reads the routed width", "expert_mlp(c, x, j->Wgs, j->Wus, j->Wds, j->wd, c->S,",
-     "expert_mlp(c, x, j->Wgs, j->Wus, j->Wds, j->wd, c->S / 2,"),
+    ("dense MLP reads the routed width", "j->sc[4], j->sc[5], c->S, NULL, NULL, NULL,\n               j->Y",
+     "j->sc[4], j->sc[5], c->S / 2, NULL, NULL, NULL,\n               j->Y"),
     ("rmsnorm without eps", "sqrt(ss / (double)H + eps)", "sqrt(ss / (double)H)"),
     ("rmsnorm over H - 1", "sqrt(ss / (double)H + eps)", "sqrt(ss / (double)(H - 1) + eps)"),
     ("rmsnorm by the mean square, not its root", "const double r = sqrt(ss / (double)H + eps);",
      "const double r = ss / (double)H + eps;"),
     ("Gemma norm without the + 1", "(gemma ? 1.0 + w[h] : w[h])", "(gemma ? w[h] : w[h])"),
     ("norm weight ignored", "(gemma ? 1.0 + w[h] : w[h])", "(gemma ? 1.0 + w[h] : 1.0)"),
+    # block-scaled expert weights
+    ("MX scales read row-major", "scale[(c / 32) * rows + r]", "scale[r * (cols / 32) + c / 32]"),
+    ("E4M3 exponent bias 8", "ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    ("E4M3 subnormals decoded as normals", "e == 0 ? ldexp((double)m / 8.0, -6)", "e == 0 ? ldexp(1.0 + (double)m / 8.0, -7)"),
+    ("E4M3 mantissa of 2 bits", "(double)m / 8.0, e - 7", "(double)m / 4.0, e - 7"),
+    ("E2M1 nibbles swapped", "(i & 1) ? b >> 4 : b & 15", "(i & 1) ? b & 15 : b >> 4"),
+    ("E2M1 exponent bias 0", "ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e)"),
+    ("E8M0 bias 128", "ldexp(1.0, (int)s - 127)", "ldexp(1.0, (int)s - 128)"),
+    ("MX block of 16", "scale[(c / 32) * rows + r]", "scale[(c / 16) * rows + r]"),
+    ("MX scale of the up projection used for gate", "gi += wget(Wg, sg, wd,", "gi += wget(Wg, su, wd,"),
 ]
 
 PIN_TESTS = [(name, fn) for name, fn in inspect.getmembers(pins, inspect.isfunction)

