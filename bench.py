@@ -6,7 +6,9 @@ dispatch sort, gate/up + activation, down, combine; with the sandwich norms
 also the pre-MLP RMSNorm and, inside the combine, the post-MLP RMSNorm and the
 residual add; a dense prefix layer: its MLP GEMMs and the combine), inputs
 resident in HBM.
-L2 is flushed (a 256 MiB write) before every step, outside the timed events.
+L2 is flushed before every step, outside the timed events: a 256 MiB write, then
+a 256 MiB read, so that the step neither finds its inputs in L2 nor pays for
+writing back the flush buffer's dirty lines (--flush write: the write alone).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -149,10 +151,16 @@ def run_ours(args, shape):
     X = inputs["X"]
     Y = torch.empty_like(X)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if args.flush == "clean" else None
+
+    def flush_l2():
+        flush.fill_(1)  # evicts L2; not inside the timed events
+        if flush_rd is not None:  # then replace the dirty lines by clean ones (their write-back happens here)
+            flush_rd.sum()
 
     def step():
         if not args.no_flush:
-            flush.fill_(1)  # evicts L2; not inside the timed events
+            flush_l2()
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record()
@@ -255,7 +263,7 @@ def run_ours(args, shape):
         blk.forward_host(Xh, Yh)
     e2e_t = []
     for _ in range(args.steps):
-        flush.fill_(1)
+        flush_l2()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         blk.forward_host(Xh, Yh)
@@ -309,7 +317,9 @@ def run_ours(args, shape):
                    "hidden_act": shape.hidden_act, "mlp_norm": shape.mlp_norm, "path": {1: "decode", 2: "grouped", 3: "swapped"}[path],
                    "parallelism": f"replicas{world}",
                    "l2": ("not flushed: inputs larger than L2" if args.no_flush else
-                          "flushed before every step (256 MiB write), flush outside the timed events")},
+                          "flushed before every step (256 MiB write), flush outside the timed events" +
+                          ("; then a 256 MiB read, so the step starts with no dirty L2 lines"
+                           if args.flush == "clean" else ""))},
         "roofline": roof,
         "block_roofline": {"t_roof_us": round(max(t_tc, t_hbm) * 1e6, 2), "t_meas_us": round(ms * 1e3, 2),
                            "frac": round(max(t_tc, t_hbm) / (ms / 1e3), 4),
@@ -439,6 +449,8 @@ def main():
     ap.add_argument("--no-prefetch", action="store_true", help="no L2 prefetch of expert weights while routing")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--preroll", type=float, default=1.0, help="seconds of untimed steps before timing")
+    ap.add_argument("--flush", choices=["write", "clean"], default="clean",
+                    help="L2 flush before each step: a 256 MiB write, or the write and then a 256 MiB read")
     ap.add_argument("--no-flush", action="store_true",
                     help="skip the L2 flush between steps (only valid when the inputs exceed L2)")
     args = ap.parse_args()

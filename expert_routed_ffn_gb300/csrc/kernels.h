@@ -120,7 +120,7 @@ struct PrefetchArgs {
     const void *ptr[2];
     unsigned long long bytes[2];
 };
-cudaError_t launch_l2_prefetch(const PrefetchArgs &a, cudaStream_t s);
+cudaError_t launch_l2_prefetch(const PrefetchArgs &a, int grid, cudaStream_t s);
 // Split fp32 weights w into bf16 hi + mid + lo == w; *flags |= 1 when some w
 // needs mid, |= 2 when some w needs lo.
 cudaError_t launch_split_router(const float *wr, int E, int H, bf16 *parts, int *flags, cudaStream_t s);

@@ -54,7 +54,17 @@ constexpr int kSwapMaxTokensPerExpert = 0;
 // auto path always takes it; the decode kernels stay selectable.
 constexpr int kDecodeMaxTokens = 0;
 // L2 budget for the weight prefetch issued while routing (L2 is 129 MB).
-constexpr unsigned long long kPrefetchBytes = 72ull << 20;
+#ifndef MOE_PREFETCH_MB
+#define MOE_PREFETCH_MB 72
+#endif
+constexpr unsigned long long kPrefetchBytes = (unsigned long long)MOE_PREFETCH_MB << 20;
+// CTAs issuing the prefetch (0: one per SM).  Measured on GB300 (Nano decode):
+// from 18 CTAs the prefetch lands while the router runs without slowing it; from
+// one CTA per SM it takes memory bandwidth from the latency-bound router and the
+// step gets no faster.
+#ifndef MOE_PREFETCH_GRID
+#define MOE_PREFETCH_GRID 18
+#endif
 
 }  // namespace
 
@@ -719,7 +729,7 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
         moe::PrefetchArgs pa{{h->w.gate, h->w.up}, {each < all ? each : all, each < all ? each : all}};
         cudaError_t e = cudaEventRecord(h->ev_fork, s);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
-        if (e == cudaSuccess) e = moe::launch_l2_prefetch(pa, h->side);
+        if (e == cudaSuccess) e = moe::launch_l2_prefetch(pa, MOE_PREFETCH_GRID > 0 ? MOE_PREFETCH_GRID : h->num_sms, h->side);
         if (e == cudaSuccess) e = cudaEventRecord(h->ev_join, h->side);
         if (e != cudaSuccess) return cuda_fail(e, "weight prefetch");
     }

@@ -329,16 +329,27 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
 // L2 prefetch of byte ranges (a hint; nothing is written).  Runs on a side
 // stream next to the routing kernels: a CTA cannot retire before its bulk
 // prefetches complete, so they must stay off the forward's dependency chain.
+// An SM's bulk-copy engine moves on the order of 100-200 GB/s, so the ranges are
+// cut into one contiguous share per CTA over a grid of one CTA per SM, each
+// share issued by the warp's lanes in 16-byte-aligned pieces.
 __global__ void __launch_bounds__(32) l2_prefetch_kernel(const PrefetchArgs p) {
-    constexpr unsigned long long kChunk = 128 * 1024;
-    const unsigned long long stride = (unsigned long long)gridDim.x * 32 * kChunk;
-    for (int r = 0; r < 2; ++r) {
+    const unsigned long long total = p.bytes[0] + p.bytes[1];
+    const unsigned long long share = (total / gridDim.x + 32 * 16 - 1) / (32 * 16) * (32 * 16);
+    const unsigned long long piece = share / 32;
+    unsigned long long c = (unsigned long long)blockIdx.x * share + threadIdx.x * piece;
+    unsigned long long left = piece;
+    for (int r = 0; r < 2 && left > 0; ++r) {
         const unsigned long long n = p.bytes[r];
-        const char *base = static_cast<const char *>(p.ptr[r]);
-        for (unsigned long long c = ((unsigned long long)blockIdx.x * 32 + threadIdx.x) * kChunk; c < n; c += stride) {
-            const unsigned bytes = (unsigned)(n - c < kChunk ? n - c : kChunk);
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + c), "r"(bytes) : "memory");
+        if (c >= n) {
+            c -= n;
+            continue;
         }
+        const unsigned long long len = n - c < left ? n - c : left;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(static_cast<const char *>(p.ptr[r]) + c),
+                     "r"((unsigned)len)
+                     : "memory");
+        left -= len;
+        c = 0;
     }
 }
 
@@ -381,14 +392,17 @@ RouterTcPlan plan_router_tc(int E, int parts) {
     return pl;
 }
 
-cudaError_t launch_l2_prefetch(const PrefetchArgs &a, cudaStream_t s) {
+cudaError_t launch_l2_prefetch(const PrefetchArgs &a, int grid, cudaStream_t s) {
     // runs beside the expert GEMM's CTAs: keep the SM's shared memory available to them
     static std::once_flag once;
     std::call_once(once, [] {
         cudaFuncSetAttribute(l2_prefetch_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     });
-    l2_prefetch_kernel<<<64, 32, 0, s>>>(a);
+    if ((a.bytes[0] | a.bytes[1]) % 16 != 0 || grid < 1) return cudaErrorInvalidValue;
+    // a piece must fit the instruction's 32-bit size
+    if ((a.bytes[0] + a.bytes[1]) / (unsigned long long)grid / 32 >= (1ull << 31)) return cudaErrorInvalidValue;
+    l2_prefetch_kernel<<<grid, 32, 0, s>>>(a);
     return cudaGetLastError();
 }
 
