@@ -55,19 +55,24 @@ def work_model(shape, U: int):
     width S as the "shared" term).  With the sandwich norms add the two fp32
     norm weights (8H bytes) and 8TH FLOPs (square, sum, scale and gain per
     element of both norms, and the residual add counted with them).
-    Intermediate buffers are implementation traffic and are not counted."""
+    Intermediate buffers are implementation traffic and are not counted.
+    MX weights: 1 (E4M3) or 1/2 (E2M1) byte per weight plus 1/32 byte of scale
+    in place of the 2 bytes of bf16."""
     T, H, E, k, I, S = shape.T, shape.H, shape.E, shape.k, shape.I, shape.S
+    # bytes per expert weight: bf16, or an MX element code plus its share of an
+    # E8M0 scale byte per 32 weights
+    bpw = {"bf16": 2.0, "mxfp8": 1.0 + 1.0 / 32, "mxfp4": 0.5 + 1.0 / 32}[getattr(shape, "weight_format", "bf16")]
     F = T * (2 * H * E + 6 * H * I * k + 6 * H * S)
-    B = U * 3 * H * I * 2 + 3 * H * S * 2 + 4 * E * H + 4 * E + 2 * 2 * T * H
+    B = int((U * 3 * H * I + 3 * H * S) * bpw) + 4 * E * H + 4 * E + 2 * 2 * T * H
     if shape.mlp_norm != "none":
         F += 8 * T * H
         B += 8 * H
     kernels = {
-        "gate_up": dict(flops=4 * T * H * (k * I + S), bytes=(U * 2 * H * I + 2 * H * S) * 2 + 2 * T * H),
-        "down": dict(flops=2 * T * H * (k * I + S), bytes=(U * H * I + H * S) * 2 + 2 * T * H),
+        "gate_up": dict(flops=4 * T * H * (k * I + S), bytes=int((U * 2 * H * I + 2 * H * S) * bpw) + 2 * T * H),
+        "down": dict(flops=2 * T * H * (k * I + S), bytes=int((U * H * I + H * S) * bpw) + 2 * T * H),
     }
     kernels["experts"] = dict(flops=kernels["gate_up"]["flops"] + kernels["down"]["flops"],
-                              bytes=(U * 3 * H * I + 3 * H * S) * 2 + 2 * 2 * T * H)
+                              bytes=int((U * 3 * H * I + 3 * H * S) * bpw) + 2 * 2 * T * H)
     return F, B, kernels
 
 
@@ -314,7 +319,8 @@ def run_ours(args, shape):
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, U(-0.1,0.1) or Zipf bias)",
         "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "E": shape.E, "k": shape.k,
                    "I": shape.I, "S": shape.S, "shared_packed": shape.shared_packed,
-                   "hidden_act": shape.hidden_act, "mlp_norm": shape.mlp_norm, "path": {1: "decode", 2: "grouped", 3: "swapped"}[path],
+                   "hidden_act": shape.hidden_act, "mlp_norm": shape.mlp_norm,
+                   "weight_format": shape.weight_format, "path": {1: "decode", 2: "grouped", 3: "swapped"}[path],
                    "parallelism": f"replicas{world}",
                    "l2": ("not flushed: inputs larger than L2" if args.no_flush else
                           "flushed before every step (256 MiB write), flush outside the timed events" +

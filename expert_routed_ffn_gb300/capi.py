@@ -25,6 +25,9 @@ MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
 MOE_ACT_SILU, MOE_ACT_SWIGLU_OAI = 0, 1
 MOE_DTYPE_BF16, MOE_DTYPE_F32 = 0, 1
 MOE_NORM_NONE, MOE_NORM_RMS, MOE_NORM_GEMMA = 0, 1, 2
+MOE_WEIGHTS_BF16, MOE_WEIGHTS_MXFP8, MOE_WEIGHTS_MXFP4 = 0, 1, 2
+WEIGHT_FORMATS = {"bf16": MOE_WEIGHTS_BF16, "mxfp8": MOE_WEIGHTS_MXFP8, "mxfp4": MOE_WEIGHTS_MXFP4}
+SCALE_KEYS = ("gate_scale", "up_scale", "down_scale", "sh_gate_scale", "sh_up_scale", "sh_down_scale")
 MOE_OPT_PATH, MOE_OPT_WAIT_LIMIT_NS, MOE_OPT_STAGE_EVENTS, MOE_OPT_FUSE_EXPERTS, MOE_OPT_PREFETCH = 0, 1, 2, 3, 4
 MOE_OPT_TRACE = 5
 MOE_OPT_GEMM_PAIR = 6
@@ -47,13 +50,15 @@ class MoeConfig(ctypes.Structure):
         ("route_scale", ctypes.c_float), ("hidden_act", ctypes.c_int), ("act_alpha", ctypes.c_float),
         ("act_limit", ctypes.c_float), ("act_beta", ctypes.c_float), ("act_dtype", ctypes.c_int),
         ("max_tokens", ctypes.c_int), ("mlp_norm", ctypes.c_int), ("rms_norm_eps", ctypes.c_float),
+        ("weight_format", ctypes.c_int),
     ]
 
 
 class MoeWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("router_w", "expert_bias", "gate", "up", "down", "sh_gate", "sh_up", "sh_down",
-                 "pre_norm_w", "post_norm_w")]
+                 "pre_norm_w", "post_norm_w", "gate_scale", "up_scale", "down_scale", "sh_gate_scale",
+                 "sh_up_scale", "sh_down_scale")]
 
 
 class MoeStats(ctypes.Structure):
@@ -131,7 +136,8 @@ def config_from_shape(shape, max_tokens: int = None) -> MoeConfig:
         act_dtype={"bf16": MOE_DTYPE_BF16, "f32": MOE_DTYPE_F32}[shape.dtype],
         max_tokens=max(1, shape.T if max_tokens is None else max_tokens),
         mlp_norm={"none": MOE_NORM_NONE, "rms": MOE_NORM_RMS, "gemma": MOE_NORM_GEMMA}[shape.mlp_norm],
-        rms_norm_eps=shape.rms_norm_eps)
+        rms_norm_eps=shape.rms_norm_eps,
+        weight_format=WEIGHT_FORMATS[getattr(shape, "weight_format", "bf16")])
 
 
 def _ptr(t):
@@ -150,7 +156,9 @@ class MoeBlock:
     weights: dict with router_w [E,H] fp32, expert_bias [E] fp32 (or None),
     gate/up [E',I,H], down [E',H,I] bf16 and sh_gate/sh_up [S,H], sh_down [H,S]
     bf16 (or None), and pre_norm_w / post_norm_w [H] fp32 with the sandwich
-    norms.  The tensors are kept referenced for the handle's lifetime.
+    norms.  MX weight formats: the six expert tensors hold uint8 element codes
+    and gate_scale ... sh_down_scale their uint8 E8M0 scales.  The tensors are
+    kept referenced for the handle's lifetime.
     """
 
     def __init__(self, config: MoeConfig, weights: dict):
@@ -160,7 +168,7 @@ class MoeBlock:
         self._keep = {k: v for k, v in weights.items() if isinstance(v, torch.Tensor)}
         w = MoeWeights(**{k: (None if weights.get(k) is None else weights[k].data_ptr())
                           for k in ("router_w", "expert_bias", "gate", "up", "down", "sh_gate",
-                                    "sh_up", "sh_down", "pre_norm_w", "post_norm_w")})
+                                    "sh_up", "sh_down", "pre_norm_w", "post_norm_w") + SCALE_KEYS})
         h = ctypes.c_void_p()
         check(load().moe_create(ctypes.byref(config), ctypes.byref(w), ctypes.byref(h)), "moe_create")
         self.h = h
@@ -239,6 +247,7 @@ def block_from_inputs(shape, inputs: dict, max_tokens: int = None) -> MoeBlock:
     rounded to bf16 when the workload stores them in fp32)."""
     from .workloads import expert_weights_bf16
     w = dict(router_w=inputs["router_w"], expert_bias=inputs["expert_bias"], **expert_weights_bf16(inputs),
-             pre_norm_w=inputs.get("pre_norm_w"), post_norm_w=inputs.get("post_norm_w"))
+             pre_norm_w=inputs.get("pre_norm_w"), post_norm_w=inputs.get("post_norm_w"),
+             **{k: inputs.get(k) for k in SCALE_KEYS})
     blk = MoeBlock(config_from_shape(shape, max_tokens), w)
     return blk

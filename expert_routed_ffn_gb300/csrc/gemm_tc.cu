@@ -33,6 +33,8 @@
 // concurrent CTAs share the weight tile in L2.  Every wait is bounded: on timeout the kernel records
 // ERR_TIMEOUT, stops all roles, drains its in-flight copies and MMAs, frees
 // TMEM and returns.
+#include <cuda_fp16.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -176,6 +178,140 @@ __device__ __forceinline__ bool epi_all(bool v) {
 }
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
+
+// Barrier addresses and shared state the epilogue warps use (every kernel lays
+// out ring_full[kRing], ring_empty[kRing], tfull[2], tempty[2] contiguously).
+struct EpiCtx {
+    uint32_t ring_full0, ring_empty0, tfull0, tempty0;
+    volatile int *ring;
+    volatile int *abort_flag;
+    uint32_t tmem_base;
+    int total;
+    const int *s_seg_end, *s_offs, *s_toffs;
+    int half;
+};
+
+// Epilogue role (kEpiWarps warps, named barrier 1): for each tile id from the
+// ring, wait for its accumulator, apply the activation (gate/up) and store bf16
+// rows, release the accumulator, and publish the m-tile's completion.
+template <bool PAIR, int kBM>
+__device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c, int warp, int lane) {
+    auto ring_full = [&](int i) { return c.ring_full0 + 8u * i; };
+    auto ring_empty = [&](int i) { return c.ring_empty0 + 8u * i; };
+    auto tfull_bar = [&](uint32_t a) { return c.tfull0 + 8u * a; };
+    auto tempty_bar = [&](uint32_t a) { return c.tempty0 + 8u * a; };
+    volatile int *ring = c.ring;
+    volatile int *abort_flag = c.abort_flag;
+    const uint32_t tmem_base = c.tmem_base;
+    const int total = c.total, half = c.half;
+    const int *s_seg_end = c.s_seg_end, *s_offs = c.s_offs, *s_toffs = c.s_toffs;
+    unsigned long long *const stats = p.stats;
+    auto abort_all = [&]() {
+        if (PAIR)
+            raise_abort_pair(p.err, abort_flag);
+        else
+            raise_abort(p.err, abort_flag);
+    };
+    const int q = warp & 3;               // TMEM lane quadrant this warp may read
+    const int part = (warp - 2) / 4;      // which slice of the tile's columns
+    const bool lead_thread = q == 0 && part == 0 && lane == 0;
+    const int r = q * 32 + lane;
+    uint32_t n_acc = 0;
+    uint64_t w_tfull = 0, w_work = 0;
+    for (int n = 0;; ++n) {
+        const int slot = n % kRing;
+        const uint64_t t0 = stats ? global_timer_ns() : 0;
+        const bool have = __all_sync(0xffffffffu, mbar_wait(ring_full(slot), (n / kRing) & 1u, p.wait_ns, abort_flag));
+        const int tile = have ? ring[slot] : total;
+        // all four epilogue warps agree to go on or stop (they share barrier 1), and
+        // have read the id before it is released; the tcgen05.ld below is .sync.aligned
+        if (!epi_all(have)) {
+            if (lane == 0) abort_all();
+            break;
+        }
+        if (lead_thread) mbar_arrive(ring_empty(slot));
+        if (tile >= total) break;
+        const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
+        const GemmSegment &sg = p.seg[t.seg];
+        const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
+        const bool ready = __all_sync(0xffffffffu, PAIR ? mbar_wait_cluster(tfull_bar(a), aph, p.wait_ns, abort_flag)
+                                                        : mbar_wait(tfull_bar(a), aph, p.wait_ns, abort_flag));
+        const uint64_t t1 = stats ? global_timer_ns() : 0;
+        w_tfull += t1 - t0;
+        if (!epi_all(ready)) {
+            if (lane == 0) abort_all();
+            break;
+        }
+        tc_fence_after();
+        const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + a * kGemmBN;
+        const bool row_ok = r < t.m_valid;
+        bf16 *orow = sg.out + t.ks * sg.split_stride + (size_t)(t.row0 + (row_ok ? r : 0)) * sg.ldo;
+        if (sg.glu) {
+            constexpr int kSpan = 128 / kEpiParts;  // output columns per slice
+#pragma unroll 1
+            for (int c0 = part * kSpan; c0 < (part + 1) * kSpan; c0 += 32) {
+                uint32_t g[32], u[32];
+                tmem_ld32(tb + c0, g);
+                tmem_ld32(tb + 128 + c0, u);
+                tmem_ld_wait();
+                const int col = t.nt * 128 + c0;
+                if (row_ok && col < sg.n_out) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = pack_bf16x2(
+                            glu_act(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), p.act,
+                                    p.alpha, p.limit, p.beta),
+                            glu_act(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]),
+                                    p.act, p.alpha, p.limit, p.beta));
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                }
+            }
+        } else {
+            constexpr int kSpan = kGemmBN / kEpiParts;
+#pragma unroll 1
+            for (int c0 = part * kSpan; c0 < (part + 1) * kSpan; c0 += 32) {
+                uint32_t v32[32];
+                tmem_ld32(tb + c0, v32);
+                tmem_ld_wait();
+                const int col = t.nt * kGemmBN + c0;
+                if (row_ok && col < sg.n_out) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = pack_bf16x2(__uint_as_float(v32[2 * i]), __uint_as_float(v32[2 * i + 1]));
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                }
+            }
+        }
+        tc_fence_before();
+        if (PAIR)  // rank 0's barrier counts both CTAs' epilogue threads
+            mbar_arrive_cluster(mapa_shared(tempty_bar(a), 0));
+        else
+            mbar_arrive(tempty_bar(a));
+        if (sg.signal != nullptr) {
+            // publish the stored rows: proxy fence for the consumer's TMA reads,
+            // device-scope fence, all four warps done, then one release increment
+            fence_proxy_async();
+            __threadfence();
+            epi_bar();
+            if (lead_thread) atomicAdd(sg.signal + t.ready, 1);
+        }
+        if (stats) w_work += global_timer_ns() - t1;
+        ++n_acc;
+    }
+    if (stats && lead_thread) {
+        atomicAdd(stats + 4, (unsigned long long)w_tfull);
+        atomicAdd(stats + 5, (unsigned long long)w_work);
+    }
+}
 
 template <bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmArgs p) {
@@ -464,104 +600,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
     } else {
         // ----------------------------------------------------------- epilogue
-        const int q = warp & 3;               // TMEM lane quadrant this warp may read
-        const int part = (warp - 2) / 4;      // which slice of the tile's columns
-        const bool lead_thread = q == 0 && part == 0 && lane == 0;
-        const int r = q * 32 + lane;
-        uint32_t n_acc = 0;
-        uint64_t w_tfull = 0, w_work = 0;
-        for (int n = 0;; ++n) {
-            const int slot = n % kRing;
-            const uint64_t t0 = stats ? global_timer_ns() : 0;
-            const bool have = __all_sync(0xffffffffu, mbar_wait(ring_full(slot), (n / kRing) & 1u, p.wait_ns, abort_flag));
-            const int tile = have ? ring[slot] : total;
-            // all four epilogue warps agree to go on or stop (they share barrier 1), and
-            // have read the id before it is released; the tcgen05.ld below is .sync.aligned
-            if (!epi_all(have)) {
-                if (lane == 0) abort_all();
-                break;
-            }
-            if (lead_thread) mbar_arrive(ring_empty(slot));
-            if (tile >= total) break;
-            const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
-            const GemmSegment &sg = p.seg[t.seg];
-            const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
-            const bool ready = __all_sync(0xffffffffu, PAIR ? mbar_wait_cluster(tfull_bar(a), aph, p.wait_ns, abort_flag)
-                                                            : mbar_wait(tfull_bar(a), aph, p.wait_ns, abort_flag));
-            const uint64_t t1 = stats ? global_timer_ns() : 0;
-            w_tfull += t1 - t0;
-            if (!epi_all(ready)) {
-                if (lane == 0) abort_all();
-                break;
-            }
-            tc_fence_after();
-            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + a * kGemmBN;
-            const bool row_ok = r < t.m_valid;
-            bf16 *orow = sg.out + t.ks * sg.split_stride + (size_t)(t.row0 + (row_ok ? r : 0)) * sg.ldo;
-            if (sg.glu) {
-                constexpr int kSpan = 128 / kEpiParts;  // output columns per slice
-#pragma unroll 1
-                for (int c0 = part * kSpan; c0 < (part + 1) * kSpan; c0 += 32) {
-                    uint32_t g[32], u[32];
-                    tmem_ld32(tb + c0, g);
-                    tmem_ld32(tb + 128 + c0, u);
-                    tmem_ld_wait();
-                    const int col = t.nt * 128 + c0;
-                    if (row_ok && col < sg.n_out) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pk[i] = pack_bf16x2(
-                                glu_act(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), p.act,
-                                        p.alpha, p.limit, p.beta),
-                                glu_act(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]),
-                                        p.act, p.alpha, p.limit, p.beta));
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-                    }
-                }
-            } else {
-                constexpr int kSpan = kGemmBN / kEpiParts;
-#pragma unroll 1
-                for (int c0 = part * kSpan; c0 < (part + 1) * kSpan; c0 += 32) {
-                    uint32_t v32[32];
-                    tmem_ld32(tb + c0, v32);
-                    tmem_ld_wait();
-                    const int col = t.nt * kGemmBN + c0;
-                    if (row_ok && col < sg.n_out) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pk[i] = pack_bf16x2(__uint_as_float(v32[2 * i]), __uint_as_float(v32[2 * i + 1]));
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-                    }
-                }
-            }
-            tc_fence_before();
-            if (PAIR)  // rank 0's barrier counts both CTAs' epilogue threads
-                mbar_arrive_cluster(mapa_shared(tempty_bar(a), 0));
-            else
-                mbar_arrive(tempty_bar(a));
-            if (sg.signal != nullptr) {
-                // publish the stored rows: proxy fence for the consumer's TMA reads,
-                // device-scope fence, all four warps done, then one release increment
-                fence_proxy_async();
-                __threadfence();
-                epi_bar();
-                if (lead_thread) atomicAdd(sg.signal + t.ready, 1);
-            }
-            if (stats) w_work += global_timer_ns() - t1;
-            ++n_acc;
-        }
-        if (stats && lead_thread) {
-            atomicAdd(stats + 4, (unsigned long long)w_tfull);
-            atomicAdd(stats + 5, (unsigned long long)w_work);
-        }
+        EpiCtx c{ring_full(0), ring_empty(0), tfull_bar(0), tempty_bar(0), ring, abort_flag, tmem_base, total,
+                 s_seg_end, s_offs, s_toffs, half};
+        epilogue_role<PAIR, kBM>(p, c, warp, lane);
     }
 
     tc_fence_before();
@@ -576,6 +617,431 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             tmem_dealloc_pair(tmem_base, kTmemCols);
         else
             tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------------
+// Expert GEMM on block-scaled (OCP microscaling) weights.
+//
+// The weights are stored as MX element codes with one E8M0 scale per 32
+// consecutive K values of a row (the checkpoint formats the Arcee AFMoE issue
+// lists: "Checkpoint confirmed", 4-bit and MXFP8 variants).  A weight is
+// code_value * 2^(scale - 127).  The activations stay bf16, so the block still
+// multiplies bf16 tokens by the exact decoded weights: every decoded value is a
+// bf16 number (3 or 1 mantissa bits times a power of two), the MMA is the same
+// bf16 tcgen05 MMA as above, and only the weight bytes streamed from HBM shrink
+// (1 byte per weight for E4M3, half a byte for E2M1, plus 1/32 byte of scale).
+//
+// One CTA per SM, 11 warps:
+//   warp 0     TMA producer of the weight codes and scales (the HBM stream): a
+//              raw ring of kRawStages k-blocks, 256 rows x 64 codes + 2 x 256 scales
+//   warp 1     tcgen05.mma issue (as above), operands from the operand ring
+//   warps 2-5  epilogue (as above)
+//   warp 6     TMA producer of the A rows (bf16, 128-byte swizzle) into the operand ring
+//   warps 7-10 converters: decode a raw k-block into the operand ring's bf16 B tile,
+//              written in the 128-byte-swizzled K-major layout the MMA descriptor reads
+// The raw ring runs up to kRawStages k-blocks ahead of the MMA, so the weight
+// stream keeps that many bytes in flight while the operand ring (2 stages) is
+// being converted and consumed.
+template <int WF>
+struct MxCfg {
+    static constexpr int kRawRow = WF == kWeightsMxfp8 ? kGemmBK : kGemmBK / 2;  // bytes of a row's k-block
+    static constexpr int kRawCodes = kGemmBN * kRawRow;                         // 16 KB / 8 KB
+    static constexpr int kScaleBytes = 2 * 2 * 128;  // [row half][32-value block][128 rows]
+    static constexpr int kRawStage = kRawCodes + kScaleBytes;
+    static constexpr int kRawStages = WF == kWeightsMxfp8 ? 7 : 12;
+    static constexpr int kOpStages = 2;
+    static constexpr int kBBytes = kGemmBN * kGemmBK * 2;  // converted B tile, 32 KB
+    static constexpr int kOpStage = kABytes + kBBytes;
+    static constexpr int kBarBytes = 1024;
+    static constexpr int kSmemBytes = kOpStages * kOpStage + kRawStages * kRawStage + 1024 /*align*/ + kBarBytes;
+    static constexpr int kConvWarps = 4;
+    static constexpr int kThreads = 32 * (7 + kConvWarps);  // warps 0-6 as listed, then the converters
+    static_assert(kRawStage % 128 == 0, "raw stages stay 128-byte aligned");
+};
+
+// 2^(code - 127) for an E8M0 scale code (255 is NaN; 0 is 2^-127, an fp32 subnormal).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t code) {
+    if (code == 0u) return __uint_as_float(0x00400000u);
+    if (code == 255u) return __uint_as_float(0x7fc00000u);
+    return __uint_as_float(code << 23);
+}
+
+// Two E4M3 codes (low byte = lower K index) -> bf16x2 of code * scale.  The
+// hardware conversion to f16 is exact (every E4M3 value is a normal f16 or
+// zero); the product by a power of two is exact in fp32 and in bf16 unless it
+// leaves bf16's range, where it rounds to nearest.
+__device__ __forceinline__ uint32_t e4m3x2_scaled(uint32_t pair16, float scale) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)pair16));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    return pack_bf16x2(f.x * scale, f.y * scale);
+}
+
+// Two E2M1 codes in one byte (low nibble = lower K index) -> bf16x2 of code * scale.
+__device__ __forceinline__ uint32_t e2m1x2_scaled(uint32_t byte, float scale) {
+    uint32_t h;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h) : "r"(byte));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    return pack_bf16x2(f.x * scale, f.y * scale);
+}
+
+// Converter warp cw (0..3): rows [64 cw, 64 cw + 64) of one raw k-block -> bf16 B
+// tile.  Row r's 16-byte chunk j (K values 8j..8j+7) goes to r * 128 + ((j ^ (r % 8))
+// * 16): the 128-byte swizzle of a 1024-byte-aligned tile.  Lanes read consecutive
+// 16-byte pieces of the raw rows and store chunks of 8 distinct swizzle positions
+// per quarter-warp, so neither side has bank conflicts.
+template <int WF>
+__device__ __forceinline__ void mx_convert(const uint8_t *raw, const uint8_t *sc, uint8_t *out, int cw, int lane) {
+    using M = MxCfg<WF>;
+    if (WF == kWeightsMxfp8) {
+#pragma unroll 2
+        for (int it = 0; it < 8; ++it) {
+            const int row = cw * 64 + it * 8 + (lane >> 2), c = lane & 3;  // 16 codes: K 16c..16c+15
+            const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * M::kRawRow + c * 16);
+            const float f = e8m0_to_f32(sc[(row >> 7) * 256 + (c >> 1) * 128 + (row & 127)]);
+            const uint4 o0 = make_uint4(e4m3x2_scaled(v.x, f), e4m3x2_scaled(v.x >> 16, f),
+                                        e4m3x2_scaled(v.y, f), e4m3x2_scaled(v.y >> 16, f));
+            const uint4 o1 = make_uint4(e4m3x2_scaled(v.z, f), e4m3x2_scaled(v.z >> 16, f),
+                                        e4m3x2_scaled(v.w, f), e4m3x2_scaled(v.w >> 16, f));
+            uint8_t *rp = out + row * 128;
+            *reinterpret_cast<uint4 *>(rp + (((2 * c) ^ (row & 7)) << 4)) = o0;
+            *reinterpret_cast<uint4 *>(rp + (((2 * c + 1) ^ (row & 7)) << 4)) = o1;
+        }
+    } else {
+#pragma unroll 2
+        for (int it = 0; it < 4; ++it) {
+            const int row = cw * 64 + it * 16 + (lane >> 1), c = lane & 1;  // 32 codes: K 32c..32c+31
+            const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * M::kRawRow + c * 16);
+            const float f = e8m0_to_f32(sc[(row >> 7) * 256 + c * 128 + (row & 127)]);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint8_t *rp = out + row * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {  // chunk 4c + q: K 32c + 8q .. + 7 = the four bytes of w[q]
+                const uint4 o = make_uint4(e2m1x2_scaled(w[q] & 0xffu, f), e2m1x2_scaled((w[q] >> 8) & 0xffu, f),
+                                           e2m1x2_scaled((w[q] >> 16) & 0xffu, f), e2m1x2_scaled(w[q] >> 24, f));
+                *reinterpret_cast<uint4 *>(rp + (((4 * c + q) ^ (row & 7)) << 4)) = o;
+            }
+        }
+    }
+}
+
+template <int WF>
+__global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const __grid_constant__ GemmArgs p) {
+    using M = MxCfg<WF>;
+    constexpr int R = M::kRawStages, P = M::kOpStages, NCW = M::kConvWarps;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    // operand stages (A 16 KB, B 32 KB; 1024-byte aligned), then the raw stages, then the barriers
+    auto opA = [&](int s) { return smem + s * M::kOpStage; };
+    auto opB = [&](int s) { return smem + s * M::kOpStage + kABytes; };
+    uint8_t *const raw0 = smem + P * M::kOpStage;
+    auto rawS = [&](int s) { return raw0 + s * M::kRawStage; };
+    uint64_t *bars = reinterpret_cast<uint64_t *>(raw0 + R * M::kRawStage);
+    const uint32_t bar0 = smem_u32(bars);
+    // barriers: ring_full[kRing], ring_empty[kRing], tfull[2], tempty[2] (the epilogue's
+    // contiguous block), then raw_full[R], raw_empty[R], a_full[P], op_full[P], op_empty[P], drain
+    auto ring_full = [&](int i) { return bar0 + 8u * i; };
+    auto ring_empty = [&](int i) { return bar0 + 8u * (kRing + i); };
+    auto tfull_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kRing + a); };
+    auto tempty_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kRing + 2 + a); };
+    auto raw_full = [&](int s) { return bar0 + 8u * (2 * kRing + 4 + s); };
+    auto raw_empty = [&](int s) { return bar0 + 8u * (2 * kRing + 4 + R + s); };
+    auto a_full = [&](int s) { return bar0 + 8u * (2 * kRing + 4 + 2 * R + s); };
+    auto op_full = [&](int s) { return bar0 + 8u * (2 * kRing + 4 + 2 * R + P + s); };
+    auto op_empty = [&](int s) { return bar0 + 8u * (2 * kRing + 4 + 2 * R + 2 * P + s); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kRing + 4 + 2 * R + 3 * P);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kRing + 5 + 2 * R + 3 * P);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *ring = reinterpret_cast<volatile int *>(tmem_slot + 2);  // [kRing] tile ids
+    static_assert(8 * (2 * kRing + 5 + 2 * R + 3 * P) + 8 + 4 * kRing <= M::kBarBytes, "barrier block");
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto abort_all = [&]() { raise_abort(p.err, abort_flag); };
+    trace_mark(p.trace, 0);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(ring_full(i), 1);
+            mbar_init(ring_empty(i), 3 + NCW);  // MMA, epilogue, A producer, each converter warp
+        }
+        for (uint32_t a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), kEpiThreads);
+        }
+        for (int s = 0; s < R; ++s) {
+            mbar_init(raw_full(s), 1);
+            mbar_init(raw_empty(s), NCW);
+        }
+        for (int s = 0; s < P; ++s) {
+            mbar_init(a_full(s), 1);     // the A copy
+            mbar_init(op_full(s), NCW);  // each converter warp
+            mbar_init(op_empty(s), 1);
+        }
+        mbar_init(drain_bar, 1);
+        fence_mbar_init();
+        *abort_flag = 0;
+    }
+    if (warp == 0 && lane == 0)
+        for (int m = 0; m < kGemmMaxMaps; ++m) tma_prefetch_desc(&p.maps[m]);
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_wait();
+    trace_mark(p.trace, 1);
+    pdl_trigger();
+    unsigned long long *const stats = p.stats;
+    const uint64_t t_ready = stats ? global_timer_ns() : 0;
+    __shared__ int s_offs[257], s_toffs[257];
+    __shared__ int s_seg_end[kGemmMaxSegments];
+    int grouped = -1;
+    for (int s = 0; s < p.num_segs; ++s)
+        if (!p.seg[s].dense) grouped = s;
+    if (grouped >= 0)
+        for (int i = threadIdx.x; i <= p.seg[grouped].num_groups; i += blockDim.x) {
+            s_offs[i] = p.seg[grouped].offs[i];
+            s_toffs[i] = p.seg[grouped].tile_offs[i];
+        }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int s = 0; s < p.num_segs; ++s) {
+            run += seg_tiles<kGemmBM>(p.seg[s], s_toffs);
+            s_seg_end[s] = run;
+        }
+    }
+    __syncthreads();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = s_seg_end[p.num_segs - 1];
+
+    if (warp == 0) {
+        // ------------------------------------------- weight codes and scales
+        if (lane == 0) {
+            uint32_t L = 0;
+            bool ok = true;
+            uint64_t w_empty = 0;
+            const bool dyn = p.tile_counter != nullptr;
+            int next = dyn ? atomicAdd(p.tile_counter, 1) : (int)blockIdx.x;
+            for (int n = 0;; ++n) {
+                const int tile = next < total ? next : total;
+                const int slot = n % kRing;
+                if (!mbar_wait(ring_empty(slot), ((n / kRing) & 1u) ^ 1u, p.wait_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ring[slot] = tile;
+                mbar_arrive(ring_full(slot));
+                if (tile >= total) break;
+                const Tile t = decode_tile<kGemmBM>(p, tile, s_seg_end, s_offs, s_toffs, 0);
+                const GemmSegment &sg = p.seg[t.seg];
+                const int g = sg.group_base + t.group;
+                const int claim_at = sg.k_blocks > 3 ? sg.k_blocks - 3 : 0;
+                // rows of the tile's two 128-row halves: gate and up rows of n-tile nt, or
+                // the 256 rows of a down tile
+                const int r0 = sg.glu ? t.nt * 128 : t.nt * kGemmBN, r1 = sg.glu ? r0 : r0 + 128;
+                const CUtensorMap *mC0 = &p.maps[sg.map_b0], *mC1 = &p.maps[sg.glu ? sg.map_b1 : sg.map_b0];
+                const CUtensorMap *mS0 = &p.maps[sg.map_s0], *mS1 = &p.maps[sg.glu ? sg.map_s1 : sg.map_s0];
+                for (int kb = 0; kb < sg.k_blocks; ++kb) {
+                    const int s = L % R;
+                    const uint32_t ph = (L / R) & 1u;
+                    if (kb == claim_at) next = dyn ? atomicAdd(p.tile_counter, 1) : tile + (int)gridDim.x;
+                    const uint64_t t0 = stats ? global_timer_ns() : 0;
+                    if (!mbar_wait(raw_empty(s), ph ^ 1u, p.wait_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (stats) w_empty += global_timer_ns() - t0;
+                    const int kx = (sg.k_base + t.ks * sg.k_blocks + kb) * kGemmBK;  // first K value
+                    const int xb = WF == kWeightsMxfp8 ? kx : kx / 2;                // its byte in a code row
+                    const uint32_t dst = smem_u32(rawS(s));
+                    mbar_arrive_expect_tx(raw_full(s), M::kRawStage);
+                    tma_load_3d(dst, mC0, raw_full(s), xb, r0, g);
+                    tma_load_3d(dst + 128 * M::kRawRow, mC1, raw_full(s), xb, r1, g);
+                    tma_load_3d(dst + M::kRawCodes, mS0, raw_full(s), r0, kx / 32, g);
+                    tma_load_3d(dst + M::kRawCodes + 256, mS1, raw_full(s), r1, kx / 32, g);
+                    ++L;
+                }
+                if (!ok) break;
+            }
+            if (stats) atomicAdd(stats + 0, (unsigned long long)w_empty);
+            if (!ok) {
+                abort_all();
+                for (uint32_t i = 0; i < (uint32_t)R && i < L; ++i) {  // copies still in flight
+                    const uint32_t l = L - 1 - i;
+                    mbar_wait(raw_full(l % R), (l / R) & 1u, kDrainNs, nullptr);
+                }
+            }
+        }
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ A rows
+        if (lane == 0) {
+            uint32_t L = 0;
+            bool ok = true;
+            uint64_t w_dep = 0;
+            for (int n = 0;; ++n) {
+                const int slot = n % kRing;
+                if (!mbar_wait(ring_full(slot), (n / kRing) & 1u, p.wait_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int tile = ring[slot];
+                mbar_arrive(ring_empty(slot));
+                if (tile >= total) break;
+                const Tile t = decode_tile<kGemmBM>(p, tile, s_seg_end, s_offs, s_toffs, 0);
+                const GemmSegment &sg = p.seg[t.seg];
+                if (sg.wait != nullptr) {  // A rows written earlier in this launch
+                    const uint64_t t0 = stats ? global_timer_ns() : 0;
+                    if (!wait_counter(sg.wait + t.ready, sg.wait_count, p.wait_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (stats) w_dep += global_timer_ns() - t0;
+                    fence_proxy_async();
+                }
+                const CUtensorMap *mA = &p.maps[sg.map_a];
+                for (int kb = 0; kb < sg.k_blocks; ++kb) {
+                    const int s = L % P;
+                    const uint32_t ph = (L / P) & 1u;
+                    if (!mbar_wait(op_empty(s), ph ^ 1u, p.wait_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const int kx = (sg.k_base + t.ks * sg.k_blocks + kb) * kGemmBK;
+                    mbar_arrive_expect_tx(a_full(s), kABytes);
+                    tma_load_2d(smem_u32(opA(s)), mA, a_full(s), kx, t.row0);
+                    ++L;
+                }
+                if (!ok) break;
+            }
+            if (stats) atomicAdd(stats + 1, (unsigned long long)w_dep);
+            if (!ok) {
+                abort_all();
+                for (uint32_t i = 0; i < (uint32_t)P && i < L; ++i) {  // copies still in flight
+                    const uint32_t l = L - 1 - i;
+                    mbar_wait(a_full(l % P), (l / P) & 1u, kDrainNs, nullptr);
+                }
+            }
+        }
+    } else if (warp >= 7) {
+        // -------------------------------------------------------- converters
+        const int cw = warp - 7;
+        uint32_t L = 0;
+        bool ok = true;
+        for (int n = 0; ok; ++n) {
+            const int slot = n % kRing;
+            const bool have = __all_sync(0xffffffffu, mbar_wait(ring_full(slot), (n / kRing) & 1u, p.wait_ns, abort_flag));
+            if (!have) {
+                if (lane == 0) abort_all();
+                break;
+            }
+            const int tile = ring[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ring_empty(slot));
+            if (tile >= total) break;
+            const Tile t = decode_tile<kGemmBM>(p, tile, s_seg_end, s_offs, s_toffs, 0);
+            const int kbs = p.seg[t.seg].k_blocks;
+            for (int kb = 0; kb < kbs; ++kb) {
+                const int rs = L % R, os = L % P;
+                const bool got = __all_sync(0xffffffffu, mbar_wait(raw_full(rs), (L / R) & 1u, p.wait_ns, abort_flag) &&
+                                                             mbar_wait(op_empty(os), ((L / P) & 1u) ^ 1u, p.wait_ns, abort_flag));
+                if (!got) {
+                    if (lane == 0) abort_all();
+                    ok = false;
+                    break;
+                }
+                mx_convert<WF>(rawS(rs), rawS(rs) + M::kRawCodes, opB(os), cw, lane);
+                fence_proxy_async();  // the generic-proxy stores, before the MMA (async proxy) reads them
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(raw_empty(rs));
+                    mbar_arrive(op_full(os));
+                }
+                ++L;
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kGemmBM, kGemmBN);
+            uint32_t L = 0, n_acc = 0;
+            bool ok = true, issued = false;
+            uint64_t w_full = 0, w_acc = 0;
+            for (int n = 0; ok; ++n) {
+                const int slot = n % kRing;
+                if (!mbar_wait(ring_full(slot), (n / kRing) & 1u, p.wait_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int tile = ring[slot];
+                mbar_arrive(ring_empty(slot));
+                if (tile >= total) break;
+                const Tile t = decode_tile<kGemmBM>(p, tile, s_seg_end, s_offs, s_toffs, 0);
+                const GemmSegment &sg = p.seg[t.seg];
+                const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
+                const uint64_t t0 = stats ? global_timer_ns() : 0;
+                if (!mbar_wait(tempty_bar(a), aph ^ 1u, p.wait_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (stats) w_acc += global_timer_ns() - t0;
+                tc_fence_after();
+                const uint32_t d = tmem_base + a * kGemmBN;
+                for (int kb = 0; kb < sg.k_blocks; ++kb) {
+                    const int s = L % P;
+                    const uint32_t ph = (L / P) & 1u;
+                    const uint64_t t1 = stats ? global_timer_ns() : 0;
+                    if (!mbar_wait(a_full(s), ph, p.wait_ns, abort_flag) ||
+                        !mbar_wait(op_full(s), ph, p.wait_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (stats) w_full += global_timer_ns() - t1;
+                    tc_fence_after();
+                    const uint64_t ad = smem_desc_k128(smem_u32(opA(s)));
+                    const uint64_t bd = smem_desc_k128(smem_u32(opB(s)));
+#pragma unroll
+                    for (int kk = 0; kk < kGemmBK / 16; ++kk)
+                        tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    issued = true;
+                    tc_commit(op_empty(s));
+                    ++L;
+                }
+                if (!ok) break;
+                tc_commit(tfull_bar(a));
+                ++n_acc;
+            }
+            if (stats) {
+                atomicAdd(stats + 2, (unsigned long long)w_full);
+                atomicAdd(stats + 3, (unsigned long long)w_acc);
+                atomicAdd(stats + 7, (unsigned long long)n_acc);
+            }
+            if (!ok) {
+                abort_all();
+                if (issued) {
+                    tc_commit(drain_bar);
+                    mbar_wait(drain_bar, 0, kDrainNs, nullptr);
+                }
+            }
+        }
+    } else {
+        // ----------------------------------------------------------- epilogue
+        EpiCtx c{ring_full(0), ring_empty(0), tfull_bar(0), tempty_bar(0), ring, abort_flag, tmem_base, total,
+                 s_seg_end, s_offs, s_toffs, 0};
+        epilogue_role<false, kGemmBM>(p, c, warp, lane);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    trace_exit(p.trace);
+    if (stats && threadIdx.x == 0) atomicAdd(stats + 6, (unsigned long long)(global_timer_ns() - t_ready));
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -657,6 +1123,31 @@ CUresult encode_map_b_kb2(CUtensorMap *m, const void *ptr, int groups, int rows,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+CUresult encode_map_mx_codes(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int wfmt) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+    const int row_bytes = wfmt == kWeightsMxfp8 ? K : K / 2;
+    const cuuint64_t dims[3] = {(cuuint64_t)row_bytes, (cuuint64_t)rows, (cuuint64_t)groups};
+    const cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows * row_bytes};
+    const cuuint32_t box[3] = {(cuuint32_t)(wfmt == kWeightsMxfp8 ? kGemmBK : kGemmBK / 2), 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult encode_map_mx_scales(CUtensorMap *m, const void *ptr, int groups, int rows, int K) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t dims[3] = {(cuuint64_t)rows, (cuuint64_t)(K / 32), (cuuint64_t)groups};
+    const cuuint64_t strides[2] = {(cuuint64_t)rows, (cuuint64_t)rows * (K / 32)};
+    const cuuint32_t box[3] = {128, 2, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
     static std::once_flag once;
     std::call_once(once, [] {
@@ -664,7 +1155,20 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
                              GemmCfg<false>::kSmemBytes);
         cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              GemmCfg<true>::kSmemBytes);
+        cudaFuncSetAttribute(gemm_mx_kernel<kWeightsMxfp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             MxCfg<kWeightsMxfp8>::kSmemBytes);
+        cudaFuncSetAttribute(gemm_mx_kernel<kWeightsMxfp4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             MxCfg<kWeightsMxfp4>::kSmemBytes);
     });
+    if (a.wfmt == kWeightsMxfp8 || a.wfmt == kWeightsMxfp4) {
+        if (a.pair) return cudaErrorInvalidValue;  // MX weights run on single CTAs
+        if (a.wfmt == kWeightsMxfp8)
+            return launch_pdl(gemm_mx_kernel<kWeightsMxfp8>, dim3(a.num_ctas), dim3(MxCfg<kWeightsMxfp8>::kThreads),
+                              (size_t)MxCfg<kWeightsMxfp8>::kSmemBytes, s, a);
+        return launch_pdl(gemm_mx_kernel<kWeightsMxfp4>, dim3(a.num_ctas), dim3(MxCfg<kWeightsMxfp4>::kThreads),
+                          (size_t)MxCfg<kWeightsMxfp4>::kSmemBytes, s, a);
+    }
+    if (a.wfmt != kWeightsBf16) return cudaErrorInvalidValue;
     if (a.pair) {
         if (a.num_ctas < 2 || (a.num_ctas & 1) || a.tile_counter != nullptr) return cudaErrorInvalidValue;
         return launch_pdl_cluster(gemm_tc_kernel<true>, dim3(a.num_ctas), dim3(kThreads),

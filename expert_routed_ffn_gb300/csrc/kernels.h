@@ -214,7 +214,11 @@ constexpr int kGemmBK = 64;    // K per pipeline stage (one 128-byte swizzle row
 constexpr int kGemmBN = 256;   // MMA N; gate/up tiles hold 128 gate + 128 up columns
 
 constexpr int kGemmMaxSegments = 5;
-constexpr int kGemmMaxMaps = 10;
+constexpr int kGemmMaxMaps = 16;
+
+// Storage of the expert weights (the B operand): bf16, or OCP microscaling
+// (MX) codes with one E8M0 scale per 32 consecutive K values.
+enum WeightFormat { kWeightsBf16 = 0, kWeightsMxfp8 = 1, kWeightsMxfp4 = 2 };
 struct GemmSegment {
     int dense;             // 1: one group of m_dense rows from row 0; 0: groups by offs
     int num_groups;
@@ -242,6 +246,8 @@ struct GemmSegment {
     // product at out + j * split_stride
     int k_splits;
     size_t split_stride;
+    // MX weights: maps of the E8M0 scales of b0 and b1 ([groups, K / 32, rows] uint8)
+    int map_s0, map_s1;
 };
 
 struct GemmArgs {
@@ -262,6 +268,7 @@ struct GemmArgs {
     // waiting for an accumulator, epilogue waiting for an accumulator,
     // epilogue working, CTA time past the dependency wait, tiles
     unsigned long long *stats;
+    int wfmt;              // WeightFormat of every segment's B maps; MX only without CTA pairs
 };
 constexpr int kGemmStats = 8;
 cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s);
@@ -299,6 +306,12 @@ CUresult encode_map_a_kb2(CUtensorMap *m, const void *ptr, int rows, int K);
 CUresult encode_map_b_kb2(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int box_rows);
 CUresult encode_map_a_box(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows);
 CUresult encode_map_b(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int box_rows);
+// MX weights: element codes [groups, rows, K] (E4M3, one byte each) or [groups,
+// rows, K / 2] (E2M1, two per byte, element 2j in the low nibble), box of one
+// 64-element k-block x 128 rows; E8M0 scales [groups, K / 32, rows], box 128
+// rows x 2 (the k-block's two scale blocks).  No swizzle.
+CUresult encode_map_mx_codes(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int wfmt);
+CUresult encode_map_mx_scales(CUtensorMap *m, const void *ptr, int groups, int rows, int K);
 
 // ------------------------------------------------- decode streamers (K6)
 // CUDA-core kernels for few tokens per expert: each CTA streams a block of

@@ -124,6 +124,9 @@ struct moe_handle {
     // CTA-pair expert GEMM: the same tensors with K viewed as (64, K / 64), two
     // k-blocks per box (A: 128 rows; weights: 128 rows)
     CUtensorMap m_xs2, m_hb2, m_hs2, m_xbf2, m_gate2, m_up2, m_down2, m_shg2, m_shu2, m_shd2, m_x2;
+    // MX weights: m_gate ... m_shd map the element codes; these map their E8M0 scales
+    int wfmt = 0;  // moe_weight_format
+    CUtensorMap m_gate_s, m_up_s, m_down_s, m_shg_s, m_shu_s, m_shd_s;
     const void *m_x2_ptr = nullptr;
     int m_x2_rows = 0;
     // descriptor of the caller's X for the shared-expert GEMM (cached by pointer and T)
@@ -153,6 +156,9 @@ moe_status validate_config(const moe_config *c, int *S_eff) {
         return fail(MOE_ERR_INVALID_ARG, "rms_norm_eps must be finite and >= 0");
     if (c->num_shared_experts < 0 || c->shared_intermediate_size < 0)
         return fail(MOE_ERR_INVALID_ARG, "negative shared expert count or width");
+    if (c->weight_format != MOE_WEIGHTS_BF16 && c->weight_format != MOE_WEIGHTS_MXFP8 &&
+        c->weight_format != MOE_WEIGHTS_MXFP4)
+        return fail(MOE_ERR_INVALID_ARG, "weight_format %d", c->weight_format);
     if (c->num_experts == 0) {
         // a dense MLP layer: no router, the shared tensors are its gate/up/down
         if (c->num_experts_per_tok != 0 || c->shared_packed)
@@ -305,16 +311,25 @@ moe_status build_maps(moe_handle *h) {
     MAP(moe::encode_map_a(&h->m_hbuf, h->hbuf, MT * k, I));
     MAP(moe::encode_map_a_kb2(&h->m_xs2, h->x_sorted, MT * k, H));
     MAP(moe::encode_map_a_kb2(&h->m_hb2, h->hbuf, MT * k, I));
+    MAP(moe::encode_map_b(&h->m_wr, h->wr_parts, h->rplan.parts, h->E, H, h->rplan.Np));
+    if (h->wfmt != MOE_WEIGHTS_BF16) {
+        MAP(moe::encode_map_mx_codes(&h->m_gate, h->w.gate, Ep, I, H, h->wfmt));
+        MAP(moe::encode_map_mx_codes(&h->m_up, h->w.up, Ep, I, H, h->wfmt));
+        MAP(moe::encode_map_mx_codes(&h->m_down, h->w.down, Ep, H, I, h->wfmt));
+        MAP(moe::encode_map_mx_scales(&h->m_gate_s, h->w.gate_scale, Ep, I, H));
+        MAP(moe::encode_map_mx_scales(&h->m_up_s, h->w.up_scale, Ep, I, H));
+        MAP(moe::encode_map_mx_scales(&h->m_down_s, h->w.down_scale, Ep, H, I));
+    } else {
     MAP(moe::encode_map_b_kb2(&h->m_gate2, h->w.gate, Ep, I, H, 128));
     MAP(moe::encode_map_b_kb2(&h->m_up2, h->w.up, Ep, I, H, 128));
     MAP(moe::encode_map_b_kb2(&h->m_down2, h->w.down, Ep, H, I, 128));
     MAP(moe::encode_map_b(&h->m_gate, h->w.gate, Ep, I, H, 128));
     MAP(moe::encode_map_b(&h->m_up, h->w.up, Ep, I, H, 128));
     MAP(moe::encode_map_b(&h->m_down, h->w.down, Ep, H, I, moe::kGemmBN));
-    MAP(moe::encode_map_b(&h->m_wr, h->wr_parts, h->rplan.parts, h->E, H, h->rplan.Np));
     MAP(moe::encode_map_b(&h->m_gate64, h->w.gate, Ep, I, H, 64));
     MAP(moe::encode_map_b(&h->m_up64, h->w.up, Ep, I, H, 64));
     MAP(moe::encode_map_b(&h->m_down128, h->w.down, Ep, H, I, 128));
+    }
     }
     for (int v = 0; v < 2; ++v) {
         const int n = v ? 64 : 32;
@@ -334,12 +349,22 @@ moe_status build_maps(moe_handle *h) {
             h->m_shg = h->m_gate;
             h->m_shu = h->m_up;
             h->m_shd = h->m_down;
+            h->m_shg_s = h->m_gate_s;
+            h->m_shu_s = h->m_up_s;
+            h->m_shd_s = h->m_down_s;
             h->m_shg64 = h->m_gate64;
             h->m_shu64 = h->m_up64;
             h->m_shd128 = h->m_down128;
             h->m_shg2 = h->m_gate2;
             h->m_shu2 = h->m_up2;
             h->m_shd2 = h->m_down2;
+        } else if (h->wfmt != MOE_WEIGHTS_BF16) {
+            MAP(moe::encode_map_mx_codes(&h->m_shg, h->w.sh_gate, 1, S, H, h->wfmt));
+            MAP(moe::encode_map_mx_codes(&h->m_shu, h->w.sh_up, 1, S, H, h->wfmt));
+            MAP(moe::encode_map_mx_codes(&h->m_shd, h->w.sh_down, 1, H, S, h->wfmt));
+            MAP(moe::encode_map_mx_scales(&h->m_shg_s, h->w.sh_gate_scale, 1, S, H));
+            MAP(moe::encode_map_mx_scales(&h->m_shu_s, h->w.sh_up_scale, 1, S, H));
+            MAP(moe::encode_map_mx_scales(&h->m_shd_s, h->w.sh_down_scale, 1, H, S));
         } else {
             MAP(moe::encode_map_b(&h->m_shg, h->w.sh_gate, 1, S, H, 128));
             MAP(moe::encode_map_b(&h->m_shu, h->w.sh_up, 1, S, H, 128));
@@ -532,7 +557,9 @@ moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n
 // per m-tile for their gate/up rows) or in two launches.
 moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int *n) {
     const int H = h->H, I = h->I, S = h->S, E = h->E;
-    enum { kXs = 0, kX = 1, kHb = 2, kHs = 3, kG = 4, kU = 5, kSG = 6, kSU = 7, kD = 8, kSD = 9 };
+    enum { kXs = 0, kX = 1, kHb = 2, kHs = 3, kG = 4, kU = 5, kSG = 6, kSU = 7, kD = 8, kSD = 9,
+           kGs = 10, kUs = 11, kSGs = 12, kSUs = 13, kDs = 14, kSDs = 15 };
+    const bool mx = h->wfmt != MOE_WEIGHTS_BF16;
     moe::GemmArgs g{};
     g.err = h->err;
     g.wait_ns = h->wait_ns;
@@ -553,6 +580,11 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         g.maps[kG] = pair ? h->m_gate2 : h->m_gate;
         g.maps[kU] = pair ? h->m_up2 : h->m_up;
         g.maps[kD] = pair ? h->m_down2 : h->m_down;
+        if (mx) {
+            g.maps[kGs] = h->m_gate_s;
+            g.maps[kUs] = h->m_up_s;
+            g.maps[kDs] = h->m_down_s;
+        }
     }
     if (h->has_shared) {
         if (h->x_f32) {
@@ -574,17 +606,23 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         g.maps[kSG] = pair ? h->m_shg2 : h->m_shg;
         g.maps[kSU] = pair ? h->m_shu2 : h->m_shu;
         g.maps[kSD] = pair ? h->m_shd2 : h->m_shd;
+        if (mx) {
+            g.maps[kSGs] = h->m_shg_s;
+            g.maps[kSUs] = h->m_shu_s;
+            g.maps[kSDs] = h->m_shd_s;
+        }
     }
+    g.wfmt = h->wfmt;
     const int sh_base = h->cfg.shared_packed ? E : 0;
     const int nt_gu = (I + 127) / 128, nt_sgu = (S + 127) / 128, nt_d = (H + moe::kGemmBN - 1) / moe::kGemmBN;
     const bool fused = h->fuse_experts;
     int *sig = fused ? h->ready : nullptr;
     const moe::GemmSegment gu{0, E, 0, 0, h->offs, h->tile_offs, nt_gu, H / 64, 0, I, h->hbuf, I,
-                              1, kXs, kG, kU, sig, nullptr, 0, 0};
+                              1, kXs, kG, kU, sig, nullptr, 0, 0, 0, 0, kGs, kUs};
     const moe::GemmSegment sgu{1, 1, sh_base, T, nullptr, nullptr, nt_sgu, H / 64, 0, S, h->hs, S,
-                               1, kX, kSG, kSU, sig, nullptr, 0, h->ready_shared_base};
+                               1, kX, kSG, kSU, sig, nullptr, 0, h->ready_shared_base, 0, 0, kSGs, kSUs};
     const moe::GemmSegment dn{0, E, 0, 0, h->offs, h->tile_offs, nt_d, I / 64, 0, H, h->yslot, H,
-                              0, kHb, kD, kD, nullptr, fused ? h->ready : nullptr, nt_gu, 0};
+                              0, kHb, kD, kD, nullptr, fused ? h->ready : nullptr, nt_gu, 0, 0, 0, kDs, kDs};
     // At small T the shared down projection (K = S) is the longest tile chain: its K
     // runs as `parts` ranges into as many partial outputs, which the combine adds in
     // fixed order (for two concatenated shared experts of width I and two parts,
@@ -592,7 +630,8 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     const int parts = h->shared_parts;
     moe::GemmSegment sdn{1, 1, sh_base, T, nullptr, nullptr, nt_d, S / 64 / parts, 0, H,
                          parts > 1 ? h->ys_split : h->ys, H, 0, kHs, kSD, kSD, nullptr,
-                         fused ? h->ready : nullptr, nt_sgu, h->ready_shared_base, parts, (size_t)T * H};
+                         fused ? h->ready : nullptr, nt_sgu, h->ready_shared_base, parts, (size_t)T * H,
+                         kSDs, kSDs};
     if (fused) {
         int ns = 0;
         if (!h->dense) g.seg[ns++] = gu;
@@ -715,7 +754,7 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     if (path == kPathAuto)
         path = T <= kDecodeMaxTokens ? kPathDecode
                                      : (slots <= (long long)kSwapMaxTokensPerExpert * h->E ? kPathSwapped : kPathGrouped);
-    if (h->dense) path = kPathGrouped;  // a dense layer: the grouped GEMM's shared segments
+    if (h->dense || h->wfmt != MOE_WEIGHTS_BF16) path = kPathGrouped;  // dense layer, MX weights: grouped GEMMs
     const int n_tok = slots <= 24ll * h->E ? 32 : 64;  // token tile of the swapped GEMMs
     h->ev_recorded = 0;
     // Decode-sized batches touch nearly every expert (about two or more tokens
@@ -724,7 +763,9 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     const bool prefetch = h->prefetch_opt && !h->dense && path == kPathGrouped && h->fuse_experts &&
                           slots >= 2ll * h->E && h->side != nullptr;
     if (prefetch) {
-        const unsigned long long slice = (unsigned long long)h->I * h->H * 2;
+        // bytes of one expert's gate (or up) slice: bf16, or MX codes (1 or 1/2 byte per weight)
+        const unsigned long long slice = (unsigned long long)h->I * h->H *
+                                         (h->wfmt == MOE_WEIGHTS_BF16 ? 4 : h->wfmt == MOE_WEIGHTS_MXFP8 ? 2 : 1) / 2;
         const unsigned long long each = kPrefetchBytes / 2 / slice * slice, all = slice * h->E;
         moe::PrefetchArgs pa{{h->w.gate, h->w.up}, {each < all ? each : all, each < all ? each : all}};
         cudaError_t e = cudaEventRecord(h->ev_fork, s);
@@ -743,7 +784,7 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     }
     // CTA pairs once the weight tiles are reused by 256 rows on average (a dense
     // layer: T >= 256)
-    h->pair_now = path == kPathGrouped && h->num_sms >= 2 &&
+    h->pair_now = path == kPathGrouped && h->num_sms >= 2 && h->wfmt == MOE_WEIGHTS_BF16 &&
                   (h->pair_opt == 1 || (h->pair_opt == 2 && (h->dense ? T >= 256 : slots >= 256ll * h->E)));
     h->shared_parts = path == kPathGrouped && h->has_shared ? shared_parts(h, T) : 1;
     mark(h, 0, s);
@@ -818,6 +859,16 @@ moe_status moe_create(const moe_config *config, const moe_weights *weights, moe_
     const bool has_shared = S > 0;
     if (has_shared && !config->shared_packed && (!w.sh_gate || !w.sh_up || !w.sh_down))
         return fail(MOE_ERR_INVALID_ARG, "shared width %d needs sh_gate, sh_up and sh_down", S);
+    const bool mx = config->weight_format != MOE_WEIGHTS_BF16;
+    if (mx) {
+        if (!dense && (!w.gate_scale || !w.up_scale || !w.down_scale))
+            return fail(MOE_ERR_INVALID_ARG, "MX weights need gate_scale, up_scale and down_scale");
+        if (has_shared && !config->shared_packed && (!w.sh_gate_scale || !w.sh_up_scale || !w.sh_down_scale))
+            return fail(MOE_ERR_INVALID_ARG, "MX shared weights need sh_gate_scale, sh_up_scale and sh_down_scale");
+        const void *sp[] = {w.gate_scale, w.up_scale, w.down_scale, w.sh_gate_scale, w.sh_up_scale, w.sh_down_scale};
+        for (const void *p : sp)
+            if (p && !aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "scale pointer %p is not 16-byte aligned", p);
+    }
 
     moe_handle *h = new moe_handle();
     h->cfg = *config;
@@ -833,6 +884,7 @@ moe_status moe_create(const moe_config *config, const moe_weights *weights, moe_
     h->dense = dense;
     h->norm = config->mlp_norm;
     h->eps = config->rms_norm_eps;
+    h->wfmt = config->weight_format;
     if (config->shared_packed) {
         const size_t slice = (size_t)h->E * h->I * h->H;
         h->sh_gate = static_cast<const bf16 *>(w.gate) + slice;
@@ -1002,6 +1054,8 @@ moe_status moe_set_option(moe_handle *h, int option, long long value) {
     switch (option) {
     case MOE_OPT_PATH:
         if (value < kPathAuto || value > kPathSwapped) return fail(MOE_ERR_INVALID_ARG, "path %lld", value);
+        if (h->wfmt != MOE_WEIGHTS_BF16 && (value == kPathDecode || value == kPathSwapped))
+            return fail(MOE_ERR_UNSUPPORTED, "MX weights run on the grouped tensor-core path only");
         h->path_opt = (int)value;
         return MOE_OK;
     case MOE_OPT_WAIT_LIMIT_NS:

@@ -69,9 +69,25 @@ typedef enum { MOE_SCORE_SIGMOID = 0, MOE_SCORE_SOFTMAX = 1 } moe_score_func;
  * convention that bullet names). */
 typedef enum { MOE_ACT_SILU = 0, MOE_ACT_SWIGLU_OAI = 1 } moe_act;
 
-/* dtype of X and Y.  Expert weights are always bf16; router weights and the
- * expert bias are always fp32. */
+/* dtype of X and Y.  Router weights and the expert bias are always fp32; the
+ * expert weights are bf16 or block-scaled (moe_weight_format). */
 typedef enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 } moe_dtype;
+
+/* Storage of the expert weights (routed, shared and dense-layer gate/up/down).
+ * The Arcee AFMoE issue ("Checkpoint confirmed") lists 4-bit and MXFP8
+ * checkpoints; the MX variants follow the OCP Microscaling Formats v1.0: every
+ * 32 consecutive values along a row's input dimension K (H for gate/up, I or S
+ * for down) share one E8M0 scale byte c, and a weight is element(code) * 2^(c - 127)
+ * (c = 255 is NaN).  The activations stay bf16: the block multiplies bf16 tokens
+ * by the exactly decoded weights (each decoded value is a bf16 number as long as
+ * it lies in bf16's range; outside it rounds to nearest).
+ *   MXFP8: one E4M3 code per byte, [rows, K] per weight slice.
+ *   MXFP4: two E2M1 codes per byte, [rows, K / 2], element 2j in the low nibble.
+ *   Scales: uint8 [K / 32, rows] per weight slice (block-major: for each
+ *           32-value block, the scales of all rows).
+ * MX weights run on the grouped tensor-core path only (moe_set_option
+ * MOE_OPT_PATH 1 or 3 is refused, and MOE_OPT_GEMM_PAIR has no effect). */
+typedef enum { MOE_WEIGHTS_BF16 = 0, MOE_WEIGHTS_MXFP8 = 1, MOE_WEIGHTS_MXFP4 = 2 } moe_weight_format;
 
 /* Norms around the MLP (y = x / sqrt(mean(x^2) + eps) * g over the H values of a row). */
 typedef enum {
@@ -103,6 +119,7 @@ typedef struct {
                                      post_norm(mlp(pre_norm(X))) (Arcee AFMoE issue: four norms per
                                      layer; MiniMax-M3 issue: Gemma-style RMSNorm, weight + 1) */
     float rms_norm_eps;           /* eps of both norms (AfmoeConfig rms_norm_eps 1e-5) */
+    int weight_format;            /* moe_weight_format of the expert weights (0: bf16) */
 } moe_config;
 
 /* Device pointers to the block's weights.  BORROWED: they must stay valid and
@@ -118,6 +135,14 @@ typedef struct {
     const void *sh_down;      /* [H, S] bf16 */
     const float *pre_norm_w;  /* [H] fp32 (pre_mlp_layernorm.weight); required when mlp_norm != 0 */
     const float *post_norm_w; /* [H] fp32 (post_mlp_layernorm.weight); required when mlp_norm != 0 */
+    /* MX weight formats only (NULL otherwise): the E8M0 scales of the tensors
+     * above, uint8, block-major per slice (see moe_weight_format), each required
+     * exactly where its weight tensor is.  gate_scale, up_scale: [E', H/32, I];
+     * down_scale: [E', I/32, H]; sh_gate_scale, sh_up_scale: [H/32, S];
+     * sh_down_scale: [S/32, H].  The element tensors gate, up, down, sh_* then
+     * hold the codes: MXFP8 [.., rows, K] uint8, MXFP4 [.., rows, K/2] uint8. */
+    const uint8_t *gate_scale, *up_scale, *down_scale;
+    const uint8_t *sh_gate_scale, *sh_up_scale, *sh_down_scale;
 } moe_weights;
 
 typedef struct moe_handle moe_handle;
