@@ -178,6 +178,10 @@ __device__ __forceinline__ bool epi_all(bool v) {
 }
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async;" ::: "memory"); }
+// the same ordering for this thread's shared-memory stores only (operands the MMA reads)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 
 // Barrier addresses and shared state the epilogue warps use (every kernel lays
@@ -635,27 +639,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 // One CTA per SM, 11 warps:
 //   warp 0     TMA producer of the weight codes and scales (the HBM stream): a
 //              raw ring of kRawStages k-blocks, 256 rows x 64 codes + 2 x 256 scales
-//   warp 1     tcgen05.mma issue (as above), operands from the operand ring
+//   warp 1     tcgen05.mma issue (as above): A from the A ring, B from the B ring
 //   warps 2-5  epilogue (as above)
-//   warp 6     TMA producer of the A rows (bf16, 128-byte swizzle) into the operand ring
-//   warps 7-10 converters: decode a raw k-block into the operand ring's bf16 B tile,
-//              written in the 128-byte-swizzled K-major layout the MMA descriptor reads
-// The raw ring runs up to kRawStages k-blocks ahead of the MMA, so the weight
-// stream keeps that many bytes in flight while the operand ring (2 stages) is
-// being converted and consumed.
+//   warp 6     TMA producer of the A rows (bf16, 128-byte swizzle) into the A ring
+//   warps 7-   converters: decode a raw k-block into the B ring's bf16 tile, written
+//              in the 128-byte-swizzled K-major layout the MMA descriptor reads
+// Three rings: raw (kRawStages, freed by the converters), A (kAStages, freed by the
+// MMA) and converted B (kBStages, freed by the MMA), so the weight stream and the
+// A rows each run several k-blocks ahead of the MMA while B is being converted.
+// Every k-block moves about 130 KB through shared memory (codes in and out, the
+// bf16 B tile in and out, the A tile in and out), which bounds this design at
+// roughly one k-block per 1000 cycles.
 template <int WF>
 struct MxCfg {
     static constexpr int kRawRow = WF == kWeightsMxfp8 ? kGemmBK : kGemmBK / 2;  // bytes of a row's k-block
     static constexpr int kRawCodes = kGemmBN * kRawRow;                         // 16 KB / 8 KB
     static constexpr int kScaleBytes = 2 * 2 * 128;  // [row half][32-value block][128 rows]
     static constexpr int kRawStage = kRawCodes + kScaleBytes;
-    static constexpr int kRawStages = WF == kWeightsMxfp8 ? 7 : 12;
-    static constexpr int kOpStages = 2;
+    static constexpr int kRawStages = WF == kWeightsMxfp8 ? 5 : 10;
+    static constexpr int kAStages = 4;
+    static constexpr int kBStages = 2;
     static constexpr int kBBytes = kGemmBN * kGemmBK * 2;  // converted B tile, 32 KB
-    static constexpr int kOpStage = kABytes + kBBytes;
     static constexpr int kBarBytes = 1024;
-    static constexpr int kSmemBytes = kOpStages * kOpStage + kRawStages * kRawStage + 1024 /*align*/ + kBarBytes;
-    static constexpr int kConvWarps = 4;
+    static constexpr int kSmemBytes =
+        kBStages * kBBytes + kAStages * kABytes + kRawStages * kRawStage + 1024 /*align*/ + kBarBytes;
+#ifndef MOE_MX_CONV_WARPS
+#define MOE_MX_CONV_WARPS 8
+#endif
+    static constexpr int kConvWarps = MOE_MX_CONV_WARPS;
     static constexpr int kThreads = 32 * (7 + kConvWarps);  // warps 0-6 as listed, then the converters
     static_assert(kRawStage % 128 == 0, "raw stages stay 128-byte aligned");
 };
@@ -686,7 +697,46 @@ __device__ __forceinline__ uint32_t e2m1x2_scaled(uint32_t byte, float scale) {
     return pack_bf16x2(f.x * scale, f.y * scale);
 }
 
-// Converter warp cw (0..3): rows [64 cw, 64 cw + 64) of one raw k-block -> bf16 B
+// Decoders that keep the conversion pipe nearly idle.  A bf16x2 word whose bit
+// patterns are built from the codes represents code * 2^-b exactly (zero, the
+// codes' subnormals and their normals all map onto the same form of bf16), and
+// one bf16x2 multiply by 2^(scale - 127 + b) applies the E8M0 scale: exact when
+// the product is a bf16 number, rounded to nearest otherwise.  The multiplier
+// must itself be a normal bf16: scale + b <= 254, checked per block.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// 2^(code + bias - 127) in both halves of a bf16x2 (its exponent field is code + bias)
+__device__ __forceinline__ uint32_t pow2_bf16x2(uint32_t code, int bias) {
+    return ((code + bias) << 7) * 0x00010001u;
+}
+// f16x2 of two MX codes (hardware unpack) -> the same bits as bf16x2 of value * 2^-112:
+// every E4M3 / E2M1 value is a normal f16 (or zero) with its low 7 mantissa bits zero,
+// so dropping 3 bits keeps sign, exponent field and mantissa.
+__device__ __forceinline__ uint32_t f16x2_as_bf16x2_scaled(uint32_t h) {
+    return ((h & 0x7fff7fffu) >> 3) | (h & 0x80008000u);
+}
+// Four E4M3 codes (byte i = K index i) -> bf16x2 (codes 0, 1) and (2, 3) of value * 2^-120:
+// the code's 7 magnitude bits become bf16 bits 4..10 (exponent field = the code's
+// exponent field, mantissa = its 3 bits), its sign bit 15.
+__device__ __forceinline__ void e4m3x4_as_bf16x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t m = w & 0x7f7f7f7fu, sg = w & 0x80808080u;
+    lo = __byte_perm(m, 0u, 0x4140) * 16u + __byte_perm(sg, 0u, 0x1404);
+    hi = __byte_perm(m, 0u, 0x4342) * 16u + __byte_perm(sg, 0u, 0x3424);
+}
+
+// Decoder: 0 = fp32 products (conversion pipe), 1 = f16 unpack + bit reinterpretation +
+// one bf16x2 multiply, 2 = (E4M3) integer bit spreading + one bf16x2 multiply.  Measured
+// on GB300 (Nano decode): all three run at the same speed; the converters are bound by
+// shared-memory traffic, not by their arithmetic.
+#ifndef MOE_MX_CVT
+#define MOE_MX_CVT 1
+#endif
+
+// Converter warp cw (of kConvWarps): rows [cw * 256 / kConvWarps, + 256 / kConvWarps)
+// of one raw k-block -> bf16 B
 // tile.  Row r's 16-byte chunk j (K values 8j..8j+7) goes to r * 128 + ((j ^ (r % 8))
 // * 16): the 128-byte swizzle of a 1024-byte-aligned tile.  Lanes read consecutive
 // 16-byte pieces of the raw rows and store chunks of 8 distinct swizzle positions
@@ -694,33 +744,80 @@ __device__ __forceinline__ uint32_t e2m1x2_scaled(uint32_t byte, float scale) {
 template <int WF>
 __device__ __forceinline__ void mx_convert(const uint8_t *raw, const uint8_t *sc, uint8_t *out, int cw, int lane) {
     using M = MxCfg<WF>;
+    constexpr int kRowsPerWarp = kGemmBN / M::kConvWarps;
+    static_assert(kRowsPerWarp % 16 == 0, "converter rows");
     if (WF == kWeightsMxfp8) {
 #pragma unroll 2
-        for (int it = 0; it < 8; ++it) {
-            const int row = cw * 64 + it * 8 + (lane >> 2), c = lane & 3;  // 16 codes: K 16c..16c+15
+        for (int it = 0; it < kRowsPerWarp / 8; ++it) {
+            const int row = cw * kRowsPerWarp + it * 8 + (lane >> 2), c = lane & 3;  // 16 codes: K 16c..16c+15
             const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * M::kRawRow + c * 16);
-            const float f = e8m0_to_f32(sc[(row >> 7) * 256 + (c >> 1) * 128 + (row & 127)]);
-            const uint4 o0 = make_uint4(e4m3x2_scaled(v.x, f), e4m3x2_scaled(v.x >> 16, f),
-                                        e4m3x2_scaled(v.y, f), e4m3x2_scaled(v.y >> 16, f));
-            const uint4 o1 = make_uint4(e4m3x2_scaled(v.z, f), e4m3x2_scaled(v.z >> 16, f),
-                                        e4m3x2_scaled(v.w, f), e4m3x2_scaled(v.w >> 16, f));
+            const uint32_t code = sc[(row >> 7) * 256 + (c >> 1) * 128 + (row & 127)];
+            uint4 o0, o1;
+            constexpr int kB = MOE_MX_CVT == 2 ? 120 : 112;  // the decoders' 2^-b
+            if (MOE_MX_CVT != 0 && code + kB <= 254u) {
+                const uint32_t s2 = pow2_bf16x2(code, kB);
+                uint32_t r[8];
+                if (MOE_MX_CVT == 2) {
+                    e4m3x4_as_bf16x2(v.x, r[0], r[1]);
+                    e4m3x4_as_bf16x2(v.y, r[2], r[3]);
+                    e4m3x4_as_bf16x2(v.z, r[4], r[5]);
+                    e4m3x4_as_bf16x2(v.w, r[6], r[7]);
+                } else {
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t h0, h1;
+                        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h0) : "h"((unsigned short)w[i]));
+                        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h1) : "h"((unsigned short)(w[i] >> 16)));
+                        r[2 * i] = f16x2_as_bf16x2_scaled(h0);
+                        r[2 * i + 1] = f16x2_as_bf16x2_scaled(h1);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) r[i] = bf16x2_mul(r[i], s2);
+                o0 = make_uint4(r[0], r[1], r[2], r[3]);
+                o1 = make_uint4(r[4], r[5], r[6], r[7]);
+            } else {
+                const float f = e8m0_to_f32(code);
+                o0 = make_uint4(e4m3x2_scaled(v.x, f), e4m3x2_scaled(v.x >> 16, f), e4m3x2_scaled(v.y, f),
+                                e4m3x2_scaled(v.y >> 16, f));
+                o1 = make_uint4(e4m3x2_scaled(v.z, f), e4m3x2_scaled(v.z >> 16, f), e4m3x2_scaled(v.w, f),
+                                e4m3x2_scaled(v.w >> 16, f));
+            }
             uint8_t *rp = out + row * 128;
             *reinterpret_cast<uint4 *>(rp + (((2 * c) ^ (row & 7)) << 4)) = o0;
             *reinterpret_cast<uint4 *>(rp + (((2 * c + 1) ^ (row & 7)) << 4)) = o1;
         }
     } else {
 #pragma unroll 2
-        for (int it = 0; it < 4; ++it) {
-            const int row = cw * 64 + it * 16 + (lane >> 1), c = lane & 1;  // 32 codes: K 32c..32c+31
+        for (int it = 0; it < kRowsPerWarp / 16; ++it) {
+            const int row = cw * kRowsPerWarp + it * 16 + (lane >> 1), c = lane & 1;  // 32 codes: K 32c..32c+31
             const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * M::kRawRow + c * 16);
-            const float f = e8m0_to_f32(sc[(row >> 7) * 256 + c * 128 + (row & 127)]);
+            const uint32_t code = sc[(row >> 7) * 256 + c * 128 + (row & 127)];
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
             uint8_t *rp = out + row * 128;
+            if (MOE_MX_CVT != 0 && code + 112u <= 254u) {
+                const uint32_t s2 = pow2_bf16x2(code, 112);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {  // chunk 4c + q: K 32c + 8q .. + 7 = the four bytes of w[q]
-                const uint4 o = make_uint4(e2m1x2_scaled(w[q] & 0xffu, f), e2m1x2_scaled((w[q] >> 8) & 0xffu, f),
-                                           e2m1x2_scaled((w[q] >> 16) & 0xffu, f), e2m1x2_scaled(w[q] >> 24, f));
-                *reinterpret_cast<uint4 *>(rp + (((4 * c + q) ^ (row & 7)) << 4)) = o;
+                for (int q = 0; q < 4; ++q) {  // chunk 4c + q: K 32c + 8q .. + 7 = the four bytes of w[q]
+                    uint32_t r[4];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        uint32_t h;
+                        asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+                            : "=r"(h) : "r"(w[q] >> (8 * b)));
+                        r[b] = bf16x2_mul(f16x2_as_bf16x2_scaled(h), s2);
+                    }
+                    *reinterpret_cast<uint4 *>(rp + (((4 * c + q) ^ (row & 7)) << 4)) = make_uint4(r[0], r[1], r[2], r[3]);
+                }
+            } else {
+                const float f = e8m0_to_f32(code);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 o = make_uint4(e2m1x2_scaled(w[q] & 0xffu, f), e2m1x2_scaled((w[q] >> 8) & 0xffu, f),
+                                               e2m1x2_scaled((w[q] >> 16) & 0xffu, f), e2m1x2_scaled(w[q] >> 24, f));
+                    *reinterpret_cast<uint4 *>(rp + (((4 * c + q) ^ (row & 7)) << 4)) = o;
+                }
             }
         }
     }
@@ -729,33 +826,36 @@ __device__ __forceinline__ void mx_convert(const uint8_t *raw, const uint8_t *sc
 template <int WF>
 __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const __grid_constant__ GemmArgs p) {
     using M = MxCfg<WF>;
-    constexpr int R = M::kRawStages, P = M::kOpStages, NCW = M::kConvWarps;
+    constexpr int R = M::kRawStages, RA = M::kAStages, P = M::kBStages, NCW = M::kConvWarps;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    // operand stages (A 16 KB, B 32 KB; 1024-byte aligned), then the raw stages, then the barriers
-    auto opA = [&](int s) { return smem + s * M::kOpStage; };
-    auto opB = [&](int s) { return smem + s * M::kOpStage + kABytes; };
-    uint8_t *const raw0 = smem + P * M::kOpStage;
+    // converted B stages (32 KB), A stages (16 KB; both 1024-byte aligned), raw stages, barriers
+    auto opB = [&](int s) { return smem + s * M::kBBytes; };
+    auto opA = [&](int s) { return smem + P * M::kBBytes + s * kABytes; };
+    uint8_t *const raw0 = smem + P * M::kBBytes + RA * kABytes;
     auto rawS = [&](int s) { return raw0 + s * M::kRawStage; };
     uint64_t *bars = reinterpret_cast<uint64_t *>(raw0 + R * M::kRawStage);
     const uint32_t bar0 = smem_u32(bars);
     // barriers: ring_full[kRing], ring_empty[kRing], tfull[2], tempty[2] (the epilogue's
-    // contiguous block), then raw_full[R], raw_empty[R], a_full[P], op_full[P], op_empty[P], drain
+    // contiguous block), then raw_full[R], raw_empty[R], a_full[RA], a_empty[RA], op_full[P],
+    // op_empty[P] (op: the converted B ring), drain
     auto ring_full = [&](int i) { return bar0 + 8u * i; };
     auto ring_empty = [&](int i) { return bar0 + 8u * (kRing + i); };
     auto tfull_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kRing + a); };
     auto tempty_bar = [&](uint32_t a) { return bar0 + 8u * (2 * kRing + 2 + a); };
-    auto raw_full = [&](int s) { return bar0 + 8u * (2 * kRing + 4 + s); };
-    auto raw_empty = [&](int s) { return bar0 + 8u * (2 * kRing + 4 + R + s); };
-    auto a_full = [&](int s) { return bar0 + 8u * (2 * kRing + 4 + 2 * R + s); };
-    auto op_full = [&](int s) { return bar0 + 8u * (2 * kRing + 4 + 2 * R + P + s); };
-    auto op_empty = [&](int s) { return bar0 + 8u * (2 * kRing + 4 + 2 * R + 2 * P + s); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * kRing + 4 + 2 * R + 3 * P);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kRing + 5 + 2 * R + 3 * P);
+    constexpr int kB0 = 2 * kRing + 4;
+    auto raw_full = [&](int s) { return bar0 + 8u * (kB0 + s); };
+    auto raw_empty = [&](int s) { return bar0 + 8u * (kB0 + R + s); };
+    auto a_full = [&](int s) { return bar0 + 8u * (kB0 + 2 * R + s); };
+    auto a_empty = [&](int s) { return bar0 + 8u * (kB0 + 2 * R + RA + s); };
+    auto op_full = [&](int s) { return bar0 + 8u * (kB0 + 2 * R + 2 * RA + s); };
+    auto op_empty = [&](int s) { return bar0 + 8u * (kB0 + 2 * R + 2 * RA + P + s); };
+    const uint32_t drain_bar = bar0 + 8u * (kB0 + 2 * R + 2 * RA + 2 * P);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kB0 + 2 * R + 2 * RA + 2 * P + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *ring = reinterpret_cast<volatile int *>(tmem_slot + 2);  // [kRing] tile ids
-    static_assert(8 * (2 * kRing + 5 + 2 * R + 3 * P) + 8 + 4 * kRing <= M::kBarBytes, "barrier block");
+    static_assert(8 * (kB0 + 2 * R + 2 * RA + 2 * P + 1) + 8 + 4 * kRing <= M::kBarBytes, "barrier block");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto abort_all = [&]() { raise_abort(p.err, abort_flag); };
@@ -773,10 +873,13 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
             mbar_init(raw_full(s), 1);
             mbar_init(raw_empty(s), NCW);
         }
+        for (int s = 0; s < RA; ++s) {
+            mbar_init(a_full(s), 1);   // the A copy
+            mbar_init(a_empty(s), 1);  // the MMA's commit
+        }
         for (int s = 0; s < P; ++s) {
-            mbar_init(a_full(s), 1);     // the A copy
             mbar_init(op_full(s), NCW);  // each converter warp
-            mbar_init(op_empty(s), 1);
+            mbar_init(op_empty(s), 1);   // the MMA's commit
         }
         mbar_init(drain_bar, 1);
         fence_mbar_init();
@@ -904,9 +1007,9 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                 }
                 const CUtensorMap *mA = &p.maps[sg.map_a];
                 for (int kb = 0; kb < sg.k_blocks; ++kb) {
-                    const int s = L % P;
-                    const uint32_t ph = (L / P) & 1u;
-                    if (!mbar_wait(op_empty(s), ph ^ 1u, p.wait_ns, abort_flag)) {
+                    const int s = L % RA;
+                    const uint32_t ph = (L / RA) & 1u;
+                    if (!mbar_wait(a_empty(s), ph ^ 1u, p.wait_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -920,9 +1023,9 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
             if (stats) atomicAdd(stats + 1, (unsigned long long)w_dep);
             if (!ok) {
                 abort_all();
-                for (uint32_t i = 0; i < (uint32_t)P && i < L; ++i) {  // copies still in flight
+                for (uint32_t i = 0; i < (uint32_t)RA && i < L; ++i) {  // copies still in flight
                     const uint32_t l = L - 1 - i;
-                    mbar_wait(a_full(l % P), (l / P) & 1u, kDrainNs, nullptr);
+                    mbar_wait(a_full(l % RA), (l / RA) & 1u, kDrainNs, nullptr);
                 }
             }
         }
@@ -954,7 +1057,7 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                     break;
                 }
                 mx_convert<WF>(rawS(rs), rawS(rs) + M::kRawCodes, opB(os), cw, lane);
-                fence_proxy_async();  // the generic-proxy stores, before the MMA (async proxy) reads them
+                fence_proxy_async_smem();  // the generic-proxy stores, before the MMA (async proxy) reads them
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(raw_empty(rs));
@@ -991,23 +1094,23 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                 tc_fence_after();
                 const uint32_t d = tmem_base + a * kGemmBN;
                 for (int kb = 0; kb < sg.k_blocks; ++kb) {
-                    const int s = L % P;
-                    const uint32_t ph = (L / P) & 1u;
+                    const int sa = L % RA, sb = L % P;
                     const uint64_t t1 = stats ? global_timer_ns() : 0;
-                    if (!mbar_wait(a_full(s), ph, p.wait_ns, abort_flag) ||
-                        !mbar_wait(op_full(s), ph, p.wait_ns, abort_flag)) {
+                    if (!mbar_wait(a_full(sa), (L / RA) & 1u, p.wait_ns, abort_flag) ||
+                        !mbar_wait(op_full(sb), (L / P) & 1u, p.wait_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
                     if (stats) w_full += global_timer_ns() - t1;
                     tc_fence_after();
-                    const uint64_t ad = smem_desc_k128(smem_u32(opA(s)));
-                    const uint64_t bd = smem_desc_k128(smem_u32(opB(s)));
+                    const uint64_t ad = smem_desc_k128(smem_u32(opA(sa)));
+                    const uint64_t bd = smem_desc_k128(smem_u32(opB(sb)));
 #pragma unroll
                     for (int kk = 0; kk < kGemmBK / 16; ++kk)
                         tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
                     issued = true;
-                    tc_commit(op_empty(s));
+                    tc_commit(a_empty(sa));
+                    tc_commit(op_empty(sb));
                     ++L;
                 }
                 if (!ok) break;
