@@ -248,26 +248,37 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
     // would take the shared memory that this grid's later waves need
     __syncthreads();
     {
-        // eight independent loads in flight per thread, then the shared sums
-        constexpr int kU = 8;
-        const int tot = E * nbk;
-        for (int i0 = threadIdx.x; i0 < tot; i0 += kU * kScatterThreads) {
-            int v[kU];
+        // cnt[e] = rows of expert e, pre[e] = its rows in the blocks before this one:
+        // G threads per expert (a power of two dividing 32) sum strided blocks, eight
+        // loads in flight each, then a shuffle reduction.  No shared-memory atomics
+        // (with a few experts and many blocks they serialise on one address).
+        int G = 1;
+        while (G * 2 * E <= kScatterThreads && G < 32) G *= 2;
+        const int e = threadIdx.x / G, g = threadIdx.x % G;
+        int c = 0, pr = 0;
+        if (e < E) {
+            constexpr int kU = 8;
+            for (int b0 = g; b0 < nbk; b0 += kU * G) {
+                int v[kU];
 #pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int i = i0 + u * kScatterThreads;
-                const int e = i / nbk, bb = i - e * nbk;
-                v[u] = i < tot ? __ldg(a.blk_hist + (size_t)bb * hb + (size_t)e * he) : 0;
-            }
+                for (int u = 0; u < kU; ++u) {
+                    const int bb = b0 + u * G;
+                    v[u] = bb < nbk ? __ldg(a.blk_hist + (size_t)bb * hb + (size_t)e * he) : 0;
+                }
 #pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int i = i0 + u * kScatterThreads;
-                if (v[u]) {
-                    const int e = i / nbk, bb = i - e * nbk;
-                    atomicAdd(&cnt[e], v[u]);
-                    if (bb < b) atomicAdd(&pre[e], v[u]);
+                for (int u = 0; u < kU; ++u) {
+                    c += v[u];
+                    if (b0 + u * G < b) pr += v[u];
                 }
             }
+        }
+        for (int o = G / 2; o > 0; o >>= 1) {
+            c += __shfl_xor_sync(0xffffffffu, c, o);
+            pr += __shfl_xor_sync(0xffffffffu, pr, o);
+        }
+        if (e < E && g == 0) {
+            cnt[e] = c;
+            pre[e] = pr;
         }
     }
     __syncthreads();
