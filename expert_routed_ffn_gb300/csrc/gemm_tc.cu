@@ -654,7 +654,10 @@ template <int WF>
 struct MxCfg {
     static constexpr int kRawRow = WF == kWeightsMxfp8 ? kGemmBK : kGemmBK / 2;  // bytes of a row's k-block
     static constexpr int kRawCodes = kGemmBN * kRawRow;                         // 16 KB / 8 KB
-    static constexpr int kScaleBytes = 2 * 2 * 128;  // [row half][32-value block][128 rows]
+    // scales [row half][32-value block][128 rows]: every copy lands 128-byte aligned, as a
+    // tensor copy's shared-memory destination must
+    static constexpr int kScaleStride = 128;
+    static constexpr int kScaleBytes = 4 * kScaleStride;
     static constexpr int kRawStage = kRawCodes + kScaleBytes;
     static constexpr int kRawStages = WF == kWeightsMxfp8 ? 5 : 10;
     static constexpr int kAStages = 4;
@@ -751,7 +754,7 @@ __device__ __forceinline__ void mx_convert(const uint8_t *raw, const uint8_t *sc
         for (int it = 0; it < kRowsPerWarp / 8; ++it) {
             const int row = cw * kRowsPerWarp + it * 8 + (lane >> 2), c = lane & 3;  // 16 codes: K 16c..16c+15
             const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * M::kRawRow + c * 16);
-            const uint32_t code = sc[(row >> 7) * 256 + (c >> 1) * 128 + (row & 127)];
+            const uint32_t code = sc[((row >> 7) * 2 + (c >> 1)) * M::kScaleStride + (row & 127)];
             uint4 o0, o1;
             constexpr int kB = MOE_MX_CVT == 2 ? 120 : 112;  // the decoders' 2^-b
             if (MOE_MX_CVT != 0 && code + kB <= 254u) {
@@ -793,7 +796,7 @@ __device__ __forceinline__ void mx_convert(const uint8_t *raw, const uint8_t *sc
         for (int it = 0; it < kRowsPerWarp / 16; ++it) {
             const int row = cw * kRowsPerWarp + it * 16 + (lane >> 1), c = lane & 1;  // 32 codes: K 32c..32c+31
             const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * M::kRawRow + c * 16);
-            const uint32_t code = sc[(row >> 7) * 256 + c * 128 + (row & 127)];
+            const uint32_t code = sc[((row >> 7) * 2 + c) * M::kScaleStride + (row & 127)];
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
             uint8_t *rp = out + row * 128;
             if (MOE_MX_CVT != 0 && code + 112u <= 254u) {
@@ -965,7 +968,7 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                     tma_load_3d(dst, mC0, raw_full(s), xb, r0, g);
                     tma_load_3d(dst + 128 * M::kRawRow, mC1, raw_full(s), xb, r1, g);
                     tma_load_3d(dst + M::kRawCodes, mS0, raw_full(s), r0, kx / 32, g);
-                    tma_load_3d(dst + M::kRawCodes + 256, mS1, raw_full(s), r1, kx / 32, g);
+                    tma_load_3d(dst + M::kRawCodes + 2 * M::kScaleStride, mS1, raw_full(s), r1, kx / 32, g);
                     ++L;
                 }
                 if (!ok) break;
