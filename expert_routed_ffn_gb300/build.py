@@ -21,7 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmoe.so")
 
-SOURCES = ["router.cu", "router_tc.cu", "stream.cu", "gemm_tc.cu", "gemm_sab.cu", "moe_capi.cu", "dispatch_static.cu"]
+SOURCES = ["router.cu", "router_tc.cu", "stream.cu", "gemm_tc.cu", "gemm_sab.cu", "gemm_mxt.cu", "moe_capi.cu",
+           "dispatch_static.cu"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "kernels.h"), os.path.join(CSRC, "routing.cuh"),
            os.path.join(INCLUDE, "moe.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

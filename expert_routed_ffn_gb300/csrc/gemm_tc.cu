@@ -1229,25 +1229,26 @@ CUresult encode_map_b_kb2(CUtensorMap *m, const void *ptr, int groups, int rows,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-CUresult encode_map_mx_codes(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int wfmt) {
+CUresult encode_map_mx_codes(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int wfmt, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
     const int row_bytes = wfmt == kWeightsMxfp8 ? K : K / 2;
     const cuuint64_t dims[3] = {(cuuint64_t)row_bytes, (cuuint64_t)rows, (cuuint64_t)groups};
     const cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows * row_bytes};
-    const cuuint32_t box[3] = {(cuuint32_t)(wfmt == kWeightsMxfp8 ? kGemmBK : kGemmBK / 2), 128, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)(wfmt == kWeightsMxfp8 ? kGemmBK : kGemmBK / 2), (cuuint32_t)box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-CUresult encode_map_mx_scales(CUtensorMap *m, const void *ptr, int groups, int rows, int K) {
+CUresult encode_map_mx_scales(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int box_rows,
+                              int box_blocks) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
     const cuuint64_t dims[3] = {(cuuint64_t)rows, (cuuint64_t)(K / 32), (cuuint64_t)groups};
     const cuuint64_t strides[2] = {(cuuint64_t)rows, (cuuint64_t)rows * (K / 32)};
-    const cuuint32_t box[3] = {128, 2, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)box_rows, (cuuint32_t)box_blocks, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -298,6 +298,31 @@ struct SabArgs {
 };
 cudaError_t launch_gemm_sab(const SabArgs &a, int n_tokens, cudaStream_t s);
 
+// Swapped-operand expert GEMMs on MX weights (gemm_mxt.cu): the weight rows are
+// the MMA's A operand (M = 128), decoded from their codes and scales by one thread
+// per row straight into tensor memory; n_tokens (32 or 64) token rows from shared
+// memory are its N.  Segments as in SabArgs; per segment, W?a / W?b map the codes of
+// gate (or down) and up with boxes of 64 rows (gate/up) or 128 rows (down), S?a / S?b
+// their scales with boxes of those rows x all K / 32 blocks of the segment (one copy
+// per tile), and X? the token rows (box n_tokens x 64).  sblk: the largest K / 32 of
+// the segments (sizes the per-tile scale buffers).
+struct MxtArgs {
+    CUtensorMap Wa0, Wb0, Sa0, Sb0, X0;
+    CUtensorMap Wa1, Wb1, Sa1, Sb1, X1;
+    SabSegment seg[2];
+    int num_segs, glu, act;
+    float alpha, limit, beta;
+    int *err;
+    unsigned long long wait_ns;
+    int num_ctas, stages, wfmt, sblk;
+    // nullptr, or kGemmStats ns sums over CTAs: producer waiting for a free stage,
+    // converters waiting for codes, converters waiting for a free TMEM buffer, MMA
+    // waiting for operands, MMA waiting for an accumulator, epilogue waiting for an
+    // accumulator, epilogue working; then the tiles
+    unsigned long long *stats;
+};
+cudaError_t launch_gemm_mxt(const MxtArgs &a, int n_tokens, cudaStream_t s);
+
 // Tensor maps (TMA descriptors) for the GEMMs.  A: [rows, K] bf16, box 128 x 64.
 // B: [groups, rows, K] bf16, box box_rows x 64.  Both with 128-byte swizzle.
 CUresult encode_map_a(CUtensorMap *m, const void *ptr, int rows, int K);
@@ -310,8 +335,10 @@ CUresult encode_map_b(CUtensorMap *m, const void *ptr, int groups, int rows, int
 // rows, K / 2] (E2M1, two per byte, element 2j in the low nibble), box of one
 // 64-element k-block x 128 rows; E8M0 scales [groups, K / 32, rows], box 128
 // rows x 2 (the k-block's two scale blocks).  No swizzle.
-CUresult encode_map_mx_codes(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int wfmt);
-CUresult encode_map_mx_scales(CUtensorMap *m, const void *ptr, int groups, int rows, int K);
+CUresult encode_map_mx_codes(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int wfmt,
+                             int box_rows = 128);
+CUresult encode_map_mx_scales(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int box_rows = 128,
+                              int box_blocks = 2);
 
 // ------------------------------------------------- decode streamers (K6)
 // CUDA-core kernels for few tokens per expert: each CTA streams a block of

@@ -49,6 +49,13 @@ constexpr int kPathAuto = 0, kPathDecode = 1, kPathGrouped = 2, kPathSwapped = 3
 // sizes and lose where the shared expert sees many tokens (each weight tile is
 // re-read per token tile), so the auto path keeps the grouped GEMMs.
 constexpr int kSwapMaxTokensPerExpert = 0;
+// MX weights: the auto path takes the swapped-operand kernel (weights decoded into
+// tensor memory) up to this many routed slots per expert on average.  Measured on
+// GB300 (Nano decode, MXFP8): it is slower than the grouped MX kernel at every size
+// (47 + 29 us against 51 us), because each of its 128 x 32 x 16 MMAs costs about 280
+// cycles to issue and it needs twice as many per weight as the grouped kernel's
+// 128 x 256 x 16, so the auto path keeps the grouped kernel; MOE_OPT_PATH 3 selects it.
+constexpr int kMxtMaxSlotsPerExpert = 0;
 // Auto path: the decode kernels only up to this many tokens.  Measured on
 // GB300, the tcgen05 grouped path is at least as fast down to T = 1, so the
 // auto path always takes it; the decode kernels stay selectable.
@@ -127,6 +134,9 @@ struct moe_handle {
     // MX weights: m_gate ... m_shd map the element codes; these map their E8M0 scales
     int wfmt = 0;  // moe_weight_format
     CUtensorMap m_gate_s, m_up_s, m_down_s, m_shg_s, m_shu_s, m_shd_s;
+    // and with boxes of a whole tile's scales (the swapped MX kernel: 64 rows x H/32 for
+    // gate/up, 128 rows x K/32 for down; its gate/up codes go in m_gate64 ...)
+    CUtensorMap m_gate_st, m_up_st, m_down_st, m_shg_st, m_shu_st, m_shd_st;
     const void *m_x2_ptr = nullptr;
     int m_x2_rows = 0;
     // descriptor of the caller's X for the shared-expert GEMM (cached by pointer and T)
@@ -319,6 +329,11 @@ moe_status build_maps(moe_handle *h) {
         MAP(moe::encode_map_mx_scales(&h->m_gate_s, h->w.gate_scale, Ep, I, H));
         MAP(moe::encode_map_mx_scales(&h->m_up_s, h->w.up_scale, Ep, I, H));
         MAP(moe::encode_map_mx_scales(&h->m_down_s, h->w.down_scale, Ep, H, I));
+        MAP(moe::encode_map_mx_codes(&h->m_gate64, h->w.gate, Ep, I, H, h->wfmt, 64));
+        MAP(moe::encode_map_mx_codes(&h->m_up64, h->w.up, Ep, I, H, h->wfmt, 64));
+        MAP(moe::encode_map_mx_scales(&h->m_gate_st, h->w.gate_scale, Ep, I, H, 64, H / 32));
+        MAP(moe::encode_map_mx_scales(&h->m_up_st, h->w.up_scale, Ep, I, H, 64, H / 32));
+        MAP(moe::encode_map_mx_scales(&h->m_down_st, h->w.down_scale, Ep, H, I, 128, I / 32));
     } else {
     MAP(moe::encode_map_b_kb2(&h->m_gate2, h->w.gate, Ep, I, H, 128));
     MAP(moe::encode_map_b_kb2(&h->m_up2, h->w.up, Ep, I, H, 128));
@@ -352,6 +367,9 @@ moe_status build_maps(moe_handle *h) {
             h->m_shg_s = h->m_gate_s;
             h->m_shu_s = h->m_up_s;
             h->m_shd_s = h->m_down_s;
+            h->m_shg_st = h->m_gate_st;
+            h->m_shu_st = h->m_up_st;
+            h->m_shd_st = h->m_down_st;
             h->m_shg64 = h->m_gate64;
             h->m_shu64 = h->m_up64;
             h->m_shd128 = h->m_down128;
@@ -365,6 +383,11 @@ moe_status build_maps(moe_handle *h) {
             MAP(moe::encode_map_mx_scales(&h->m_shg_s, h->w.sh_gate_scale, 1, S, H));
             MAP(moe::encode_map_mx_scales(&h->m_shu_s, h->w.sh_up_scale, 1, S, H));
             MAP(moe::encode_map_mx_scales(&h->m_shd_s, h->w.sh_down_scale, 1, H, S));
+            MAP(moe::encode_map_mx_codes(&h->m_shg64, h->w.sh_gate, 1, S, H, h->wfmt, 64));
+            MAP(moe::encode_map_mx_codes(&h->m_shu64, h->w.sh_up, 1, S, H, h->wfmt, 64));
+            MAP(moe::encode_map_mx_scales(&h->m_shg_st, h->w.sh_gate_scale, 1, S, H, 64, H / 32));
+            MAP(moe::encode_map_mx_scales(&h->m_shu_st, h->w.sh_up_scale, 1, S, H, 64, H / 32));
+            MAP(moe::encode_map_mx_scales(&h->m_shd_st, h->w.sh_down_scale, 1, H, S, 128, S / 32));
         } else {
             MAP(moe::encode_map_b(&h->m_shg, h->w.sh_gate, 1, S, H, 128));
             MAP(moe::encode_map_b(&h->m_shu, h->w.sh_up, 1, S, H, 128));
@@ -659,6 +682,72 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     return launched(h, moe::launch_gemm_tc(g, s), "down_gemm", n, s);
 }
 
+// Swapped-operand expert GEMMs on MX weights (gemm_mxt.cu): gate/up, then down,
+// routed and shared segments in each launch, n_tok token rows per tile.
+moe_status run_mx_swapped(moe_handle *h, const void *X, int T, cudaStream_t s, int *n, int n_tok) {
+    const int H = h->H, I = h->I, S = h->S, E = h->E, v = n_tok == 32 ? 0 : 1;
+    moe::MxtArgs g{};
+    g.err = h->err;
+    g.wait_ns = h->wait_ns;
+    g.act = h->cfg.hidden_act;
+    g.alpha = h->cfg.act_alpha;
+    g.limit = h->cfg.act_limit;
+    g.beta = h->cfg.act_beta;
+    g.num_ctas = h->num_sms;
+    g.wfmt = h->wfmt;
+    const int sh_base = h->cfg.shared_packed ? E : 0;
+    // unused map slots hold a valid descriptor
+    g.Wa0 = g.Wb0 = g.Wa1 = g.Wb1 = g.Sa0 = g.Sb0 = g.Sa1 = g.Sb1 = h->m_down;
+    g.X0 = g.X1 = h->m_xs_n[v];
+
+    g.glu = 1;
+    g.Wa0 = h->m_gate64;
+    g.Wb0 = h->m_up64;
+    g.Sa0 = h->m_gate_st;
+    g.Sb0 = h->m_up_st;
+    g.sblk = H / 32;
+    g.X0 = h->m_xs_n[v];
+    g.seg[0] = moe::SabSegment{0, E, 0, 0, h->offs, h->tile_offs, (I + 63) / 64, H / 64, I, h->hbuf, I};
+    g.num_segs = 1;
+    if (h->has_shared) {
+        if (h->x_f32) {
+            g.X1 = h->m_xbf_n[v];
+        } else {
+            const CUtensorMap *mx = nullptr;
+            moe_status st = x_map_box(h, X, T, v, &mx);
+            if (st != MOE_OK) return st;
+            g.X1 = *mx;
+        }
+        g.Wa1 = h->m_shg64;
+        g.Wb1 = h->m_shu64;
+        g.Sa1 = h->m_shg_st;
+        g.Sb1 = h->m_shu_st;
+        g.seg[1] = moe::SabSegment{1, 1, sh_base, T, nullptr, nullptr, (S + 63) / 64, H / 64, S, h->hs, S};
+        g.num_segs = 2;
+    }
+    g.stats = h->trace_on ? h->gemm_stats : nullptr;
+    moe_status st = launched(h, moe::launch_gemm_mxt(g, n_tok, s), "gate_up_gemm_swapped", n, s);
+    if (st != MOE_OK) return st;
+
+    g.glu = 0;
+    g.stats = nullptr;  // the statistics describe the gate/up launch
+    g.Wa0 = g.Wb0 = h->m_down;
+    g.Sa0 = g.Sb0 = h->m_down_st;
+    g.sblk = I / 32;
+    g.X0 = h->m_hb_n[v];
+    g.seg[0] = moe::SabSegment{0, E, 0, 0, h->offs, h->tile_offs, (H + 127) / 128, I / 64, H, h->yslot, H};
+    g.num_segs = 1;
+    if (h->has_shared) {
+        g.Wa1 = g.Wb1 = h->m_shd;
+        g.Sa1 = g.Sb1 = h->m_shd_st;
+        g.sblk = I > S ? I / 32 : S / 32;
+        g.X1 = h->m_hs_n[v];
+        g.seg[1] = moe::SabSegment{1, 1, sh_base, T, nullptr, nullptr, (H + 127) / 128, S / 64, H, h->ys, H};
+        g.num_segs = 2;
+    }
+    return launched(h, moe::launch_gemm_mxt(g, n_tok, s), "down_gemm_swapped", n, s);
+}
+
 moe_status run_decode(moe_handle *h, const void *X, int T, cudaStream_t s, int *n) {
     moe::DecodeGroups grp{h->offs, h->active, h->E, h->has_shared ? 1 : 0, T};
     moe::DecodeGluArgs ga{};
@@ -754,7 +843,9 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     if (path == kPathAuto)
         path = T <= kDecodeMaxTokens ? kPathDecode
                                      : (slots <= (long long)kSwapMaxTokensPerExpert * h->E ? kPathSwapped : kPathGrouped);
-    if (h->dense || h->wfmt != MOE_WEIGHTS_BF16) path = kPathGrouped;  // dense layer, MX weights: grouped GEMMs
+    if (h->dense) path = kPathGrouped;  // a dense layer: the grouped GEMM's shared segments
+    if (h->wfmt != MOE_WEIGHTS_BF16 && !h->dense && h->path_opt == kPathAuto)
+        path = slots <= (long long)kMxtMaxSlotsPerExpert * h->E ? kPathSwapped : kPathGrouped;
     const int n_tok = slots <= 24ll * h->E ? 32 : 64;  // token tile of the swapped GEMMs
     h->ev_recorded = 0;
     // Decode-sized batches touch nearly every expert (about two or more tokens
@@ -813,7 +904,7 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
         if (path == kPathDecode)
             st = run_decode(h, Xm, T, s, &n);
         else if (path == kPathSwapped)
-            st = run_swapped(h, Xm, T, s, &n, n_tok);
+            st = h->wfmt != MOE_WEIGHTS_BF16 ? run_mx_swapped(h, Xm, T, s, &n, n_tok) : run_swapped(h, Xm, T, s, &n, n_tok);
         else
             st = run_grouped(h, Xm, T, s, &n);
     }
@@ -1054,8 +1145,8 @@ moe_status moe_set_option(moe_handle *h, int option, long long value) {
     switch (option) {
     case MOE_OPT_PATH:
         if (value < kPathAuto || value > kPathSwapped) return fail(MOE_ERR_INVALID_ARG, "path %lld", value);
-        if (h->wfmt != MOE_WEIGHTS_BF16 && (value == kPathDecode || value == kPathSwapped))
-            return fail(MOE_ERR_UNSUPPORTED, "MX weights run on the grouped tensor-core path only");
+        if (h->wfmt != MOE_WEIGHTS_BF16 && value == kPathDecode)
+            return fail(MOE_ERR_UNSUPPORTED, "MX weights run on the tensor-core paths only (2 grouped, 3 swapped)");
         h->path_opt = (int)value;
         return MOE_OK;
     case MOE_OPT_WAIT_LIMIT_NS:

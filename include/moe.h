@@ -85,8 +85,10 @@ typedef enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 } moe_dtype;
  *   MXFP4: two E2M1 codes per byte, [rows, K / 2], element 2j in the low nibble.
  *   Scales: uint8 [K / 32, rows] per weight slice (block-major: for each
  *           32-value block, the scales of all rows).
- * MX weights run on the grouped tensor-core path only (moe_set_option
- * MOE_OPT_PATH 1 or 3 is refused, and MOE_OPT_GEMM_PAIR has no effect). */
+ * MX weights run on the tensor-core paths: the grouped GEMM (the auto path) or,
+ * with moe_set_option MOE_OPT_PATH 3, the swapped-operand GEMM that decodes the
+ * weights straight into tensor memory; MOE_OPT_PATH 1 is refused and
+ * MOE_OPT_GEMM_PAIR has no effect. */
 typedef enum { MOE_WEIGHTS_BF16 = 0, MOE_WEIGHTS_MXFP8 = 1, MOE_WEIGHTS_MXFP4 = 2 } moe_weight_format;
 
 /* Norms around the MLP (y = x / sqrt(mean(x^2) + eps) * g over the H values of a row). */

@@ -9,10 +9,12 @@ activations stay bf16.  Checks:
     token, outputs of every token on small shapes, sampled tokens at full size,
     with the bf16 tolerance (decoding is exact, so the arithmetic is the bf16
     path's);
-  * bit-for-bit against the bf16 path on the decoded weights: the MX GEMM issues
-    the same tcgen05 MMAs on the same operand values in the same order, so Y must
-    be identical, which pins the decoder (byte and nibble order, scale index,
-    swizzled layout) independently of any tolerance;
+  * bit-for-bit against the bf16 path on the decoded weights: both MX GEMMs (the
+    grouped one, tokens as M, and the swapped one, weights decoded into tensor
+    memory as M) issue the same tcgen05 MMAs on the same operand values in the same
+    order as their bf16 counterparts, so Y must be identical, which pins the
+    decoders (byte and nibble order, scale index, operand layouts) independently of
+    any tolerance;
   * the options the MX path refuses.
 """
 
@@ -97,11 +99,19 @@ SMALL = {
 FORMATS = ["mxfp8", "mxfp4"]
 
 
+PATHS = {"grouped": capi.PATH_GROUPED, "swapped": capi.PATH_SWAPPED}
+
+
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("name", list(SMALL))
-def test_mx_small_every_token(name, fmt):
+def test_mx_small_every_token(name, fmt, path):
     shape = SMALL[name].replace(name=f"{SMALL[name].name}_{fmt}", weight_format=fmt)
     inputs, blk = P.make_case(shape)
+    if shape.E > 0:
+        blk.set_option(capi.MOE_OPT_PATH, PATHS[path])
+    elif path == "swapped":
+        pytest.skip("a dense layer runs on the grouped GEMM only")
     Y = _forward(blk, inputs["X"])
     if shape.E > 0 and shape.mlp_norm == "none":
         idx, w = (blk.inspect(b, shape.T * shape.k, dt).view(shape.T, shape.k).cpu().numpy()
@@ -111,16 +121,23 @@ def test_mx_small_every_token(name, fmt):
     blk.close()
 
 
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("name", ["nano", "m3_small_packed", "afmoe_ragged", "dense_small", "nano_T1"])
-def test_mx_bit_identical_to_bf16_path_on_decoded_weights(name, fmt):
+def test_mx_bit_identical_to_bf16_path_on_decoded_weights(name, fmt, path):
     shape = SMALL[name].replace(name=f"{SMALL[name].name}_{fmt}", weight_format=fmt)
+    if shape.E == 0 and path == "swapped":
+        pytest.skip("a dense layer runs on the grouped GEMM only")
     inputs, blk = P.make_case(shape)
+    if shape.E > 0:
+        blk.set_option(capi.MOE_OPT_PATH, PATHS[path])
     Y = _forward(blk, inputs["X"])
     dec = decoded_bf16_inputs(shape, inputs)
     bshape = shape.replace(weight_format="bf16")
     ref_blk = capi.block_from_inputs(bshape, dec)
-    ref_blk.set_option(capi.MOE_OPT_GEMM_PAIR, 0)  # the MX GEMM runs one CTA per tile
+    if shape.E > 0:
+        ref_blk.set_option(capi.MOE_OPT_PATH, PATHS[path])
+    ref_blk.set_option(capi.MOE_OPT_GEMM_PAIR, 0)  # the MX GEMMs run one CTA per tile
     Yb = _forward(ref_blk, dec["X"])
     assert torch.equal(Y, Yb), "MX path differs from the bf16 path on the decoded weights"
     ref_blk.close()
@@ -131,6 +148,7 @@ def test_mx_bit_identical_to_bf16_path_on_decoded_weights(name, fmt):
 def test_mx_two_launches_and_repeat_are_bit_identical(fmt):
     shape = wl.NANO_DECODE.replace(name=f"nano_{fmt}", T=200, weight_format=fmt)
     inputs, blk = P.make_case(shape)
+    blk.set_option(capi.MOE_OPT_PATH, capi.PATH_GROUPED)  # the fused launch is the grouped kernel's
     Y1 = _forward(blk, inputs["X"]).clone()
     Y2 = _forward(blk, inputs["X"]).clone()
     blk.set_option(capi.MOE_OPT_FUSE_EXPERTS, 0)
@@ -142,10 +160,10 @@ def test_mx_two_launches_and_repeat_are_bit_identical(fmt):
 def test_mx_refuses_other_paths():
     shape = wl.NANO_DECODE.replace(name="nano_mx8", T=16, weight_format="mxfp8")
     inputs, blk = P.make_case(shape)
-    for path in (capi.PATH_DECODE, capi.PATH_SWAPPED):
-        with pytest.raises(capi.MoeError) as ei:
-            blk.set_option(capi.MOE_OPT_PATH, path)
-        assert ei.value.status == capi.MOE_ERR_UNSUPPORTED
+    with pytest.raises(capi.MoeError) as ei:
+        blk.set_option(capi.MOE_OPT_PATH, capi.PATH_DECODE)
+    assert ei.value.status == capi.MOE_ERR_UNSUPPORTED
+    blk.set_option(capi.MOE_OPT_PATH, capi.PATH_GROUPED)
     blk.set_option(capi.MOE_OPT_GEMM_PAIR, 1)  # no effect: the MX GEMM has no CTA-pair variant
     _oracle_check(shape, inputs, _forward(blk, inputs["X"]), tag="mx_pair_opt")
     blk.close()
