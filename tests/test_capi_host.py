@@ -105,6 +105,35 @@ def test_create_rejects_bad_dense_and_norm_configs(lib):
     assert h.value is None
 
 
+def test_create_rejects_bad_mx_configs(lib):
+    """Block-scaled weights: the format must be known, every used weight tensor needs
+    its scale tensor, and scale pointers must be 16-byte aligned."""
+    h = ctypes.c_void_p()
+    fake = ctypes.c_void_p(1 << 20)
+    bad = capi.config_from_shape(wl.NANO_DECODE)
+    bad.weight_format = 3
+    assert lib.moe_create(ctypes.byref(bad), ctypes.byref(_weights()), ctypes.byref(h)) == capi.MOE_ERR_INVALID_ARG
+    cfg = capi.config_from_shape(wl.WORKLOADS["nano_decode_mxfp8"])
+    assert cfg.weight_format == capi.MOE_WEIGHTS_MXFP8
+    w = _weights()  # no scales at all
+    assert lib.moe_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == capi.MOE_ERR_INVALID_ARG
+    assert "scale" in lib.moe_last_error().decode()
+    w.gate_scale = w.up_scale = w.down_scale = fake
+    assert lib.moe_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == capi.MOE_ERR_INVALID_ARG
+    assert "sh_gate_scale" in lib.moe_last_error().decode()  # the separate shared expert's scales
+    w.sh_gate_scale = w.sh_up_scale = fake
+    w.sh_down_scale = ctypes.c_void_p((1 << 20) + 8)  # misaligned
+    assert lib.moe_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == capi.MOE_ERR_INVALID_ARG
+    assert "aligned" in lib.moe_last_error().decode()
+    packed = capi.config_from_shape(wl.WORKLOADS["m3_mxfp8"])  # packed shared expert: routed scales suffice
+    w = _weights()
+    w.sh_gate = w.sh_up = w.sh_down = None
+    w.gate_scale = w.up_scale = None
+    w.down_scale = fake
+    assert lib.moe_create(ctypes.byref(packed), ctypes.byref(w), ctypes.byref(h)) == capi.MOE_ERR_INVALID_ARG
+    assert h.value is None
+
+
 def test_null_handle_calls_fail_cleanly(lib):
     assert lib.moe_forward(None, None, 4, None, None) == capi.MOE_ERR_INVALID_ARG
     assert lib.moe_route(None, None, 4, None, None, None) == capi.MOE_ERR_INVALID_ARG
