@@ -246,6 +246,7 @@ def run_ours(args, shape):
         # per CTA and step, us: the tensor-core router's phases
         keys = ["main_loop", "cluster_barrier", "push_partials", "sum_and_route", "histogram"]
         router_phases = {k: round(v * 1e-3 / rw_sum[5], 2) for k, v in zip(keys, rw_sum[:5])}
+        router_phases["of_which_partial_sums"] = round(rw_sum[6] * 1e-3 / rw_sum[5], 2)
         router_phases["ctas"] = rw_sum[5] // tl_n
     # per kernel: first begin, first ready, last ready, first end, last end
     timeline = ({t[0]: [round(t[j] / tl_n, 2) for j in range(1, capi.TRACE_FIELDS + 1)] for t in tl_sum}

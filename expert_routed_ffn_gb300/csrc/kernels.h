@@ -106,7 +106,8 @@ struct RouterTcArgs {
     unsigned long long *trace;
     // nullptr, or kRouterStats ns sums over CTAs: main loop, first cluster
     // barrier, pushing the partials with the second barrier, adding them and
-    // routing, histogram; then the number of CTAs
+    // routing, histogram; then the number of CTAs; then the part of "adding them
+    // and routing" spent adding the partials
     unsigned long long *stats;
 };
 constexpr int kRouterStats = 8;

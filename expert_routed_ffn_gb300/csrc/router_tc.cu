@@ -276,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
         cluster_sync_all();  // all partials of this CTA's tokens have arrived
     }
     const uint64_t t_pushed = stats ? global_timer_ns() : 0;
+    uint64_t t_summed = t_pushed;
 
     // routing of tokens [rank * TT, (rank + 1) * TT) of the m-tile, LPT lanes per token
     constexpr int kGroups = kThreads / LPT;
@@ -299,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
                 lg[4] += b.x; lg[5] += b.y; lg[6] += b.z; lg[7] += b.w;
             }
         }
+        if (stats && threadIdx.x == 0 && base == 0) t_summed = global_timer_ns();  // thread 0's sums are in
         route_token_group<LPT, true>(lg, sub, valid, t, p.E, p.k, p.bias, p.score_func, p.route_norm,
                                      p.route_scale, p.topk_idx, p.topk_w, p.blk_hist ? hist : nullptr);
     }
@@ -318,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
         atomicAdd(stats + 3, (unsigned long long)(t_routed - t_pushed));
         atomicAdd(stats + 4, (unsigned long long)(t_end - t_routed));
         atomicAdd(stats + 5, 1ull);
+        atomicAdd(stats + 6, (unsigned long long)(t_summed - t_pushed));
     }
     if (warp == 1) {
         __syncwarp();
