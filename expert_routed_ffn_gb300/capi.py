@@ -31,6 +31,7 @@ SCALE_KEYS = ("gate_scale", "up_scale", "down_scale", "sh_gate_scale", "sh_up_sc
 MOE_OPT_PATH, MOE_OPT_WAIT_LIMIT_NS, MOE_OPT_STAGE_EVENTS, MOE_OPT_FUSE_EXPERTS, MOE_OPT_PREFETCH = 0, 1, 2, 3, 4
 MOE_OPT_TRACE = 5
 MOE_OPT_GEMM_PAIR = 6
+MOE_OPT_GRAPH = 8
 MOE_BUF_GEMM_STATS = 6
 MOE_BUF_ROUTER_STATS = 7
 MOE_BUF_NORMED_X = 8

@@ -149,6 +149,18 @@ struct moe_handle {
     // optional per-kernel timing of moe_forward
     static constexpr int kMaxStages = 8;
     bool stage_events = false;
+    // moe_forward_host replayed from a CUDA graph: the copy in, the forward and the copy
+    // out, captured on the second call with the same buffers, T and options
+    bool graph_opt = true;
+    unsigned opt_gen = 0;  // bumped by every option change
+    cudaGraphExec_t graph_exec = nullptr;
+    const void *g_x = nullptr;
+    void *g_y = nullptr;
+    int g_T = -1;
+    unsigned g_gen = 0;
+    int g_seen = 0;        // consecutive eager calls with this key
+    cudaStream_t hstream = nullptr;  // the graph runs here when the caller passes the legacy stream
+    cudaEvent_t ev_host = nullptr;
     cudaEvent_t ev[kMaxStages + 1] = {};
     int ev_recorded = 0;
     const char *stage_name[kMaxStages] = {};
@@ -1020,6 +1032,11 @@ moe_status moe_create(const moe_config *config, const moe_weights *weights, moe_
         cudaGetLastError();
         h->side = nullptr;  // no prefetch without its stream
     }
+    if (cudaStreamCreateWithFlags(&h->hstream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_host, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        h->hstream = nullptr;  // graphs then only on a caller's non-legacy stream
+    }
     st = build_maps(h);
     if (st != MOE_OK) {
         cudaFree(h->ws);
@@ -1091,6 +1108,46 @@ moe_status moe_forward(moe_handle *h, const void *X, int T, void *Y, moe_stream_
     return forward_device(h, X, T, Y, reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace {
+
+// The host-buffer forward's stream work: copy X in, the block, copy Y out.
+moe_status forward_host_ops(moe_handle *h, const void *X_host, int T, void *Y_host, cudaStream_t s) {
+    const size_t bytes = (size_t)T * h->H * (h->x_f32 ? 4 : 2);
+    cudaError_t e = cudaMemcpyAsync(h->x_stage, X_host, bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy of X");
+    moe_status st = forward_device(h, h->x_stage, T, h->y_stage, s);
+    if (st != MOE_OK) return st;
+    e = cudaMemcpyAsync(Y_host, h->y_stage, bytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy of Y");
+    return MOE_OK;
+}
+
+// Capture forward_host_ops into h->graph_exec; false (and no graph) if anything fails,
+// e.g. pageable host buffers, which a graph's copies cannot use.
+bool capture_forward_host(moe_handle *h, const void *X_host, int T, void *Y_host, cudaStream_t s) {
+    if (h->graph_exec) {
+        cudaGraphExecDestroy(h->graph_exec);
+        h->graph_exec = nullptr;
+    }
+    cudaGraph_t graph = nullptr;
+    if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    const moe_status st = forward_host_ops(h, X_host, T, Y_host, s);
+    const cudaError_t e = cudaStreamEndCapture(s, &graph);
+    bool ok = st == MOE_OK && e == cudaSuccess && graph != nullptr;
+    if (ok) ok = cudaGraphInstantiate(&h->graph_exec, graph, 0) == cudaSuccess;
+    if (graph) cudaGraphDestroy(graph);
+    if (!ok) {
+        h->graph_exec = nullptr;
+        cudaGetLastError();
+    }
+    return ok;
+}
+
+}  // namespace
+
 moe_status moe_forward_host(moe_handle *h, const void *X_host, int T, void *Y_host, moe_stream_t stream) {
     if (h == nullptr) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
     if (T < 0 || T > h->cfg.max_tokens)
@@ -1099,14 +1156,38 @@ moe_status moe_forward_host(moe_handle *h, const void *X_host, int T, void *Y_ho
     if (T == 0) return MOE_OK;
     if (!X_host || !Y_host) return fail(MOE_ERR_INVALID_ARG, "X_host and Y_host are required");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const size_t bytes = (size_t)T * h->H * (h->x_f32 ? 4 : 2);
-    cudaError_t e = cudaMemcpyAsync(h->x_stage, X_host, bytes, cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy of X");
-    moe_status st = forward_device(h, h->x_stage, T, h->y_stage, s);
+    // graphs only without per-kernel events or traces (those read host-side state per call);
+    // the legacy stream cannot be captured: the call (synchronous anyway) then runs on the
+    // handle's own stream, after the work already queued on the caller's
+    const bool graphable = h->graph_opt && !h->stage_events && !h->trace_on && (s != nullptr || h->hstream != nullptr);
+    if (graphable && s == nullptr) {
+        cudaError_t e = cudaEventRecord(h->ev_host, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->hstream, h->ev_host, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "ordering after the caller's stream");
+        s = h->hstream;
+    }
+    const bool same = h->g_x == X_host && h->g_y == Y_host && h->g_T == T && h->g_gen == h->opt_gen;
+    if (graphable && same && h->graph_exec != nullptr) {
+        cudaError_t e = cudaGraphLaunch(h->graph_exec, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "graph launch of the host-buffer forward");
+        return MOE_OK;
+    }
+    h->g_seen = same ? h->g_seen + 1 : 1;
+    h->g_x = X_host;
+    h->g_y = Y_host;
+    h->g_T = T;
+    h->g_gen = h->opt_gen;
+    if (graphable && h->g_seen >= 2 && capture_forward_host(h, X_host, T, Y_host, s)) {
+        // the launches recorded in the graph keep the counts and names of the eager forward
+        cudaError_t e = cudaGraphLaunch(h->graph_exec, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "graph launch of the host-buffer forward");
+        return MOE_OK;
+    }
+    moe_status st = forward_host_ops(h, X_host, T, Y_host, s);
     if (st != MOE_OK) return st;
-    e = cudaMemcpyAsync(Y_host, h->y_stage, bytes, cudaMemcpyDeviceToHost, s);
-    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy of Y");
-    e = cudaStreamSynchronize(s);
+    cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
     return MOE_OK;
 }
@@ -1129,6 +1210,9 @@ moe_status moe_sync_status(moe_handle *h) {
 void moe_destroy(moe_handle *h) {
     if (h == nullptr) return;
     cudaDeviceSynchronize();
+    if (h->graph_exec) cudaGraphExecDestroy(h->graph_exec);
+    if (h->hstream) cudaStreamDestroy(h->hstream);
+    if (h->ev_host) cudaEventDestroy(h->ev_host);
     for (auto &e : h->ev)
         if (e != nullptr) cudaEventDestroy(e);
     if (h->ev_fork) cudaEventDestroy(h->ev_fork);
@@ -1142,7 +1226,12 @@ const char *moe_last_error(void) { return g_last_error.c_str(); }
 
 moe_status moe_set_option(moe_handle *h, int option, long long value) {
     if (h == nullptr) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+    ++h->opt_gen;  // a captured forward no longer matches the options
     switch (option) {
+    case MOE_OPT_GRAPH:
+        if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "graph %lld", value);
+        h->graph_opt = value != 0;
+        return MOE_OK;
     case MOE_OPT_PATH:
         if (value < kPathAuto || value > kPathSwapped) return fail(MOE_ERR_INVALID_ARG, "path %lld", value);
         if (h->wfmt != MOE_WEIGHTS_BF16 && value == kPathDecode)

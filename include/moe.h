@@ -211,10 +211,16 @@ typedef enum {
                                   first and last CTA passed the wait on the previous kernel, and when
                                   its first and last CTA finished (the GPU's global timer), for
                                   moe_get_trace.  Costs a memset and a few atomics per CTA; default 0 */
-    MOE_OPT_GEMM_PAIR = 6      /* path 2: expert GEMM tiles of 256 rows on CTA pairs (tcgen05 with
+    MOE_OPT_GEMM_PAIR = 6,     /* path 2: expert GEMM tiles of 256 rows on CTA pairs (tcgen05 with
                                   cta_group::2: each CTA of a two-CTA cluster stages its 128 token rows
                                   and half of the weight tile); 0 never, 1 always, 2 (default) when
                                   T*k >= 256*E (tensor-bound sizes) */
+    MOE_OPT_GRAPH = 8          /* moe_forward_host: 1 (default) captures the copy in, the forward and the
+                                  copy out into a CUDA graph on the second call with the same host
+                                  buffers, T and options, and replays it on later such calls (host
+                                  buffers must then be pinned: with pageable ones the capture fails
+                                  and the call runs eagerly); 0 always runs eagerly.  Graphs are not
+                                  used while stage events or the trace are on. */
 } moe_option;
 
 /* Set an option.  Errors: INVALID_ARG (unknown option or value). */

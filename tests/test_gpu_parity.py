@@ -249,6 +249,53 @@ def test_forward_host_matches_forward_and_edge_sizes():
     assert empty.shape[0] == 0
 
 
+def test_forward_host_graph_replay_matches_forward():
+    """moe_forward_host runs eagerly, then captures a CUDA graph on the second call with
+    the same buffers and T, then replays it: every call equals moe_forward bit for bit,
+    on the legacy stream and on a caller's stream; new inputs in the same pinned buffer
+    are picked up by the replay; an option change or another T goes back to eager runs."""
+    for name in ("nano_decode", "afmoe_ragged", "m3_small_packed"):
+        shape = SMALL[name]
+        inputs, blk, Y = _run(shape, max_tokens=shape.T)
+        Xh = inputs["X"].cpu().pin_memory()
+        Yh = torch.empty_like(Xh).pin_memory()
+        ref = Y.cpu()
+        for _ in range(4):  # eager, capture, replay, replay
+            Yh.zero_()
+            blk.forward_host(Xh, Yh)
+            assert torch.equal(Yh, ref)
+        side = torch.cuda.Stream()
+        for _ in range(3):
+            Yh.zero_()
+            blk.forward_host(Xh, Yh, stream=side)
+            assert torch.equal(Yh, ref)
+        # new token values in the captured buffer
+        X2 = torch.roll(inputs["X"], 1, 0).contiguous()
+        Xh.copy_(X2.cpu())
+        Y2 = blk.forward(X2)
+        torch.cuda.synchronize()
+        for _ in range(2):
+            blk.forward_host(Xh, Yh)
+            assert torch.equal(Yh, Y2.cpu())
+        blk.set_option(capi.MOE_OPT_PREFETCH, 0)  # a changed option: eager, then a new capture
+        for _ in range(3):
+            blk.forward_host(Xh, Yh)
+            assert torch.equal(Yh, Y2.cpu())
+        blk.set_option(capi.MOE_OPT_GRAPH, 0)
+        blk.forward_host(Xh, Yh)
+        assert torch.equal(Yh, Y2.cpu())
+        half = shape.T // 2  # another T
+        Yh2 = torch.empty_like(Xh[:half]).pin_memory()
+        blk.set_option(capi.MOE_OPT_GRAPH, 1)
+        for _ in range(3):
+            blk.forward_host(Xh[:half], Yh2)
+        Yd = blk.forward(X2[:half].contiguous())
+        torch.cuda.synchronize()
+        assert torch.equal(Yh2, Yd.cpu())
+        assert blk.sync_status() == capi.MOE_OK
+        blk.close()
+
+
 # ---------------------------------------------------- full sizes, sampled
 
 def _full(shape, n_sample=16):
