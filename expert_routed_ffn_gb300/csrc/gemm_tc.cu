@@ -745,84 +745,108 @@ __device__ __forceinline__ void e4m3x4_as_bf16x2(uint32_t w, uint32_t &lo, uint3
 // tile.  Row r's 16-byte chunk j (K values 8j..8j+7) goes to r * 128 + ((j ^ (r % 8))
 // * 16): the 128-byte swizzle of a 1024-byte-aligned tile.  Lanes read consecutive
 // 16-byte pieces of the raw rows and store chunks of 8 distinct swizzle positions
-// per quarter-warp, so neither side has bank conflicts.
+// per quarter-warp, so neither side has bank conflicts.  The scale codes of the
+// warp's rows are read first: when all of them allow the bf16 multiplier (the usual
+// case) the loop has no per-row branch and its code loads are issued together
+// (measured: 0.35 against 0.58 us per k-block for eight warps with the branch).
 template <int WF>
 __device__ __forceinline__ void mx_convert(const uint8_t *raw, const uint8_t *sc, uint8_t *out, int cw, int lane) {
     using M = MxCfg<WF>;
     constexpr int kRowsPerWarp = kGemmBN / M::kConvWarps;
     static_assert(kRowsPerWarp % 16 == 0, "converter rows");
-    if (WF == kWeightsMxfp8) {
-#pragma unroll 2
-        for (int it = 0; it < kRowsPerWarp / 8; ++it) {
-            const int row = cw * kRowsPerWarp + it * 8 + (lane >> 2), c = lane & 3;  // 16 codes: K 16c..16c+15
-            const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * M::kRawRow + c * 16);
-            const uint32_t code = sc[((row >> 7) * 2 + (c >> 1)) * M::kScaleStride + (row & 127)];
-            uint4 o0, o1;
-            constexpr int kB = MOE_MX_CVT == 2 ? 120 : 112;  // the decoders' 2^-b
-            if (MOE_MX_CVT != 0 && code + kB <= 254u) {
-                const uint32_t s2 = pow2_bf16x2(code, kB);
-                uint32_t r[8];
-                if (MOE_MX_CVT == 2) {
-                    e4m3x4_as_bf16x2(v.x, r[0], r[1]);
-                    e4m3x4_as_bf16x2(v.y, r[2], r[3]);
-                    e4m3x4_as_bf16x2(v.z, r[4], r[5]);
-                    e4m3x4_as_bf16x2(v.w, r[6], r[7]);
-                } else {
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    constexpr int kRowsPerIt = WF == kWeightsMxfp8 ? 8 : 16;  // rows a warp covers per iteration
+    constexpr int kIt = kRowsPerWarp / kRowsPerIt;
+    constexpr int kB = (WF == kWeightsMxfp8 && MOE_MX_CVT == 2) ? 120 : 112;  // the decoders' 2^-b
+    // fp8: lane -> row + lane / 4, 16 codes (K 16c .. 16c + 15, c = lane % 4);
+    // fp4: lane -> row + lane / 2, 32 codes (K 32c .. 32c + 31, c = lane % 2)
+    const int c = WF == kWeightsMxfp8 ? (lane & 3) : (lane & 1);
+    const int r_lane = WF == kWeightsMxfp8 ? (lane >> 2) : (lane >> 1);
+    const int sblk = WF == kWeightsMxfp8 ? (c >> 1) : c;  // 32-value scale block of the lane's codes
+    uint32_t code[kIt];
+    bool fast = MOE_MX_CVT != 0;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint32_t h0, h1;
-                        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h0) : "h"((unsigned short)w[i]));
-                        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h1) : "h"((unsigned short)(w[i] >> 16)));
-                        r[2 * i] = f16x2_as_bf16x2_scaled(h0);
-                        r[2 * i + 1] = f16x2_as_bf16x2_scaled(h1);
+    for (int it = 0; it < kIt; ++it) {
+        const int row = cw * kRowsPerWarp + it * kRowsPerIt + r_lane;
+        code[it] = sc[((row >> 7) * 2 + sblk) * M::kScaleStride + (row & 127)];
+        fast = fast && code[it] + kB <= 254u;
+    }
+    if (__all_sync(0xffffffffu, fast)) {
+        constexpr int U = kIt < 4 ? kIt : 4;
+#pragma unroll
+        for (int i0 = 0; i0 < kIt; i0 += U) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int row = cw * kRowsPerWarp + (i0 + u) * kRowsPerIt + r_lane;
+                v[u] = *reinterpret_cast<const uint4 *>(raw + row * M::kRawRow + c * 16);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int row = cw * kRowsPerWarp + (i0 + u) * kRowsPerIt + r_lane;
+                const uint32_t s2 = pow2_bf16x2(code[i0 + u], kB);
+                uint8_t *rp = out + row * 128;
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                if (WF == kWeightsMxfp8) {
+                    uint32_t r[8];
+                    if (MOE_MX_CVT == 2) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) e4m3x4_as_bf16x2(w[i], r[2 * i], r[2 * i + 1]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t h0, h1;
+                            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h0) : "h"((unsigned short)w[i]));
+                            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h1) : "h"((unsigned short)(w[i] >> 16)));
+                            r[2 * i] = f16x2_as_bf16x2_scaled(h0);
+                            r[2 * i + 1] = f16x2_as_bf16x2_scaled(h1);
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) r[i] = bf16x2_mul(r[i], s2);
+                    *reinterpret_cast<uint4 *>(rp + (((2 * c) ^ (row & 7)) << 4)) = make_uint4(r[0], r[1], r[2], r[3]);
+                    *reinterpret_cast<uint4 *>(rp + (((2 * c + 1) ^ (row & 7)) << 4)) =
+                        make_uint4(r[4], r[5], r[6], r[7]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {  // chunk 4c + q: K 32c + 8q .. + 7 = the four bytes of w[q]
+                        uint32_t r[4];
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            uint32_t h;
+                            asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+                                : "=r"(h) : "r"(w[q] >> (8 * b)));
+                            r[b] = bf16x2_mul(f16x2_as_bf16x2_scaled(h), s2);
+                        }
+                        *reinterpret_cast<uint4 *>(rp + (((4 * c + q) ^ (row & 7)) << 4)) =
+                            make_uint4(r[0], r[1], r[2], r[3]);
                     }
                 }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) r[i] = bf16x2_mul(r[i], s2);
-                o0 = make_uint4(r[0], r[1], r[2], r[3]);
-                o1 = make_uint4(r[4], r[5], r[6], r[7]);
-            } else {
-                const float f = e8m0_to_f32(code);
-                o0 = make_uint4(e4m3x2_scaled(v.x, f), e4m3x2_scaled(v.x >> 16, f), e4m3x2_scaled(v.y, f),
-                                e4m3x2_scaled(v.y >> 16, f));
-                o1 = make_uint4(e4m3x2_scaled(v.z, f), e4m3x2_scaled(v.z >> 16, f), e4m3x2_scaled(v.w, f),
-                                e4m3x2_scaled(v.w >> 16, f));
             }
-            uint8_t *rp = out + row * 128;
+        }
+        return;
+    }
+    // some scale of the warp's rows leaves the bf16 multiplier's range (or the fp32
+    // decoder is selected): fp32 products, rounded once to bf16
+#pragma unroll 1
+    for (int it = 0; it < kIt; ++it) {
+        const int row = cw * kRowsPerWarp + it * kRowsPerIt + r_lane;
+        const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * M::kRawRow + c * 16);
+        const float f = e8m0_to_f32(sc[((row >> 7) * 2 + sblk) * M::kScaleStride + (row & 127)]);
+        uint8_t *rp = out + row * 128;
+        if (WF == kWeightsMxfp8) {
+            const uint4 o0 = make_uint4(e4m3x2_scaled(v.x, f), e4m3x2_scaled(v.x >> 16, f), e4m3x2_scaled(v.y, f),
+                                        e4m3x2_scaled(v.y >> 16, f));
+            const uint4 o1 = make_uint4(e4m3x2_scaled(v.z, f), e4m3x2_scaled(v.z >> 16, f), e4m3x2_scaled(v.w, f),
+                                        e4m3x2_scaled(v.w >> 16, f));
             *reinterpret_cast<uint4 *>(rp + (((2 * c) ^ (row & 7)) << 4)) = o0;
             *reinterpret_cast<uint4 *>(rp + (((2 * c + 1) ^ (row & 7)) << 4)) = o1;
-        }
-    } else {
-#pragma unroll 2
-        for (int it = 0; it < kRowsPerWarp / 16; ++it) {
-            const int row = cw * kRowsPerWarp + it * 16 + (lane >> 1), c = lane & 1;  // 32 codes: K 32c..32c+31
-            const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * M::kRawRow + c * 16);
-            const uint32_t code = sc[((row >> 7) * 2 + c) * M::kScaleStride + (row & 127)];
+        } else {
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint8_t *rp = out + row * 128;
-            if (MOE_MX_CVT != 0 && code + 112u <= 254u) {
-                const uint32_t s2 = pow2_bf16x2(code, 112);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {  // chunk 4c + q: K 32c + 8q .. + 7 = the four bytes of w[q]
-                    uint32_t r[4];
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        uint32_t h;
-                        asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-                            : "=r"(h) : "r"(w[q] >> (8 * b)));
-                        r[b] = bf16x2_mul(f16x2_as_bf16x2_scaled(h), s2);
-                    }
-                    *reinterpret_cast<uint4 *>(rp + (((4 * c + q) ^ (row & 7)) << 4)) = make_uint4(r[0], r[1], r[2], r[3]);
-                }
-            } else {
-                const float f = e8m0_to_f32(code);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 o = make_uint4(e2m1x2_scaled(w[q] & 0xffu, f), e2m1x2_scaled((w[q] >> 8) & 0xffu, f),
-                                               e2m1x2_scaled((w[q] >> 16) & 0xffu, f), e2m1x2_scaled(w[q] >> 24, f));
-                    *reinterpret_cast<uint4 *>(rp + (((4 * c + q) ^ (row & 7)) << 4)) = o;
-                }
+            for (int q = 0; q < 4; ++q) {
+                const uint4 o = make_uint4(e2m1x2_scaled(w[q] & 0xffu, f), e2m1x2_scaled((w[q] >> 8) & 0xffu, f),
+                                           e2m1x2_scaled((w[q] >> 16) & 0xffu, f), e2m1x2_scaled(w[q] >> 24, f));
+                *reinterpret_cast<uint4 *>(rp + (((4 * c + q) ^ (row & 7)) << 4)) = o;
             }
         }
     }

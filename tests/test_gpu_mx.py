@@ -184,3 +184,36 @@ def test_mx_full_size_sampled(name):
     tokens = sorted(set([0, T - 1] + np.linspace(0, T - 1, 24).astype(int).tolist()))
     _oracle_check(shape, inputs, Y, tokens=tokens, tag=f"mx_full[{name}]")
     blk.close()
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_mx_scales_outside_the_fast_decoder_range(fmt, path):
+    """Scale codes above 142 (2^15) put the fast decoder's bf16 multiplier
+    2^(scale - 15) out of bf16's normal range, so the converters take the fp32
+    products for those rows; codes near 0 give bf16 subnormal products.  Both
+    decoders must give the exactly decoded weights: bit-identity with the bf16 path
+    on the decoded weights, and the oracle."""
+    shape = SMALL["nano"].replace(name=f"nano_scales_{fmt}", T=64, weight_format=fmt)
+    inputs = wl.make_inputs(shape, "cuda", row_filter=oracle.margin_filter(shape, P.MARGIN))
+    g = torch.Generator().manual_seed(11)
+    # 3 is the smallest code whose products stay exact in bf16 (E4M3's 2^-9 times
+    # 2^-124 is bf16's smallest subnormal)
+    for key, code in (("gate_scale", 145), ("up_scale", 150), ("down_scale", 3)):
+        sc = inputs[key]
+        u = torch.rand(sc.shape, generator=g)
+        sc[(u < 0.02).to(sc.device)] = code
+        sc[(u > 0.99).to(sc.device)] = code + 1
+    blk = capi.block_from_inputs(shape, inputs)
+    blk.set_option(capi.MOE_OPT_PATH, PATHS[path])
+    Y = _forward(blk, inputs["X"])
+    dec = decoded_bf16_inputs(shape, inputs)
+    ref_blk = capi.block_from_inputs(shape.replace(weight_format="bf16"), dec)
+    ref_blk.set_option(capi.MOE_OPT_PATH, PATHS[path])
+    ref_blk.set_option(capi.MOE_OPT_GEMM_PAIR, 0)
+    Yb = _forward(ref_blk, dec["X"])
+    assert torch.isfinite(Y.float()).all()
+    assert torch.equal(Y, Yb), "MX path differs from the bf16 path on the decoded weights"
+    _oracle_check(shape, inputs, Y, tag=f"mx_scales[{fmt},{path}]")
+    ref_blk.close()
+    blk.close()
