@@ -396,8 +396,17 @@ def cpu_baseline(shape, inputs, budget_s=10.0):
         if time.perf_counter() - t_start > 3 * budget_s:
             break
     med = statistics.median(times)
+    # the same oracle on one thread, on a smaller token sample (about budget_s / 3)
+    n1 = max(1, min(shape.T, int(budget_s / 9 / max(per_tok * min(shape.T, cores), 1e-9))))
+    t1 = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        oracle.block_output(shape, host, tokens=list(range(n1)), nthreads=1)
+        t1.append(time.perf_counter() - t0)
     return {"value": round(n / med, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"tokens 0..{n - 1} of the {shape.name} workload, {len(times)} passes, median"}
+            "sample": f"tokens 0..{n - 1} of the {shape.name} workload, {len(times)} passes, median",
+            "one_thread": {"value": round(n1 / statistics.median(t1), 2), "unit": "tokens/s",
+                           "sample": f"tokens 0..{n1 - 1}, 3 passes, median"}}
 
 
 def run_reference(args, shape):
