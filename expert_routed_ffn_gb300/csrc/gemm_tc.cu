@@ -650,21 +650,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 // Every k-block moves about 130 KB through shared memory (codes in and out, the
 // bf16 B tile in and out, the A tile in and out), which bounds this design at
 // roughly one k-block per 1000 cycles.
-template <int WF>
+//
+// CTA pairs (PAIR): 256-row tiles, rank 0 issues tcgen05.mma.cta_group::2; each CTA
+// streams and decodes its 128 weight rows and loads its 128 A rows (completing on
+// rank 0's barrier).  Bit-identical to the bf16 pair kernel on the decoded weights,
+// but measured slower than one CTA per tile (AFMoE MXFP8 prefill expert GEMM 1028
+// against 758 us), so it runs only when asked for.
+template <int WF, bool PAIR = false>
 struct MxCfg {
+    // B rows a CTA converts per k-block: all 256 of the tile, or its half of a CTA pair's
+    static constexpr int kBRows = PAIR ? kGemmBN / 2 : kGemmBN;
     static constexpr int kRawRow = WF == kWeightsMxfp8 ? kGemmBK : kGemmBK / 2;  // bytes of a row's k-block
-    static constexpr int kRawCodes = kGemmBN * kRawRow;                         // 16 KB / 8 KB
+    static constexpr int kRawCodes = kBRows * kRawRow;                          // 16 KB / 8 KB (halved in a pair)
     // scales [row half][32-value block][128 rows]: every copy lands 128-byte aligned, as a
     // tensor copy's shared-memory destination must
     static constexpr int kScaleStride = 128;
-    static constexpr int kScaleBytes = 4 * kScaleStride;
+    static constexpr int kScaleBytes = (kBRows / 128) * 2 * kScaleStride;
     static constexpr int kRawStage = kRawCodes + kScaleBytes;
     // ring depths measured on GB300 (Nano decode and AFMoE prefill, MXFP8 and MXFP4):
-    // three converted B stages beat two by 2-4%; deeper A or raw rings change nothing
-    static constexpr int kRawStages = WF == kWeightsMxfp8 ? 4 : 6;
-    static constexpr int kAStages = 3;
-    static constexpr int kBStages = 3;
-    static constexpr int kBBytes = kGemmBN * kGemmBK * 2;  // converted B tile, 32 KB
+    // three converted B stages beat two by 2-4%; deeper A or raw rings change nothing.
+    // A pair's stages are half as large (B) and the MMA waits on both CTAs: 4 of each.
+    static constexpr int kRawStages = PAIR ? (WF == kWeightsMxfp8 ? 6 : 8) : (WF == kWeightsMxfp8 ? 4 : 6);
+    static constexpr int kAStages = PAIR ? 4 : 3;
+    static constexpr int kBStages = PAIR ? 4 : 3;
+    static constexpr int kBBytes = kBRows * kGemmBK * 2;  // converted B tile, 32 KB (16 KB in a pair)
     static constexpr int kBarBytes = 1024;
     static constexpr int kSmemBytes =
         kBStages * kBBytes + kAStages * kABytes + kRawStages * kRawStage + 1024 /*align*/ + kBarBytes;
@@ -740,8 +749,8 @@ __device__ __forceinline__ void e4m3x4_as_bf16x2(uint32_t w, uint32_t &lo, uint3
 #define MOE_MX_CVT 1
 #endif
 
-// Converter warp cw (of kConvWarps): rows [cw * 256 / kConvWarps, + 256 / kConvWarps)
-// of one raw k-block -> bf16 B
+// Converter warp cw (of kConvWarps): rows [cw * kRows / kConvWarps, + kRows / kConvWarps)
+// of one raw k-block (kRows = 256, or 128 in a CTA pair) -> bf16 B
 // tile.  Row r's 16-byte chunk j (K values 8j..8j+7) goes to r * 128 + ((j ^ (r % 8))
 // * 16): the 128-byte swizzle of a 1024-byte-aligned tile.  Lanes read consecutive
 // 16-byte pieces of the raw rows and store chunks of 8 distinct swizzle positions
@@ -749,10 +758,10 @@ __device__ __forceinline__ void e4m3x4_as_bf16x2(uint32_t w, uint32_t &lo, uint3
 // warp's rows are read first: when all of them allow the bf16 multiplier (the usual
 // case) the loop has no per-row branch and its code loads are issued together
 // (measured: 0.35 against 0.58 us per k-block for eight warps with the branch).
-template <int WF>
+template <int WF, int kRows>
 __device__ __forceinline__ void mx_convert(const uint8_t *raw, const uint8_t *sc, uint8_t *out, int cw, int lane) {
     using M = MxCfg<WF>;
-    constexpr int kRowsPerWarp = kGemmBN / M::kConvWarps;
+    constexpr int kRowsPerWarp = kRows / M::kConvWarps;
     static_assert(kRowsPerWarp % 16 == 0, "converter rows");
     constexpr int kRowsPerIt = WF == kWeightsMxfp8 ? 8 : 16;  // rows a warp covers per iteration
     constexpr int kIt = kRowsPerWarp / kRowsPerIt;
@@ -852,14 +861,16 @@ __device__ __forceinline__ void mx_convert(const uint8_t *raw, const uint8_t *sc
     }
 }
 
-template <int WF>
+template <int WF, bool PAIR>
 __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const __grid_constant__ GemmArgs p) {
-    using M = MxCfg<WF>;
+    using M = MxCfg<WF, PAIR>;
     constexpr int R = M::kRawStages, RA = M::kAStages, P = M::kBStages, NCW = M::kConvWarps;
+    constexpr int kBM = PAIR ? 2 * kGemmBM : kGemmBM;  // rows per tile (128 per CTA)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    // converted B stages (32 KB), A stages (16 KB; both 1024-byte aligned), raw stages, barriers
+    // converted B stages (32 KB, 16 KB in a pair), A stages (16 KB; both 1024-byte aligned),
+    // raw stages, barriers
     auto opB = [&](int s) { return smem + s * M::kBBytes; };
     auto opA = [&](int s) { return smem + P * M::kBBytes + s * kABytes; };
     uint8_t *const raw0 = smem + P * M::kBBytes + RA * kABytes;
@@ -881,13 +892,26 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
     auto op_full = [&](int s) { return bar0 + 8u * (kB0 + 2 * R + 2 * RA + s); };
     auto op_empty = [&](int s) { return bar0 + 8u * (kB0 + 2 * R + 2 * RA + P + s); };
     const uint32_t drain_bar = bar0 + 8u * (kB0 + 2 * R + 2 * RA + 2 * P);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kB0 + 2 * R + 2 * RA + 2 * P + 1);
+    // CTA pair: this CTA's converter warps arrive on op_conv; rank 1 relays its completed
+    // k-blocks with one cluster-scope arrival each on rank 0's op_full
+    auto op_conv = [&](int s) { return bar0 + 8u * (kB0 + 2 * R + 2 * RA + 2 * P + 1 + s); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kB0 + 2 * R + 2 * RA + 3 * P + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *ring = reinterpret_cast<volatile int *>(tmem_slot + 2);  // [kRing] tile ids
-    static_assert(8 * (kB0 + 2 * R + 2 * RA + 2 * P + 1) + 8 + 4 * kRing <= M::kBarBytes, "barrier block");
+    static_assert(8 * (kB0 + 2 * R + 2 * RA + 3 * P + 1) + 8 + 4 * kRing <= M::kBarBytes, "barrier block");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    auto abort_all = [&]() { raise_abort(p.err, abort_flag); };
+    // CTA pair: rank 0 issues the MMAs (M = 256: 128 A rows in each CTA, B split along N,
+    // each CTA converting its half); its A-full, converted-B-full and accumulator-empty
+    // barriers count both CTAs
+    const int half = PAIR ? (int)cluster_ctarank() : 0;
+    const bool leader = half == 0;
+    auto abort_all = [&]() {
+        if (PAIR)
+            raise_abort_pair(p.err, abort_flag);
+        else
+            raise_abort(p.err, abort_flag);
+    };
     trace_mark(p.trace, 0);
     if (threadIdx.x == 0) {
         for (int i = 0; i < kRing; ++i) {
@@ -896,7 +920,7 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
         }
         for (uint32_t a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), kEpiThreads);
+            mbar_init(tempty_bar(a), PAIR ? 2 * kEpiThreads : kEpiThreads);
         }
         for (int s = 0; s < R; ++s) {
             mbar_init(raw_full(s), 1);
@@ -907,8 +931,9 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
             mbar_init(a_empty(s), 1);  // the MMA's commit
         }
         for (int s = 0; s < P; ++s) {
-            mbar_init(op_full(s), NCW);  // each converter warp
-            mbar_init(op_empty(s), 1);   // the MMA's commit
+            mbar_init(op_full(s), PAIR ? 1 : NCW);  // each converter warp, or rank 1's relay
+            mbar_init(op_empty(s), 1);              // the MMA's commit
+            mbar_init(op_conv(s), NCW);             // each converter warp (CTA pair)
         }
         mbar_init(drain_bar, 1);
         fence_mbar_init();
@@ -917,11 +942,17 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
     if (warp == 0 && lane == 0)
         for (int m = 0; m < kGemmMaxMaps; ++m) tma_prefetch_desc(&p.maps[m]);
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // both CTAs' barriers exist before any copy or arrival crosses over
     tc_fence_after();
     pdl_wait();
     trace_mark(p.trace, 1);
@@ -942,7 +973,7 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
     if (threadIdx.x == 0) {
         int run = 0;
         for (int s = 0; s < p.num_segs; ++s) {
-            run += seg_tiles<kGemmBM>(p.seg[s], s_toffs);
+            run += seg_tiles<kBM>(p.seg[s], s_toffs);
             s_seg_end[s] = run;
         }
     }
@@ -956,8 +987,11 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
             uint32_t L = 0;
             bool ok = true;
             uint64_t w_empty = 0;
-            const bool dyn = p.tile_counter != nullptr;
-            int next = dyn ? atomicAdd(p.tile_counter, 1) : (int)blockIdx.x;
+            // tiles: from the launch-wide ticket, or round-robin (both CTAs of a pair
+            // take the same sequence)
+            const bool dyn = !PAIR && p.tile_counter != nullptr;
+            const int stride = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
+            int next = dyn ? atomicAdd(p.tile_counter, 1) : (PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x);
             for (int n = 0;; ++n) {
                 const int tile = next < total ? next : total;
                 const int slot = n % kRing;
@@ -968,19 +1002,22 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                 ring[slot] = tile;
                 mbar_arrive(ring_full(slot));
                 if (tile >= total) break;
-                const Tile t = decode_tile<kGemmBM>(p, tile, s_seg_end, s_offs, s_toffs, 0);
+                const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
                 const GemmSegment &sg = p.seg[t.seg];
                 const int g = sg.group_base + t.group;
                 const int claim_at = sg.k_blocks > 3 ? sg.k_blocks - 3 : 0;
                 // rows of the tile's two 128-row halves: gate and up rows of n-tile nt, or
-                // the 256 rows of a down tile
-                const int r0 = sg.glu ? t.nt * 128 : t.nt * kGemmBN, r1 = sg.glu ? r0 : r0 + 128;
-                const CUtensorMap *mC0 = &p.maps[sg.map_b0], *mC1 = &p.maps[sg.glu ? sg.map_b1 : sg.map_b0];
-                const CUtensorMap *mS0 = &p.maps[sg.map_s0], *mS1 = &p.maps[sg.glu ? sg.map_s1 : sg.map_s0];
+                // the 256 rows of a down tile; a CTA of a pair loads its half only (gate
+                // rows in rank 0, up rows in rank 1: accumulator columns 0-127 / 128-255)
+                const int r0 = sg.glu ? t.nt * 128 : t.nt * kGemmBN + half * 128, r1 = sg.glu ? r0 : r0 + 128;
+                const CUtensorMap *mC0 = &p.maps[(sg.glu && half) ? sg.map_b1 : sg.map_b0],
+                                  *mC1 = &p.maps[sg.glu ? sg.map_b1 : sg.map_b0];
+                const CUtensorMap *mS0 = &p.maps[(sg.glu && half) ? sg.map_s1 : sg.map_s0],
+                                  *mS1 = &p.maps[sg.glu ? sg.map_s1 : sg.map_s0];
                 for (int kb = 0; kb < sg.k_blocks; ++kb) {
                     const int s = L % R;
                     const uint32_t ph = (L / R) & 1u;
-                    if (kb == claim_at) next = dyn ? atomicAdd(p.tile_counter, 1) : tile + (int)gridDim.x;
+                    if (kb == claim_at) next = dyn ? atomicAdd(p.tile_counter, 1) : tile + stride;
                     const uint64_t t0 = stats ? global_timer_ns() : 0;
                     if (!mbar_wait(raw_empty(s), ph ^ 1u, p.wait_ns, abort_flag)) {
                         ok = false;
@@ -992,9 +1029,11 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                     const uint32_t dst = smem_u32(rawS(s));
                     mbar_arrive_expect_tx(raw_full(s), M::kRawStage);
                     tma_load_3d(dst, mC0, raw_full(s), xb, r0, g);
-                    tma_load_3d(dst + 128 * M::kRawRow, mC1, raw_full(s), xb, r1, g);
                     tma_load_3d(dst + M::kRawCodes, mS0, raw_full(s), r0, kx / 32, g);
-                    tma_load_3d(dst + M::kRawCodes + 2 * M::kScaleStride, mS1, raw_full(s), r1, kx / 32, g);
+                    if (!PAIR) {
+                        tma_load_3d(dst + 128 * M::kRawRow, mC1, raw_full(s), xb, r1, g);
+                        tma_load_3d(dst + M::kRawCodes + 2 * M::kScaleStride, mS1, raw_full(s), r1, kx / 32, g);
+                    }
                     ++L;
                 }
                 if (!ok) break;
@@ -1023,7 +1062,7 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                 const int tile = ring[slot];
                 mbar_arrive(ring_empty(slot));
                 if (tile >= total) break;
-                const Tile t = decode_tile<kGemmBM>(p, tile, s_seg_end, s_offs, s_toffs, 0);
+                const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
                 const GemmSegment &sg = p.seg[t.seg];
                 if (sg.wait != nullptr) {  // A rows written earlier in this launch
                     const uint64_t t0 = stats ? global_timer_ns() : 0;
@@ -1043,8 +1082,15 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                         break;
                     }
                     const int kx = (sg.k_base + t.ks * sg.k_blocks + kb) * kGemmBK;
-                    mbar_arrive_expect_tx(a_full(s), kABytes);
-                    tma_load_2d(smem_u32(opA(s)), mA, a_full(s), kx, t.row0);
+                    if (PAIR) {
+                        // both CTAs' A rows complete on rank 0's barrier, which expects both
+                        const uint32_t fb = mapa_shared(a_full(s), 0);
+                        if (leader) mbar_arrive_expect_tx(a_full(s), 2 * kABytes);
+                        tma_load_2d_pair(smem_u32(opA(s)), mA, fb, kx, t.row0);
+                    } else {
+                        mbar_arrive_expect_tx(a_full(s), kABytes);
+                        tma_load_2d(smem_u32(opA(s)), mA, a_full(s), kx, t.row0);
+                    }
                     ++L;
                 }
                 if (!ok) break;
@@ -1052,9 +1098,16 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
             if (stats) atomicAdd(stats + 1, (unsigned long long)w_dep);
             if (!ok) {
                 abort_all();
-                for (uint32_t i = 0; i < (uint32_t)RA && i < L; ++i) {  // copies still in flight
-                    const uint32_t l = L - 1 - i;
-                    mbar_wait(a_full(l % RA), (l / RA) & 1u, kDrainNs, nullptr);
+                if (PAIR) {
+                    // the copies complete on rank 0's barrier together with the other CTA's,
+                    // which may never be issued after an abort: wait a fixed time instead
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < kPairDrainNs) __nanosleep(1000);
+                } else {
+                    for (uint32_t i = 0; i < (uint32_t)RA && i < L; ++i) {  // copies still in flight
+                        const uint32_t l = L - 1 - i;
+                        mbar_wait(a_full(l % RA), (l / RA) & 1u, kDrainNs, nullptr);
+                    }
                 }
             }
         }
@@ -1074,7 +1127,7 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
             __syncwarp();
             if (lane == 0) mbar_arrive(ring_empty(slot));
             if (tile >= total) break;
-            const Tile t = decode_tile<kGemmBM>(p, tile, s_seg_end, s_offs, s_toffs, 0);
+            const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
             const int kbs = p.seg[t.seg].k_blocks;
             for (int kb = 0; kb < kbs; ++kb) {
                 const int rs = L % R, os = L % P;
@@ -1085,20 +1138,43 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                     ok = false;
                     break;
                 }
-                mx_convert<WF>(rawS(rs), rawS(rs) + M::kRawCodes, opB(os), cw, lane);
+                mx_convert<WF, M::kBRows>(rawS(rs), rawS(rs) + M::kRawCodes, opB(os), cw, lane);
                 fence_proxy_async_smem();  // the generic-proxy stores, before the MMA (async proxy) reads them
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(raw_empty(rs));
-                    mbar_arrive(op_full(os));
+                    mbar_arrive(PAIR ? op_conv(os) : op_full(os));
                 }
                 ++L;
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(kGemmBM, kGemmBN);
+        if (PAIR && !leader && lane == 0) {
+            // rank 1 issues no MMA: it relays each k-block its converters completed to rank 0
+            // with one cluster-scope release (measured, AFMoE MXFP8 prefill: 1095 us against
+            // 1312 us when each converter warp arrives on rank 0's barrier itself)
+            uint32_t L = 0;
+            bool ok = true;
+            for (int n = 0; ok; ++n) {
+                const int slot = n % kRing;
+                if (!mbar_wait(ring_full(slot), (n / kRing) & 1u, p.wait_ns, abort_flag)) break;
+                const int tile = ring[slot];
+                mbar_arrive(ring_empty(slot));
+                if (tile >= total) break;
+                const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
+                for (int kb = 0; kb < p.seg[t.seg].k_blocks; ++kb, ++L) {
+                    const int sb = L % P;
+                    if (!mbar_wait(op_conv(sb), (L / P) & 1u, p.wait_ns, abort_flag)) {
+                        abort_all();
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_cluster(mapa_shared(op_full(sb), 0));
+                }
+            }
+        } else if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * kGemmBM : kGemmBM, kGemmBN);
             uint32_t L = 0, n_acc = 0;
             bool ok = true, issued = false;
             uint64_t w_full = 0, w_acc = 0;
@@ -1111,11 +1187,12 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                 const int tile = ring[slot];
                 mbar_arrive(ring_empty(slot));
                 if (tile >= total) break;
-                const Tile t = decode_tile<kGemmBM>(p, tile, s_seg_end, s_offs, s_toffs, 0);
+                const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
                 const GemmSegment &sg = p.seg[t.seg];
                 const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
                 const uint64_t t0 = stats ? global_timer_ns() : 0;
-                if (!mbar_wait(tempty_bar(a), aph ^ 1u, p.wait_ns, abort_flag)) {
+                if (!(PAIR ? mbar_wait_cluster(tempty_bar(a), aph ^ 1u, p.wait_ns, abort_flag)
+                           : mbar_wait(tempty_bar(a), aph ^ 1u, p.wait_ns, abort_flag))) {
                     ok = false;
                     break;
                 }
@@ -1125,8 +1202,12 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                 for (int kb = 0; kb < sg.k_blocks; ++kb) {
                     const int sa = L % RA, sb = L % P;
                     const uint64_t t1 = stats ? global_timer_ns() : 0;
+                    // (a pair: this CTA's converted half, then rank 1's relayed completion,
+                    // with a cluster-scope acquire)
                     if (!mbar_wait(a_full(sa), (L / RA) & 1u, p.wait_ns, abort_flag) ||
-                        !mbar_wait(op_full(sb), (L / P) & 1u, p.wait_ns, abort_flag)) {
+                        !(PAIR ? mbar_wait(op_conv(sb), (L / P) & 1u, p.wait_ns, abort_flag) &&
+                                     mbar_wait_cluster(op_full(sb), (L / P) & 1u, p.wait_ns, abort_flag)
+                               : mbar_wait(op_full(sb), (L / P) & 1u, p.wait_ns, abort_flag))) {
                         ok = false;
                         break;
                     }
@@ -1135,15 +1216,28 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                     const uint64_t ad = smem_desc_k128(smem_u32(opA(sa)));
                     const uint64_t bd = smem_desc_k128(smem_u32(opB(sb)));
 #pragma unroll
-                    for (int kk = 0; kk < kGemmBK / 16; ++kk)
-                        tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    for (int kk = 0; kk < kGemmBK / 16; ++kk) {
+                        if (PAIR)
+                            tc_mma_bf16_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                        else
+                            tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    }
                     issued = true;
-                    tc_commit(a_empty(sa));
-                    tc_commit(op_empty(sb));
+                    // frees the stages (in both CTAs of a pair) once these MMAs have read them
+                    if (PAIR) {
+                        tc_commit_pair(a_empty(sa), 3);
+                        tc_commit_pair(op_empty(sb), 3);
+                    } else {
+                        tc_commit(a_empty(sa));
+                        tc_commit(op_empty(sb));
+                    }
                     ++L;
                 }
                 if (!ok) break;
-                tc_commit(tfull_bar(a));
+                if (PAIR)  // accumulator complete, in both CTAs' TMEM
+                    tc_commit_pair(tfull_bar(a), 3);
+                else
+                    tc_commit(tfull_bar(a));
                 ++n_acc;
             }
             if (stats) {
@@ -1154,7 +1248,10 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
             if (!ok) {
                 abort_all();
                 if (issued) {
-                    tc_commit(drain_bar);
+                    if (PAIR)
+                        tc_commit_pair(drain_bar, 1);
+                    else
+                        tc_commit(drain_bar);
                     mbar_wait(drain_bar, 0, kDrainNs, nullptr);
                 }
             }
@@ -1162,18 +1259,22 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
     } else {
         // ----------------------------------------------------------- epilogue
         EpiCtx c{ring_full(0), ring_empty(0), tfull_bar(0), tempty_bar(0), ring, abort_flag, tmem_base, total,
-                 s_seg_end, s_offs, s_toffs, 0};
-        epilogue_role<false, kGemmBM>(p, c, warp, lane);
+                 s_seg_end, s_offs, s_toffs, half};
+        epilogue_role<PAIR, kBM>(p, c, warp, lane);
     }
 
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // neither CTA leaves while the other may still reach its memory
     trace_exit(p.trace);
     if (stats && threadIdx.x == 0) atomicAdd(stats + 6, (unsigned long long)(global_timer_ns() - t_ready));
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -1288,17 +1389,31 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
                              GemmCfg<false>::kSmemBytes);
         cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              GemmCfg<true>::kSmemBytes);
-        cudaFuncSetAttribute(gemm_mx_kernel<kWeightsMxfp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(gemm_mx_kernel<kWeightsMxfp8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              MxCfg<kWeightsMxfp8>::kSmemBytes);
-        cudaFuncSetAttribute(gemm_mx_kernel<kWeightsMxfp4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(gemm_mx_kernel<kWeightsMxfp4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              MxCfg<kWeightsMxfp4>::kSmemBytes);
+        cudaFuncSetAttribute(gemm_mx_kernel<kWeightsMxfp8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             MxCfg<kWeightsMxfp8, true>::kSmemBytes);
+        cudaFuncSetAttribute(gemm_mx_kernel<kWeightsMxfp4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             MxCfg<kWeightsMxfp4, true>::kSmemBytes);
     });
     if (a.wfmt == kWeightsMxfp8 || a.wfmt == kWeightsMxfp4) {
-        if (a.pair) return cudaErrorInvalidValue;  // MX weights run on single CTAs
-        if (a.wfmt == kWeightsMxfp8)
-            return launch_pdl(gemm_mx_kernel<kWeightsMxfp8>, dim3(a.num_ctas), dim3(MxCfg<kWeightsMxfp8>::kThreads),
-                              (size_t)MxCfg<kWeightsMxfp8>::kSmemBytes, s, a);
-        return launch_pdl(gemm_mx_kernel<kWeightsMxfp4>, dim3(a.num_ctas), dim3(MxCfg<kWeightsMxfp4>::kThreads),
+        const bool f8 = a.wfmt == kWeightsMxfp8;
+        if (a.pair) {
+            if (a.num_ctas < 2 || (a.num_ctas & 1) || a.tile_counter != nullptr) return cudaErrorInvalidValue;
+            if (f8)
+                return launch_pdl_cluster(gemm_mx_kernel<kWeightsMxfp8, true>, dim3(a.num_ctas),
+                                          dim3(MxCfg<kWeightsMxfp8>::kThreads),
+                                          (size_t)MxCfg<kWeightsMxfp8, true>::kSmemBytes, s, dim3(2, 1, 1), a);
+            return launch_pdl_cluster(gemm_mx_kernel<kWeightsMxfp4, true>, dim3(a.num_ctas),
+                                      dim3(MxCfg<kWeightsMxfp4>::kThreads),
+                                      (size_t)MxCfg<kWeightsMxfp4, true>::kSmemBytes, s, dim3(2, 1, 1), a);
+        }
+        if (f8)
+            return launch_pdl(gemm_mx_kernel<kWeightsMxfp8, false>, dim3(a.num_ctas),
+                              dim3(MxCfg<kWeightsMxfp8>::kThreads), (size_t)MxCfg<kWeightsMxfp8>::kSmemBytes, s, a);
+        return launch_pdl(gemm_mx_kernel<kWeightsMxfp4, false>, dim3(a.num_ctas), dim3(MxCfg<kWeightsMxfp4>::kThreads),
                           (size_t)MxCfg<kWeightsMxfp4>::kSmemBytes, s, a);
     }
     if (a.wfmt != kWeightsBf16) return cudaErrorInvalidValue;

@@ -603,18 +603,20 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     g.limit = h->cfg.act_limit;
     g.beta = h->cfg.act_beta;
     // CTA pairs: an even grid, static tile order, down weights in 128-row boxes
-    // (each CTA of a pair loads half of a 256-row tile)
+    // (each CTA of a pair loads half of a 256-row tile); the bf16 kernel's pair stages
+    // hold two k-blocks (maps with two-k-block boxes), the MX kernel's one
     const bool pair = h->pair_now;
+    const bool kb2 = pair && !mx;
     g.pair = pair ? 1 : 0;
     g.num_ctas = pair ? h->num_sms / 2 * 2 : h->num_sms;
     // unused slots hold a valid descriptor (a dense layer has only the shared ones)
     for (auto &m : g.maps) m = h->dense ? h->m_hs : h->m_xsorted;
     if (!h->dense) {
-        g.maps[kXs] = pair ? h->m_xs2 : h->m_xsorted;
-        g.maps[kHb] = pair ? h->m_hb2 : h->m_hbuf;
-        g.maps[kG] = pair ? h->m_gate2 : h->m_gate;
-        g.maps[kU] = pair ? h->m_up2 : h->m_up;
-        g.maps[kD] = pair ? h->m_down2 : h->m_down;
+        g.maps[kXs] = kb2 ? h->m_xs2 : h->m_xsorted;
+        g.maps[kHb] = kb2 ? h->m_hb2 : h->m_hbuf;
+        g.maps[kG] = kb2 ? h->m_gate2 : h->m_gate;
+        g.maps[kU] = kb2 ? h->m_up2 : h->m_up;
+        g.maps[kD] = kb2 ? h->m_down2 : h->m_down;
         if (mx) {
             g.maps[kGs] = h->m_gate_s;
             g.maps[kUs] = h->m_up_s;
@@ -623,8 +625,8 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     }
     if (h->has_shared) {
         if (h->x_f32) {
-            g.maps[kX] = pair ? h->m_xbf2 : h->m_xbf16;
-        } else if (pair) {
+            g.maps[kX] = kb2 ? h->m_xbf2 : h->m_xbf16;
+        } else if (kb2) {
             if (h->m_x2_ptr != X || h->m_x2_rows != T) {
                 CUresult r = moe::encode_map_a_kb2(&h->m_x2, X, T, H);
                 if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(X) failed: %d", (int)r);
@@ -637,10 +639,10 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
             if (st != MOE_OK) return st;
             g.maps[kX] = h->m_x;
         }
-        g.maps[kHs] = pair ? h->m_hs2 : h->m_hs;
-        g.maps[kSG] = pair ? h->m_shg2 : h->m_shg;
-        g.maps[kSU] = pair ? h->m_shu2 : h->m_shu;
-        g.maps[kSD] = pair ? h->m_shd2 : h->m_shd;
+        g.maps[kHs] = kb2 ? h->m_hs2 : h->m_hs;
+        g.maps[kSG] = kb2 ? h->m_shg2 : h->m_shg;
+        g.maps[kSU] = kb2 ? h->m_shu2 : h->m_shu;
+        g.maps[kSD] = kb2 ? h->m_shd2 : h->m_shd;
         if (mx) {
             g.maps[kSGs] = h->m_shg_s;
             g.maps[kSUs] = h->m_shu_s;
@@ -887,8 +889,10 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     }
     // CTA pairs once the weight tiles are reused by 256 rows on average (a dense
     // layer: T >= 256)
-    h->pair_now = path == kPathGrouped && h->num_sms >= 2 && h->wfmt == MOE_WEIGHTS_BF16 &&
-                  (h->pair_opt == 1 || (h->pair_opt == 2 && (h->dense ? T >= 256 : slots >= 256ll * h->E)));
+    // (MX weights: only when asked; measured slower than one CTA per tile, see the MX kernel)
+    h->pair_now = path == kPathGrouped && h->num_sms >= 2 &&
+                  (h->pair_opt == 1 || (h->pair_opt == 2 && h->wfmt == MOE_WEIGHTS_BF16 &&
+                                        (h->dense ? T >= 256 : slots >= 256ll * h->E)));
     h->shared_parts = path == kPathGrouped && h->has_shared ? shared_parts(h, T) : 1;
     mark(h, 0, s);
     moe_status st = MOE_OK;

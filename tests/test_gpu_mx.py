@@ -10,11 +10,11 @@ activations stay bf16.  Checks:
     with the bf16 tolerance (decoding is exact, so the arithmetic is the bf16
     path's);
   * bit-for-bit against the bf16 path on the decoded weights: both MX GEMMs (the
-    grouped one, tokens as M, and the swapped one, weights decoded into tensor
-    memory as M) issue the same tcgen05 MMAs on the same operand values in the same
-    order as their bf16 counterparts, so Y must be identical, which pins the
-    decoders (byte and nibble order, scale index, operand layouts) independently of
-    any tolerance;
+    grouped one, tokens as M, on one CTA or on CTA pairs, and the swapped one,
+    weights decoded into tensor memory as M) issue the same tcgen05 MMAs on the same
+    operand values in the same order as their bf16 counterparts, so Y must be
+    identical, which pins the decoders (byte and nibble order, scale index, operand
+    layouts, the pair's halves) independently of any tolerance;
   * the options the MX path refuses.
 """
 
@@ -100,55 +100,64 @@ FORMATS = ["mxfp8", "mxfp4"]
 
 
 PATHS = {"grouped": capi.PATH_GROUPED, "swapped": capi.PATH_SWAPPED}
+# GEMM variants: (path, MOE_OPT_GEMM_PAIR)
+GEMMS = {"grouped": (capi.PATH_GROUPED, 0), "grouped_pairs": (capi.PATH_GROUPED, 1),
+         "swapped": (capi.PATH_SWAPPED, 0)}
 
 
-@pytest.mark.parametrize("path", list(PATHS))
+@pytest.mark.parametrize("gemm", list(GEMMS))
 @pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("name", list(SMALL))
-def test_mx_small_every_token(name, fmt, path):
+def test_mx_small_every_token(name, fmt, gemm):
     shape = SMALL[name].replace(name=f"{SMALL[name].name}_{fmt}", weight_format=fmt)
+    path, pair = GEMMS[gemm]
     inputs, blk = P.make_case(shape)
+    blk.set_option(capi.MOE_OPT_GEMM_PAIR, pair)
     if shape.E > 0:
-        blk.set_option(capi.MOE_OPT_PATH, PATHS[path])
-    elif path == "swapped":
+        blk.set_option(capi.MOE_OPT_PATH, path)
+    elif path == capi.PATH_SWAPPED:
         pytest.skip("a dense layer runs on the grouped GEMM only")
     Y = _forward(blk, inputs["X"])
     if shape.E > 0 and shape.mlp_norm == "none":
         idx, w = (blk.inspect(b, shape.T * shape.k, dt).view(shape.T, shape.k).cpu().numpy()
                   for b, dt in ((capi.MOE_BUF_TOPK_IDX, torch.int32), (capi.MOE_BUF_TOPK_W, torch.float32)))
         P.check_route(shape, P.host_inputs(inputs), idx, w)
-    _oracle_check(shape, inputs, Y, tag=f"mx_small[{name},{fmt}]")
+    _oracle_check(shape, inputs, Y, tag=f"mx_small[{name},{fmt},{gemm}]")
     blk.close()
 
 
-@pytest.mark.parametrize("path", list(PATHS))
+@pytest.mark.parametrize("gemm", list(GEMMS))
 @pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("name", ["nano", "m3_small_packed", "afmoe_ragged", "dense_small", "nano_T1"])
-def test_mx_bit_identical_to_bf16_path_on_decoded_weights(name, fmt, path):
+def test_mx_bit_identical_to_bf16_path_on_decoded_weights(name, fmt, gemm):
     shape = SMALL[name].replace(name=f"{SMALL[name].name}_{fmt}", weight_format=fmt)
-    if shape.E == 0 and path == "swapped":
+    path, pair = GEMMS[gemm]
+    if shape.E == 0 and path == capi.PATH_SWAPPED:
         pytest.skip("a dense layer runs on the grouped GEMM only")
     inputs, blk = P.make_case(shape)
     if shape.E > 0:
-        blk.set_option(capi.MOE_OPT_PATH, PATHS[path])
+        blk.set_option(capi.MOE_OPT_PATH, path)
+    blk.set_option(capi.MOE_OPT_GEMM_PAIR, pair)
     Y = _forward(blk, inputs["X"])
     dec = decoded_bf16_inputs(shape, inputs)
     bshape = shape.replace(weight_format="bf16")
     ref_blk = capi.block_from_inputs(bshape, dec)
     if shape.E > 0:
-        ref_blk.set_option(capi.MOE_OPT_PATH, PATHS[path])
-    ref_blk.set_option(capi.MOE_OPT_GEMM_PAIR, 0)  # the MX GEMMs run one CTA per tile
+        ref_blk.set_option(capi.MOE_OPT_PATH, path)
+    ref_blk.set_option(capi.MOE_OPT_GEMM_PAIR, pair)  # the same tile shape and MMAs
     Yb = _forward(ref_blk, dec["X"])
     assert torch.equal(Y, Yb), "MX path differs from the bf16 path on the decoded weights"
     ref_blk.close()
     blk.close()
 
 
+@pytest.mark.parametrize("pair", [0, 1])
 @pytest.mark.parametrize("fmt", FORMATS)
-def test_mx_two_launches_and_repeat_are_bit_identical(fmt):
+def test_mx_two_launches_and_repeat_are_bit_identical(fmt, pair):
     shape = wl.NANO_DECODE.replace(name=f"nano_{fmt}", T=200, weight_format=fmt)
     inputs, blk = P.make_case(shape)
     blk.set_option(capi.MOE_OPT_PATH, capi.PATH_GROUPED)  # the fused launch is the grouped kernel's
+    blk.set_option(capi.MOE_OPT_GEMM_PAIR, pair)
     Y1 = _forward(blk, inputs["X"]).clone()
     Y2 = _forward(blk, inputs["X"]).clone()
     blk.set_option(capi.MOE_OPT_FUSE_EXPERTS, 0)
@@ -164,7 +173,7 @@ def test_mx_refuses_other_paths():
         blk.set_option(capi.MOE_OPT_PATH, capi.PATH_DECODE)
     assert ei.value.status == capi.MOE_ERR_UNSUPPORTED
     blk.set_option(capi.MOE_OPT_PATH, capi.PATH_GROUPED)
-    blk.set_option(capi.MOE_OPT_GEMM_PAIR, 1)  # no effect: the MX GEMM has no CTA-pair variant
+    blk.set_option(capi.MOE_OPT_GEMM_PAIR, 1)  # CTA pairs at a decode size (T = 16)
     _oracle_check(shape, inputs, _forward(blk, inputs["X"]), tag="mx_pair_opt")
     blk.close()
 
