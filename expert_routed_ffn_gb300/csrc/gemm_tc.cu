@@ -636,13 +636,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 // bf16 tcgen05 MMA as above, and only the weight bytes streamed from HBM shrink
 // (1 byte per weight for E4M3, half a byte for E2M1, plus 1/32 byte of scale).
 //
-// One CTA per SM, 11 warps:
+// One CTA per SM, 15 warps (7 + kConvWarps = 8 converters):
 //   warp 0     TMA producer of the weight codes and scales (the HBM stream): a
 //              raw ring of kRawStages k-blocks, 256 rows x 64 codes + 2 x 256 scales
 //   warp 1     tcgen05.mma issue (as above): A from the A ring, B from the B ring
 //   warps 2-5  epilogue (as above)
 //   warp 6     TMA producer of the A rows (bf16, 128-byte swizzle) into the A ring
-//   warps 7-   converters: decode a raw k-block into the B ring's bf16 tile, written
+//   warps 7-14 converters: decode a raw k-block into the B ring's bf16 tile, written
 //              in the 128-byte-swizzled K-major layout the MMA descriptor reads
 // Three rings: raw (kRawStages, freed by the converters), A (kAStages, freed by the
 // MMA) and converted B (kBStages, freed by the MMA), so the weight stream and the
