@@ -249,6 +249,27 @@ def test_forward_host_matches_forward_and_edge_sizes():
     assert empty.shape[0] == 0
 
 
+def test_forward_host_pinned_pageable_and_fp32_buffers():
+    """Pinned host buffers are read and written by the GPU itself; pageable ones (or a
+    pinned one paired with a pageable one) go through the copy engines; fp32 tokens
+    move 4 bytes per value.  Every combination equals moe_forward bit for bit."""
+    for name in ("nano_decode", "tiny_f32"):
+        shape = SMALL[name]
+        inputs, blk, Y = _run(shape, max_tokens=shape.T)
+        ref = Y.cpu()
+        Xp, Xg = inputs["X"].cpu().pin_memory(), inputs["X"].cpu()
+        for xh, pinned_y in ((Xp, True), (Xg, False), (Xp, False), (Xg, True)):
+            Yh = torch.empty_like(Xg)
+            if pinned_y:
+                Yh = Yh.pin_memory()
+            for _ in range(3):  # eager, then (pinned pairs) capture and replay
+                Yh.zero_()
+                blk.forward_host(xh, Yh)
+                assert torch.equal(Yh, ref), (name, xh.is_pinned(), pinned_y)
+        assert blk.sync_status() == capi.MOE_OK
+        blk.close()
+
+
 def test_forward_host_graph_replay_matches_forward():
     """moe_forward_host runs eagerly, then captures a CUDA graph on the second call with
     the same buffers and T, then replays it: every call equals moe_forward bit for bit,
@@ -287,11 +308,16 @@ def test_forward_host_graph_replay_matches_forward():
         half = shape.T // 2  # another T
         Yh2 = torch.empty_like(Xh[:half]).pin_memory()
         blk.set_option(capi.MOE_OPT_GRAPH, 1)
-        for _ in range(3):
-            blk.forward_host(Xh[:half], Yh2)
         Yd = blk.forward(X2[:half].contiguous())
         torch.cuda.synchronize()
-        assert torch.equal(Yh2, Yd.cpu())
+        for _ in range(3):  # every call writes this call's output buffer
+            Yh2.zero_()
+            blk.forward_host(Xh[:half], Yh2)
+            assert torch.equal(Yh2, Yd.cpu())
+        for _ in range(3):  # and back to the first buffers: a new capture, not the old graph
+            Yh.zero_()
+            blk.forward_host(Xh, Yh)
+            assert torch.equal(Yh, Y2.cpu())
         assert blk.sync_status() == capi.MOE_OK
         blk.close()
 
