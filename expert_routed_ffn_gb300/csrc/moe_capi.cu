@@ -1116,10 +1116,9 @@ moe_status moe_forward(moe_handle *h, const void *X, int T, void *Y, moe_stream_
 namespace {
 
 // The host-buffer forward's stream work: copy X in, the block, copy Y out.
-// Copy of n 16-byte words of which one end is the caller's page-locked host buffer: the
-// GPU reads or writes it itself over the host link.  Measured on GB300 around a 60 us
-// step with 512 KB each way: 7 us per step for the two copies, against 15 us through
-// the copy engines.
+// Copy of n 16-byte words from the caller's page-locked host buffer: the GPU reads it
+// itself over the host link.  Measured on GB300 around a 60 us step with 512 KB each
+// way: 7 us per step for two such copies, against 15 us through the copy engines.
 __global__ void __launch_bounds__(256) copy_words_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
                                                          size_t n) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
@@ -1153,14 +1152,10 @@ moe_status forward_host_ops(moe_handle *h, const void *X_host, const void *xm, i
         e = cudaMemcpyAsync(h->x_stage, X_host, bytes, cudaMemcpyHostToDevice, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy of X");
-    moe_status st = forward_device(h, h->x_stage, T, h->y_stage, s);
-    if (st != MOE_OK) return st;
-    if (direct) {
-        copy_words_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4 *>(h->y_stage), static_cast<uint4 *>(ym), words);
-        e = cudaGetLastError();
-    } else {
-        e = cudaMemcpyAsync(Y_host, h->y_stage, bytes, cudaMemcpyDeviceToHost, s);
-    }
+    // page-locked Y: the block's last kernel (the combine) stores its rows there itself
+    moe_status st = forward_device(h, h->x_stage, T, direct ? ym : h->y_stage, s);
+    if (st != MOE_OK || direct) return st;
+    e = cudaMemcpyAsync(Y_host, h->y_stage, bytes, cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy of Y");
     return MOE_OK;
 }

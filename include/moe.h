@@ -171,9 +171,10 @@ moe_status moe_forward(moe_handle *h, const void *X, int T, void *Y, moe_stream_
 /* moe_forward with HOST buffers: copies X_host to the handle's device staging
  * buffer, runs the block and copies the result back to Y_host, all on
  * `stream`; the call returns once Y_host holds the result.  When both buffers
- * are page-locked (pinned) and 16-byte aligned, a copy kernel reads X_host and
- * writes Y_host over the host link itself; otherwise the copy engines move the
- * bytes (pageable memory works but is slower).  Errors: INVALID_ARG, CUDA. */
+ * are page-locked (pinned) and 16-byte aligned, a copy kernel reads X_host over
+ * the host link and the block's last kernel stores its rows into Y_host itself;
+ * otherwise the copy engines move the bytes (pageable memory works but is
+ * slower).  Errors: INVALID_ARG, CUDA. */
 moe_status moe_forward_host(moe_handle *h, const void *X_host, int T, void *Y_host,
                             moe_stream_t stream);
 
