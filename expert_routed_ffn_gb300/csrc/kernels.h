@@ -363,6 +363,7 @@ struct DecodeGluArgs {
     __nv_bfloat16 *h_shared;        // [T, S]
     int act;
     float alpha, limit, beta;
+    int num_sms;                    // persistent grid: kDecodeCtasPerSm CTAs per SM
 };
 cudaError_t launch_decode_glu(const DecodeGluArgs &a, cudaStream_t s);
 
@@ -375,6 +376,7 @@ struct DecodeDownArgs {
     int H, I, S;
     __nv_bfloat16 *y_routed;        // [T*k, H]
     __nv_bfloat16 *y_shared;        // [T, H]
+    int num_sms;
 };
 cudaError_t launch_decode_down(const DecodeDownArgs &a, cudaStream_t s);
 

@@ -782,6 +782,7 @@ moe_status run_decode(moe_handle *h, const void *X, int T, cudaStream_t s, int *
     ga.alpha = h->cfg.act_alpha;
     ga.limit = h->cfg.act_limit;
     ga.beta = h->cfg.act_beta;
+    ga.num_sms = h->num_sms;
     moe_status st = launched(h, moe::launch_decode_glu(ga, s), "decode_gate_up", n, s);
     if (st != MOE_OK) return st;
     moe::DecodeDownArgs da{};
@@ -795,6 +796,7 @@ moe_status run_decode(moe_handle *h, const void *X, int T, cudaStream_t s, int *
     da.S = h->S;
     da.y_routed = h->yslot;
     da.y_shared = h->ys;
+    da.num_sms = h->num_sms;
     st = launched(h, moe::launch_decode_down(da, s), "decode_down", n, s);
     if (st != MOE_OK) return st;
     return MOE_OK;

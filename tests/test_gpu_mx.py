@@ -178,13 +178,16 @@ def test_mx_refuses_other_paths():
     blk.close()
 
 
-FULL = ["nano_decode_mxfp8", "nano_decode_mxfp4", "afmoe_prefill_mxfp8", "m3_mxfp8"]
+FULL = [("nano_decode_mxfp8", 2), ("nano_decode_mxfp4", 2), ("afmoe_prefill_mxfp8", 2), ("m3_mxfp8", 2),
+        ("afmoe_prefill_mxfp8", 1)]
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_mx_full_size_sampled(name):
+@pytest.mark.parametrize("name,pair", FULL)
+def test_mx_full_size_sampled(name, pair):
+    """The bench's launch configuration (pair 2: automatic), and CTA pairs forced."""
     shape = wl.WORKLOADS[name]
     inputs, blk = P.make_case(shape, max_tokens=shape.T)
+    blk.set_option(capi.MOE_OPT_GEMM_PAIR, pair)
     Y = _forward(blk, inputs["X"])
     T = shape.T
     idx, w = (blk.inspect(b, T * shape.k, dt).view(T, shape.k).cpu().numpy()
