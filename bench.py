@@ -116,6 +116,23 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(v: float, world: int, device="cpu") -> float:
+    """The largest value any rank reports (every rank must call it: a collective)."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, seconds: float) -> float:
+    """Whole-job tokens/s: every rank (a replica) processes its own batch in `seconds`,
+    the slowest rank's time."""
+    return world * tokens_per_rank / seconds
+
+
 def dist_setup(gpus: int):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -255,12 +272,8 @@ def run_ours(args, shape):
     if status != capi.MOE_OK:
         raise SystemExit(f"device error during the timed steps: {capi.STATUS_NAMES[status]}")
 
-    ms = sum(per_step) / len(per_step)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * shape.T / (ms / 1e3)
+    ms = max_over_ranks(sum(per_step) / len(per_step), world, dev)
+    value = job_throughput(shape.T, world, ms / 1e3)
 
     # end to end through the host-buffer entry point: H2D of X, forward, D2H of Y per step
     Xh = X.cpu().pin_memory()
@@ -274,11 +287,7 @@ def run_ours(args, shape):
         t0 = time.perf_counter()
         blk.forward_host(Xh, Yh)
         e2e_t.append(time.perf_counter() - t0)
-    e2e_s = sum(e2e_t) / len(e2e_t)
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(sum(e2e_t) / len(e2e_t), world, dev)
     xbytes = Xh.numel() * Xh.element_size()
 
     pk, pk_src = peaks()
@@ -337,7 +346,7 @@ def run_ours(args, shape):
         "timeline_us": timeline,
         "gemm_role_us": gemm_waits,
         "router_phase_us": router_phases,
-        "e2e": {"value": round(world * shape.T / e2e_s, 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_throughput(shape.T, world, e2e_s), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": xbytes, "d2h_bytes_per_step": xbytes},
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
