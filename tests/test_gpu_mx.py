@@ -93,6 +93,8 @@ SMALL = {
     "afmoe_ragged": wl.AFMOE_PREFILL.replace(name="afmoe_ragged", T=333, hidden_size=512,
                                              moe_intermediate_size=192, shared_intermediate_size=384),
     "nano_sandwich": wl.NANO_DECODE.replace(name="nano_sw", T=64, mlp_norm="rms"),
+    "afmoe_T4": wl.AFMOE_PREFILL.replace(name="afmoe_T4", T=4, hidden_size=512, moe_intermediate_size=1024,
+                                                shared_intermediate_size=512),
     "dense_small": wl.dense_layer(200, "afmoe").replace(name="dense_small", hidden_size=512,
                                                          shared_intermediate_size=1024),
 }
@@ -128,7 +130,8 @@ def test_mx_small_every_token(name, fmt, gemm):
 
 @pytest.mark.parametrize("gemm", list(GEMMS))
 @pytest.mark.parametrize("fmt", FORMATS)
-@pytest.mark.parametrize("name", ["nano", "m3_small_packed", "afmoe_ragged", "dense_small", "nano_T1"])
+@pytest.mark.parametrize("name", ["nano", "m3_small_packed", "afmoe_ragged", "dense_small", "nano_T1",
+                                  "afmoe_T4"])
 def test_mx_bit_identical_to_bf16_path_on_decoded_weights(name, fmt, gemm):
     shape = SMALL[name].replace(name=f"{SMALL[name].name}_{fmt}", weight_format=fmt)
     path, pair = GEMMS[gemm]

@@ -69,6 +69,11 @@ SMALL = {
     "afmoe_ragged": wl.AFMOE_PREFILL.replace(name="afmoe_ragged", T=333, hidden_size=512,
                                              moe_intermediate_size=192, shared_intermediate_size=384),
     "nano_T1": wl.NANO_DECODE.replace(name="nano_T1", T=1),
+    # a few tokens with a wide expert (I = 1024, 16 k-blocks)
+    "afmoe_T4": wl.AFMOE_PREFILL.replace(name="afmoe_T4", T=4, hidden_size=512, moe_intermediate_size=1024,
+                                                shared_intermediate_size=512),
+    "afmoe_T1": wl.AFMOE_PREFILL.replace(name="afmoe_T1", T=1, hidden_size=512, moe_intermediate_size=1024,
+                                                shared_intermediate_size=1024),
     "nano_T129": wl.NANO_DECODE.replace(name="nano_T129", T=129),
 }
 
