@@ -27,7 +27,11 @@ def pytest_collection_modifyitems(config, items):
 
 
 def pytest_sessionfinish(session, exitstatus):
-    """Write the output-parity errors the GPU tests measured to gpurun_out/."""
+    """Write the output-parity errors the GPU tests measured to
+    $MOE_PARITY_DIR/parity_summary.json (nothing when the variable is unset)."""
+    out = os.environ.get("MOE_PARITY_DIR")
+    if not out:
+        return
     try:
         from tests import parity
     except Exception:
@@ -35,7 +39,6 @@ def pytest_sessionfinish(session, exitstatus):
     if not parity.RESULTS:
         return
     import json
-    out = os.path.join(ROOT, "gpurun_out")
     os.makedirs(out, exist_ok=True)
     with open(os.path.join(out, "parity_summary.json"), "w") as f:
         json.dump([{"case": c, "max_abs_err_over_rms": a, "err_over_bound": b} for c, a, b in parity.RESULTS],
