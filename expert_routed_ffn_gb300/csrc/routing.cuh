@@ -8,8 +8,36 @@
 
 namespace moe {
 
-__device__ __forceinline__ bool better(float c, int e, float bc, int be) {
-    return c > bc || (c == bc && e < be);
+// Selection key of a candidate: a larger key is a larger biased score c, and among
+// equal c the lower expert index e.  High word: c as an order-preserving integer (c is
+// never NaN here; -0 is taken as +0, they compare equal); low word: 0xFFFF - e.  The
+// key 0 sorts below every candidate, even c = -inf.
+__device__ __forceinline__ unsigned long long sel_key(float c, int e) {
+    uint32_t u = __float_as_uint(c == 0.f ? 0.f : c);
+    u ^= (u >> 31) ? 0xFFFFFFFFu : 0x80000000u;
+    return ((unsigned long long)u << 32) | (uint32_t)(0xFFFF - e);
+}
+__device__ __forceinline__ void cas_desc(unsigned long long &a, unsigned long long &b) {
+    const unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
+    a = hi;
+    b = lo;
+}
+// The 8 keys of this lane in descending order (a bitonic sorting network).
+__device__ __forceinline__ void sort8_desc(unsigned long long (&k)[8]) {
+#pragma unroll
+    for (int size = 2; size <= 8; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    if ((i & size) == 0)
+                        cas_desc(k[i], k[j]);
+                    else
+                        cas_desc(k[j], k[i]);
+                }
+            }
 }
 
 // The routing rule for one token, by a group of LPT consecutive lanes: lane
@@ -49,18 +77,22 @@ __device__ __forceinline__ void route_token_group(const float (&lg)[8], int sub,
 #pragma unroll
         for (int j = 0; j < 8; ++j) s[j] = 1.0f / (1.0f + expf(-lg[j]));
     }
-    uint32_t open = 0;  // bit j: expert sub + LPT*j is still a candidate
+    // Each lane sorts its candidates' selection keys once; a round then takes the
+    // largest head over the group (log2(LPT) shuffle levels, no scan of the candidates)
+    // and the lane that held it drops its head.
+    unsigned long long key[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int e = expert_of(j);
         if (e < E) {
-            const float cj = s[j] + (bias ? __ldg(bias + e) : 0.f);
-            c[j] = (cj != cj) ? -INFINITY : cj;  // NaN never wins
-            open |= 1u << j;
+            float cj = s[j] + (bias ? __ldg(bias + e) : 0.f);
+            cj = (cj != cj) ? -INFINITY : cj;  // NaN never wins
+            key[j] = sel_key(cj, e);
         } else {
-            c[j] = -INFINITY;
+            key[j] = 0ull;
         }
     }
+    sort8_desc(key);
     // Slot r is kept by lane r mod LPT of the group (entry r / LPT of its
     // own[] arrays), so the k rounds compile to one loop body: the routing
     // kernels run once per forward with a cold instruction cache.
@@ -75,29 +107,23 @@ __device__ __forceinline__ void route_token_group(const float (&lg)[8], int sub,
     float wsum = 0.f;
 #pragma unroll 1
     for (int r = 0; r < k; ++r) {
-        float bc = -INFINITY;
-        int be = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if ((open >> j & 1u) && better(c[j], expert_of(j), bc, be)) {
-                bc = c[j];
-                be = expert_of(j);
-            }
+        unsigned long long best = key[0];
 #pragma unroll
         for (int o = LPT / 2; o > 0; o >>= 1) {
-            const float oc = __shfl_xor_sync(0xffffffffu, bc, o, LPT);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o, LPT);
-            if (better(oc, oe, bc, be)) {
-                bc = oc;
-                be = oe;
-            }
+            const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o, LPT);
+            best = other > best ? other : best;
         }
+        if (key[0] == best) {  // this lane's head was chosen (keys are unique)
+#pragma unroll
+            for (int q = 0; q < 7; ++q) key[q] = key[q + 1];
+            key[7] = 0ull;
+        }
+        const int be = 0xFFFF - (int)(uint32_t)(best & 0xFFFFull);
         const int owner = CONTIG ? be >> 3 : be & (LPT - 1), jj = CONTIG ? be & 7 : be / LPT;
         float sv = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (j == jj) sv = s[j];
-        if (sub == owner) open &= ~(1u << jj);
+        for (int q = 0; q < 8; ++q)
+            if (q == jj) sv = s[q];
         sv = __shfl_sync(0xffffffffu, sv, owner, LPT);
         wsum += sv;
         if ((r & (LPT - 1)) == sub) {
