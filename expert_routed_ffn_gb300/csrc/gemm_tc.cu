@@ -198,8 +198,10 @@ struct EpiCtx {
 
 // Epilogue role (kEpiWarps warps, named barrier 1): for each tile id from the
 // ring, wait for its accumulator, apply the activation (gate/up) and store bf16
-// rows, release the accumulator, and publish the m-tile's completion.
-template <bool PAIR, int kBM>
+// rows, release the accumulator, and publish the m-tile's completion.  HALVES = 2:
+// 256-row tiles in one CTA, one accumulator of 2 x 256 columns (half h's rows in
+// columns 256 h ..), no second buffer.
+template <bool PAIR, int kBM, int HALVES = 1>
 __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c, int warp, int lane) {
     auto ring_full = [&](int i) { return c.ring_full0 + 8u * i; };
     auto ring_empty = [&](int i) { return c.ring_empty0 + 8u * i; };
@@ -236,9 +238,9 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
         }
         if (lead_thread) mbar_arrive(ring_empty(slot));
         if (tile >= total) break;
-        const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
-        const GemmSegment &sg = p.seg[t.seg];
-        const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
+        const Tile tile0 = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, HALVES == 2 ? 0 : half);
+        const GemmSegment &sg = p.seg[tile0.seg];
+        const uint32_t a = HALVES == 2 ? 0u : n_acc & 1u, aph = HALVES == 2 ? n_acc & 1u : (n_acc >> 1) & 1u;
         const bool ready = __all_sync(0xffffffffu, PAIR ? mbar_wait_cluster(tfull_bar(a), aph, p.wait_ns, abort_flag)
                                                         : mbar_wait(tfull_bar(a), aph, p.wait_ns, abort_flag));
         const uint64_t t1 = stats ? global_timer_ns() : 0;
@@ -248,7 +250,10 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
             break;
         }
         tc_fence_after();
-        const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + a * kGemmBN;
+#pragma unroll 1
+        for (int hh = 0; hh < HALVES; ++hh) {
+        const Tile t = hh == 0 ? tile0 : decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, hh);
+        const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (a + hh) * kGemmBN;
         const bool row_ok = r < t.m_valid;
         bf16 *orow = sg.out + t.ks * sg.split_stride + (size_t)(t.row0 + (row_ok ? r : 0)) * sg.ldo;
         if (sg.glu) {
@@ -295,6 +300,7 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
                 }
             }
         }
+        }  // halves
         tc_fence_before();
         if (PAIR)  // rank 0's barrier counts both CTAs' epilogue threads
             mbar_arrive_cluster(mapa_shared(tempty_bar(a), 0));
@@ -306,7 +312,8 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
             fence_proxy_async();
             __threadfence();
             epi_bar();
-            if (lead_thread) atomicAdd(sg.signal + t.ready, 1);
+            if (lead_thread)
+                for (int hh = 0; hh < HALVES; ++hh) atomicAdd(sg.signal + tile0.ready + hh, 1);
         }
         if (stats) w_work += global_timer_ns() - t1;
         ++n_acc;
@@ -651,17 +658,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 // bf16 B tile in and out, the A tile in and out), which bounds this design at
 // roughly one k-block per 1000 cycles.
 //
-// CTA pairs (PAIR): 256-row tiles, rank 0 issues tcgen05.mma.cta_group::2; each CTA
-// streams and decodes its 128 weight rows and loads its 128 A rows (completing on
-// rank 0's barrier).  Bit-identical to the bf16 pair kernel on the decoded weights,
-// but measured slower than one CTA per tile (AFMoE MXFP8 prefill expert GEMM 1028
-// against 758 us), so it runs only when asked for.
-template <int WF, bool PAIR = false>
+// 256-row tiles (M256, where the host picks the CTA-pair tile size): one CTA loads both
+// 128-row halves of the A rows and issues two M = 128 MMAs on every decoded weight
+// tile into one accumulator of 2 x 256 TMEM columns, so each decoded weight serves
+// twice the rows; the epilogue then runs between tiles (one accumulator).  Measured:
+// AFMoE MXFP8 prefill expert GEMM 555 against 758 us with 128-row tiles; a CTA-pair
+// version (each CTA decoding half of the weight tile, rank 1 relaying its k-blocks to
+// rank 0's cta_group::2 MMAs) took 1028 us.  Bit-identical to the bf16 CTA-pair path.
+template <int WF, bool M256 = false>
 struct MxCfg {
-    // B rows a CTA converts per k-block: all 256 of the tile, or its half of a CTA pair's
-    static constexpr int kBRows = PAIR ? kGemmBN / 2 : kGemmBN;
+    // B rows converted per k-block (the tile's 256 columns)
+    static constexpr int kBRows = kGemmBN;
     static constexpr int kRawRow = WF == kWeightsMxfp8 ? kGemmBK : kGemmBK / 2;  // bytes of a row's k-block
-    static constexpr int kRawCodes = kBRows * kRawRow;                          // 16 KB / 8 KB (halved in a pair)
+    static constexpr int kRawCodes = kBRows * kRawRow;                          // 16 KB / 8 KB
     // scales [row half][32-value block][128 rows]: every copy lands 128-byte aligned, as a
     // tensor copy's shared-memory destination must
     static constexpr int kScaleStride = 128;
@@ -669,14 +678,15 @@ struct MxCfg {
     static constexpr int kRawStage = kRawCodes + kScaleBytes;
     // ring depths measured on GB300 (Nano decode and AFMoE prefill, MXFP8 and MXFP4):
     // three converted B stages beat two by 2-4%; deeper A or raw rings change nothing.
-    // A pair's stages are half as large (B) and the MMA waits on both CTAs: 4 of each.
-    static constexpr int kRawStages = PAIR ? (WF == kWeightsMxfp8 ? 6 : 8) : (WF == kWeightsMxfp8 ? 4 : 6);
-    static constexpr int kAStages = PAIR ? 4 : 3;
-    static constexpr int kBStages = PAIR ? 4 : 3;
-    static constexpr int kBBytes = kBRows * kGemmBK * 2;  // converted B tile, 32 KB (16 KB in a pair)
+    // 256-row tiles (M256): an A stage holds both 128-row halves (32 KB), two of them.
+    static constexpr int kRawStages = M256 ? (WF == kWeightsMxfp8 ? 3 : 4) : (WF == kWeightsMxfp8 ? 4 : 6);
+    static constexpr int kAStages = M256 ? 2 : 3;
+    static constexpr int kBStages = 3;
+    static constexpr int kAStageBytes = (M256 ? 2 : 1) * kABytes;
+    static constexpr int kBBytes = kBRows * kGemmBK * 2;  // converted B tile, 32 KB
     static constexpr int kBarBytes = 1024;
     static constexpr int kSmemBytes =
-        kBStages * kBBytes + kAStages * kABytes + kRawStages * kRawStage + 1024 /*align*/ + kBarBytes;
+        kBStages * kBBytes + kAStages * kAStageBytes + kRawStages * kRawStage + 1024 /*align*/ + kBarBytes;
 #ifndef MOE_MX_CONV_WARPS
 #define MOE_MX_CONV_WARPS 8
 #endif
@@ -861,19 +871,19 @@ __device__ __forceinline__ void mx_convert(const uint8_t *raw, const uint8_t *sc
     }
 }
 
-template <int WF, bool PAIR>
+template <int WF, bool M256>
 __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const __grid_constant__ GemmArgs p) {
-    using M = MxCfg<WF, PAIR>;
+    using M = MxCfg<WF, M256>;
     constexpr int R = M::kRawStages, RA = M::kAStages, P = M::kBStages, NCW = M::kConvWarps;
-    constexpr int kBM = PAIR ? 2 * kGemmBM : kGemmBM;  // rows per tile (128 per CTA)
+    constexpr int kBM = M256 ? 2 * kGemmBM : kGemmBM;  // rows per tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    // converted B stages (32 KB, 16 KB in a pair), A stages (16 KB; both 1024-byte aligned),
-    // raw stages, barriers
+    // converted B stages (32 KB), A stages (16 KB, or 32 KB for 256-row tiles; both
+    // 1024-byte aligned), raw stages, barriers
     auto opB = [&](int s) { return smem + s * M::kBBytes; };
-    auto opA = [&](int s) { return smem + P * M::kBBytes + s * kABytes; };
-    uint8_t *const raw0 = smem + P * M::kBBytes + RA * kABytes;
+    auto opA = [&](int s) { return smem + P * M::kBBytes + s * M::kAStageBytes; };
+    uint8_t *const raw0 = smem + P * M::kBBytes + RA * M::kAStageBytes;
     auto rawS = [&](int s) { return raw0 + s * M::kRawStage; };
     uint64_t *bars = reinterpret_cast<uint64_t *>(raw0 + R * M::kRawStage);
     const uint32_t bar0 = smem_u32(bars);
@@ -892,26 +902,16 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
     auto op_full = [&](int s) { return bar0 + 8u * (kB0 + 2 * R + 2 * RA + s); };
     auto op_empty = [&](int s) { return bar0 + 8u * (kB0 + 2 * R + 2 * RA + P + s); };
     const uint32_t drain_bar = bar0 + 8u * (kB0 + 2 * R + 2 * RA + 2 * P);
-    // CTA pair: this CTA's converter warps arrive on op_conv; rank 1 relays its completed
-    // k-blocks with one cluster-scope arrival each on rank 0's op_full
-    auto op_conv = [&](int s) { return bar0 + 8u * (kB0 + 2 * R + 2 * RA + 2 * P + 1 + s); };
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kB0 + 2 * R + 2 * RA + 3 * P + 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kB0 + 2 * R + 2 * RA + 2 * P + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *ring = reinterpret_cast<volatile int *>(tmem_slot + 2);  // [kRing] tile ids
-    static_assert(8 * (kB0 + 2 * R + 2 * RA + 3 * P + 1) + 8 + 4 * kRing <= M::kBarBytes, "barrier block");
+    static_assert(8 * (kB0 + 2 * R + 2 * RA + 2 * P + 1) + 8 + 4 * kRing <= M::kBarBytes, "barrier block");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // CTA pair: rank 0 issues the MMAs (M = 256: 128 A rows in each CTA, B split along N,
-    // each CTA converting its half); its A-full, converted-B-full and accumulator-empty
-    // barriers count both CTAs
-    const int half = PAIR ? (int)cluster_ctarank() : 0;
-    const bool leader = half == 0;
-    auto abort_all = [&]() {
-        if (PAIR)
-            raise_abort_pair(p.err, abort_flag);
-        else
-            raise_abort(p.err, abort_flag);
-    };
+    // 256-row tiles: both 128-row halves in this CTA, one accumulator of 2 x 256 columns
+    // (no second buffer: the epilogue of a tile precedes the next tile's MMAs)
+    const int half = 0;
+    auto abort_all = [&]() { raise_abort(p.err, abort_flag); };
     trace_mark(p.trace, 0);
     if (threadIdx.x == 0) {
         for (int i = 0; i < kRing; ++i) {
@@ -920,7 +920,7 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
         }
         for (uint32_t a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), PAIR ? 2 * kEpiThreads : kEpiThreads);
+            mbar_init(tempty_bar(a), kEpiThreads);
         }
         for (int s = 0; s < R; ++s) {
             mbar_init(raw_full(s), 1);
@@ -931,9 +931,8 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
             mbar_init(a_empty(s), 1);  // the MMA's commit
         }
         for (int s = 0; s < P; ++s) {
-            mbar_init(op_full(s), PAIR ? 1 : NCW);  // each converter warp, or rank 1's relay
-            mbar_init(op_empty(s), 1);              // the MMA's commit
-            mbar_init(op_conv(s), NCW);             // each converter warp (CTA pair)
+            mbar_init(op_full(s), NCW);  // each converter warp
+            mbar_init(op_empty(s), 1);   // the MMA's commit
         }
         mbar_init(drain_bar, 1);
         fence_mbar_init();
@@ -942,17 +941,11 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
     if (warp == 0 && lane == 0)
         for (int m = 0; m < kGemmMaxMaps; ++m) tma_prefetch_desc(&p.maps[m]);
     if (warp == 1) {
-        if (PAIR) {
-            tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
-            tmem_relinquish_pair();
-        } else {
-            tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-            tmem_relinquish();
-        }
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
-    if (PAIR) cluster_sync();  // both CTAs' barriers exist before any copy or arrival crosses over
     tc_fence_after();
     pdl_wait();
     trace_mark(p.trace, 1);
@@ -987,11 +980,10 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
             uint32_t L = 0;
             bool ok = true;
             uint64_t w_empty = 0;
-            // tiles: from the launch-wide ticket, or round-robin (both CTAs of a pair
-            // take the same sequence)
-            const bool dyn = !PAIR && p.tile_counter != nullptr;
-            const int stride = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
-            int next = dyn ? atomicAdd(p.tile_counter, 1) : (PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x);
+            // tiles: from the launch-wide ticket, or round-robin
+            const bool dyn = p.tile_counter != nullptr;
+            const int stride = (int)gridDim.x;
+            int next = dyn ? atomicAdd(p.tile_counter, 1) : (int)blockIdx.x;
             for (int n = 0;; ++n) {
                 const int tile = next < total ? next : total;
                 const int slot = n % kRing;
@@ -1006,14 +998,11 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                 const GemmSegment &sg = p.seg[t.seg];
                 const int g = sg.group_base + t.group;
                 const int claim_at = sg.k_blocks > 3 ? sg.k_blocks - 3 : 0;
-                // rows of the tile's two 128-row halves: gate and up rows of n-tile nt, or
-                // the 256 rows of a down tile; a CTA of a pair loads its half only (gate
-                // rows in rank 0, up rows in rank 1: accumulator columns 0-127 / 128-255)
-                const int r0 = sg.glu ? t.nt * 128 : t.nt * kGemmBN + half * 128, r1 = sg.glu ? r0 : r0 + 128;
-                const CUtensorMap *mC0 = &p.maps[(sg.glu && half) ? sg.map_b1 : sg.map_b0],
-                                  *mC1 = &p.maps[sg.glu ? sg.map_b1 : sg.map_b0];
-                const CUtensorMap *mS0 = &p.maps[(sg.glu && half) ? sg.map_s1 : sg.map_s0],
-                                  *mS1 = &p.maps[sg.glu ? sg.map_s1 : sg.map_s0];
+                // rows of the B tile's two 128-row halves: gate and up rows of n-tile nt,
+                // or the 256 rows of a down tile
+                const int r0 = sg.glu ? t.nt * 128 : t.nt * kGemmBN, r1 = sg.glu ? r0 : r0 + 128;
+                const CUtensorMap *mC0 = &p.maps[sg.map_b0], *mC1 = &p.maps[sg.glu ? sg.map_b1 : sg.map_b0];
+                const CUtensorMap *mS0 = &p.maps[sg.map_s0], *mS1 = &p.maps[sg.glu ? sg.map_s1 : sg.map_s0];
                 for (int kb = 0; kb < sg.k_blocks; ++kb) {
                     const int s = L % R;
                     const uint32_t ph = (L / R) & 1u;
@@ -1030,10 +1019,8 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                     mbar_arrive_expect_tx(raw_full(s), M::kRawStage);
                     tma_load_3d(dst, mC0, raw_full(s), xb, r0, g);
                     tma_load_3d(dst + M::kRawCodes, mS0, raw_full(s), r0, kx / 32, g);
-                    if (!PAIR) {
-                        tma_load_3d(dst + 128 * M::kRawRow, mC1, raw_full(s), xb, r1, g);
-                        tma_load_3d(dst + M::kRawCodes + 2 * M::kScaleStride, mS1, raw_full(s), r1, kx / 32, g);
-                    }
+                    tma_load_3d(dst + 128 * M::kRawRow, mC1, raw_full(s), xb, r1, g);
+                    tma_load_3d(dst + M::kRawCodes + 2 * M::kScaleStride, mS1, raw_full(s), r1, kx / 32, g);
                     ++L;
                 }
                 if (!ok) break;
@@ -1064,9 +1051,10 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                 if (tile >= total) break;
                 const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
                 const GemmSegment &sg = p.seg[t.seg];
-                if (sg.wait != nullptr) {  // A rows written earlier in this launch
+                if (sg.wait != nullptr) {  // A rows written earlier in this launch (both halves)
                     const uint64_t t0 = stats ? global_timer_ns() : 0;
-                    if (!wait_counter(sg.wait + t.ready, sg.wait_count, p.wait_ns, abort_flag)) {
+                    if (!wait_counter(sg.wait + t.ready, sg.wait_count, p.wait_ns, abort_flag) ||
+                        (M256 && !wait_counter(sg.wait + t.ready + 1, sg.wait_count, p.wait_ns, abort_flag))) {
                         ok = false;
                         break;
                     }
@@ -1082,15 +1070,9 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                         break;
                     }
                     const int kx = (sg.k_base + t.ks * sg.k_blocks + kb) * kGemmBK;
-                    if (PAIR) {
-                        // both CTAs' A rows complete on rank 0's barrier, which expects both
-                        const uint32_t fb = mapa_shared(a_full(s), 0);
-                        if (leader) mbar_arrive_expect_tx(a_full(s), 2 * kABytes);
-                        tma_load_2d_pair(smem_u32(opA(s)), mA, fb, kx, t.row0);
-                    } else {
-                        mbar_arrive_expect_tx(a_full(s), kABytes);
-                        tma_load_2d(smem_u32(opA(s)), mA, a_full(s), kx, t.row0);
-                    }
+                    mbar_arrive_expect_tx(a_full(s), M::kAStageBytes);
+                    tma_load_2d(smem_u32(opA(s)), mA, a_full(s), kx, t.row0);
+                    if (M256) tma_load_2d(smem_u32(opA(s)) + kABytes, mA, a_full(s), kx, t.row0 + 128);
                     ++L;
                 }
                 if (!ok) break;
@@ -1098,16 +1080,9 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
             if (stats) atomicAdd(stats + 1, (unsigned long long)w_dep);
             if (!ok) {
                 abort_all();
-                if (PAIR) {
-                    // the copies complete on rank 0's barrier together with the other CTA's,
-                    // which may never be issued after an abort: wait a fixed time instead
-                    const uint64_t t0 = global_timer_ns();
-                    while (global_timer_ns() - t0 < kPairDrainNs) __nanosleep(1000);
-                } else {
-                    for (uint32_t i = 0; i < (uint32_t)RA && i < L; ++i) {  // copies still in flight
-                        const uint32_t l = L - 1 - i;
-                        mbar_wait(a_full(l % RA), (l / RA) & 1u, kDrainNs, nullptr);
-                    }
+                for (uint32_t i = 0; i < (uint32_t)RA && i < L; ++i) {  // copies still in flight
+                    const uint32_t l = L - 1 - i;
+                    mbar_wait(a_full(l % RA), (l / RA) & 1u, kDrainNs, nullptr);
                 }
             }
         }
@@ -1143,38 +1118,15 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(raw_empty(rs));
-                    mbar_arrive(PAIR ? op_conv(os) : op_full(os));
+                    mbar_arrive(op_full(os));
                 }
                 ++L;
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
-        if (PAIR && !leader && lane == 0) {
-            // rank 1 issues no MMA: it relays each k-block its converters completed to rank 0
-            // with one cluster-scope release (measured, AFMoE MXFP8 prefill: 1095 us against
-            // 1312 us when each converter warp arrives on rank 0's barrier itself)
-            uint32_t L = 0;
-            bool ok = true;
-            for (int n = 0; ok; ++n) {
-                const int slot = n % kRing;
-                if (!mbar_wait(ring_full(slot), (n / kRing) & 1u, p.wait_ns, abort_flag)) break;
-                const int tile = ring[slot];
-                mbar_arrive(ring_empty(slot));
-                if (tile >= total) break;
-                const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
-                for (int kb = 0; kb < p.seg[t.seg].k_blocks; ++kb, ++L) {
-                    const int sb = L % P;
-                    if (!mbar_wait(op_conv(sb), (L / P) & 1u, p.wait_ns, abort_flag)) {
-                        abort_all();
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_cluster(mapa_shared(op_full(sb), 0));
-                }
-            }
-        } else if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * kGemmBM : kGemmBM, kGemmBN);
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kGemmBM, kGemmBN);
             uint32_t L = 0, n_acc = 0;
             bool ok = true, issued = false;
             uint64_t w_full = 0, w_acc = 0;
@@ -1189,10 +1141,10 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                 if (tile >= total) break;
                 const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
                 const GemmSegment &sg = p.seg[t.seg];
-                const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
+                // two accumulators in turn, or (256-row tiles) one of 2 x 256 columns
+                const uint32_t a = M256 ? 0u : n_acc & 1u, aph = M256 ? n_acc & 1u : (n_acc >> 1) & 1u;
                 const uint64_t t0 = stats ? global_timer_ns() : 0;
-                if (!(PAIR ? mbar_wait_cluster(tempty_bar(a), aph ^ 1u, p.wait_ns, abort_flag)
-                           : mbar_wait(tempty_bar(a), aph ^ 1u, p.wait_ns, abort_flag))) {
+                if (!mbar_wait(tempty_bar(a), aph ^ 1u, p.wait_ns, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -1202,42 +1154,29 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                 for (int kb = 0; kb < sg.k_blocks; ++kb) {
                     const int sa = L % RA, sb = L % P;
                     const uint64_t t1 = stats ? global_timer_ns() : 0;
-                    // (a pair: this CTA's converted half, then rank 1's relayed completion,
-                    // with a cluster-scope acquire)
                     if (!mbar_wait(a_full(sa), (L / RA) & 1u, p.wait_ns, abort_flag) ||
-                        !(PAIR ? mbar_wait(op_conv(sb), (L / P) & 1u, p.wait_ns, abort_flag) &&
-                                     mbar_wait_cluster(op_full(sb), (L / P) & 1u, p.wait_ns, abort_flag)
-                               : mbar_wait(op_full(sb), (L / P) & 1u, p.wait_ns, abort_flag))) {
+                        !mbar_wait(op_full(sb), (L / P) & 1u, p.wait_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
                     if (stats) w_full += global_timer_ns() - t1;
                     tc_fence_after();
-                    const uint64_t ad = smem_desc_k128(smem_u32(opA(sa)));
                     const uint64_t bd = smem_desc_k128(smem_u32(opB(sb)));
+                    // each 128-row half of the tile's A rows against the same decoded B tile
 #pragma unroll
-                    for (int kk = 0; kk < kGemmBK / 16; ++kk) {
-                        if (PAIR)
-                            tc_mma_bf16_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
-                        else
-                            tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    for (int hh = 0; hh < (M256 ? 2 : 1); ++hh) {
+                        const uint64_t ad = smem_desc_k128(smem_u32(opA(sa)) + hh * kABytes);
+#pragma unroll
+                        for (int kk = 0; kk < kGemmBK / 16; ++kk)
+                            tc_mma_bf16(d + hh * kGemmBN, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
                     }
                     issued = true;
-                    // frees the stages (in both CTAs of a pair) once these MMAs have read them
-                    if (PAIR) {
-                        tc_commit_pair(a_empty(sa), 3);
-                        tc_commit_pair(op_empty(sb), 3);
-                    } else {
-                        tc_commit(a_empty(sa));
-                        tc_commit(op_empty(sb));
-                    }
+                    tc_commit(a_empty(sa));
+                    tc_commit(op_empty(sb));
                     ++L;
                 }
                 if (!ok) break;
-                if (PAIR)  // accumulator complete, in both CTAs' TMEM
-                    tc_commit_pair(tfull_bar(a), 3);
-                else
-                    tc_commit(tfull_bar(a));
+                tc_commit(tfull_bar(a));
                 ++n_acc;
             }
             if (stats) {
@@ -1248,10 +1187,7 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
             if (!ok) {
                 abort_all();
                 if (issued) {
-                    if (PAIR)
-                        tc_commit_pair(drain_bar, 1);
-                    else
-                        tc_commit(drain_bar);
+                    tc_commit(drain_bar);
                     mbar_wait(drain_bar, 0, kDrainNs, nullptr);
                 }
             }
@@ -1260,21 +1196,17 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
         // ----------------------------------------------------------- epilogue
         EpiCtx c{ring_full(0), ring_empty(0), tfull_bar(0), tempty_bar(0), ring, abort_flag, tmem_base, total,
                  s_seg_end, s_offs, s_toffs, half};
-        epilogue_role<PAIR, kBM>(p, c, warp, lane);
+        epilogue_role<false, kBM, M256 ? 2 : 1>(p, c, warp, lane);
     }
 
     tc_fence_before();
     __syncthreads();
-    if (PAIR) cluster_sync();  // neither CTA leaves while the other may still reach its memory
     trace_exit(p.trace);
     if (stats && threadIdx.x == 0) atomicAdd(stats + 6, (unsigned long long)(global_timer_ns() - t_ready));
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        if (PAIR)
-            tmem_dealloc_pair(tmem_base, kTmemCols);
-        else
-            tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -1400,15 +1332,13 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
     });
     if (a.wfmt == kWeightsMxfp8 || a.wfmt == kWeightsMxfp4) {
         const bool f8 = a.wfmt == kWeightsMxfp8;
-        if (a.pair) {
-            if (a.num_ctas < 2 || (a.num_ctas & 1) || a.tile_counter != nullptr) return cudaErrorInvalidValue;
+        if (a.pair) {  // 256-row tiles (the dispatch counted them), one CTA each
             if (f8)
-                return launch_pdl_cluster(gemm_mx_kernel<kWeightsMxfp8, true>, dim3(a.num_ctas),
-                                          dim3(MxCfg<kWeightsMxfp8>::kThreads),
-                                          (size_t)MxCfg<kWeightsMxfp8, true>::kSmemBytes, s, dim3(2, 1, 1), a);
-            return launch_pdl_cluster(gemm_mx_kernel<kWeightsMxfp4, true>, dim3(a.num_ctas),
-                                      dim3(MxCfg<kWeightsMxfp4>::kThreads),
-                                      (size_t)MxCfg<kWeightsMxfp4, true>::kSmemBytes, s, dim3(2, 1, 1), a);
+                return launch_pdl(gemm_mx_kernel<kWeightsMxfp8, true>, dim3(a.num_ctas),
+                                  dim3(MxCfg<kWeightsMxfp8>::kThreads), (size_t)MxCfg<kWeightsMxfp8, true>::kSmemBytes,
+                                  s, a);
+            return launch_pdl(gemm_mx_kernel<kWeightsMxfp4, true>, dim3(a.num_ctas), dim3(MxCfg<kWeightsMxfp4>::kThreads),
+                              (size_t)MxCfg<kWeightsMxfp4, true>::kSmemBytes, s, a);
         }
         if (f8)
             return launch_pdl(gemm_mx_kernel<kWeightsMxfp8, false>, dim3(a.num_ctas),

@@ -892,10 +892,9 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     }
     // CTA pairs once the weight tiles are reused by 256 rows on average (a dense
     // layer: T >= 256)
-    // (MX weights: only when asked; measured slower than one CTA per tile, see the MX kernel)
+    // (MX weights: 256-row tiles in one CTA each, two MMAs on every decoded weight tile)
     h->pair_now = path == kPathGrouped && h->num_sms >= 2 &&
-                  (h->pair_opt == 1 || (h->pair_opt == 2 && h->wfmt == MOE_WEIGHTS_BF16 &&
-                                        (h->dense ? T >= 256 : slots >= 256ll * h->E)));
+                  (h->pair_opt == 1 || (h->pair_opt == 2 && (h->dense ? T >= 256 : slots >= 256ll * h->E)));
     h->shared_parts = path == kPathGrouped && h->has_shared ? shared_parts(h, T) : 1;
     mark(h, 0, s);
     moe_status st = MOE_OK;

@@ -85,8 +85,9 @@ typedef enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 } moe_dtype;
  *   MXFP4: two E2M1 codes per byte, [rows, K / 2], element 2j in the low nibble.
  *   Scales: uint8 [K / 32, rows] per weight slice (block-major: for each
  *           32-value block, the scales of all rows).
- * MX weights run on the tensor-core paths: the grouped GEMM (the auto path; CTA
- * pairs with MOE_OPT_GEMM_PAIR 1, each CTA decoding its half of the weight tile) or,
+ * MX weights run on the tensor-core paths: the grouped GEMM (the auto path; where
+ * MOE_OPT_GEMM_PAIR picks 256-row tiles, one CTA runs both 128-row halves against
+ * each decoded weight tile) or,
  * with moe_set_option MOE_OPT_PATH 3, the swapped-operand GEMM that decodes the
  * weights straight into tensor memory; MOE_OPT_PATH 1 is refused. */
 typedef enum { MOE_WEIGHTS_BF16 = 0, MOE_WEIGHTS_MXFP8 = 1, MOE_WEIGHTS_MXFP4 = 2 } moe_weight_format;
@@ -215,9 +216,9 @@ typedef enum {
                                   moe_get_trace.  Costs a memset and a few atomics per CTA; default 0 */
     MOE_OPT_GEMM_PAIR = 6,     /* path 2: expert GEMM tiles of 256 rows on CTA pairs (tcgen05 with
                                   cta_group::2: each CTA of a two-CTA cluster stages its 128 token rows
-                                  and half of the weight tile, decoded there for MX weights); 0 never,
-                                  1 always, 2 (default) when T*k >= 256*E (tensor-bound sizes) with
-                                  bf16 weights (MX weights: one CTA per tile, measured faster) */
+                                  and half of the weight tile; MX weights: one CTA per 256-row tile,
+                                  two 128-row MMAs on each decoded weight tile); 0 never, 1 always,
+                                  2 (default) when T*k >= 256*E (tensor-bound sizes) */
     MOE_OPT_GRAPH = 8          /* moe_forward_host: 1 (default) captures the copy in, the forward and the
                                   copy out into a CUDA graph on the second call with the same host
                                   buffers, T and options, and replays it on later such calls (host

@@ -10,11 +10,11 @@ activations stay bf16.  Checks:
     with the bf16 tolerance (decoding is exact, so the arithmetic is the bf16
     path's);
   * bit-for-bit against the bf16 path on the decoded weights: both MX GEMMs (the
-    grouped one, tokens as M, on one CTA or on CTA pairs, and the swapped one,
-    weights decoded into tensor memory as M) issue the same tcgen05 MMAs on the same
-    operand values in the same order as their bf16 counterparts, so Y must be
-    identical, which pins the decoders (byte and nibble order, scale index, operand
-    layouts, the pair's halves) independently of any tolerance;
+    grouped one, tokens as M, with 128-row tiles or 256-row tiles (against the bf16
+    CTA-pair path), and the swapped one, weights decoded into tensor memory as M)
+    multiply the same operand values in the same order as their bf16 counterparts, so
+    Y must be identical, which pins the decoders (byte and nibble order, scale index,
+    operand layouts, the tile halves) independently of any tolerance;
   * the options the MX path refuses.
 """
 
