@@ -296,13 +296,6 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask) {
 }
 // TMA loads into this CTA's shared memory whose completion is counted on a
 // barrier of either CTA of the pair (bar: address from mapa_shared)
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-        : "memory");
-}
 __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
                                                  int c2, int c3) {
     asm volatile(
