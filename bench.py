@@ -12,6 +12,11 @@ writing back the flush buffer's dirty lines (--flush write: the write alone).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
+The headline workload is the largest configuration, the MiniMax-M3-shaped block
+(T 2048, H 6144, 128 experts of width 3072, packed shared expert); on one GPU
+the other configurations (tiny, Nano decode, AFMoE prefill, the Zipf sweep) are
+timed after it and reported under "other_configs" of the same line.
+
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica
 of the block on its own GPU (the block has no cross-GPU exchange): weak scaling.
 --impl reference times the fp64 CPU oracle on the host cores instead.
@@ -353,11 +358,73 @@ def run_ours(args, shape):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(shape, inputs, budget_s=args.cpu_seconds)
+    blk.close()
+    del inputs, X, Y, blk
+    if world == 1 and args.other_configs:
+        out["other_configs"] = other_configs(args, shape.name, dev, flush_l2)
     if rank == 0:
         print(json.dumps(out), flush=True)
-    blk.close()
     if world > 1:
         dist.destroy_process_group()
+
+
+# the other workloads of the block's configuration list, timed after the headline one
+OTHER_CONFIGS = ("tiny", "nano_decode", "afmoe_prefill", "zipf_T1", "zipf_T8", "zipf_T64", "zipf_T512",
+                 "zipf_T4096", "zipf_T16384")
+
+
+def other_configs(args, headline: str, dev, flush_l2):
+    """Step time, tokens/s, block roofline fraction and clocks of each other
+    workload: the same timed steps as the headline (L2 flushed before each,
+    CUDA events around the forward), fewer of them."""
+    import torch
+
+    from expert_routed_ffn_gb300 import capi
+    from expert_routed_ffn_gb300 import workloads as wl
+    pk, _ = peaks()
+    res = {}
+    for name in OTHER_CONFIGS:
+        shape = wl.WORKLOADS[name]
+        if shape.name == headline:
+            continue
+        inputs = wl.make_inputs(shape, dev)
+        blk = capi.block_from_inputs(shape, inputs, max_tokens=shape.T)
+        X = inputs["X"]
+        Y = torch.empty_like(X)
+
+        def step():
+            flush_l2()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            blk.forward(X, Y)
+            e.record()
+            return s, e
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        U = int(torch.unique(blk.inspect(capi.MOE_BUF_TOPK_IDX, shape.T * shape.k, torch.int32)).numel())
+        t_end = time.perf_counter() + 0.3
+        while time.perf_counter() < t_end:
+            step()
+            torch.cuda.synchronize()
+        sampler = ClockSampler(f"GPU-{torch.cuda.get_device_properties(dev).uuid}")
+        evs = [step() for _ in range(args.other_steps)]
+        torch.cuda.synchronize()
+        clocks = sampler.stop()
+        if blk.sync_status() != capi.MOE_OK:
+            raise SystemExit(f"device error while timing {name}")
+        ms = sum(s.elapsed_time(e) for s, e in evs) / len(evs)
+        F, B, _ = work_model(shape, U)
+        t_tc, t_hbm = F / (pk["bf16_tflops"] * 1e12), B / (pk["hbm_gbs"] * 1e9)
+        res[shape.name] = {"ms_per_step": round(ms, 5), "tokens_per_s": round(shape.T / (ms / 1e3), 1),
+                           "block_roofline_frac": round(max(t_tc, t_hbm) / (ms / 1e3), 4),
+                           "bound": "tensor" if t_tc > t_hbm else "hbm", "t_roof_us": round(max(t_tc, t_hbm) * 1e6, 2),
+                           "experts_touched": U, "steps": len(evs), "clocks": clocks}
+        blk.close()
+        del inputs, X, Y, blk
+        torch.cuda.empty_cache()
+    return res
 
 
 def traffic_of(stage: str, workload: str):
@@ -465,7 +532,11 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="nano_decode")
+    ap.add_argument("--workload", default="m3",
+                    help="workload of the headline line (default: the largest configuration, the MiniMax-M3 block)")
+    ap.add_argument("--other-configs", type=int, choices=[0, 1], default=1,
+                    help="also time the other configurations (one GPU only), under other_configs")
+    ap.add_argument("--other-steps", type=int, default=20)
     ap.add_argument("--path", choices=["decode", "grouped", "swapped"], default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gemm-pair", type=int, choices=[0, 1, 2], default=None,

@@ -31,8 +31,40 @@ constexpr int kMaxDevices = 64;
 // [blocks * E] histograms, then [E + 1] tile offsets, then [E + 1] active list
 __device__ __align__(256) int32_t g_dispatch_scratch[MOE_DISPATCH_NOALLOC_SCRATCH_INTS];
 
+// Device address of the array per device, with the unique id of the context it
+// was looked up in: after a device reset the library's module is loaded again in
+// a new context and the array may sit elsewhere, so a changed id means a new
+// lookup.
 std::mutex g_setup_mutex;
 int32_t *g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+// The current context's unique id (driver entry points fetched once), or 0.
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 __global__ void __launch_bounds__(kThreads) static_hist_kernel(const int32_t *topk_idx, int T, int k, int E,
                                                                 int32_t *blk_hist, int *bad) {
@@ -91,9 +123,15 @@ extern "C" moe_status moe_dispatch_noalloc(const int32_t *topk_idx, int T, int k
     using namespace moe;
     if (T < 0 || k < 1 || k > 16 || E < 1 || E > 256)
         return fail(MOE_ERR_INVALID_ARG, "moe_dispatch_noalloc: need T >= 0, 1 <= k <= 16, 1 <= E <= 256");
-    if (T == 0) return MOE_OK;
-    if (!topk_idx || !expert_offs || !sorted_token || !slot || !bad_index)
+    if (!expert_offs || !bad_index || (T > 0 && (!topk_idx || !sorted_token || !slot)))
         return fail(MOE_ERR_INVALID_ARG, "moe_dispatch_noalloc: NULL pointer");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (T == 0) {  // no rows: every offset 0, no bad index
+        if (cudaMemsetAsync(expert_offs, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess ||
+            cudaMemsetAsync(bad_index, 0, sizeof(int), s) != cudaSuccess)
+            return fail(MOE_ERR_CUDA, "moe_dispatch_noalloc: cudaMemsetAsync failed");
+        return MOE_OK;
+    }
     const long long nb = (T + kTokensPerBlock - 1) / kTokensPerBlock;
     if (nb * E + 2ll * (E + 1) > MOE_DISPATCH_NOALLOC_SCRATCH_INTS)
         return fail(MOE_ERR_UNSUPPORTED,
@@ -103,21 +141,25 @@ extern "C" moe_status moe_dispatch_noalloc(const int32_t *topk_idx, int T, int k
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return fail(MOE_ERR_CUDA, "moe_dispatch_noalloc: no usable current device");
+    // make the device's primary context current on this thread (allocates nothing)
+    if (cudaSetDevice(dev) != cudaSuccess) return fail(MOE_ERR_CUDA, "moe_dispatch_noalloc: cudaSetDevice failed");
     int32_t *scratch = nullptr;
     {
-        // first call on this device: the device address of the array (host code
-        // only sees a host-side stand-in for the symbol)
+        // first call on this device (or in a new context after a reset): the
+        // device address of the array; host code only sees a host-side stand-in
+        // for the symbol.  Without a context id the address is looked up each call.
+        const unsigned long long ctx = current_context_id();
         std::lock_guard<std::mutex> lock(g_setup_mutex);
-        if (g_scratch_addr[dev] == nullptr) {
+        if (g_scratch_addr[dev] == nullptr || ctx == 0 || g_scratch_ctx[dev] != ctx) {
             void *p = nullptr;
             e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
             if (e != cudaSuccess || p == nullptr)
                 return fail(MOE_ERR_CUDA, "moe_dispatch_noalloc: cudaGetSymbolAddress failed");
             g_scratch_addr[dev] = static_cast<int32_t *>(p);
+            g_scratch_ctx[dev] = ctx;
         }
         scratch = g_scratch_addr[dev];
     }
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int32_t *blk_hist = scratch;
     int32_t *tile_offs = scratch + nb * E;
     int32_t *active = tile_offs + (E + 1);

@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mxt_kernel(const __grid_cons
                             if (col_ok && c < t.m_valid) {
                                 const float h = glu_act(__uint_as_float(v[i]), x[r * (N + 1) + c], p.act, p.alpha,
                                                         p.limit, p.beta);
-                                sg.out[(size_t)(t.row0 + c) * sg.ldo + col] = __float2bfloat16_rn(h);
+                                static_cast<bf16 *>(sg.out)[(size_t)(t.row0 + c) * sg.ldo + col] = __float2bfloat16_rn(h);
                             }
                         }
                     }
@@ -561,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mxt_kernel(const __grid_cons
                     for (int i = 0; i < 32; ++i) {
                         const int c = c0 + i;
                         if (col_ok && c < t.m_valid)
-                            sg.out[(size_t)(t.row0 + c) * sg.ldo + col] = __float2bfloat16_rn(__uint_as_float(v[i]));
+                            static_cast<float *>(sg.out)[(size_t)(t.row0 + c) * sg.ldo + col] = __uint_as_float(v[i]);
                     }
                 }
             }

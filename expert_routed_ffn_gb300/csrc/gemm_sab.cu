@@ -14,7 +14,7 @@
 //       0-63 through shared memory, which apply the activation and store
 //       h[r][i0 + lane] (bf16)
 //   down    (glu = 0): D[128, N] = Wd[g][j0:j0+128] . h[r0:r0+N]^T
-//       lane l stores y[r][j0 + l] (bf16)
+//       lane l stores y[r][j0 + l] (fp32)
 // (stacked [out, in] expert weights: Arcee AFMoE issue, "Checkpoint weight
 // layout"; activation: HF AFMoE docs hidden_act silu, MiniMax-M3 issue
 // clamp-SwiGLU.)  Segments, persistent scheduling and bounded waits follow
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_sab_kernel(const __grid_cons
                             if (col_ok && c < t.m_valid) {
                                 const float h = glu_act(__uint_as_float(v[i]), x[r * (N + 1) + c], p.act,
                                                         p.alpha, p.limit, p.beta);
-                                sg.out[(size_t)(t.row0 + c) * sg.ldo + col] = __float2bfloat16_rn(h);
+                                static_cast<bf16 *>(sg.out)[(size_t)(t.row0 + c) * sg.ldo + col] = __float2bfloat16_rn(h);
                             }
                         }
                     }
@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_sab_kernel(const __grid_cons
                     for (int i = 0; i < 32; ++i) {
                         const int c = c0 + i;
                         if (col_ok && c < t.m_valid)
-                            sg.out[(size_t)(t.row0 + c) * sg.ldo + col] = __float2bfloat16_rn(__uint_as_float(v[i]));
+                            static_cast<float *>(sg.out)[(size_t)(t.row0 + c) * sg.ldo + col] = __uint_as_float(v[i]);
                     }
                 }
             }

@@ -25,7 +25,8 @@
 //              TMEM accumulators, so the epilogue of one tile overlaps the
 //              main loop of the next
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
-//              32*(w%4)..+31 = tile rows), activation (gate/up), bf16 stores
+//              32*(w%4)..+31 = tile rows), activation and bf16 stores (gate/up),
+//              fp32 stores (down projections)
 // Tiles are (segment, group, m-tile, n-tile) in a fixed order; the producer
 // claims them from a launch-wide ticket (the CTA that is free first takes the
 // next tile) and passes each id to the MMA and epilogue warps through a ring
@@ -197,8 +198,8 @@ struct EpiCtx {
 };
 
 // Epilogue role (kEpiWarps warps, named barrier 1): for each tile id from the
-// ring, wait for its accumulator, apply the activation (gate/up) and store bf16
-// rows, release the accumulator, and publish the m-tile's completion.  HALVES = 2:
+// ring, wait for its accumulator, apply the activation and store bf16 rows
+// (gate/up) or store the fp32 rows (down projections), release the accumulator, and publish the m-tile's completion.  HALVES = 2:
 // 256-row tiles in one CTA, one accumulator of 2 x 256 columns (half h's rows in
 // columns 256 h ..), no second buffer.
 template <bool PAIR, int kBM, int HALVES = 1>
@@ -255,7 +256,7 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
         const Tile t = hh == 0 ? tile0 : decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, hh);
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (a + hh) * kGemmBN;
         const bool row_ok = r < t.m_valid;
-        bf16 *orow = sg.out + t.ks * sg.split_stride + (size_t)(t.row0 + (row_ok ? r : 0)) * sg.ldo;
+        const size_t orow = t.ks * sg.split_stride + (size_t)(t.row0 + (row_ok ? r : 0)) * sg.ldo;
         if (sg.glu) {
             constexpr int kSpan = 128 / kEpiParts;  // output columns per slice
 #pragma unroll 1
@@ -274,7 +275,7 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
                                     p.alpha, p.limit, p.beta),
                             glu_act(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]),
                                     p.act, p.alpha, p.limit, p.beta));
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<bf16 *>(sg.out) + orow + col);
 #pragma unroll
                     for (int v = 0; v < 4; ++v)
                         dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
@@ -288,15 +289,11 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
                 tmem_ld32(tb + c0, v32);
                 tmem_ld_wait();
                 const int col = t.nt * kGemmBN + c0;
-                if (row_ok && col < sg.n_out) {
-                    uint32_t pk[16];
+                if (row_ok && col < sg.n_out) {  // fp32 rows: the combine rounds once
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<float *>(sg.out) + orow + col);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        pk[i] = pack_bf16x2(__uint_as_float(v32[2 * i]), __uint_as_float(v32[2 * i + 1]));
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    for (int v = 0; v < 8; ++v)
+                        dst[v] = make_uint4(v32[4 * v], v32[4 * v + 1], v32[4 * v + 2], v32[4 * v + 3]);
                 }
             }
         }

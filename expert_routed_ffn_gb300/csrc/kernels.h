@@ -169,9 +169,11 @@ cudaError_t launch_scatter(const ScatterArgs &a, cudaStream_t s);
 
 // --------------------------------------------------------------- combine (K7)
 // Y[t] = sum_j w[t,j] * Yslot[slot_of[t,j]] + Ys[t]  (fp32 sum, fixed order).
+// The slot and shared outputs are fp32: the one rounding to the output dtype is
+// the combine's.
 struct CombineArgs {
-    const __nv_bfloat16 *yslot;  // [T*k, H]
-    const __nv_bfloat16 *ys;     // shared output part 0 [T, H], or nullptr
+    const float *yslot;          // [T*k, H]
+    const float *ys;             // shared output part 0 [T, H], or nullptr
     int ys_parts;                // parts of a K-split shared down projection (>= 1), summed in order
     size_t ys_part_stride;       // elements from one part to the next
     const float *topk_w;         // [T, k]
@@ -231,7 +233,7 @@ struct GemmSegment {
     int k_blocks;          // K / 64 (of this segment)
     int k_base;            // first 64-wide k-block of A's columns and B's columns
     int n_out;             // valid output columns
-    __nv_bfloat16 *out;    // [rows, ldo]
+    void *out;             // [rows, ldo]: bf16 activations (glu), fp32 projection outputs (otherwise)
     int ldo;
     int glu;               // 1: gate/up pair (maps b0, b1) with the activation; 0: one projection (map b0)
     int map_a, map_b0, map_b1;  // indices into GemmArgs::maps
@@ -284,7 +286,7 @@ struct SabSegment {
     int w_tiles;               // weight tiles per group (64 gate/up outputs, or 128 down outputs)
     int k_blocks;              // K / 64
     int n_out;                 // valid output columns
-    __nv_bfloat16 *out;        // [rows, ldo]
+    void *out;                 // [rows, ldo]: bf16 activations (gate/up), fp32 outputs (down)
     int ldo;
 };
 struct SabArgs {
@@ -374,8 +376,8 @@ struct DecodeDownArgs {
     const __nv_bfloat16 *down;      // [E', H, I]
     const __nv_bfloat16 *sh_down;   // [H, S]
     int H, I, S;
-    __nv_bfloat16 *y_routed;        // [T*k, H]
-    __nv_bfloat16 *y_shared;        // [T, H]
+    float *y_routed;                // [T*k, H]
+    float *y_shared;                // [T, H]
     int num_sms;
 };
 cudaError_t launch_decode_down(const DecodeDownArgs &a, cudaStream_t s);

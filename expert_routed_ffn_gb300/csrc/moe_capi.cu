@@ -100,8 +100,10 @@ struct moe_handle {
     int32_t *topk_idx = nullptr, *blk_hist = nullptr, *offs = nullptr, *tile_offs = nullptr,
             *active = nullptr, *sorted_tok = nullptr, *slot_of = nullptr;
     float *topk_w = nullptr;
-    bf16 *x_sorted = nullptr, *x_bf16 = nullptr, *hbuf = nullptr, *hs = nullptr, *yslot = nullptr,
-         *ys = nullptr, *ys_split = nullptr;
+    bf16 *x_sorted = nullptr, *x_bf16 = nullptr, *hbuf = nullptr, *hs = nullptr;
+    // per-slot, shared and K-split partial outputs of the down projections: fp32, so
+    // that the combine rounds to the output dtype once
+    float *yslot = nullptr, *ys = nullptr, *ys_split = nullptr;
     void *x_stage = nullptr, *y_stage = nullptr;
     int *err = nullptr;
     bf16 *wr_parts = nullptr;  // router weights as exact bf16 splits [3, E, H]
@@ -301,11 +303,11 @@ void carve(moe_handle *h, void *base) {
     h->x_bf16 = h->x_f32 ? c.take<bf16>(base, MT * H) : nullptr;
     h->hbuf = c.take<bf16>(base, MT * k * h->I);
     h->hs = h->has_shared ? c.take<bf16>(base, MT * h->S) : nullptr;
-    h->yslot = c.take<bf16>(base, MT * k * H);
-    h->ys = h->has_shared ? c.take<bf16>(base, MT * H) : nullptr;
+    h->yslot = c.take<float>(base, MT * k * H);
+    h->ys = h->has_shared ? c.take<float>(base, MT * H) : nullptr;
     // partial products of a K-split shared down projection: the split is taken only
     // while parts x output tiles fit the SMs, so parts * T * H <= SMs * 128 * 256
-    h->ys_split = h->has_shared ? c.take<bf16>(base, split_elems(h)) : nullptr;
+    h->ys_split = h->has_shared ? c.take<float>(base, split_elems(h)) : nullptr;
     h->x_stage = c.take<char>(base, MT * H * elt);
     h->x_norm = h->norm ? c.take<char>(base, MT * H * elt) : nullptr;
     h->y_stage = c.take<char>(base, MT * H * elt);

@@ -391,33 +391,41 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
 constexpr int kRowMaxThreads = 1024;
 constexpr int kSlotBatch = 4;
 
-__device__ __forceinline__ void fma8(float w, const uint4 &r, float (&acc)[8]) {
-    acc[0] = fmaf(w, bf16_lo(r.x), acc[0]); acc[1] = fmaf(w, bf16_hi(r.x), acc[1]);
-    acc[2] = fmaf(w, bf16_lo(r.y), acc[2]); acc[3] = fmaf(w, bf16_hi(r.y), acc[3]);
-    acc[4] = fmaf(w, bf16_lo(r.z), acc[4]); acc[5] = fmaf(w, bf16_hi(r.z), acc[5]);
-    acc[6] = fmaf(w, bf16_lo(r.w), acc[6]); acc[7] = fmaf(w, bf16_hi(r.w), acc[7]);
+// 8 fp32 values at p (32-byte aligned)
+__device__ __forceinline__ void ld8(const float *p, float4 (&r)[2]) {
+    r[0] = __ldg(reinterpret_cast<const float4 *>(p));
+    r[1] = __ldg(reinterpret_cast<const float4 *>(p) + 1);
 }
 
-__device__ __forceinline__ void add8(const uint4 &r, float (&acc)[8]) {
-    acc[0] += bf16_lo(r.x); acc[1] += bf16_hi(r.x); acc[2] += bf16_lo(r.y); acc[3] += bf16_hi(r.y);
-    acc[4] += bf16_lo(r.z); acc[5] += bf16_hi(r.z); acc[6] += bf16_lo(r.w); acc[7] += bf16_hi(r.w);
+__device__ __forceinline__ void fma8(float w, const float4 (&r)[2], float (&acc)[8]) {
+    acc[0] = fmaf(w, r[0].x, acc[0]); acc[1] = fmaf(w, r[0].y, acc[1]);
+    acc[2] = fmaf(w, r[0].z, acc[2]); acc[3] = fmaf(w, r[0].w, acc[3]);
+    acc[4] = fmaf(w, r[1].x, acc[4]); acc[5] = fmaf(w, r[1].y, acc[5]);
+    acc[6] = fmaf(w, r[1].z, acc[6]); acc[7] = fmaf(w, r[1].w, acc[7]);
 }
 
-// Sum of the token's slot outputs (weights w) plus the shared outputs, in fp32,
-// in a fixed order (slots 0..k-1, then the shared expert's parts 0..P-1) for the
-// 8 columns at c.
+__device__ __forceinline__ void add8(const float4 (&r)[2], float (&acc)[8]) {
+    acc[0] += r[0].x; acc[1] += r[0].y; acc[2] += r[0].z; acc[3] += r[0].w;
+    acc[4] += r[1].x; acc[5] += r[1].y; acc[6] += r[1].z; acc[7] += r[1].w;
+}
+
+// Sum of the token's fp32 slot outputs (weights w) plus the shared outputs, in
+// fp32, in a fixed order (slots 0..k-1, then the shared expert's parts 0..P-1)
+// for the 8 columns at c.
 __device__ __forceinline__ void combine_columns(const CombineArgs &a, int t, int c, const int *s_slot,
                                                 const float *s_w, float (&acc)[8]) {
     const int H = a.H;
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = 0.f;
     for (int j0 = 0; j0 < a.k; j0 += kSlotBatch) {
-        uint4 r[kSlotBatch];
+        float4 r[kSlotBatch][2];
 #pragma unroll
         for (int u = 0; u < kSlotBatch; ++u) {
             const int slot = j0 + u < a.k ? s_slot[j0 + u] : -1;
-            r[u] = slot >= 0 ? __ldg(reinterpret_cast<const uint4 *>(a.yslot + (size_t)slot * H + c))
-                             : make_uint4(0u, 0u, 0u, 0u);
+            if (slot >= 0)
+                ld8(a.yslot + (size_t)slot * H + c, r[u]);
+            else
+                r[u][0] = r[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int u = 0; u < kSlotBatch; ++u)
@@ -425,12 +433,10 @@ __device__ __forceinline__ void combine_columns(const CombineArgs &a, int t, int
     }
     if (a.ys != nullptr) {
         for (int p0 = 0; p0 < a.ys_parts; p0 += kSlotBatch) {
-            uint4 r[kSlotBatch];
+            float4 r[kSlotBatch][2];
 #pragma unroll
             for (int u = 0; u < kSlotBatch; ++u)
-                if (p0 + u < a.ys_parts)
-                    r[u] = __ldg(reinterpret_cast<const uint4 *>(a.ys + (p0 + u) * a.ys_part_stride +
-                                                                 (size_t)t * H + c));
+                if (p0 + u < a.ys_parts) ld8(a.ys + (p0 + u) * a.ys_part_stride + (size_t)t * H + c, r[u]);
 #pragma unroll
             for (int u = 0; u < kSlotBatch; ++u)
                 if (p0 + u < a.ys_parts) add8(r[u], acc);

@@ -9,7 +9,7 @@
 // dispatch sort lists them).
 //
 // Gate/up: h[r, i] = act(Wg[e][i,:] . x_r, Wu[e][i,:] . x_r)   (bf16 out)
-// Down:    y[r, j] = Wd[e][j,:] . h_r                           (bf16 out)
+// Down:    y[r, j] = Wd[e][j,:] . h_r                           (fp32 out)
 // (stacked [out, in] expert weights: Arcee AFMoE issue, "Checkpoint weight layout")
 #include <mutex>
 
@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) decode_down_kernel(const DecodeDownA
         const int K = shared ? a.S : a.I;
         const bf16 *src = shared ? a.h_shared : a.h_routed + (size_t)row0 * a.I;
         const bf16 *Wd = shared ? a.sh_down : a.down + (size_t)expert * H * a.I;
-        bf16 *out = shared ? a.y_shared : a.y_routed + (size_t)row0 * H;
+        float *out = shared ? a.y_shared : a.y_routed + (size_t)row0 * H;
         const int j = rb * kRowsPerCta + warp;
         for (int tc = 0; tc < m; tc += kMT) {
             const int mt = min(kMT, m - tc);
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kThreads) decode_down_kernel(const DecodeDownA
             for (int t = 0; t < kMT; ++t) {
                 if (t < mt) {
                     const float y = warp_sum(acc[t]);
-                    if (lane == t) out[(size_t)(tc + t) * H + j] = __float2bfloat16_rn(y);
+                    if (lane == t) out[(size_t)(tc + t) * H + j] = y;
                 }
             }
         }

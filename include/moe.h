@@ -322,8 +322,11 @@ moe_status moe_inspect(const moe_handle *h, int buffer, void *dst, size_t bytes,
  * Limits: 1 <= k <= 16, 1 <= E <= 256 and ceil(T / 32) * E + 2 * (E + 1) <=
  *      MOE_DISPATCH_NOALLOC_SCRATCH_INTS (for E = 128: T <= 65440); larger
  *      sizes return MOE_ERR_UNSUPPORTED with a message, before any launch.
+ *      T = 0 writes zeros to expert_offs[0 .. E] and bad_index (topk_idx,
+ *      sorted_token and slot may then be NULL).
  * The first call on a device looks up the device address of the array (with
- * that device current); make that first call before any stream capture.  All
+ * that device current), and again after the device's context was reset; make
+ * that first call before any stream capture.  All
  * calls on one device share the array and it keeps the last call's contents
  * (every entry a call reads it writes first, so nothing needs clearing); calls
  * that overlap on the GPU race on it, so the caller must serialise them.

@@ -41,5 +41,6 @@ def pytest_sessionfinish(session, exitstatus):
     import json
     os.makedirs(out, exist_ok=True)
     with open(os.path.join(out, "parity_summary.json"), "w") as f:
-        json.dump([{"case": c, "max_abs_err_over_rms": a, "err_over_bound": b} for c, a, b in parity.RESULTS],
+        json.dump([{"case": c, "max_abs_err_over_rms": a, "max_err_vs_rounded_ref_over_rms": b,
+                    "elements_off_rounded_ref": n, "elements": m} for c, a, b, n, m in parity.RESULTS],
                   f, indent=1)

@@ -6,16 +6,21 @@ Tolerances:
     order inside a set is compared where neighbouring biased scores differ by
     more than 1e-5 (closer scores may legitimately swap between fp32 and fp64);
   * routing weights: per expert id, |w_gpu - w_ref| <= 1e-5 |w_ref| + 1e-7;
-  * outputs: |Y_gpu - Y_ref| <= 2e-2 * rms(Y_ref) + (half a bf16 ulp of Y_ref
-    when Y is stored in bf16), element-wise.  A bf16 output cannot be closer to
-    the fp64 value than half an ulp, and at |Y| ~ 5 rms that alone is up to
-    ~1.9% of rms, so the storage rounding of Y is added to the 2e-2 * rms budget
-    of the computation (bf16 expert weights and activations, fp32 accumulation).
-    The literal ratio max|Y_gpu - Y_ref| / rms(Y_ref) is recorded as well.
+  * outputs: max |Y_gpu - Y_ref| <= 2e-2 * rms(Y_ref), element-wise, with
+    Y_ref the fp64 oracle's output (bf16 storage of the activations between
+    the two projections, fp32 accumulation).  Two ratios are recorded per
+    check: that literal one, and max |Y_gpu - rne_bf16(Y_ref)| / rms(Y_ref)
+    against the oracle's output rounded once to the output dtype, with the
+    number of elements that land on the other bf16 neighbour of Y_ref.  The
+    second is recorded, not asserted: one bf16 ulp is 2^-5 rms at |Y| in
+    [4, 8) rms, so any disagreement in the last bit of such an element exceeds
+    2e-2 rms, and the bf16 hidden activations alone move Y by ~1e-3 rms.
 
 The oracle reads the same stored buffers as the CUDA path: the block takes
 bf16 expert weights, so a workload drawn in fp32 hands both sides the same
-bf16-rounded expert tensors (X and the router stay fp32 on both sides).
+bf16-rounded expert tensors (X and the router stay fp32 on both sides), except
+where a test asks for the fp32 originals (``host_inputs(..., as_drawn=True)``)
+to measure the rounding of the expert weights as well.
 """
 
 from __future__ import annotations
@@ -38,11 +43,17 @@ def make_case(shape, max_tokens=None, device="cuda"):
     return inputs, blk
 
 
-RESULTS = []  # (test id, literal max|dY|/rms, bound-normalised error) of every output check
+# every output check: (test id, max|Y - Y_ref| / rms, max|Y - rne_bf16(Y_ref)| / rms,
+# elements on the other bf16 neighbour of Y_ref, elements compared)
+RESULTS = []
 
 
-def host_inputs(inputs):
-    """Host copies of what the CUDA path reads (expert weights as stored: bf16)."""
+def host_inputs(inputs, as_drawn=False):
+    """Host copies of what the CUDA path reads (expert weights as stored: bf16),
+    or, with ``as_drawn``, of the tensors as the workload drew them (fp32 expert
+    weights of the fp32 workload)."""
+    if as_drawn:
+        return {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inputs.items()}
     experts = wl.expert_weights_bf16(inputs)
     out = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inputs.items() if k not in experts}
     for k, v in experts.items():
@@ -80,17 +91,30 @@ def check_route(shape, inputs_h, idx_gpu, w_gpu, tokens=None, w_rtol=W_RTOL):
     return ref
 
 
+def rne_bf16(y):
+    """fp64 values rounded to the nearest bf16 (ties to even), via fp32 (exact for
+    the magnitudes here: the fp32 rounding cannot create a bf16 tie)."""
+    f = np.ascontiguousarray(np.asarray(y, dtype=np.float64).astype(np.float32))
+    b = f.view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
+    return b.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def check_output(Y_gpu, Y_ref, out_bf16=True, tol=Y_TOL, tag=""):
+    """Asserts max |Y_gpu - Y_ref| <= tol * rms(Y_ref); returns that ratio."""
     Yg = np.asarray(Y_gpu, dtype=np.float64)
     rms = float(np.sqrt(np.mean(Y_ref ** 2)))
     assert np.isfinite(Yg).all(), "non-finite output"
     diff = np.abs(Yg - Y_ref)
-    bound = tol * rms + (bf16_half_ulp(Y_ref) if out_bf16 else 0.0)
-    worst = float((diff / bound).max())
     literal = float(diff.max()) / rms
-    RESULTS.append((tag, literal, worst))
-    assert worst <= 1.0, (f"|Y-Yref| exceeds {tol}*rms(+half bf16 ulp) by x{worst:.3f}; "
-                          f"max|Y-Yref|/rms = {literal:.4f}")
+    if out_bf16:
+        R = rne_bf16(Y_ref)
+        rounded = float(np.abs(Yg - R).max()) / rms
+        other = int((Yg != R).sum())
+    else:
+        rounded, other = literal, 0
+    RESULTS.append((tag, literal, rounded, other, int(Yg.size)))
+    assert literal <= tol, f"max|Y-Yref|/rms(Yref) = {literal:.4f} exceeds {tol}"
     return literal
 
 

@@ -78,8 +78,9 @@ def _check_layer(shape, inputs, blk, Y, tokens=None, tag=""):
     out_bf16 = shape.dtype == "bf16"
     P.check_output(Yg, Yref, out_bf16, tag=tag)
     if shape.mlp_norm != "none":
-        # the normed MLP output alone: the residual X is exact on both sides, the
-        # bf16 storage of the sum is the half ulp of the sum
+        # the normed MLP output alone, recovered as Y - X: the residual X is exact on
+        # both sides, and what is stored is the sum, so its bf16 rounding (half an
+        # ulp of Y, not of the MLP part) is part of this difference
         x = oracle.to_f64(ih["X"])
         if tokens is not None:
             x = x[tokens]

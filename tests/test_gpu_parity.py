@@ -90,6 +90,22 @@ def test_small_workload_every_token(name, path):
     assert blk.stats().path == PATHS[path][0]
 
 
+@pytest.mark.parametrize("path", list(PATHS))
+def test_tiny_fp32_against_fp32_expert_weights(path):
+    """The tiny workload as drawn: fp32 X, router and expert weights.  The block
+    stores its expert weights in bf16 and its GEMMs read X in bf16; the oracle
+    here runs on the fp32 originals, so the output error includes the rounding
+    of every expert weight and of X, and still meets 2e-2 rms.  The routing
+    stays fp32 on both sides, so the top-k is compared as everywhere else."""
+    shape = wl.TINY
+    inputs, blk, Y = _run(shape, PATHS[path])
+    assert inputs["gate"].dtype == torch.float32 and inputs["X"].dtype == torch.float32
+    drawn = P.host_inputs(inputs, as_drawn=True)
+    idx, w = _topk(blk, shape.T, shape.k)
+    P.check_route(shape, drawn, idx, w)
+    P.check_output(P.to_np(Y), oracle.forward_inputs(shape, drawn), out_bf16=False, tag=f"tiny_fp32_drawn-{path}")
+
+
 def test_clamp_swiglu_fires_and_matches():
     """Scaled gate/up weights push |gate| and |up| past limit 7 on many entries."""
     shape = SMALL["m3_small_packed"]

@@ -77,3 +77,35 @@ def test_noalloc_dispatch_rejects_sizes_beyond_its_scratch():
     st = lib.moe_dispatch_noalloc(_ptr(idx), T, 1, 128, _ptr(out), _ptr(out), _ptr(out), _ptr(out), None)
     assert st == capi.MOE_ERR_UNSUPPORTED
     assert "scratch" in lib.moe_last_error().decode()
+
+
+def test_noalloc_dispatch_out_of_range_ids_and_empty_batch():
+    """Ids outside [0, E) get slot -1 and raise bad_index; the valid slots keep
+    the stable (expert, token, slot) order and the offsets count only them.
+    An empty batch writes zero offsets and a clear bad_index."""
+    T, k, E = 70, 3, 16
+    g = torch.Generator().manual_seed(7)
+    idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    idx[0, 0] = -1
+    idx[33, 2] = E
+    idx[69, 1] = -1
+    offs, tok, slot, bad = _noalloc(idx.cuda(), T, k, E)
+    assert bad == 1
+    valid = [(int(idx[t, j]), t, j) for t in range(T) for j in range(k) if 0 <= idx[t, j] < E]
+    order = sorted(valid)
+    offs, tok, slot = offs.cpu(), tok.cpu(), slot.cpu().view(T, k)
+    assert int(offs[E]) == len(valid) and int(offs[0]) == 0
+    counts = torch.bincount(torch.tensor([e for e, _, _ in valid]), minlength=E)
+    assert torch.equal(offs[1:] - offs[:-1], counts.to(torch.int32))
+    for row, (e, t, j) in enumerate(order):
+        assert int(tok[row]) == t and int(slot[t, j]) == row
+    assert int(slot[0, 0]) == -1 and int(slot[33, 2]) == -1 and int(slot[69, 1]) == -1
+
+    lib = capi.load()
+    offs0 = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    bad0 = torch.full((1,), 5, dtype=torch.int32, device="cuda")
+    st = lib.moe_dispatch_noalloc(None, 0, k, E, _ptr(offs0), None, None, _ptr(bad0),
+                                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == capi.MOE_OK, lib.moe_last_error().decode()
+    torch.cuda.synchronize()
+    assert int(bad0.item()) == 0 and bool((offs0 == 0).all())
