@@ -45,29 +45,23 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 constexpr int kPathAuto = 0, kPathDecode = 1, kPathGrouped = 2, kPathSwapped = 3;
-// Auto path: the swapped-operand GEMMs only up to this many expected tokens
-// per expert (T*k/E).  Measured on GB300 they tie the grouped GEMMs on decode
-// sizes and lose where the shared expert sees many tokens (each weight tile is
-// re-read per token tile), so the auto path keeps the grouped GEMMs.
-constexpr int kSwapMaxTokensPerExpert = 0;
-// MX weights: the auto path takes the swapped-operand kernel (weights decoded into
-// tensor memory) up to this many routed slots per expert on average.  Measured on
-// GB300 (Nano decode, MXFP8): it is slower than the grouped MX kernel at every size
-// (47 + 29 us against 51 us), because each of its 128 x 32 x 16 MMAs costs about 280
-// cycles to issue and it needs twice as many per weight as the grouped kernel's
-// 128 x 256 x 16, so the auto path keeps the grouped kernel; MOE_OPT_PATH 3 selects it.
-constexpr int kMxtMaxSlotsPerExpert = 0;
-// Auto path: the decode kernels only up to this many tokens.  Measured on
-// GB300, the tcgen05 grouped path is at least as fast down to T = 1, so the
-// auto path always takes it; the decode kernels stay selectable.
-constexpr int kDecodeMaxTokens = 0;
-// L2 budget for the weight prefetch issued while routing (L2 is 129 MB).  Measured on
-// GB300 (Nano decode, two runs of 50 steps each): 88 MB 62.4 / 62.9 us per step,
-// 72 MB 63.3 / 63.3, 104 MB 63.5 / 63.6.
-#ifndef MOE_PREFETCH_MB
-#define MOE_PREFETCH_MB 88
+// Auto path: the tcgen05 grouped GEMMs (path 2) at every size, for bf16 and MX
+// weights.  Measured on GB300: the CUDA-core decode kernels (path 1) are slower
+// from T = 1 up (Zipf T = 1: 82 against 60 us per step; T = 8: 277 against 120);
+// the swapped-operand GEMMs (path 3) tie path 2 at decode sizes (Nano: 40.3 + 25.0
+// against 42.8 + 22.7 us) and lose 1.7x on the MiniMax-M3 block, where the shared
+// expert's 2048 tokens re-read every weight tile per token tile; with MX weights
+// path 3 is slower at every size (Nano MXFP8: 47 + 29 against 51 us: each of its
+// 128 x 32 x 16 MMAs costs about 280 cycles to issue and it needs twice as many
+// per weight as the grouped kernel's 128 x 256 x 16).  Paths 1 and 3 stay
+// selectable with MOE_OPT_PATH as diagnostic alternatives.
+// L2 share for the weight prefetch issued while routing, in tenths of the
+// device's L2 (GB300: 126.5 MB reported).  Measured on GB300 (Nano decode, two
+// runs of 50 steps each): 88 MB (0.7) 62.4 / 62.9 us per step, 72 MB 63.3 / 63.3,
+// 104 MB 63.5 / 63.6.  The prefetch never exceeds the experts' gate/up weights.
+#ifndef MOE_PREFETCH_L2_TENTHS
+#define MOE_PREFETCH_L2_TENTHS 7
 #endif
-constexpr unsigned long long kPrefetchBytes = (unsigned long long)MOE_PREFETCH_MB << 20;
 // CTAs issuing the prefetch (0: one per SM).  Measured on GB300 (Nano decode):
 // from 18 CTAs the prefetch lands while the router runs without slowing it; from
 // one CTA per SM it takes memory bandwidth from the latency-bound router and the
@@ -84,6 +78,7 @@ struct moe_handle {
     moe_config cfg;
     moe_weights w;
     int device = 0, num_sms = 0;
+    unsigned long long l2_bytes = 0;  // the device's L2 size (sizes the weight prefetch)
     int H = 0, E = 0, Ep = 0, k = 0, I = 0, S = 0;  // S: shared width actually used (I when packed)
     bool has_shared = false, x_f32 = false;
     bool dense = false;        // num_experts == 0: a dense MLP layer (the shared segments only)
@@ -860,13 +855,8 @@ moe_status run_swapped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
 moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStream_t s) {
     int n = 0;
     const long long slots = (long long)T * h->k;
-    int path = h->path_opt;
-    if (path == kPathAuto)
-        path = T <= kDecodeMaxTokens ? kPathDecode
-                                     : (slots <= (long long)kSwapMaxTokensPerExpert * h->E ? kPathSwapped : kPathGrouped);
+    int path = h->path_opt == kPathAuto ? kPathGrouped : h->path_opt;
     if (h->dense) path = kPathGrouped;  // a dense layer: the grouped GEMM's shared segments
-    if (h->wfmt != MOE_WEIGHTS_BF16 && !h->dense && h->path_opt == kPathAuto)
-        path = slots <= (long long)kMxtMaxSlotsPerExpert * h->E ? kPathSwapped : kPathGrouped;
     const int n_tok = slots <= 24ll * h->E ? 32 : 64;  // token tile of the swapped GEMMs
     h->ev_recorded = 0;
     // Decode-sized batches touch nearly every expert (about two or more tokens
@@ -878,7 +868,8 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
         // bytes of one expert's gate (or up) slice: bf16, or MX codes (1 or 1/2 byte per weight)
         const unsigned long long slice = (unsigned long long)h->I * h->H *
                                          (h->wfmt == MOE_WEIGHTS_BF16 ? 4 : h->wfmt == MOE_WEIGHTS_MXFP8 ? 2 : 1) / 2;
-        const unsigned long long each = kPrefetchBytes / 2 / slice * slice, all = slice * h->E;
+        const unsigned long long budget = h->l2_bytes * MOE_PREFETCH_L2_TENTHS / 10;
+        const unsigned long long each = budget / 2 / slice * slice, all = slice * h->E;
         moe::PrefetchArgs pa{{h->w.gate, h->w.up}, {each < all ? each : all, each < all ? each : all}};
         cudaError_t e = cudaEventRecord(h->ev_fork, s);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
@@ -1010,6 +1001,9 @@ moe_status moe_create(const moe_config *config, const moe_weights *weights, moe_
     }
     cudaError_t e = cudaGetDevice(&h->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+    int l2 = 0;
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, h->device);
+    h->l2_bytes = (unsigned long long)(l2 > 0 ? l2 : 0);
     if (e != cudaSuccess) {
         delete h;
         return cuda_fail(e, "device query");

@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
 // One CTA per token row, one thread per 8 columns: blockDim = 32 * ceil(H / 256)
 // (H <= 8192).  Loads go out in batches of four slot rows per thread.
 constexpr int kRowMaxThreads = 1024;
-constexpr int kSlotBatch = 4;
+constexpr int kSlotBatch = 2;  // fp32 rows: two slots (64 bytes per thread) in flight keep the 1024-thread CTA unspilled
 
 // 8 fp32 values at p (32-byte aligned)
 __device__ __forceinline__ void ld8(const float *p, float4 (&r)[2]) {
@@ -534,6 +534,99 @@ __global__ void __launch_bounds__(kRowMaxThreads) combine_kernel(const CombineAr
     trace_exit(a.trace);
 }
 
+// Without the post-norm every output element depends on its own column only.
+// The work is T * H / 4 units (token, 4-column group), consecutive units on
+// consecutive groups of a row; each CTA takes one contiguous range of units (a
+// multiple of its thread count) and walks it kFlatTok tokens at a time: it stages
+// those tokens' slot ids and weights in shared memory (one coalesced round trip),
+// then each thread takes units of the range, so a warp reads 512 contiguous bytes
+// of each term.  A unit's terms are its k slot rows (weights w) and then its P
+// shared parts (weight 1: fmaf(1, x, acc) rounds exactly as acc + x), in that
+// fixed order, in batches of kFlatBatch whose loads are all issued before any is
+// added: one round trip per unit and batch, up to kFlatBatch 16-byte loads in
+// flight per thread.
+constexpr int kFlatThreads = 256;
+constexpr int kFlatBatch = 8;
+constexpr int kFlatTok = 64;
+
+__global__ void __launch_bounds__(kFlatThreads, 3) combine_flat_kernel(const CombineArgs a) {
+    __shared__ int s_slot[kFlatTok * 16];
+    __shared__ float s_w[kFlatTok * 16];
+    trace_mark(a.trace, 0);
+    pdl_wait();
+    trace_mark(a.trace, 1);
+    pdl_trigger();
+    const int k = a.k, H = a.H, groups = H / 4;
+    const int parts = a.ys != nullptr ? a.ys_parts : 0, terms = k + parts;
+    const long long units = (long long)a.T * groups;
+    long long per = (units + gridDim.x - 1) / gridDim.x;
+    per = (per + kFlatThreads - 1) / kFlatThreads * kFlatThreads;
+    const long long u_begin = blockIdx.x * per, u_end = min(units, u_begin + per);
+    if (u_begin >= u_end) {
+        trace_exit(a.trace);
+        return;
+    }
+    const int t_last = (int)((u_end - 1) / groups);
+    for (int ts = (int)(u_begin / groups); ts <= t_last; ts += kFlatTok) {
+        const int nt = min(kFlatTok, t_last + 1 - ts);
+        __syncthreads();  // the previous tokens' ids are no longer read
+        for (int i = threadIdx.x; i < nt * k; i += kFlatThreads) {
+            s_slot[i] = __ldg(a.slot_of + (size_t)ts * k + i);
+            s_w[i] = __ldg(a.topk_w + (size_t)ts * k + i);
+        }
+        __syncthreads();
+        const long long lo = max(u_begin, (long long)ts * groups);
+        const long long hi = min(u_end, (long long)(ts + nt) * groups);
+        for (long long u = lo + threadIdx.x; u < hi; u += kFlatThreads) {
+            const int t = (int)(u / groups);
+            const int tl = t - ts;
+            const int c = (int)(u - (long long)t * groups) * 4;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j0 = 0; j0 < terms; j0 += kFlatBatch) {
+                float4 r[kFlatBatch];
+                float w[kFlatBatch];
+                bool on[kFlatBatch];
+#pragma unroll
+                for (int v = 0; v < kFlatBatch; ++v) {
+                    const int j = j0 + v;
+                    const float *src = nullptr;
+                    w[v] = 1.f;
+                    if (j < k) {
+                        const int slot = s_slot[tl * k + j];
+                        if (slot >= 0) {
+                            src = a.yslot + (size_t)slot * H + c;
+                            w[v] = s_w[tl * k + j];
+                        }
+                    } else if (j < terms) {
+                        src = a.ys + (size_t)(j - k) * a.ys_part_stride + (size_t)t * H + c;
+                    }
+                    on[v] = src != nullptr;
+                    if (on[v]) r[v] = __ldg(reinterpret_cast<const float4 *>(src));
+                }
+#pragma unroll
+                for (int v = 0; v < kFlatBatch; ++v) {
+                    if (on[v]) {
+                        acc.x = fmaf(w[v], r[v].x, acc.x);
+                        acc.y = fmaf(w[v], r[v].y, acc.y);
+                        acc.z = fmaf(w[v], r[v].z, acc.z);
+                        acc.w = fmaf(w[v], r[v].w, acc.w);
+                    }
+                }
+            }
+            const size_t off = (size_t)t * H + c;
+            if (a.y_f32) {
+                *reinterpret_cast<float4 *>(static_cast<float *>(a.Y) + off) = acc;
+            } else {
+                uint2 o;
+                o.x = pack_bf16x2(acc.x, acc.y);
+                o.y = pack_bf16x2(acc.z, acc.w);
+                *reinterpret_cast<uint2 *>(static_cast<bf16 *>(a.Y) + off) = o;
+            }
+        }
+    }
+    trace_exit(a.trace);
+}
+
 // ------------------------------------------------------------- pre-MLP norm
 
 __global__ void __launch_bounds__(kRowMaxThreads) rmsnorm_kernel(const NormArgs a) {
@@ -613,8 +706,8 @@ static int row_threads(int H) { return ((H / 8 + 31) / 32) * 32; }
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
     static std::once_flag once;
     std::call_once(once, [] {
-        max_smem_carveout(combine_kernel<false>);
         max_smem_carveout(combine_kernel<true>);
+        max_smem_carveout(combine_flat_kernel);
     });
     if (a.H % 8 != 0 || row_threads(a.H) > kRowMaxThreads || a.k > 16 || (a.ys != nullptr && a.ys_parts < 1))
         return cudaErrorInvalidValue;
@@ -624,12 +717,24 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return cudaErrorInvalidValue;
-    const int grid = a.T < sms * kCombineCtasPerSm ? a.T : sms * kCombineCtasPerSm;
     if (a.norm != 0) {
         if (a.residual == nullptr || a.post_w == nullptr) return cudaErrorInvalidValue;
+        const int grid = a.T < sms * kCombineCtasPerSm ? a.T : sms * kCombineCtasPerSm;
         return launch_pdl(combine_kernel<true>, dim3(grid), dim3(row_threads(a.H)), 0, s, a);
     }
-    return launch_pdl(combine_kernel<false>, dim3(grid), dim3(row_threads(a.H)), 0, s, a);
+    // the flat kernel: as many CTAs as are resident at once on every SM, capped by the chunks
+    static int flat_per_sm = 0;
+    static std::once_flag occ;
+    std::call_once(occ, [] {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&flat_per_sm, combine_flat_kernel, kFlatThreads, 0) !=
+                cudaSuccess || flat_per_sm < 1)
+            flat_per_sm = 1;
+    });
+    // CTAs: as many as are resident at once, at most one per kFlatThreads units
+    const long long units = (long long)a.T * (a.H / 4);
+    const long long need = (units + kFlatThreads - 1) / kFlatThreads;
+    const int grid = (int)(need < (long long)sms * flat_per_sm ? need : (long long)sms * flat_per_sm);
+    return launch_pdl(combine_flat_kernel, dim3(grid), dim3(kFlatThreads), 0, s, a);
 }
 
 cudaError_t launch_rmsnorm(const NormArgs &a, cudaStream_t s) {

@@ -193,9 +193,12 @@ const char *moe_last_error(void);
  * Options, statistics and inspection (tests and measurement).
  */
 typedef enum {
-    MOE_OPT_PATH = 0,          /* 0 auto, 1 weight-streaming decode kernels, 2 tcgen05 grouped GEMMs
-                                  (tokens as M), 3 tcgen05 swapped-operand GEMMs (weights as M, for
-                                  few tokens per expert) */
+    MOE_OPT_PATH = 0,          /* 0 auto (= 2 at every size), 1 weight-streaming decode kernels on
+                                  the CUDA cores, 2 tcgen05 grouped GEMMs (tokens as M), 3 tcgen05
+                                  swapped-operand GEMMs (weights as M).  Paths 1 and 3 are
+                                  diagnostic alternatives kept for comparison and parity tests: on
+                                  GB300 path 1 is slower than path 2 from T = 1 up and path 3 at
+                                  best ties it, so the auto path never selects them */
     MOE_OPT_WAIT_LIMIT_NS = 1, /* bound of every device-side wait in ns (default 500000000);
                                   0 makes the first wait that finds its data not ready give up,
                                   which exercises the timeout path */
