@@ -537,6 +537,9 @@ def main():
     ap.add_argument("--other-configs", type=int, choices=[0, 1], default=1,
                     help="also time the other configurations (one GPU only), under other_configs")
     ap.add_argument("--other-steps", type=int, default=20)
+    ap.add_argument("--shape", action="append", default=[], metavar="KEY=VALUE",
+                    help="override a field of the workload (e.g. T=256, num_experts=16) for a smaller "
+                         "case of the same kernels, such as a profiler capture")
     ap.add_argument("--path", choices=["decode", "grouped", "swapped"], default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gemm-pair", type=int, choices=[0, 1, 2], default=None,
@@ -554,6 +557,13 @@ def main():
         raise SystemExit("--warmup must be at least 3")
     from expert_routed_ffn_gb300 import workloads as wl
     shape = wl.WORKLOADS[args.workload]
+    if args.shape:
+        kw = {}
+        for item in args.shape:
+            key, val = item.split("=", 1)
+            cur = getattr(shape, key)
+            kw[key] = val in ("1", "true", "True") if isinstance(cur, bool) else type(cur)(val)
+        shape = shape.replace(name=shape.name + "_" + "_".join(args.shape), **kw)
     if args.impl == "reference":
         run_reference(args, shape)
     else:
