@@ -63,12 +63,17 @@ constexpr int kRing = 8;                        // tile ids in flight from the p
 // 32 KB: larger copies keep a CTA's TMA stream near the MMA's rate), 3 stages;
 // a tile is 256 rows (128 per CTA).  A stage holds kKB consecutive 16 KB
 // (A) and kBBytes / kKB (B) k-block tiles.
-template <bool PAIR>
+// THIN (one CTA, every m-tile at most kThinRows rows, i.e. T <= kThinRows): the A
+// rows come in boxes of kThinRows rows (4 KB), so six stages of 36 KB keep 192 KB of
+// weights in flight instead of 128 KB; the MMA still reads 128 rows of A, the rows
+// past the box being whatever shared memory follows (their outputs are never stored).
+constexpr int kThinRows = 32;
+template <bool PAIR, bool THIN = false>
 struct GemmCfg {
     static constexpr int kKB = PAIR ? 2 : 1;     // k-blocks per stage
-    static constexpr int kStages = PAIR ? 3 : 4;
+    static constexpr int kStages = PAIR ? 3 : (THIN ? 6 : 4);
     static constexpr int kBBytes = (PAIR ? kGemmBN / 2 : kGemmBN) * kGemmBK * 2 * kKB;
-    static constexpr int kAStage = kABytes * kKB;
+    static constexpr int kAStage = (THIN ? kThinRows * kGemmBK * 2 : kABytes) * kKB;
     static constexpr int kStageBytes = kAStage + kBBytes;
     static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers, tile ring*/;
     static constexpr int kBM = PAIR ? 2 * kGemmBM : kGemmBM;  // rows per tile
@@ -321,9 +326,9 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
     }
 }
 
-template <bool PAIR>
+template <bool PAIR, bool THIN = false>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmArgs p) {
-    using C = GemmCfg<PAIR>;
+    using C = GemmCfg<PAIR, THIN>;
     constexpr int kStages = C::kStages, kBBytes = C::kBBytes, kStageBytes = C::kStageBytes, kBM = C::kBM;
     constexpr int kKB = C::kKB, kAStage = C::kAStage;
     extern __shared__ uint8_t smem_raw[];
@@ -1318,6 +1323,8 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
                              GemmCfg<false>::kSmemBytes);
         cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              GemmCfg<true>::kSmemBytes);
+        cudaFuncSetAttribute(gemm_tc_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             GemmCfg<false, true>::kSmemBytes);
         cudaFuncSetAttribute(gemm_mx_kernel<kWeightsMxfp8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              MxCfg<kWeightsMxfp8>::kSmemBytes);
         cudaFuncSetAttribute(gemm_mx_kernel<kWeightsMxfp4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1349,6 +1356,9 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
         return launch_pdl_cluster(gemm_tc_kernel<true>, dim3(a.num_ctas), dim3(kThreads),
                                   (size_t)GemmCfg<true>::kSmemBytes, s, dim3(2, 1, 1), a);
     }
+    if (a.thin)
+        return launch_pdl(gemm_tc_kernel<false, true>, dim3(a.num_ctas), dim3(kThreads),
+                          (size_t)GemmCfg<false, true>::kSmemBytes, s, a);
     return launch_pdl(gemm_tc_kernel<false>, dim3(a.num_ctas), dim3(kThreads), (size_t)GemmCfg<false>::kSmemBytes,
                       s, a);
 }

@@ -272,6 +272,8 @@ struct GemmArgs {
     // epilogue working, CTA time past the dependency wait, tiles
     unsigned long long *stats;
     int wfmt;              // WeightFormat of every segment's B maps; MX only without CTA pairs
+    int thin;              // one CTA per tile, bf16, every m-tile <= 32 rows: A maps with boxes of 32
+                           // rows, six stages (gemm_tc.cu, kThinRows)
 };
 constexpr int kGemmStats = 8;
 cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s);

@@ -650,6 +650,27 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         }
     }
     g.wfmt = h->wfmt;
+    // at most 32 tokens: every m-tile has at most 32 rows (a token picks an expert
+    // once), so the A rows come in 32-row boxes and the ring holds more weights
+    const bool thin = !pair && !mx && T <= 32;
+    g.thin = thin ? 1 : 0;
+    if (thin) {
+        if (!h->dense) {
+            g.maps[kXs] = h->m_xs_n[0];
+            g.maps[kHb] = h->m_hb_n[0];
+        }
+        if (h->has_shared) {
+            if (h->x_f32) {
+                g.maps[kX] = h->m_xbf_n[0];
+            } else {
+                const CUtensorMap *mx32 = nullptr;
+                moe_status st = x_map_box(h, X, T, 0, &mx32);
+                if (st != MOE_OK) return st;
+                g.maps[kX] = *mx32;
+            }
+            g.maps[kHs] = h->m_hs_n[0];
+        }
+    }
     const int sh_base = h->cfg.shared_packed ? E : 0;
     const int nt_gu = (I + 127) / 128, nt_sgu = (S + 127) / 128, nt_d = (H + moe::kGemmBN - 1) / moe::kGemmBN;
     const bool fused = h->fuse_experts;
@@ -862,8 +883,13 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     // Decode-sized batches touch nearly every expert (about two or more tokens
     // per expert expected): while the routing kernels run, a side stream warms
     // L2 with the first experts' gate and up slices, the fused GEMM's first tiles.
+    // Not when the dispatch's copy of the token rows alone would sweep L2 (more
+    // than a quarter of it): measured on GB300, the prefetch then costs 0.2-0.7%
+    // (AFMoE prefill, MiniMax-M3, Zipf T = 4096) instead of saving 2-6% (Nano
+    // decode, Zipf T = 64 and 512).
     const bool prefetch = h->prefetch_opt && !h->dense && path == kPathGrouped && h->fuse_experts &&
-                          slots >= 2ll * h->E && h->side != nullptr;
+                          slots >= 2ll * h->E && (unsigned long long)slots * h->H * 2 <= h->l2_bytes / 4 &&
+                          h->side != nullptr;
     if (prefetch) {
         // bytes of one expert's gate (or up) slice: bf16, or MX codes (1 or 1/2 byte per weight)
         const unsigned long long slice = (unsigned long long)h->I * h->H *

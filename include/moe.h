@@ -207,7 +207,8 @@ typedef enum {
     MOE_OPT_FUSE_EXPERTS = 3,  /* path 2: 1 (default) runs the gate/up and down GEMMs as one
                                   persistent launch whose down tiles wait for their gate/up rows;
                                   0 runs them as two launches */
-    MOE_OPT_PREFETCH = 4,      /* 1 (default): when T*k >= 2E (nearly every expert is touched), an
+    MOE_OPT_PREFETCH = 4,      /* 1 (default): when T*k >= 2E (nearly every expert is touched) and the
+                                  expert-sorted copy of the T*k token rows is at most a quarter of L2, an
                                   internal side stream prefetches the first experts' gate/up weights
                                   into L2 while the routing kernels run (forked from and joined back
                                   into the caller's stream); 0: no prefetch.  A hint: results are
