@@ -376,7 +376,7 @@ OTHER_CONFIGS = ("tiny", "nano_decode", "afmoe_prefill", "zipf_T1", "zipf_T8", "
 def other_configs(args, headline: str, dev, flush_l2):
     """Step time, tokens/s, block roofline fraction and clocks of each other
     workload: the same timed steps as the headline (L2 flushed before each,
-    CUDA events around the forward), fewer of them."""
+    CUDA events around the forward), repeated for at least 0.4 s."""
     import torch
 
     from expert_routed_ffn_gb300 import capi
@@ -408,9 +408,14 @@ def other_configs(args, headline: str, dev, flush_l2):
         while time.perf_counter() < t_end:
             step()
             torch.cuda.synchronize()
+        # at least other_steps timed steps and at least 0.4 s of them, so that the
+        # clock sampler (every 100 ms) sees this workload under load
         sampler = ClockSampler(f"GPU-{torch.cuda.get_device_properties(dev).uuid}")
-        evs = [step() for _ in range(args.other_steps)]
-        torch.cuda.synchronize()
+        evs = []
+        t_end = time.perf_counter() + 0.4
+        while len(evs) < args.other_steps or time.perf_counter() < t_end:
+            evs.extend(step() for _ in range(args.other_steps))
+            torch.cuda.synchronize()
         clocks = sampler.stop()
         if blk.sync_status() != capi.MOE_OK:
             raise SystemExit(f"device error while timing {name}")
