@@ -63,10 +63,11 @@ constexpr int kRing = 8;                        // tile ids in flight from the p
 // 32 KB: larger copies keep a CTA's TMA stream near the MMA's rate), 3 stages;
 // a tile is 256 rows (128 per CTA).  A stage holds kKB consecutive 16 KB
 // (A) and kBBytes / kKB (B) k-block tiles.
-// THIN (one CTA, every m-tile at most kThinRows rows, i.e. T <= kThinRows): the A
-// rows come in boxes of kThinRows rows (4 KB), so six stages of 36 KB keep 192 KB of
-// weights in flight instead of 128 KB; the MMA still reads 128 rows of A, the rows
-// past the box being whatever shared memory follows (their outputs are never stored).
+// THIN (one CTA, decode sizes): tiles of kThinRows = 32 rows (the dispatch counts
+// 32-row m-tiles), A rows in boxes of 32 rows (4 KB), so six stages of 36 KB keep
+// 192 KB of weights in flight instead of 128 KB; the MMA still reads 128 rows of A,
+// the rows past the box being whatever shared memory follows (their outputs are
+// never stored).
 constexpr int kThinRows = 32;
 template <bool PAIR, bool THIN = false>
 struct GemmCfg {
@@ -76,7 +77,7 @@ struct GemmCfg {
     static constexpr int kAStage = (THIN ? kThinRows * kGemmBK * 2 : kABytes) * kKB;
     static constexpr int kStageBytes = kAStage + kBBytes;
     static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers, tile ring*/;
-    static constexpr int kBM = PAIR ? 2 * kGemmBM : kGemmBM;  // rows per tile
+    static constexpr int kBM = PAIR ? 2 * kGemmBM : (THIN ? kThinRows : kGemmBM);  // rows per tile
 };
 
 struct Tile {
@@ -103,7 +104,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, const i
     while (t.seg + 1 < p.num_segs && tile >= seg_end[t.seg]) ++t.seg;
     if (t.seg > 0) tile -= seg_end[t.seg - 1];
     const GemmSegment &s = p.seg[t.seg];
-    constexpr int kSub = BM / kGemmBM;  // 128-row parts of a tile
+    constexpr int kRows = BM < kGemmBM ? BM : kGemmBM;  // rows of a tile per CTA
+    constexpr int kSub = BM / kRows;                    // CTA parts of a tile (2 with CTA pairs)
     if (s.dense) {
         const int mtiles = (s.m_dense + BM - 1) / BM;
         t.group = 0;
@@ -111,8 +113,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, const i
         tile -= t.ks * mtiles * s.n_tiles;
         t.nt = tile / mtiles;
         t.mt = tile % mtiles;
-        t.row0 = t.mt * BM + half * kGemmBM;
-        t.m_valid = min(kGemmBM, s.m_dense - t.row0);
+        t.row0 = t.mt * BM + half * kRows;
+        t.m_valid = min(kRows, s.m_dense - t.row0);
         t.ready = s.ready_base + kSub * t.mt + half;
     } else {
         // largest group whose first tile is <= tile (empty groups own no tiles)
@@ -131,8 +133,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, const i
         t.nt = local / mt_g;
         t.mt = local % mt_g;
         const int start = offs[lo];
-        t.row0 = start + t.mt * BM + half * kGemmBM;
-        t.m_valid = min(kGemmBM, offs[lo + 1] - t.row0);  // <= 0: the odd CTA of a pair past the group's rows
+        t.row0 = start + t.mt * BM + half * kRows;
+        t.m_valid = min(kRows, offs[lo + 1] - t.row0);  // <= 0: the odd CTA of a pair past the group's rows
         t.ready = s.ready_base + kSub * (toffs[lo] + t.mt) + half;
     }
     return t;

@@ -59,6 +59,8 @@ constexpr int kPathAuto = 0, kPathDecode = 1, kPathGrouped = 2, kPathSwapped = 3
 // device's L2 (GB300: 126.5 MB reported).  Measured on GB300 (Nano decode, two
 // runs of 50 steps each): 88 MB (0.7) 62.4 / 62.9 us per step, 72 MB 63.3 / 63.3,
 // 104 MB 63.5 / 63.6.  The prefetch never exceeds the experts' gate/up weights.
+// rows of an m-tile at decode sizes (gemm_tc.cu kThinRows)
+constexpr int kThinRows = 32;
 #ifndef MOE_PREFETCH_L2_TENTHS
 #define MOE_PREFETCH_L2_TENTHS 7
 #endif
@@ -87,6 +89,7 @@ struct moe_handle {
     void *x_norm = nullptr;    // pre_mlp norm output [max_tokens, H] in the activation dtype
     const bf16 *sh_gate = nullptr, *sh_up = nullptr, *sh_down = nullptr;  // shared tensors (or slice E)
     int path_opt = kPathAuto;
+    bool thin_now = false;  // this forward: 32-row m-tiles, the GEMM's 32-row A boxes (gemm_tc.cu THIN)
     unsigned long long wait_ns = 500000000ull;
 
     // workspace
@@ -310,11 +313,12 @@ void carve(moe_handle *h, void *base) {
     h->trace = c.take<unsigned long long>(base, MOE_TRACE_FIELDS * moe_handle::kMaxStages);
     h->gemm_stats = c.take<unsigned long long>(base, moe::kGemmStats);
     h->router_stats = c.take<unsigned long long>(base, moe::kRouterStats);
-    // routed m-tiles number at most T*k/128 + E; the shared expert's follow
-    // (with CTA pairs, 2 counters per 256-row tile: at most T*k/128 + 2E + 2 routed and
-    // 2*ceil(T/256) + 2 shared)
-    h->ready_shared_base = (int)(MT * k / 128 + 2 * E + 2);
-    h->ready = c.take<int>(base, (size_t)h->ready_shared_base + 2 * ((MT + 255) / 256) + 2);
+    // routed m-tiles number at most T*k/32 + E (32-row m-tiles at decode sizes; with
+    // CTA pairs 2 counters per 256-row tile: at most T*k/128 + 2E + 2); the shared
+    // expert's follow (at most ceil(T/32) + 2)
+    h->ready_shared_base = (int)(MT * k / kThinRows + 2 * E + 2);
+    const size_t shared_counters = std::max((MT + kThinRows - 1) / kThinRows, 2 * ((MT + 255) / 256)) + 2;
+    h->ready = c.take<int>(base, (size_t)h->ready_shared_base + shared_counters);
     h->wr_flags = c.take<int>(base, 64);
     h->tile_counters = c.take<int>(base, 64);
     h->ws_bytes = round_up(c.off, 256);
@@ -561,7 +565,8 @@ moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n
     xa.ready = h->ready;
     xa.ready_shared_base = h->ready_shared_base;
     xa.ready_per_tile = h->pair_now ? 2 : 1;
-    xa.ready_shared_count = h->pair_now ? 2 * ((T + 255) / 256) : (T + 127) / 128;
+    xa.ready_shared_count = h->pair_now ? 2 * ((T + 255) / 256) : (h->thin_now ? (T + kThinRows - 1) / kThinRows
+                                                                               : (T + 127) / 128);
     xa.tile_counters = h->tile_counters;
     xa.T = T;
     xa.k = h->k;
@@ -650,9 +655,9 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         }
     }
     g.wfmt = h->wfmt;
-    // at most 32 tokens: every m-tile has at most 32 rows (a token picks an expert
-    // once), so the A rows come in 32-row boxes and the ring holds more weights
-    const bool thin = !pair && !mx && T <= 32;
+    // decode sizes: 32-row m-tiles (the dispatch counted them), A rows in 32-row
+    // boxes, so the ring holds more weights
+    const bool thin = h->thin_now;
     g.thin = thin ? 1 : 0;
     if (thin) {
         if (!h->dense) {
@@ -916,6 +921,10 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     // (MX weights: 256-row tiles in one CTA each, two MMAs on every decoded weight tile)
     h->pair_now = path == kPathGrouped && h->num_sms >= 2 &&
                   (h->pair_opt == 1 || (h->pair_opt == 2 && (h->dense ? T >= 256 : slots >= 256ll * h->E)));
+    // 32-row m-tiles at decode sizes: at most 32 routed rows per expert on average
+    // (T * k <= 32 E) or at most 32 tokens (then no m-tile has more than 32 rows)
+    h->thin_now = path == kPathGrouped && !h->pair_now && h->wfmt == MOE_WEIGHTS_BF16 &&
+                  (T <= kThinRows || (h->E > 0 && slots <= (long long)kThinRows * h->E));
     h->shared_parts = path == kPathGrouped && h->has_shared ? shared_parts(h, T) : 1;
     mark(h, 0, s);
     moe_status st = MOE_OK;
@@ -923,7 +932,7 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     // a dense layer has no router and no dispatch: its GEMM's counters (zeroed by
     // the dispatch in a MoE layer) are zeroed by the pre-norm kernel, or here
     int *const zero_a = h->dense ? h->ready + h->ready_shared_base : nullptr;
-    const int zero_a_n = h->dense ? 2 * ((T + 255) / 256) + 2 : 0;
+    const int zero_a_n = h->dense ? std::max((T + kThinRows - 1) / kThinRows, 2 * ((T + 255) / 256)) + 2 : 0;
     int *const zero_b = h->dense ? h->tile_counters : nullptr;
     const int zero_b_n = h->dense ? 2 : 0;
     if (h->norm) {
@@ -938,7 +947,8 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     }
     if (st == MOE_OK && !h->dense)
         st = run_front(h, Xm, T, s, &n,
-                       path == kPathSwapped ? n_tok : (h->pair_now ? 2 * moe::kGemmBM : moe::kGemmBM));
+                       path == kPathSwapped ? n_tok
+                                            : (h->pair_now ? 2 * moe::kGemmBM : (h->thin_now ? kThinRows : moe::kGemmBM)));
     if (st == MOE_OK) {
         if (path == kPathDecode)
             st = run_decode(h, Xm, T, s, &n);
