@@ -21,6 +21,13 @@ from expert_routed_ffn_gb300 import workloads as wl
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from expert_routed_ffn_gb300 import build
+    build.build()
+    capi.load()
+
+
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
@@ -54,8 +61,6 @@ def _noalloc(idx, T, k, E):
 
 
 def test_noalloc_dispatch_matches_forward_on_two_calls_in_a_row():
-    from expert_routed_ffn_gb300 import build
-    build.build()
     big = wl.NANO_DECODE                                   # T 256, E 128, k 8
     small = wl.AFMOE_PREFILL.replace(T=333, hidden_size=512, moe_intermediate_size=192,
                                      shared_intermediate_size=384)  # ragged T, E 64, k 6
