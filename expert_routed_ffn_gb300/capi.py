@@ -32,6 +32,7 @@ MOE_OPT_PATH, MOE_OPT_WAIT_LIMIT_NS, MOE_OPT_STAGE_EVENTS, MOE_OPT_FUSE_EXPERTS,
 MOE_OPT_TRACE = 5
 MOE_OPT_GEMM_PAIR = 6
 MOE_OPT_GRAPH = 8
+MOE_OPT_PAIR_SWAP = 9
 MOE_BUF_GEMM_STATS = 6
 MOE_BUF_ROUTER_STATS = 7
 MOE_BUF_NORMED_X = 8

@@ -17,6 +17,16 @@
 // resident (one per SM): a down tile only waits for tiles claimed before it,
 // which do not wait, so the waits end.
 //
+// CTA pairs (256-row m-tiles): an expert's m-tile of at most 128 rows (its last, or
+// its only one) runs with the operands swapped, the pair's 256 weight rows as M and
+// the tile's rows, rounded up to 32, as N: each CTA loads half of those token rows
+// and 128 weight rows (a gate/up tile: 64 gate and 64 up rows of the same 64
+// features), and the MMA skips most of the padding rows that a 256-row token tile
+// would carry.  Each output is the same K-ordered sum of the same products, so the
+// results are bit-identical to the unswapped tile (tested).  Measured on GB300:
+// AFMoE prefill 552 against 571 us, Zipf T = 4096 575 against 595 us; a bound of 64
+// or 96 rows instead of 128 is slower.
+//
 // Persistent kernel, one CTA per SM, 6 warps:
 //   warp 0     TMA producer: A tile 128 x 64 and B tile 256 x 64 (gate/up: 128
 //              gate rows + 128 up rows) per stage, 128-byte swizzle, 4 stages
@@ -76,14 +86,23 @@ struct GemmCfg {
     static constexpr int kBBytes = (PAIR ? kGemmBN / 2 : kGemmBN) * kGemmBK * 2 * kKB;
     static constexpr int kAStage = (THIN ? kThinRows * kGemmBK * 2 : kABytes) * kKB;
     static constexpr int kStageBytes = kAStage + kBBytes;
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers, tile ring*/;
+    // CTA pairs: the gate values' hand-over buffer of swapped gate/up tiles, 2 x 32 x 32 fp32
+    static constexpr int kXBufBytes = PAIR ? 8192 : 0;
+    static constexpr int kSmemBytes =
+        kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers, tile ring*/ + kXBufBytes;
     static constexpr int kBM = PAIR ? 2 * kGemmBM : (THIN ? kThinRows : kGemmBM);  // rows per tile
 };
 
 struct Tile {
     int seg, group, mt, nt, ks, row0, m_valid, ready;  // ks: K range; row0, m_valid: this CTA's rows;
                                                        // ready: its m-tile's counter
+    int swp;  // swapped operands (CTA pairs): row0, m_valid = the whole m-tile's rows
 };
+
+// Swapped-operand tiles of a CTA pair: the MMA's N (token columns, a multiple of 32,
+// half of them in each CTA's shared memory) and the rows of the token box each CTA loads.
+__device__ __forceinline__ int swap_n(int rows) { return (rows + 31) / 32 * 32; }
+__device__ __forceinline__ int swap_box(int rows) { return swap_n(rows) / 2 <= 32 ? 32 : 64; }
 
 // offs / toffs: shared-memory copies of the grouped segments' dispatch offsets
 // (toffs counts tiles of BM rows)
@@ -101,6 +120,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, const i
                                             const int *toffs, int half) {
     Tile t;
     t.seg = 0;
+    t.swp = 0;
     while (t.seg + 1 < p.num_segs && tile >= seg_end[t.seg]) ++t.seg;
     if (t.seg > 0) tile -= seg_end[t.seg - 1];
     const GemmSegment &s = p.seg[t.seg];
@@ -133,8 +153,16 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, const i
         t.nt = local / mt_g;
         t.mt = local % mt_g;
         const int start = offs[lo];
-        t.row0 = start + t.mt * BM + half * kRows;
-        t.m_valid = min(kRows, offs[lo + 1] - t.row0);  // <= 0: the odd CTA of a pair past the group's rows
+        const int rows = min(BM, offs[lo + 1] - (start + t.mt * BM));  // of the m-tile
+        if (kSub == 2 && p.swap_rem && rows <= kSwapMaxRows) {
+            // weights as M, the m-tile's rows as N: both CTAs' outputs cover all its rows
+            t.swp = 1;
+            t.row0 = start + t.mt * BM;
+            t.m_valid = rows;
+        } else {
+            t.row0 = start + t.mt * BM + half * kRows;
+            t.m_valid = min(kRows, offs[lo + 1] - t.row0);  // <= 0: the odd CTA of a pair past the group's rows
+        }
         t.ready = s.ready_base + kSub * (toffs[lo] + t.mt) + half;
     }
     return t;
@@ -202,6 +230,7 @@ struct EpiCtx {
     int total;
     const int *s_seg_end, *s_offs, *s_toffs;
     int half;
+    float *xbuf;  // CTA pairs: [2][32][32] hand-over of swapped gate/up tiles
 };
 
 // Epilogue role (kEpiWarps warps, named barrier 1): for each tile id from the
@@ -258,6 +287,65 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
             break;
         }
         tc_fence_after();
+        if (PAIR && tile0.swp) {
+            // Swapped operands: TMEM lane r = weight row r of this CTA's half, column j =
+            // token row0 + j.  Gate/up: lanes 0-63 gate and 64-127 up of the features
+            // nt * 128 + 64 * half + (r % 64).  Down: lane r = output column
+            // nt * 256 + 128 * half + r.
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + a * kGemmBN;
+            const int R = tile0.m_valid, nch = swap_n(R) / 32;
+            if (sg.glu) {
+                // warps q and q + 2 hold the gate and up values of the same 32 features; per
+                // chunk of 32 tokens the gate warp activates tokens 0-15 and the up warp 16-31,
+                // each handing the other the half it needs
+                const bool gate_w = q < 2;
+                const int f = tile0.nt * 128 + 64 * half + 32 * (q & 1) + lane;
+                float *xg = c.xbuf + (q & 1) * 1024, *xu = xg + 512;  // [16][32] each
+#pragma unroll 1
+                for (int ch = 0; ch < nch; ++ch) {
+                    uint32_t v[32];
+                    tmem_ld32(tb + 32 * ch, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        if (gate_w)
+                            xg[j * 32 + lane] = __uint_as_float(v[16 + j]);
+                        else
+                            xu[j * 32 + lane] = __uint_as_float(v[j]);
+                    }
+                    epi_bar();
+                    const int t0 = 32 * ch + (gate_w ? 0 : 16);
+                    if (f < sg.n_out) {
+                        bf16 *o = static_cast<bf16 *>(sg.out) + (size_t)(tile0.row0 + t0) * sg.ldo + f;
+                        const int nj = min(16, R - t0);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (j < nj)
+                                o[(size_t)j * sg.ldo] = __float2bfloat16_rn(
+                                    gate_w ? glu_act(__uint_as_float(v[j]), xu[j * 32 + lane], p.act, p.alpha,
+                                                     p.limit, p.beta)
+                                           : glu_act(xg[j * 32 + lane], __uint_as_float(v[16 + j]), p.act, p.alpha,
+                                                     p.limit, p.beta));
+                    }
+                    epi_bar();
+                }
+            } else {
+                const int col = tile0.nt * kGemmBN + 128 * half + 32 * q + lane;
+#pragma unroll 1
+                for (int ch = 0; ch < nch; ++ch) {
+                    uint32_t v[32];
+                    tmem_ld32(tb + 32 * ch, v);
+                    tmem_ld_wait();
+                    if (col < sg.n_out) {
+                        float *o = static_cast<float *>(sg.out) + (size_t)(tile0.row0 + 32 * ch) * sg.ldo + col;
+                        const int nj = min(32, R - 32 * ch);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nj) o[(size_t)j * sg.ldo] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+        } else
 #pragma unroll 1
         for (int hh = 0; hh < HALVES; ++hh) {
         const Tile t = hh == 0 ? tile0 : decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, hh);
@@ -351,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 5 + 2 * kRing);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *ring = reinterpret_cast<volatile int *>(tmem_slot + 2);  // [kRing] tile ids
+    float *xbuf = reinterpret_cast<float *>(smem + kStages * kStageBytes + 512);  // C::kXBufBytes
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // CTA pair: rank 0 issues the MMAs; the full and accumulator-empty barriers
@@ -454,7 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const int claim_at = sg.k_blocks > 3 * kKB ? sg.k_blocks - 3 * kKB : 0;
                 if (sg.wait != nullptr) {  // A rows written earlier in this launch
                     const uint64_t t0 = stats ? global_timer_ns() : 0;
-                    if (!wait_counter(sg.wait + t.ready, sg.wait_count, p.wait_ns, abort_flag)) {
+                    // a swapped tile reads rows of both 128-row halves of its m-tile
+                    if (!wait_counter(sg.wait + t.ready - (t.swp ? half : 0), sg.wait_count, p.wait_ns, abort_flag) ||
+                        (t.swp && !wait_counter(sg.wait + t.ready - half + 1, sg.wait_count, p.wait_ns, abort_flag))) {
                         ok = false;
                         break;
                     }
@@ -475,7 +566,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         break;
                     }
                     if (stats) w_empty += global_timer_ns() - t0;
-                    if (PAIR) {
+                    if (PAIR && t.swp) {
+                        // swapped: this CTA's token rows (half of the MMA's N) in a 32- or 64-row
+                        // box, and 128 weight rows: the down tile's half, or 64 gate and 64 up
+                        // rows of the same features (one box per k-block and projection)
+                        const uint32_t fb = mapa_shared(full_bar(s), 0);
+                        const int box = swap_box(t.m_valid), nh = swap_n(t.m_valid) / 2;
+                        if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * (kBBytes + box * kGemmBK * 2 * kKB));
+                        const int kc = sg.k_base + t.ks * sg.k_blocks + kb;
+                        tma_load_3d_pair(sA + s * kAStage, &p.maps[sg.map_aw[box == 64]], fb, 0, t.row0 + half * nh, kc);
+                        if (sg.glu) {
+                            const int f0 = t.nt * 128 + 64 * half;
+#pragma unroll
+                            for (int j = 0; j < kKB; ++j) {
+                                const uint32_t dst = sB + s * kBBytes + j * (kBBytes / kKB);
+                                tma_load_3d_pair(dst, &p.maps[sg.map_bw0], fb, (kc + j) * kGemmBK, f0, g);
+                                tma_load_3d_pair(dst + kBBytes / kKB / 2, &p.maps[sg.map_bw1], fb, (kc + j) * kGemmBK, f0, g);
+                            }
+                        } else {
+                            tma_load_4d_pair(sB + s * kBBytes, mB, fb, 0, t.nt * kGemmBN + half * 128, kc, g);
+                        }
+                    } else if (PAIR) {
                         // both CTAs' copies complete on rank 0's full barrier; rank 0 expects their bytes.
                         // Maps view K as (64, K / 64) so that one box brings k-blocks kb, kb + 1
                         // (past the last k-block: zero fill, no MMA)
@@ -559,6 +670,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 if (stats) w_acc += global_timer_ns() - t0;
                 tc_fence_after();
                 const uint32_t d = tmem_base + a * kGemmBN;
+                // swapped: A = the weight rows (B's stage), B = the token rows, N = swap_n(rows)
+                const bool swp = PAIR && t.swp;
+                const uint32_t id = swp ? idesc_bf16_f32(2 * kGemmBM, swap_n(t.m_valid)) : idesc;
+                const uint32_t tok_kb = swp ? (uint32_t)swap_box(t.m_valid) * kGemmBK * 2 : (uint32_t)kABytes;
                 for (int kb = 0; kb < sg.k_blocks; kb += kKB) {
                     const int s = L % kStages;
                     const uint32_t ph = (L / kStages) & 1u;
@@ -572,14 +687,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #pragma unroll
                     for (int j = 0; j < kKB; ++j) {
                         if (kKB > 1 && kb + j >= sg.k_blocks) break;
-                        const uint64_t ad = smem_desc_k128(sA + s * kAStage + j * kABytes);
-                        const uint64_t bd = smem_desc_k128(sB + s * kBBytes + j * (kBBytes / kKB));
+                        const uint64_t td = smem_desc_k128(sA + s * kAStage + j * tok_kb);
+                        const uint64_t wd = smem_desc_k128(sB + s * kBBytes + j * (kBBytes / kKB));
+                        const uint64_t ad = swp ? wd : td, bd = swp ? td : wd;
 #pragma unroll
                         for (int kk = 0; kk < kGemmBK / 16; ++kk) {  // +32 bytes per K step of 16
                             if (PAIR)
-                                tc_mma_bf16_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | j | kk) != 0);
+                                tc_mma_bf16_pair(d, ad + 2 * kk, bd + 2 * kk, id, (kb | j | kk) != 0);
                             else
-                                tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | j | kk) != 0);
+                                tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, id, (kb | j | kk) != 0);
                         }
                     }
                     issued = true;
@@ -616,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     } else {
         // ----------------------------------------------------------- epilogue
         EpiCtx c{ring_full(0), ring_empty(0), tfull_bar(0), tempty_bar(0), ring, abort_flag, tmem_base, total,
-                 s_seg_end, s_offs, s_toffs, half};
+                 s_seg_end, s_offs, s_toffs, half, xbuf};
         epilogue_role<PAIR, kBM>(p, c, warp, lane);
     }
 
@@ -1199,7 +1315,7 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
     } else {
         // ----------------------------------------------------------- epilogue
         EpiCtx c{ring_full(0), ring_empty(0), tfull_bar(0), tempty_bar(0), ring, abort_flag, tmem_base, total,
-                 s_seg_end, s_offs, s_toffs, half};
+                 s_seg_end, s_offs, s_toffs, half, nullptr};
         epilogue_role<false, kBM, M256 ? 2 : 1>(p, c, warp, lane);
     }
 
@@ -1268,12 +1384,12 @@ CUresult encode_map_b(CUtensorMap *m, const void *ptr, int groups, int rows, int
 // The same tensors viewed with K split as (64, K / 64), box of two 64-column
 // chunks: one copy brings two consecutive k-blocks, each a 128-byte-swizzled
 // [rows][64] tile, one after the other in shared memory (CTA-pair GEMM).
-CUresult encode_map_a_kb2(CUtensorMap *m, const void *ptr, int rows, int K) {
+CUresult encode_map_a_kb2(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
     const cuuint64_t dims[3] = {(cuuint64_t)kGemmBK, (cuuint64_t)rows, (cuuint64_t)(K / kGemmBK)};
     const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)kGemmBK * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)kGemmBK, (cuuint32_t)kGemmBM, 2};
+    const cuuint32_t box[3] = {(cuuint32_t)kGemmBK, (cuuint32_t)box_rows, 2};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -251,7 +251,14 @@ struct GemmSegment {
     size_t split_stride;
     // MX weights: maps of the E8M0 scales of b0 and b1 ([groups, K / 32, rows] uint8)
     int map_s0, map_s1;
+    // CTA pairs, grouped segments: an m-tile of at most kSwapMaxRows rows runs with the
+    // operands swapped (the weight rows as M = 256, the tokens as N); its token rows come
+    // from map_aw[0] (boxes of 32 rows, two k-blocks) or map_aw[1] (64 rows), and a
+    // gate/up tile's weights from map_bw0 / map_bw1 (boxes of 64 rows, one k-block)
+    int map_aw[2];
+    int map_bw0, map_bw1;
 };
+constexpr int kSwapMaxRows = 128;
 
 struct GemmArgs {
     CUtensorMap maps[kGemmMaxMaps];
@@ -274,6 +281,7 @@ struct GemmArgs {
     int wfmt;              // WeightFormat of every segment's B maps; MX only without CTA pairs
     int thin;              // one CTA per tile, bf16, every m-tile <= 32 rows: A maps with boxes of 32
                            // rows, six stages (gemm_tc.cu, kThinRows)
+    int swap_rem;          // CTA pairs: grouped m-tiles of <= kSwapMaxRows rows with swapped operands
 };
 constexpr int kGemmStats = 8;
 cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s);
@@ -331,8 +339,8 @@ cudaError_t launch_gemm_mxt(const MxtArgs &a, int n_tokens, cudaStream_t s);
 // Tensor maps (TMA descriptors) for the GEMMs.  A: [rows, K] bf16, box 128 x 64.
 // B: [groups, rows, K] bf16, box box_rows x 64.  Both with 128-byte swizzle.
 CUresult encode_map_a(CUtensorMap *m, const void *ptr, int rows, int K);
-// K viewed as (64, K / 64), box 64 x 128 rows x 2 chunks (CTA-pair expert GEMM)
-CUresult encode_map_a_kb2(CUtensorMap *m, const void *ptr, int rows, int K);
+// K viewed as (64, K / 64), box 64 x box_rows x 2 chunks (CTA-pair expert GEMM)
+CUresult encode_map_a_kb2(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows = 128);
 CUresult encode_map_b_kb2(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int box_rows);
 CUresult encode_map_a_box(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows);
 CUresult encode_map_b(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int box_rows);

@@ -110,6 +110,7 @@ struct moe_handle {
     int ready_shared_base = 0; // first counter of the shared expert's m-tiles
     bool fuse_experts = true;  // gate/up and down in one persistent launch
     int pair_opt = 2;          // CTA-pair expert GEMM: 0 never, 1 always, 2 when T*k >= 256*E
+    bool pair_swap = true;     // CTA pairs: m-tiles of <= 128 rows with swapped operands
     bool pair_now = false;     // the current forward's choice
     int shared_parts = 1;      // K ranges of the shared (dense) down projection this forward
     bool prefetch_opt = true;  // L2 prefetch of expert weights during routing
@@ -134,6 +135,8 @@ struct moe_handle {
     // CTA-pair expert GEMM: the same tensors with K viewed as (64, K / 64), two
     // k-blocks per box (A: 128 rows; weights: 128 rows)
     CUtensorMap m_xs2, m_hb2, m_hs2, m_xbf2, m_gate2, m_up2, m_down2, m_shg2, m_shu2, m_shd2, m_x2;
+    // and the token rows of its swapped-operand tiles: two k-blocks, 32 ([0]) or 64 ([1]) rows
+    CUtensorMap m_xs2_n[2], m_hb2_n[2];
     // MX weights: m_gate ... m_shd map the element codes; these map their E8M0 scales
     int wfmt = 0;  // moe_weight_format
     CUtensorMap m_gate_s, m_up_s, m_down_s, m_shg_s, m_shu_s, m_shd_s;
@@ -337,6 +340,10 @@ moe_status build_maps(moe_handle *h) {
     MAP(moe::encode_map_a(&h->m_hbuf, h->hbuf, MT * k, I));
     MAP(moe::encode_map_a_kb2(&h->m_xs2, h->x_sorted, MT * k, H));
     MAP(moe::encode_map_a_kb2(&h->m_hb2, h->hbuf, MT * k, I));
+    for (int v = 0; v < 2; ++v) {
+        MAP(moe::encode_map_a_kb2(&h->m_xs2_n[v], h->x_sorted, MT * k, H, v ? 64 : 32));
+        MAP(moe::encode_map_a_kb2(&h->m_hb2_n[v], h->hbuf, MT * k, I, v ? 64 : 32));
+    }
     MAP(moe::encode_map_b(&h->m_wr, h->wr_parts, h->rplan.parts, h->E, H, h->rplan.Np));
     if (h->wfmt != MOE_WEIGHTS_BF16) {
         MAP(moe::encode_map_mx_codes(&h->m_gate, h->w.gate, Ep, I, H, h->wfmt));
@@ -599,6 +606,8 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     const int H = h->H, I = h->I, S = h->S, E = h->E;
     enum { kXs = 0, kX = 1, kHb = 2, kHs = 3, kG = 4, kU = 5, kSG = 6, kSU = 7, kD = 8, kSD = 9,
            kGs = 10, kUs = 11, kSGs = 12, kSUs = 13, kDs = 14, kSDs = 15 };
+    // bf16 CTA pairs (no scale maps): the swapped tiles' token and 64-row weight maps
+    enum { kXw32 = 10, kXw64 = 11, kHw32 = 12, kHw64 = 13, kGw = 14, kUw = 15 };
     const bool mx = h->wfmt != MOE_WEIGHTS_BF16;
     moe::GemmArgs g{};
     g.err = h->err;
@@ -627,6 +636,17 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
             g.maps[kUs] = h->m_up_s;
             g.maps[kDs] = h->m_down_s;
         }
+    }
+    // expert tiles of at most 128 rows on CTA pairs: weights as M, tokens as N
+    const bool swap = pair && !mx && !h->dense && h->pair_swap;
+    g.swap_rem = swap ? 1 : 0;
+    if (swap) {
+        g.maps[kXw32] = h->m_xs2_n[0];
+        g.maps[kXw64] = h->m_xs2_n[1];
+        g.maps[kHw32] = h->m_hb2_n[0];
+        g.maps[kHw64] = h->m_hb2_n[1];
+        g.maps[kGw] = h->m_gate64;
+        g.maps[kUw] = h->m_up64;
     }
     if (h->has_shared) {
         if (h->x_f32) {
@@ -681,11 +701,13 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     const bool fused = h->fuse_experts;
     int *sig = fused ? h->ready : nullptr;
     const moe::GemmSegment gu{0, E, 0, 0, h->offs, h->tile_offs, nt_gu, H / 64, 0, I, h->hbuf, I,
-                              1, kXs, kG, kU, sig, nullptr, 0, 0, 0, 0, kGs, kUs};
+                              1, kXs, kG, kU, sig, nullptr, 0, 0, 0, 0, kGs, kUs,
+                              {swap ? kXw32 : 0, swap ? kXw64 : 0}, swap ? kGw : 0, swap ? kUw : 0};
     const moe::GemmSegment sgu{1, 1, sh_base, T, nullptr, nullptr, nt_sgu, H / 64, 0, S, h->hs, S,
                                1, kX, kSG, kSU, sig, nullptr, 0, h->ready_shared_base, 0, 0, kSGs, kSUs};
     const moe::GemmSegment dn{0, E, 0, 0, h->offs, h->tile_offs, nt_d, I / 64, 0, H, h->yslot, H,
-                              0, kHb, kD, kD, nullptr, fused ? h->ready : nullptr, nt_gu, 0, 0, 0, kDs, kDs};
+                              0, kHb, kD, kD, nullptr, fused ? h->ready : nullptr, nt_gu, 0, 0, 0, kDs, kDs,
+                              {swap ? kHw32 : 0, swap ? kHw64 : 0}, 0, 0};
     // At small T the shared down projection (K = S) is the longest tile chain: its K
     // runs as `parts` ranges into as many partial outputs, which the combine adds in
     // fixed order (for two concatenated shared experts of width I and two parts,
@@ -1334,6 +1356,10 @@ moe_status moe_set_option(moe_handle *h, int option, long long value) {
     case MOE_OPT_GEMM_PAIR:
         if (value < 0 || value > 2) return fail(MOE_ERR_INVALID_ARG, "gemm pair %lld", value);
         h->pair_opt = (int)value;
+        return MOE_OK;
+    case MOE_OPT_PAIR_SWAP:
+        if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "pair swap %lld", value);
+        h->pair_swap = value != 0;
         return MOE_OK;
     case MOE_OPT_TRACE:
         if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "trace %lld", value);

@@ -223,12 +223,17 @@ typedef enum {
                                   and half of the weight tile; MX weights: one CTA per 256-row tile,
                                   two 128-row MMAs on each decoded weight tile); 0 never, 1 always,
                                   2 (default) when T*k >= 256*E (tensor-bound sizes) */
-    MOE_OPT_GRAPH = 8          /* moe_forward_host: 1 (default) captures the copy in, the forward and the
+    MOE_OPT_GRAPH = 8,         /* moe_forward_host: 1 (default) captures the copy in, the forward and the
                                   copy out into a CUDA graph on the second call with the same host
                                   buffers, T and options, and replays it on later such calls (host
                                   buffers must then be pinned: with pageable ones the capture fails
                                   and the call runs eagerly); 0 always runs eagerly.  Graphs are not
                                   used while stage events or the trace are on. */
+    MOE_OPT_PAIR_SWAP = 9      /* path 2 on CTA pairs with bf16 weights: 1 (default) runs an expert's
+                                  last 256-row tile with the operands swapped when it holds at most
+                                  128 rows (the pair's 256 weight rows as M, the tile's rows rounded
+                                  up to 32 as N), so the MMA skips most of the padding rows; 0 runs
+                                  every tile with the tokens as M.  Results are unchanged */
 } moe_option;
 
 /* Set an option.  Errors: INVALID_ARG (unknown option or value). */

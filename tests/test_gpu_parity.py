@@ -241,6 +241,30 @@ def test_pair_gemm_fused_equals_two_launches_and_oracle():
         P.check_output(P.to_np(Y1), oracle.forward_inputs(shape, ih), shape.dtype == "bf16", tag=f"{name}-pair-fused")
 
 
+def test_pair_swapped_remainder_tiles_match_unswapped_and_oracle():
+    """CTA pairs: m-tiles of at most 128 rows run with the weights as M and the tokens
+    as N.  A mix of experts (full 256-row tiles, remainders of <= 128 and of > 128
+    rows) against the same forward with every tile unswapped (bit-identical: each
+    output is the same K-ordered sum of the same products) and against the oracle on
+    every token."""
+    shape = wl.AFMOE_PREFILL.replace(name="afmoe_mixed", T=1500, hidden_size=512, moe_intermediate_size=192,
+                                     shared_intermediate_size=384)
+    inputs, blk = P.make_case(shape)
+    blk.set_option(capi.MOE_OPT_PATH, capi.PATH_GROUPED)
+    blk.set_option(capi.MOE_OPT_GEMM_PAIR, 1)
+    Y1 = blk.forward(inputs["X"]).clone()
+    torch.cuda.synchronize()
+    assert blk.sync_status() == capi.MOE_OK
+    blk.set_option(capi.MOE_OPT_PAIR_SWAP, 0)
+    Y0 = blk.forward(inputs["X"])
+    torch.cuda.synchronize()
+    assert blk.sync_status() == capi.MOE_OK
+    assert torch.equal(Y1, Y0), "swapped remainder tiles differ from unswapped ones"
+    ih = P.host_inputs(inputs)
+    P.check_output(P.to_np(Y1), oracle.forward_inputs(shape, ih), True, tag="afmoe_mixed-pair-swap")
+    blk.close()
+
+
 def test_token_permutation_equivariance_and_determinism():
     shape = SMALL["afmoe_ragged"]
     for path in PATHS.values():
