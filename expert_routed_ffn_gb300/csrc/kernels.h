@@ -188,6 +188,8 @@ struct CombineArgs {
     float eps;
     const float *post_w;
     const void *residual;
+    int *err;                    // ERR_TIMEOUT when a bounded wait gives up (or nullptr)
+    unsigned long long wait_ns;  // bound of each wait
 };
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 

@@ -984,7 +984,7 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
         moe::CombineArgs ca{h->yslot, h->has_shared ? (split ? h->ys_split : h->ys) : nullptr, h->shared_parts,
                             (size_t)T * h->H, h->topk_w, h->slot_of,
                             T, h->k, h->H, Y, h->x_f32 ? 1 : 0, trace_slot(h, n),
-                            h->norm, h->eps, h->w.post_norm_w, X};
+                            h->norm, h->eps, h->w.post_norm_w, X, h->err, h->wait_ns};
         st = launched(h, moe::launch_combine(ca, s), "combine", &n, s);
     }
     if (prefetch) {  // the caller's stream ends ordered after the side stream

@@ -627,6 +627,143 @@ __global__ void __launch_bounds__(kFlatThreads, 3) combine_flat_kernel(const Com
     trace_exit(a.trace);
 }
 
+// Without the post-norm, with bulk copies: the work is T * H / kBulkCols units
+// (token, chunk of kBulkCols columns); each CTA takes a contiguous range of units and
+// stages the ids and weights of their tokens in shared memory.  Warp w takes units w,
+// w + kBulkWarps, ... of the range: lane 0 copies a unit's terms (its k slot rows,
+// then the P shared parts, kBulkCols fp32 each) with cp.async.bulk into one of the
+// warp's two stages, completing on the stage's mbarrier, so that the next unit's
+// copies are in flight while the warp adds the current one.  The sum is the flat
+// kernel's: fmaf in the fixed term order from zero, weight 1 for the shared parts.
+//
+// Used when a unit has at most kBulkMaxTerms terms, where the flat kernel has few
+// loads in flight per thread.  Measured on GB300: MiniMax-M3 block (4 slots + 1
+// shared part, H = 6144) 53 against 61.5 us; with 7 terms (AFMoE prefill) 61 against
+// 56 us and with 9 (Nano decode) 10.2 against 8.2 us, so those stay on the flat
+// kernel; 512- or 1024-column units (4 or 2 warps) are slower still.
+constexpr int kBulkCols = 256;
+constexpr int kBulkWarps = 8;
+constexpr int kBulkVec = kBulkCols / 128;  // float4 per lane and term
+constexpr int kBulkTok = 64;
+constexpr int kBulkMaxTerms = 5;
+constexpr uint64_t kBulkDrainNs = 1000000000ull;
+
+__global__ void __launch_bounds__(kBulkWarps * 32) combine_bulk_kernel(const CombineArgs a) {
+    extern __shared__ __align__(128) uint8_t bulk_smem[];
+    __shared__ __align__(8) uint64_t bars[kBulkWarps][2];
+    __shared__ int s_slot[kBulkTok * 16];
+    __shared__ float s_w[kBulkTok * 16];
+    trace_mark(a.trace, 0);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int k = a.k, H = a.H, chunks = H / kBulkCols;
+    const int parts = a.ys != nullptr ? a.ys_parts : 0, terms = k + parts;
+    constexpr uint32_t kTermBytes = kBulkCols * 4;
+    const uint32_t stage_bytes = (uint32_t)terms * kTermBytes;
+    const uint32_t stage0 = smem_u32(bulk_smem) + (uint32_t)(2 * warp) * stage_bytes;
+    const float *stage_f = reinterpret_cast<const float *>(bulk_smem) + (size_t)(2 * warp) * terms * kBulkCols;
+    const uint32_t bar0 = smem_u32(&bars[warp][0]);
+    if (lane == 0) {
+        mbar_init(bar0, 1);
+        mbar_init(bar0 + 8, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    pdl_wait();
+    trace_mark(a.trace, 1);
+    pdl_trigger();
+    const long long units = (long long)a.T * chunks;
+    const long long per = (units + gridDim.x - 1) / gridDim.x;
+    const long long u_begin = blockIdx.x * per, u_end = min(units, u_begin + per);
+    uint32_t issued = 0, done = 0;  // this warp's units copied / added (stage = count & 1)
+    bool ok = true;
+    for (long long ub = u_begin; ub < u_end && ok;) {
+        // a pass: the units of at most kBulkTok tokens
+        const int ts = (int)(ub / chunks);
+        const int nt = (int)min((long long)kBulkTok, (u_end - 1) / chunks + 1 - ts);
+        const long long ue = min(u_end, (long long)(ts + nt) * chunks);
+        for (int i = threadIdx.x; i < nt * k; i += kBulkWarps * 32) {
+            s_slot[i] = __ldg(a.slot_of + (size_t)ts * k + i);
+            s_w[i] = __ldg(a.topk_w + (size_t)ts * k + i);
+        }
+        __syncthreads();
+        auto issue = [&](long long u) {
+            const uint32_t st = issued & 1u;
+            if (lane == 0) {
+                const int t = (int)(u / chunks), tl = t - ts, c0 = (int)(u - (long long)t * chunks) * kBulkCols;
+                const uint32_t bar = bar0 + 8u * st, dst = stage0 + st * stage_bytes;
+                int valid = parts;
+                for (int j = 0; j < k; ++j) valid += s_slot[tl * k + j] >= 0;
+                // the stage was last read by this warp's lanes (generic proxy) before __syncwarp
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive_expect_tx(bar, (uint32_t)valid * kTermBytes);
+                for (int j = 0; j < k; ++j) {
+                    const int slot = s_slot[tl * k + j];
+                    if (slot >= 0) bulk_g2s(dst + j * kTermBytes, a.yslot + (size_t)slot * H + c0, kTermBytes, bar);
+                }
+                for (int q = 0; q < parts; ++q)
+                    bulk_g2s(dst + (k + q) * kTermBytes, a.ys + q * a.ys_part_stride + (size_t)t * H + c0, kTermBytes,
+                             bar);
+            }
+            ++issued;
+        };
+        long long un = ub + warp;
+        if (un < ue) issue(un);
+        for (long long u = un; u < ue; u += kBulkWarps) {
+            if (u + kBulkWarps < ue) issue(u + kBulkWarps);  // the other stage: read two units ago
+            const uint32_t st = done & 1u, ph = (done >> 1) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * st, ph, a.wait_ns, nullptr))) {
+                if (lane == 0 && a.err != nullptr) atomicOr(a.err, ERR_TIMEOUT);
+                ok = false;
+                break;
+            }
+            const int t = (int)(u / chunks), tl = t - ts, c0 = (int)(u - (long long)t * chunks) * kBulkCols;
+            const float *sf = stage_f + (size_t)st * terms * kBulkCols;
+            float4 acc[kBulkVec];
+#pragma unroll
+            for (int h = 0; h < kBulkVec; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < terms; ++j) {
+                float w = 1.f;
+                if (j < k) {
+                    if (s_slot[tl * k + j] < 0) continue;
+                    w = s_w[tl * k + j];
+                }
+#pragma unroll
+                for (int h = 0; h < kBulkVec; ++h) {
+                    const float4 x = *reinterpret_cast<const float4 *>(sf + j * kBulkCols + 128 * h + 4 * lane);
+                    acc[h].x = fmaf(w, x.x, acc[h].x);
+                    acc[h].y = fmaf(w, x.y, acc[h].y);
+                    acc[h].z = fmaf(w, x.z, acc[h].z);
+                    acc[h].w = fmaf(w, x.w, acc[h].w);
+                }
+            }
+            __syncwarp();  // every lane has read the stage before lane 0 refills it
+            ++done;
+#pragma unroll
+            for (int h = 0; h < kBulkVec; ++h) {
+                const size_t off = (size_t)t * H + c0 + 128 * h + 4 * lane;
+                if (a.y_f32) {
+                    *reinterpret_cast<float4 *>(static_cast<float *>(a.Y) + off) = acc[h];
+                } else {
+                    uint2 o;
+                    o.x = pack_bf16x2(acc[h].x, acc[h].y);
+                    o.y = pack_bf16x2(acc[h].z, acc[h].w);
+                    *reinterpret_cast<uint2 *>(static_cast<bf16 *>(a.Y) + off) = o;
+                }
+            }
+        }
+        ub = ue;
+        // every warp is done with this pass's ids (and agrees whether to go on)
+        ok = __syncthreads_and(ok) != 0;
+    }
+    if (!ok) {
+        // copies still in flight land before the CTA's shared memory is released
+        for (; done < issued; ++done)
+            mbar_wait(bar0 + 8u * (done & 1u), (done >> 1) & 1u, kBulkDrainNs, nullptr);
+    }
+    __syncthreads();
+    trace_exit(a.trace);
+}
+
 // ------------------------------------------------------------- pre-MLP norm
 
 __global__ void __launch_bounds__(kRowMaxThreads) rmsnorm_kernel(const NormArgs a) {
@@ -721,6 +858,29 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
         if (a.residual == nullptr || a.post_w == nullptr) return cudaErrorInvalidValue;
         const int grid = a.T < sms * kCombineCtasPerSm ? a.T : sms * kCombineCtasPerSm;
         return launch_pdl(combine_kernel<true>, dim3(grid), dim3(row_threads(a.H)), 0, s, a);
+    }
+    // bulk copies when a unit's terms fit two stages per warp
+    const int terms = a.k + (a.ys != nullptr ? a.ys_parts : 0);
+    if (a.H % kBulkCols == 0 && terms >= 1 && terms <= kBulkMaxTerms &&
+        kBulkWarps * 2 * terms * kBulkCols * 4 <= 200 * 1024) {
+        const int smem = kBulkWarps * 2 * terms * kBulkCols * 4;
+        static int bulk_per_sm[kBulkMaxTerms + 1] = {};
+        static std::once_flag bulk_once;
+        std::call_once(bulk_once, [] {
+            cudaFuncSetAttribute(combine_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+            for (int tm = 1; tm <= kBulkMaxTerms; ++tm) {
+                const int sb = kBulkWarps * 2 * tm * kBulkCols * 4;
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bulk_per_sm[tm], combine_bulk_kernel,
+                                                                  kBulkWarps * 32, sb) != cudaSuccess ||
+                    bulk_per_sm[tm] < 1)
+                    bulk_per_sm[tm] = 1;
+            }
+        });
+        const long long units = (long long)a.T * (a.H / kBulkCols);
+        const long long need = (units + kBulkWarps - 1) / kBulkWarps;
+        const long long cap = (long long)sms * bulk_per_sm[terms];
+        const int grid = (int)(need < cap ? need : cap);
+        return launch_pdl(combine_bulk_kernel, dim3(grid), dim3(kBulkWarps * 32), (size_t)smem, s, a);
     }
     // the flat kernel: as many CTAs as are resident at once on every SM, capped by the chunks
     static int flat_per_sm = 0;
