@@ -77,6 +77,23 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// Wait (bounded by limit_ns of global time) until *p >= target, with acquire
+// semantics at GPU scope: what was written before the matching release is visible.
+__device__ __forceinline__ int ld_acquire_s32(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ bool wait_at_least(const int *p, int target, uint64_t limit_ns) {
+    if (ld_acquire_s32(p) >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        __nanosleep(256);
+        if (ld_acquire_s32(p) >= target) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

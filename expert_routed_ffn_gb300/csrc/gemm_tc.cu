@@ -344,6 +344,12 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
                             if (j < nj) o[(size_t)j * sg.ldo] = __uint_as_float(v[j]);
                     }
                 }
+                if (sg.tok_done != nullptr) {  // this CTA's half of every row is stored
+                    __threadfence();
+                    epi_bar();
+                    for (int j = q * 32 + lane; j < R; j += kEpiThreads)
+                        atomicAdd(sg.tok_done + sg.row_tok[tile0.row0 + j], 1);
+                }
             }
         } else
 #pragma unroll 1
@@ -390,6 +396,11 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
                     for (int v = 0; v < 8; ++v)
                         dst[v] = make_uint4(v32[4 * v], v32[4 * v + 1], v32[4 * v + 2], v32[4 * v + 3]);
                 }
+            }
+            if (sg.tok_done != nullptr && row_ok) {  // this row's columns of the tile are stored
+                const int row = t.row0 + r;
+                __threadfence();
+                atomicAdd(sg.tok_done + (sg.row_tok != nullptr ? sg.row_tok[row] : row), 2);
             }
         }
         }  // halves

@@ -164,6 +164,7 @@ struct ScatterArgs {
     int32_t *slot_of;         // [T*k]
     __nv_bfloat16 *x_sorted;  // [T*k, H]
     int *err;
+    int *tok_done;            // [T] per-token output counters, zeroed here (CTAs y = 0), or nullptr
 };
 cudaError_t launch_scatter(const ScatterArgs &a, cudaStream_t s);
 
@@ -190,6 +191,11 @@ struct CombineArgs {
     const void *residual;
     int *err;                    // ERR_TIMEOUT when a bounded wait gives up (or nullptr)
     unsigned long long wait_ns;  // bound of each wait
+    // Overlap with the expert GEMM (no post-norm): instead of waiting for the GEMM to
+    // finish, a token is combined once tok_done[t] reaches tok_unit * (its valid slots +
+    // ys_parts) (the down tiles' epilogues count its stored rows); nullptr: wait first
+    const int *tok_done;
+    int tok_unit;
 };
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 
@@ -259,6 +265,12 @@ struct GemmSegment {
     // gate/up tile's weights from map_bw0 / map_bw1 (boxes of 64 rows, one k-block)
     int map_aw[2];
     int map_bw0, map_bw1;
+    // down projections feeding a combine that overlaps the launch: after a tile's rows are
+    // stored, tok_done[token] += 2 for each of its rows (swapped pair tiles: += 1 from each
+    // CTA, which stores half of every row's columns); token = row_tok[row], or the row
+    // itself when row_tok is nullptr (dense segments)
+    int *tok_done;
+    const int32_t *row_tok;
 };
 constexpr int kSwapMaxRows = 128;
 

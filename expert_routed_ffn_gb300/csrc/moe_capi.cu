@@ -107,6 +107,9 @@ struct moe_handle {
     bf16 *wr_parts = nullptr;  // router weights as exact bf16 splits [3, E, H]
     int *ready = nullptr;      // per-m-tile gate/up completion counters of the fused expert GEMM
     int *tile_counters = nullptr;  // [2] tile tickets of the expert GEMM launches
+    int *tok_done = nullptr;   // [max_tokens] rows stored per token, for the overlapped combine
+    bool combine_overlap = true;  // the combine waits per token instead of for the whole GEMM
+    bool ovl_now = false;      // this forward: combine overlapped with the grouped GEMM
     int ready_shared_base = 0; // first counter of the shared expert's m-tiles
     bool fuse_experts = true;  // gate/up and down in one persistent launch
     int pair_opt = 2;          // CTA-pair expert GEMM: 0 never, 1 always, 2 when T*k >= 256*E
@@ -324,6 +327,7 @@ void carve(moe_handle *h, void *base) {
     h->ready = c.take<int>(base, (size_t)h->ready_shared_base + shared_counters);
     h->wr_flags = c.take<int>(base, 64);
     h->tile_counters = c.take<int>(base, 64);
+    h->tok_done = c.take<int>(base, (size_t)MT);
     h->ws_bytes = round_up(c.off, 256);
 }
 
@@ -593,6 +597,7 @@ moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n
     xa.slot_of = h->slot_of;
     xa.x_sorted = h->x_sorted;
     xa.err = h->err;
+    xa.tok_done = h->tok_done;
     xa.trace = trace_slot(h, *n);
     st = launched(h, moe::launch_scatter(xa, s), "dispatch_scatter", n, s);
     if (st != MOE_OK) return st;
@@ -705,9 +710,10 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
                               {swap ? kXw32 : 0, swap ? kXw64 : 0}, swap ? kGw : 0, swap ? kUw : 0};
     const moe::GemmSegment sgu{1, 1, sh_base, T, nullptr, nullptr, nt_sgu, H / 64, 0, S, h->hs, S,
                                1, kX, kSG, kSU, sig, nullptr, 0, h->ready_shared_base, 0, 0, kSGs, kSUs};
+    int *const tok_done = h->ovl_now ? h->tok_done : nullptr;  // the combine waits per token
     const moe::GemmSegment dn{0, E, 0, 0, h->offs, h->tile_offs, nt_d, I / 64, 0, H, h->yslot, H,
                               0, kHb, kD, kD, nullptr, fused ? h->ready : nullptr, nt_gu, 0, 0, 0, kDs, kDs,
-                              {swap ? kHw32 : 0, swap ? kHw64 : 0}, 0, 0};
+                              {swap ? kHw32 : 0, swap ? kHw64 : 0}, 0, 0, tok_done, h->sorted_tok};
     // At small T the shared down projection (K = S) is the longest tile chain: its K
     // runs as `parts` ranges into as many partial outputs, which the combine adds in
     // fixed order (for two concatenated shared experts of width I and two parts,
@@ -716,7 +722,7 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     moe::GemmSegment sdn{1, 1, sh_base, T, nullptr, nullptr, nt_d, S / 64 / parts, 0, H,
                          parts > 1 ? h->ys_split : h->ys, H, 0, kHs, kSD, kSD, nullptr,
                          fused ? h->ready : nullptr, nt_sgu, h->ready_shared_base, parts, (size_t)T * H,
-                         kSDs, kSDs};
+                         kSDs, kSDs, {0, 0}, 0, 0, tok_done, nullptr};
     if (fused) {
         int ns = 0;
         if (!h->dense) g.seg[ns++] = gu;
@@ -948,6 +954,9 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     h->thin_now = path == kPathGrouped && !h->pair_now && h->wfmt == MOE_WEIGHTS_BF16 &&
                   (T <= kThinRows || (h->E > 0 && slots <= (long long)kThinRows * h->E));
     h->shared_parts = path == kPathGrouped && h->has_shared ? shared_parts(h, T) : 1;
+    // the combine (no post-norm) overlaps the grouped expert GEMM: it waits per token for
+    // the down tiles' counts instead of for the whole launch
+    h->ovl_now = path == kPathGrouped && !h->dense && h->norm == 0 && h->combine_overlap;
     mark(h, 0, s);
     moe_status st = MOE_OK;
     const void *Xm = X;  // the MLP's input: X, or pre_mlp_norm(X)
@@ -984,7 +993,8 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
         moe::CombineArgs ca{h->yslot, h->has_shared ? (split ? h->ys_split : h->ys) : nullptr, h->shared_parts,
                             (size_t)T * h->H, h->topk_w, h->slot_of,
                             T, h->k, h->H, Y, h->x_f32 ? 1 : 0, trace_slot(h, n),
-                            h->norm, h->eps, h->w.post_norm_w, X, h->err, h->wait_ns};
+                            h->norm, h->eps, h->w.post_norm_w, X, h->err, h->wait_ns,
+                            h->ovl_now ? h->tok_done : nullptr, 2 * ((h->H + moe::kGemmBN - 1) / moe::kGemmBN)};
         st = launched(h, moe::launch_combine(ca, s), "combine", &n, s);
     }
     if (prefetch) {  // the caller's stream ends ordered after the side stream
@@ -1356,6 +1366,10 @@ moe_status moe_set_option(moe_handle *h, int option, long long value) {
     case MOE_OPT_GEMM_PAIR:
         if (value < 0 || value > 2) return fail(MOE_ERR_INVALID_ARG, "gemm pair %lld", value);
         h->pair_opt = (int)value;
+        return MOE_OK;
+    case MOE_OPT_COMBINE_OVERLAP:
+        if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "combine overlap %lld", value);
+        h->combine_overlap = value != 0;
         return MOE_OK;
     case MOE_OPT_PAIR_SWAP:
         if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "pair swap %lld", value);

@@ -243,6 +243,8 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
     trace_mark(a.trace, 0);
     pdl_wait();
     trace_mark(a.trace, 1);
+    if (a.tok_done != nullptr && blockIdx.y == 0)  // this block's per-token counters of the combine
+        for (int i = threadIdx.x; i < TT && tok0 + i < a.T; i += kScatterThreads) a.tok_done[tok0 + i] = 0;
     // the expert GEMM is launched only when every CTA has reached the end of its
     // gather (launch_dependents below): launched earlier, its one-per-SM CTAs
     // would take the shared memory that this grid's later waves need
@@ -549,12 +551,30 @@ constexpr int kFlatThreads = 256;
 constexpr int kFlatBatch = 8;
 constexpr int kFlatTok = 64;
 
+// Overlapped with the expert GEMM (a.tok_done): each 64-token chunk first waits until
+// its tokens' rows are stored (loads then bypass L1), and the wait on the GEMM grid
+// comes at the end.
+__device__ __forceinline__ bool wait_tokens(const CombineArgs &a, int ts, int nt, const int *s_slot, int parts) {
+    bool good = true;
+    if (threadIdx.x < 32)
+        for (int i = threadIdx.x; i < nt; i += 32) {
+            int valid = parts;
+            for (int j = 0; j < a.k; ++j) valid += s_slot[i * a.k + j] >= 0;
+            good = good && wait_at_least(a.tok_done + ts + i, a.tok_unit * valid, a.wait_ns);
+        }
+    if (!good && a.err != nullptr) atomicOr(a.err, ERR_TIMEOUT);
+    return good;
+}
+
 __global__ void __launch_bounds__(kFlatThreads, 3) combine_flat_kernel(const CombineArgs a) {
     __shared__ int s_slot[kFlatTok * 16];
     __shared__ float s_w[kFlatTok * 16];
+    const bool ovl = a.tok_done != nullptr;
     trace_mark(a.trace, 0);
-    pdl_wait();
-    trace_mark(a.trace, 1);
+    if (!ovl) {
+        pdl_wait();
+        trace_mark(a.trace, 1);
+    }
     pdl_trigger();
     const int k = a.k, H = a.H, groups = H / 4;
     const int parts = a.ys != nullptr ? a.ys_parts : 0, terms = k + parts;
@@ -563,6 +583,7 @@ __global__ void __launch_bounds__(kFlatThreads, 3) combine_flat_kernel(const Com
     per = (per + kFlatThreads - 1) / kFlatThreads * kFlatThreads;
     const long long u_begin = blockIdx.x * per, u_end = min(units, u_begin + per);
     if (u_begin >= u_end) {
+        if (ovl) pdl_wait();
         trace_exit(a.trace);
         return;
     }
@@ -575,6 +596,10 @@ __global__ void __launch_bounds__(kFlatThreads, 3) combine_flat_kernel(const Com
             s_w[i] = __ldg(a.topk_w + (size_t)ts * k + i);
         }
         __syncthreads();
+        if (ovl) {
+            wait_tokens(a, ts, nt, s_slot, parts);
+            __syncthreads();
+        }
         const long long lo = max(u_begin, (long long)ts * groups);
         const long long hi = min(u_end, (long long)(ts + nt) * groups);
         for (long long u = lo + threadIdx.x; u < hi; u += kFlatThreads) {
@@ -601,7 +626,9 @@ __global__ void __launch_bounds__(kFlatThreads, 3) combine_flat_kernel(const Com
                         src = a.ys + (size_t)(j - k) * a.ys_part_stride + (size_t)t * H + c;
                     }
                     on[v] = src != nullptr;
-                    if (on[v]) r[v] = __ldg(reinterpret_cast<const float4 *>(src));
+                    if (on[v])
+                        r[v] = ovl ? __ldcg(reinterpret_cast<const float4 *>(src))
+                                   : __ldg(reinterpret_cast<const float4 *>(src));
                 }
 #pragma unroll
                 for (int v = 0; v < kFlatBatch; ++v) {
@@ -623,6 +650,10 @@ __global__ void __launch_bounds__(kFlatThreads, 3) combine_flat_kernel(const Com
                 *reinterpret_cast<uint2 *>(static_cast<bf16 *>(a.Y) + off) = o;
             }
         }
+    }
+    if (ovl) {  // the grid ends after the expert GEMM's
+        pdl_wait();
+        trace_mark(a.trace, 1);
     }
     trace_exit(a.trace);
 }
@@ -668,8 +699,11 @@ __global__ void __launch_bounds__(kBulkWarps * 32) combine_bulk_kernel(const Com
         fence_mbar_init();
     }
     __syncwarp();
-    pdl_wait();
-    trace_mark(a.trace, 1);
+    const bool ovl = a.tok_done != nullptr;
+    if (!ovl) {
+        pdl_wait();
+        trace_mark(a.trace, 1);
+    }
     pdl_trigger();
     const long long units = (long long)a.T * chunks;
     const long long per = (units + gridDim.x - 1) / gridDim.x;
@@ -686,6 +720,10 @@ __global__ void __launch_bounds__(kBulkWarps * 32) combine_bulk_kernel(const Com
             s_w[i] = __ldg(a.topk_w + (size_t)ts * k + i);
         }
         __syncthreads();
+        if (ovl) {
+            wait_tokens(a, ts, nt, s_slot, parts);
+            __syncthreads();
+        }
         auto issue = [&](long long u) {
             const uint32_t st = issued & 1u;
             if (lane == 0) {
@@ -693,8 +731,9 @@ __global__ void __launch_bounds__(kBulkWarps * 32) combine_bulk_kernel(const Com
                 const uint32_t bar = bar0 + 8u * st, dst = stage0 + st * stage_bytes;
                 int valid = parts;
                 for (int j = 0; j < k; ++j) valid += s_slot[tl * k + j] >= 0;
-                // the stage was last read by this warp's lanes (generic proxy) before __syncwarp
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                // the stage was last read by this warp's lanes (generic proxy) before __syncwarp;
+                // with the overlap, the rows were stored by the GEMM's generic stores
+                asm volatile("fence.proxy.async;" ::: "memory");
                 mbar_arrive_expect_tx(bar, (uint32_t)valid * kTermBytes);
                 for (int j = 0; j < k; ++j) {
                     const int slot = s_slot[tl * k + j];
@@ -761,6 +800,10 @@ __global__ void __launch_bounds__(kBulkWarps * 32) combine_bulk_kernel(const Com
             mbar_wait(bar0 + 8u * (done & 1u), (done >> 1) & 1u, kBulkDrainNs, nullptr);
     }
     __syncthreads();
+    if (ovl) {  // the grid ends after the expert GEMM's
+        pdl_wait();
+        trace_mark(a.trace, 1);
+    }
     trace_exit(a.trace);
 }
 

@@ -229,11 +229,16 @@ typedef enum {
                                   buffers must then be pinned: with pageable ones the capture fails
                                   and the call runs eagerly); 0 always runs eagerly.  Graphs are not
                                   used while stage events or the trace are on. */
-    MOE_OPT_PAIR_SWAP = 9      /* path 2 on CTA pairs with bf16 weights: 1 (default) runs an expert's
+    MOE_OPT_PAIR_SWAP = 9,     /* path 2 on CTA pairs with bf16 weights: 1 (default) runs an expert's
                                   last 256-row tile with the operands swapped when it holds at most
                                   128 rows (the pair's 256 weight rows as M, the tile's rows rounded
                                   up to 32 as N), so the MMA skips most of the padding rows; 0 runs
                                   every tile with the tokens as M.  Results are unchanged */
+    MOE_OPT_COMBINE_OVERLAP = 10 /* path 2 without the post-MLP norm: 1 (default) launches the combine
+                                  while the expert GEMM runs; the down tiles count each token's
+                                  stored rows and the combine adds a token as soon as all of its
+                                  rows are in (the same fixed-order sum); 0 waits for the whole GEMM
+                                  first.  Results are unchanged */
 } moe_option;
 
 /* Set an option.  Errors: INVALID_ARG (unknown option or value). */

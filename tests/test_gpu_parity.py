@@ -265,6 +265,26 @@ def test_pair_swapped_remainder_tiles_match_unswapped_and_oracle():
     blk.close()
 
 
+@pytest.mark.parametrize("name", ["nano_decode", "afmoe_ragged", "m3_small_packed", "nano_T1"])
+def test_combine_overlapped_with_gemm_is_bit_identical(name):
+    """The combine that starts while the expert GEMM runs (each token once its rows
+    are counted in) adds the same terms in the same order as the combine that waits
+    for the whole GEMM: bit-identical, with one and with two GEMM launches."""
+    shape = SMALL[name]
+    inputs, blk = P.make_case(shape)
+    blk.set_option(capi.MOE_OPT_PATH, capi.PATH_GROUPED)
+    ys = []
+    for fuse in (1, 0):
+        blk.set_option(capi.MOE_OPT_FUSE_EXPERTS, fuse)
+        for ovl in (1, 0):
+            blk.set_option(capi.MOE_OPT_COMBINE_OVERLAP, ovl)
+            ys.append(blk.forward(inputs["X"]).clone())
+            torch.cuda.synchronize()
+            assert blk.sync_status() == capi.MOE_OK
+    assert all(torch.equal(ys[0], y) for y in ys[1:])
+    blk.close()
+
+
 def test_token_permutation_equivariance_and_determinism():
     shape = SMALL["afmoe_ragged"]
     for path in PATHS.values():
