@@ -796,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 // AFMoE MXFP8 prefill expert GEMM 555 against 758 us with 128-row tiles; a CTA-pair
 // version (each CTA decoding half of the weight tile, rank 1 relaying its k-blocks to
 // rank 0's cta_group::2 MMAs) took 1028 us.  Bit-identical to the bf16 CTA-pair path.
-template <int WF, bool M256 = false>
+template <int WF, bool M256 = false, int CW = 8>
 struct MxCfg {
     // B rows converted per k-block (the tile's 256 columns)
     static constexpr int kBRows = kGemmBN;
@@ -818,10 +818,9 @@ struct MxCfg {
     static constexpr int kBarBytes = 1024;
     static constexpr int kSmemBytes =
         kBStages * kBBytes + kAStages * kAStageBytes + kRawStages * kRawStage + 1024 /*align*/ + kBarBytes;
-#ifndef MOE_MX_CONV_WARPS
-#define MOE_MX_CONV_WARPS 8
-#endif
-    static constexpr int kConvWarps = MOE_MX_CONV_WARPS;
+    // converter warps: 8, or 16 where the weight stream of 128-row tiles outruns eight
+    // (GemmArgs::mx_conv16)
+    static constexpr int kConvWarps = CW;
     static constexpr int kThreads = 32 * (7 + kConvWarps);  // warps 0-6 as listed, then the converters
     static_assert(kRawStage % 128 == 0, "raw stages stay 128-byte aligned");
 };
@@ -899,9 +898,9 @@ __device__ __forceinline__ void e4m3x4_as_bf16x2(uint32_t w, uint32_t &lo, uint3
 // warp's rows are read first: when all of them allow the bf16 multiplier (the usual
 // case) the loop has no per-row branch and its code loads are issued together
 // (measured: 0.35 against 0.58 us per k-block for eight warps with the branch).
-template <int WF, int kRows>
+template <int WF, int kRows, int CW>
 __device__ __forceinline__ void mx_convert(const uint8_t *raw, const uint8_t *sc, uint8_t *out, int cw, int lane) {
-    using M = MxCfg<WF>;
+    using M = MxCfg<WF, false, CW>;
     constexpr int kRowsPerWarp = kRows / M::kConvWarps;
     static_assert(kRowsPerWarp % 16 == 0, "converter rows");
     constexpr int kRowsPerIt = WF == kWeightsMxfp8 ? 8 : 16;  // rows a warp covers per iteration
@@ -1002,9 +1001,9 @@ __device__ __forceinline__ void mx_convert(const uint8_t *raw, const uint8_t *sc
     }
 }
 
-template <int WF, bool M256>
-__global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const __grid_constant__ GemmArgs p) {
-    using M = MxCfg<WF, M256>;
+template <int WF, bool M256, int CW = 8>
+__global__ void __launch_bounds__(MxCfg<WF, M256, CW>::kThreads, 1) gemm_mx_kernel(const __grid_constant__ GemmArgs p) {
+    using M = MxCfg<WF, M256, CW>;
     constexpr int R = M::kRawStages, RA = M::kAStages, P = M::kBStages, NCW = M::kConvWarps;
     constexpr int kBM = M256 ? 2 * kGemmBM : kGemmBM;  // rows per tile
     extern __shared__ uint8_t smem_raw[];
@@ -1244,7 +1243,7 @@ __global__ void __launch_bounds__(MxCfg<WF>::kThreads, 1) gemm_mx_kernel(const _
                     ok = false;
                     break;
                 }
-                mx_convert<WF, M::kBRows>(rawS(rs), rawS(rs) + M::kRawCodes, opB(os), cw, lane);
+                mx_convert<WF, M::kBRows, CW>(rawS(rs), rawS(rs) + M::kRawCodes, opB(os), cw, lane);
                 fence_proxy_async_smem();  // the generic-proxy stores, before the MMA (async proxy) reads them
                 __syncwarp();
                 if (lane == 0) {
@@ -1462,6 +1461,10 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
                              MxCfg<kWeightsMxfp8, true>::kSmemBytes);
         cudaFuncSetAttribute(gemm_mx_kernel<kWeightsMxfp4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              MxCfg<kWeightsMxfp4, true>::kSmemBytes);
+        cudaFuncSetAttribute(gemm_mx_kernel<kWeightsMxfp8, false, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             MxCfg<kWeightsMxfp8, false, 16>::kSmemBytes);
+        cudaFuncSetAttribute(gemm_mx_kernel<kWeightsMxfp4, false, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             MxCfg<kWeightsMxfp4, false, 16>::kSmemBytes);
     });
     if (a.wfmt == kWeightsMxfp8 || a.wfmt == kWeightsMxfp4) {
         const bool f8 = a.wfmt == kWeightsMxfp8;
@@ -1472,6 +1475,15 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
                                   s, a);
             return launch_pdl(gemm_mx_kernel<kWeightsMxfp4, true>, dim3(a.num_ctas), dim3(MxCfg<kWeightsMxfp4>::kThreads),
                               (size_t)MxCfg<kWeightsMxfp4, true>::kSmemBytes, s, a);
+        }
+        if (a.mx_conv16) {
+            if (f8)
+                return launch_pdl(gemm_mx_kernel<kWeightsMxfp8, false, 16>, dim3(a.num_ctas),
+                                  dim3(MxCfg<kWeightsMxfp8, false, 16>::kThreads),
+                                  (size_t)MxCfg<kWeightsMxfp8, false, 16>::kSmemBytes, s, a);
+            return launch_pdl(gemm_mx_kernel<kWeightsMxfp4, false, 16>, dim3(a.num_ctas),
+                              dim3(MxCfg<kWeightsMxfp4, false, 16>::kThreads),
+                              (size_t)MxCfg<kWeightsMxfp4, false, 16>::kSmemBytes, s, a);
         }
         if (f8)
             return launch_pdl(gemm_mx_kernel<kWeightsMxfp8, false>, dim3(a.num_ctas),

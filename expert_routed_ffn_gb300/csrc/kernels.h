@@ -296,6 +296,7 @@ struct GemmArgs {
     int thin;              // one CTA per tile, bf16, every m-tile <= 32 rows: A maps with boxes of 32
                            // rows, six stages (gemm_tc.cu, kThinRows)
     int swap_rem;          // CTA pairs: grouped m-tiles of <= kSwapMaxRows rows with swapped operands
+    int mx_conv16;         // MX weights, 128-row tiles: 16 converter warps instead of 8
 };
 constexpr int kGemmStats = 8;
 cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s);

@@ -680,6 +680,11 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         }
     }
     g.wfmt = h->wfmt;
+    // MX weights on 128-row tiles with at least 32 routed rows per expert on average: the
+    // weight stream outruns eight converter warps (measured on GB300: MiniMax-M3 MXFP8
+    // 2797 -> 2636 us with sixteen; at Nano decode sizes, 16 rows per expert, sixteen
+    // are slower: 76.2 -> 77.2 us)
+    g.mx_conv16 = mx && !pair && E > 0 && (long long)T * h->k >= 32ll * E ? 1 : 0;
     // decode sizes: 32-row m-tiles (the dispatch counted them), A rows in 32-row
     // boxes, so the ring holds more weights
     const bool thin = h->thin_now;

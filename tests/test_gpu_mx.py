@@ -97,6 +97,9 @@ SMALL = {
                                                 shared_intermediate_size=512),
     "dense_small": wl.dense_layer(200, "afmoe").replace(name="dense_small", hidden_size=512,
                                                          shared_intermediate_size=1024),
+    # >= 32 routed rows per expert on 128-row tiles: the kernel with sixteen converter warps
+    "afmoe_rows48": wl.AFMOE_PREFILL.replace(name="afmoe_rows48", T=512, hidden_size=512,
+                                             moe_intermediate_size=192, shared_intermediate_size=384),
 }
 FORMATS = ["mxfp8", "mxfp4"]
 
@@ -131,7 +134,7 @@ def test_mx_small_every_token(name, fmt, gemm):
 @pytest.mark.parametrize("gemm", list(GEMMS))
 @pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("name", ["nano", "m3_small_packed", "afmoe_ragged", "dense_small", "nano_T1",
-                                  "afmoe_T4"])
+                                  "afmoe_T4", "afmoe_rows48"])
 def test_mx_bit_identical_to_bf16_path_on_decoded_weights(name, fmt, gemm):
     shape = SMALL[name].replace(name=f"{SMALL[name].name}_{fmt}", weight_format=fmt)
     path, pair = GEMMS[gemm]
