@@ -61,6 +61,13 @@ constexpr int kPathAuto = 0, kPathDecode = 1, kPathGrouped = 2, kPathSwapped = 3
 // 104 MB 63.5 / 63.6.  The prefetch never exceeds the experts' gate/up weights.
 // rows of an m-tile at decode sizes (gemm_tc.cu kThinRows)
 constexpr int kThinRows = 32;
+// 32-row m-tiles pay while the experts average at most 16 routed rows: above that, many
+// experts need two or more of them and their weight tiles are streamed once per m-tile.
+// Measured on GB300 (step us, 32-row tiles up to 32 / up to 16 rows per expert on
+// average): MiniMax-M3 block T = 768 2138 / 1885, T = 1024 2410 / 1951; Nano decode
+// T = 384 76.7 / 73.3, T = 512 87.1 / 80.1; AFMoE Zipf T = 256 217 / 206, T = 341
+// 233 / 211; equal at 16 rows (Nano decode T = 256: 68.4 / 68.9).
+constexpr int kThinAvgRows = 16;
 #ifndef MOE_PREFETCH_L2_TENTHS
 #define MOE_PREFETCH_L2_TENTHS 7
 #endif
@@ -954,10 +961,10 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     // (MX weights: 256-row tiles in one CTA each, two MMAs on every decoded weight tile)
     h->pair_now = path == kPathGrouped && h->num_sms >= 2 &&
                   (h->pair_opt == 1 || (h->pair_opt == 2 && (h->dense ? T >= 256 : slots >= 256ll * h->E)));
-    // 32-row m-tiles at decode sizes: at most 32 routed rows per expert on average
-    // (T * k <= 32 E) or at most 32 tokens (then no m-tile has more than 32 rows)
+    // 32-row m-tiles at decode sizes: at most 16 routed rows per expert on average
+    // (T * k <= 16 E) or at most 32 tokens (then no m-tile has more than 32 rows)
     h->thin_now = path == kPathGrouped && !h->pair_now && h->wfmt == MOE_WEIGHTS_BF16 &&
-                  (T <= kThinRows || (h->E > 0 && slots <= (long long)kThinRows * h->E));
+                  (T <= kThinRows || (h->E > 0 && slots <= (long long)kThinAvgRows * h->E));
     h->shared_parts = path == kPathGrouped && h->has_shared ? shared_parts(h, T) : 1;
     // the combine (no post-norm) overlaps the grouped expert GEMM: it waits per token for
     // the down tiles' counts instead of for the whole launch
