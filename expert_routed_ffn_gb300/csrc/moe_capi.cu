@@ -956,11 +956,15 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
             e = cudaMemsetAsync(h->router_stats, 0, moe::kRouterStats * sizeof(unsigned long long), s);
         if (e != cudaSuccess) return cuda_fail(e, "trace reset");
     }
-    // CTA pairs once the weight tiles are reused by 256 rows on average (a dense
-    // layer: T >= 256)
-    // (MX weights: 256-row tiles in one CTA each, two MMAs on every decoded weight tile)
+    // CTA pairs once the weight tiles are reused by enough rows on average: 160 with bf16
+    // weights (measured on GB300, step us without / with pairs: AFMoE-shaped T = 1536
+    // (144 rows) 308 / 303, T = 2048 (192) 363 / 355, Zipf T = 2048 375 / 348, Zipf
+    // T = 1024 255 / 269; the HBM-bound MiniMax-M3 shape at 128 rows 2977 / 3007), 256
+    // with MX weights (256-row tiles in one CTA each, two MMAs on every decoded weight
+    // tile); a dense layer: T >= 256
+    const long long pair_rows = h->wfmt == MOE_WEIGHTS_BF16 ? 160 : 256;
     h->pair_now = path == kPathGrouped && h->num_sms >= 2 &&
-                  (h->pair_opt == 1 || (h->pair_opt == 2 && (h->dense ? T >= 256 : slots >= 256ll * h->E)));
+                  (h->pair_opt == 1 || (h->pair_opt == 2 && (h->dense ? T >= 256 : slots >= pair_rows * h->E)));
     // 32-row m-tiles at decode sizes: at most 16 routed rows per expert on average
     // (T * k <= 16 E) or at most 32 tokens (then no m-tile has more than 32 rows)
     h->thin_now = path == kPathGrouped && !h->pair_now && h->wfmt == MOE_WEIGHTS_BF16 &&
