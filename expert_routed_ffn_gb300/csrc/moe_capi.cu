@@ -961,10 +961,13 @@ moe_status forward_device(moe_handle *h, const void *X, int T, void *Y, cudaStre
     // (144 rows) 308 / 303, T = 2048 (192) 363 / 355, Zipf T = 2048 375 / 348, Zipf
     // T = 1024 255 / 269; the HBM-bound MiniMax-M3 shape at 128 rows 2977 / 3007), 256
     // with MX weights (256-row tiles in one CTA each, two MMAs on every decoded weight
-    // tile); a dense layer: T >= 256
+    // tile); a dense layer: T >= 256.  Not for narrow experts (I < 512): their down
+    // tiles have a short K and the tile epilogues dominate (Nano-shaped, I = 256, T =
+    // 4096: 216 / 245, T = 2048: 136 / 167).
     const long long pair_rows = h->wfmt == MOE_WEIGHTS_BF16 ? 160 : 256;
     h->pair_now = path == kPathGrouped && h->num_sms >= 2 &&
-                  (h->pair_opt == 1 || (h->pair_opt == 2 && (h->dense ? T >= 256 : slots >= pair_rows * h->E)));
+                  (h->pair_opt == 1 ||
+                   (h->pair_opt == 2 && (h->dense ? T >= 256 : (h->I >= 512 && slots >= pair_rows * h->E))));
     // 32-row m-tiles at decode sizes: at most 16 routed rows per expert on average
     // (T * k <= 16 E) or at most 32 tokens (then no m-tile has more than 32 rows)
     h->thin_now = path == kPathGrouped && !h->pair_now && h->wfmt == MOE_WEIGHTS_BF16 &&

@@ -223,7 +223,8 @@ typedef enum {
                                   and half of the weight tile; MX weights: one CTA per 256-row tile,
                                   two 128-row MMAs on each decoded weight tile); 0 never, 1 always,
                                   2 (default) when T*k >= 160*E with bf16 weights, 256*E with MX
-                                  weights, T >= 256 for a dense layer (tensor-bound sizes) */
+                                  weights, and the expert width is at least 512; T >= 256 for
+                                  a dense layer (tensor-bound sizes) */
     MOE_OPT_GRAPH = 8,         /* moe_forward_host: 1 (default) captures the copy in, the forward and the
                                   copy out into a CUDA graph on the second call with the same host
                                   buffers, T and options, and replays it on later such calls (host
