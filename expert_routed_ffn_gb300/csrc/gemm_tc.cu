@@ -66,6 +66,11 @@ constexpr uint32_t kTmemCols = 512;             // two 128 x 256 fp32 accumulato
 constexpr uint64_t kDrainNs = 1000000000ull;    // bound of the drain after an abort
 constexpr uint64_t kPairDrainNs = 1000000ull;   // CTA pair: grace for the copies in flight after an abort
 constexpr int kRing = 8;                        // tile ids in flight from the producer to the other roles
+// CTA pairs: the last waves of tiles are claimed, not assigned.  Measured on GB300 (step
+// us, static order / 1 / 2 / 4 claimed waves): AFMoE prefill 547 / 542.5 / 542.9 / 545.3,
+// Zipf T = 4096 571 / 564.7 / 566.2 / 563.8, T = 16384 1820 / 1792 / 1788 / 1791; a fully
+// claimed order keeps fewer weight tiles shared in L2 (578 us on AFMoE prefill).
+constexpr int kTailWaves = 2;
 
 // Per-variant layout.  One CTA: stage = one k-block of 64, A 128 x 64 + B
 // 256 x 64 (48 KB), 4 stages.  CTA pair: each CTA stages its own 128 A rows and
@@ -447,9 +452,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
     auto ring_full = [&](int i) { return bar0 + 8u * (2 * kStages + 5 + i); };
     auto ring_empty = [&](int i) { return bar0 + 8u * (2 * kStages + 5 + kRing + i); };
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 5 + 2 * kRing);
+    // CTA pairs, tiles claimed at the tail: rank 0 hands each claimed id to rank 1 through
+    // a two-slot mailbox in rank 1's shared memory (claim_full in rank 1, claim_empty in rank 0)
+    auto claim_full = [&](uint32_t i) { return bar0 + 8u * (2 * kStages + 5 + 2 * kRing + i); };
+    auto claim_empty = [&](uint32_t i) { return bar0 + 8u * (2 * kStages + 5 + 2 * kRing + 2 + i); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 5 + 2 * kRing + 4);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *ring = reinterpret_cast<volatile int *>(tmem_slot + 2);  // [kRing] tile ids
+    volatile int *mailbox = ring + kRing;                                   // [2] claimed tile ids
+    static_assert(8 * (2 * kStages + 5 + 2 * kRing + 4) + 8 + 4 * kRing + 8 <= 512, "barrier block");
     float *xbuf = reinterpret_cast<float *>(smem + kStages * kStageBytes + 512);  // C::kXBufBytes
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -477,6 +488,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         for (int i = 0; i < kRing; ++i) {
             mbar_init(ring_full(i), 1);
             mbar_init(ring_empty(i), 2);  // the MMA thread and the epilogue have read the id
+        }
+        for (uint32_t i = 0; i < 2; ++i) {
+            mbar_init(claim_full(i), 1);   // rank 0's hand-over (rank 1's barrier)
+            mbar_init(claim_empty(i), 1);  // rank 1 has read the id (rank 0's barrier)
         }
         fence_mbar_init();
         *abort_flag = 0;
@@ -537,8 +552,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             // so the atomic's latency hides behind them while the claim stays late.
             const bool dyn = !PAIR && p.tile_counter != nullptr;
             const int stride = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
-            int next = dyn ? atomicAdd(p.tile_counter, 1) : (PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x);
-            for (int n = 0;; ++n) {
+            // CTA pairs: tiles in static round-robin order up to n_static (neighbouring pairs on
+            // neighbouring tiles of one weight tile, which then stays in L2), the last kTailWaves
+            // waves claimed from the ticket by whichever pair is free first
+            const int n_static = PAIR && p.tile_counter != nullptr ? max(0, total - kTailWaves * stride) : total;
+            uint32_t n_claim = 0;
+            auto claim_pair = [&](int &out) -> bool {
+                const uint32_t c = n_claim++, slot = c & 1u, ph = (c >> 1) & 1u;
+                if (leader) {
+                    if (!mbar_wait(claim_empty(slot), ph ^ 1u, p.wait_ns, abort_flag)) return false;
+                    out = n_static + atomicAdd(p.tile_counter, 1);
+                    st_cluster_s32(mapa_shared(smem_u32(const_cast<int *>(mailbox + slot)), 1), out);
+                    mbar_arrive_cluster(mapa_shared(claim_full(slot), 1));
+                } else {
+                    if (!mbar_wait_cluster(claim_full(slot), ph, p.wait_ns, abort_flag)) return false;
+                    out = mailbox[slot];
+                    mbar_arrive_cluster(mapa_shared(claim_empty(slot), 0));
+                }
+                return true;
+            };
+            // the tile after `cur`: the static one, or a claimed one past the static part
+            auto next_tile = [&](int cur, int &out) -> bool {
+                if (!PAIR) {
+                    out = dyn ? atomicAdd(p.tile_counter, 1) : cur + stride;
+                    return true;
+                }
+                if (cur + stride < n_static) {
+                    out = cur + stride;
+                    return true;
+                }
+                return claim_pair(out);
+            };
+            int next = 0;
+            if (!next_tile((PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x) - stride, next)) ok = false;
+            for (int n = 0; ok; ++n) {
                 const int tile = next < total ? next : total;  // total: the end marker
                 const int slot = n % kRing;
                 if (!mbar_wait(ring_empty(slot), ((n / kRing) & 1u) ^ 1u, p.wait_ns, abort_flag)) {
@@ -569,8 +616,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 for (int kb = 0; kb < sg.k_blocks; kb += kKB) {
                     const int s = L % kStages;
                     const uint32_t ph = (L / kStages) & 1u;
-                    if (kb == claim_at || (kKB > 1 && kb + 1 == claim_at))
-                        next = dyn ? atomicAdd(p.tile_counter, 1) : tile + stride;
+                    if ((kb == claim_at || (kKB > 1 && kb + 1 == claim_at)) && !next_tile(tile, next)) {
+                        ok = false;
+                        break;
+                    }
                     const uint64_t t0 = stats ? global_timer_ns() : 0;
                     if (!mbar_wait(empty_bar(s), ph ^ 1u, p.wait_ns, abort_flag)) {
                         ok = false;
@@ -1493,7 +1542,7 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
     }
     if (a.wfmt != kWeightsBf16) return cudaErrorInvalidValue;
     if (a.pair) {
-        if (a.num_ctas < 2 || (a.num_ctas & 1) || a.tile_counter != nullptr) return cudaErrorInvalidValue;
+        if (a.num_ctas < 2 || (a.num_ctas & 1)) return cudaErrorInvalidValue;
         return launch_pdl_cluster(gemm_tc_kernel<true>, dim3(a.num_ctas), dim3(kThreads),
                                   (size_t)GemmCfg<true>::kSmemBytes, s, dim3(2, 1, 1), a);
     }

@@ -283,9 +283,10 @@ struct GemmArgs {
     int *err;
     unsigned long long wait_ns;
     int num_ctas;
-    int pair;              // 1: CTA pairs (cta_group::2, 256-row tiles, static order; num_ctas even,
+    int pair;              // 1: CTA pairs (cta_group::2, 256-row tiles; num_ctas even,
                            //    tile_offs counting 256-row tiles; all maps from encode_map_*_kb2)
-    int *tile_counter;     // zeroed ticket: tiles claimed in order (dynamic); nullptr: round-robin
+    int *tile_counter;     // zeroed ticket: tiles claimed in order (one CTA per tile: every tile; CTA
+                           // pairs: the last waves, after a static round-robin part); nullptr: round-robin
     unsigned long long *trace;
     // nullptr, or kGemmStats ns sums over CTAs: producer waiting for a free
     // stage, producer waiting for gate/up rows, MMA waiting for data, MMA

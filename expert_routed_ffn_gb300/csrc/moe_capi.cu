@@ -742,7 +742,8 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
         if (!h->dense) g.seg[ns++] = dn;
         if (h->has_shared) g.seg[ns++] = sdn;
         g.num_segs = ns;
-        g.tile_counter = pair ? nullptr : h->tile_counters;
+        // CTA pairs claim only their last waves of tiles; MX 256-row tiles keep the static order
+        g.tile_counter = pair && mx ? nullptr : h->tile_counters;
         g.trace = trace_slot(h, *n);
         g.stats = h->trace_on ? h->gemm_stats : nullptr;
         return launched(h, moe::launch_gemm_tc(g, s), "experts_gemm", n, s);
@@ -750,14 +751,14 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     g.num_segs = 0;
     if (!h->dense) g.seg[g.num_segs++] = gu;
     if (h->has_shared) g.seg[g.num_segs++] = sgu;
-    g.tile_counter = pair ? nullptr : h->tile_counters;
+    g.tile_counter = pair && mx ? nullptr : h->tile_counters;
     g.trace = trace_slot(h, *n);
     moe_status st = launched(h, moe::launch_gemm_tc(g, s), "gate_up_gemm", n, s);
     if (st != MOE_OK) return st;
     g.num_segs = 0;
     if (!h->dense) g.seg[g.num_segs++] = dn;
     if (h->has_shared) g.seg[g.num_segs++] = sdn;
-    g.tile_counter = pair ? nullptr : h->tile_counters + 1;
+    g.tile_counter = pair && mx ? nullptr : h->tile_counters + 1;
     g.trace = trace_slot(h, *n);
     return launched(h, moe::launch_gemm_tc(g, s), "down_gemm", n, s);
 }
