@@ -119,7 +119,7 @@ struct moe_handle {
     bool ovl_now = false;      // this forward: combine overlapped with the grouped GEMM
     int ready_shared_base = 0; // first counter of the shared expert's m-tiles
     bool fuse_experts = true;  // gate/up and down in one persistent launch
-    int pair_opt = 2;          // CTA-pair expert GEMM: 0 never, 1 always, 2 when T*k >= 256*E
+    int pair_opt = 2;          // CTA-pair expert GEMM: 0 never, 1 always, 2 at tensor-bound sizes
     bool pair_swap = true;     // CTA pairs: m-tiles of <= 128 rows with swapped operands
     bool pair_now = false;     // the current forward's choice
     int shared_parts = 1;      // K ranges of the shared (dense) down projection this forward
