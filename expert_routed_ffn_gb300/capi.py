@@ -34,6 +34,7 @@ MOE_OPT_GEMM_PAIR = 6
 MOE_OPT_GRAPH = 8
 MOE_OPT_PAIR_SWAP = 9
 MOE_OPT_COMBINE_OVERLAP = 10
+MOE_OPT_STAGED_STORES = 11
 MOE_BUF_GEMM_STATS = 6
 MOE_BUF_ROUTER_STATS = 7
 MOE_BUF_NORMED_X = 8

@@ -93,8 +93,12 @@ struct GemmCfg {
     static constexpr int kStageBytes = kAStage + kBBytes;
     // CTA pairs: the gate values' hand-over buffer of swapped gate/up tiles, 2 x 32 x 32 fp32
     static constexpr int kXBufBytes = PAIR ? 8192 : 0;
-    static constexpr int kSmemBytes =
-        kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers, tile ring*/ + kXBufBytes;
+    // the epilogue's store staging: one [32 rows][128 bytes] slice per TMEM lane quadrant,
+    // 1024-byte aligned.  Thin tiles store from registers: their one quadrant of rows is
+    // mostly partial, and staging it measured slower (Nano decode 68.6 -> 74.4 us)
+    static constexpr int kEpiOff = (kStages * kStageBytes + 512 + kXBufBytes + 1023) / 1024 * 1024;
+    static constexpr int kEpiBufBytes = THIN ? 0 : 4 * 4096;
+    static constexpr int kSmemBytes = kEpiOff + kEpiBufBytes + 1024 /*align*/;
     static constexpr int kBM = PAIR ? 2 * kGemmBM : (THIN ? kThinRows : kGemmBM);  // rows per tile
 };
 
@@ -236,7 +240,41 @@ struct EpiCtx {
     const int *s_seg_end, *s_offs, *s_toffs;
     int half;
     float *xbuf;  // CTA pairs: [2][32][32] hand-over of swapped gate/up tiles
+    // store staging, [ebuf_quads][32 rows][128 bytes] (quadrant q uses slice q % ebuf_quads);
+    // 0: none, every row stored from registers
+    uint32_t ebuf;
+    int ebuf_quads;
 };
+
+// One warp's staged store of a [32 rows][128 bytes] slice: lane i has written row i into
+// its 128-byte-swizzled staging buffer `sb` (16-byte unit j at j ^ (i % 8)).  All 32 rows
+// valid: one TMA store of the box at (x, y) by lane 0.  Fewer (`rows`): 16-byte stores
+// of the valid rows, eight lanes per row, row i at `dst + i * ld_bytes` (coalesced).
+__device__ __forceinline__ void epi_flush(const CUtensorMap *map, uint32_t sb, int rows, int x, int y, char *dst,
+                                          size_t ld_bytes, int lane) {
+    if (rows == 32) {
+        fence_proxy_async_smem();  // the rows' generic writes -> the TMA's reads
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(map, sb, x, y);
+            bulk_commit();
+        }
+    } else {
+        __syncwarp();
+        const int u = lane & 7;
+        for (int i = lane >> 3; i < rows; i += 4) {
+            uint4 v;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(sb + (uint32_t)i * 128u + ((uint32_t)(u ^ (i & 7)) << 4)));
+            *reinterpret_cast<uint4 *>(dst + (size_t)i * ld_bytes + 16 * u) = v;
+        }
+        __syncwarp();  // the buffer is read before the next slice overwrites it
+    }
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
 
 // Epilogue role (kEpiWarps warps, named barrier 1): for each tile id from the
 // ring, wait for its accumulator, apply the activation and store bf16 rows
@@ -363,7 +401,81 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (a + hh) * kGemmBN;
         const bool row_ok = r < t.m_valid;
         const size_t orow = t.ks * sg.split_stride + (size_t)(t.row0 + (row_ok ? r : 0)) * sg.ldo;
-        if (sg.glu) {
+        if (c.ebuf != 0 && sg.map_out != 0) {
+            // Staged: each 32-column (fp32) or 64-column (bf16) slice of this warp's 32 rows
+            // goes through shared memory and leaves as one TMA store (or coalesced stores
+            // when the quadrant holds fewer valid rows), instead of one row per lane
+            const int rows = min(32, t.m_valid - q * 32);
+            if (rows > 0) {  // warp-uniform
+                const uint32_t sb = c.ebuf + (uint32_t)(q % c.ebuf_quads) * 4096u;
+                const uint32_t srow = sb + (uint32_t)lane * 128u;
+                const int sw = lane & 7;
+                const CUtensorMap *map = &p.maps[sg.map_out];
+                const int y = (t.ks != 0 ? t.ks * (int)(sg.split_stride / sg.ldo) : 0) + t.row0 + q * 32;
+                const size_t esz = sg.glu ? 2 : 4;
+                char *const obase = static_cast<char *>(sg.out) + (t.ks * sg.split_stride + (size_t)(t.row0 + q * 32) * sg.ldo) * esz;
+                const size_t ld_bytes = (size_t)sg.ldo * esz;
+                if (sg.glu) {
+                    static_assert(128 / kEpiParts % 64 == 0, "bf16 slices of 64 columns");
+#pragma unroll 1
+                    for (int c0 = part * (128 / kEpiParts); c0 < (part + 1) * (128 / kEpiParts); c0 += 64) {
+                        const int col = t.nt * 128 + c0;
+                        if (col >= sg.n_out) break;
+                        if (lane == 0) bulk_wait_read_all();  // the previous slice's store has read the buffer
+                        __syncwarp();
+#pragma unroll 1
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            uint32_t g[32], u[32];
+                            tmem_ld32(tb + c0 + 32 * h2, g);
+                            tmem_ld32(tb + 128 + c0 + 32 * h2, u);
+                            tmem_ld_wait();
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                pk[i] = pack_bf16x2(
+                                    glu_act(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), p.act, p.alpha,
+                                            p.limit, p.beta),
+                                    glu_act(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]), p.act,
+                                            p.alpha, p.limit, p.beta));
+#pragma unroll
+                            for (int v = 0; v < 4; ++v)
+                                st_shared_v4(srow + ((uint32_t)((4 * h2 + v) ^ sw) << 4), pk[4 * v], pk[4 * v + 1],
+                                             pk[4 * v + 2], pk[4 * v + 3]);
+                        }
+                        epi_flush(map, sb, rows, col, y, obase + (size_t)col * 2, ld_bytes, lane);
+                    }
+                } else {
+                    constexpr int kSpan = kGemmBN / kEpiParts;
+#pragma unroll 1
+                    for (int c0 = part * kSpan; c0 < (part + 1) * kSpan; c0 += 32) {
+                        const int col = t.nt * kGemmBN + c0;
+                        if (col >= sg.n_out) break;
+                        uint32_t v32[32];
+                        tmem_ld32(tb + c0, v32);
+                        tmem_ld_wait();
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            st_shared_v4(srow + ((uint32_t)(v ^ sw) << 4), v32[4 * v], v32[4 * v + 1], v32[4 * v + 2],
+                                         v32[4 * v + 3]);
+                        epi_flush(map, sb, rows, col, y, obase + (size_t)col * 4, ld_bytes, lane);
+                    }
+                }
+                if (sg.tok_done != nullptr) {  // the rows are stored: this tile's columns of each token
+                    if (lane == 0) {
+                        bulk_wait_all();
+                        fence_proxy_async();
+                    }
+                    __syncwarp();
+                    if (row_ok) {
+                        const int row = t.row0 + r;
+                        __threadfence();
+                        atomicAdd(sg.tok_done + (sg.row_tok != nullptr ? sg.row_tok[row] : row), 2);
+                    }
+                }
+            }
+        } else if (sg.glu) {
             constexpr int kSpan = 128 / kEpiParts;  // output columns per slice
 #pragma unroll 1
             for (int c0 = part * kSpan; c0 < (part + 1) * kSpan; c0 += 32) {
@@ -415,8 +527,10 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
         else
             mbar_arrive(tempty_bar(a));
         if (sg.signal != nullptr) {
-            // publish the stored rows: proxy fence for the consumer's TMA reads,
-            // device-scope fence, all four warps done, then one release increment
+            // publish the stored rows: this warp's TMA stores complete, proxy fence for the
+            // consumer's TMA reads, device-scope fence, all four warps done, then one
+            // release increment
+            if (c.ebuf != 0 && lane == 0) bulk_wait_all();
             fence_proxy_async();
             __threadfence();
             epi_bar();
@@ -426,6 +540,7 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
         if (stats) w_work += global_timer_ns() - t1;
         ++n_acc;
     }
+    if (c.ebuf != 0 && lane == 0) bulk_wait_all();  // no store may still read the buffer when the CTA exits
     if (stats && lead_thread) {
         atomicAdd(stats + 4, (unsigned long long)w_tfull);
         atomicAdd(stats + 5, (unsigned long long)w_work);
@@ -792,7 +907,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     } else {
         // ----------------------------------------------------------- epilogue
         EpiCtx c{ring_full(0), ring_empty(0), tfull_bar(0), tempty_bar(0), ring, abort_flag, tmem_base, total,
-                 s_seg_end, s_offs, s_toffs, half, xbuf};
+                 s_seg_end, s_offs, s_toffs, half, xbuf, THIN ? 0u : smem_u32(smem + C::kEpiOff),
+                 C::kEpiBufBytes / 4096 > 0 ? C::kEpiBufBytes / 4096 : 1};
         epilogue_role<PAIR, kBM>(p, c, warp, lane);
     }
 
@@ -1374,7 +1490,7 @@ __global__ void __launch_bounds__(MxCfg<WF, M256, CW>::kThreads, 1) gemm_mx_kern
     } else {
         // ----------------------------------------------------------- epilogue
         EpiCtx c{ring_full(0), ring_empty(0), tfull_bar(0), tempty_bar(0), ring, abort_flag, tmem_base, total,
-                 s_seg_end, s_offs, s_toffs, half, nullptr};
+                 s_seg_end, s_offs, s_toffs, half, nullptr, 0u, 1};
         epilogue_role<false, kBM, M256 ? 2 : 1>(p, c, warp, lane);
     }
 
@@ -1426,6 +1542,19 @@ CUresult encode_map_a_box(CUtensorMap *m, const void *ptr, int rows, int K, int 
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult encode_map_out(CUtensorMap *m, const void *ptr, int rows, int cols, int f32) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t es = f32 ? 4 : 2;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * es};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / es), 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr),
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 CUresult encode_map_b(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int box_rows) {

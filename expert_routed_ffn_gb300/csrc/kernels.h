@@ -225,7 +225,7 @@ constexpr int kGemmBK = 64;    // K per pipeline stage (one 128-byte swizzle row
 constexpr int kGemmBN = 256;   // MMA N; gate/up tiles hold 128 gate + 128 up columns
 
 constexpr int kGemmMaxSegments = 5;
-constexpr int kGemmMaxMaps = 16;
+constexpr int kGemmMaxMaps = 20;
 
 // Storage of the expert weights (the B operand): bf16, or OCP microscaling
 // (MX) codes with one E8M0 scale per 32 consecutive K values.
@@ -271,6 +271,10 @@ struct GemmSegment {
     // itself when row_tok is nullptr (dense segments)
     int *tok_done;
     const int32_t *row_tok;
+    // tiles with the tokens as M: the output's store map (encode_map_out: boxes of 32 rows of
+    // 128 bytes), through which the epilogue writes each 32-row slice whose rows are all
+    // valid; 0: none (map 0 is always an A operand), every row stored from registers
+    int map_out;
 };
 constexpr int kSwapMaxRows = 128;
 
@@ -359,6 +363,9 @@ CUresult encode_map_a(CUtensorMap *m, const void *ptr, int rows, int K);
 CUresult encode_map_a_kb2(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows = 128);
 CUresult encode_map_b_kb2(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int box_rows);
 CUresult encode_map_a_box(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows);
+// [rows, cols] bf16 (f32 = 0) or fp32 (f32 = 1) output: boxes of 32 rows x 128 bytes,
+// 128-byte swizzle (the GEMM epilogue's TMA stores)
+CUresult encode_map_out(CUtensorMap *m, const void *ptr, int rows, int cols, int f32);
 CUresult encode_map_b(CUtensorMap *m, const void *ptr, int groups, int rows, int K, int box_rows);
 // MX weights: element codes [groups, rows, K] (E4M3, one byte each) or [groups,
 // rows, K / 2] (E2M1, two per byte, element 2j in the low nibble), box of one

@@ -116,6 +116,7 @@ struct moe_handle {
     int *tile_counters = nullptr;  // [2] tile tickets of the expert GEMM launches
     int *tok_done = nullptr;   // [max_tokens] rows stored per token, for the overlapped combine
     bool combine_overlap = true;  // the combine waits per token instead of for the whole GEMM
+    bool staged_stores = true;    // the expert GEMM's epilogue stores through shared memory
     bool ovl_now = false;      // this forward: combine overlapped with the grouped GEMM
     int ready_shared_base = 0; // first counter of the shared expert's m-tiles
     bool fuse_experts = true;  // gate/up and down in one persistent launch
@@ -136,6 +137,9 @@ struct moe_handle {
 
     // TMA descriptors fixed at create
     CUtensorMap m_xsorted, m_hbuf, m_hs, m_xbf16, m_gate, m_up, m_down, m_shg, m_shu, m_shd, m_wr;
+    // the grouped GEMM's output store maps: routed and shared activations, routed slot rows,
+    // shared output and its K-split partials
+    CUtensorMap m_out_hbuf, m_out_hs, m_out_yslot, m_out_ys, m_out_ysp;
     // swapped-operand GEMMs: weight boxes of 64 (gate/up) and 128 (down) rows,
     // token boxes of 32 ([0]) or 64 ([1]) rows
     CUtensorMap m_gate64, m_up64, m_down128, m_shg64, m_shu64, m_shd128;
@@ -347,6 +351,8 @@ moe_status build_maps(moe_handle *h) {
         if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", #call, (int)r); \
     } while (0)
     if (!h->dense) {
+    MAP(moe::encode_map_out(&h->m_out_hbuf, h->hbuf, MT * k, I, 0));
+    MAP(moe::encode_map_out(&h->m_out_yslot, h->yslot, MT * k, H, 1));
     MAP(moe::encode_map_a(&h->m_xsorted, h->x_sorted, MT * k, H));
     MAP(moe::encode_map_a(&h->m_hbuf, h->hbuf, MT * k, I));
     MAP(moe::encode_map_a_kb2(&h->m_xs2, h->x_sorted, MT * k, H));
@@ -390,6 +396,9 @@ moe_status build_maps(moe_handle *h) {
         if (h->has_shared && h->x_f32) MAP(moe::encode_map_a_box(&h->m_xbf_n[v], h->x_bf16, MT, H, n));
     }
     if (h->has_shared) {
+        MAP(moe::encode_map_out(&h->m_out_hs, h->hs, MT, S, 0));
+        MAP(moe::encode_map_out(&h->m_out_ys, h->ys, MT, H, 1));
+        MAP(moe::encode_map_out(&h->m_out_ysp, h->ys_split, (int)(split_elems(h) / H), H, 1));
         MAP(moe::encode_map_a(&h->m_hs, h->hs, MT, S));
         if (h->x_f32) MAP(moe::encode_map_a(&h->m_xbf16, h->x_bf16, MT, H));
         MAP(moe::encode_map_a_kb2(&h->m_hs2, h->hs, MT, S));
@@ -620,6 +629,8 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
            kGs = 10, kUs = 11, kSGs = 12, kSUs = 13, kDs = 14, kSDs = 15 };
     // bf16 CTA pairs (no scale maps): the swapped tiles' token and 64-row weight maps
     enum { kXw32 = 10, kXw64 = 11, kHw32 = 12, kHw64 = 13, kGw = 14, kUw = 15 };
+    // the epilogue's output store maps
+    enum { kOutH = 16, kOutHs = 17, kOutY = 18, kOutYs = 19 };
     const bool mx = h->wfmt != MOE_WEIGHTS_BF16;
     moe::GemmArgs g{};
     g.err = h->err;
@@ -717,13 +728,13 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
     const int nt_gu = (I + 127) / 128, nt_sgu = (S + 127) / 128, nt_d = (H + moe::kGemmBN - 1) / moe::kGemmBN;
     const bool fused = h->fuse_experts;
     int *sig = fused ? h->ready : nullptr;
-    const moe::GemmSegment gu{0, E, 0, 0, h->offs, h->tile_offs, nt_gu, H / 64, 0, I, h->hbuf, I,
+    moe::GemmSegment gu{0, E, 0, 0, h->offs, h->tile_offs, nt_gu, H / 64, 0, I, h->hbuf, I,
                               1, kXs, kG, kU, sig, nullptr, 0, 0, 0, 0, kGs, kUs,
                               {swap ? kXw32 : 0, swap ? kXw64 : 0}, swap ? kGw : 0, swap ? kUw : 0};
-    const moe::GemmSegment sgu{1, 1, sh_base, T, nullptr, nullptr, nt_sgu, H / 64, 0, S, h->hs, S,
+    moe::GemmSegment sgu{1, 1, sh_base, T, nullptr, nullptr, nt_sgu, H / 64, 0, S, h->hs, S,
                                1, kX, kSG, kSU, sig, nullptr, 0, h->ready_shared_base, 0, 0, kSGs, kSUs};
     int *const tok_done = h->ovl_now ? h->tok_done : nullptr;  // the combine waits per token
-    const moe::GemmSegment dn{0, E, 0, 0, h->offs, h->tile_offs, nt_d, I / 64, 0, H, h->yslot, H,
+    moe::GemmSegment dn{0, E, 0, 0, h->offs, h->tile_offs, nt_d, I / 64, 0, H, h->yslot, H,
                               0, kHb, kD, kD, nullptr, fused ? h->ready : nullptr, nt_gu, 0, 0, 0, kDs, kDs,
                               {swap ? kHw32 : 0, swap ? kHw64 : 0}, 0, 0, tok_done, h->sorted_tok};
     // At small T the shared down projection (K = S) is the longest tile chain: its K
@@ -735,6 +746,20 @@ moe_status run_grouped(moe_handle *h, const void *X, int T, cudaStream_t s, int 
                          parts > 1 ? h->ys_split : h->ys, H, 0, kHs, kSD, kSD, nullptr,
                          fused ? h->ready : nullptr, nt_sgu, h->ready_shared_base, parts, (size_t)T * H,
                          kSDs, kSDs, {0, 0}, 0, 0, tok_done, nullptr};
+    // output store maps (the epilogue of tiles with the tokens as M); the K-split partials
+    // are rows ks * T + token of one [parts * T, H] map
+    if (h->staged_stores) {
+        g.maps[kOutH] = h->dense ? g.maps[kOutH] : h->m_out_hbuf;
+        g.maps[kOutY] = h->dense ? g.maps[kOutY] : h->m_out_yslot;
+        if (h->has_shared) {
+            g.maps[kOutHs] = h->m_out_hs;
+            g.maps[kOutYs] = parts > 1 ? h->m_out_ysp : h->m_out_ys;
+        }
+        gu.map_out = kOutH;
+        dn.map_out = kOutY;
+        sgu.map_out = kOutHs;
+        sdn.map_out = kOutYs;
+    }
     if (fused) {
         int ns = 0;
         if (!h->dense) g.seg[ns++] = gu;
@@ -1390,6 +1415,10 @@ moe_status moe_set_option(moe_handle *h, int option, long long value) {
     case MOE_OPT_COMBINE_OVERLAP:
         if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "combine overlap %lld", value);
         h->combine_overlap = value != 0;
+        return MOE_OK;
+    case MOE_OPT_STAGED_STORES:
+        if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "staged stores %lld", value);
+        h->staged_stores = value != 0;
         return MOE_OK;
     case MOE_OPT_PAIR_SWAP:
         if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "pair swap %lld", value);

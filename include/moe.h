@@ -236,11 +236,15 @@ typedef enum {
                                   128 rows (the pair's 256 weight rows as M, the tile's rows rounded
                                   up to 32 as N), so the MMA skips most of the padding rows; 0 runs
                                   every tile with the tokens as M.  Results are unchanged */
-    MOE_OPT_COMBINE_OVERLAP = 10 /* path 2 without the post-MLP norm: 1 (default) launches the combine
+    MOE_OPT_COMBINE_OVERLAP = 10, /* path 2 without the post-MLP norm: 1 (default) launches the combine
                                   while the expert GEMM runs; the down tiles count each token's
                                   stored rows and the combine adds a token as soon as all of its
                                   rows are in (the same fixed-order sum); 0 waits for the whole GEMM
                                   first.  Results are unchanged */
+    MOE_OPT_STAGED_STORES = 11 /* path 2, bf16 weights: 1 (default) stores the expert GEMM's outputs
+                                  of tiles with the tokens as M through shared memory (TMA stores of
+                                  32-row slices, coalesced stores of partial ones); 0 stores each
+                                  row from registers.  Results are unchanged */
 } moe_option;
 
 /* Set an option.  Errors: INVALID_ARG (unknown option or value). */

@@ -227,6 +227,26 @@ def test_dense_fused_equals_two_launches_and_has_no_router():
         blk.inspect(capi.MOE_BUF_TOPK_IDX, 4, torch.int32)
 
 
+@pytest.mark.parametrize("name", ["dense_afmoe_ragged", "dense_split16", "dense_T1"])
+def test_dense_staged_stores_are_bit_identical(name):
+    """Hidden activations and K-split partial outputs stored through shared memory (TMA
+    stores of full 32-row slices, coalesced stores of partial ones) equal the rows stored
+    from registers: the same hidden rows and the same block output, bit for bit."""
+    shape = DENSE[name]
+    S = shape.shared_intermediate_size
+    for pair in (0, 1):
+        inputs, blk, _ = _run(shape, (capi.PATH_GROUPED, pair))
+        outs = []
+        for staged in (1, 0):
+            blk.set_option(capi.MOE_OPT_STAGED_STORES, staged)
+            Y = blk.forward(inputs["X"]).clone()
+            torch.cuda.synchronize()
+            assert blk.sync_status() == capi.MOE_OK
+            outs.append((Y, blk.inspect(capi.MOE_BUF_SHARED_HIDDEN, shape.T * S, torch.bfloat16)))
+        assert torch.equal(outs[0][1], outs[1][1]), (name, pair)
+        assert torch.equal(outs[0][0], outs[1][0]), (name, pair)
+
+
 def test_dense_token_permutation_equivariance():
     shape = DENSE["dense_afmoe_ragged"]
     inputs, blk, Y = _run(shape)

@@ -285,6 +285,38 @@ def test_combine_overlapped_with_gemm_is_bit_identical(name):
     blk.close()
 
 
+@pytest.mark.parametrize("name,pair", [("nano_decode", 2), ("nano_T1", 2), ("nano_T129", 2), ("afmoe_ragged", 0),
+                                       ("afmoe_ragged", 1), ("m3_small_packed", 2)])
+def test_staged_stores_are_bit_identical(name, pair):
+    """The expert GEMM's outputs stored through shared memory (a TMA store per full
+    32-row slice, coalesced stores of the rows of a partial one) equal the rows each
+    lane stores from registers, bit for bit: routed hidden activations, the shared
+    expert's hidden activations and the block output; 32-row (decode), 128-row and
+    256-row (CTA pair) tiles, ragged experts, one token."""
+    shape = SMALL[name]
+    inputs, blk = P.make_case(shape)
+    blk.set_option(capi.MOE_OPT_PATH, capi.PATH_GROUPED)
+    blk.set_option(capi.MOE_OPT_GEMM_PAIR, pair)
+    T, k, I, S = shape.T, shape.k, shape.I, shape.S
+    outs = []
+    for staged in (1, 0):
+        blk.set_option(capi.MOE_OPT_STAGED_STORES, staged)
+        Y = blk.forward(inputs["X"]).clone()
+        torch.cuda.synchronize()
+        assert blk.sync_status() == capi.MOE_OK
+        hid = blk.inspect(capi.MOE_BUF_HIDDEN, T * k * I, torch.bfloat16)
+        sh = blk.inspect(capi.MOE_BUF_SHARED_HIDDEN, T * S, torch.bfloat16) if S else None
+        outs.append((Y, hid, sh))
+    (Y1, h1, s1), (Y0, h0, s0) = outs
+    assert torch.equal(h1, h0), "routed hidden rows differ"
+    if S:
+        assert torch.equal(s1, s0), "shared hidden rows differ"
+    assert torch.equal(Y1, Y0), "block output differs"
+    ih = P.host_inputs(inputs)
+    P.check_output(P.to_np(Y1), oracle.forward_inputs(shape, ih), True, tag=f"{name}-staged")
+    blk.close()
+
+
 def test_token_permutation_equivariance_and_determinism():
     shape = SMALL["afmoe_ragged"]
     for path in PATHS.values():
