@@ -121,6 +121,18 @@ __device__ __forceinline__ int seg_tiles(const GemmSegment &s, const int *toffs)
     return toffs[s.num_groups] * s.n_tiles;
 }
 
+// The launch's segments, copied from the kernel parameters into shared memory when
+// a kernel of this file starts (load_segments): every role reads them per tile, and a
+// parameter read that misses the constant cache costs about a microsecond under load.
+__shared__ GemmSegment s_seg[kGemmMaxSegments];
+__device__ __forceinline__ void load_segments(const GemmArgs &p) {
+    static_assert(sizeof(GemmSegment) % 4 == 0, "segments copied as words");
+    constexpr int kWords = (int)(sizeof(GemmSegment) * kGemmMaxSegments / 4);
+    const int *src = reinterpret_cast<const int *>(p.seg);
+    int *dst = reinterpret_cast<int *>(s_seg);
+    for (int i = threadIdx.x; i < kWords; i += blockDim.x) dst[i] = src[i];
+}
+
 // Tile -> segment, group, m-tile, n-tile.  With CTA pairs (BM = 256) the CTA of
 // cluster rank `half` takes rows [128 * half, 128 * half + 128) of the tile, and
 // the per-128-row counters are numbered 2 * m-tile + half.
@@ -132,7 +144,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &p, int tile, const i
     t.swp = 0;
     while (t.seg + 1 < p.num_segs && tile >= seg_end[t.seg]) ++t.seg;
     if (t.seg > 0) tile -= seg_end[t.seg - 1];
-    const GemmSegment &s = p.seg[t.seg];
+    const GemmSegment &s = s_seg[t.seg];
     constexpr int kRows = BM < kGemmBM ? BM : kGemmBM;  // rows of a tile per CTA
     constexpr int kSub = BM / kRows;                    // CTA parts of a tile (2 with CTA pairs)
     if (s.dense) {
@@ -293,6 +305,8 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
     const int total = c.total, half = c.half;
     const int *s_seg_end = c.s_seg_end, *s_offs = c.s_offs, *s_toffs = c.s_toffs;
     unsigned long long *const stats = p.stats;
+    const int act = p.act;  // loop-invariant: read the parameters once
+    const float alpha = p.alpha, limit = p.limit, beta = p.beta;
     auto abort_all = [&]() {
         if (PAIR)
             raise_abort_pair(p.err, abort_flag);
@@ -319,7 +333,7 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
         if (lead_thread) mbar_arrive(ring_empty(slot));
         if (tile >= total) break;
         const Tile tile0 = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, HALVES == 2 ? 0 : half);
-        const GemmSegment &sg = p.seg[tile0.seg];
+        const GemmSegment &sg = s_seg[tile0.seg];
         const uint32_t a = HALVES == 2 ? 0u : n_acc & 1u, aph = HALVES == 2 ? n_acc & 1u : (n_acc >> 1) & 1u;
         const bool ready = __all_sync(0xffffffffu, PAIR ? mbar_wait_cluster(tfull_bar(a), aph, p.wait_ns, abort_flag)
                                                         : mbar_wait(tfull_bar(a), aph, p.wait_ns, abort_flag));
@@ -365,10 +379,8 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
                         for (int j = 0; j < 16; ++j)
                             if (j < nj)
                                 o[(size_t)j * sg.ldo] = __float2bfloat16_rn(
-                                    gate_w ? glu_act(__uint_as_float(v[j]), xu[j * 32 + lane], p.act, p.alpha,
-                                                     p.limit, p.beta)
-                                           : glu_act(xg[j * 32 + lane], __uint_as_float(v[16 + j]), p.act, p.alpha,
-                                                     p.limit, p.beta));
+                                    gate_w ? glu_act(__uint_as_float(v[j]), xu[j * 32 + lane], act, alpha, limit, beta)
+                                           : glu_act(xg[j * 32 + lane], __uint_as_float(v[16 + j]), act, alpha, limit, beta));
                     }
                     epi_bar();
                 }
@@ -433,10 +445,8 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
                                 pk[i] = pack_bf16x2(
-                                    glu_act(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), p.act, p.alpha,
-                                            p.limit, p.beta),
-                                    glu_act(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]), p.act,
-                                            p.alpha, p.limit, p.beta));
+                                    glu_act(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), act, alpha, limit, beta),
+                                    glu_act(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]), act, alpha, limit, beta));
 #pragma unroll
                             for (int v = 0; v < 4; ++v)
                                 st_shared_v4(srow + ((uint32_t)((4 * h2 + v) ^ sw) << 4), pk[4 * v], pk[4 * v + 1],
@@ -489,10 +499,9 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs &p, const EpiCtx &c
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         pk[i] = pack_bf16x2(
-                            glu_act(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), p.act,
-                                    p.alpha, p.limit, p.beta),
+                            glu_act(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), act, alpha, limit, beta),
                             glu_act(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]),
-                                    p.act, p.alpha, p.limit, p.beta));
+                                    act, alpha, limit, beta));
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<bf16 *>(sg.out) + orow + col);
 #pragma unroll
                     for (int v = 0; v < 4; ++v)
@@ -590,6 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             raise_abort(p.err, abort_flag);
     };
     trace_mark(p.trace, 0);
+    load_segments(p);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full_bar(s), 1);
@@ -638,17 +648,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     __shared__ int s_seg_end[kGemmMaxSegments];
     int grouped = -1;
     for (int s = 0; s < p.num_segs; ++s)
-        if (!p.seg[s].dense) grouped = s;
+        if (!s_seg[s].dense) grouped = s;
     if (grouped >= 0)
-        for (int i = threadIdx.x; i <= p.seg[grouped].num_groups; i += blockDim.x) {
-            s_offs[i] = p.seg[grouped].offs[i];
-            s_toffs[i] = p.seg[grouped].tile_offs[i];
+        for (int i = threadIdx.x; i <= s_seg[grouped].num_groups; i += blockDim.x) {
+            s_offs[i] = s_seg[grouped].offs[i];
+            s_toffs[i] = s_seg[grouped].tile_offs[i];
         }
     __syncthreads();
     if (threadIdx.x == 0) {
         int run = 0;
         for (int s = 0; s < p.num_segs; ++s) {
-            run += seg_tiles<kBM>(p.seg[s], s_toffs);
+            run += seg_tiles<kBM>(s_seg[s], s_toffs);
             s_seg_end[s] = run;
         }
     }
@@ -711,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 mbar_arrive(ring_full(slot));
                 if (tile >= total) break;
                 const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
-                const GemmSegment &sg = p.seg[t.seg];
+                const GemmSegment &sg = s_seg[t.seg];
                 const int g = sg.group_base + t.group;
                 const int claim_at = sg.k_blocks > 3 * kKB ? sg.k_blocks - 3 * kKB : 0;
                 if (sg.wait != nullptr) {  // A rows written earlier in this launch
@@ -834,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 mbar_arrive(ring_empty(slot));
                 if (tile >= total) break;
                 const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
-                const GemmSegment &sg = p.seg[t.seg];
+                const GemmSegment &sg = s_seg[t.seg];
                 const uint32_t a = n_acc & 1u, aph = (n_acc >> 1) & 1u;
                 const uint64_t t0 = stats ? global_timer_ns() : 0;
                 if (!(PAIR ? mbar_wait_cluster(tempty_bar(a), aph ^ 1u, p.wait_ns, abort_flag)
@@ -1208,6 +1218,7 @@ __global__ void __launch_bounds__(MxCfg<WF, M256, CW>::kThreads, 1) gemm_mx_kern
     const int half = 0;
     auto abort_all = [&]() { raise_abort(p.err, abort_flag); };
     trace_mark(p.trace, 0);
+    load_segments(p);
     if (threadIdx.x == 0) {
         for (int i = 0; i < kRing; ++i) {
             mbar_init(ring_full(i), 1);
@@ -1251,17 +1262,17 @@ __global__ void __launch_bounds__(MxCfg<WF, M256, CW>::kThreads, 1) gemm_mx_kern
     __shared__ int s_seg_end[kGemmMaxSegments];
     int grouped = -1;
     for (int s = 0; s < p.num_segs; ++s)
-        if (!p.seg[s].dense) grouped = s;
+        if (!s_seg[s].dense) grouped = s;
     if (grouped >= 0)
-        for (int i = threadIdx.x; i <= p.seg[grouped].num_groups; i += blockDim.x) {
-            s_offs[i] = p.seg[grouped].offs[i];
-            s_toffs[i] = p.seg[grouped].tile_offs[i];
+        for (int i = threadIdx.x; i <= s_seg[grouped].num_groups; i += blockDim.x) {
+            s_offs[i] = s_seg[grouped].offs[i];
+            s_toffs[i] = s_seg[grouped].tile_offs[i];
         }
     __syncthreads();
     if (threadIdx.x == 0) {
         int run = 0;
         for (int s = 0; s < p.num_segs; ++s) {
-            run += seg_tiles<kBM>(p.seg[s], s_toffs);
+            run += seg_tiles<kBM>(s_seg[s], s_toffs);
             s_seg_end[s] = run;
         }
     }
@@ -1290,7 +1301,7 @@ __global__ void __launch_bounds__(MxCfg<WF, M256, CW>::kThreads, 1) gemm_mx_kern
                 mbar_arrive(ring_full(slot));
                 if (tile >= total) break;
                 const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
-                const GemmSegment &sg = p.seg[t.seg];
+                const GemmSegment &sg = s_seg[t.seg];
                 const int g = sg.group_base + t.group;
                 const int claim_at = sg.k_blocks > 3 ? sg.k_blocks - 3 : 0;
                 // rows of the B tile's two 128-row halves: gate and up rows of n-tile nt,
@@ -1345,7 +1356,7 @@ __global__ void __launch_bounds__(MxCfg<WF, M256, CW>::kThreads, 1) gemm_mx_kern
                 mbar_arrive(ring_empty(slot));
                 if (tile >= total) break;
                 const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
-                const GemmSegment &sg = p.seg[t.seg];
+                const GemmSegment &sg = s_seg[t.seg];
                 if (sg.wait != nullptr) {  // A rows written earlier in this launch (both halves)
                     const uint64_t t0 = stats ? global_timer_ns() : 0;
                     if (!wait_counter(sg.wait + t.ready, sg.wait_count, p.wait_ns, abort_flag) ||
@@ -1398,7 +1409,7 @@ __global__ void __launch_bounds__(MxCfg<WF, M256, CW>::kThreads, 1) gemm_mx_kern
             if (lane == 0) mbar_arrive(ring_empty(slot));
             if (tile >= total) break;
             const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
-            const int kbs = p.seg[t.seg].k_blocks;
+            const int kbs = s_seg[t.seg].k_blocks;
             for (int kb = 0; kb < kbs; ++kb) {
                 const int rs = L % R, os = L % P;
                 const bool got = __all_sync(0xffffffffu, mbar_wait(raw_full(rs), (L / R) & 1u, p.wait_ns, abort_flag) &&
@@ -1435,7 +1446,7 @@ __global__ void __launch_bounds__(MxCfg<WF, M256, CW>::kThreads, 1) gemm_mx_kern
                 mbar_arrive(ring_empty(slot));
                 if (tile >= total) break;
                 const Tile t = decode_tile<kBM>(p, tile, s_seg_end, s_offs, s_toffs, half);
-                const GemmSegment &sg = p.seg[t.seg];
+                const GemmSegment &sg = s_seg[t.seg];
                 // two accumulators in turn, or (256-row tiles) one of 2 x 256 columns
                 const uint32_t a = M256 ? 0u : n_acc & 1u, aph = M256 ? n_acc & 1u : (n_acc >> 1) & 1u;
                 const uint64_t t0 = stats ? global_timer_ns() : 0;
