@@ -350,15 +350,20 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
         slot_s[i] = slot;
     }
     __syncthreads();
-    // row copy: a warp per row, each lane up to kG 16-byte chunks in flight
-    // (all loads of a batch before its stores)
+    // row copy in units of (row, batch of 32 * kG 16-byte chunks), dealt round-robin to
+    // the block's warps so that every warp copies the same number of bytes (a warp per
+    // row left some warps a third more rows when a row is several batches long); each
+    // lane has up to kG chunks in flight, all loads of a batch before its stores
     constexpr int kG = 8;
     const int nw = kScatterThreads / 32, chunks = H / 8;
-    for (int i = blockIdx.y * nw + warp; i < n; i += gridDim.y * nw) {
+    const int batches = (chunks + 32 * kG - 1) / (32 * kG);
+    for (int w = blockIdx.y * nw + warp; w < n * batches; w += gridDim.y * nw) {
+        const int i = w / batches;
         const int slot = slot_s[i];
         if (slot < 0) continue;
         const size_t src = (size_t)(tok0 + i / k) * H, dst = (size_t)slot * H;
-        for (int c0 = lane; c0 < chunks; c0 += 32 * kG) {
+        {
+            const int c0 = lane + (w % batches) * 32 * kG;
             uint4 o[kG];
 #pragma unroll
             for (int u = 0; u < kG; ++u) {
