@@ -167,6 +167,8 @@ struct ScatterArgs {
     int *tok_done;            // [T] per-token output counters, zeroed here (CTAs y = 0), or nullptr
 };
 cudaError_t launch_scatter(const ScatterArgs &a, cudaStream_t s);
+// CTAs of the dispatch kernel resident at once on one SM (occupancy query, cached)
+int scatter_ctas_per_sm();
 
 // --------------------------------------------------------------- combine (K7)
 // Y[t] = sum_j w[t,j] * Yslot[slot_of[t,j]] + Ys[t]  (fp32 sum, fixed order).

@@ -601,11 +601,18 @@ moe_status run_front(moe_handle *h, const void *X, int T, cudaStream_t s, int *n
     xa.H = h->H;
     xa.tokens_per_block = TT;
     {
-        // spread the row gather over about two CTAs per SM, at least 8 rows per CTA
+        // spread the row gather over about two CTAs per SM, at least 8 rows per CTA and no
+        // more CTAs than are resident at once; then take a split whose busiest SM copies at
+        // least 10% fewer rows (ceil(nb * g / SMs) / g blocks' worth), if every SM still
+        // gets a CTA (measured: MiniMax-M3 dispatch 36.3 -> 31.2 us with 7 instead of 5)
         const int per_block_rows = TT * h->k;
-        int g = (2 * h->num_sms + nb - 1) / nb;
-        const int gmax = (per_block_rows + 7) / 8;
-        xa.gather_split = g < 1 ? 1 : (g > gmax ? gmax : g);
+        const int gmax = std::max(1, std::min((per_block_rows + 7) / 8, moe::scatter_ctas_per_sm() * h->num_sms / nb));
+        const int g = std::min(std::max(1, (2 * h->num_sms + nb - 1) / nb), gmax);
+        auto busiest = [&](int x) { return (double)((nb * x + h->num_sms - 1) / h->num_sms) / x; };
+        int best = g;
+        for (int x = 1; x <= gmax; ++x)
+            if (nb * x >= h->num_sms && busiest(x) < 0.9 * busiest(best)) best = x;
+        xa.gather_split = best;
     }
     xa.X = X;
     xa.x_f32 = h->x_f32;

@@ -877,6 +877,19 @@ cudaError_t launch_scan(const ScanArgs &a, cudaStream_t s) {
     return launch_pdl(scan_kernel, dim3(1), dim3(kScanThreads), 0, s, a);
 }
 
+int scatter_ctas_per_sm() {
+    static int n = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scatter_kernel, kScatterThreads, 0) != cudaSuccess ||
+            n < 1) {
+            cudaGetLastError();
+            n = 1;
+        }
+    });
+    return n;
+}
+
 cudaError_t launch_scatter(const ScatterArgs &a, cudaStream_t s) {
     static std::once_flag once;
     std::call_once(once, [] { max_smem_carveout(scatter_kernel); });
