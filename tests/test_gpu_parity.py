@@ -317,6 +317,29 @@ def test_staged_stores_are_bit_identical(name, pair):
     blk.close()
 
 
+def test_set_option_takes_only_documented_values():
+    """Every option accepts only its documented values and an unknown option id is
+    refused, before anything runs; a refused call leaves the handle as it was."""
+    shape = SMALL["nano_T1"]
+    inputs, blk = P.make_case(shape)
+    Y0 = blk.forward(inputs["X"]).clone()
+    binary = [capi.MOE_OPT_GRAPH, capi.MOE_OPT_PREFETCH, capi.MOE_OPT_FUSE_EXPERTS, capi.MOE_OPT_COMBINE_OVERLAP,
+              capi.MOE_OPT_STAGED_STORES, capi.MOE_OPT_PAIR_SWAP, capi.MOE_OPT_TRACE, capi.MOE_OPT_STAGE_EVENTS]
+    for opt in binary:
+        for bad in (-1, 2):
+            with pytest.raises(capi.MoeError):
+                blk.set_option(opt, bad)
+    for opt, bad in ((capi.MOE_OPT_GEMM_PAIR, 3), (capi.MOE_OPT_PATH, 4), (capi.MOE_OPT_PATH, -1),
+                     (capi.MOE_OPT_WAIT_LIMIT_NS, -1), (7, 0), (12, 0)):
+        with pytest.raises(capi.MoeError):
+            blk.set_option(opt, bad)
+    Y1 = blk.forward(inputs["X"])
+    torch.cuda.synchronize()
+    assert blk.sync_status() == capi.MOE_OK
+    assert torch.equal(Y0, Y1)
+    blk.close()
+
+
 def test_token_permutation_equivariance_and_determinism():
     shape = SMALL["afmoe_ragged"]
     for path in PATHS.values():
