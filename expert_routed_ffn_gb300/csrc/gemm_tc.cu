@@ -35,8 +35,11 @@
 //              TMEM accumulators, so the epilogue of one tile overlaps the
 //              main loop of the next
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
-//              32*(w%4)..+31 = tile rows), activation and bf16 stores (gate/up),
-//              fp32 stores (down projections)
+//              32*(w%4)..+31 = tile rows), activation, bf16 rows (gate/up) or fp32
+//              rows (down projections); 128-row and CTA-pair tiles stage each
+//              32-row slice in shared memory and write it with one TMA store
+//              (measured on GB300: AFMoE prefill 549 -> 525 us against a 16-byte
+//              store per lane and row), thin tiles store from registers
 // Tiles are (segment, group, m-tile, n-tile) in a fixed order; the producer
 // claims them from a launch-wide ticket (the CTA that is free first takes the
 // next tile) and passes each id to the MMA and epilogue warps through a ring
